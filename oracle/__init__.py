@@ -1,0 +1,118 @@
+"""Float64 CPU oracle for the tcgen05 swizzled GEMM and its layout probes.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline / reference leg of ``bench.py`` may import this package.  The
+product library never links, loads or calls it, and it shares no code with the
+CUDA path.
+
+* :func:`gemm` -- D = A.B (optionally block-scaled) and the error scale
+  S = sum |a||b| in float64, from the raw storage bits (C, ``gemm_oracle.c``).
+* :mod:`oracle.layouts` -- the pages' descriptor walk, swizzles, TMEM
+  register images, ldmatrix ownership and scale-factor placement.
+
+Parity status: every function here is pinned by ``tests/test_oracle_*.py``
+against library routines, closed forms and the pages' worked examples, except
+where DESIGN.md's readings table says "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+from . import layouts  # noqa: F401
+from .build import LIB, build
+
+F32, F16, BF16, E4M3 = 0, 1, 2, 3
+K_MAJOR, MN_MAJOR = 0, 1
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        path = LIB if os.path.exists(LIB) else build()
+        lib = ctypes.CDLL(path)
+        i64, vp, ci, dp = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p
+        lib.oracle_gemm.argtypes = [i64, i64, i64, vp, ci, ci, i64, vp, ci, ci, i64,
+                                    vp, i64, vp, i64, vp, i64, dp, dp, ci]
+        lib.oracle_gemm.restype = ci
+        for name, t in (("oracle_dec_f16", ctypes.c_uint16), ("oracle_dec_bf16", ctypes.c_uint16),
+                        ("oracle_dec_f32", ctypes.c_uint32), ("oracle_dec_e4m3", ctypes.c_uint8),
+                        ("oracle_dec_e8m0", ctypes.c_uint8)):
+            f = getattr(lib, name)
+            f.argtypes = [t]
+            f.restype = ctypes.c_double
+        lib.oracle_num_threads.restype = ci
+        _lib = lib
+    return _lib
+
+
+def num_threads() -> int:
+    return _load().oracle_num_threads()
+
+
+def decode(bits: np.ndarray, dtype: int) -> np.ndarray:
+    """Decode raw storage bits to float64 with the oracle's C decoders
+    (element by element; meant for pins and small arrays)."""
+    lib = _load()
+    f = {F32: lib.oracle_dec_f32, F16: lib.oracle_dec_f16, BF16: lib.oracle_dec_bf16,
+         E4M3: lib.oracle_dec_e4m3}[dtype]
+    flat = np.asarray(bits).ravel()
+    return np.array([f(int(x)) for x in flat], dtype=np.float64).reshape(np.shape(bits))
+
+
+def decode_e8m0(bits: np.ndarray) -> np.ndarray:
+    lib = _load()
+    flat = np.asarray(bits).ravel()
+    return np.array([lib.oracle_dec_e8m0(int(x)) for x in flat],
+                    dtype=np.float64).reshape(np.shape(bits))
+
+
+_STORAGE = {F32: np.uint32, F16: np.uint16, BF16: np.uint16, E4M3: np.uint8}
+
+
+def gemm(M: int, N: int, K: int, A: np.ndarray, a_type: int, a_major: int, lda: int,
+         B: np.ndarray, b_type: int, b_major: int, ldb: int,
+         SFA: np.ndarray | None = None, SFB: np.ndarray | None = None,
+         rows=None, nthreads: int = 0):
+    """Float64 D and S for the requested rows (all rows when ``rows`` is None).
+
+    A/B are raw storage arrays (uint32 for fp32, uint16 for f16/bf16, uint8 for
+    e4m3) laid out as the C file's header states.  SFA/SFB are plain
+    row-major e8m0 arrays [M][ceil(K/32)] / [N][ceil(K/32)].
+    Returns (D, S) of shape (len(rows), N).
+    """
+    lib = _load()
+    A = np.ascontiguousarray(A, dtype=_STORAGE[a_type])
+    B = np.ascontiguousarray(B, dtype=_STORAGE[b_type])
+    if rows is None:
+        nrows = M
+        rows_arr = None
+    else:
+        rows_arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        nrows = rows_arr.size
+        if nrows and (rows_arr.min() < 0 or rows_arr.max() >= M):
+            raise ValueError("row index out of range")
+    D = np.zeros((nrows, N), dtype=np.float64)
+    S = np.zeros((nrows, N), dtype=np.float64)
+    kb = -(-K // 32)
+    sfa_p = sfb_p = None
+    if SFA is not None:
+        SFA = np.ascontiguousarray(SFA, dtype=np.uint8)
+        assert SFA.shape == (M, kb), SFA.shape
+        sfa_p = SFA.ctypes.data
+    if SFB is not None:
+        SFB = np.ascontiguousarray(SFB, dtype=np.uint8)
+        assert SFB.shape == (N, kb), SFB.shape
+        sfb_p = SFB.ctypes.data
+    rc = lib.oracle_gemm(M, N, K, A.ctypes.data, a_type, a_major, lda,
+                         B.ctypes.data, b_type, b_major, ldb,
+                         sfa_p, kb, sfb_p, kb,
+                         None if rows_arr is None else rows_arr.ctypes.data, nrows,
+                         D.ctypes.data, S.ctypes.data, nthreads)
+    if rc != 0:
+        raise RuntimeError(f"oracle_gemm failed with {rc}")
+    return D, S

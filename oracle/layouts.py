@@ -1,0 +1,286 @@
+"""Layout models from the Apache TVM TIRx tcgen05 / ldmatrix documentation pages.
+
+TEST INFRASTRUCTURE ONLY: used by the tests to predict, bit for bit, what the
+GPU layout probes must return.  Shares nothing with the CUDA library.
+
+Every function cites the page and section it restates.  Readings of points the
+pages leave open are marked READING and are listed in the design doc's table of
+readings.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+# ---------------------------------------------------------------------------
+# Swizzle modes ("tcgen05.cp" page, "Shared descriptor address walk";
+# "tcgen05.mma" page, "Shared descriptors are byte-stride contracts" and
+# "swizzle=4").
+# ---------------------------------------------------------------------------
+
+#: swizzle period in bytes for the pages' logical modes 0..4
+SWIZZLE_PERIOD = {0: 16, 1: 256, 2: 512, 3: 1024, 4: 512}
+
+
+def row_bytes(swizzle: int) -> int:
+    """A descriptor row is ``16 << swizzle`` bytes for modes 0..3 and 128 bytes
+    for mode 4 (128-byte span)."""
+    return 128 if swizzle == 4 else (16 << swizzle)
+
+
+def rows_per_group(swizzle: int) -> int:
+    """Modes 0..3 group eight rows per SDO; mode 4 groups four K rows."""
+    return 4 if swizzle == 4 else 8
+
+
+def swizzle_addr(addr, swizzle: int):
+    """Physical shared byte address for a logical one.
+
+    Mode 4 is the page's formula ``offset ^ ((offset >> 2) & 96)``.
+    READING (modes 1..3, the pages give only their 256/512/1024-byte periods):
+    the 16-byte chunk index (address bits 4..3+s) is XORed with the s address
+    bits starting at bit 7, i.e. ``addr ^ ((addr >> 3) & (((1 << s) - 1) << 4))``,
+    applied to the absolute address; this is what makes the period alignment
+    of swizzled bases and the origin's swizzle phase matter.
+    Works elementwise on numpy integer arrays.
+    """
+    if swizzle == 0:
+        return addr
+    if swizzle == 4:
+        return addr ^ ((addr >> 2) & 96)
+    mask = ((1 << swizzle) - 1) << 4
+    return addr ^ ((addr >> 3) & mask)
+
+
+def cp_walk(r, w, ldo: int, sdo: int, swizzle: int):
+    """Logical byte offset of (row r, b32 word w) of a tcgen05.cp source image
+    relative to the descriptor origin ("tcgen05.cp" page, "Shared descriptor
+    address walk"): row r starts at (r//8)*SDO + (r%8)*(16<<swizzle); without
+    swizzle word w adds (w//4)*LDO + (w%4)*4; with swizzle words are contiguous
+    and add 4*w (LDO ignored)."""
+    r = np.asarray(r)
+    w = np.asarray(w)
+    base = (r // 8) * sdo + (r % 8) * (16 << swizzle)
+    if swizzle == 0:
+        return base + (w // 4) * ldo + (w % 4) * 4
+    return base + 4 * w
+
+
+def check_descriptor(origin: int, ldo: int, sdo: int, swizzle: int) -> None:
+    """Field constraints ("tcgen05.cp" page, "Shared descriptor address walk";
+    "tcgen05.mma" page, descriptor contract): strides are non-negative 16-byte
+    multiples below 2^18, origins 16-byte aligned, swizzled bases aligned to the
+    256/512/1024-byte period (512 for mode 4).  Raises ValueError."""
+    for name, v in (("ldo", ldo), ("sdo", sdo)):
+        if v < 0 or v % 16 or v >= (1 << 18):
+            raise ValueError(f"{name}={v} must be a non-negative multiple of 16 below 2^18")
+    if origin % 16:
+        raise ValueError(f"origin {origin} is not 16-byte aligned")
+    if swizzle not in (0, 1, 2, 3, 4):
+        raise ValueError(f"swizzle mode {swizzle} not in 0..4")
+
+
+def cp_physical(origin: int, r, w, ldo: int, sdo: int, swizzle: int, base_align: int = 0):
+    """Physical byte address (relative to a period-aligned allocation) of word
+    (r, w) read by tcgen05.cp: the selected swizzle of origin + walk.  The
+    origin is given un-swizzled ("tcgen05.mma" page: the origin is
+    inverse-swizzled before encoding so it is not permuted twice; the swizzles
+    are involutions, so the un-swizzled origin is what the descriptor holds)."""
+    check_descriptor(origin, ldo, sdo, swizzle)
+    return swizzle_addr(base_align + origin + cp_walk(r, w, ldo, sdo, swizzle), swizzle) - base_align
+
+
+def mma_operand_offset(mn, k, elem_bytes: int, major: str, ldo: int, sdo: int, swizzle: int):
+    """Logical byte offset of operand element (mn, k) of a tcgen05.mma shared
+    operand ("tcgen05.mma" page, "Shared descriptors are byte-stride
+    contracts" and "swizzle=4").
+
+    K-major: rows enumerate M/N, a row holds contiguous K elements; the next
+    row group (8 rows) is SDO away and the next 16-byte chunk (unswizzled) LDO
+    away; swizzled instruction atoms fit within one row.
+    MN-major swizzled: rows enumerate K; row group stride SDO; the next
+    contiguous M/N chunk (one row width) is LDO away.
+    MN-major unswizzled: the two strides swap (LDO for row groups, SDO for
+    chunks).
+    Mode 4 (32-bit MN-major only): four K rows of 128 bytes per SDO, LDO to the
+    next 128-byte M/N chunk.
+    """
+    mn = np.asarray(mn)
+    k = np.asarray(k)
+    rb = row_bytes(swizzle)
+    g = rows_per_group(swizzle)
+    if major == "k":
+        byte = k * elem_bytes
+        if swizzle == 0:
+            return (mn // 8) * sdo + (mn % 8) * 16 + (byte // 16) * ldo + byte % 16
+        if np.any(byte >= rb):
+            raise ValueError("a K-major swizzled atom must fit within one row")
+        return (mn // g) * sdo + (mn % g) * rb + byte
+    if major == "mn":
+        byte = mn * elem_bytes
+        if swizzle == 0:
+            return (k // 8) * ldo + (k % 8) * 16 + (byte // 16) * sdo + byte % 16
+        return (k // g) * sdo + (k % g) * rb + (byte // rb) * ldo + byte % rb
+    raise ValueError(major)
+
+
+# ---------------------------------------------------------------------------
+# tcgen05.ld / tcgen05.st register images ("tcgen05.ld / tcgen05.st" page,
+# "Native images").
+# ---------------------------------------------------------------------------
+
+LD_SHAPES = ("32x32b", "16x64b", "16x128b", "16x256b")
+
+
+def ld_regs_per_lane(shape: str, n: int) -> int:
+    return {"32x32b": n, "16x64b": n, "16x128b": 2 * n, "16x256b": 4 * n}[shape]
+
+
+def ld_atom_extent(shape: str, n: int):
+    return {"32x32b": (32, n), "16x64b": (16, 2 * n), "16x128b": (16, 4 * n),
+            "16x256b": (16, 8 * n)}[shape]
+
+
+def ld_owner(shape: str, lane, reg):
+    """(row, column) of the atom held in register ``reg`` of lane ``lane``.
+
+    32x32b:  (l, r)
+    16x64b:  (l//4 + 8(l%2), l//2%2 + 2r)        READING: as printed
+    16x128b: (l//4 + 8(r%2), l%4 + 4(r//2))
+    16x256b: (l//4 + 8(r//2%2), r%2 + 2(l%4) + 8(r//4))
+    (The garbled "8(x)" of the page is 8*(x).)
+    """
+    l = np.asarray(lane)
+    r = np.asarray(reg)
+    if shape == "32x32b":
+        row, col = l + 0 * r, r + 0 * l
+    elif shape == "16x64b":
+        row, col = l // 4 + 8 * (l % 2) + 0 * r, (l // 2) % 2 + 2 * r
+    elif shape == "16x128b":
+        row, col = l // 4 + 8 * (r % 2), l % 4 + 4 * (r // 2)
+    elif shape == "16x256b":
+        row, col = l // 4 + 8 * ((r // 2) % 2), r % 2 + 2 * (l % 4) + 8 * (r // 4)
+    else:
+        raise ValueError(shape)
+    return row, col
+
+
+def ld_image(shape: str, n: int, tmem_word):
+    """Registers every lane receives from ``tcgen05.ld.<shape>.x<n>`` given
+    ``tmem_word(row, col)`` for the atom's rows/cols; returns (32, regs)."""
+    regs = ld_regs_per_lane(shape, n)
+    lanes = np.arange(32)[:, None]
+    rr = np.arange(regs)[None, :]
+    row, col = ld_owner(shape, lanes, rr)
+    return tmem_word(row, col)
+
+
+def layout_b_position(i, j):
+    """Layout B ("tcgen05.ld / tcgen05.st" page, example): logical [i, j] of a
+    (64, 128) tile sits at lane i + 64*(j//64), column j % 64."""
+    i = np.asarray(i)
+    j = np.asarray(j)
+    return i + 64 * (j // 64), j % 64
+
+
+# ---------------------------------------------------------------------------
+# ldmatrix / stmatrix m8n8.b16 ("ldmatrix / stmatrix" page, "Address providers
+# and result owners", "Transpose and stores").
+# ---------------------------------------------------------------------------
+
+
+def ldmatrix_address_provider(matrix: int, row: int) -> int:
+    """Lane 8*matrix + row provides the shared address of that row."""
+    return 8 * matrix + row
+
+
+def ldmatrix_owner(matrix: int, row: int, word: int):
+    """Register word (matrix, row, word) belongs to lane 4*row + word, in that
+    lane's ``matrix``-th destination register."""
+    return 4 * row + word, matrix
+
+
+def ldmatrix_load(shared_rows, count: int, trans: bool = False):
+    """Simulate ``ldmatrix.m8n8.x<count>[.trans].b16``.
+
+    ``shared_rows[matrix][row]`` is the list of four b32 words (each two
+    16-bit halves, low half first) of that 16-byte row, as supplied by the
+    address-providing lane.  Returns regs[lane][matrix] as b32 ints.
+    With .trans, register element (row, 2*word+half) comes from shared element
+    (2*word+half, row) of the same 8x8 matrix of 16-bit values.
+    """
+    regs = [[None] * count for _ in range(32)]
+    for m in range(count):
+        halves = [[(shared_rows[m][r][c // 2] >> (16 * (c % 2))) & 0xFFFF for c in range(8)]
+                  for r in range(8)]
+        for row in range(8):
+            for word in range(4):
+                lane, reg = ldmatrix_owner(m, row, word)
+                if trans:
+                    lo = halves[2 * word][row]
+                    hi = halves[2 * word + 1][row]
+                else:
+                    lo = halves[row][2 * word]
+                    hi = halves[row][2 * word + 1]
+                regs[lane][reg] = lo | (hi << 16)
+    return regs
+
+
+# ---------------------------------------------------------------------------
+# Block-scale factors in TMEM ("tcgen05.mma" page, "Weight-stationary and block
+# scaling"; "tcgen05.cp" page, shape table).
+# ---------------------------------------------------------------------------
+
+
+def sf_tmem_position(r, sf):
+    """Scale row r uses lane r%32 and byte-column 4*(r//32)+sf, with four
+    replicas 32 lanes apart.  Returns (lanes[4], b32 column, byte in column)."""
+    r = np.asarray(r)
+    bytecol = 4 * (r // 32) + np.asarray(sf)
+    lanes = np.stack([r % 32 + 32 * q for q in range(4)])
+    return lanes, bytecol // 4, bytecol % 4
+
+
+def cp_32x128b_warpx4_position(row, byte):
+    """tcgen05.cp .32x128b.warpx4: a (32, 4)-word source image; source row i
+    goes to 32 consecutive lanes (i) replicated four times 32 lanes apart;
+    columns are consecutive b32 cells, so byte b of the 16-byte row lands in
+    column b//4, byte b%4."""
+    row = np.asarray(row)
+    byte = np.asarray(byte)
+    lanes = np.stack([row + 32 * q for q in range(4)])
+    return lanes, byte // 4, byte % 4
+
+
+def sf_chunk_offset(r, kb):
+    """Byte offset, inside one 512-byte scale chunk (128 rows x 4 K blocks),
+    at which the scale of row r and K block kb must sit so that one
+    .32x128b.warpx4 copy puts it where the MMA reads it: 16*(r%32) +
+    4*(r//32) + kb (source row r%32, byte 4*(r//32)+kb)."""
+    r = np.asarray(r)
+    return 16 * (r % 32) + 4 * (r // 32) + np.asarray(kb)
+
+
+def sf_prepare(sf: np.ndarray, rows: int, kblocks: int, tile_rows: int) -> np.ndarray:
+    """Rearrange plain row-major e8m0 scales ``sf[rows][kblocks]`` into the
+    cp-ready image the kernels stream: for every K step of 4 scale blocks
+    (128 K elements) and every tile of ``tile_rows`` rows, ceil(tile_rows/128)
+    consecutive 512-byte chunks laid out by :func:`sf_chunk_offset`.
+    Missing rows/blocks (ragged tails) hold 127 (a scale of 1.0; the matching
+    operand values are zero-filled, so the value does not matter).
+    Image order: [kstep][tile][chunk][512]."""
+    ksteps = -(-kblocks // 4)
+    tiles = -(-rows // tile_rows)
+    chunks = -(-tile_rows // 128)
+    out = np.full((ksteps, tiles, chunks, 512), 127, dtype=np.uint8)
+    for t in range(tiles):
+        for c in range(chunks):
+            for rl in range(128):
+                r = t * tile_rows + c * 128 + rl
+                if rl + c * 128 >= tile_rows or r >= rows:
+                    continue
+                for ks in range(ksteps):
+                    for kb in range(4):
+                        kk = ks * 4 + kb
+                        if kk < kblocks:
+                            out[ks, t, c, int(sf_chunk_offset(rl, kb))] = sf[r, kk]
+    return out

@@ -1,0 +1,126 @@
+"""Seeded synthetic inputs for the GEMM workloads (shared by tests and bench).
+
+This module holds no GEMM arithmetic: it only draws random numbers with
+numpy's ``default_rng``, rounds them to the storage dtype with torch's
+round-to-nearest-even conversions, and lays them out K-major or MN-major.
+Both the CUDA path and the oracle consume what it returns; neither is
+imported here.
+
+Storage conventions: A K-major is M x K row-major, A MN-major is K x M
+row-major; B K-major is N x K row-major, B MN-major is K x N row-major
+(rows of a K-major operand enumerate M/N, rows of an MN-major one enumerate
+K).  Scale factors are plain row-major e8m0 bytes, [M][ceil(K/32)] for A and
+[N][ceil(K/32)] for B.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+import torch
+
+DTYPES = ("f16", "bf16", "tf32", "e4m3")
+
+_TORCH = {"f16": torch.float16, "bf16": torch.bfloat16, "tf32": torch.float32,
+          "e4m3": torch.float8_e4m3fn}
+_BITS = {"f16": torch.int16, "bf16": torch.int16, "tf32": torch.int32, "e4m3": torch.uint8}
+_NP_BITS = {"f16": np.uint16, "bf16": np.uint16, "tf32": np.uint32, "e4m3": np.uint8}
+
+
+@dataclass
+class Workload:
+    """One GEMM problem: shapes, operand dtype/majors, value distribution."""
+    name: str
+    M: int
+    N: int
+    K: int
+    dtype: str                 # operand storage dtype: f16 | bf16 | tf32 | e4m3
+    a_major: str = "k"         # "k" | "mn"
+    b_major: str = "k"
+    dist: str = "normal"       # "normal": N(0,1)/sqrt(K); "uniform": U[-1,1]; "normal1": N(0,1)
+    acc: str = "f32"           # accumulator dtype: f32 | f16
+    out: str = "bf16"          # output dtype: f32 | f16 | bf16
+    cta_group: int = 1
+    block_scaled: bool = False
+    seed_base: int = 0
+    extra: dict = field(default_factory=dict)
+
+
+# The five problems the benchmark and parity tests are built around.
+WORKLOADS = {
+    "tile_f16_128x128x64": Workload("tile_f16_128x128x64", 128, 128, 64, "f16", "k", "k",
+                                    "uniform", "f32", "f32", 1, False, 1),
+    "bf16_4096_kmn_cta1": Workload("bf16_4096_kmn_cta1", 4096, 4096, 4096, "bf16", "k", "mn",
+                                   "normal", "f32", "bf16", 1, False, 2),
+    "tf32_2048x2048x8192": Workload("tf32_2048x2048x8192", 2048, 2048, 8192, "tf32", "k", "k",
+                                    "uniform", "f32", "f32", 1, False, 3),
+    "bf16_8192_cta2": Workload("bf16_8192_cta2", 8192, 8192, 8192, "bf16", "k", "k",
+                               "normal", "f32", "bf16", 2, False, 4),
+    "f16acc_8192_cta2": Workload("f16acc_8192_cta2", 8192, 8192, 8192, "f16", "k", "k",
+                                 "normal", "f16", "f16", 2, False, 4),
+    "mxf8_8192": Workload("mxf8_8192", 8192, 8192, 8192, "e4m3", "k", "k",
+                          "normal1", "f32", "bf16", 2, True, 5),
+}
+
+
+def draw(shape, seed: int, dist: str, K: int) -> np.ndarray:
+    rng = np.random.default_rng(seed)
+    if dist == "uniform":
+        return rng.uniform(-1.0, 1.0, size=shape)
+    if dist == "normal":
+        return rng.standard_normal(size=shape) / np.sqrt(max(K, 1))
+    if dist == "normal1":
+        return rng.standard_normal(size=shape)
+    if dist == "int4":  # small integers / 4 in [-1, 1]; exact sums
+        return rng.integers(-4, 5, size=shape) / 4.0
+    raise ValueError(dist)
+
+
+def to_bits(x64: np.ndarray, dtype: str) -> np.ndarray:
+    """Round float64 values to the storage dtype (torch RNE) and return the raw
+    storage bits as a numpy unsigned array."""
+    t = torch.from_numpy(np.ascontiguousarray(x64, dtype=np.float64))
+    if dtype in ("f16", "bf16", "e4m3"):
+        t = t.to(torch.float32)  # exact for the draws used; then one RNE rounding
+    t = t.to(_TORCH[dtype]).contiguous()
+    return t.view(_BITS[dtype]).numpy().view(_NP_BITS[dtype]).copy()
+
+
+def lay_out_a(a_logical: np.ndarray, major: str) -> np.ndarray:
+    """Logical A (M x K) to storage (M x K for K-major, K x M for MN-major)."""
+    return np.ascontiguousarray(a_logical if major == "k" else a_logical.T)
+
+
+def lay_out_b(b_logical: np.ndarray, major: str) -> np.ndarray:
+    """Logical B (K x N) to storage (N x K for K-major, K x N for MN-major)."""
+    return np.ascontiguousarray(b_logical.T if major == "k" else b_logical)
+
+
+def scales(rows: int, K: int, seed: int, lo: int = -4, hi: int = 4) -> np.ndarray:
+    """e8m0 scale bytes 127 + U{lo..hi}, one per 32 K elements per row."""
+    rng = np.random.default_rng(seed)
+    return (127 + rng.integers(lo, hi + 1, size=(rows, -(-K // 32)))).astype(np.uint8)
+
+
+def make_inputs(w: Workload, M: int | None = None, N: int | None = None, K: int | None = None,
+                dist: str | None = None):
+    """Storage-bit arrays (A, B, SFA, SFB) for a workload, optionally resized.
+
+    Seeds follow the workload index: A 1000+i, B 2000+i, scales 3000+i (A) and
+    4000+i (B).  Returns a dict with numpy arrays and leading dimensions.
+    """
+    M = w.M if M is None else M
+    N = w.N if N is None else N
+    K = w.K if K is None else K
+    dist = w.dist if dist is None else dist
+    i = w.seed_base
+    a = draw((M, K), 1000 + i, dist, K)
+    b = draw((K, N), 2000 + i, dist, K)
+    A = lay_out_a(to_bits(a, w.dtype), w.a_major)
+    B = lay_out_b(to_bits(b, w.dtype), w.b_major)
+    out = {"A": A, "B": B, "lda": A.shape[1], "ldb": B.shape[1], "M": M, "N": N, "K": K,
+           "SFA": None, "SFB": None}
+    if w.block_scaled:
+        out["SFA"] = scales(M, K, 3000 + i)
+        out["SFB"] = scales(N, K, 4000 + i)
+    return out

@@ -1,0 +1,205 @@
+"""Pins for the float64 GEMM oracle (CPU only).
+
+Each pin ties the oracle to something other than itself: a library routine
+(torch dtype decoding, numpy.matmul), a closed form (identity, permutation,
+all-ones, power-of-two scales) or the worked example of the "tcgen05.mma"
+page ("four K16 issues for a 128x64x64 product").  A planted-mistake test
+shows the pins notice a transposed operand or a dropped scale.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synthetic as syn
+
+
+
+
+# ---------------------------------------------------------------- decoders
+
+def _torch_decode(bits, tdtype, itype):
+    return torch.from_numpy(bits.astype(np.int64)).to(itype).view(tdtype).double().numpy()
+
+
+def _same(a, b):
+    nan = np.isnan(a)
+    assert np.array_equal(nan, np.isnan(b))
+    assert np.array_equal(a[~nan], b[~nan])
+
+
+def test_decode_f16_all_patterns(oracle_mod):
+    bits = np.arange(65536, dtype=np.uint16)
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.float16).double().numpy()
+    _same(oracle_mod.decode(bits, oracle_mod.F16), ref)
+
+
+def test_decode_bf16_all_patterns(oracle_mod):
+    bits = np.arange(65536, dtype=np.uint16)
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).double().numpy()
+    _same(oracle_mod.decode(bits, oracle_mod.BF16), ref)
+
+
+def test_decode_e4m3_all_patterns(oracle_mod):
+    bits = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(bits).view(torch.float8_e4m3fn).double().numpy()
+    _same(oracle_mod.decode(bits, oracle_mod.E4M3), ref)
+
+
+def test_decode_e8m0_all_patterns(oracle_mod):
+    bits = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(bits).view(torch.float8_e8m0fnu).double().numpy()
+    _same(oracle_mod.decode_e8m0(bits), ref)
+
+
+def test_decode_f32_sampled_and_special(oracle_mod):
+    rng = np.random.default_rng(7)
+    bits = rng.integers(0, 2**32, size=20000, dtype=np.uint64).astype(np.uint32)
+    special = np.array([0, 1, 0x007FFFFF, 0x00800000, 0x3F800000, 0x7F7FFFFF, 0x7F800000,
+                        0x7FC00000, 0x80000000, 0x80000001, 0xFF800000], dtype=np.uint32)
+    bits = np.concatenate([bits, special])
+    ref = bits.view(np.float32).astype(np.float64)
+    _same(oracle_mod.decode(bits, oracle_mod.F32), ref)
+
+
+# ---------------------------------------------------------------- GEMM
+
+def _logical(oracle_mod, A, a_type, a_major, B, b_type, b_major, M, N, K):
+    """Decoded logical A (MxK) and B (KxN) via torch dtype views (library)."""
+    tmap = {oracle_mod.F32: (np.uint32, None), oracle_mod.F16: (np.uint16, torch.float16),
+            oracle_mod.BF16: (np.uint16, torch.bfloat16), oracle_mod.E4M3: (np.uint8, torch.float8_e4m3fn)}
+
+    def dec(x, t):
+        if t == oracle_mod.F32:
+            return x.view(np.float32).astype(np.float64)
+        npt, tt = tmap[t]
+        if npt is np.uint16:
+            return torch.from_numpy(x.view(np.int16)).view(tt).double().numpy()
+        return torch.from_numpy(x).view(tt).double().numpy()
+
+    a = dec(A, a_type)
+    b = dec(B, b_type)
+    a = a if a_major == oracle_mod.K_MAJOR else a.T
+    b = b.T if b_major == oracle_mod.K_MAJOR else b
+    return a[:M, :K], b[:K, :N]
+
+
+CASES = [
+    ("bf16", "k", "k", 70, 90, 130),
+    ("bf16", "k", "mn", 129, 64, 200),
+    ("f16", "mn", "k", 33, 257, 96),
+    ("f16", "mn", "mn", 1, 7, 48),
+    ("tf32", "k", "k", 64, 40, 72),
+    ("tf32", "mn", "mn", 17, 31, 33),
+    ("e4m3", "k", "k", 40, 50, 128),
+]
+TYPE = {"f16": 1, "bf16": 2, "tf32": 0, "e4m3": 3}
+
+
+@pytest.mark.parametrize("dtype,am,bm,M,N,K", CASES)
+def test_gemm_matches_numpy_matmul(oracle_mod, dtype, am, bm, M, N, K):
+    w = syn.Workload("t", M, N, K, dtype, am, bm, "uniform")
+    x = syn.make_inputs(w)
+    t = TYPE[dtype]
+    ai = 0 if am == "k" else 1
+    bi = 0 if bm == "k" else 1
+    D, S = oracle_mod.gemm(M, N, K, x["A"], t, ai, x["lda"], x["B"], t, bi, x["ldb"])
+    a, b = _logical(oracle_mod, x["A"], t, ai, x["B"], t, bi, M, N, K)
+    np.testing.assert_allclose(D, a @ b, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(S, np.abs(a) @ np.abs(b), rtol=1e-12, atol=1e-12)
+
+
+def test_gemm_row_subset_matches_full(oracle_mod):
+    w = syn.Workload("t", 50, 33, 70, "bf16", "k", "mn", "normal")
+    x = syn.make_inputs(w)
+    D, S = oracle_mod.gemm(50, 33, 70, x["A"], 2, 0, x["lda"], x["B"], 2, 1, x["ldb"])
+    rows = [49, 0, 17, 17]
+    Dr, Sr = oracle_mod.gemm(50, 33, 70, x["A"], 2, 0, x["lda"], x["B"], 2, 1, x["ldb"], rows=rows)
+    assert np.array_equal(Dr, D[rows]) and np.array_equal(Sr, S[rows])
+
+
+def test_gemm_identity_and_permutation_exact(oracle_mod):
+    # A = I reproduces B bit for bit; A = P permutes B's rows.
+    n = 64
+    b = syn.draw((n, 96), 5, "uniform", n)
+    B = syn.lay_out_b(syn.to_bits(b, "bf16"), "k")
+    bdec = torch.from_numpy(B.view(np.int16)).view(torch.bfloat16).double().numpy().T
+    I = syn.to_bits(np.eye(n), "bf16")
+    D, _ = oracle_mod.gemm(n, 96, n, I, 2, 0, n, B, 2, 0, n)
+    assert np.array_equal(D, bdec)
+    perm = np.random.default_rng(3).permutation(n)
+    P = syn.to_bits(np.eye(n)[perm], "bf16")
+    D, _ = oracle_mod.gemm(n, 96, n, P, 2, 0, n, B, 2, 0, n)
+    assert np.array_equal(D, bdec[perm])
+
+
+def test_gemm_all_ones_gives_k(oracle_mod):
+    M, N, K = 9, 11, 1000
+    A = syn.to_bits(np.ones((M, K)), "f16")
+    B = syn.to_bits(np.ones((N, K)), "f16")
+    D, S = oracle_mod.gemm(M, N, K, A, 1, 0, K, B, 1, 0, K)
+    assert np.all(D == K) and np.all(S == K)
+
+
+def test_gemm_k_zero_gives_zero(oracle_mod):
+    A = np.zeros((4, 0), np.uint16)
+    B = np.zeros((5, 0), np.uint16)
+    D, S = oracle_mod.gemm(4, 5, 0, A, 2, 0, 0, B, 2, 0, 0)
+    assert np.all(D == 0) and np.all(S == 0)
+
+
+def test_page_example_four_k16_issues_exact(oracle_mod):
+    # "tcgen05.mma" page, example: a, b = integers(-4,5)/4 as float16 from
+    # default_rng(0), a (128,64), b stored (N,K) = (64,64), checked against a @ b.T.
+    rng = np.random.default_rng(0)
+    a = (rng.integers(-4, 5, (128, 64)) / 4).astype("float16")
+    b = (rng.integers(-4, 5, (64, 64)) / 4).astype("float16")
+    D, _ = oracle_mod.gemm(128, 64, 64, a.view(np.uint16), 1, 0, 64, b.view(np.uint16), 1, 0, 64)
+    ref = a.astype(np.float64) @ b.astype(np.float64).T
+    assert np.array_equal(D, ref)  # quarter-integers: every partial sum is exact
+
+
+def test_blockscaled_identity_closed_form(oracle_mod):
+    # A = I (e4m3 1.0) with per-(row, K-block) exponents ea and B with exponents
+    # eb: D[m,n] = 2^(ea[m, m//32] + eb[n, m//32] - 254) * e4m3(B)[m, n].
+    n, N = 128, 40
+    A = syn.to_bits(np.eye(n), "e4m3")
+    b = syn.draw((n, N), 11, "normal1", n)
+    B = syn.lay_out_b(syn.to_bits(b, "e4m3"), "k")
+    rng = np.random.default_rng(12)
+    SFA = (127 + rng.integers(-6, 7, size=(n, n // 32))).astype(np.uint8)
+    SFB = (127 + rng.integers(-6, 7, size=(N, n // 32))).astype(np.uint8)
+    D, _ = oracle_mod.gemm(n, N, n, A, 3, 0, n, B, 3, 0, n, SFA=SFA, SFB=SFB)
+    bdec = torch.from_numpy(B).view(torch.float8_e4m3fn).double().numpy().T  # (K, N)
+    m = np.arange(n)
+    expo = SFA[m, m // 32].astype(np.int64)[:, None] + SFB[:, m // 32].T.astype(np.int64) - 254
+    assert np.array_equal(D, np.ldexp(bdec, expo))
+
+
+def test_blockscaled_matches_numpy(oracle_mod):
+    w = syn.WORKLOADS["mxf8_8192"]
+    x = syn.make_inputs(w, M=48, N=72, K=160)
+    D, S = oracle_mod.gemm(48, 72, 160, x["A"], 3, 0, x["lda"], x["B"], 3, 0, x["ldb"],
+                           SFA=x["SFA"], SFB=x["SFB"])
+    a = torch.from_numpy(x["A"]).view(torch.float8_e4m3fn).double().numpy()
+    b = torch.from_numpy(x["B"]).view(torch.float8_e4m3fn).double().numpy().T
+    sa = np.repeat(np.ldexp(1.0, x["SFA"].astype(np.int64) - 127), 32, axis=1)[:, :160]
+    sb = np.repeat(np.ldexp(1.0, x["SFB"].astype(np.int64) - 127), 32, axis=1)[:, :160].T
+    ref = (a * sa) @ (b * sb)
+    np.testing.assert_allclose(D, ref, rtol=1e-12, atol=0)
+    np.testing.assert_allclose(S, np.abs(a * sa) @ np.abs(b * sb), rtol=1e-12)
+
+
+def test_planted_mistakes_are_caught(oracle_mod):
+    # Plant the mistakes a reader could make (transposed B, dropped scale) by
+    # calling the oracle wrongly; the numpy pin must reject each one.
+    w = syn.Workload("t", 24, 40, 64, "bf16", "k", "k", "uniform")
+    x = syn.make_inputs(w)
+    a, b = _logical(oracle_mod, x["A"], 2, 0, x["B"], 2, 0, 24, 40, 64)
+    D_wrong_major, _ = oracle_mod.gemm(24, 40, 64, x["A"], 2, 0, x["lda"], x["B"], 2, 1, 40)
+    assert not np.allclose(D_wrong_major, a @ b)
+    wm = syn.WORKLOADS["mxf8_8192"]
+    y = syn.make_inputs(wm, M=16, N=16, K=64)
+    D_noscale, _ = oracle_mod.gemm(16, 16, 64, y["A"], 3, 0, 64, y["B"], 3, 0, 64, SFA=y["SFA"])
+    D_full, _ = oracle_mod.gemm(16, 16, 64, y["A"], 3, 0, 64, y["B"], 3, 0, 64,
+                                SFA=y["SFA"], SFB=y["SFB"])
+    assert not np.allclose(D_noscale, D_full)

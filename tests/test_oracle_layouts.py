@@ -1,0 +1,220 @@
+"""Pins for the oracle's layout models (CPU only).
+
+Pinned against: the pages' worked examples (the "tcgen05.cp" 128x128b copy of
+arange(512) with (ldo=16, sdo=128, swizzle=0); the "tcgen05.mma" 128x64 fp16
+K-major operand with (16, 1024, 3) and its K16 view rearrangement; the
+"ldmatrix / stmatrix" interleaved-slots example), the CUDA driver header's
+description of the TMA swizzle modes, the PTX mma.sync m16n8 accumulator
+fragment (a textbook layout the 16x256b image must reduce to), and brute-force
+bijection checks on every small case.
+"""
+import itertools
+
+import numpy as np
+import pytest
+
+from oracle import layouts as L
+
+
+# ------------------------------------------------------------ descriptor walk
+
+def test_cp_walk_page_example_is_dense_row_major():
+    # "tcgen05.cp" page example: shared (128, 4) uint32 written row-major from
+    # arange(512), copied with (ldo=16, sdo=128, swizzle=0), read back equal.
+    r, w = np.meshgrid(np.arange(128), np.arange(4), indexing="ij")
+    off = L.cp_physical(0, r, w, 16, 128, 0)
+    assert np.array_equal(off // 4, np.arange(512).reshape(128, 4))
+
+
+def test_mma_page_example_operand_is_dense_and_k16_steps_are_32_bytes():
+    # "tcgen05.mma" page example: fp16 (128, 64) K-major, descriptor (16, 1024, 3).
+    m, k = np.meshgrid(np.arange(128), np.arange(64), indexing="ij")
+    off = L.mma_operand_offset(m, k, 2, "k", 16, 1024, 3)
+    assert np.array_equal(off, 128 * m + 2 * k)
+    # The K16 repeat (view "m (kr k) -> kr m k") moves the origin by 32 bytes.
+    for kr in range(4):
+        k16 = np.arange(16)
+        assert np.array_equal(L.mma_operand_offset(m[:, :16], 16 * kr + k16[None, :], 2, "k", 16, 1024, 3),
+                              L.mma_operand_offset(m[:, :16], k16[None, :], 2, "k", 16, 1024, 3) + 32 * kr)
+
+
+@pytest.mark.parametrize("s", [0, 1, 2, 3, 4])
+def test_swizzle_is_a_period_closed_bijection(s):
+    P = L.SWIZZLE_PERIOD[s] if s else 1024
+    a = np.arange(4 * P)
+    p = L.swizzle_addr(a, s)
+    assert np.array_equal(np.sort(p), a)                      # bijection
+    assert np.array_equal(L.swizzle_addr(p, s), a)            # involution
+    assert np.array_equal(p[P:] - P, p[:-P])                  # period closure
+    assert np.array_equal(p // L.SWIZZLE_PERIOD[s] if s else p // P, a // L.SWIZZLE_PERIOD[s] if s else a // P)
+
+
+@pytest.mark.parametrize("s,span,gran", [(1, 32, 16), (2, 64, 16), (3, 128, 16), (4, 128, 32)])
+def test_swizzle_matches_driver_header_description(s, span, gran):
+    # cuda.h, CUtensorMapSwizzle: "Swizzle 16B chunks within 32B/64B/128B span"
+    # and "Swizzle 32B chunks within 128B span" (the 128B_ATOM_32B mode).
+    a = np.arange(8192)
+    p = L.swizzle_addr(a, s)
+    assert np.array_equal(p // span, a // span)                # stays in its span
+    assert np.array_equal(p % gran, a % gran)                  # granules move whole
+    # row 0 of every period is left in place
+    per = L.SWIZZLE_PERIOD[s]
+    first = (a % per) < span
+    assert np.array_equal(p[first], a[first])
+
+
+def test_swizzle_mode4_page_formula_on_example_offsets():
+    # "swizzle=4": offset ^ ((offset >> 2) & 96): bytes 128..159 (K row 1,
+    # first 32B granule) land in granule 1 of that row.
+    assert L.swizzle_addr(128, 4) == 160
+    assert L.swizzle_addr(256 + 96, 4) == 256 + 32
+    assert L.swizzle_addr(384 + 64, 4) == 384 + 32  # row 3, granule 2 -> 2^3 = 1
+
+
+def test_cp_walk_swizzled_words_contiguous_and_ldo_ignored():
+    r, w = np.meshgrid(np.arange(16), np.arange(8), indexing="ij")
+    for s in (1, 2, 3):
+        a = L.cp_walk(r, w, 16, 1024, s)
+        b = L.cp_walk(r, w, 4096, 1024, s)
+        assert np.array_equal(a, b)
+        assert np.array_equal(a - L.cp_walk(r, 0 * w, 16, 1024, s), 4 * w)
+
+
+def test_descriptor_field_checks():
+    L.check_descriptor(0, 16, 1024, 3)
+    for bad in [(8, 16, 1024, 3), (0, 8, 1024, 3), (0, 16, 1 << 18, 3), (0, -16, 16, 0), (0, 16, 16, 5)]:
+        with pytest.raises(ValueError):
+            L.check_descriptor(*bad)
+
+
+def test_mma_mn_major_unswizzled_swaps_strides():
+    # MN-major unswizzled: row groups (of K) at LDO, contiguous 16-byte chunks at SDO.
+    mn, k = np.meshgrid(np.arange(32), np.arange(16), indexing="ij")
+    off = L.mma_operand_offset(mn, k, 2, "mn", 256, 4096, 0)
+    assert np.array_equal(off, (k // 8) * 256 + (k % 8) * 16 + (mn // 8) * 4096 + (mn % 8) * 2)
+    # and K-major unswizzled the other way round
+    off = L.mma_operand_offset(mn, k, 2, "k", 256, 4096, 0)
+    assert np.array_equal(off, (mn // 8) * 4096 + (mn % 8) * 16 + (k // 8) * 256 + (k % 8) * 2)
+
+
+@pytest.mark.parametrize("eb,s,ldo", [(2, 3, 8192), (1, 3, 16384), (4, 4, 4096), (2, 1, 4096)])
+def test_mma_mn_major_swizzled_tile_is_a_bijection(eb, s, ldo):
+    rb = L.row_bytes(s)
+    g = L.rows_per_group(s)
+    mn_n = 2 * rb // eb
+    k_n = 4 * g
+    sdo = g * rb
+    mn, k = np.meshgrid(np.arange(mn_n), np.arange(k_n), indexing="ij")
+    off = L.mma_operand_offset(mn, k, eb, "mn", ldo, sdo, s)
+    phys = L.swizzle_addr(off, s)
+    vals = np.sort(phys.ravel())
+    assert np.unique(vals // eb).size == mn_n * k_n
+
+
+# ------------------------------------------------------------ TMEM ld/st images
+
+@pytest.mark.parametrize("shape", L.LD_SHAPES)
+@pytest.mark.parametrize("n", [1, 2, 4, 8, 16, 32, 64, 128])
+def test_ld_images_are_bijections(shape, n):
+    if shape != "32x32b" and n > 64:
+        pytest.skip("x128 only for 32x32b")
+    regs = L.ld_regs_per_lane(shape, n)
+    rows, cols = L.ld_atom_extent(shape, n)
+    lanes = np.arange(32)[:, None]
+    rr = np.arange(regs)[None, :]
+    row, col = L.ld_owner(shape, lanes, rr)
+    assert row.min() >= 0 and row.max() < rows and col.min() >= 0 and col.max() < cols
+    assert np.unique(row * cols + col).size == rows * cols == 32 * regs
+
+
+def test_ld_32x32b_is_lane_row_register_column():
+    row, col = L.ld_owner("32x32b", np.arange(32)[:, None], np.arange(8)[None, :])
+    assert np.array_equal(row, np.repeat(np.arange(32)[:, None], 8, 1))
+    assert np.array_equal(col, np.repeat(np.arange(8)[None, :], 32, 0))
+
+
+def test_ld_16x256b_x1_is_mma_m16n8_accumulator_fragment():
+    # PTX ISA, mma.m16n8k16 f32 accumulator: groupID = lane>>2,
+    # threadID_in_group = lane%4; c0,c1 at (groupID, 2*tig + {0,1}),
+    # c2,c3 at (groupID + 8, 2*tig + {0,1}).
+    for lane in range(32):
+        g, t = lane >> 2, lane % 4
+        expect = [(g, 2 * t), (g, 2 * t + 1), (g + 8, 2 * t), (g + 8, 2 * t + 1)]
+        got = [tuple(int(v) for v in L.ld_owner("16x256b", lane, r)) for r in range(4)]
+        assert got == expect
+
+
+def test_layout_b_roundtrip_positions_cover_tmem():
+    i, j = np.meshgrid(np.arange(64), np.arange(128), indexing="ij")
+    lane, col = L.layout_b_position(i, j)
+    assert np.unique(lane * 64 + col).size == 128 * 64
+    # the page's explicit register layout: [i, j] -> thread i + 64*(j//64), slot j%64
+    assert np.array_equal(lane, i + 64 * (j // 64)) and np.array_equal(col, j % 64)
+
+
+# ------------------------------------------------------------ ldmatrix
+
+def test_ldmatrix_page_example_interleaved_slots():
+    # "ldmatrix / stmatrix" page example: x (16,4,2) = arange(128); shared
+    # layout (16,4,2):(8,1,128); S_std[k,m,r,w] = SM[2r+m, w, k]; two x2
+    # issues (k = 0, 1) into register slots {0, 2} and {8, 10}; every other
+    # slot keeps the sentinel 4294966519.
+    x = np.arange(128, dtype=np.uint64).reshape(16, 4, 2)
+    out = np.full((32, 12), 4294966519, dtype=np.uint64)
+    for k in range(2):
+        rows = [[[int(x[2 * r + m, w, k]) for w in range(4)] for r in range(8)] for m in range(2)]
+        regs = L.ldmatrix_load(rows, 2)
+        for lane in range(32):
+            for m in range(2):
+                # each b32 word is whole here (values < 2^16 sit in the low half)
+                out[lane, 8 * k + 2 * m] = regs[lane][m]
+    # expected array exactly as the page prints it
+    expected = np.full((32, 12), 4294966519, dtype=np.uint64)
+    for lane in range(32):
+        for k in range(2):
+            for matrix in range(2):
+                expected[lane, 8 * k + 2 * matrix] = x[2 * (lane // 4) + matrix, lane % 4, k]
+    assert np.array_equal(out, expected)
+
+
+def test_ldmatrix_address_providers_and_trans():
+    assert [L.ldmatrix_address_provider(m, r) for m in range(4) for r in range(8)] == list(range(32))
+    # .trans: register element (row, 2w+h) comes from shared element (2w+h, row)
+    rows = [[[((2 * w) + 16 * r) | (((2 * w + 1) + 16 * r) << 16) for w in range(4)] for r in range(8)]]
+    regs = L.ldmatrix_load(rows, 1, trans=True)  # shared element (r, c) holds 16r + c
+    for lane in range(32):
+        row, w = lane // 4, lane % 4
+        lo, hi = regs[lane][0] & 0xFFFF, regs[lane][0] >> 16
+        assert lo == 16 * (2 * w) + row and hi == 16 * (2 * w + 1) + row
+
+
+# ------------------------------------------------------------ scale factors
+
+def test_sf_chunk_offset_through_cp_warpx4_lands_where_mma_reads():
+    # "tcgen05.cp" table (32x128b.warpx4: 32 lanes, four replicas 32 apart) composed
+    # with the chunk offset must give the "tcgen05.mma" block-scale placement
+    # (lane r%32, byte-column 4*(r//32)+sf, four replicas).
+    for r, kb in itertools.product(range(128), range(4)):
+        off = int(L.sf_chunk_offset(r, kb))
+        lanes_cp, col_cp, byte_cp = L.cp_32x128b_warpx4_position(off // 16, off % 16)
+        lanes_sf, col_sf, byte_sf = L.sf_tmem_position(r, kb)
+        assert np.array_equal(lanes_cp, lanes_sf) and col_cp == col_sf and byte_cp == byte_sf
+
+
+def test_sf_chunk_offsets_fill_one_chunk_once():
+    r, kb = np.meshgrid(np.arange(128), np.arange(4), indexing="ij")
+    off = L.sf_chunk_offset(r, kb)
+    assert np.array_equal(np.sort(off.ravel()), np.arange(512))
+
+
+@pytest.mark.parametrize("rows,kblocks,tile_rows", [(128, 4, 128), (300, 9, 128), (256, 8, 256), (500, 5, 224)])
+def test_sf_prepare_is_invertible(rows, kblocks, tile_rows):
+    rng = np.random.default_rng(rows)
+    sf = rng.integers(0, 255, size=(rows, kblocks)).astype(np.uint8)
+    img = L.sf_prepare(sf, rows, kblocks, tile_rows)
+    for r in range(rows):
+        t, rl = divmod(r, tile_rows)
+        c, rc = divmod(rl, 128)
+        for kk in range(kblocks):
+            ks, kb = divmod(kk, 4)
+            assert img[ks, t, c, int(L.sf_chunk_offset(rc, kb))] == sf[r, kk]
