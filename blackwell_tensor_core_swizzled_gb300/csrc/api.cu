@@ -1,0 +1,609 @@
+// Host side of the C ABI declared in include/tcg.h: argument validation, TMA
+// tensor-map encoding, tile/variant selection, launches, the per-device error
+// word and the block-scale workspace.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <utility>
+
+#include "common.h"
+#include "gemm_kernel.cuh"
+
+namespace tcg {
+
+// Per-device error word: a kernel whose bounded wait runs out writes a code
+// here (see ErrSite); tcg_check() reads and clears it.
+__device__ unsigned long long g_error_word;
+
+namespace {
+
+thread_local std::string t_last_error;
+thread_local int t_last_launches = 0;
+std::atomic<uint64_t> g_timeout_ns{2000000000ull};
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  bool init = false;
+  bool usable = false;
+  int sms = 0;
+  unsigned long long* err = nullptr;
+  // per kernel host stub: smem attribute set, max co-resident clusters
+  std::map<const void*, int> max_clusters;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+struct Workspace {
+  void* ptr = nullptr;
+  size_t bytes = 0;
+};
+std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
+
+void load_timeout_env() {
+  static std::once_flag once;
+  std::call_once(once, [] {
+    if (const char* v = std::getenv("TCG_WAIT_TIMEOUT_NS")) {
+      const unsigned long long ns = std::strtoull(v, nullptr, 10);
+      if (ns > 0) g_timeout_ns.store(ns < 1000 ? 1000 : ns);
+    }
+  });
+}
+
+DeviceState* device_state(int dev) {
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState& d = g_dev[dev];
+  if (!d.init) {
+    d.init = true;
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return &d;
+    }
+    d.sms = prop.multiProcessorCount;
+    d.usable = (prop.major == 10 && prop.minor == 3);
+    void* p = nullptr;
+    if (d.usable && cudaGetSymbolAddress(&p, g_error_word) == cudaSuccess) {
+      d.err = static_cast<unsigned long long*>(p);
+      cudaMemset(d.err, 0, sizeof(unsigned long long));
+    } else {
+      cudaGetLastError();
+      d.usable = false;
+    }
+  }
+  return &d;
+}
+
+int encode_ready() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    else
+      cudaGetLastError();
+  });
+  return g_encode ? TCG_OK : TCG_ERR_CUDA;
+}
+
+// 2-D tiled tensor map over a row-major matrix: `inner` elements per row
+// (contiguous), `outer` rows, `ld` elements between rows.
+int make_map_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int esize, uint64_t inner,
+                uint64_t outer, uint64_t ld, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
+  if (encode_ready() != TCG_OK) {
+    t_last_error = "cuTensorMapEncodeTiled entry point unavailable";
+    return TCG_ERR_CUDA;
+  }
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {ld * static_cast<uint64_t>(esize)};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = g_encode(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    char buf[160];
+    std::snprintf(buf, sizeof buf, "cuTensorMapEncodeTiled failed (%d): dims %llu x %llu, ld %llu, box %u x %u",
+                  static_cast<int>(r), static_cast<unsigned long long>(inner),
+                  static_cast<unsigned long long>(outer), static_cast<unsigned long long>(ld), box_inner, box_outer);
+    t_last_error = buf;
+    return TCG_ERR_CUDA;
+  }
+  return TCG_OK;
+}
+
+int esize_of(tcg_input t) { return t == TCG_IN_TF32 ? 4 : t == TCG_IN_E4M3 ? 1 : 2; }
+int dsize_of(tcg_dtype t) { return t == TCG_F32 ? 4 : 2; }
+
+// Validates one operand; fills its leading dimension when 0 (packed).
+int check_operand(const void* ptr, tcg_major major, int64_t mn, int64_t K, int64_t* ld, int esize) {
+  if (major != TCG_K_MAJOR && major != TCG_MN_MAJOR) return TCG_ERR_INVALID;
+  const int64_t inner = major == TCG_K_MAJOR ? K : mn;
+  if (*ld == 0) *ld = inner;
+  if (*ld < inner || *ld < 1) return TCG_ERR_INVALID;
+  if (!ptr) return TCG_ERR_INVALID;
+  if (reinterpret_cast<uintptr_t>(ptr) % 16) return TCG_ERR_ALIGNMENT;
+  if ((*ld * esize) % 16) return TCG_ERR_ALIGNMENT;
+  return TCG_OK;
+}
+
+struct Plan {
+  KernelInfo ki;
+  int cta_group;
+};
+
+int pick_cta_group(const tcg_gemm_args& a) {
+  if (a.cta_group == 1 || a.cta_group == 2) return a.cta_group;
+  if (a.in_type == TCG_IN_E4M3 && a.b_major == TCG_MN_MAJOR) return 1;
+  // pairs halve the B traffic per SM; use them once there are enough 256-row tiles
+  return (a.M >= 1024 && a.N >= 1024) ? 2 : 1;
+}
+
+int get_plan(const tcg_gemm_args& a, Plan* plan) {
+  const int cg = pick_cta_group(a);
+  if (a.in_type == TCG_IN_E4M3 && cg == 2 && a.b_major == TCG_MN_MAJOR) return TCG_ERR_UNSUPPORTED;
+  plan->cta_group = cg;
+  switch (a.in_type) {
+    case TCG_IN_F16:
+    case TCG_IN_BF16: plan->ki = kinfo_f16(cg); break;
+    case TCG_IN_TF32: plan->ki = kinfo_tf32(cg); break;
+    case TCG_IN_E4M3: plan->ki = kinfo_mxf8(cg); break;
+    default: return TCG_ERR_INVALID;
+  }
+  return TCG_OK;
+}
+
+int max_clusters_for(DeviceState* d, const KernelInfo& ki, int* out) {
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = d->max_clusters.find(ki.func);
+    if (it != d->max_clusters.end()) {
+      *out = it->second;
+      return TCG_OK;
+    }
+  }
+  cudaError_t e = cudaFuncSetAttribute(ki.func, cudaFuncAttributeMaxDynamicSharedMemorySize, ki.smem_bytes);
+  if (e != cudaSuccess) return record_cuda(e);
+  int n = d->sms / ki.cta_group;
+  if (ki.cta_group > 1) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(ki.cta_group * n, 1, 1);
+    cfg.blockDim = dim3(ki.threads, 1, 1);
+    cfg.dynamicSmemBytes = ki.smem_bytes;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = ki.cta_group;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    e = cudaOccupancyMaxActiveClusters(&clusters, ki.func, &cfg);
+    if (e == cudaSuccess && clusters > 0)
+      n = std::min(n, clusters);
+    else
+      cudaGetLastError();
+  }
+  std::lock_guard<std::mutex> lk(g_mu);
+  d->max_clusters[ki.func] = n;
+  *out = n;
+  return TCG_OK;
+}
+
+int launch_gemm(const KernelInfo& ki, const GemmParams& prm, int clusters, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ki.cta_group * clusters, 1, 1);
+  cfg.blockDim = dim3(ki.threads, 1, 1);
+  cfg.dynamicSmemBytes = ki.smem_bytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr;
+  if (ki.cta_group > 1) {
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = ki.cta_group;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+  }
+  void* args[] = {const_cast<GemmParams*>(&prm)};
+  const cudaError_t e = cudaLaunchKernelExC(&cfg, ki.func, args);
+  if (e != cudaSuccess) return record_cuda(e);
+  return TCG_OK;
+}
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int64_t sf_image_bytes(int64_t rows, int64_t K, int tile_rows) {
+  const int64_t ksteps = cdiv(cdiv(K, 32), 4);
+  return ksteps * cdiv(rows, tile_rows) * cdiv(tile_rows, 128) * 512;
+}
+
+int workspace(int dev, cudaStream_t s, size_t bytes, void** out) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  Workspace& w = g_ws[std::make_pair(dev, s)];
+  if (w.bytes < bytes) {
+    if (w.ptr) {
+      cudaError_t e = cudaFree(w.ptr);  // synchronises: no queued kernel still reads it
+      w.ptr = nullptr;
+      w.bytes = 0;
+      if (e != cudaSuccess) return record_cuda(e);
+    }
+    const size_t want = std::max(bytes, static_cast<size_t>(1) << 20);
+    cudaError_t e = cudaMalloc(&w.ptr, want);
+    if (e != cudaSuccess) return record_cuda(e);
+    w.bytes = want;
+  }
+  *out = w.ptr;
+  return TCG_OK;
+}
+
+CUtensorMapDataType map_dtype(tcg_input t) {
+  switch (t) {
+    case TCG_IN_F16: return CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    case TCG_IN_BF16: return CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    case TCG_IN_TF32: return CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    default: return CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  }
+}
+
+// Tensor map + descriptor constants for one operand tile of `rows` M/N rows
+// and one ring stage of K (128 bytes).
+int setup_operand(const void* ptr, tcg_input it, tcg_major major, int64_t mn, int64_t K, int64_t ld, int rows,
+                  CUtensorMap* map, int* mn_major, int* boxes, int* box_mn, uint32_t* box_bytes, uint64_t* desc_hi,
+                  uint32_t* kstep) {
+  const int es = esize_of(it);
+  const int bk = 128 / es;  // K elements per stage
+  const int mma_k = it == TCG_IN_TF32 ? 8 : it == TCG_IN_E4M3 ? 32 : 16;
+  const CUtensorMapDataType dt = map_dtype(it);
+  if (major == TCG_K_MAJOR) {
+    // rows enumerate M/N: one 128-byte swizzle row per M/N row, 8-row groups
+    // 1024 bytes apart (SDO); the K step moves the start 32 bytes.
+    *mn_major = 0;
+    *boxes = 1;
+    *box_mn = 0;
+    *box_bytes = static_cast<uint32_t>(rows) * 128u;
+    *desc_hi = sdesc_hi(16, 1024, SW_128B);
+    *kstep = static_cast<uint32_t>(mma_k * es);
+    return make_map_2d(map, ptr, dt, es, static_cast<uint64_t>(K), static_cast<uint64_t>(mn),
+                       static_cast<uint64_t>(ld), static_cast<uint32_t>(bk), static_cast<uint32_t>(rows),
+                       CU_TENSOR_MAP_SWIZZLE_128B);
+  }
+  // MN-major: rows enumerate K; one 128-byte row holds 128/es M/N elements.
+  *mn_major = 1;
+  const int chunk = 128 / es;
+  *box_mn = chunk;
+  *boxes = (rows + chunk - 1) / chunk;
+  *box_bytes = static_cast<uint32_t>(bk) * 128u;
+  if (it == TCG_IN_TF32) {
+    // "swizzle=4": four K rows of 128 bytes per SDO, LDO to the next 128-byte chunk
+    *desc_hi = sdesc_hi(*box_bytes, 512, SW_128B_ATOM32);
+    *kstep = static_cast<uint32_t>(mma_k / 4) * 512u;
+  } else {
+    *desc_hi = sdesc_hi(*box_bytes, 1024, SW_128B);
+    *kstep = static_cast<uint32_t>(mma_k / 8) * 1024u;
+  }
+  return make_map_2d(map, ptr, dt, es, static_cast<uint64_t>(mn), static_cast<uint64_t>(K),
+                     static_cast<uint64_t>(ld), static_cast<uint32_t>(chunk), static_cast<uint32_t>(bk),
+                     it == TCG_IN_TF32 ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B : CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+int run_gemm(const tcg_gemm_args* args, cudaStream_t s) {
+  load_timeout_env();
+  t_last_launches = 0;
+  if (!args) return TCG_ERR_INVALID;
+  tcg_gemm_args a = *args;
+  if (a.M < 0 || a.N < 0 || a.K < 0) return TCG_ERR_INVALID;
+  if (a.in_type < TCG_IN_F16 || a.in_type > TCG_IN_E4M3) return TCG_ERR_INVALID;
+  if (a.d_type < TCG_F32 || a.d_type > TCG_BF16 || a.acc_type < TCG_F32 || a.acc_type > TCG_BF16)
+    return TCG_ERR_INVALID;
+  if (a.acc_type == TCG_BF16) return TCG_ERR_UNSUPPORTED;
+  if (a.acc_type == TCG_F16 && (a.in_type != TCG_IN_F16 || a.d_type != TCG_F16)) return TCG_ERR_UNSUPPORTED;
+  if (a.cta_group < 0 || a.cta_group > 2 || a.raster_group < 0) return TCG_ERR_INVALID;
+  if (a.M > INT32_MAX / 2 || a.N > INT32_MAX / 2 || a.K > INT32_MAX / 2) return TCG_ERR_UNSUPPORTED;
+  if (a.M == 0 || a.N == 0) return TCG_OK;
+  if (!a.D) return TCG_ERR_INVALID;
+  if (a.ldd == 0) a.ldd = a.N;
+  if (a.ldd < a.N) return TCG_ERR_INVALID;
+  const int ds = dsize_of(a.d_type);
+  if (reinterpret_cast<uintptr_t>(a.D) % ds) return TCG_ERR_ALIGNMENT;
+  const bool scaled = a.in_type == TCG_IN_E4M3;
+  if (a.K > 0) {
+    const int es = esize_of(a.in_type);
+    if (int rc = check_operand(a.A, a.a_major, a.M, a.K, &a.lda, es)) return rc;
+    if (int rc = check_operand(a.B, a.b_major, a.N, a.K, &a.ldb, es)) return rc;
+    if (scaled) {
+      const bool plain = a.SFA || a.SFB;
+      const bool img = a.SFA_img || a.SFB_img;
+      if (plain == img) return TCG_ERR_INVALID;
+      if (plain && (!a.SFA || !a.SFB)) return TCG_ERR_INVALID;
+      if (img && (!a.SFA_img || !a.SFB_img)) return TCG_ERR_INVALID;
+      if (img && ((reinterpret_cast<uintptr_t>(a.SFA_img) | reinterpret_cast<uintptr_t>(a.SFB_img)) % 16))
+        return TCG_ERR_ALIGNMENT;
+    } else if (a.SFA || a.SFB || a.SFA_img || a.SFB_img) {
+      return TCG_ERR_INVALID;
+    }
+  }
+  Plan plan;
+  if (int rc = get_plan(a, &plan)) return rc;
+  int dev;
+  if (int rc = current_device_checked(&dev)) return rc;
+  DeviceState* d = device_state(dev);
+
+  if (a.K == 0) {
+    const cudaError_t e = cudaMemset2DAsync(a.D, static_cast<size_t>(a.ldd) * ds, 0, static_cast<size_t>(a.N) * ds,
+                                            static_cast<size_t>(a.M), s);
+    if (e != cudaSuccess) return record_cuda(e);
+    t_last_launches = 1;
+    return TCG_OK;
+  }
+
+  const KernelInfo& ki = plan.ki;
+  const int cg = plan.cta_group;
+  const int bn = ki.bn;
+  GemmParams prm;
+  std::memset(&prm, 0, sizeof prm);
+  prm.M = static_cast<int>(a.M);
+  prm.N = static_cast<int>(a.N);
+  prm.K = static_cast<int>(a.K);
+  prm.num_m_tiles = static_cast<int>(cdiv(a.M, 128 * cg));
+  prm.num_n_tiles = static_cast<int>(cdiv(a.N, bn));
+  const int es = esize_of(a.in_type);
+  prm.num_k_blocks = static_cast<int>(cdiv(a.K * es, 128));
+  prm.num_tiles = prm.num_m_tiles * prm.num_n_tiles;
+  prm.raster_group = a.raster_group > 0 ? a.raster_group : 8;
+  if (int rc = setup_operand(a.A, a.in_type, a.a_major, a.M, a.K, a.lda, 128, &prm.tmap_a, &prm.a_mn_major,
+                             &prm.a_boxes, &prm.a_box_mn, &prm.a_box_bytes, &prm.a_desc_hi, &prm.a_kstep))
+    return rc;
+  if (int rc = setup_operand(a.B, a.in_type, a.b_major, a.N, a.K, a.ldb, bn / cg, &prm.tmap_b, &prm.b_mn_major,
+                             &prm.b_boxes, &prm.b_box_mn, &prm.b_box_bytes, &prm.b_desc_hi, &prm.b_kstep))
+    return rc;
+  const bool a_mn = a.a_major == TCG_MN_MAJOR, b_mn = a.b_major == TCG_MN_MAJOR;
+  if (a.in_type == TCG_IN_TF32)
+    prm.idesc = idesc_tf32(a_mn, b_mn, 128 * cg, bn);
+  else if (scaled)
+    prm.idesc = idesc_mxf8(a_mn, b_mn, 128 * cg, bn);
+  else
+    prm.idesc = idesc_f16(a.in_type == TCG_IN_BF16, a.acc_type == TCG_F32, a_mn, b_mn, 128 * cg, bn);
+  prm.D = a.D;
+  prm.ldd = a.ldd;
+  prm.d_type = a.d_type == TCG_F32 ? OUT_F32 : a.d_type == TCG_F16 ? OUT_F16 : OUT_BF16;
+  prm.acc_f16 = a.acc_type == TCG_F16;
+  prm.d_vec_ok = (reinterpret_cast<uintptr_t>(a.D) % 16 == 0) && ((a.ldd * ds) % 16 == 0);
+  prm.err = d->err;
+  prm.timeout_ns = g_timeout_ns.load();
+
+  int launches = 0;
+  if (scaled) {
+    const int sfa_tiles = static_cast<int>(cdiv(a.M, 128));
+    const int chunks = static_cast<int>(cdiv(bn, 128));
+    const int64_t ksteps = cdiv(cdiv(a.K, 32), 4);
+    const uint8_t* sfa_img = a.SFA_img;
+    const uint8_t* sfb_img = a.SFB_img;
+    if (!sfa_img) {
+      const size_t ba = static_cast<size_t>(sf_image_bytes(a.M, a.K, 128));
+      const size_t bb = static_cast<size_t>(sf_image_bytes(a.N, a.K, bn));
+      void* ws = nullptr;
+      if (int rc = workspace(dev, s, ba + bb, &ws)) return rc;
+      uint8_t* wa = static_cast<uint8_t*>(ws);
+      uint8_t* wb = wa + ba;  // ba is a multiple of 512
+      cudaError_t e = launch_sf_prepare(a.SFA, a.M, a.K, 128, wa, s);
+      if (e == cudaSuccess) e = launch_sf_prepare(a.SFB, a.N, a.K, bn, wb, s);
+      if (e != cudaSuccess) return record_cuda(e);
+      launches += 2;
+      sfa_img = wa;
+      sfb_img = wb;
+    }
+    prm.sf_a_tiles = sfa_tiles;
+    if (int rc = make_map_2d(&prm.tmap_sfa, sfa_img, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, 128,
+                             static_cast<uint64_t>(ksteps * sfa_tiles), 128, 128, 1, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return rc;
+    if (int rc = make_map_2d(&prm.tmap_sfb, sfb_img, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4,
+                             static_cast<uint64_t>(128 * chunks), static_cast<uint64_t>(ksteps * prm.num_n_tiles),
+                             static_cast<uint64_t>(128 * chunks), static_cast<uint32_t>(128 * chunks), 1,
+                             CU_TENSOR_MAP_SWIZZLE_NONE))
+      return rc;
+  }
+
+  int max_clusters = 0;
+  if (int rc = max_clusters_for(d, ki, &max_clusters)) return rc;
+  const int clusters = std::max(1, std::min(prm.num_tiles, max_clusters));
+  if (int rc = launch_gemm(ki, prm, clusters, s)) return rc;
+  t_last_launches = launches + 1;
+  return TCG_OK;
+}
+
+}  // namespace
+
+int record_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return TCG_OK;
+  t_last_error = std::string(cudaGetErrorName(e)) + ": " + cudaGetErrorString(e);
+  return TCG_ERR_CUDA;
+}
+
+int current_device_checked(int* dev) {
+  int d = 0;
+  cudaError_t e = cudaGetDevice(&d);
+  if (e != cudaSuccess) {
+    record_cuda(e);
+    cudaGetLastError();
+    return TCG_ERR_NO_DEVICE;
+  }
+  DeviceState* st = device_state(d);
+  if (!st || !st->usable) {
+    t_last_error = "current device is not an sm_103 GPU";
+    return TCG_ERR_NO_DEVICE;
+  }
+  *dev = d;
+  return TCG_OK;
+}
+
+unsigned long long* device_error_word(int dev) {
+  DeviceState* st = device_state(dev);
+  return st ? st->err : nullptr;
+}
+
+uint64_t wait_timeout_ns() {
+  load_timeout_env();
+  return g_timeout_ns.load();
+}
+
+void set_launch_count(int n) { t_last_launches = n; }
+
+}  // namespace tcg
+
+using namespace tcg;
+
+namespace {
+
+int named_gemm(tcg_input in, int64_t M, int64_t N, int64_t K, const void* A, tcg_major a_major, int64_t lda,
+               const void* B, tcg_major b_major, int64_t ldb, const uint8_t* SFA, const uint8_t* SFB, void* D,
+               tcg_dtype d_type, int64_t ldd, tcg_dtype acc_type, void* stream) {
+  tcg_gemm_args a;
+  std::memset(&a, 0, sizeof a);
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.in_type = in;
+  a.A = A;
+  a.a_major = a_major;
+  a.lda = lda;
+  a.B = B;
+  a.b_major = b_major;
+  a.ldb = ldb;
+  a.SFA = SFA;
+  a.SFB = SFB;
+  a.D = D;
+  a.d_type = d_type;
+  a.ldd = ldd;
+  a.acc_type = acc_type;
+  return run_gemm(&a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+int tcg_gemm(const tcg_gemm_args* args, void* stream) {
+  return run_gemm(args, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int tcg_gemm_f16(int64_t M, int64_t N, int64_t K, const void* A, tcg_major a_major, int64_t lda, const void* B,
+                 tcg_major b_major, int64_t ldb, void* D, tcg_dtype d_type, int64_t ldd, tcg_dtype acc_type,
+                 void* stream) {
+  return named_gemm(TCG_IN_F16, M, N, K, A, a_major, lda, B, b_major, ldb, nullptr, nullptr, D, d_type, ldd, acc_type,
+                    stream);
+}
+
+int tcg_gemm_bf16(int64_t M, int64_t N, int64_t K, const void* A, tcg_major a_major, int64_t lda, const void* B,
+                  tcg_major b_major, int64_t ldb, void* D, tcg_dtype d_type, int64_t ldd, tcg_dtype acc_type,
+                  void* stream) {
+  return named_gemm(TCG_IN_BF16, M, N, K, A, a_major, lda, B, b_major, ldb, nullptr, nullptr, D, d_type, ldd,
+                    acc_type, stream);
+}
+
+int tcg_gemm_tf32(int64_t M, int64_t N, int64_t K, const void* A, tcg_major a_major, int64_t lda, const void* B,
+                  tcg_major b_major, int64_t ldb, void* D, tcg_dtype d_type, int64_t ldd, tcg_dtype acc_type,
+                  void* stream) {
+  return named_gemm(TCG_IN_TF32, M, N, K, A, a_major, lda, B, b_major, ldb, nullptr, nullptr, D, d_type, ldd,
+                    acc_type, stream);
+}
+
+int tcg_gemm_mxf8_blockscaled(int64_t M, int64_t N, int64_t K, const void* A, tcg_major a_major, int64_t lda,
+                              const void* B, tcg_major b_major, int64_t ldb, const uint8_t* SFA,
+                              const uint8_t* SFB, void* D, tcg_dtype d_type, int64_t ldd, tcg_dtype acc_type,
+                              void* stream) {
+  if (K > 0 && (!SFA || !SFB)) return TCG_ERR_INVALID;
+  return named_gemm(TCG_IN_E4M3, M, N, K, A, a_major, lda, B, b_major, ldb, SFA, SFB, D, d_type, ldd, acc_type,
+                    stream);
+}
+
+int64_t tcg_mxf8_scale_image_bytes(int64_t rows, int64_t K, int tile_rows) {
+  if (rows < 0 || K < 0 || tile_rows <= 0) return -1;
+  return sf_image_bytes(rows, K, tile_rows);
+}
+
+int tcg_mxf8_tile_n(int64_t M, int64_t N, int64_t K, tcg_major b_major, int cta_group) {
+  tcg_gemm_args a;
+  std::memset(&a, 0, sizeof a);
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.in_type = TCG_IN_E4M3;
+  a.b_major = b_major;
+  a.cta_group = cta_group;
+  Plan p;
+  if (int rc = get_plan(a, &p)) return rc;
+  return p.ki.bn;
+}
+
+int tcg_mxf8_prepare_scales(const uint8_t* sf, int64_t rows, int64_t K, int tile_rows, uint8_t* img, void* stream) {
+  if (rows < 0 || K < 0 || tile_rows <= 0 || tile_rows > 65536) return TCG_ERR_INVALID;
+  if (rows == 0 || K == 0) return TCG_OK;
+  if (!sf || !img) return TCG_ERR_INVALID;
+  int dev;
+  if (int rc = current_device_checked(&dev)) return rc;
+  const cudaError_t e = launch_sf_prepare(sf, rows, K, tile_rows, img, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return record_cuda(e);
+  set_launch_count(1);
+  return TCG_OK;
+}
+
+int tcg_check(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return record_cuda(e);
+  int dev = 0;
+  e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return record_cuda(e);
+  DeviceState* st = device_state(dev);
+  if (!st || !st->err) return TCG_OK;
+  unsigned long long w = 0;
+  e = cudaMemcpy(&w, st->err, sizeof w, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return record_cuda(e);
+  if (w == 0) return TCG_OK;
+  e = cudaMemset(st->err, 0, sizeof w);
+  if (e != cudaSuccess) return record_cuda(e);
+  char buf[128];
+  std::snprintf(buf, sizeof buf, "kernel wait timed out (site %llu, block %llu)", (w >> 8) & 0xFF, (w >> 16) & 0xFFFFFFFF);
+  t_last_error = buf;
+  return (w & 0xFF) == 1 ? TCG_ERR_TIMEOUT : TCG_ERR_CUDA;
+}
+
+void tcg_set_wait_timeout_ns(uint64_t ns) {
+  load_timeout_env();
+  g_timeout_ns.store(ns < 1000 ? 1000 : ns);
+}
+
+const char* tcg_status_string(int status) {
+  switch (status) {
+    case TCG_OK: return "ok";
+    case TCG_ERR_INVALID: return "invalid argument";
+    case TCG_ERR_ALIGNMENT: return "misaligned pointer or leading dimension (TMA needs 16-byte alignment)";
+    case TCG_ERR_UNSUPPORTED: return "unsupported combination";
+    case TCG_ERR_CUDA: return "CUDA error";
+    case TCG_ERR_TIMEOUT: return "kernel wait timed out";
+    case TCG_ERR_NO_DEVICE: return "no usable sm_103 device";
+    default: return "unknown status";
+  }
+}
+
+const char* tcg_last_error_string(void) { return t_last_error.c_str(); }
+
+int tcg_last_launch_count(void) { return t_last_launches; }
+
+}  // extern "C"

@@ -1,0 +1,40 @@
+// Internal host-side interface shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "tcg.h"
+
+namespace tcg {
+
+struct GemmParams;
+
+// One compiled GEMM kernel variant.
+struct KernelInfo {
+  const void* func;  // host stub of the __global__ function
+  int smem_bytes;    // dynamic shared memory it needs
+  int cta_group;     // 1 or 2 (cluster of 2 CTAs)
+  int bn;            // accumulator columns (N tile)
+  int kind;          // Kind
+  int threads;
+};
+
+// Variant getters (one per translation unit that instantiates kernels).
+KernelInfo kinfo_f16(int cta_group);
+KernelInfo kinfo_tf32(int cta_group);
+KernelInfo kinfo_mxf8(int cta_group);  // cta_group 2: BN 224, 2 accumulators; 1: BN 256, 1 accumulator
+
+// Scale-factor rearrangement kernel launch (gemm_mxf8.cu).
+cudaError_t launch_sf_prepare(const uint8_t* sf, int64_t rows, int64_t K, int tile_rows, uint8_t* img,
+                              cudaStream_t stream);
+
+// Host state helpers (api.cu).
+int record_cuda(cudaError_t e);              // stores the message, returns TCG_ERR_CUDA (or TCG_OK)
+int current_device_checked(int* dev);        // TCG_OK if the current device is usable sm_103
+unsigned long long* device_error_word(int dev);
+uint64_t wait_timeout_ns();
+void set_launch_count(int n);
+
+}  // namespace tcg

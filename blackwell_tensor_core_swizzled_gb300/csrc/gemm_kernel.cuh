@@ -1,0 +1,472 @@
+// Persistent, warp-specialised tcgen05 GEMM for sm_103a.
+//
+//   D[m,n] = sum_k A[m,k] B[k,n]       (kind::f16, kind::tf32)
+//   D[m,n] = sum_k (SFA.A)[m,k] (SFB.B)[k,n]   (kind::mxf8f6f4.block_scale)
+//
+// Structure (one CTA per SM, or one CTA pair per two SMs for cta_group::2):
+//   warp 0      TMA producer: 128B-swizzled A/B tiles (and scale images) into
+//               a STAGES-deep ring, full[s] barriers counting bytes;
+//   warp 1      MMA issuer (one thread; pair leader only): for each ring stage
+//               the tcgen05.cp scale staging (block-scaled) and KSTEPS
+//               tcgen05.mma issues, then tcgen05.commit -> empty[s]; at the
+//               end of a tile a commit -> acc_full[b];
+//   warp 2      TMEM allocation / deallocation (512 columns);
+//   warps 4..7  epilogue: tcgen05.ld .32x32b from accumulator b (warp w
+//               reads lanes 32*(w%4)..+31), convert, store to global, then
+//               arrive acc_empty[b].
+// Accumulators are double buffered in TMEM so the epilogue of one tile
+// overlaps the main loop of the next.
+//
+// The MMA issue follows the "tcgen05.mma" page: one elected thread issues the
+// K repeats as separate instructions with accumulation disabled only on the
+// very first, and one commit covers the sequence; the epilogue follows the
+// "tcgen05.ld / tcgen05.st" page's completion rules (commit, mbarrier wait,
+// tcgen05.fence::after_thread_sync, ld, wait::ld).  Block-scale placement in
+// TMEM is the page's "lane r%32, byte-column 4*(r//32)+sf, four replicas",
+// produced by tcgen05.cp .32x128b.warpx4 ("tcgen05.cp" page, shape table).
+//
+// Every mbarrier wait is bounded (GemmParams::timeout_ns); a wait that runs
+// out records an error word, raises a CTA-local abort flag and the kernel
+// drains its in-flight copies / MMAs (again bounded), frees TMEM and returns.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <cstdint>
+
+#include "desc.cuh"
+#include "ptx.cuh"
+
+namespace tcg {
+
+enum Kind : int { KIND_F16 = 0, KIND_TF32 = 1, KIND_MXF8 = 2 };
+enum OutType : int { OUT_F32 = 0, OUT_F16 = 1, OUT_BF16 = 2 };
+
+// Error word layout: bits [0,8) status (1 = wait timeout), [8,16) site,
+// [16,48) block index.
+enum ErrSite : uint32_t {
+  SITE_PROD_EMPTY = 1,
+  SITE_MMA_FULL = 2,
+  SITE_MMA_ACC_EMPTY = 3,
+  SITE_EPI_ACC_FULL = 4,
+  SITE_DRAIN = 5,
+  SITE_PROBE = 6
+};
+
+struct GemmParams {
+  CUtensorMap tmap_a;
+  CUtensorMap tmap_b;
+  CUtensorMap tmap_sfa;
+  CUtensorMap tmap_sfb;
+  int M, N, K;
+  int num_m_tiles;   // tiles of 128*CG rows
+  int num_n_tiles;   // tiles of BN columns
+  int num_k_blocks;  // ring stages per tile (128 bytes of K each)
+  int num_tiles;
+  int raster_group;
+  int a_mn_major, b_mn_major;
+  int a_boxes, b_boxes;  // TMA boxes per stage (1 for K-major)
+  int a_box_mn, b_box_mn;  // M/N extent of one MN-major box
+  uint32_t a_box_bytes, b_box_bytes;
+  uint64_t a_desc_hi, b_desc_hi;
+  uint32_t a_kstep, b_kstep;  // descriptor start advance (bytes) per MMA K step
+  uint32_t idesc;
+  int sf_a_tiles;  // 128-row SFA tiles per K step in the scale image
+  void* D;
+  int64_t ldd;
+  int d_type;
+  int acc_f16;
+  int d_vec_ok;
+  unsigned long long* err;
+  uint64_t timeout_ns;
+};
+
+template <int CG, int BN, int ACC, int STAGES, int KIND>
+struct GemmCfg {
+  static constexpr int BM = 128;            // accumulator rows per CTA
+  static constexpr int BN_LOCAL = BN / CG;  // B rows staged per CTA
+  static constexpr int A_BYTES = BM * 128;
+  static constexpr int B_BYTES = BN_LOCAL * 128;
+  static constexpr int SFB_CHUNKS = (BN + 127) / 128;
+  static constexpr int SFA_BYTES = KIND == KIND_MXF8 ? 512 : 0;
+  static constexpr int SFB_BYTES = KIND == KIND_MXF8 ? 512 * SFB_CHUNKS : 0;
+  static constexpr int LOAD_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+  static constexpr int STAGE_BYTES = (LOAD_BYTES + 1023) / 1024 * 1024;
+  static constexpr int TX_BYTES = LOAD_BYTES * CG;
+  static constexpr int MMA_M = 128 * CG;
+  static constexpr int MMA_K = KIND == KIND_F16 ? 16 : KIND == KIND_TF32 ? 8 : 32;
+  static constexpr int ELEM_BYTES = KIND == KIND_F16 ? 2 : KIND == KIND_TF32 ? 4 : 1;
+  static constexpr int BK = 128 / ELEM_BYTES;  // K elements per stage
+  static constexpr int KSTEPS = BK / MMA_K;    // MMA issues per stage
+  static constexpr int SF_COL0 = ACC * BN;     // scale-factor slots follow the accumulators
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int SF_SLOT_COLS = 16;      // SFA 4 columns + SFB 4 per 128 rows
+  // Scale slots rotate over the free TMEM columns; before a slot is
+  // rewritten the MMA thread waits for the stage that last used it to retire.
+  static constexpr int SF_SLOTS_FREE = (TMEM_COLS - ACC * BN) / SF_SLOT_COLS;
+  static constexpr int SF_SLOTS = SF_SLOTS_FREE < 4 ? SF_SLOTS_FREE : 4;
+  static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
+  static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC + 1;
+  static constexpr int SMEM_BYTES = 1024 + BAR_OFF + NUM_BARS * 8 + 16;
+  static constexpr int THREADS = 256;
+  static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "epilogue drains 32-column chunks");
+  static_assert(BN % (16 * CG) == 0, "MMA N constraint / per-CTA B split");
+  static_assert(ACC * BN + (KIND == KIND_MXF8 ? SF_SLOTS * SF_SLOT_COLS : 0) <= TMEM_COLS, "TMEM budget");
+  static_assert(KIND != KIND_MXF8 || (SF_SLOTS >= 1 && SF_SLOTS <= STAGES), "scale slots");
+  static_assert(KIND != KIND_MXF8 || SFB_CHUNKS * 4 + 4 <= SF_SLOT_COLS, "scale slot too small");
+  static_assert(SMEM_BYTES <= 232448, "dynamic shared memory");
+};
+
+struct WaitCtx {
+  uint64_t timeout_ns;
+  unsigned long long* err;
+  volatile uint32_t* abort_flag;
+};
+
+__device__ __forceinline__ unsigned long long make_err(uint32_t status, uint32_t site) {
+  return static_cast<unsigned long long>(status) | (static_cast<unsigned long long>(site) << 8) |
+         (static_cast<unsigned long long>(blockIdx.x) << 16);
+}
+
+// Bounded parity wait by the calling thread.  Returns false on timeout (error
+// recorded, abort raised) or when another role already aborted.
+static __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, WaitCtx w, uint32_t site) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (;;) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*w.abort_flag) return false;
+    if (globaltimer() - t0 > w.timeout_ns) {
+      *w.abort_flag = 1u;
+      if (w.err) atomicCAS(w.err, 0ull, make_err(1u, site));
+      return false;
+    }
+  }
+}
+
+// Every lane waits (each gets its own acquire), the outcome is made uniform
+// across the warp.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, WaitCtx w, uint32_t site) {
+  const bool ok = wait_bounded(bar, parity, w, site);
+  return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ void tile_coords(int t, const GemmParams& p, int& mt, int& nt) {
+  const int G = p.raster_group;
+  const int per_group = G * p.num_n_tiles;
+  const int g = t / per_group;
+  const int first_m = g * G;
+  const int gs = min(p.num_m_tiles - first_m, G);
+  const int r = t - g * per_group;
+  mt = first_m + r % gs;
+  nt = r / gs;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(uint32_t lo, uint32_t hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(lo), __uint_as_float(hi));
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint32_t pack_f16(uint32_t lo, uint32_t hi) {
+  __half2 v = __floats2half2_rn(__uint_as_float(lo), __uint_as_float(hi));
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Store 32 consecutive output columns of one row from 16 packed 16-bit pairs.
+__device__ __forceinline__ void store_row16(const GemmParams& p, int row, int col0, const uint32_t (&h)[16]) {
+  const int ncols = min(32, p.N - col0);
+  uint16_t* dst = reinterpret_cast<uint16_t*>(p.D) + static_cast<int64_t>(row) * p.ldd + col0;
+  if (ncols == 32 && p.d_vec_ok) {
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) d4[i] = make_uint4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (i < ncols) dst[i] = static_cast<uint16_t>((h[i >> 1] >> (16 * (i & 1))) & 0xFFFFu);
+  }
+}
+
+// Store 32 consecutive fp32 accumulator columns of one row, converted.
+__device__ __forceinline__ void store_row32(const GemmParams& p, int row, int col0, const uint32_t (&r)[32]) {
+  if (p.d_type == OUT_F32) {
+    const int ncols = min(32, p.N - col0);
+    uint32_t* dst = reinterpret_cast<uint32_t*>(p.D) + static_cast<int64_t>(row) * p.ldd + col0;
+    if (ncols == 32 && p.d_vec_ok) {
+      uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) d4[i] = make_uint4(r[4 * i], r[4 * i + 1], r[4 * i + 2], r[4 * i + 3]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (i < ncols) dst[i] = r[i];
+    }
+  } else {
+    uint32_t h[16];
+    if (p.d_type == OUT_BF16) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) h[i] = pack_bf16(r[2 * i], r[2 * i + 1]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) h[i] = pack_f16(r[2 * i], r[2 * i + 1]);
+    }
+    store_row16(p, row, col0, h);
+  }
+}
+
+template <int CG, int BN, int ACC, int STAGES, int KIND>
+__global__ void __launch_bounds__(256, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
+  using C = GemmCfg<CG, BN, ACC, STAGES, KIND>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (sbase - raw);
+  const uint32_t bar0 = sbase + C::BAR_OFF;
+  // barrier addresses
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto accf_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
+  auto acce_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + ACC + b); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 2 * ACC);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::BAR_OFF + 8 * C::NUM_BARS);
+  volatile uint32_t* abort_flag = tmem_slot + 1;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = (CG == 2) ? cluster_ctarank() : 0u;
+  const int cluster_id = blockIdx.x / CG;
+  const int num_clusters = gridDim.x / CG;
+  const WaitCtx wctx{p.timeout_ns, p.err, abort_flag};
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < ACC; ++b) {
+      mbar_init(accf_bar(b), 1);
+      mbar_init(acce_bar(b), 4 * CG);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0u;
+    fence_mbarrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&p.tmap_a);
+    prefetch_tmap(&p.tmap_b);
+    if constexpr (KIND == KIND_MXF8) {
+      prefetch_tmap(&p.tmap_sfa);
+      prefetch_tmap(&p.tmap_sfb);
+    }
+  }
+  if (warp == 2) {
+    tmem_alloc<CG>(smem_u32(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish<CG>();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if constexpr (CG == 2) cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    uint32_t it = 0;
+    bool ok = true;
+    for (int t = cluster_id; t < p.num_tiles && ok; t += num_clusters) {
+      int mt, nt;
+      tile_coords(t, p, mt, nt);
+      const int m0 = mt * C::MMA_M + static_cast<int>(rank) * C::BM;
+      const int n0 = nt * BN + static_cast<int>(rank) * C::BN_LOCAL;
+      for (int kb = 0; kb < p.num_k_blocks; ++kb, ++it) {
+        const int s = static_cast<int>(it % STAGES);
+        const uint32_t ph = (it / STAGES) & 1u;
+        if (!warp_wait(empty_bar(s), ph ^ 1u, wctx, SITE_PROD_EMPTY)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          const uint32_t fb = (CG == 2) ? mapa_shared(full_bar(s), 0) : full_bar(s);
+          if (rank == 0) mbar_arrive_expect_tx(full_bar(s), C::TX_BYTES);
+          const uint32_t sa = sbase + s * C::STAGE_BYTES;
+          const uint32_t sb = sa + C::A_BYTES;
+          const int k0 = kb * C::BK;
+          if (!p.a_mn_major) {
+            tma_load<CG>(sa, &p.tmap_a, k0, m0, fb);
+          } else {
+            for (int i = 0; i < p.a_boxes; ++i) tma_load<CG>(sa + i * p.a_box_bytes, &p.tmap_a, m0 + i * p.a_box_mn, k0, fb);
+          }
+          if (!p.b_mn_major) {
+            tma_load<CG>(sb, &p.tmap_b, k0, n0, fb);
+          } else {
+            for (int i = 0; i < p.b_boxes; ++i) tma_load<CG>(sb + i * p.b_box_bytes, &p.tmap_b, n0 + i * p.b_box_mn, k0, fb);
+          }
+          if constexpr (KIND == KIND_MXF8) {
+            const uint32_t ssfa = sb + C::B_BYTES;
+            const uint32_t ssfb = ssfa + C::SFA_BYTES;
+            // a pair tile's second half may lie wholly beyond M: its A rows are
+            // zero-filled, so any valid scale row will do
+            const int sfa_tile = min(mt * CG + static_cast<int>(rank), p.sf_a_tiles - 1);
+            tma_load<CG>(ssfa, &p.tmap_sfa, 0, kb * p.sf_a_tiles + sfa_tile, fb);
+            tma_load<CG>(ssfb, &p.tmap_sfb, 0, kb * p.num_n_tiles + nt, fb);
+          }
+        }
+        __syncwarp();
+      }
+    }
+    if (!ok && lane == 0) {
+      // Drain: let the copies this CTA issued land before the CTA can exit.
+      if (CG == 1 || rank == 0) {
+        const uint32_t n_out = it < static_cast<uint32_t>(STAGES) ? it : static_cast<uint32_t>(STAGES);
+        WaitCtx dctx{20000000ull, nullptr, abort_flag};
+        for (uint32_t j = it - n_out; j < it; ++j) {
+          const uint64_t t0 = globaltimer();
+          while (!mbar_try_wait(full_bar(j % STAGES), (j / STAGES) & 1u) && globaltimer() - t0 < dctx.timeout_ns) {
+          }
+        }
+      } else {
+        const uint64_t t0 = globaltimer();
+        while (globaltimer() - t0 < 2000000ull) {
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (CG == 1 || rank == 0) {
+      uint32_t it = 0, tcount = 0;
+      bool ok = true;
+      for (int t = cluster_id; t < p.num_tiles && ok; t += num_clusters, ++tcount) {
+        const int b = static_cast<int>(tcount % ACC);
+        const uint32_t aph = (tcount / ACC) & 1u;
+        if (!warp_wait(acce_bar(b), aph ^ 1u, wctx, SITE_MMA_ACC_EMPTY)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * BN);
+        for (int kb = 0; kb < p.num_k_blocks; ++kb, ++it) {
+          const int s = static_cast<int>(it % STAGES);
+          const uint32_t ph = (it / STAGES) & 1u;
+          if (!warp_wait(full_bar(s), ph, wctx, SITE_MMA_FULL)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t sa = sbase + s * C::STAGE_BYTES;
+            const uint32_t sb = sa + C::A_BYTES;
+            const uint64_t adesc = sdesc(sa, p.a_desc_hi);
+            const uint64_t bdesc = sdesc(sb, p.b_desc_hi);
+            if constexpr (KIND == KIND_MXF8) {
+              const uint32_t ssfa = sb + C::B_BYTES;
+              const uint32_t ssfb = ssfa + C::SFA_BYTES;
+              const uint32_t sf_col = tmem_base + C::SF_COL0 + (it % C::SF_SLOTS) * C::SF_SLOT_COLS;
+              bool slot_free = true;
+              if (it >= static_cast<uint32_t>(C::SF_SLOTS)) {
+                // the MMAs of iteration it - SF_SLOTS read this slot; their
+                // stage's empty barrier completes when they have finished
+                const uint32_t j = it - C::SF_SLOTS;
+                slot_free = wait_bounded(empty_bar(j % STAGES), (j / STAGES) & 1u, wctx, SITE_MMA_FULL);
+              }
+              // on abort (slot wait failed) nothing is issued; the next warp_wait
+              // sees the abort flag and stops every lane
+              if (slot_free) {
+              // 32 rows x 16 bytes, rows 16 bytes apart: (ldo 16, sdo 128, no swizzle)
+              const uint64_t cp_hi = sdesc_hi(16, 128, SW_NONE);
+              tc_cp_32x128b_warpx4<CG>(sf_col, sdesc(ssfa, cp_hi));
+#pragma unroll
+              for (int c = 0; c < C::SFB_CHUNKS; ++c)
+                tc_cp_32x128b_warpx4<CG>(sf_col + 4 + 4 * c, sdesc(ssfb + 512 * c, cp_hi));
+#pragma unroll
+              for (int j = 0; j < C::KSTEPS; ++j) {
+                mma_mxf8<CG>(d_tmem, adesc + ((j * p.a_kstep) >> 4), bdesc + ((j * p.b_kstep) >> 4),
+                             p.idesc | idesc_sf_ids(j, j), sf_col, sf_col + 4, (kb | j) != 0);
+              }
+                tc_commit<CG>(empty_bar(s));
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < C::KSTEPS; ++j) {
+                const uint64_t ad = adesc + ((j * p.a_kstep) >> 4);
+                const uint64_t bd = bdesc + ((j * p.b_kstep) >> 4);
+                if constexpr (KIND == KIND_F16)
+                  mma_f16<CG>(d_tmem, ad, bd, p.idesc, (kb | j) != 0);
+                else
+                  mma_tf32<CG>(d_tmem, ad, bd, p.idesc, (kb | j) != 0);
+              }
+              tc_commit<CG>(empty_bar(s));
+            }
+          }
+          __syncwarp();
+        }
+        if (!ok) break;
+        if (lane == 0) tc_commit<CG>(accf_bar(b));
+        __syncwarp();
+      }
+      if (!ok) {
+        // Drain: wait (bounded) for every MMA / cp this thread issued.
+        if (lane == 0) {
+          tc_commit<CG>(drain_bar);
+          const uint64_t t0 = globaltimer();
+          while (!mbar_try_wait(drain_bar, 0) && globaltimer() - t0 < 20000000ull) {
+          }
+        }
+        __syncwarp();
+      }
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    uint32_t tcount = 0;
+    for (int t = cluster_id; t < p.num_tiles; t += num_clusters, ++tcount) {
+      const int b = static_cast<int>(tcount % ACC);
+      const uint32_t aph = (tcount / ACC) & 1u;
+      if (!warp_wait(accf_bar(b), aph, wctx, SITE_EPI_ACC_FULL)) break;
+      tc_fence_after();
+      int mt, nt;
+      tile_coords(t, p, mt, nt);
+      const int row = mt * C::MMA_M + static_cast<int>(rank) * C::BM + 32 * q + lane;
+      const int n0 = nt * BN;
+      const uint32_t tb = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(b * BN);
+      if (p.acc_f16) {
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t h[16];
+          tmem_ld_32x32b_x16_pack16(tb + 32 * c, h);
+          tc_wait_ld();
+          if (row < p.M && n0 + 32 * c < p.N) store_row16(p, row, n0 + 32 * c, h);
+        }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(tb + 32 * c, r);
+          tc_wait_ld();
+          if (row < p.M && n0 + 32 * c < p.N) store_row32(p, row, n0 + 32 * c, r);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if constexpr (CG == 2)
+          mbar_arrive_cluster(mapa_shared(acce_bar(b), 0));
+        else
+          mbar_arrive(acce_bar(b));
+      }
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  tc_fence_before();
+  __syncthreads();
+  if constexpr (CG == 2) cluster_sync();
+  tc_fence_after();
+  if (warp == 2) tmem_dealloc<CG>(tmem_base, C::TMEM_COLS);
+}
+
+}  // namespace tcg

@@ -1,0 +1,430 @@
+// Single-CTA layout probes.  Each exposes one mechanism the tcgen05 / ldmatrix
+// documentation pages describe, so the tests can compare it bit for bit with
+// those pages' layout rules:
+//   * TMEM st/ld round trip ("tcgen05.ld / tcgen05.st" page, Layout B example;
+//     the copy_async -> tcgen05_ldst page's 128x8 demonstration);
+//   * tcgen05.cp from a descriptor-walked shared image ("tcgen05.cp" page,
+//     shape table and "Shared descriptor address walk");
+//   * tcgen05.ld register images of the 16-row shapes ("Native images");
+//   * one MMA tile with generic-store swizzled operands ("tcgen05.mma" page,
+//     "four K16 issues" example);
+//   * ldmatrix .x2 into separated register slots ("ldmatrix / stmatrix" page
+//     example);
+//   * a bounded wait that runs out (failure detection without a GPU fault).
+#include <cuda_runtime.h>
+
+#include "common.h"
+#include "gemm_kernel.cuh"
+#include "tmem_ldst.cuh"
+
+namespace tcg {
+namespace {
+
+__device__ __forceinline__ WaitCtx probe_wait_ctx(unsigned long long* err, uint64_t timeout_ns,
+                                                  volatile uint32_t* abort_flag) {
+  return WaitCtx{timeout_ns, err, abort_flag};
+}
+
+// ------------------------------------------------------------------ TMEM round trip
+
+template <int NC>
+__device__ __forceinline__ void st_x(uint32_t taddr, const uint32_t* r) {
+  if constexpr (NC == 1) stx_32x32b_x1(taddr, r);
+  if constexpr (NC == 2) stx_32x32b_x2(taddr, r);
+  if constexpr (NC == 4) stx_32x32b_x4(taddr, r);
+  if constexpr (NC == 8) stx_32x32b_x8(taddr, r);
+  if constexpr (NC == 16) stx_32x32b_x16(taddr, r);
+  if constexpr (NC == 32) stx_32x32b_x32(taddr, r);
+  if constexpr (NC == 64) stx_32x32b_x64(taddr, r);
+}
+
+template <int NC>
+__device__ __forceinline__ void ld_x(uint32_t taddr, uint32_t* r) {
+  if constexpr (NC == 1) ldx_32x32b_x1(taddr, r);
+  if constexpr (NC == 2) ldx_32x32b_x2(taddr, r);
+  if constexpr (NC == 4) ldx_32x32b_x4(taddr, r);
+  if constexpr (NC == 8) ldx_32x32b_x8(taddr, r);
+  if constexpr (NC == 16) ldx_32x32b_x16(taddr, r);
+  if constexpr (NC == 32) ldx_32x32b_x32(taddr, r);
+  if constexpr (NC == 64) ldx_32x32b_x64(taddr, r);
+}
+
+template <int NC>
+__global__ void __launch_bounds__(128, 1) probe_tmem_roundtrip_kernel(const uint32_t* in, uint32_t* out) {
+  constexpr uint32_t COLS = NC < 32 ? 32 : NC;
+  __shared__ uint32_t slot;
+  const int warp = threadIdx.x >> 5;
+  const int t = threadIdx.x;
+  if (warp == 0) {
+    tmem_alloc<1>(smem_u32(&slot), COLS);
+    tmem_relinquish<1>();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t taddr = slot + (static_cast<uint32_t>(32 * warp) << 16);
+  uint32_t r[NC];
+#pragma unroll
+  for (int j = 0; j < NC; ++j) r[j] = in[t * NC + j];
+  st_x<NC>(taddr, r);
+  tc_wait_st();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  uint32_t o[NC];
+  ld_x<NC>(taddr, o);
+  tc_wait_ld();
+#pragma unroll
+  for (int j = 0; j < NC; ++j) out[t * NC + j] = o[j];
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc<1>(slot, COLS);
+}
+
+// ------------------------------------------------------------------ tcgen05.cp
+
+constexpr int CP_IMAGE_MAX_WORDS = 12288;  // 48 KiB
+
+__global__ void __launch_bounds__(128, 1) probe_cp_kernel(const uint32_t* image, int image_words, int shape,
+                                                          uint32_t origin, uint64_t desc_hi, uint32_t* out,
+                                                          unsigned long long* err, uint64_t timeout_ns) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint32_t slot;
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ uint32_t abort_flag;
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint32_t* img = reinterpret_cast<uint32_t*>(smem_raw + (base - raw));
+  const int warp = threadIdx.x >> 5;
+  for (int i = threadIdx.x; i < image_words; i += blockDim.x) img[i] = image[i];
+  if (warp == 0) {
+    tmem_alloc<1>(smem_u32(&slot), 32);
+    tmem_relinquish<1>();
+  }
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  // Fill the 8 columns with a sentinel so cells the copy does not write show.
+  const uint32_t taddr = slot + (static_cast<uint32_t>(32 * warp) << 16);
+  uint32_t sent[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) sent[j] = 0xDEADBEEFu;
+  stx_32x32b_x8(taddr, sent);
+  tc_wait_st();
+  fence_proxy_async_shared();  // generic-proxy image writes -> async proxy (tcgen05.cp)
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (threadIdx.x == 0) {
+    const uint64_t d = sdesc(base + origin, desc_hi);
+    switch (shape) {
+      case 0: asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(slot), "l"(d) : "memory"); break;
+      case 1: asm volatile("tcgen05.cp.cta_group::1.128x128b [%0], %1;" ::"r"(slot), "l"(d) : "memory"); break;
+      case 2: asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(slot), "l"(d) : "memory"); break;
+      default: asm volatile("tcgen05.cp.cta_group::1.4x256b [%0], %1;" ::"r"(slot), "l"(d) : "memory"); break;
+    }
+    tc_commit<1>(smem_u32(&bar));
+  }
+  const bool ok = warp_wait(smem_u32(&bar), 0, probe_wait_ctx(err, timeout_ns, &abort_flag), SITE_PROBE);
+  tc_fence_after();
+  uint32_t o[8];
+  ldx_32x32b_x8(taddr, o);
+  tc_wait_ld();
+  if (ok) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) out[threadIdx.x * 8 + j] = o[j];
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc<1>(slot, 32);
+}
+
+// ------------------------------------------------------------------ ld shapes
+
+template <int SHAPE, int NUM>
+__device__ __forceinline__ void ld_shape(uint32_t taddr, uint32_t* r) {
+  if constexpr (SHAPE == 0) {
+    if constexpr (NUM == 1) ldx_32x32b_x1(taddr, r);
+    if constexpr (NUM == 2) ldx_32x32b_x2(taddr, r);
+    if constexpr (NUM == 4) ldx_32x32b_x4(taddr, r);
+  } else if constexpr (SHAPE == 1) {
+    if constexpr (NUM == 1) ldx_16x64b_x1(taddr, r);
+    if constexpr (NUM == 2) ldx_16x64b_x2(taddr, r);
+    if constexpr (NUM == 4) ldx_16x64b_x4(taddr, r);
+  } else if constexpr (SHAPE == 2) {
+    if constexpr (NUM == 1) ldx_16x128b_x1(taddr, r);
+    if constexpr (NUM == 2) ldx_16x128b_x2(taddr, r);
+    if constexpr (NUM == 4) ldx_16x128b_x4(taddr, r);
+  } else {
+    if constexpr (NUM == 1) ldx_16x256b_x1(taddr, r);
+    if constexpr (NUM == 2) ldx_16x256b_x2(taddr, r);
+    if constexpr (NUM == 4) ldx_16x256b_x4(taddr, r);
+  }
+}
+
+template <int SHAPE, int NUM>
+__global__ void __launch_bounds__(128, 1) probe_ld_shape_kernel(const uint32_t* in, int half, uint32_t* out) {
+  constexpr int REGS = SHAPE == 0 ? NUM : SHAPE == 1 ? NUM : SHAPE == 2 ? 2 * NUM : 4 * NUM;
+  __shared__ uint32_t slot;
+  const int warp = threadIdx.x >> 5;
+  const int t = threadIdx.x;
+  if (warp == 0) {
+    tmem_alloc<1>(smem_u32(&slot), 32);
+    tmem_relinquish<1>();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t lane_base = slot + (static_cast<uint32_t>(32 * warp) << 16);
+  uint32_t img[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) img[j] = in[t * 32 + j];
+  stx_32x32b_x32(lane_base, img);
+  tc_wait_st();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t taddr = lane_base + (SHAPE == 0 ? 0u : (static_cast<uint32_t>(16 * half) << 16));
+  uint32_t r[REGS];
+  ld_shape<SHAPE, NUM>(taddr, r);
+  tc_wait_ld();
+#pragma unroll
+  for (int j = 0; j < REGS; ++j) out[t * REGS + j] = r[j];
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc<1>(slot, 32);
+}
+
+// ------------------------------------------------------------------ one MMA tile
+
+// A (128 x K) and B (N x K), both K-major 16-bit, written with ordinary
+// stores into 128B-swizzled shared tiles (descriptor (LDO 16, SDO 1024,
+// swizzle 128B): row r at (r/8)*1024 + (r%8)*128, element k at 2k, then the
+// mode-3 XOR), K/16 MMA issues whose start address advances 32 bytes each.
+__global__ void __launch_bounds__(128, 1) probe_mma_tile_kernel(const uint16_t* A, const uint16_t* B, int N, int K,
+                                                                uint32_t idesc, float* D, unsigned long long* err,
+                                                                uint64_t timeout_ns) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint32_t slot;
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ uint32_t abort_flag;
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* g = smem_raw + (base - raw);
+  const uint32_t a_base = base;               // 128 rows x 128 B
+  const uint32_t b_base = base + 128 * 128;   // up to 256 rows x 128 B
+  const int warp = threadIdx.x >> 5;
+  const int t = threadIdx.x;
+  // zero both tiles, then scatter the operands at their swizzled addresses
+  for (int i = t; i < (128 + 256) * 128 / 4; i += blockDim.x) reinterpret_cast<uint32_t*>(g)[i] = 0u;
+  __syncthreads();
+  for (int i = t; i < 128 * K; i += blockDim.x) {
+    const int m = i / K, k = i % K;
+    const uint32_t logical = a_base + (m / 8) * 1024u + (m % 8) * 128u + 2u * k;
+    *reinterpret_cast<uint16_t*>(g + (swizzle_addr(logical, SW_128B) - base)) = A[i];
+  }
+  for (int i = t; i < N * K; i += blockDim.x) {
+    const int n = i / K, k = i % K;
+    const uint32_t logical = b_base + (n / 8) * 1024u + (n % 8) * 128u + 2u * k;
+    *reinterpret_cast<uint16_t*>(g + (swizzle_addr(logical, SW_128B) - base)) = B[i];
+  }
+  uint32_t ncols = 32;
+  while (ncols < static_cast<uint32_t>(N)) ncols <<= 1;
+  if (warp == 0) {
+    tmem_alloc<1>(smem_u32(&slot), ncols);
+    tmem_relinquish<1>();
+  }
+  if (t == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  fence_proxy_async_shared();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (t == 0) {
+    const uint64_t hi = sdesc_hi(16, 1024, SW_128B);
+    for (int kr = 0; kr < K / 16; ++kr) {
+      mma_f16<1>(slot, sdesc(a_base + 32u * kr, hi), sdesc(b_base + 32u * kr, hi), idesc, kr > 0);
+    }
+    tc_commit<1>(smem_u32(&bar));
+  }
+  const bool ok = warp_wait(smem_u32(&bar), 0, probe_wait_ctx(err, timeout_ns, &abort_flag), SITE_PROBE);
+  tc_fence_after();
+  const uint32_t tb = slot + (static_cast<uint32_t>(32 * warp) << 16);
+  for (int c = 0; c < N; c += 32) {
+    uint32_t r[32];
+    tmem_ld_32x32b_x32(tb + c, r);
+    tc_wait_ld();
+    if (ok) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (c + j < N) D[t * N + c + j] = __uint_as_float(r[j]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc<1>(slot, ncols);
+}
+
+// ------------------------------------------------------------------ ldmatrix
+
+// x (16,4,2) row-major words; shared layout (16,4,2):(8,1,128).  Matrix m,
+// row r of issue k is shared row (2r+m, :, k); lane 8m+r provides its address
+// (lanes 16..31 repeat lanes 0..15).  The register words of issue k land in
+// slots 8k (matrix 0) and 8k+2 (matrix 1).
+__global__ void probe_ldmatrix_kernel(const uint32_t* x, uint32_t* out) {
+  __shared__ __align__(16) uint32_t sm[256];
+  const int lane = threadIdx.x & 31;
+  for (int i = lane; i < 256; i += 32) sm[i] = 0u;
+  __syncwarp();
+  for (int q = 0; q < 4; ++q) {
+    const int n = lane + 32 * q;
+    const int i = n / 8, j = (n / 2) % 4, k = n % 2;
+    sm[8 * i + j + 128 * k] = x[n];
+  }
+  __syncwarp();
+  uint32_t raw[12];
+#pragma unroll
+  for (int i = 0; i < 12; ++i) raw[i] = 4294966519u;
+  const int l = lane & 15;
+  const int m = l >> 3, r = l & 7;
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const uint32_t addr = smem_u32(&sm[8 * (2 * r + m) + 128 * k]);
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];"
+                 : "=r"(raw[8 * k]), "=r"(raw[8 * k + 2])
+                 : "r"(addr));
+  }
+#pragma unroll
+  for (int i = 0; i < 12; ++i) out[lane * 12 + i] = raw[i];
+}
+
+// ------------------------------------------------------------------ bounded wait
+
+__global__ void probe_wait_timeout_kernel(unsigned long long* err, uint64_t timeout_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ uint32_t abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);  // nobody ever arrives
+    abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  __syncthreads();
+  warp_wait(smem_u32(&bar), 0, probe_wait_ctx(err, timeout_ns, &abort_flag), SITE_PROBE);
+}
+
+cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+int finish_launch(int launches) {
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return record_cuda(e);
+  set_launch_count(launches);
+  return TCG_OK;
+}
+
+}  // namespace
+}  // namespace tcg
+
+using namespace tcg;
+
+extern "C" int tcg_probe_tmem_roundtrip(const uint32_t* in, uint32_t* out, int ncols, void* stream) {
+  if (!in || !out) return TCG_ERR_INVALID;
+  int dev;
+  if (int rc = current_device_checked(&dev)) return rc;
+  const cudaStream_t s = as_stream(stream);
+  switch (ncols) {
+    case 1: probe_tmem_roundtrip_kernel<1><<<1, 128, 0, s>>>(in, out); break;
+    case 2: probe_tmem_roundtrip_kernel<2><<<1, 128, 0, s>>>(in, out); break;
+    case 4: probe_tmem_roundtrip_kernel<4><<<1, 128, 0, s>>>(in, out); break;
+    case 8: probe_tmem_roundtrip_kernel<8><<<1, 128, 0, s>>>(in, out); break;
+    case 16: probe_tmem_roundtrip_kernel<16><<<1, 128, 0, s>>>(in, out); break;
+    case 32: probe_tmem_roundtrip_kernel<32><<<1, 128, 0, s>>>(in, out); break;
+    case 64: probe_tmem_roundtrip_kernel<64><<<1, 128, 0, s>>>(in, out); break;
+    default: return TCG_ERR_INVALID;
+  }
+  return finish_launch(1);
+}
+
+extern "C" int tcg_probe_cp(const uint32_t* image, int image_words, int shape, uint32_t origin_bytes, uint32_t ldo,
+                            uint32_t sdo, int swizzle, uint32_t* out, void* stream) {
+  if (!image || !out || image_words <= 0 || image_words > CP_IMAGE_MAX_WORDS) return TCG_ERR_INVALID;
+  if (shape < 0 || shape > 3 || swizzle < 0 || swizzle > 3) return TCG_ERR_INVALID;
+  if (!sdesc_fields_ok(origin_bytes, ldo, sdo, swizzle, 0)) return TCG_ERR_INVALID;
+  // the copy's whole walk must stay inside the image
+  const uint32_t rows = shape == 2 ? 32u : shape == 3 ? 4u : 128u;
+  const uint32_t words = shape == 0 || shape == 3 ? 8u : 4u;
+  const uint32_t rb = 16u << swizzle;
+  const uint32_t last_row = ((rows - 1) / 8) * sdo + ((rows - 1) % 8) * rb;
+  const uint32_t last_word = swizzle == 0 ? ((words - 1) / 4) * ldo + ((words - 1) % 4) * 4 : 4 * (words - 1);
+  const uint32_t span = origin_bytes + last_row + last_word + 4;
+  const uint32_t period = swizzle_period(swizzle);
+  if ((span + period - 1) / period * period > static_cast<uint32_t>(image_words) * 4u) return TCG_ERR_INVALID;
+  int dev;
+  if (int rc = current_device_checked(&dev)) return rc;
+  const size_t smem = 1024 + static_cast<size_t>(image_words) * 4;
+  cudaError_t e = cudaFuncSetAttribute(probe_cp_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return record_cuda(e);
+  probe_cp_kernel<<<1, 128, smem, as_stream(stream)>>>(image, image_words, shape, origin_bytes,
+                                                       sdesc_hi(ldo, sdo, swizzle), out, device_error_word(dev),
+                                                       wait_timeout_ns());
+  return finish_launch(1);
+}
+
+extern "C" int tcg_probe_ld_shape(const uint32_t* in, int shape, int num, int half, uint32_t* out, void* stream) {
+  if (!in || !out || shape < 0 || shape > 3 || (half != 0 && half != 1)) return TCG_ERR_INVALID;
+  int dev;
+  if (int rc = current_device_checked(&dev)) return rc;
+  const cudaStream_t s = as_stream(stream);
+#define TCG_LD_CASE(SH, NU) \
+  if (shape == SH && num == NU) { probe_ld_shape_kernel<SH, NU><<<1, 128, 0, s>>>(in, half, out); return finish_launch(1); }
+  TCG_LD_CASE(0, 1) TCG_LD_CASE(0, 2) TCG_LD_CASE(0, 4)
+  TCG_LD_CASE(1, 1) TCG_LD_CASE(1, 2) TCG_LD_CASE(1, 4)
+  TCG_LD_CASE(2, 1) TCG_LD_CASE(2, 2) TCG_LD_CASE(2, 4)
+  TCG_LD_CASE(3, 1) TCG_LD_CASE(3, 2) TCG_LD_CASE(3, 4)
+#undef TCG_LD_CASE
+  return TCG_ERR_INVALID;
+}
+
+extern "C" int tcg_probe_mma_tile(const void* A, const void* B, int N, int K, int is_bf16, float* D, void* stream) {
+  if (!A || !B || !D || N < 16 || N > 256 || N % 16 || K < 16 || K > 64 || K % 16) return TCG_ERR_INVALID;
+  int dev;
+  if (int rc = current_device_checked(&dev)) return rc;
+  const size_t smem = 1024 + (128 + 256) * 128;
+  cudaError_t e = cudaFuncSetAttribute(probe_mma_tile_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return record_cuda(e);
+  const uint32_t idesc = idesc_f16(is_bf16 != 0, true, false, false, 128, N);
+  probe_mma_tile_kernel<<<1, 128, smem, as_stream(stream)>>>(static_cast<const uint16_t*>(A),
+                                                             static_cast<const uint16_t*>(B), N, K, idesc, D,
+                                                             device_error_word(dev), wait_timeout_ns());
+  return finish_launch(1);
+}
+
+extern "C" int tcg_probe_ldmatrix_x2(const uint32_t* x, uint32_t* out, void* stream) {
+  if (!x || !out) return TCG_ERR_INVALID;
+  int dev;
+  if (int rc = current_device_checked(&dev)) return rc;
+  probe_ldmatrix_kernel<<<1, 32, 0, as_stream(stream)>>>(x, out);
+  return finish_launch(1);
+}
+
+extern "C" int tcg_probe_wait_timeout(uint64_t timeout_ns, void* stream) {
+  int dev;
+  if (int rc = current_device_checked(&dev)) return rc;
+  if (timeout_ns < 1000) timeout_ns = 1000;
+  if (timeout_ns > 10000000000ull) timeout_ns = 10000000000ull;
+  probe_wait_timeout_kernel<<<1, 32, 0, as_stream(stream)>>>(device_error_word(dev), timeout_ns);
+  return finish_launch(1);
+}

@@ -1,0 +1,241 @@
+/*
+ * tcg.h -- C ABI of the GB300 (sm_103a) tcgen05 swizzled GEMM library.
+ *
+ * The operation is the dense contraction that the Apache TVM TIRx
+ * "tcgen05.mma" page defines ("Operands and repeat axes": D, A, B with A and B
+ * in shared memory, D an fp32/fp16 accumulator in tensor memory), tiled over
+ * a whole matrix:
+ *
+ *     D[m, n] = sum_k A[m, k] * B[k, n]                 (gemm_f16/bf16/tf32)
+ *     D[m, n] = sum_k (SFA (.) A)[m, k] * (SFB (.) B)[k, n]   (block scaled,
+ *               "Weight-stationary and block scaling": one e8m0 scale per 32
+ *               K elements per row of A and per column of B)
+ *
+ * Operand majorness follows the page's descriptor contract ("Shared
+ * descriptors are byte-stride contracts": K-major rows enumerate M/N,
+ * MN-major rows enumerate K):
+ *     A, TCG_K_MAJOR : M x K row-major, element (m,k) at A[m*lda + k]
+ *     A, TCG_MN_MAJOR: K x M row-major, element (m,k) at A[k*lda + m]
+ *     B, TCG_K_MAJOR : N x K row-major, element (k,n) at B[n*ldb + k]
+ *     B, TCG_MN_MAJOR: K x N row-major, element (k,n) at B[k*ldb + n]
+ *     D              : M x N row-major, element (m,n) at D[m*ldd + n]
+ * A leading dimension of 0 means "packed" (K, M, N or N as appropriate).
+ *
+ * Ownership: every pointer is caller-owned DEVICE memory (except where a
+ * function says host) that must stay valid until the work queued on `stream`
+ * has finished.  All calls are asynchronous on `stream` (a cudaStream_t; 0 is
+ * the legacy default stream) and never synchronise the host, except
+ * tcg_check().  The block-scaled GEMM with plain scale arrays uses a
+ * library-owned device workspace per (device, stream), allocated on first use
+ * and grown when needed; no other call allocates device memory.
+ *
+ * Errors: every function returns TCG_OK (0) or a negative tcg_status.
+ * Argument errors are detected on the host before anything is queued.
+ * Device-side failures (a bounded wait in a kernel that ran out, see
+ * tcg_set_wait_timeout_ns) are recorded in a per-device error word and
+ * reported by the next tcg_check().
+ */
+#ifndef TCG_H_
+#define TCG_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  TCG_OK = 0,
+  TCG_ERR_INVALID = -1,     /* null pointer, negative size, bad enum, ld too small */
+  TCG_ERR_ALIGNMENT = -2,   /* TMA needs 16-byte aligned bases and row strides */
+  TCG_ERR_UNSUPPORTED = -3, /* valid request this library does not implement */
+  TCG_ERR_CUDA = -4,        /* a CUDA runtime/driver call failed (see tcg_last_error_string) */
+  TCG_ERR_TIMEOUT = -5,     /* a kernel's bounded mbarrier wait ran out (from tcg_check) */
+  TCG_ERR_NO_DEVICE = -6    /* no usable sm_103 device */
+} tcg_status;
+
+typedef enum { TCG_K_MAJOR = 0, TCG_MN_MAJOR = 1 } tcg_major;
+
+/* Accumulator / output element types. */
+typedef enum { TCG_F32 = 0, TCG_F16 = 1, TCG_BF16 = 2 } tcg_dtype;
+
+/* Operand storage types (generic entry point). */
+typedef enum {
+  TCG_IN_F16 = 0,   /* IEEE binary16, MMA kind::f16 */
+  TCG_IN_BF16 = 1,  /* bfloat16, kind::f16 */
+  TCG_IN_TF32 = 2,  /* float32 storage read as TF32, kind::tf32 */
+  TCG_IN_E4M3 = 3   /* OCP E4M3FN with e8m0 block scales, kind::mxf8f6f4.block_scale */
+} tcg_input;
+
+/* ---------------------------------------------------------------------------
+ * The four GEMMs.  M, N, K >= 0 (M == 0 or N == 0: no-op; K == 0: D = 0).
+ * acc_type: TCG_F32, or TCG_F16 for gemm_f16 only (fp16 accumulation in TMEM,
+ * output then must be TCG_F16).  d_type: TCG_F32, TCG_F16 or TCG_BF16.
+ * Alignment: A, B base addresses and lda*sizeof, ldb*sizeof must be multiples
+ * of 16 bytes (TMA); D must be at least 2-byte aligned (4 for F32).
+ * ------------------------------------------------------------------------- */
+int tcg_gemm_f16(int64_t M, int64_t N, int64_t K,
+                 const void* A, tcg_major a_major, int64_t lda,
+                 const void* B, tcg_major b_major, int64_t ldb,
+                 void* D, tcg_dtype d_type, int64_t ldd,
+                 tcg_dtype acc_type, void* stream);
+
+int tcg_gemm_bf16(int64_t M, int64_t N, int64_t K,
+                  const void* A, tcg_major a_major, int64_t lda,
+                  const void* B, tcg_major b_major, int64_t ldb,
+                  void* D, tcg_dtype d_type, int64_t ldd,
+                  tcg_dtype acc_type, void* stream);
+
+/* A and B are float32 storage; the tensor cores read them as TF32
+ * ("tcgen05.mma" page, "Operands": the tf32 format is given explicitly for
+ * float32 storage).  MN-major TF32 uses the 128-byte-span / 32-byte-atom
+ * swizzle ("swizzle=4" section). */
+int tcg_gemm_tf32(int64_t M, int64_t N, int64_t K,
+                  const void* A, tcg_major a_major, int64_t lda,
+                  const void* B, tcg_major b_major, int64_t ldb,
+                  void* D, tcg_dtype d_type, int64_t ldd,
+                  tcg_dtype acc_type, void* stream);
+
+/* MXFP8: A, B are E4M3FN bytes; SFA is a plain row-major [M][ceil(K/32)]
+ * e8m0 array, SFB [N][ceil(K/32)] (one scale per 32 K elements per row of A
+ * and per column of B).  Scales are rearranged on the device into the
+ * tcgen05.cp-ready image (tcg_mxf8_prepare_scales) in a library workspace,
+ * then staged into TMEM with tcgen05.cp .32x128b.warpx4 ("tcgen05.cp" page,
+ * shape table; "tcgen05.mma" page, block-scale placement).  acc_type must be
+ * TCG_F32.  Uses the per-(device, stream) workspace described above: calls on
+ * one stream are ordered; calls on different streams use different buffers. */
+int tcg_gemm_mxf8_blockscaled(int64_t M, int64_t N, int64_t K,
+                              const void* A, tcg_major a_major, int64_t lda,
+                              const void* B, tcg_major b_major, int64_t ldb,
+                              const uint8_t* SFA, const uint8_t* SFB,
+                              void* D, tcg_dtype d_type, int64_t ldd,
+                              tcg_dtype acc_type, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Generic entry point: every knob of the four calls above plus the CTA-group
+ * and tile choices (0 = let the library choose).
+ * ------------------------------------------------------------------------- */
+typedef struct {
+  int64_t M, N, K;
+  tcg_input in_type;
+  const void* A; tcg_major a_major; int64_t lda;
+  const void* B; tcg_major b_major; int64_t ldb;
+  /* block scaling (TCG_IN_E4M3 only): either plain scales ... */
+  const uint8_t* SFA; const uint8_t* SFB;
+  /* ... or images already built by tcg_mxf8_prepare_scales (then SFA/SFB must
+   * be NULL).  The images must have been prepared for the same M/N/K and the
+   * tile_n this call resolves to (tcg_mxf8_tile_n). */
+  const uint8_t* SFA_img; const uint8_t* SFB_img;
+  void* D; tcg_dtype d_type; int64_t ldd;
+  tcg_dtype acc_type;
+  int cta_group;     /* 0 auto, 1 (one CTA per 128xN tile), 2 (CTA pair, 256xN) */
+  int raster_group;  /* 0 auto; tiles are visited in groups of this many M tiles */
+} tcg_gemm_args;
+
+int tcg_gemm(const tcg_gemm_args* args, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Block-scale layout (the scale-factor rearrangement step).
+ *
+ * The "tcgen05.mma" page places the scale of row r at TMEM lane r%32,
+ * byte-column 4*(r//32)+sf, replicated in four 32-lane groups, which is what
+ * one tcgen05.cp .32x128b.warpx4 produces from a 512-byte shared image in
+ * which the scale of row r and K block kb sits at byte 16*(r%32) + 4*(r//32)
+ * + kb.  The prepared image is, for every K step of 4 scale blocks (128 K
+ * elements) and every tile of `tile_rows` rows, ceil(tile_rows/128) such
+ * 512-byte chunks: [K step][tile][chunk][512 bytes].  Missing rows and K
+ * blocks hold 127 (2^0).
+ * ------------------------------------------------------------------------- */
+
+/* Bytes of the image for `rows` rows, K elements, tiles of tile_rows rows. */
+int64_t tcg_mxf8_scale_image_bytes(int64_t rows, int64_t K, int tile_rows);
+
+/* tile_rows the GEMM uses for SFA (always 128 per CTA) and SFB (the N tile),
+ * for a given problem and cta_group request (0 = auto). */
+int tcg_mxf8_tile_n(int64_t M, int64_t N, int64_t K, tcg_major b_major, int cta_group);
+
+/* Device-side rearrangement: `sf` plain [rows][ceil(K/32)] (device) -> `img`
+ * (device, tcg_mxf8_scale_image_bytes bytes). */
+int tcg_mxf8_prepare_scales(const uint8_t* sf, int64_t rows, int64_t K, int tile_rows,
+                            uint8_t* img, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Status and configuration.
+ * ------------------------------------------------------------------------- */
+
+/* Synchronises `stream`, then returns and clears the current device's error
+ * word: TCG_OK, TCG_ERR_TIMEOUT (a bounded wait ran out; the kernel returned
+ * early, its output is incomplete) or TCG_ERR_CUDA. */
+int tcg_check(void* stream);
+
+/* Upper bound, in nanoseconds, of every mbarrier wait inside the kernels
+ * launched after this call (default 2e9, i.e. 2 s; values < 1000 are
+ * clamped).  Also settable through the TCG_WAIT_TIMEOUT_NS environment
+ * variable at library load. */
+void tcg_set_wait_timeout_ns(uint64_t ns);
+
+const char* tcg_status_string(int status);
+
+/* Text of the last CUDA error seen by this thread (empty if none). */
+const char* tcg_last_error_string(void);
+
+/* Number of kernels the most recent successful call on this thread queued. */
+int tcg_last_launch_count(void);
+
+/* ---------------------------------------------------------------------------
+ * Layout probes: single-CTA kernels that expose one tcgen05 / ldmatrix
+ * mechanism each, so the tests can compare it bit for bit with the pages'
+ * layout rules.  All buffers are device memory.
+ * ------------------------------------------------------------------------- */
+
+/* "tcgen05.ld / tcgen05.st" page example (Layout B) and the copy_async
+ * round trip: 128 threads; thread t stores in[t*ncols .. +ncols) to TMEM lane
+ * t with tcgen05.st .32x32b.x<ncols>, waits, reads it back with
+ * tcgen05.ld .32x32b.x<ncols> into out.  ncols in {1,2,4,8,16,32,64,128}. */
+int tcg_probe_tmem_roundtrip(const uint32_t* in, uint32_t* out, int ncols, void* stream);
+
+/* "tcgen05.cp" page: fills a 1024-byte-aligned shared buffer with
+ * `image_words` words of `image`, issues one tcgen05.cp of `shape`
+ * (0 = 128x256b, 1 = 128x128b, 2 = 32x128b.warpx4, 3 = 4x256b) with the
+ * descriptor (origin_bytes, ldo, sdo, swizzle 0..3), waits on its commit and
+ * reads 128 lanes x 8 columns back with tcgen05.ld .32x32b.x8 into out
+ * (128 x 8 words, lane-major).  image_words <= 12288. */
+int tcg_probe_cp(const uint32_t* image, int image_words, int shape,
+                 uint32_t origin_bytes, uint32_t ldo, uint32_t sdo, int swizzle,
+                 uint32_t* out, void* stream);
+
+/* "tcgen05.ld / tcgen05.st" page, native images: stores `in` (128 lanes x 32
+ * columns, lane-major) with .32x32b.x32, then every warp loads lanes
+ * [32w + half*16, +16) with tcgen05.ld.<shape>.x<num>; out receives, for
+ * thread t, its registers at out[t*regs + r] (regs = registers per lane).
+ * shape: 0 = 32x32b, 1 = 16x64b, 2 = 16x128b, 3 = 16x256b; num in {1,2,4};
+ * half in {0,1} (16-row shapes only). */
+int tcg_probe_ld_shape(const uint32_t* in, int shape, int num, int half,
+                       uint32_t* out, void* stream);
+
+/* "tcgen05.mma" page example, generalised: one CTA; A (128 x K, K-major) and
+ * B (N x K, K-major) f16/bf16 bytes are written into 128B-swizzled shared
+ * memory with ordinary stores at the addresses the descriptor walk gives,
+ * then K/16 tcgen05.mma kind::f16 (M=128, N, K=16) issues, one commit, and a
+ * tcgen05.ld .32x32b drain into D (128 x N fp32).  K in {16..64} step 16,
+ * N in {16..256} step 16.  is_bf16 selects the A/B format. */
+int tcg_probe_mma_tile(const void* A, const void* B, int N, int K, int is_bf16,
+                       float* D, void* stream);
+
+/* "ldmatrix / stmatrix" page example: x = 128 words viewed as (16,4,2) with
+ * shared layout (16,4,2):(8,1,128); one warp issues two ldmatrix .m8n8.x2
+ * into register slots {0,2} and {8,10} of a 12-word array preset to the
+ * sentinel 4294966519; out is 32 x 12 words. */
+int tcg_probe_ldmatrix_x2(const uint32_t* x, uint32_t* out, void* stream);
+
+/* Failure-detection probe: launches one CTA that waits on an mbarrier no one
+ * arrives at, bounded by `timeout_ns`; the kernel records TCG_ERR_TIMEOUT in
+ * the error word and returns.  Returns the launch status; tcg_check() then
+ * reports the timeout. */
+int tcg_probe_wait_timeout(uint64_t timeout_ns, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TCG_H_ */

@@ -1,0 +1,91 @@
+"""C-ABI checks that need no GPU: the library builds, loads, exports every
+function ``include/tcg.h`` declares, and rejects bad arguments on the host
+before touching the device.  Nothing here launches a kernel."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def tcg():
+    from blackwell_tensor_core_swizzled_gb300 import build
+    build.build()
+    import blackwell_tensor_core_swizzled_gb300 as m
+    return m
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "tcg.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(tcg_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_four_gemms():
+    names = _declared()
+    for n in ("tcg_gemm_f16", "tcg_gemm_bf16", "tcg_gemm_tf32", "tcg_gemm_mxf8_blockscaled"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(tcg):
+    lib = ctypes.CDLL(tcg.LIB_PATH)
+    missing = [n for n in _declared() if not hasattr(lib, n)]
+    assert not missing, missing
+    assert sorted(tcg.EXPORTED) == _declared()
+
+
+def test_status_strings(tcg):
+    for s in range(0, -7, -1):
+        assert tcg.status_string(s) != "unknown status"
+
+
+def _call(tcg, name, M=256, N=256, K=64, A=0x10000, am=0, lda=0, B=0x20000, bm=0, ldb=0, D=0x30000,
+          dt=2, ldd=0, acc=0):
+    return tcg.raw_call(f"tcg_gemm_{name}", M, N, K, A, am, lda, B, bm, ldb, D, dt, ldd, acc, None)
+
+
+def test_host_validation_rejects_bad_arguments(tcg):
+    assert _call(tcg, "bf16", M=-1) == tcg.ERR_INVALID
+    assert _call(tcg, "bf16", A=None) == tcg.ERR_INVALID
+    assert _call(tcg, "bf16", D=None) == tcg.ERR_INVALID
+    assert _call(tcg, "bf16", am=7) == tcg.ERR_INVALID
+    assert _call(tcg, "bf16", lda=32) == tcg.ERR_INVALID            # lda < K
+    assert _call(tcg, "bf16", ldd=100) == tcg.ERR_INVALID           # ldd < N
+    assert _call(tcg, "bf16", A=0x10008) == tcg.ERR_ALIGNMENT       # TMA base alignment
+    assert _call(tcg, "bf16", K=60, lda=60) == tcg.ERR_ALIGNMENT    # 120-byte rows
+    assert _call(tcg, "bf16", acc=1, dt=1) == tcg.ERR_UNSUPPORTED   # bf16 with f16 accumulation
+    assert _call(tcg, "f16", acc=1, dt=2) == tcg.ERR_UNSUPPORTED    # f16 accumulation needs f16 out
+    assert _call(tcg, "tf32", dt=5) == tcg.ERR_INVALID
+    # mxf8 without scales
+    rc = tcg.raw_call("tcg_gemm_mxf8_blockscaled", 64, 64, 64, 0x10000, 0, 0, 0x20000, 0, 0, None, None,
+                      0x30000, 2, 0, 0, None)
+    assert rc == tcg.ERR_INVALID
+
+
+def test_empty_problems_are_noops(tcg):
+    # M == 0 or N == 0 returns before any device work, even with null pointers
+    assert _call(tcg, "bf16", M=0, A=None, B=None, D=None) == tcg.OK
+    assert _call(tcg, "f16", N=0, A=None, B=None, D=None) == tcg.OK
+
+
+def test_scale_image_sizes(tcg):
+    # [K step][tile][chunk][512 B]: K=8192 -> 256 blocks -> 64 steps
+    assert tcg.mxf8_scale_image_bytes(8192, 8192, 128) == 64 * 64 * 512
+    assert tcg.mxf8_scale_image_bytes(8192, 8192, 224) == 64 * 37 * 2 * 512
+    assert tcg.mxf8_scale_image_bytes(300, 96, 128) == 1 * 3 * 512
+    assert tcg.mxf8_tile_n(8192, 8192, 8192, tcg.K_MAJOR, 2) == 224
+    assert tcg.mxf8_tile_n(8192, 8192, 8192, tcg.MN_MAJOR, 0) == 256
+    assert tcg.mxf8_tile_n(8192, 8192, 8192, tcg.MN_MAJOR, 2) == tcg.ERR_UNSUPPORTED
+
+
+@pytest.mark.skipif(os.environ.get("CUDA_VISIBLE_DEVICES_FORCE_GPU") is not None, reason="GPU present")
+def test_fails_loudly_without_a_device(tcg):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert _call(tcg, "bf16") == tcg.ERR_NO_DEVICE
+    with pytest.raises(tcg.TcgError):
+        tcg.gemm_bf16(256, 256, 64, 0x10000, 0, 0, 0x20000, 0, 0, 0x30000, 2, 0, 0, stream=0)

@@ -1,0 +1,191 @@
+"""GEMM parity: the CUDA path through the C ABI against the float64 oracle.
+
+Tolerance (per element): |D_gpu - D_ref| <= tau * sum_k |a||b| with tau = 2e-3
+for fp32 accumulation and 1e-2 for fp16 accumulation.  Small cases compare
+every element (several tiles, ragged tails in M, N and K); the full-size
+workloads compare sampled rows (all N columns of each) in the launch
+configuration the benchmark times.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synthetic as syn
+from gpu_helpers import TAU, assert_parity, make_case, oracle_rows, run_gpu, sample_rows, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tcg():
+    assert torch.cuda.is_available(), "GPU tests need a GPU"
+    from blackwell_tensor_core_swizzled_gb300 import build
+    build.build()
+    import blackwell_tensor_core_swizzled_gb300 as m
+    return m
+
+
+def _check_full(tcg, oracle_mod, x, out, acc, cg, **kw):
+    D = run_gpu(tcg, x, out=out, acc=acc, cta_group=cg, **kw)
+    got = D[:x["M"], :x["N"]].double().cpu().numpy()
+    ref, S = oracle_rows(oracle_mod, x)
+    return assert_parity(got, ref, S, TAU[acc], f"{x['w'].dtype} {x['w'].a_major}{x['w'].b_major} cg{cg}")
+
+
+SMALL = [
+    # dtype, a_major, b_major, M, N, K, cta_group, out, acc
+    ("f16", "k", "k", 128, 128, 64, 1, "f32", "f32"),
+    ("f16", "k", "k", 128, 128, 64, 2, "f32", "f32"),
+    ("bf16", "k", "mn", 300, 520, 200, 1, "bf16", "f32"),
+    ("bf16", "k", "k", 300, 520, 200, 2, "bf16", "f32"),
+    ("bf16", "mn", "k", 513, 300, 136, 2, "f32", "f32"),
+    ("bf16", "mn", "mn", 257, 257, 264, 1, "f16", "f32"),
+    ("bf16", "k", "k", 1000, 1100, 640, 0, "bf16", "f32"),
+    ("f16", "k", "k", 640, 768, 512, 2, "f16", "f16"),
+    ("f16", "mn", "mn", 200, 300, 96, 1, "f16", "f16"),
+    ("f16", "k", "mn", 384, 512, 1024, 1, "f16", "f16"),
+    ("tf32", "k", "k", 300, 520, 200, 1, "f32", "f32"),
+    ("tf32", "mn", "mn", 260, 300, 72, 2, "f32", "f32"),
+    ("tf32", "k", "mn", 128, 256, 128, 1, "f32", "f32"),
+    ("tf32", "mn", "k", 384, 256, 96, 2, "bf16", "f32"),
+    ("e4m3", "k", "k", 300, 520, 256, 2, "bf16", "f32"),
+    ("e4m3", "k", "k", 300, 520, 208, 1, "f32", "f32"),
+    ("e4m3", "k", "k", 512, 448, 512, 2, "bf16", "f32"),
+    ("e4m3", "mn", "mn", 200, 300, 256, 1, "bf16", "f32"),
+    ("e4m3", "mn", "k", 260, 230, 160, 2, "f32", "f32"),
+]
+
+
+@pytest.mark.parametrize("dtype,am,bm,M,N,K,cg,out,acc", SMALL)
+def test_small_ragged_full_compare(tcg, oracle_mod, dtype, am, bm, M, N, K, cg, out, acc):
+    x = make_case(dtype, am, bm, M, N, K, seed=M + N + K)
+    _check_full(tcg, oracle_mod, x, out, acc, cg)
+
+
+def test_identity_gives_b_exactly(tcg, oracle_mod):
+    # A = I: every D row is a B row, exact in bf16 out; pins the output layout.
+    n, N = 256, 384
+    A = syn.to_bits(np.eye(n), "bf16")
+    b = syn.draw((n, N), 3, "uniform", n)
+    B = syn.lay_out_b(syn.to_bits(b, "bf16"), "mn")
+    D = torch.zeros((n, N), dtype=torch.bfloat16, device="cuda")
+    tcg.gemm(n, N, n, 1, to_device(A), 0, n, to_device(B), 1, N, D, 2, N, 0, cta_group=2)
+    assert tcg.check() == 0
+    bdec = torch.from_numpy(B.view(np.int16)).view(torch.bfloat16).double().numpy()
+    assert np.array_equal(D.double().cpu().numpy(), bdec)
+
+
+def test_permutation_rows_land_in_place(tcg):
+    n, N = 512, 256
+    perm = np.random.default_rng(9).permutation(n)
+    P = syn.to_bits(np.eye(n)[perm], "f16")
+    b = syn.draw((n, N), 4, "uniform", n)
+    B = syn.lay_out_b(syn.to_bits(b, "f16"), "k")
+    D = torch.zeros((n, N), dtype=torch.float32, device="cuda")
+    tcg.gemm(n, N, n, 0, to_device(P), 0, n, to_device(B), 0, n, D, 0, N, 0, cta_group=1)
+    assert tcg.check() == 0
+    bdec = torch.from_numpy(B.view(np.int16)).view(torch.float16).double().numpy().T
+    assert np.array_equal(D.double().cpu().numpy(), bdec[perm])
+
+
+def test_blockscaled_identity_pins_scale_placement(tcg):
+    # A = I in e4m3 with per-(row, 32-block) scales: D[m,n] =
+    # 2^(sfa[m, m//32] + sfb[n, m//32] - 254) * B[m,n]; any misplaced scale
+    # byte (lane, column, replica or SF id) changes an output by a power of two.
+    n, N = 256, 448
+    A = syn.to_bits(np.eye(n), "e4m3")
+    b = syn.draw((n, N), 21, "normal1", n)
+    B = syn.lay_out_b(syn.to_bits(b, "e4m3"), "k")
+    rng = np.random.default_rng(22)
+    SFA = (127 + rng.integers(-5, 6, size=(n, n // 32))).astype(np.uint8)
+    SFB = (127 + rng.integers(-5, 6, size=(N, n // 32))).astype(np.uint8)
+    bdec = torch.from_numpy(B).view(torch.float8_e4m3fn).double().numpy().T
+    m = np.arange(n)
+    expo = SFA[m, m // 32].astype(np.int64)[:, None] + SFB[:, m // 32].T.astype(np.int64) - 254
+    ref = np.ldexp(bdec, expo)
+    for cg in (1, 2):
+        D = torch.zeros((n, N), dtype=torch.float32, device="cuda")
+        tcg.gemm(n, N, n, 3, to_device(A), 0, n, to_device(B), 0, n, D, 0, N, 0, SFA=to_device(SFA),
+                 SFB=to_device(SFB), cta_group=cg)
+        assert tcg.check() == 0
+        assert np.array_equal(D.double().cpu().numpy(), ref), f"cta_group {cg}"
+
+
+def test_scale_prepare_kernel_matches_oracle_image(tcg):
+    from oracle import layouts as L
+    for rows, K, tile in [(300, 200, 128), (8192, 8192, 224), (500, 1024, 256)]:
+        kb = -(-K // 32)
+        sf = np.random.default_rng(rows).integers(0, 255, size=(rows, kb)).astype(np.uint8)
+        nbytes = tcg.mxf8_scale_image_bytes(rows, K, tile)
+        img = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+        tcg.mxf8_prepare_scales(to_device(sf), rows, K, tile, img)
+        assert tcg.check() == 0
+        exp = L.sf_prepare(sf, rows, kb, tile).reshape(-1)
+        assert np.array_equal(img.cpu().numpy(), exp), (rows, K, tile)
+
+
+def test_prepared_scale_images_path(tcg, oracle_mod):
+    x = make_case("e4m3", "k", "k", 384, 600, 320, seed=5)
+    M, N, K = 384, 600, 320
+    tn = tcg.mxf8_tile_n(M, N, K, 0, 2)
+    ia = torch.zeros(tcg.mxf8_scale_image_bytes(M, K, 128), dtype=torch.uint8, device="cuda")
+    ib = torch.zeros(tcg.mxf8_scale_image_bytes(N, K, tn), dtype=torch.uint8, device="cuda")
+    tcg.mxf8_prepare_scales(to_device(x["SFA"]), M, K, 128, ia)
+    tcg.mxf8_prepare_scales(to_device(x["SFB"]), N, K, tn, ib)
+    D = run_gpu(tcg, x, out="f32", cta_group=2, sf_img=(ia, ib))
+    ref, S = oracle_rows(oracle_mod, x)
+    assert_parity(D[:M, :N].double().cpu().numpy(), ref, S, TAU["f32"], "prepared images")
+
+
+def test_padded_leading_dims_and_unaligned_output(tcg, oracle_mod):
+    x = make_case("bf16", "k", "k", 200, 300, 128, seed=3, extra_pad=2)
+    _check_full(tcg, oracle_mod, x, "bf16", "f32", 1, ldd=307)   # odd ldd: scalar stores
+    x = make_case("f16", "mn", "k", 200, 300, 128, seed=4, extra_pad=1)
+    _check_full(tcg, oracle_mod, x, "f32", "f32", 2, ldd=320)
+
+
+def test_k_zero_zeroes_d_and_empty_is_noop(tcg):
+    D = torch.full((64, 80), 7.0, dtype=torch.float32, device="cuda")
+    tcg.gemm_bf16(64, 80, 0, 0, 0, 0, 0, 0, 0, D, 0, 80, 0)
+    assert tcg.check() == 0
+    assert torch.count_nonzero(D).item() == 0
+    D.fill_(7.0)
+    tcg.gemm_bf16(0, 80, 64, 0, 0, 0, 0, 0, 0, D, 0, 80, 0)
+    tcg.gemm_bf16(64, 0, 64, 0, 0, 0, 0, 0, 0, D, 0, 80, 0)
+    assert tcg.check() == 0
+    assert torch.all(D == 7.0)
+
+
+def test_named_entry_points(tcg, oracle_mod):
+    x = make_case("bf16", "k", "mn", 256, 384, 192, seed=8)
+    D = torch.zeros((256, 384), dtype=torch.bfloat16, device="cuda")
+    tcg.gemm_bf16(256, 384, 192, to_device(x["A"]), 0, x["lda"], to_device(x["B"]), 1, x["ldb"], D, 2, 384, 0)
+    assert tcg.check() == 0
+    ref, S = oracle_rows(oracle_mod, x)
+    assert_parity(D.double().cpu().numpy(), ref, S, TAU["f32"], "gemm_bf16")
+    x = make_case("e4m3", "k", "k", 256, 384, 256, seed=9)
+    D = torch.zeros((256, 384), dtype=torch.bfloat16, device="cuda")
+    tcg.gemm_mxf8_blockscaled(256, 384, 256, to_device(x["A"]), 0, x["lda"], to_device(x["B"]), 0, x["ldb"],
+                              to_device(x["SFA"]), to_device(x["SFB"]), D, 2, 384, 0)
+    assert tcg.check() == 0
+    ref, S = oracle_rows(oracle_mod, x)
+    assert_parity(D.double().cpu().numpy(), ref, S, TAU["f32"], "gemm_mxf8_blockscaled")
+
+
+# ------------------------------------------------------------- full-size workloads
+
+FULL = ["tile_f16_128x128x64", "bf16_4096_kmn_cta1", "tf32_2048x2048x8192", "bf16_8192_cta2",
+        "f16acc_8192_cta2", "mxf8_8192"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_workloads_sampled_rows(tcg, oracle_mod, name):
+    w = syn.WORKLOADS[name]
+    x = syn.make_inputs(w)
+    x["w"] = w
+    D = run_gpu(tcg, x, out=w.out, acc=w.acc, cta_group=w.cta_group)
+    rows = sample_rows(w.M) if w.M > 256 else list(range(w.M))
+    got = D[rows, :w.N].double().cpu().numpy()
+    ref, S = oracle_rows(oracle_mod, x, rows=rows)
+    ratio = assert_parity(got, ref, S, TAU[w.acc], name)
+    print(f"{name}: max err/S {ratio:.3e} over {len(rows)} rows")

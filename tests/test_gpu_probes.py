@@ -1,0 +1,210 @@
+"""GPU layout probes, bit-exact against the pages' layout rules as restated
+in ``oracle.layouts`` (and the pages' worked examples in
+``tests/golden/page_examples.json``)."""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import layouts as L
+
+pytestmark = pytest.mark.gpu
+GOLDEN = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "page_examples.json")))
+
+
+@pytest.fixture(scope="module")
+def tcg():
+    assert torch.cuda.is_available(), "GPU tests need a GPU"
+    from blackwell_tensor_core_swizzled_gb300 import build
+    build.build()
+    import blackwell_tensor_core_swizzled_gb300 as m
+    return m
+
+
+def _u32(a):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.uint32).view(np.int32)).cuda()
+
+
+def _np(t):
+    return t.cpu().numpy().view(np.uint32)
+
+
+# ------------------------------------------------------------- TMEM round trips
+
+def test_tmem_roundtrip_layout_b_page_example(tcg):
+    ex = GOLDEN["tmem_st_ld_layout_b"]
+    x = np.arange(8192, dtype=np.float32).reshape(ex["shape"])
+    inp = _u32(x.view(np.uint32))
+    out = torch.zeros_like(inp)
+    tcg.probe_tmem_roundtrip(inp, out, 64)
+    assert tcg.check() == 0
+    assert np.array_equal(_np(out).view(np.float32).reshape(128, 64), x)
+
+
+@pytest.mark.parametrize("ncols", [1, 2, 4, 8, 16, 32, 64])
+def test_tmem_roundtrip_random_bits(tcg, ncols):
+    rng = np.random.default_rng(ncols)
+    bits = rng.integers(0, 2**32, size=(128, ncols), dtype=np.uint64).astype(np.uint32)
+    inp = _u32(bits)
+    out = torch.zeros_like(inp)
+    tcg.probe_tmem_roundtrip(inp, out, ncols)
+    assert tcg.check() == 0
+    assert np.array_equal(_np(out).reshape(128, ncols), bits)
+
+
+def test_tmem_roundtrip_128x8_f16(tcg):
+    # copy_async -> tcgen05_ldst page demonstration: a 128x8 fp16 tile through
+    # 32x32b.x4 (two fp16 per 32-bit cell)
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((128, 8)).astype(np.float16)
+    inp = _u32(x.view(np.uint32).reshape(128, 4))
+    out = torch.zeros_like(inp)
+    tcg.probe_tmem_roundtrip(inp, out, 4)
+    assert tcg.check() == 0
+    assert np.array_equal(_np(out).reshape(128, 4).view(np.float16), x)
+
+
+# ------------------------------------------------------------- tcgen05.cp
+
+CP_ROWS = {0: 128, 1: 128, 2: 32, 3: 4}
+CP_WORDS = {0: 8, 1: 4, 2: 4, 3: 8}
+
+
+def _cp_expected(image, shape, origin, ldo, sdo, sw):
+    exp = np.full((128, 8), 0xDEADBEEF, dtype=np.uint32)
+    r, w = np.meshgrid(np.arange(CP_ROWS[shape]), np.arange(CP_WORDS[shape]), indexing="ij")
+    phys = L.cp_physical(origin, r, w, ldo, sdo, sw)
+    vals = image[phys // 4]
+    if shape in (0, 1):
+        exp[:, :CP_WORDS[shape]] = vals
+    elif shape == 2:  # 32x128b.warpx4: four replicas 32 lanes apart
+        for q in range(4):
+            exp[32 * q:32 * q + 32, :4] = vals
+    else:  # 4x256b: lanes 0, 32, 64, 96
+        for i in range(4):
+            exp[32 * i, :] = vals[i]
+    return exp
+
+
+CP_CASES = [
+    # shape, origin, ldo, sdo, swizzle, image_words
+    (1, 0, 16, 128, 0, 512),       # the page's example (128x128b, (16, 128, 0))
+    (0, 0, 256, 128, 0, 2048),     # unswizzled 8-word rows: words 4..7 at LDO
+    (0, 0, 2048, 256, 0, 2048),
+    (0, 0, 16, 256, 1, 2048),      # 32-byte rows, 256-byte period
+    (0, 0, 16, 512, 2, 4096),      # 64-byte rows, 512-byte period
+    (0, 0, 16, 1024, 3, 4096),     # 128-byte rows, 1024-byte period
+    (0, 64, 16, 1024, 3, 4352),    # origin inside the first row: swizzle phase
+    (1, 16, 16, 1024, 3, 4352),
+    (0, 32, 16, 2048, 3, 8448),    # gaps between row groups
+    (1, 48, 16, 512, 2, 4352),
+    (2, 0, 16, 128, 0, 128),       # 32x128b.warpx4: the scale-factor staging shape
+    (2, 0, 16, 1024, 3, 1024),
+    (3, 0, 16, 128, 0, 64),        # 4x256b
+]
+
+
+@pytest.mark.parametrize("shape,origin,ldo,sdo,sw,words", CP_CASES)
+def test_cp_walk_and_swizzle(tcg, shape, origin, ldo, sdo, sw, words):
+    if shape == 1 and origin == 0 and sw == 0:
+        image = np.arange(words, dtype=np.uint32)          # arange(512), as on the page
+    else:
+        image = (np.arange(words, dtype=np.uint32) * 2654435761) & 0xFFFFFFFF
+        image = image.astype(np.uint32)
+    img = _u32(image)
+    out = torch.zeros((128, 8), dtype=torch.int32, device="cuda")
+    tcg.probe_cp(img, words, shape, origin, ldo, sdo, sw, out)
+    assert tcg.check() == 0
+    got = _np(out)
+    exp = _cp_expected(image, shape, origin, ldo, sdo, sw)
+    if not np.array_equal(got, exp):
+        bad = np.argwhere(got != exp)[:6]
+        raise AssertionError(f"mismatch at {bad.tolist()}: got {[hex(got[tuple(b)]) for b in bad]} "
+                             f"exp {[hex(exp[tuple(b)]) for b in bad]}")
+    if shape == 1 and origin == 0 and sw == 0:
+        assert np.array_equal(got[:, :4], np.arange(512).reshape(128, 4))  # page: out == x
+
+
+# ------------------------------------------------------------- ld images
+
+SHAPE_ID = {"32x32b": 0, "16x64b": 1, "16x128b": 2, "16x256b": 3}
+
+
+@pytest.mark.parametrize("shape", list(SHAPE_ID))
+@pytest.mark.parametrize("num", [1, 2, 4])
+@pytest.mark.parametrize("half", [0, 1])
+def test_ld_register_images(tcg, shape, num, half):
+    if shape == "32x32b" and half == 1:
+        pytest.skip("32-row shape has no half")
+    image = (np.arange(128)[:, None] * 32 + np.arange(32)[None, :]).astype(np.uint32)
+    out = torch.zeros((128, 4 * num), dtype=torch.int32, device="cuda")
+    tcg.probe_ld_shape(_u32(image), SHAPE_ID[shape], num, half, out)
+    assert tcg.check() == 0
+    regs = L.ld_regs_per_lane(shape, num)
+    got = _np(out).reshape(-1)[:128 * regs].reshape(128, regs)
+    for warp in range(4):
+        lane0 = 32 * warp + (16 * half if shape != "32x32b" else 0)
+        exp = L.ld_image(shape, num, lambda row, col: image[lane0 + row, col])
+        assert np.array_equal(got[32 * warp:32 * warp + 32], exp), (shape, num, half, warp)
+
+
+# ------------------------------------------------------------- one MMA tile
+
+def test_mma_tile_page_example_exact(tcg, oracle_mod):
+    ex = GOLDEN["mma_four_k16"]
+    rng = np.random.default_rng(ex["seed"])
+    a = (rng.integers(-4, 5, (128, 64)) / 4).astype("float16")
+    b = (rng.integers(-4, 5, (64, 64)) / 4).astype("float16")
+    D = torch.zeros((128, 64), dtype=torch.float32, device="cuda")
+    tcg.probe_mma_tile(torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda(), 64, 64, 0, D)
+    assert tcg.check() == 0
+    got = D.cpu().numpy()
+    np.testing.assert_allclose(got, a.astype("float32") @ b.astype("float32").T, rtol=ex["rtol"], atol=ex["atol"])
+    ref, _ = oracle_mod.gemm(128, 64, 64, a.view(np.uint16), 1, 0, 64, b.view(np.uint16), 1, 0, 64)
+    assert np.array_equal(got.astype(np.float64), ref)   # exact: quarter-integer sums
+
+
+@pytest.mark.parametrize("N,K,bf16", [(128, 64, 0), (256, 64, 1), (16, 16, 0), (48, 32, 1)])
+def test_mma_tile_random(tcg, oracle_mod, N, K, bf16):
+    import synthetic as syn
+    dt = "bf16" if bf16 else "f16"
+    a = syn.to_bits(syn.draw((128, K), 100 + N, "uniform", K), dt)
+    b = syn.to_bits(syn.draw((N, K), 200 + N, "uniform", K), dt)
+    D = torch.zeros((128, N), dtype=torch.float32, device="cuda")
+    tcg.probe_mma_tile(torch.from_numpy(a.view(np.int16)).cuda(), torch.from_numpy(b.view(np.int16)).cuda(),
+                       N, K, bf16, D)
+    assert tcg.check() == 0
+    ref, S = oracle_mod.gemm(128, N, K, a, 2 if bf16 else 1, 0, K, b, 2 if bf16 else 1, 0, K)
+    err = np.abs(D.cpu().numpy().astype(np.float64) - ref)
+    assert np.all(err <= 2e-3 * S)
+
+
+# ------------------------------------------------------------- ldmatrix
+
+def test_ldmatrix_x2_page_example(tcg):
+    ex = GOLDEN["ldmatrix_x2_interleaved"]
+    x = np.arange(128, dtype=np.uint32).reshape(16, 4, 2)
+    out = torch.zeros((32, 12), dtype=torch.int32, device="cuda")
+    tcg.probe_ldmatrix_x2(_u32(x.reshape(-1)), out)
+    assert tcg.check() == 0
+    expected = np.full((32, 12), ex["sentinel"], dtype=np.uint64)
+    for lane in range(32):
+        for k in range(2):
+            for matrix in range(2):
+                expected[lane, 8 * k + 2 * matrix] = x[2 * (lane // 4) + matrix, lane % 4, k]
+    assert np.array_equal(_np(out).astype(np.uint64), expected)
+
+
+# ------------------------------------------------------------- failure detection
+
+def test_bounded_wait_reports_timeout_and_context_survives(tcg):
+    assert tcg.check() == 0
+    tcg.probe_wait_timeout(2_000_000)      # 2 ms on a barrier nobody arrives at
+    assert tcg.check() == tcg.ERR_TIMEOUT
+    assert tcg.check() == 0                # the error word was cleared
+    vals = torch.arange(128 * 8, dtype=torch.int32, device="cuda")
+    out = torch.zeros_like(vals)
+    tcg.probe_tmem_roundtrip(vals, out, 8)  # the context is still usable
+    assert tcg.check() == 0 and torch.equal(out, vals)
