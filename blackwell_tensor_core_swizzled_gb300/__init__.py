@@ -4,7 +4,7 @@ Argument marshalling only: every function forwards to the C ABI of
 ``libtcg.so`` with the same name (``tcg_`` prefix dropped).  Tensors are
 passed by ``data_ptr()``; streams default to torch's current CUDA stream.
 No computation happens in Python and there is no fallback: if the library is
-not built, importing this package raises.  Build it with
+not built, every call raises ImportError.  Build it with
 ``python -c "import __graft_entry__ as g; g.build()"`` (or ``build.py``).
 """
 from __future__ import annotations
@@ -20,12 +20,6 @@ OK, ERR_INVALID, ERR_ALIGNMENT, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_NO_D
 K_MAJOR, MN_MAJOR = 0, 1
 F32, F16, BF16 = 0, 1, 2
 IN_F16, IN_BF16, IN_TF32, IN_E4M3 = 0, 1, 2, 3
-
-if not os.path.exists(LIB_PATH):
-    raise ImportError(f"{LIB_PATH} is not built; run blackwell_tensor_core_swizzled_gb300/build.py "
-                      "(nvcc for sm_103a) first")
-
-_lib = ctypes.CDLL(LIB_PATH)
 
 _i64, _i32, _u32, _u64, _vp = ctypes.c_int64, ctypes.c_int, ctypes.c_uint32, ctypes.c_uint64, ctypes.c_void_p
 
@@ -63,10 +57,32 @@ _SIGS = {
     "tcg_probe_ldmatrix_x2": ([_vp, _vp, _vp], _i32),
     "tcg_probe_wait_timeout": ([_u64, _vp], _i32),
 }
-for _name, (_args, _res) in _SIGS.items():
-    _f = getattr(_lib, _name)
-    _f.argtypes = _args
-    _f.restype = _res
+
+_lib_handle = None
+
+
+def _load():
+    """The loaded library; raises (never falls back) if it is not built."""
+    global _lib_handle
+    if _lib_handle is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is not built; run blackwell_tensor_core_swizzled_gb300/build.py "
+                              "(nvcc for sm_103a) first")
+        lib = ctypes.CDLL(LIB_PATH)
+        for name, (args, res) in _SIGS.items():
+            f = getattr(lib, name)
+            f.argtypes = args
+            f.restype = res
+        _lib_handle = lib
+    return _lib_handle
+
+
+class _Lazy:
+    def __getattr__(self, name):
+        return getattr(_load(), name)
+
+
+_lib = _Lazy()
 
 EXPORTED = tuple(_SIGS)
 
