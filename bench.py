@@ -1,0 +1,452 @@
+"""Benchmark: GEMM TFLOP/s of the tcgen05 swizzled GEMM on one GB300.
+
+One step = one full GEMM of the workload (all hot-path stages: scale
+rearrangement for block-scaled inputs, TMA ring, descriptor walk, tcgen05.mma,
+tcgen05.ld epilogue), inputs already resident in HBM.  Default workload: bf16
+M=N=K=8192 with CTA pairs (cta_group::2, 256x256 pair tiles), fp32
+accumulation, bf16 output; the block-scaled MXFP8 8192^3 GEMM is measured the
+same way and reported under "secondary".
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+Timing: CUDA events on the stream the kernels are launched on, W untimed
+warm-up steps, then exactly K timed steps between a barrier +
+synchronize on both sides; max over ranks.  A and B together exceed the
+129 MB L2, so no flush is needed between steps.  Multi-GPU runs are
+independent replicas (the GEMM needs no exchange): value = all ranks' FLOPs /
+max time.  The reference arm times the float64 CPU oracle on a bounded row
+sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synthetic as syn  # noqa: E402
+
+METRIC = "GEMM TFLOP/s at 1 GB300 and % of dtype dense tensor peak (bf16/mxf8 8192^3)"
+UNIT = "TFLOP/s"
+IN_TYPE = {"f16": 0, "bf16": 1, "tf32": 2, "e4m3": 3}
+OUT = {"f32": 0, "f16": 1, "bf16": 2}
+ACC = {"f32": 0, "f16": 1}
+ESIZE = {"f16": 2, "bf16": 2, "tf32": 4, "e4m3": 1}
+# nominal dense tensor rate relative to bf16 (NVIDIA GB300 figures: tf32 1.1,
+# bf16/fp16 2.25, fp8 4.5 PFLOP/s)
+NOMINAL_RATIO = {"bf16": 1.0, "f16": 1.0, "tf32": 1.1 / 2.25, "e4m3": 2.0}
+PROFILE_DIR = os.path.join(ROOT, "profiles")
+KERNEL_SOURCES = ["gemm_kernel.cuh", "ptx.cuh", "desc.cuh", "gemm_f16.cu", "gemm_tf32.cu", "gemm_mxf8.cu", "api.cu"]
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "blackwell_tensor_core_swizzled_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            d = json.load(fh)
+        return {"bf16_tflops": d.get("bf16_tflops"), "bf16_tflops_sustained": d.get("bf16_tflops_sustained"),
+                "hbm_gbs": d.get("hbm_gbs"), "source": "measured"}
+    return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch of the GEMM kernel from the committed ncu summary,
+    or None if there is none or the kernel sources changed since."""
+    p = os.path.join(PROFILE_DIR, f"gemm_{workload}.md")
+    if not os.path.exists(p):
+        return None
+    txt = open(p).read()
+    m_hash = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", txt)
+    m_t = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    if not m_hash or not m_t or m_hash.group(1) != kernel_source_hash():
+        return None
+    return float(m_t.group(1))
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms in a thread."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.samples = []  # (host time, sm, max, power, hw, hwt, swt, swpc)
+        self.proc = None
+        self.dev = device_index
+
+    def start(self):
+        try:
+            import torch
+            props = torch.cuda.get_device_properties(self.dev)
+            sel = []
+            bus = getattr(props, "pci_bus_id", None)
+            if bus is not None:
+                sel = ["-i", f"{getattr(props, 'pci_domain_id', 0):08X}:{bus:02X}:"
+                             f"{getattr(props, 'pci_device_id', 0):02X}.0"]
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "100"] + sel, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True, bufsize=1)
+        except Exception:
+            self.proc = None
+            return
+        threading.Thread(target=self._read, daemon=True).start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 7:
+                self.samples.append((time.time(), *parts[:7]))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float) -> dict:
+        inside = [s for s in self.samples if t0 <= s[0] <= t1]
+        window = "timed region"
+        if not inside:  # region shorter than the sampling period: nearest samples under load
+            inside = sorted(self.samples, key=lambda s: min(abs(s[0] - t0), abs(s[0] - t1)))[:3]
+            window = "nearest samples to the timed region (shorter than 100 ms)"
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+
+        sm = [num(s[1]) for s in inside if num(s[1]) is not None]
+        mx = [num(s[2]) for s in inside if num(s[2]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for s in inside:
+            for n, v in zip(names, s[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(inside), "window": window}
+
+
+# ----------------------------------------------------------------- GPU arm
+
+def to_dev(bits, torch):
+    view = {np.dtype(np.uint8): np.uint8, np.dtype(np.uint16): np.int16, np.dtype(np.uint32): np.int32}[bits.dtype]
+    return torch.from_numpy(np.ascontiguousarray(bits).view(view)).cuda()
+
+
+def run_workload(tcg, torch, w, steps, warmup, dist_ctx, measure_e2e=True):
+    x = syn.make_inputs(w)
+    M, N, K = w.M, w.N, w.K
+    A = to_dev(x["A"], torch)
+    B = to_dev(x["B"], torch)
+    out_t = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[w.out]
+    D = torch.empty((M, N), dtype=out_t, device="cuda")
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+    scaled = w.block_scaled
+    a_maj = 0 if w.a_major == "k" else 1
+    b_maj = 0 if w.b_major == "k" else 1
+    if scaled:
+        SFA = to_dev(x["SFA"], torch)
+        SFB = to_dev(x["SFB"], torch)
+        tn = tcg.mxf8_tile_n(M, N, K, b_maj, w.cta_group)
+        ia = torch.empty(tcg.mxf8_scale_image_bytes(M, K, 128), dtype=torch.uint8, device="cuda")
+        ib = torch.empty(tcg.mxf8_scale_image_bytes(N, K, tn), dtype=torch.uint8, device="cuda")
+
+    launches = [0]
+
+    def step(ev_pair=None):
+        n = 0
+        if scaled:
+            tcg.mxf8_prepare_scales(SFA, M, K, 128, ia, stream=sp)
+            tcg.mxf8_prepare_scales(SFB, N, K, tn, ib, stream=sp)
+            n += 2
+            if ev_pair:
+                ev_pair[0].record(stream)
+            tcg.gemm(M, N, K, 3, A, a_maj, x["lda"], B, b_maj, x["ldb"], D, OUT[w.out], N, ACC[w.acc],
+                     SFA_img=ia, SFB_img=ib, cta_group=w.cta_group, stream=sp)
+        else:
+            if ev_pair:
+                ev_pair[0].record(stream)
+            tcg.gemm(M, N, K, IN_TYPE[w.dtype], A, a_maj, x["lda"], B, b_maj, x["ldb"], D, OUT[w.out], N,
+                     ACC[w.acc], cta_group=w.cta_group, stream=sp)
+        n += tcg.last_launch_count()
+        if ev_pair:
+            ev_pair[1].record(stream)
+        launches[0] += n
+
+    for _ in range(warmup):
+        step()
+    rc = tcg.check(sp)
+    if rc != 0:
+        raise RuntimeError(f"warm-up failed: {tcg.status_string(rc)} {tcg.last_error_string()}")
+
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    dist_ctx.barrier()
+    torch.cuda.synchronize()
+    launches[0] = 0
+    t_host0 = time.time()
+    start.record(stream)
+    for i in range(steps):
+        step(kev[i])
+    end.record(stream)
+    torch.cuda.synchronize()
+    t_host1 = time.time()
+    dist_ctx.barrier()
+    rc = tcg.check(sp)
+    if rc != 0:
+        raise RuntimeError(f"timed run failed: {tcg.status_string(rc)} {tcg.last_error_string()}")
+    total_ms = start.elapsed_time(end)
+    kernel_ms = float(np.mean([a.elapsed_time(b) for a, b in kev]))
+    res = {"total_ms": total_ms, "kernel_ms": kernel_ms, "launches": launches[0], "t0": t_host0, "t1": t_host1}
+
+    if measure_e2e:
+        # End to end through the C ABI: pinned host inputs copied in, GEMM,
+        # result copied out, every step.
+        hA = torch.from_numpy(x["A"].view({np.dtype(np.uint8): np.uint8, np.dtype(np.uint16): np.int16,
+                                           np.dtype(np.uint32): np.int32}[x["A"].dtype])).pin_memory()
+        hB = torch.from_numpy(x["B"].view({np.dtype(np.uint8): np.uint8, np.dtype(np.uint16): np.int16,
+                                           np.dtype(np.uint32): np.int32}[x["B"].dtype])).pin_memory()
+        hD = torch.empty((M, N), dtype=out_t).pin_memory()
+        e_steps = max(1, min(steps, 10))
+        h2d = hA.numel() * hA.element_size() + hB.numel() * hB.element_size()
+        if scaled:
+            hSFA = torch.from_numpy(x["SFA"]).pin_memory()
+            hSFB = torch.from_numpy(x["SFB"]).pin_memory()
+            h2d += hSFA.numel() + hSFB.numel()
+        d2h = hD.numel() * hD.element_size()
+
+        def e2e_step():
+            A.copy_(hA, non_blocking=True)
+            B.copy_(hB, non_blocking=True)
+            if scaled:
+                SFA.copy_(hSFA, non_blocking=True)
+                SFB.copy_(hSFB, non_blocking=True)
+                tcg.gemm_mxf8_blockscaled(M, N, K, A, a_maj, x["lda"], B, b_maj, x["ldb"], SFA, SFB, D,
+                                          OUT[w.out], N, ACC[w.acc], stream=sp)
+            else:
+                fn = {"f16": tcg.gemm_f16, "bf16": tcg.gemm_bf16, "tf32": tcg.gemm_tf32}[w.dtype]
+                fn(M, N, K, A, a_maj, x["lda"], B, b_maj, x["ldb"], D, OUT[w.out], N, ACC[w.acc], stream=sp)
+            hD.copy_(D, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        dist_ctx.barrier()
+        torch.cuda.synchronize()
+        es.record(stream)
+        for _ in range(e_steps):
+            e2e_step()
+        ee.record(stream)
+        torch.cuda.synchronize()
+        rc = tcg.check(sp)
+        if rc != 0:
+            raise RuntimeError(f"e2e run failed: {tcg.status_string(rc)}")
+        res.update({"e2e_ms": es.elapsed_time(ee) / e_steps, "h2d": h2d, "d2h": d2h})
+    return res
+
+
+def roofline(w, kernel_ms, peaks, traffic):
+    flops = 2.0 * w.M * w.N * w.K
+    achieved = flops / (kernel_ms * 1e-3) / 1e12
+    ratio = NOMINAL_RATIO[w.dtype]
+    peak = peaks["bf16_tflops"] * ratio
+    src = f"{peaks['source']} bf16 burst" + ("" if ratio == 1.0 else f" x nominal {w.dtype}/bf16 ratio {ratio:g}")
+    return {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak, 1), "unit": "TFLOP/s",
+            "frac": round(achieved / peak, 4), "traffic": traffic, "peak_source": src,
+            "kernel": "tcg::gemm_kernel", "algorithmic_flops_per_launch": flops}
+
+
+# ----------------------------------------------------------------- CPU (oracle) arm
+
+def oracle_inputs(w):
+    import oracle
+    oracle.build()
+    return syn.make_inputs(w)
+
+
+def oracle_sample(w, x, rows_n: int):
+    """Time the float64 oracle on `rows_n` output rows (all N columns) of the
+    workload (inputs `x` already generated); returns (TFLOP/s, seconds, threads)."""
+    import oracle
+    t = {"f16": oracle.F16, "bf16": oracle.BF16, "tf32": oracle.F32, "e4m3": oracle.E4M3}[w.dtype]
+    rows = np.linspace(0, w.M - 1, rows_n).astype(np.int64)
+    threads = oracle.num_threads()
+    t0 = time.perf_counter()
+    oracle.gemm(w.M, w.N, w.K, x["A"], t, 0 if w.a_major == "k" else 1, x["lda"], x["B"], t,
+                0 if w.b_major == "k" else 1, x["ldb"], SFA=x["SFA"], SFB=x["SFB"], rows=rows, nthreads=threads)
+    dt = time.perf_counter() - t0
+    return 2.0 * rows_n * w.N * w.K / dt / 1e12, dt, threads
+
+
+# ----------------------------------------------------------------- distributed
+
+class DistCtx:
+    def __init__(self, n):
+        self.n = n
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.pg = None
+        if self.world > 1:
+            import torch
+            import torch.distributed as dist
+            local = int(os.environ.get("LOCAL_RANK", "0"))
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl")
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, v: float) -> float:
+        if not self.pg:
+            return v
+        import torch
+        t = torch.tensor([v], dtype=torch.float64, device="cuda")
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def sum(self, v: float) -> float:
+        if not self.pg:
+            return v
+        import torch
+        t = torch.tensor([v], dtype=torch.float64, device="cuda")
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.SUM)
+        return float(t.item())
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="bf16_8192_cta2", choices=sorted(syn.WORKLOADS))
+    ap.add_argument("--secondary", default="mxf8_8192", help="comma list of extra workloads ('' for none)")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-rows", type=int, default=0, help="oracle rows in the CPU baseline (0: 2 per thread)")
+    args = ap.parse_args()
+    w = syn.WORKLOADS[args.workload]
+
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        if rank != 0:
+            return
+        import oracle
+        oracle.build()
+        rows_n = args.cpu_rows or oracle.num_threads()
+        x = oracle_inputs(w)
+        vals = []
+        for _ in range(max(args.warmup, 0)):
+            oracle_sample(w, x, max(1, rows_n // 4))
+        for _ in range(args.steps):
+            v, dt, thr = oracle_sample(w, x, rows_n)
+            vals.append((v, dt))
+        value = float(np.median([v for v, _ in vals]))
+        ms = float(np.mean([dt for _, dt in vals])) * 1e3
+        sample = f"{rows_n} of {w.M} output rows (all {w.N} columns, K={w.K}) of {w.name} per step"
+        line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT,
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K,
+                                                "in": w.dtype, "sample": sample},
+                "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": thr, "kind": "oracle",
+                                 "sample": sample},
+                "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    import torch
+    dctx = DistCtx(args.gpus)
+    if dctx.world == 1:
+        torch.cuda.set_device(0)
+    from blackwell_tensor_core_swizzled_gb300.build import build as build_lib
+    build_lib()
+    import blackwell_tensor_core_swizzled_gb300 as tcg
+
+    peaks = measured_peaks()
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    try:
+        res = run_workload(tcg, torch, w, args.steps, args.warmup, dctx)
+        sec = []
+        for name in [s for s in args.secondary.split(",") if s and s != w.name]:
+            ws = syn.WORKLOADS[name]
+            r2 = run_workload(tcg, torch, ws, args.steps, args.warmup, dctx, measure_e2e=False)
+            t2 = dctx.max(r2["total_ms"])
+            sec.append({"workload": name, "value": round(dctx.world * 2.0 * ws.M * ws.N * ws.K * args.steps /
+                                                         (t2 * 1e-3) / 1e12, 1),
+                        "unit": UNIT, "ms_per_step": round(t2 / args.steps, 4), "dtype": ws.dtype,
+                        "gpu_launches": r2["launches"],
+                        "roofline": roofline(ws, r2["kernel_ms"], peaks, profiled_traffic(name))})
+    finally:
+        sampler.stop()
+    clocks = sampler.summary(res["t0"], res["t1"])
+
+    total_ms = dctx.max(res["total_ms"])
+    flops_step = 2.0 * w.M * w.N * w.K
+    value = dctx.world * flops_step * args.steps / (total_ms * 1e-3) / 1e12
+    e2e_ms = dctx.max(res["e2e_ms"])
+    e2e_val = dctx.world * flops_step / (e2e_ms * 1e-3) / 1e12
+
+    if dctx.rank != 0:
+        return
+    cpu = None
+    if dctx.world == 1 or dctx.rank == 0:
+        import oracle
+        oracle.build()
+        rows_n = args.cpu_rows or 2 * oracle.num_threads()
+        v, dt, thr = oracle_sample(w, oracle_inputs(w), rows_n)
+        cpu = {"value": round(v, 6), "unit": UNIT, "cores": thr, "kind": "oracle",
+               "sample": f"{rows_n} of {w.M} output rows (all {w.N} columns, K={w.K}) of {w.name}, "
+                         f"{dt:.2f} s wall"}
+    rl = roofline(w, res["kernel_ms"], peaks, profiled_traffic(w.name))
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": dctx.world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "in": w.dtype, "a_major": w.a_major,
+                   "b_major": w.b_major, "acc": w.acc, "out": w.out, "cta_group": w.cta_group,
+                   "l2": "inputs larger than L2 (no flush): A+B = "
+                         f"{(w.M * w.K + w.N * w.K) * ESIZE[w.dtype] / 2**20:.0f} MiB",
+                   "parallelism": f"replicas x{dctx.world}"},
+        "pct_dense_peak": round(100 * rl["frac"], 2),
+        "roofline": rl,
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(e2e_val, 1), "unit": UNIT, "h2d_bytes_per_step": res["h2d"],
+                "d2h_bytes_per_step": res["d2h"], "ms_per_step": round(e2e_ms, 3)},
+        "gpu_launches": res["launches"],
+        "clocks": clocks,
+        "secondary": sec,
+    }
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

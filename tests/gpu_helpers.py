@@ -13,6 +13,10 @@ ESIZE = {"f16": 2, "bf16": 2, "tf32": 4, "e4m3": 1}
 OUT = {"f32": (0, torch.float32), "f16": (1, torch.float16), "bf16": (2, torch.bfloat16)}
 ACC = {"f32": 0, "f16": 1}
 TAU = {"f32": 2e-3, "f16": 1e-2}   # parity tolerance per accumulator type (x sum|a||b|)
+# Unit roundoff of the output type: storing the fp32 accumulator as bf16/f16
+# (round to nearest even) adds at most U_OUT * |D| on top of the accumulation
+# error bounded by TAU * S.
+U_OUT = {"f32": 0.0, "bf16": 2.0 ** -8, "f16": 2.0 ** -11}
 
 
 def to_device(bits: np.ndarray) -> torch.Tensor:
@@ -82,11 +86,15 @@ def oracle_rows(oracle, x, rows=None):
                        SFA=x["SFA"], SFB=x["SFB"], rows=rows)
 
 
-def assert_parity(got: np.ndarray, ref: np.ndarray, S: np.ndarray, tau: float, what: str = ""):
+def assert_parity(got: np.ndarray, ref: np.ndarray, S: np.ndarray, tau: float, what: str = "",
+                  out: str = "f32"):
+    """|got - ref| <= tau*S (accumulation) + u_out*(|ref| + tau*S) (output rounding).
+    Returns max |got - ref| / S."""
     assert got.shape == ref.shape, (got.shape, ref.shape)
     assert np.all(np.isfinite(got)), f"{what}: non-finite outputs at {np.argwhere(~np.isfinite(got))[:5]}"
     err = np.abs(got - ref)
-    bad = err > tau * S
+    u = U_OUT[out]
+    bad = err > tau * S + u * (np.abs(ref) + tau * S)
     if np.any(bad):
         idx = np.argwhere(bad)[:8]
         ratio = np.max(err / np.maximum(S, 1e-300))

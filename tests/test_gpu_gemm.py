@@ -29,7 +29,7 @@ def _check_full(tcg, oracle_mod, x, out, acc, cg, **kw):
     D = run_gpu(tcg, x, out=out, acc=acc, cta_group=cg, **kw)
     got = D[:x["M"], :x["N"]].double().cpu().numpy()
     ref, S = oracle_rows(oracle_mod, x)
-    return assert_parity(got, ref, S, TAU[acc], f"{x['w'].dtype} {x['w'].a_major}{x['w'].b_major} cg{cg}")
+    return assert_parity(got, ref, S, TAU[acc], f"{x['w'].dtype} {x['w'].a_major}{x['w'].b_major} cg{cg}", out)
 
 
 SMALL = [
@@ -162,14 +162,14 @@ def test_named_entry_points(tcg, oracle_mod):
     tcg.gemm_bf16(256, 384, 192, to_device(x["A"]), 0, x["lda"], to_device(x["B"]), 1, x["ldb"], D, 2, 384, 0)
     assert tcg.check() == 0
     ref, S = oracle_rows(oracle_mod, x)
-    assert_parity(D.double().cpu().numpy(), ref, S, TAU["f32"], "gemm_bf16")
+    assert_parity(D.double().cpu().numpy(), ref, S, TAU["f32"], "gemm_bf16", "bf16")
     x = make_case("e4m3", "k", "k", 256, 384, 256, seed=9)
     D = torch.zeros((256, 384), dtype=torch.bfloat16, device="cuda")
     tcg.gemm_mxf8_blockscaled(256, 384, 256, to_device(x["A"]), 0, x["lda"], to_device(x["B"]), 0, x["ldb"],
                               to_device(x["SFA"]), to_device(x["SFB"]), D, 2, 384, 0)
     assert tcg.check() == 0
     ref, S = oracle_rows(oracle_mod, x)
-    assert_parity(D.double().cpu().numpy(), ref, S, TAU["f32"], "gemm_mxf8_blockscaled")
+    assert_parity(D.double().cpu().numpy(), ref, S, TAU["f32"], "gemm_mxf8_blockscaled", "bf16")
 
 
 # ------------------------------------------------------------- full-size workloads
@@ -187,5 +187,5 @@ def test_full_size_workloads_sampled_rows(tcg, oracle_mod, name):
     rows = sample_rows(w.M) if w.M > 256 else list(range(w.M))
     got = D[rows, :w.N].double().cpu().numpy()
     ref, S = oracle_rows(oracle_mod, x, rows=rows)
-    ratio = assert_parity(got, ref, S, TAU[w.acc], name)
+    ratio = assert_parity(got, ref, S, TAU[w.acc], name, w.out)
     print(f"{name}: max err/S {ratio:.3e} over {len(rows)} rows")
