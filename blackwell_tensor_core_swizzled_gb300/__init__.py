@@ -41,6 +41,8 @@ _SIGS = {
     "tcg_gemm_tf32": (_GEMM_SIG, _i32),
     "tcg_gemm_mxf8_blockscaled": ([_i64, _i64, _i64, _vp, _i32, _i64, _vp, _i32, _i64, _vp, _vp, _vp, _i32,
                                    _i64, _i32, _vp], _i32),
+    "tcg_gemm_mxf8_blockscaled_noalloc": ([_i64, _i64, _i64, _vp, _i32, _i64, _vp, _i32, _i64, _vp, _vp, _vp,
+                                           _i32, _i64, _i32, _vp], _i32),
     "tcg_gemm": ([ctypes.POINTER(GemmArgs), _vp], _i32),
     "tcg_mxf8_scale_image_bytes": ([_i64, _i64, _i32], _i64),
     "tcg_mxf8_tile_n": ([_i64, _i64, _i64, _i32, _i32], _i32),
@@ -138,6 +140,15 @@ def gemm_mxf8_blockscaled(M, N, K, A, a_major, lda, B, b_major, ldb, SFA, SFB, D
     return _ok(_lib.tcg_gemm_mxf8_blockscaled(M, N, K, _ptr(A), a_major, lda, _ptr(B), b_major, ldb, _ptr(SFA),
                                               _ptr(SFB), _ptr(D), d_type, ldd, acc_type, _stream(stream)),
                "gemm_mxf8_blockscaled")
+
+
+def gemm_mxf8_blockscaled_noalloc(M, N, K, A, a_major, lda, B, b_major, ldb, SFA, SFB, D, d_type, ldd,
+                                  acc_type=F32, stream=None):
+    """The allocation-free MXFP8 GEMM (scale images in the library's fixed
+    16 MiB device array; see include/tcg.h)."""
+    return _ok(_lib.tcg_gemm_mxf8_blockscaled_noalloc(M, N, K, _ptr(A), a_major, lda, _ptr(B), b_major, ldb,
+                                                      _ptr(SFA), _ptr(SFB), _ptr(D), d_type, ldd, acc_type,
+                                                      _stream(stream)), "gemm_mxf8_blockscaled_noalloc")
 
 
 def gemm(M, N, K, in_type, A, a_major, lda, B, b_major, ldb, D, d_type, ldd, acc_type=F32, SFA=None, SFB=None,

@@ -465,6 +465,8 @@ uint64_t wait_timeout_ns() {
 
 void set_launch_count(int n) { t_last_launches = n; }
 
+void set_error_message(const char* msg) { t_last_error = msg ? msg : ""; }
+
 }  // namespace tcg
 
 using namespace tcg;

@@ -38,3 +38,8 @@ uint64_t wait_timeout_ns();
 void set_launch_count(int n);
 
 }  // namespace tcg
+
+namespace tcg {
+// Sets the text tcg_last_error_string() returns on this thread.
+void set_error_message(const char* msg);
+}  // namespace tcg

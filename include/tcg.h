@@ -111,6 +111,26 @@ int tcg_gemm_mxf8_blockscaled(int64_t M, int64_t N, int64_t K,
                               void* D, tcg_dtype d_type, int64_t ldd,
                               tcg_dtype acc_type, void* stream);
 
+/* Same operation and arguments as tcg_gemm_mxf8_blockscaled, for callers that
+ * must not allocate device memory (for example a framework whose caching
+ * allocator owns all device memory, or code that cannot afford the
+ * device-wide wait of a cudaFree when a workspace grows).  No counterpart on
+ * the source pages: it only changes where the scale-factor images live.
+ * They are built in one fixed 16 MiB device array of the library (held by
+ * every GPU that loads the library until exit) instead of the per-stream
+ * workspace; problems whose two images need more return TCG_ERR_UNSUPPORTED
+ * before anything is queued.  All calls on a device share that array (each
+ * call rewrites what it reads, so nothing needs clearing); calls whose GPU
+ * work overlaps race on it and must be ordered.  The first call on a device
+ * looks up the array's address with that device current: make it before any
+ * stream capture.  Allocates nothing (no cudaMalloc/cudaFree). */
+int tcg_gemm_mxf8_blockscaled_noalloc(int64_t M, int64_t N, int64_t K,
+                                      const void* A, tcg_major a_major, int64_t lda,
+                                      const void* B, tcg_major b_major, int64_t ldb,
+                                      const uint8_t* SFA, const uint8_t* SFB,
+                                      void* D, tcg_dtype d_type, int64_t ldd,
+                                      tcg_dtype acc_type, void* stream);
+
 /* ---------------------------------------------------------------------------
  * Generic entry point: every knob of the four calls above plus the CTA-group
  * and tile choices (0 = let the library choose).
