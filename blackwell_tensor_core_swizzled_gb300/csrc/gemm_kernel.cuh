@@ -148,12 +148,27 @@ static __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, 
   }
 }
 
+// Single-thread wait: the common already-complete case stays inline, the
+// bounded slow path is a call.  The producer and MMA roles run on one thread
+// each, so their per-stage loop is this test, a few address adds and the
+// issues (a warp-wide wait + vote + warp sync per stage costs more issue time
+// than a 512-cycle stage of MMAs can hide).
+__device__ __forceinline__ bool thread_wait(uint32_t bar, uint32_t parity, const WaitCtx& w, uint32_t site) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_bounded(bar, parity, w, site);
+}
+
 // Every lane waits (each gets its own acquire), the outcome is made uniform
 // across the warp.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, WaitCtx w, uint32_t site) {
   const bool ok = wait_bounded(bar, parity, w, site);
   return __all_sync(0xffffffffu, ok);
 }
+
+// CTA-wide barrier 0 without the .aligned restriction: the threads of a warp
+// may arrive at different times (the single-thread roles finish after the
+// rest of their warp).
+__device__ __forceinline__ void cta_barrier_unaligned() { asm volatile("barrier.sync 0;" ::: "memory"); }
 
 __device__ __forceinline__ void tile_coords(int t, const GemmParams& p, int& mt, int& nt) {
   const int G = p.raster_group;
@@ -275,21 +290,20 @@ __global__ void __launch_bounds__(256, 1) gemm_kernel(const __grid_constant__ Ge
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    uint32_t it = 0;
-    bool ok = true;
-    for (int t = cluster_id; t < p.num_tiles && ok; t += num_clusters) {
-      int mt, nt;
-      tile_coords(t, p, mt, nt);
-      const int m0 = mt * C::MMA_M + static_cast<int>(rank) * C::BM;
-      const int n0 = nt * BN + static_cast<int>(rank) * C::BN_LOCAL;
-      for (int kb = 0; kb < p.num_k_blocks; ++kb, ++it) {
-        const int s = static_cast<int>(it % STAGES);
-        const uint32_t ph = (it / STAGES) & 1u;
-        if (!warp_wait(empty_bar(s), ph ^ 1u, wctx, SITE_PROD_EMPTY)) {
-          ok = false;
-          break;
-        }
-        if (lane == 0) {
+    // One thread; lanes 1..31 go straight to the teardown barrier.
+    if (lane == 0) {
+      uint32_t it = 0, s = 0, ph = 0;  // ring iteration, stage, phase of stage s
+      bool ok = true;
+      for (int t = cluster_id; t < p.num_tiles && ok; t += num_clusters) {
+        int mt, nt;
+        tile_coords(t, p, mt, nt);
+        const int m0 = mt * C::MMA_M + static_cast<int>(rank) * C::BM;
+        const int n0 = nt * BN + static_cast<int>(rank) * C::BN_LOCAL;
+        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+          if (!thread_wait(empty_bar(s), ph ^ 1u, wctx, SITE_PROD_EMPTY)) {
+            ok = false;
+            break;
+          }
           const uint32_t fb = (CG == 2) ? mapa_shared(full_bar(s), 0) : full_bar(s);
           if (rank == 0) mbar_arrive_expect_tx(full_bar(s), C::TX_BYTES);
           const uint32_t sa = sbase + s * C::STAGE_BYTES;
@@ -314,109 +328,105 @@ __global__ void __launch_bounds__(256, 1) gemm_kernel(const __grid_constant__ Ge
             tma_load<CG>(ssfa, &p.tmap_sfa, 0, kb * p.sf_a_tiles + sfa_tile, fb);
             tma_load<CG>(ssfb, &p.tmap_sfb, 0, kb * p.num_n_tiles + nt, fb);
           }
-        }
-        __syncwarp();
-      }
-    }
-    if (!ok && lane == 0) {
-      // Drain: let the copies this CTA issued land before the CTA can exit.
-      if (CG == 1 || rank == 0) {
-        const uint32_t n_out = it < static_cast<uint32_t>(STAGES) ? it : static_cast<uint32_t>(STAGES);
-        WaitCtx dctx{20000000ull, nullptr, abort_flag};
-        for (uint32_t j = it - n_out; j < it; ++j) {
-          const uint64_t t0 = globaltimer();
-          while (!mbar_try_wait(full_bar(j % STAGES), (j / STAGES) & 1u) && globaltimer() - t0 < dctx.timeout_ns) {
+          ++it;
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
           }
         }
-      } else {
-        const uint64_t t0 = globaltimer();
-        while (globaltimer() - t0 < 2000000ull) {
+      }
+      if (!ok) {
+        // Drain: let the copies this CTA issued land before the CTA can exit.
+        if (CG == 1 || rank == 0) {
+          const uint32_t n_out = it < static_cast<uint32_t>(STAGES) ? it : static_cast<uint32_t>(STAGES);
+          for (uint32_t j = it - n_out; j < it; ++j) {
+            const uint64_t t0 = globaltimer();
+            while (!mbar_try_wait(full_bar(j % STAGES), (j / STAGES) & 1u) && globaltimer() - t0 < 20000000ull) {
+            }
+          }
+        } else {
+          const uint64_t t0 = globaltimer();
+          while (globaltimer() - t0 < 2000000ull) {
+          }
         }
       }
     }
-    __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (CG == 1 || rank == 0) {
-      uint32_t it = 0, tcount = 0;
+    // One thread of the pair leader; lanes 1..31 go to the teardown barrier.
+    if (lane == 0 && (CG == 1 || rank == 0)) {
+      uint32_t it = 0, s = 0, ph = 0, tcount = 0;
       bool ok = true;
       for (int t = cluster_id; t < p.num_tiles && ok; t += num_clusters, ++tcount) {
         const int b = static_cast<int>(tcount % ACC);
         const uint32_t aph = (tcount / ACC) & 1u;
-        if (!warp_wait(acce_bar(b), aph ^ 1u, wctx, SITE_MMA_ACC_EMPTY)) {
+        if (!thread_wait(acce_bar(b), aph ^ 1u, wctx, SITE_MMA_ACC_EMPTY)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * BN);
-        for (int kb = 0; kb < p.num_k_blocks; ++kb, ++it) {
-          const int s = static_cast<int>(it % STAGES);
-          const uint32_t ph = (it / STAGES) & 1u;
-          if (!warp_wait(full_bar(s), ph, wctx, SITE_MMA_FULL)) {
+        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+          if (!thread_wait(full_bar(s), ph, wctx, SITE_MMA_FULL)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          if (lane == 0) {
-            const uint32_t sa = sbase + s * C::STAGE_BYTES;
-            const uint32_t sb = sa + C::A_BYTES;
-            const uint64_t adesc = sdesc(sa, p.a_desc_hi);
-            const uint64_t bdesc = sdesc(sb, p.b_desc_hi);
-            if constexpr (KIND == KIND_MXF8) {
-              const uint32_t ssfa = sb + C::B_BYTES;
-              const uint32_t ssfb = ssfa + C::SFA_BYTES;
-              const uint32_t sf_col = tmem_base + C::SF_COL0 + (it % C::SF_SLOTS) * C::SF_SLOT_COLS;
-              bool slot_free = true;
-              if (it >= static_cast<uint32_t>(C::SF_SLOTS)) {
-                // the MMAs of iteration it - SF_SLOTS read this slot; their
-                // stage's empty barrier completes when they have finished
-                const uint32_t j = it - C::SF_SLOTS;
-                slot_free = wait_bounded(empty_bar(j % STAGES), (j / STAGES) & 1u, wctx, SITE_MMA_FULL);
+          const uint32_t sa = sbase + s * C::STAGE_BYTES;
+          const uint32_t sb = sa + C::A_BYTES;
+          const uint64_t adesc = sdesc(sa, p.a_desc_hi);
+          const uint64_t bdesc = sdesc(sb, p.b_desc_hi);
+          if constexpr (KIND == KIND_MXF8) {
+            const uint32_t ssfa = sb + C::B_BYTES;
+            const uint32_t ssfb = ssfa + C::SFA_BYTES;
+            const uint32_t sf_col = tmem_base + C::SF_COL0 + (it % C::SF_SLOTS) * C::SF_SLOT_COLS;
+            if (it >= static_cast<uint32_t>(C::SF_SLOTS)) {
+              // the MMAs of iteration it - SF_SLOTS read this slot; their
+              // stage's empty barrier completes when they have finished
+              const uint32_t j = it - C::SF_SLOTS;
+              if (!thread_wait(empty_bar(j % STAGES), (j / STAGES) & 1u, wctx, SITE_MMA_FULL)) {
+                ok = false;
+                break;
               }
-              // on abort (slot wait failed) nothing is issued; the next warp_wait
-              // sees the abort flag and stops every lane
-              if (slot_free) {
-              // 32 rows x 16 bytes, rows 16 bytes apart: (ldo 16, sdo 128, no swizzle)
-              const uint64_t cp_hi = sdesc_hi(16, 128, SW_NONE);
-              tc_cp_32x128b_warpx4<CG>(sf_col, sdesc(ssfa, cp_hi));
+            }
+            // 32 rows x 16 bytes, rows 16 bytes apart: (ldo 16, sdo 128, no swizzle)
+            const uint64_t cp_hi = sdesc_hi(16, 128, SW_NONE);
+            tc_cp_32x128b_warpx4<CG>(sf_col, sdesc(ssfa, cp_hi));
 #pragma unroll
-              for (int c = 0; c < C::SFB_CHUNKS; ++c)
-                tc_cp_32x128b_warpx4<CG>(sf_col + 4 + 4 * c, sdesc(ssfb + 512 * c, cp_hi));
+            for (int c = 0; c < C::SFB_CHUNKS; ++c)
+              tc_cp_32x128b_warpx4<CG>(sf_col + 4 + 4 * c, sdesc(ssfb + 512 * c, cp_hi));
 #pragma unroll
-              for (int j = 0; j < C::KSTEPS; ++j) {
-                mma_mxf8<CG>(d_tmem, adesc + ((j * p.a_kstep) >> 4), bdesc + ((j * p.b_kstep) >> 4),
-                             p.idesc | idesc_sf_ids(j, j), sf_col, sf_col + 4, (kb | j) != 0);
-              }
-                tc_commit<CG>(empty_bar(s));
-              }
-            } else {
+            for (int j = 0; j < C::KSTEPS; ++j) {
+              mma_mxf8<CG>(d_tmem, adesc + ((j * p.a_kstep) >> 4), bdesc + ((j * p.b_kstep) >> 4),
+                           p.idesc | idesc_sf_ids(j, j), sf_col, sf_col + 4, (kb | j) != 0);
+            }
+          } else {
 #pragma unroll
-              for (int j = 0; j < C::KSTEPS; ++j) {
-                const uint64_t ad = adesc + ((j * p.a_kstep) >> 4);
-                const uint64_t bd = bdesc + ((j * p.b_kstep) >> 4);
-                if constexpr (KIND == KIND_F16)
-                  mma_f16<CG>(d_tmem, ad, bd, p.idesc, (kb | j) != 0);
-                else
-                  mma_tf32<CG>(d_tmem, ad, bd, p.idesc, (kb | j) != 0);
-              }
-              tc_commit<CG>(empty_bar(s));
+            for (int j = 0; j < C::KSTEPS; ++j) {
+              const uint64_t ad = adesc + ((j * p.a_kstep) >> 4);
+              const uint64_t bd = bdesc + ((j * p.b_kstep) >> 4);
+              if constexpr (KIND == KIND_F16)
+                mma_f16<CG>(d_tmem, ad, bd, p.idesc, (kb | j) != 0);
+              else
+                mma_tf32<CG>(d_tmem, ad, bd, p.idesc, (kb | j) != 0);
             }
           }
-          __syncwarp();
+          tc_commit<CG>(empty_bar(s));
+          ++it;
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
         }
         if (!ok) break;
-        if (lane == 0) tc_commit<CG>(accf_bar(b));
-        __syncwarp();
+        tc_commit<CG>(accf_bar(b));
       }
       if (!ok) {
         // Drain: wait (bounded) for every MMA / cp this thread issued.
-        if (lane == 0) {
-          tc_commit<CG>(drain_bar);
-          const uint64_t t0 = globaltimer();
-          while (!mbar_try_wait(drain_bar, 0) && globaltimer() - t0 < 20000000ull) {
-          }
+        tc_commit<CG>(drain_bar);
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try_wait(drain_bar, 0) && globaltimer() - t0 < 20000000ull) {
         }
-        __syncwarp();
       }
     }
   } else if (warp >= 4) {
@@ -463,7 +473,8 @@ __global__ void __launch_bounds__(256, 1) gemm_kernel(const __grid_constant__ Ge
 
   // ------------------------------------------------------------ teardown
   tc_fence_before();
-  __syncthreads();
+  cta_barrier_unaligned();
+  __syncwarp();
   if constexpr (CG == 2) cluster_sync();
   tc_fence_after();
   if (warp == 2) tmem_dealloc<CG>(tmem_base, C::TMEM_COLS);
