@@ -314,7 +314,8 @@ int run_gemm(const tcg_gemm_args* args, cudaStream_t s) {
     return TCG_ERR_INVALID;
   if (a.acc_type == TCG_BF16) return TCG_ERR_UNSUPPORTED;
   if (a.acc_type == TCG_F16 && (a.in_type != TCG_IN_F16 || a.d_type != TCG_F16)) return TCG_ERR_UNSUPPORTED;
-  if (a.cta_group < 0 || a.cta_group > 2 || a.raster_group < 0) return TCG_ERR_INVALID;
+  if (a.cta_group < 0 || a.cta_group > 2 || a.raster_group < 0 || a.sf_staging < 0 || a.sf_staging > 1)
+    return TCG_ERR_INVALID;
   if (a.M > INT32_MAX / 2 || a.N > INT32_MAX / 2 || a.K > INT32_MAX / 2) return TCG_ERR_UNSUPPORTED;
   if (a.M == 0 || a.N == 0) return TCG_OK;
   if (!a.D) return TCG_ERR_INVALID;
@@ -387,6 +388,7 @@ int run_gemm(const tcg_gemm_args* args, cudaStream_t s) {
   prm.d_vec_ok = (reinterpret_cast<uintptr_t>(a.D) % 16 == 0) && ((a.ldd * ds) % 16 == 0);
   prm.err = d->err;
   prm.timeout_ns = g_timeout_ns.load();
+  prm.sf_via_cp = a.sf_staging == 1;
 
   int launches = 0;
   if (scaled) {

@@ -4,16 +4,22 @@
 //   D[m,n] = sum_k (SFA.A)[m,k] (SFB.B)[k,n]   (kind::mxf8f6f4.block_scale)
 //
 // Structure (one CTA per SM, or one CTA pair per two SMs for cta_group::2):
-//   warp 0      TMA producer: 128B-swizzled A/B tiles (and scale images) into
-//               a STAGES-deep ring, full[s] barriers counting bytes;
+//   warp 0      TMA producer (one thread): 128B-swizzled A/B tiles (and scale
+//               images) into a STAGES-deep ring, full[s] barriers counting
+//               bytes;
 //   warp 1      MMA issuer (one thread; pair leader only): for each ring stage
-//               the tcgen05.cp scale staging (block-scaled) and KSTEPS
-//               tcgen05.mma issues, then tcgen05.commit -> empty[s]; at the
-//               end of a tile a commit -> acc_full[b];
+//               KSTEPS tcgen05.mma issues, then tcgen05.commit -> empty[s]; at
+//               the end of a tile a commit -> acc_full[b];
 //   warp 2      TMEM allocation / deallocation (512 columns);
 //   warps 4..7  epilogue: tcgen05.ld .32x32b from accumulator b (warp w
 //               reads lanes 32*(w%4)..+31), convert, store to global, then
-//               arrive acc_empty[b].
+//               arrive acc_empty[b];
+//   warps 8..11 (block scaling) scale staging: each writes its TMEM lane
+//               quadrant of the stage's scale slot with tcgen05.st and arrives
+//               sf_ready[slot].  Alternatively (GemmParams::sf_via_cp) the MMA
+//               thread stages the scales itself with tcgen05.cp .32x128b.warpx4;
+//               the warps are faster because every cp is an instruction in the
+//               MMA thread's in-order tensor pipe.
 // Accumulators are double buffered in TMEM so the epilogue of one tile
 // overlaps the main loop of the next.
 //
@@ -81,6 +87,7 @@ struct GemmParams {
   int d_vec_ok;
   unsigned long long* err;
   uint64_t timeout_ns;
+  int sf_via_cp;  // block scaling: 1 = MMA thread stages scales with tcgen05.cp, 0 = scale warps with tcgen05.st
 };
 
 template <int CG, int BN, int ACC, int STAGES, int KIND>
@@ -94,7 +101,10 @@ struct GemmCfg {
   static constexpr int SFB_BYTES = KIND == KIND_MXF8 ? 512 * SFB_CHUNKS : 0;
   static constexpr int LOAD_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
   static constexpr int STAGE_BYTES = (LOAD_BYTES + 1023) / 1024 * 1024;
-  static constexpr int TX_BYTES = LOAD_BYTES * CG;
+  // bytes the pair leader's full barrier counts (A and B of both CTAs); the
+  // scale images complete on each CTA's own scale barrier
+  static constexpr int TX_BYTES = (A_BYTES + B_BYTES) * CG;
+  static constexpr int SF_TX_BYTES = SFA_BYTES + SFB_BYTES;
   static constexpr int MMA_M = 128 * CG;
   static constexpr int MMA_K = KIND == KIND_F16 ? 16 : KIND == KIND_TF32 ? 8 : 32;
   static constexpr int ELEM_BYTES = KIND == KIND_F16 ? 2 : KIND == KIND_TF32 ? 4 : 1;
@@ -108,9 +118,14 @@ struct GemmCfg {
   static constexpr int SF_SLOTS_FREE = (TMEM_COLS - ACC * BN) / SF_SLOT_COLS;
   static constexpr int SF_SLOTS = SF_SLOTS_FREE < 4 ? SF_SLOTS_FREE : 4;
   static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
-  static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC + 1;
+  // full[S], empty[S], acc_full[ACC], acc_empty[ACC], drain, and for block
+  // scaling sf_loaded[S] (scale bytes in smem) and sf_ready[SF_SLOTS] (scales
+  // written to TMEM by the scale warps)
+  static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC + 1 + (KIND == KIND_MXF8 ? STAGES + SF_SLOTS : 0);
   static constexpr int SMEM_BYTES = 1024 + BAR_OFF + NUM_BARS * 8 + 16;
-  static constexpr int THREADS = 256;
+  // warps 0..7 as described above; block scaling adds warps 8..11, one per
+  // TMEM lane quadrant, which stage the scale factors into TMEM
+  static constexpr int THREADS = KIND == KIND_MXF8 ? 384 : 256;
   static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "epilogue drains 32-column chunks");
   static_assert(BN % (16 * CG) == 0, "MMA N constraint / per-CTA B split");
   static_assert(ACC * BN + (KIND == KIND_MXF8 ? SF_SLOTS * SF_SLOT_COLS : 0) <= TMEM_COLS, "TMEM budget");
@@ -234,7 +249,7 @@ __device__ __forceinline__ void store_row32(const GemmParams& p, int row, int co
 }
 
 template <int CG, int BN, int ACC, int STAGES, int KIND>
-__global__ void __launch_bounds__(256, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
+__global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
   using C = GemmCfg<CG, BN, ACC, STAGES, KIND>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -247,6 +262,8 @@ __global__ void __launch_bounds__(256, 1) gemm_kernel(const __grid_constant__ Ge
   auto accf_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
   auto acce_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + ACC + b); };
   const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 2 * ACC);
+  auto sfl_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + 2 * ACC + 1 + s); };
+  auto sfr_bar = [&](int slot) { return bar0 + 8u * (3 * STAGES + 2 * ACC + 1 + slot); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::BAR_OFF + 8 * C::NUM_BARS);
   volatile uint32_t* abort_flag = tmem_slot + 1;
 
@@ -267,6 +284,10 @@ __global__ void __launch_bounds__(256, 1) gemm_kernel(const __grid_constant__ Ge
       mbar_init(acce_bar(b), 4 * CG);
     }
     mbar_init(drain_bar, 1);
+    if constexpr (KIND == KIND_MXF8) {
+      for (int s = 0; s < STAGES; ++s) mbar_init(sfl_bar(s), 1);
+      for (int k = 0; k < C::SF_SLOTS; ++k) mbar_init(sfr_bar(k), 4 * CG);
+    }
     *abort_flag = 0u;
     fence_mbarrier_init();
   }
@@ -325,8 +346,11 @@ __global__ void __launch_bounds__(256, 1) gemm_kernel(const __grid_constant__ Ge
             // a pair tile's second half may lie wholly beyond M: its A rows are
             // zero-filled, so any valid scale row will do
             const int sfa_tile = min(mt * CG + static_cast<int>(rank), p.sf_a_tiles - 1);
-            tma_load<CG>(ssfa, &p.tmap_sfa, 0, kb * p.sf_a_tiles + sfa_tile, fb);
-            tma_load<CG>(ssfb, &p.tmap_sfb, 0, kb * p.num_n_tiles + nt, fb);
+            // the scale warps of this CTA consume these: they complete on
+            // this CTA's own sf_loaded[s]
+            mbar_arrive_expect_tx(sfl_bar(s), C::SF_TX_BYTES);
+            tma_load_2d(ssfa, &p.tmap_sfa, 0, kb * p.sf_a_tiles + sfa_tile, sfl_bar(s));
+            tma_load_2d(ssfb, &p.tmap_sfb, 0, kb * p.num_n_tiles + nt, sfl_bar(s));
           }
           ++it;
           if (++s == STAGES) {
@@ -337,8 +361,15 @@ __global__ void __launch_bounds__(256, 1) gemm_kernel(const __grid_constant__ Ge
       }
       if (!ok) {
         // Drain: let the copies this CTA issued land before the CTA can exit.
+        const uint32_t n_out = it < static_cast<uint32_t>(STAGES) ? it : static_cast<uint32_t>(STAGES);
+        if constexpr (KIND == KIND_MXF8) {
+          for (uint32_t j = it - n_out; j < it; ++j) {
+            const uint64_t t0 = globaltimer();
+            while (!mbar_try_wait(sfl_bar(j % STAGES), (j / STAGES) & 1u) && globaltimer() - t0 < 20000000ull) {
+            }
+          }
+        }
         if (CG == 1 || rank == 0) {
-          const uint32_t n_out = it < static_cast<uint32_t>(STAGES) ? it : static_cast<uint32_t>(STAGES);
           for (uint32_t j = it - n_out; j < it; ++j) {
             const uint64_t t0 = globaltimer();
             while (!mbar_try_wait(full_bar(j % STAGES), (j / STAGES) & 1u) && globaltimer() - t0 < 20000000ull) {
@@ -377,24 +408,40 @@ __global__ void __launch_bounds__(256, 1) gemm_kernel(const __grid_constant__ Ge
           const uint64_t adesc = sdesc(sa, p.a_desc_hi);
           const uint64_t bdesc = sdesc(sb, p.b_desc_hi);
           if constexpr (KIND == KIND_MXF8) {
-            const uint32_t ssfa = sb + C::B_BYTES;
-            const uint32_t ssfb = ssfa + C::SFA_BYTES;
-            const uint32_t sf_col = tmem_base + C::SF_COL0 + (it % C::SF_SLOTS) * C::SF_SLOT_COLS;
-            if (it >= static_cast<uint32_t>(C::SF_SLOTS)) {
-              // the MMAs of iteration it - SF_SLOTS read this slot; their
-              // stage's empty barrier completes when they have finished
-              const uint32_t j = it - C::SF_SLOTS;
-              if (!thread_wait(empty_bar(j % STAGES), (j / STAGES) & 1u, wctx, SITE_MMA_FULL)) {
+            // this iteration's scales go to TMEM slot it % SF_SLOTS
+            const uint32_t slot = it % C::SF_SLOTS;
+            const uint32_t sf_col = tmem_base + C::SF_COL0 + slot * C::SF_SLOT_COLS;
+            if (p.sf_via_cp) {
+              // this thread stages the scales with tcgen05.cp: wait until
+              // they are in smem and the slot's previous readers (the MMAs of
+              // iteration it - SF_SLOTS) have completed
+              if (!thread_wait(sfl_bar(s), ph, wctx, SITE_MMA_FULL)) {
                 ok = false;
                 break;
               }
-            }
-            // 32 rows x 16 bytes, rows 16 bytes apart: (ldo 16, sdo 128, no swizzle)
-            const uint64_t cp_hi = sdesc_hi(16, 128, SW_NONE);
-            tc_cp_32x128b_warpx4<CG>(sf_col, sdesc(ssfa, cp_hi));
+              if (it >= static_cast<uint32_t>(C::SF_SLOTS)) {
+                const uint32_t j = it - C::SF_SLOTS;
+                if (!thread_wait(empty_bar(j % STAGES), (j / STAGES) & 1u, wctx, SITE_MMA_FULL)) {
+                  ok = false;
+                  break;
+                }
+              }
+              const uint32_t ssfa = sb + C::B_BYTES;
+              // 32 rows x 16 bytes, rows 16 bytes apart: (ldo 16, sdo 128, no swizzle)
+              const uint64_t cp_hi = sdesc_hi(16, 128, SW_NONE);
+              tc_cp_32x128b_warpx4<CG>(sf_col, sdesc(ssfa, cp_hi));
 #pragma unroll
-            for (int c = 0; c < C::SFB_CHUNKS; ++c)
-              tc_cp_32x128b_warpx4<CG>(sf_col + 4 + 4 * c, sdesc(ssfb + 512 * c, cp_hi));
+              for (int c = 0; c < C::SFB_CHUNKS; ++c)
+                tc_cp_32x128b_warpx4<CG>(sf_col + 4 + 4 * c, sdesc(ssfa + C::SFA_BYTES + 512 * c, cp_hi));
+            } else {
+              // the scale warps of both CTAs have written this iteration's
+              // scales into the slot with tcgen05.st
+              if (!thread_wait(sfr_bar(slot), (it / C::SF_SLOTS) & 1u, wctx, SITE_MMA_FULL)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+            }
 #pragma unroll
             for (int j = 0; j < C::KSTEPS; ++j) {
               mma_mxf8<CG>(d_tmem, adesc + ((j * p.a_kstep) >> 4), bdesc + ((j * p.b_kstep) >> 4),
@@ -426,6 +473,52 @@ __global__ void __launch_bounds__(256, 1) gemm_kernel(const __grid_constant__ Ge
         tc_commit<CG>(drain_bar);
         const uint64_t t0 = globaltimer();
         while (!mbar_try_wait(drain_bar, 0) && globaltimer() - t0 < 20000000ull) {
+        }
+      }
+    }
+  } else if (KIND == KIND_MXF8 && warp >= 8) {
+    // ------------------------------------------------------------ scale warps
+    // Warp 8+q writes TMEM lane quadrant q of every scale slot: source row l
+    // of a 512-byte chunk (bytes [16l, 16l+16)) goes to lane 32q + l, four
+    // columns, which is the placement one tcgen05.cp .32x128b.warpx4 of the
+    // chunk produces (each quadrant is one of its replicas).
+    if constexpr (KIND == KIND_MXF8) {
+      if (!p.sf_via_cp) {
+        const int q = warp & 3;
+        const uint32_t my_tiles =
+            cluster_id < p.num_tiles ? (p.num_tiles - cluster_id + num_clusters - 1) / num_clusters : 0;
+        const uint32_t total_it = my_tiles * static_cast<uint32_t>(p.num_k_blocks);
+        uint32_t s = 0, ph = 0;
+        for (uint32_t it = 0; it < total_it; ++it) {
+          if (!warp_wait(sfl_bar(s), ph, wctx, SITE_MMA_FULL)) break;
+          if (it >= static_cast<uint32_t>(C::SF_SLOTS)) {
+            // the slot's previous readers: the MMAs of iteration it - SF_SLOTS
+            const uint32_t j = it - C::SF_SLOTS;
+            if (!warp_wait(empty_bar(j % STAGES), (j / STAGES) & 1u, wctx, SITE_MMA_FULL)) break;
+          }
+          tc_fence_after();
+          const uint4* sf = reinterpret_cast<const uint4*>(gbase + s * C::STAGE_BYTES + C::A_BYTES + C::B_BYTES);
+          const uint32_t slot = it % C::SF_SLOTS;
+          const uint32_t col =
+              tmem_base + (static_cast<uint32_t>(32 * q) << 16) + C::SF_COL0 + slot * C::SF_SLOT_COLS;
+          tmem_st_32x32b_x4(col, sf[lane]);  // SFA: 4 columns
+          if constexpr (C::SFB_CHUNKS == 2)
+            tmem_st_32x32b_x8(col + 4, sf[32 + lane], sf[64 + lane]);  // SFB: 8 columns
+          else
+            tmem_st_32x32b_x4(col + 4, sf[32 + lane]);
+          tc_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            if constexpr (CG == 2)
+              mbar_arrive_cluster(mapa_shared(sfr_bar(slot), 0));
+            else
+              mbar_arrive(sfr_bar(slot));
+          }
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
         }
       }
     }

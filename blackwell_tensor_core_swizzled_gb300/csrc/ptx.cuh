@@ -278,3 +278,21 @@ __device__ __forceinline__ void tmem_ld_32x32b_x16_pack16(uint32_t taddr, uint32
 }
 
 }  // namespace tcg
+
+namespace tcg {
+
+// tcgen05.st .32x32b.x4 / .x8: lane l of the warp writes TMEM lane
+// (base + l), columns [col, col+4) / [col, col+8).
+__device__ __forceinline__ void tmem_st_32x32b_x4(uint32_t taddr, const uint4& v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_32x32b_x8(uint32_t taddr, const uint4& a, const uint4& b) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+               "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
+               : "memory");
+}
+
+}  // namespace tcg

@@ -150,6 +150,9 @@ typedef struct {
   tcg_dtype acc_type;
   int cta_group;     /* 0 auto, 1 (one CTA per 128xN tile), 2 (CTA pair, 256xN) */
   int raster_group;  /* 0 auto; tiles are visited in groups of this many M tiles */
+  int sf_staging;    /* block scaling: 0 = scale warps write TMEM with tcgen05.st
+                        (default, faster), 1 = the MMA thread copies with
+                        tcgen05.cp .32x128b.warpx4 ("tcgen05.cp" page) */
 } tcg_gemm_args;
 
 int tcg_gemm(const tcg_gemm_args* args, void* stream);

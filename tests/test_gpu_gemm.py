@@ -104,11 +104,20 @@ def test_blockscaled_identity_pins_scale_placement(tcg):
     expo = SFA[m, m // 32].astype(np.int64)[:, None] + SFB[:, m // 32].T.astype(np.int64) - 254
     ref = np.ldexp(bdec, expo)
     for cg in (1, 2):
-        D = torch.zeros((n, N), dtype=torch.float32, device="cuda")
-        tcg.gemm(n, N, n, 3, to_device(A), 0, n, to_device(B), 0, n, D, 0, N, 0, SFA=to_device(SFA),
-                 SFB=to_device(SFB), cta_group=cg)
-        assert tcg.check() == 0
-        assert np.array_equal(D.double().cpu().numpy(), ref), f"cta_group {cg}"
+        for staging in (0, 1):  # scale warps with tcgen05.st / MMA thread with tcgen05.cp
+            D = torch.zeros((n, N), dtype=torch.float32, device="cuda")
+            tcg.gemm(n, N, n, 3, to_device(A), 0, n, to_device(B), 0, n, D, 0, N, 0, SFA=to_device(SFA),
+                     SFB=to_device(SFB), cta_group=cg, sf_staging=staging)
+            assert tcg.check() == 0
+            assert np.array_equal(D.double().cpu().numpy(), ref), f"cta_group {cg} staging {staging}"
+
+
+@pytest.mark.parametrize("am,bm,M,N,K,cg", [("k", "k", 300, 520, 256, 2), ("k", "k", 520, 300, 208, 1),
+                                            ("mn", "mn", 200, 300, 256, 1), ("mn", "k", 260, 460, 640, 2)])
+def test_blockscaled_tcgen05_cp_staging(tcg, oracle_mod, am, bm, M, N, K, cg):
+    # the alternative scale path: tcgen05.cp .32x128b.warpx4 issued by the MMA thread
+    x = make_case("e4m3", am, bm, M, N, K, seed=M + 3 * N + K)
+    _check_full(tcg, oracle_mod, x, "f32", "f32", cg, sf_staging=1)
 
 
 def test_scale_prepare_kernel_matches_oracle_image(tcg):
