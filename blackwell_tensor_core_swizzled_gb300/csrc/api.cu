@@ -150,7 +150,9 @@ struct Plan {
 
 int pick_cta_group(const tcg_gemm_args& a) {
   if (a.cta_group == 1 || a.cta_group == 2) return a.cta_group;
-  if (a.in_type == TCG_IN_E4M3 && a.b_major == TCG_MN_MAJOR) return 1;
+  // block-scaled: the single-CTA 128x256 tile measured faster than the pair
+  // tile (more MMA work per issued instruction, own issue thread per SM)
+  if (a.in_type == TCG_IN_E4M3) return 1;
   // pairs halve the B traffic per SM; use them once there are enough 256-row tiles
   return (a.M >= 1024 && a.N >= 1024) ? 2 : 1;
 }
@@ -367,7 +369,9 @@ int run_gemm(const tcg_gemm_args* args, cudaStream_t s) {
   const int es = esize_of(a.in_type);
   prm.num_k_blocks = static_cast<int>(cdiv(a.K * es, 128));
   prm.num_tiles = prm.num_m_tiles * prm.num_n_tiles;
-  prm.raster_group = a.raster_group > 0 ? a.raster_group : 8;
+  // M tiles per raster group (measured at 8192^3: 16 for 128-row tiles, 8 for
+  // 256-row pair tiles, i.e. 2048 rows of A either way)
+  prm.raster_group = a.raster_group > 0 ? a.raster_group : (cg == 1 ? 16 : 8);
   if (int rc = setup_operand(a.A, a.in_type, a.a_major, a.M, a.K, a.lda, 128, &prm.tmap_a, &prm.a_mn_major,
                              &prm.a_boxes, &prm.a_box_mn, &prm.a_box_bytes, &prm.a_desc_hi, &prm.a_kstep))
     return rc;

@@ -11,7 +11,7 @@
 //
 // Limits and sharing:
 //  * the two scale images of one call must fit in kScratchBytes (16 MiB;
-//    an 8192 x 8192 x 8192 problem needs 4.4 MiB); larger problems are
+//    an 8192 x 8192 x 8192 problem needs 4 MiB); larger problems are
 //    rejected with TCG_ERR_UNSUPPORTED before anything is queued;
 //  * every call on every stream of a device uses the same array, which keeps
 //    the previous call's contents.  Each call rewrites every byte of the image
