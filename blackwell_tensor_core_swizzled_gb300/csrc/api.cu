@@ -408,10 +408,9 @@ int run_gemm(const tcg_gemm_args* args, cudaStream_t s) {
       if (int rc = workspace(dev, s, ba + bb, &ws)) return rc;
       uint8_t* wa = static_cast<uint8_t*>(ws);
       uint8_t* wb = wa + ba;  // ba is a multiple of 512
-      cudaError_t e = launch_sf_prepare(a.SFA, a.M, a.K, 128, wa, s);
-      if (e == cudaSuccess) e = launch_sf_prepare(a.SFB, a.N, a.K, bn, wb, s);
+      const cudaError_t e = launch_sf_prepare_pair(a.SFA, a.M, 128, wa, a.SFB, a.N, bn, wb, a.K, s);
       if (e != cudaSuccess) return record_cuda(e);
-      launches += 2;
+      launches += 1;
       sfa_img = wa;
       sfb_img = wb;
     }

@@ -29,6 +29,10 @@ KernelInfo kinfo_mxf8(int cta_group);  // cta_group 2: BN 224, 2 accumulators; 1
 // Scale-factor rearrangement kernel launch (gemm_mxf8.cu).
 cudaError_t launch_sf_prepare(const uint8_t* sf, int64_t rows, int64_t K, int tile_rows, uint8_t* img,
                               cudaStream_t stream);
+// Both operands' images in one launch.
+cudaError_t launch_sf_prepare_pair(const uint8_t* sfa, int64_t rows_a, int tile_a, uint8_t* img_a,
+                                   const uint8_t* sfb, int64_t rows_b, int tile_b, uint8_t* img_b, int64_t K,
+                                   cudaStream_t stream);
 
 // Host state helpers (api.cu).
 int record_cuda(cudaError_t e);              // stores the message, returns TCG_ERR_CUDA (or TCG_OK)

@@ -30,48 +30,88 @@ KernelInfo kinfo_mxf8(int cta_group) {
 // tcgen05.cp .32x128b.warpx4 of such a chunk (source row i = bytes
 // [16i, 16i+16)) puts it at TMEM lane r%32 (and its three replicas),
 // byte-column 4*(r//32)+kb, which is where the "tcgen05.mma" page places
-// block scales.  Each thread writes one 32-bit word: the four K blocks of one
-// row, which are contiguous in the plain layout.  Absent rows / blocks get
-// 127 (a scale of one).
-__global__ void sf_prepare_kernel(const uint8_t* __restrict__ sf, int64_t rows, int64_t kblocks, int tile_rows,
-                                  int64_t tiles, int chunks, int64_t total_words, uint32_t* __restrict__ img) {
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total_words;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int w = static_cast<int>(i & 127);
-    int64_t chunk_id = i >> 7;
-    const int c = static_cast<int>(chunk_id % chunks);
-    chunk_id /= chunks;
-    const int64_t t = chunk_id % tiles;
-    const int64_t ks = chunk_id / tiles;
-    const int rl = c * 128 + 32 * (w & 3) + (w >> 2);
-    const int64_t r = t * tile_rows + rl;
-    uint32_t v = 0x7F7F7F7Fu;
-    if (rl < tile_rows && r < rows) {
-      v = 0u;
-#pragma unroll
-      for (int kb = 0; kb < 4; ++kb) {
-        const int64_t kk = ks * 4 + kb;
-        const uint32_t b = kk < kblocks ? static_cast<uint32_t>(sf[r * kblocks + kk]) : 127u;
-        v |= b << (8 * kb);
-      }
+// block scales; the scale warps write the same placement with tcgen05.st.
+// Absent rows / blocks get 127 (a scale of one).
+//
+// One block per 128-row chunk of one matrix (SFA and SFB in the same launch):
+// the chunk's rows are staged through shared memory SF_KB_CHUNK K blocks at a
+// time with row-contiguous reads, then each K step's 512-byte chunk is written
+// as 128 consecutive words.
+struct SfJob {
+  const uint8_t* sf;
+  int64_t rows;
+  int64_t tiles;
+  int tile_rows;
+  int chunks;
+  uint32_t* img;
+};
+
+constexpr int SF_KB_CHUNK = 128;
+
+__global__ void __launch_bounds__(256) sf_prepare_kernel(SfJob ja, SfJob jb, int64_t kblocks) {
+  __shared__ uint8_t rows_s[128][SF_KB_CHUNK + 4];
+  int64_t blk = blockIdx.x;
+  const int64_t na = ja.tiles * ja.chunks;
+  const SfJob j = blk < na ? ja : jb;
+  if (blk >= na) blk -= na;
+  const int64_t t = blk / j.chunks;
+  const int c = static_cast<int>(blk % j.chunks);
+  const int64_t row0 = t * j.tile_rows + 128 * c;
+  const int64_t in_tile = j.tile_rows - 128 * c;
+  const int64_t in_matrix = j.rows - row0;
+  const int valid = static_cast<int>(min(min(in_tile, in_matrix), static_cast<int64_t>(128)));
+  for (int64_t k0 = 0; k0 < kblocks; k0 += SF_KB_CHUNK) {
+    const int nk = static_cast<int>(min(static_cast<int64_t>(SF_KB_CHUNK), kblocks - k0));
+    __syncthreads();
+    for (int i = threadIdx.x; i < 128 * SF_KB_CHUNK; i += blockDim.x) {
+      const int rl = i / SF_KB_CHUNK, kk = i % SF_KB_CHUNK;
+      uint8_t v = 127;
+      if (rl < valid && kk < nk) v = j.sf[(row0 + rl) * kblocks + k0 + kk];
+      rows_s[rl][kk] = v;
     }
-    img[i] = v;
+    __syncthreads();
+    const int nks = (nk + 3) / 4;
+    for (int i = threadIdx.x; i < nks * 128; i += blockDim.x) {
+      const int ksl = i >> 7, w = i & 127;
+      const int rl = 32 * (w & 3) + (w >> 2);
+      const uint8_t* src = &rows_s[rl][4 * ksl];
+      const uint32_t v = static_cast<uint32_t>(src[0]) | (static_cast<uint32_t>(src[1]) << 8) |
+                         (static_cast<uint32_t>(src[2]) << 16) | (static_cast<uint32_t>(src[3]) << 24);
+      const int64_t ks = k0 / 4 + ksl;
+      j.img[((ks * j.tiles + t) * j.chunks + c) * 128 + w] = v;
+    }
   }
+}
+
+namespace {
+SfJob make_job(const uint8_t* sf, int64_t rows, int tile_rows, uint8_t* img) {
+  SfJob j;
+  j.sf = sf;
+  j.rows = rows;
+  j.tile_rows = tile_rows;
+  j.tiles = sf ? (rows + tile_rows - 1) / tile_rows : 0;
+  j.chunks = (tile_rows + 127) / 128;
+  j.img = reinterpret_cast<uint32_t*>(img);
+  return j;
+}
+}  // namespace
+
+cudaError_t launch_sf_prepare_pair(const uint8_t* sfa, int64_t rows_a, int tile_a, uint8_t* img_a,
+                                   const uint8_t* sfb, int64_t rows_b, int tile_b, uint8_t* img_b, int64_t K,
+                                   cudaStream_t stream) {
+  const int64_t kblocks = (K + 31) / 32;
+  const SfJob ja = make_job(sfa, rows_a, tile_a, img_a);
+  const SfJob jb = make_job(sfb, rows_b, tile_b, img_b);
+  const int64_t blocks = ja.tiles * ja.chunks + jb.tiles * jb.chunks;
+  if (blocks == 0 || kblocks == 0) return cudaSuccess;
+  if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
+  sf_prepare_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(ja, jb, kblocks);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_sf_prepare(const uint8_t* sf, int64_t rows, int64_t K, int tile_rows, uint8_t* img,
                               cudaStream_t stream) {
-  const int64_t kblocks = (K + 31) / 32;
-  const int64_t ksteps = (kblocks + 3) / 4;
-  const int64_t tiles = (rows + tile_rows - 1) / tile_rows;
-  const int chunks = (tile_rows + 127) / 128;
-  const int64_t total_words = ksteps * tiles * chunks * 128;
-  if (total_words == 0) return cudaSuccess;
-  int64_t blocks = (total_words + 255) / 256;
-  if (blocks > 65535 * 8) blocks = 65535 * 8;
-  sf_prepare_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(sf, rows, kblocks, tile_rows, tiles, chunks,
-                                                                        total_words, reinterpret_cast<uint32_t*>(img));
-  return cudaGetLastError();
+  return launch_sf_prepare_pair(sf, rows, tile_rows, img, nullptr, 0, 128, nullptr, K, stream);
 }
 
 }  // namespace tcg
