@@ -33,10 +33,14 @@ KernelInfo kinfo_mxf8(int cta_group) {
 // block scales; the scale warps write the same placement with tcgen05.st.
 // Absent rows / blocks get 127 (a scale of one).
 //
-// One block per 128-row chunk of one matrix (SFA and SFB in the same launch):
-// the chunk's rows are staged through shared memory SF_KB_CHUNK K blocks at a
-// time with row-contiguous reads, then each K step's 512-byte chunk is written
-// as 128 consecutive words.
+// One block per (128-row chunk of one matrix, SF_KS_CHUNK K steps); SFA and
+// SFB go in the same launch.  The four scale bytes of one row and K step are
+// contiguous in the plain layout, so each output word is one 32-bit word of
+// the input: the block reads its rows' words (consecutive threads, consecutive
+// words of a row) into shared memory and writes each K step's 512-byte chunk
+// as 128 consecutive words.  When the row stride is not a multiple of four
+// bytes (K not a multiple of 128) or the base is misaligned, the words are
+// assembled from bytes instead.
 struct SfJob {
   const uint8_t* sf;
   int64_t rows;
@@ -46,40 +50,47 @@ struct SfJob {
   uint32_t* img;
 };
 
-constexpr int SF_KB_CHUNK = 128;
+constexpr int SF_KS_CHUNK = 32;
 
-__global__ void __launch_bounds__(256) sf_prepare_kernel(SfJob ja, SfJob jb, int64_t kblocks) {
-  __shared__ uint8_t rows_s[128][SF_KB_CHUNK + 4];
-  int64_t blk = blockIdx.x;
+__global__ void __launch_bounds__(256) sf_prepare_kernel(SfJob ja, SfJob jb, int64_t kblocks, int64_t ksteps,
+                                                         int64_t kparts) {
+  __shared__ uint32_t words[128][SF_KS_CHUNK + 1];
+  int64_t blk = blockIdx.x / kparts;
+  const int64_t kp = blockIdx.x % kparts;
   const int64_t na = ja.tiles * ja.chunks;
   const SfJob j = blk < na ? ja : jb;
   if (blk >= na) blk -= na;
   const int64_t t = blk / j.chunks;
   const int c = static_cast<int>(blk % j.chunks);
   const int64_t row0 = t * j.tile_rows + 128 * c;
-  const int64_t in_tile = j.tile_rows - 128 * c;
-  const int64_t in_matrix = j.rows - row0;
-  const int valid = static_cast<int>(min(min(in_tile, in_matrix), static_cast<int64_t>(128)));
-  for (int64_t k0 = 0; k0 < kblocks; k0 += SF_KB_CHUNK) {
-    const int nk = static_cast<int>(min(static_cast<int64_t>(SF_KB_CHUNK), kblocks - k0));
-    __syncthreads();
-    for (int i = threadIdx.x; i < 128 * SF_KB_CHUNK; i += blockDim.x) {
-      const int rl = i / SF_KB_CHUNK, kk = i % SF_KB_CHUNK;
-      uint8_t v = 127;
-      if (rl < valid && kk < nk) v = j.sf[(row0 + rl) * kblocks + k0 + kk];
-      rows_s[rl][kk] = v;
+  const int valid = static_cast<int>(
+      max(static_cast<int64_t>(0), min(min(static_cast<int64_t>(j.tile_rows) - 128 * c, j.rows - row0),
+                                       static_cast<int64_t>(128))));
+  const int64_t ks0 = kp * SF_KS_CHUNK;
+  const int nks = static_cast<int>(min(static_cast<int64_t>(SF_KS_CHUNK), ksteps - ks0));
+  const bool word_loads = (kblocks % 4 == 0) && (reinterpret_cast<uintptr_t>(j.sf) % 4 == 0);
+  for (int i = threadIdx.x; i < 128 * SF_KS_CHUNK; i += blockDim.x) {
+    const int rl = i / SF_KS_CHUNK, kw = i % SF_KS_CHUNK;
+    uint32_t v = 0x7F7F7F7Fu;
+    if (rl < valid && kw < nks) {
+      const uint8_t* src = j.sf + (row0 + rl) * kblocks + 4 * (ks0 + kw);
+      if (word_loads) {
+        v = *reinterpret_cast<const uint32_t*>(src);
+      } else {
+        v = 0u;
+        for (int b = 0; b < 4; ++b) {
+          const uint32_t byte = 4 * (ks0 + kw) + b < kblocks ? static_cast<uint32_t>(src[b]) : 127u;
+          v |= byte << (8 * b);
+        }
+      }
     }
-    __syncthreads();
-    const int nks = (nk + 3) / 4;
-    for (int i = threadIdx.x; i < nks * 128; i += blockDim.x) {
-      const int ksl = i >> 7, w = i & 127;
-      const int rl = 32 * (w & 3) + (w >> 2);
-      const uint8_t* src = &rows_s[rl][4 * ksl];
-      const uint32_t v = static_cast<uint32_t>(src[0]) | (static_cast<uint32_t>(src[1]) << 8) |
-                         (static_cast<uint32_t>(src[2]) << 16) | (static_cast<uint32_t>(src[3]) << 24);
-      const int64_t ks = k0 / 4 + ksl;
-      j.img[((ks * j.tiles + t) * j.chunks + c) * 128 + w] = v;
-    }
+    words[rl][kw] = v;
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < nks * 128; i += blockDim.x) {
+    const int ksl = i >> 7, w = i & 127;
+    const int rl = 32 * (w & 3) + (w >> 2);
+    j.img[(((ks0 + ksl) * j.tiles + t) * j.chunks + c) * 128 + w] = words[rl][ksl];
   }
 }
 
@@ -100,12 +111,14 @@ cudaError_t launch_sf_prepare_pair(const uint8_t* sfa, int64_t rows_a, int tile_
                                    const uint8_t* sfb, int64_t rows_b, int tile_b, uint8_t* img_b, int64_t K,
                                    cudaStream_t stream) {
   const int64_t kblocks = (K + 31) / 32;
+  const int64_t ksteps = (kblocks + 3) / 4;
+  const int64_t kparts = (ksteps + SF_KS_CHUNK - 1) / SF_KS_CHUNK;
   const SfJob ja = make_job(sfa, rows_a, tile_a, img_a);
   const SfJob jb = make_job(sfb, rows_b, tile_b, img_b);
-  const int64_t blocks = ja.tiles * ja.chunks + jb.tiles * jb.chunks;
+  const int64_t blocks = (ja.tiles * ja.chunks + jb.tiles * jb.chunks) * kparts;
   if (blocks == 0 || kblocks == 0) return cudaSuccess;
   if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
-  sf_prepare_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(ja, jb, kblocks);
+  sf_prepare_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(ja, jb, kblocks, ksteps, kparts);
   return cudaGetLastError();
 }
 

@@ -49,8 +49,13 @@ def test_noalloc_matches_existing_entry_point_twice(tcg, oracle_mod):
 
 
 def test_noalloc_rejects_problems_beyond_its_array(tcg):
-    # 16384^3 needs about 17 MiB of scale images: rejected before anything is queued
-    rc = tcg.raw_call("tcg_gemm_mxf8_blockscaled_noalloc", 16384, 16384, 16384, 0x10000, 0, 0, 0x20000, 0, 0,
+    # 32768^3 needs far more than 16 MiB of scale images, whatever N tile is
+    # chosen; the call must be rejected before anything is queued (the
+    # pointers below are placeholders, so the precondition is checked first).
+    n = 32768
+    need = tcg.mxf8_scale_image_bytes(n, n, 128) + tcg.mxf8_scale_image_bytes(n, n, tcg.mxf8_tile_n(n, n, n))
+    assert need > 2 * (16 << 20)
+    rc = tcg.raw_call("tcg_gemm_mxf8_blockscaled_noalloc", n, n, n, 0x10000, 0, 0, 0x20000, 0, 0,
                       0x30000, 0x40000, 0x50000, 2, 0, 0, None)
     assert rc == tcg.ERR_UNSUPPORTED
     assert "16 MiB" in tcg.last_error_string()
