@@ -182,9 +182,8 @@ def run_workload(tcg, torch, w, steps, warmup, dist_ctx, measure_e2e=True):
     def step(ev_pair=None):
         n = 0
         if scaled:
-            tcg.mxf8_prepare_scales(SFA, M, K, 128, ia, stream=sp)
-            tcg.mxf8_prepare_scales(SFB, N, K, tn, ib, stream=sp)
-            n += 2
+            tcg.mxf8_prepare_scales_ab(SFA, M, ia, SFB, N, tn, ib, K, stream=sp)
+            n += 1
             if ev_pair:
                 ev_pair[0].record(stream)
             tcg.gemm(M, N, K, 3, A, a_maj, x["lda"], B, b_maj, x["ldb"], D, OUT[w.out], N, ACC[w.acc],

@@ -47,6 +47,7 @@ _SIGS = {
     "tcg_mxf8_scale_image_bytes": ([_i64, _i64, _i32], _i64),
     "tcg_mxf8_tile_n": ([_i64, _i64, _i64, _i32, _i32], _i32),
     "tcg_mxf8_prepare_scales": ([_vp, _i64, _i64, _i32, _vp, _vp], _i32),
+    "tcg_mxf8_prepare_scales_ab": ([_vp, _i64, _vp, _vp, _i64, _i32, _vp, _i64, _vp], _i32),
     "tcg_check": ([_vp], _i32),
     "tcg_set_wait_timeout_ns": ([_u64], None),
     "tcg_status_string": ([_i32], ctypes.c_char_p),
@@ -172,6 +173,11 @@ def mxf8_tile_n(M, N, K, b_major=K_MAJOR, cta_group=0) -> int:
 def mxf8_prepare_scales(sf, rows, K, tile_rows, img, stream=None):
     return _ok(_lib.tcg_mxf8_prepare_scales(_ptr(sf), rows, K, tile_rows, _ptr(img), _stream(stream)),
                "mxf8_prepare_scales")
+
+
+def mxf8_prepare_scales_ab(SFA, M, SFA_img, SFB, N, tile_n, SFB_img, K, stream=None):
+    return _ok(_lib.tcg_mxf8_prepare_scales_ab(_ptr(SFA), M, _ptr(SFA_img), _ptr(SFB), N, tile_n, _ptr(SFB_img), K,
+                                               _stream(stream)), "mxf8_prepare_scales_ab")
 
 
 def check(stream=None) -> int:

@@ -150,9 +150,9 @@ struct Plan {
 
 int pick_cta_group(const tcg_gemm_args& a) {
   if (a.cta_group == 1 || a.cta_group == 2) return a.cta_group;
-  // block-scaled: the single-CTA 128x256 tile measured faster than the pair
-  // tile (more MMA work per issued instruction, own issue thread per SM)
-  if (a.in_type == TCG_IN_E4M3) return 1;
+  // block-scaled pairs need K-major B (an MN-major 112-column half tile is
+  // not a whole 128-byte swizzle span of E4M3)
+  if (a.in_type == TCG_IN_E4M3 && a.b_major == TCG_MN_MAJOR) return 1;
   // pairs halve the B traffic per SM; use them once there are enough 256-row tiles
   return (a.M >= 1024 && a.N >= 1024) ? 2 : 1;
 }
@@ -316,7 +316,7 @@ int run_gemm(const tcg_gemm_args* args, cudaStream_t s) {
     return TCG_ERR_INVALID;
   if (a.acc_type == TCG_BF16) return TCG_ERR_UNSUPPORTED;
   if (a.acc_type == TCG_F16 && (a.in_type != TCG_IN_F16 || a.d_type != TCG_F16)) return TCG_ERR_UNSUPPORTED;
-  if (a.cta_group < 0 || a.cta_group > 2 || a.raster_group < 0 || a.sf_staging < 0 || a.sf_staging > 1)
+  if (a.cta_group < 0 || a.cta_group > 2 || a.raster_group < 0 || a.sf_staging < 0 || a.sf_staging > 3)
     return TCG_ERR_INVALID;
   if (a.M > INT32_MAX / 2 || a.N > INT32_MAX / 2 || a.K > INT32_MAX / 2) return TCG_ERR_UNSUPPORTED;
   if (a.M == 0 || a.N == 0) return TCG_OK;
@@ -392,7 +392,12 @@ int run_gemm(const tcg_gemm_args* args, cudaStream_t s) {
   prm.d_vec_ok = (reinterpret_cast<uintptr_t>(a.D) % 16 == 0) && ((a.ldd * ds) % 16 == 0);
   prm.err = d->err;
   prm.timeout_ns = g_timeout_ns.load();
-  prm.sf_via_cp = a.sf_staging == 1;
+  // auto: in a pair the warps' tcgen05.st is slow and the dedicated cp thread
+  // fastest; a single CTA is fastest with the scale warps
+  prm.sf_mode = a.sf_staging == 1   ? SF_BY_WARPS
+                : a.sf_staging == 2 ? SF_BY_MMA
+                : a.sf_staging == 3 ? SF_BY_CP
+                                    : (cg == 2 ? SF_BY_CP : SF_BY_WARPS);
 
   int launches = 0;
   if (scaled) {
@@ -566,6 +571,20 @@ int tcg_mxf8_prepare_scales(const uint8_t* sf, int64_t rows, int64_t K, int tile
   int dev;
   if (int rc = current_device_checked(&dev)) return rc;
   const cudaError_t e = launch_sf_prepare(sf, rows, K, tile_rows, img, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return record_cuda(e);
+  set_launch_count(1);
+  return TCG_OK;
+}
+
+int tcg_mxf8_prepare_scales_ab(const uint8_t* SFA, int64_t M, uint8_t* SFA_img, const uint8_t* SFB, int64_t N,
+                               int tile_n, uint8_t* SFB_img, int64_t K, void* stream) {
+  if (M < 0 || N < 0 || K < 0 || tile_n <= 0 || tile_n > 65536) return TCG_ERR_INVALID;
+  if (K == 0 || (M == 0 && N == 0)) return TCG_OK;
+  if ((M > 0 && (!SFA || !SFA_img)) || (N > 0 && (!SFB || !SFB_img))) return TCG_ERR_INVALID;
+  int dev;
+  if (int rc = current_device_checked(&dev)) return rc;
+  const cudaError_t e = launch_sf_prepare_pair(M > 0 ? SFA : nullptr, M, 128, SFA_img, N > 0 ? SFB : nullptr, N,
+                                               tile_n, SFB_img, K, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return record_cuda(e);
   set_launch_count(1);
   return TCG_OK;

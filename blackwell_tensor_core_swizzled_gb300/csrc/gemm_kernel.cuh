@@ -16,10 +16,10 @@
 //               arrive acc_empty[b];
 //   warps 8..11 (block scaling) scale staging: each writes its TMEM lane
 //               quadrant of the stage's scale slot with tcgen05.st and arrives
-//               sf_ready[slot].  Alternatively (GemmParams::sf_via_cp) the MMA
-//               thread stages the scales itself with tcgen05.cp .32x128b.warpx4;
-//               the warps are faster because every cp is an instruction in the
-//               MMA thread's in-order tensor pipe.
+//               sf_ready[slot].  Alternatively (GemmParams::sf_mode) the MMA
+//               thread stages the scales itself with tcgen05.cp .32x128b.warpx4
+//               (every cp then sits in its in-order tensor-pipe stream), or a
+//               dedicated thread (warp 3) does, committing to sf_ready[slot].
 // Accumulators are double buffered in TMEM so the epilogue of one tile
 // overlaps the main loop of the next.
 //
@@ -49,6 +49,7 @@ namespace tcg {
 
 enum Kind : int { KIND_F16 = 0, KIND_TF32 = 1, KIND_MXF8 = 2 };
 enum OutType : int { OUT_F32 = 0, OUT_F16 = 1, OUT_BF16 = 2 };
+enum SfMode : int { SF_BY_WARPS = 0, SF_BY_MMA = 1, SF_BY_CP = 2 };
 
 // Error word layout: bits [0,8) status (1 = wait timeout), [8,16) site,
 // [16,48) block index.
@@ -87,7 +88,15 @@ struct GemmParams {
   int d_vec_ok;
   unsigned long long* err;
   uint64_t timeout_ns;
-  int sf_via_cp;  // block scaling: 1 = MMA thread stages scales with tcgen05.cp, 0 = scale warps with tcgen05.st
+  // block scaling, where the scales are staged into TMEM:
+  //   SF_BY_WARPS  the four scale warps, tcgen05.st (scales complete on each
+  //                CTA's own sf_loaded[s]);
+  //   SF_BY_MMA    the MMA thread, tcgen05.cp before its MMAs;
+  //   SF_BY_CP     a dedicated thread (warp 3), tcgen05.cp + commit to
+  //                sf_ready[slot].
+  // With tcgen05.cp (a pair copies both CTAs' smem) the scale images complete
+  // on the pair leader's full[s] barrier together with A and B.
+  int sf_mode;
 };
 
 template <int CG, int BN, int ACC, int STAGES, int KIND>
@@ -286,7 +295,8 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
     mbar_init(drain_bar, 1);
     if constexpr (KIND == KIND_MXF8) {
       for (int s = 0; s < STAGES; ++s) mbar_init(sfl_bar(s), 1);
-      for (int k = 0; k < C::SF_SLOTS; ++k) mbar_init(sfr_bar(k), 4 * CG);
+      // sf_ready: one arrival per scale warp of each CTA, or one commit
+      for (int k = 0; k < C::SF_SLOTS; ++k) mbar_init(sfr_bar(k), p.sf_mode == SF_BY_WARPS ? 4 * CG : 1);
     }
     *abort_flag = 0u;
     fence_mbarrier_init();
@@ -326,7 +336,8 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
             break;
           }
           const uint32_t fb = (CG == 2) ? mapa_shared(full_bar(s), 0) : full_bar(s);
-          if (rank == 0) mbar_arrive_expect_tx(full_bar(s), C::TX_BYTES);
+          const bool sf_on_full = KIND == KIND_MXF8 && p.sf_mode != SF_BY_WARPS;
+          if (rank == 0) mbar_arrive_expect_tx(full_bar(s), C::TX_BYTES + (sf_on_full ? C::SF_TX_BYTES * CG : 0));
           const uint32_t sa = sbase + s * C::STAGE_BYTES;
           const uint32_t sb = sa + C::A_BYTES;
           const int k0 = kb * C::BK;
@@ -346,11 +357,17 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
             // a pair tile's second half may lie wholly beyond M: its A rows are
             // zero-filled, so any valid scale row will do
             const int sfa_tile = min(mt * CG + static_cast<int>(rank), p.sf_a_tiles - 1);
-            // the scale warps of this CTA consume these: they complete on
-            // this CTA's own sf_loaded[s]
-            mbar_arrive_expect_tx(sfl_bar(s), C::SF_TX_BYTES);
-            tma_load_2d(ssfa, &p.tmap_sfa, 0, kb * p.sf_a_tiles + sfa_tile, sfl_bar(s));
-            tma_load_2d(ssfb, &p.tmap_sfb, 0, kb * p.num_n_tiles + nt, sfl_bar(s));
+            if (sf_on_full) {
+              // a tcgen05.cp of a pair reads both CTAs' smem: complete with A, B
+              tma_load<CG>(ssfa, &p.tmap_sfa, 0, kb * p.sf_a_tiles + sfa_tile, fb);
+              tma_load<CG>(ssfb, &p.tmap_sfb, 0, kb * p.num_n_tiles + nt, fb);
+            } else {
+              // the scale warps of this CTA consume these: they complete on
+              // this CTA's own sf_loaded[s]
+              mbar_arrive_expect_tx(sfl_bar(s), C::SF_TX_BYTES);
+              tma_load_2d(ssfa, &p.tmap_sfa, 0, kb * p.sf_a_tiles + sfa_tile, sfl_bar(s));
+              tma_load_2d(ssfb, &p.tmap_sfb, 0, kb * p.num_n_tiles + nt, sfl_bar(s));
+            }
           }
           ++it;
           if (++s == STAGES) {
@@ -362,7 +379,7 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
       if (!ok) {
         // Drain: let the copies this CTA issued land before the CTA can exit.
         const uint32_t n_out = it < static_cast<uint32_t>(STAGES) ? it : static_cast<uint32_t>(STAGES);
-        if constexpr (KIND == KIND_MXF8) {
+        if (KIND == KIND_MXF8 && p.sf_mode == SF_BY_WARPS) {
           for (uint32_t j = it - n_out; j < it; ++j) {
             const uint64_t t0 = globaltimer();
             while (!mbar_try_wait(sfl_bar(j % STAGES), (j / STAGES) & 1u) && globaltimer() - t0 < 20000000ull) {
@@ -411,14 +428,10 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
             // this iteration's scales go to TMEM slot it % SF_SLOTS
             const uint32_t slot = it % C::SF_SLOTS;
             const uint32_t sf_col = tmem_base + C::SF_COL0 + slot * C::SF_SLOT_COLS;
-            if (p.sf_via_cp) {
-              // this thread stages the scales with tcgen05.cp: wait until
-              // they are in smem and the slot's previous readers (the MMAs of
-              // iteration it - SF_SLOTS) have completed
-              if (!thread_wait(sfl_bar(s), ph, wctx, SITE_MMA_FULL)) {
-                ok = false;
-                break;
-              }
+            if (p.sf_mode == SF_BY_MMA) {
+              // this thread stages the scales with tcgen05.cp; they arrived
+              // with full[s].  Wait until the slot's previous readers (the
+              // MMAs of iteration it - SF_SLOTS) have completed.
               if (it >= static_cast<uint32_t>(C::SF_SLOTS)) {
                 const uint32_t j = it - C::SF_SLOTS;
                 if (!thread_wait(empty_bar(j % STAGES), (j / STAGES) & 1u, wctx, SITE_MMA_FULL)) {
@@ -434,8 +447,8 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
               for (int c = 0; c < C::SFB_CHUNKS; ++c)
                 tc_cp_32x128b_warpx4<CG>(sf_col + 4 + 4 * c, sdesc(ssfa + C::SFA_BYTES + 512 * c, cp_hi));
             } else {
-              // the scale warps of both CTAs have written this iteration's
-              // scales into the slot with tcgen05.st
+              // the scale warps of both CTAs (tcgen05.st) or the cp thread
+              // (tcgen05.cp + commit) have filled this iteration's slot
               if (!thread_wait(sfr_bar(slot), (it / C::SF_SLOTS) & 1u, wctx, SITE_MMA_FULL)) {
                 ok = false;
                 break;
@@ -476,6 +489,50 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
         }
       }
     }
+  } else if (KIND == KIND_MXF8 && warp == 3) {
+    // ------------------------------------------------------------ cp thread
+    // SF_BY_CP: one thread of the pair leader copies each stage's scales into
+    // its TMEM slot with tcgen05.cp .32x128b.warpx4 (both CTAs of a pair) and
+    // commits to sf_ready[slot]; the MMA thread's tensor-pipe stream then
+    // holds only MMAs.
+    if constexpr (KIND == KIND_MXF8) {
+      if (p.sf_mode == SF_BY_CP && lane == 0 && (CG == 1 || rank == 0)) {
+        const uint32_t my_tiles =
+            cluster_id < p.num_tiles ? (p.num_tiles - cluster_id + num_clusters - 1) / num_clusters : 0;
+        const uint32_t total_it = my_tiles * static_cast<uint32_t>(p.num_k_blocks);
+        const uint64_t cp_hi = sdesc_hi(16, 128, SW_NONE);  // 32 rows x 16 B, rows 16 B apart
+        uint32_t s = 0, ph = 0, issued = 0;
+        for (uint32_t it = 0; it < total_it; ++it) {
+          if (!thread_wait(full_bar(s), ph, wctx, SITE_MMA_FULL)) break;
+          if (it >= static_cast<uint32_t>(C::SF_SLOTS)) {
+            const uint32_t j = it - C::SF_SLOTS;  // the slot's previous readers
+            if (!thread_wait(empty_bar(j % STAGES), (j / STAGES) & 1u, wctx, SITE_MMA_FULL)) break;
+          }
+          tc_fence_after();
+          const uint32_t ssfa = sbase + s * C::STAGE_BYTES + C::A_BYTES + C::B_BYTES;
+          const uint32_t col = tmem_base + C::SF_COL0 + (it % C::SF_SLOTS) * C::SF_SLOT_COLS;
+          tc_cp_32x128b_warpx4<CG>(col, sdesc(ssfa, cp_hi));
+#pragma unroll
+          for (int c = 0; c < C::SFB_CHUNKS; ++c)
+            tc_cp_32x128b_warpx4<CG>(col + 4 + 4 * c, sdesc(ssfa + C::SFA_BYTES + 512 * c, cp_hi));
+          tc_commit<CG>(sfr_bar(it % C::SF_SLOTS));
+          issued = it + 1;
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+        if (issued > 0) {
+          // let the copies land before the CTA can exit: the last commit
+          // tracks every copy this thread issued
+          const uint32_t j = issued - 1;
+          const uint64_t t0 = globaltimer();
+          while (!mbar_try_wait(sfr_bar(j % C::SF_SLOTS), (j / C::SF_SLOTS) & 1u) &&
+                 globaltimer() - t0 < 20000000ull) {
+          }
+        }
+      }
+    }
   } else if (KIND == KIND_MXF8 && warp >= 8) {
     // ------------------------------------------------------------ scale warps
     // Warp 8+q writes TMEM lane quadrant q of every scale slot: source row l
@@ -483,7 +540,7 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
     // columns, which is the placement one tcgen05.cp .32x128b.warpx4 of the
     // chunk produces (each quadrant is one of its replicas).
     if constexpr (KIND == KIND_MXF8) {
-      if (!p.sf_via_cp) {
+      if (p.sf_mode == SF_BY_WARPS) {
         const int q = warp & 3;
         const uint32_t my_tiles =
             cluster_id < p.num_tiles ? (p.num_tiles - cluster_id + num_clusters - 1) / num_clusters : 0;

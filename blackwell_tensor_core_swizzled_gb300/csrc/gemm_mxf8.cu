@@ -33,14 +33,13 @@ KernelInfo kinfo_mxf8(int cta_group) {
 // block scales; the scale warps write the same placement with tcgen05.st.
 // Absent rows / blocks get 127 (a scale of one).
 //
-// One block per (128-row chunk of one matrix, SF_KS_CHUNK K steps); SFA and
+// One warp per (128-row chunk of one matrix, group of four K steps); SFA and
 // SFB go in the same launch.  The four scale bytes of one row and K step are
-// contiguous in the plain layout, so each output word is one 32-bit word of
-// the input: the block reads its rows' words (consecutive threads, consecutive
-// words of a row) into shared memory and writes each K step's 512-byte chunk
-// as 128 consecutive words.  When the row stride is not a multiple of four
-// bytes (K not a multiple of 128) or the base is misaligned, the words are
-// assembled from bytes instead.
+// one 32-bit word of the plain layout, and output words 4i..4i+3 of a chunk
+// are rows i, 32+i, 64+i, 96+i of the same K step, so lane i reads 16 bytes
+// (four K steps) of each of its four rows and writes one 16-byte quad per K
+// step: every warp store is 512 contiguous bytes.  Narrower loads and stores
+// serve row strides or bases that are not 16-byte multiples.
 struct SfJob {
   const uint8_t* sf;
   int64_t rows;
@@ -50,14 +49,16 @@ struct SfJob {
   uint32_t* img;
 };
 
-constexpr int SF_KS_CHUNK = 32;
+constexpr int SF_WARPS = 8;  // warps per block
 
-__global__ void __launch_bounds__(256) sf_prepare_kernel(SfJob ja, SfJob jb, int64_t kblocks, int64_t ksteps,
-                                                         int64_t kparts) {
-  __shared__ uint32_t words[128][SF_KS_CHUNK + 1];
-  int64_t blk = blockIdx.x / kparts;
-  const int64_t kp = blockIdx.x % kparts;
+__global__ void __launch_bounds__(32 * SF_WARPS) sf_prepare_kernel(SfJob ja, SfJob jb, int64_t kblocks,
+                                                                   int64_t ksteps, int64_t kgroups) {
+  const int64_t gw = static_cast<int64_t>(blockIdx.x) * SF_WARPS + (threadIdx.x >> 5);
+  const int i = threadIdx.x & 31;
+  int64_t blk = gw / kgroups;
+  const int64_t kg = gw % kgroups;
   const int64_t na = ja.tiles * ja.chunks;
+  if (blk >= na + jb.tiles * jb.chunks) return;
   const SfJob j = blk < na ? ja : jb;
   if (blk >= na) blk -= na;
   const int64_t t = blk / j.chunks;
@@ -66,31 +67,55 @@ __global__ void __launch_bounds__(256) sf_prepare_kernel(SfJob ja, SfJob jb, int
   const int valid = static_cast<int>(
       max(static_cast<int64_t>(0), min(min(static_cast<int64_t>(j.tile_rows) - 128 * c, j.rows - row0),
                                        static_cast<int64_t>(128))));
-  const int64_t ks0 = kp * SF_KS_CHUNK;
-  const int nks = static_cast<int>(min(static_cast<int64_t>(SF_KS_CHUNK), ksteps - ks0));
-  const bool word_loads = (kblocks % 4 == 0) && (reinterpret_cast<uintptr_t>(j.sf) % 4 == 0);
-  for (int i = threadIdx.x; i < 128 * SF_KS_CHUNK; i += blockDim.x) {
-    const int rl = i / SF_KS_CHUNK, kw = i % SF_KS_CHUNK;
-    uint32_t v = 0x7F7F7F7Fu;
-    if (rl < valid && kw < nks) {
-      const uint8_t* src = j.sf + (row0 + rl) * kblocks + 4 * (ks0 + kw);
-      if (word_loads) {
-        v = *reinterpret_cast<const uint32_t*>(src);
-      } else {
-        v = 0u;
-        for (int b = 0; b < 4; ++b) {
-          const uint32_t byte = 4 * (ks0 + kw) + b < kblocks ? static_cast<uint32_t>(src[b]) : 127u;
-          v |= byte << (8 * b);
+  const int64_t ks0 = 4 * kg;
+  const int nks = static_cast<int>(min(static_cast<int64_t>(4), ksteps - ks0));
+  const uintptr_t base = reinterpret_cast<uintptr_t>(j.sf);
+  const bool quad_loads = nks == 4 && kblocks % 16 == 0 && base % 16 == 0;
+  const bool word_loads = kblocks % 4 == 0 && base % 4 == 0;
+  uint32_t v[4][4];  // [row group g][K step]
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    const int rl = 32 * g + i;
+    const uint8_t* src = j.sf + (row0 + rl) * kblocks + 4 * ks0;
+    if (rl >= valid) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) v[g][k] = 0x7F7F7F7Fu;
+    } else if (quad_loads) {
+      const uint4 q = *reinterpret_cast<const uint4*>(src);
+      v[g][0] = q.x;
+      v[g][1] = q.y;
+      v[g][2] = q.z;
+      v[g][3] = q.w;
+    } else {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        if (k >= nks) {
+          v[g][k] = 0x7F7F7F7Fu;
+        } else if (word_loads) {
+          v[g][k] = reinterpret_cast<const uint32_t*>(src)[k];
+        } else {
+          uint32_t w = 0u;
+          for (int b = 0; b < 4; ++b) {
+            const int64_t kb = 4 * (ks0 + k) + b;
+            w |= (kb < kblocks ? static_cast<uint32_t>(src[4 * k + b]) : 127u) << (8 * b);
+          }
+          v[g][k] = w;
         }
       }
     }
-    words[rl][kw] = v;
   }
-  __syncthreads();
-  for (int i = threadIdx.x; i < nks * 128; i += blockDim.x) {
-    const int ksl = i >> 7, w = i & 127;
-    const int rl = 32 * (w & 3) + (w >> 2);
-    j.img[(((ks0 + ksl) * j.tiles + t) * j.chunks + c) * 128 + w] = words[rl][ksl];
+  const bool quad_stores = reinterpret_cast<uintptr_t>(j.img) % 16 == 0;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    if (k < nks) {
+      uint32_t* dst = j.img + (((ks0 + k) * j.tiles + t) * j.chunks + c) * 128 + 4 * i;
+      if (quad_stores) {
+        *reinterpret_cast<uint4*>(dst) = make_uint4(v[0][k], v[1][k], v[2][k], v[3][k]);
+      } else {
+#pragma unroll
+        for (int g = 0; g < 4; ++g) dst[g] = v[g][k];
+      }
+    }
   }
 }
 
@@ -112,13 +137,14 @@ cudaError_t launch_sf_prepare_pair(const uint8_t* sfa, int64_t rows_a, int tile_
                                    cudaStream_t stream) {
   const int64_t kblocks = (K + 31) / 32;
   const int64_t ksteps = (kblocks + 3) / 4;
-  const int64_t kparts = (ksteps + SF_KS_CHUNK - 1) / SF_KS_CHUNK;
+  const int64_t kgroups = (ksteps + 3) / 4;
   const SfJob ja = make_job(sfa, rows_a, tile_a, img_a);
   const SfJob jb = make_job(sfb, rows_b, tile_b, img_b);
-  const int64_t blocks = (ja.tiles * ja.chunks + jb.tiles * jb.chunks) * kparts;
-  if (blocks == 0 || kblocks == 0) return cudaSuccess;
+  const int64_t warps = (ja.tiles * ja.chunks + jb.tiles * jb.chunks) * kgroups;
+  if (warps == 0 || kblocks == 0) return cudaSuccess;
+  const int64_t blocks = (warps + SF_WARPS - 1) / SF_WARPS;
   if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
-  sf_prepare_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(ja, jb, kblocks, ksteps, kparts);
+  sf_prepare_kernel<<<static_cast<unsigned>(blocks), 32 * SF_WARPS, 0, stream>>>(ja, jb, kblocks, ksteps, kgroups);
   return cudaGetLastError();
 }
 

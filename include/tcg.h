@@ -150,9 +150,12 @@ typedef struct {
   tcg_dtype acc_type;
   int cta_group;     /* 0 auto, 1 (one CTA per 128xN tile), 2 (CTA pair, 256xN) */
   int raster_group;  /* 0 auto; tiles are visited in groups of this many M tiles */
-  int sf_staging;    /* block scaling: 0 = scale warps write TMEM with tcgen05.st
-                        (default, faster), 1 = the MMA thread copies with
-                        tcgen05.cp .32x128b.warpx4 ("tcgen05.cp" page) */
+  int sf_staging;    /* block scaling, who stages the scales into TMEM:
+                        0 = auto (3 for CTA pairs, 1 for single CTAs),
+                        1 = four scale warps per CTA with tcgen05.st,
+                        2 = the MMA thread with tcgen05.cp .32x128b.warpx4
+                            ("tcgen05.cp" page) before its MMAs,
+                        3 = a dedicated thread with tcgen05.cp + commit */
 } tcg_gemm_args;
 
 int tcg_gemm(const tcg_gemm_args* args, void* stream);
@@ -181,6 +184,14 @@ int tcg_mxf8_tile_n(int64_t M, int64_t N, int64_t K, tcg_major b_major, int cta_
  * (device, tcg_mxf8_scale_image_bytes bytes). */
 int tcg_mxf8_prepare_scales(const uint8_t* sf, int64_t rows, int64_t K, int tile_rows,
                             uint8_t* img, void* stream);
+
+/* Both images of one GEMM in a single launch: SFA [M][ceil(K/32)] -> SFA_img
+ * with 128-row tiles, SFB [N][ceil(K/32)] -> SFB_img with tile_n-row tiles
+ * (tcg_mxf8_tile_n).  The same result as two tcg_mxf8_prepare_scales calls;
+ * M == 0 or N == 0 skips that matrix (its pointers may then be NULL). */
+int tcg_mxf8_prepare_scales_ab(const uint8_t* SFA, int64_t M, uint8_t* SFA_img,
+                               const uint8_t* SFB, int64_t N, int tile_n, uint8_t* SFB_img,
+                               int64_t K, void* stream);
 
 /* ---------------------------------------------------------------------------
  * Status and configuration.

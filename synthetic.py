@@ -59,7 +59,7 @@ WORKLOADS = {
     "f16acc_8192_cta2": Workload("f16acc_8192_cta2", 8192, 8192, 8192, "f16", "k", "k",
                                  "normal", "f16", "f16", 2, False, 4),
     "mxf8_8192": Workload("mxf8_8192", 8192, 8192, 8192, "e4m3", "k", "k",
-                          "normal1", "f32", "bf16", 1, True, 5),
+                          "normal1", "f32", "bf16", 2, True, 5),
 }
 
 

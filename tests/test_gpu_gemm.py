@@ -104,7 +104,7 @@ def test_blockscaled_identity_pins_scale_placement(tcg):
     expo = SFA[m, m // 32].astype(np.int64)[:, None] + SFB[:, m // 32].T.astype(np.int64) - 254
     ref = np.ldexp(bdec, expo)
     for cg in (1, 2):
-        for staging in (0, 1):  # scale warps with tcgen05.st / MMA thread with tcgen05.cp
+        for staging in (1, 2, 3):  # tcgen05.st by scale warps / tcgen05.cp by the MMA thread / by a cp thread
             D = torch.zeros((n, N), dtype=torch.float32, device="cuda")
             tcg.gemm(n, N, n, 3, to_device(A), 0, n, to_device(B), 0, n, D, 0, N, 0, SFA=to_device(SFA),
                      SFB=to_device(SFB), cta_group=cg, sf_staging=staging)
@@ -112,25 +112,62 @@ def test_blockscaled_identity_pins_scale_placement(tcg):
             assert np.array_equal(D.double().cpu().numpy(), ref), f"cta_group {cg} staging {staging}"
 
 
+@pytest.mark.parametrize("staging", [1, 2, 3])
 @pytest.mark.parametrize("am,bm,M,N,K,cg", [("k", "k", 300, 520, 256, 2), ("k", "k", 520, 300, 208, 1),
-                                            ("mn", "mn", 200, 300, 256, 1), ("mn", "k", 260, 460, 640, 2)])
-def test_blockscaled_tcgen05_cp_staging(tcg, oracle_mod, am, bm, M, N, K, cg):
-    # the alternative scale path: tcgen05.cp .32x128b.warpx4 issued by the MMA thread
+                                            ("mn", "mn", 200, 300, 256, 1), ("mn", "k", 260, 460, 640, 2),
+                                            ("k", "k", 1100, 1300, 1024, 2)])
+def test_blockscaled_scale_staging_modes(tcg, oracle_mod, am, bm, M, N, K, cg, staging):
+    # every explicit scale path: tcgen05.st by the scale warps (1), and
+    # tcgen05.cp .32x128b.warpx4 issued by the MMA thread (2) or by a
+    # dedicated thread that commits to a per-slot barrier (3); the larger
+    # case runs many k-blocks per tile through every scale slot
     x = make_case("e4m3", am, bm, M, N, K, seed=M + 3 * N + K)
-    _check_full(tcg, oracle_mod, x, "f32", "f32", cg, sf_staging=1)
+    _check_full(tcg, oracle_mod, x, "f32", "f32", cg, sf_staging=staging)
 
 
-def test_scale_prepare_kernel_matches_oracle_image(tcg):
+# rows, K, tile rows, byte offset of the plain scales, byte offset of the image.
+# K = 200 / 1000 (kblocks 7 / 32): byte loads / word loads (the row stride is
+# not a multiple of 16 bytes); K = 1024, 8192: 16-byte loads; offset scales:
+# byte loads; offset image: word stores; K = 1664: a partial group of K steps.
+PREPARE_CASES = [(300, 200, 128, 0, 0), (8192, 8192, 224, 0, 0), (500, 1024, 256, 0, 0),
+                 (260, 1000, 224, 0, 0), (129, 1024, 128, 1, 0), (200, 1024, 224, 0, 4),
+                 (384, 1664, 128, 0, 0), (1, 32, 224, 0, 0)]
+
+
+def _plain_and_image(tcg, rows, K, tile, off, ioff, seed):
+    kb = -(-K // 32)
+    sf = np.random.default_rng(seed).integers(0, 255, size=(rows, kb)).astype(np.uint8)
+    sf_dev = torch.zeros(rows * kb + 16, dtype=torch.uint8, device="cuda")
+    sf_dev[off:off + rows * kb] = to_device(sf.reshape(-1))
+    nbytes = tcg.mxf8_scale_image_bytes(rows, K, tile)
+    img = torch.full((nbytes + 16,), 0xAB, dtype=torch.uint8, device="cuda")
+    return sf, sf_dev[off:], img, img[ioff:ioff + nbytes]
+
+
+@pytest.mark.parametrize("rows,K,tile,off,ioff", PREPARE_CASES)
+def test_scale_prepare_kernel_matches_oracle_image(tcg, rows, K, tile, off, ioff):
     from oracle import layouts as L
-    for rows, K, tile in [(300, 200, 128), (8192, 8192, 224), (500, 1024, 256)]:
-        kb = -(-K // 32)
-        sf = np.random.default_rng(rows).integers(0, 255, size=(rows, kb)).astype(np.uint8)
-        nbytes = tcg.mxf8_scale_image_bytes(rows, K, tile)
-        img = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
-        tcg.mxf8_prepare_scales(to_device(sf), rows, K, tile, img)
-        assert tcg.check() == 0
-        exp = L.sf_prepare(sf, rows, kb, tile).reshape(-1)
-        assert np.array_equal(img.cpu().numpy(), exp), (rows, K, tile)
+    sf, sf_dev, img_all, img = _plain_and_image(tcg, rows, K, tile, off, ioff, rows + K)
+    tcg.mxf8_prepare_scales(sf_dev, rows, K, tile, img)
+    assert tcg.check() == 0
+    exp = L.sf_prepare(sf, rows, -(-K // 32), tile).reshape(-1)
+    assert np.array_equal(img.cpu().numpy(), exp), (rows, K, tile)
+    rest = torch.cat([img_all[:ioff], img_all[ioff + exp.size:]]).cpu().numpy()
+    assert (rest == 0xAB).all(), "wrote outside the image"
+
+
+@pytest.mark.parametrize("M,N,K,tn", [(8192, 8192, 8192, 224), (300, 520, 200, 256), (0, 300, 256, 224)])
+def test_scale_prepare_ab_matches_two_calls(tcg, M, N, K, tn):
+    from oracle import layouts as L
+    kb = -(-K // 32)
+    sfa, sfa_dev, _, ia = _plain_and_image(tcg, M, K, 128, 0, 0, 7 + M)
+    sfb, sfb_dev, _, ib = _plain_and_image(tcg, N, K, tn, 0, 0, 8 + N)
+    tcg.mxf8_prepare_scales_ab(sfa_dev if M else None, M, ia if M else None, sfb_dev, N, tn, ib, K)
+    assert tcg.check() == 0
+    assert tcg.last_launch_count() == 1
+    if M:
+        assert np.array_equal(ia.cpu().numpy(), L.sf_prepare(sfa, M, kb, 128).reshape(-1))
+    assert np.array_equal(ib.cpu().numpy(), L.sf_prepare(sfb, N, kb, tn).reshape(-1))
 
 
 def test_prepared_scale_images_path(tcg, oracle_mod):
