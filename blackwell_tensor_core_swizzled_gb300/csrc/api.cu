@@ -150,16 +150,12 @@ struct Plan {
 
 int pick_cta_group(const tcg_gemm_args& a) {
   if (a.cta_group == 1 || a.cta_group == 2) return a.cta_group;
-  // block-scaled pairs need K-major B (an MN-major 112-column half tile is
-  // not a whole 128-byte swizzle span of E4M3)
-  if (a.in_type == TCG_IN_E4M3 && a.b_major == TCG_MN_MAJOR) return 1;
   // pairs halve the B traffic per SM; use them once there are enough 256-row tiles
   return (a.M >= 1024 && a.N >= 1024) ? 2 : 1;
 }
 
 int get_plan(const tcg_gemm_args& a, Plan* plan) {
   const int cg = pick_cta_group(a);
-  if (a.in_type == TCG_IN_E4M3 && cg == 2 && a.b_major == TCG_MN_MAJOR) return TCG_ERR_UNSUPPORTED;
   plan->cta_group = cg;
   switch (a.in_type) {
     case TCG_IN_F16:
@@ -168,6 +164,8 @@ int get_plan(const tcg_gemm_args& a, Plan* plan) {
     case TCG_IN_E4M3: plan->ki = kinfo_mxf8(cg); break;
     default: return TCG_ERR_INVALID;
   }
+  // an MN-major B half tile must be whole 128-byte swizzle spans
+  if (a.b_major == TCG_MN_MAJOR && (plan->ki.bn / cg) % (128 / esize_of(a.in_type)) != 0) return TCG_ERR_UNSUPPORTED;
   return TCG_OK;
 }
 
@@ -390,6 +388,16 @@ int run_gemm(const tcg_gemm_args* args, cudaStream_t s) {
   prm.d_type = a.d_type == TCG_F32 ? OUT_F32 : a.d_type == TCG_F16 ? OUT_F16 : OUT_BF16;
   prm.acc_f16 = a.acc_type == TCG_F16;
   prm.d_vec_ok = (reinterpret_cast<uintptr_t>(a.D) % 16 == 0) && ((a.ldd * ds) % 16 == 0);
+  // 16-bit outputs leave through TMA tile stores when the map's alignment
+  // rules hold (16-byte base and row stride); otherwise per-thread row stores
+  prm.d_tma = 0;
+  if (a.d_type != TCG_F32 && prm.d_vec_ok) {
+    const CUtensorMapDataType dt = a.d_type == TCG_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    if (int rc = make_map_2d(&prm.tmap_d, a.D, dt, 2, static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.M),
+                             static_cast<uint64_t>(a.ldd), 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+      return rc;
+    prm.d_tma = 1;
+  }
   prm.err = d->err;
   prm.timeout_ns = g_timeout_ns.load();
   // auto: in a pair the warps' tcgen05.st is slow and the dedicated cp thread

@@ -19,9 +19,14 @@
 //               sf_ready[slot].  Alternatively (GemmParams::sf_mode) the MMA
 //               thread stages the scales itself with tcgen05.cp .32x128b.warpx4
 //               (every cp then sits in its in-order tensor-pipe stream), or a
-//               dedicated thread (warp 3) does, committing to sf_ready[slot].
-// Accumulators are double buffered in TMEM so the epilogue of one tile
-// overlaps the main loop of the next.
+//               dedicated thread (warp 3) does, committing to sf_ready[slot];
+//               warps 8..11 then join the epilogue (each of the two warps of a
+//               lane quadrant drains every other 32-column chunk).
+// With two accumulators the epilogue of one tile overlaps the main loop of the
+// next.  With one (a 256-column block-scaled tile leaves no TMEM for a second)
+// an eight-warp epilogue with 16-bit output reads the whole accumulator into
+// registers, releases it, and only then converts and stores, so the next
+// tile's MMAs wait for the TMEM reads alone.
 //
 // The MMA issue follows the "tcgen05.mma" page: one elected thread issues the
 // K repeats as separate instructions with accumulation disabled only on the
@@ -67,6 +72,7 @@ struct GemmParams {
   CUtensorMap tmap_b;
   CUtensorMap tmap_sfa;
   CUtensorMap tmap_sfb;
+  CUtensorMap tmap_d;  // 16-bit D in 32 x 32 boxes, 64-byte swizzle (used when d_tma)
   int M, N, K;
   int num_m_tiles;   // tiles of 128*CG rows
   int num_n_tiles;   // tiles of BN columns
@@ -86,6 +92,7 @@ struct GemmParams {
   int d_type;
   int acc_f16;
   int d_vec_ok;
+  int d_tma;  // 16-bit output stored by TMA from a per-warp shared staging tile
   unsigned long long* err;
   uint64_t timeout_ns;
   // block scaling, where the scales are staged into TMEM:
@@ -124,9 +131,19 @@ struct GemmCfg {
   static constexpr int SF_SLOT_COLS = 16;      // SFA 4 columns + SFB 4 per 128 rows
   // Scale slots rotate over the free TMEM columns; before a slot is
   // rewritten the MMA thread waits for the stage that last used it to retire.
+  // With as many slots as ring stages the wait is implied: full[s] of
+  // iteration it completes only after the producer saw empty[s] of it - STAGES,
+  // i.e. after the MMAs that last read slot it % STAGES retired.
   static constexpr int SF_SLOTS_FREE = (TMEM_COLS - ACC * BN) / SF_SLOT_COLS;
-  static constexpr int SF_SLOTS = SF_SLOTS_FREE < 4 ? SF_SLOTS_FREE : 4;
-  static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
+  static constexpr int SF_SLOTS = SF_SLOTS_FREE < STAGES ? SF_SLOTS_FREE : STAGES;
+  static constexpr bool SF_SLOT_WAIT = SF_SLOTS < STAGES;
+  // epilogue staging for TMA stores: per epilogue warp EPI_BUFS tiles of
+  // 32 rows x 64 bytes (32 16-bit columns), 64-byte swizzled
+  static constexpr int EPI_WARPS_MAX = KIND == KIND_MXF8 ? 8 : 4;
+  static constexpr int EPI_BUFS = KIND == KIND_MXF8 ? 1 : 2;
+  static constexpr int EPI_TILE_BYTES = 32 * 64;
+  static constexpr int EPI_OFF = STAGES * STAGE_BYTES;
+  static constexpr int BAR_OFF = EPI_OFF + EPI_WARPS_MAX * EPI_BUFS * EPI_TILE_BYTES;
   // full[S], empty[S], acc_full[ACC], acc_empty[ACC], drain, and for block
   // scaling sf_loaded[S] (scale bytes in smem) and sf_ready[SF_SLOTS] (scales
   // written to TMEM by the scale warps)
@@ -135,6 +152,10 @@ struct GemmCfg {
   // warps 0..7 as described above; block scaling adds warps 8..11, one per
   // TMEM lane quadrant, which stage the scale factors into TMEM
   static constexpr int THREADS = KIND == KIND_MXF8 ? 384 : 256;
+  // epilogue warps: 4..7, plus 8..11 when block scales are staged by tcgen05.cp
+  __host__ __device__ static constexpr int epi_warps(int sf_mode) {
+    return KIND == KIND_MXF8 && sf_mode != SF_BY_WARPS ? 8 : 4;
+  }
   static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "epilogue drains 32-column chunks");
   static_assert(BN % (16 * CG) == 0, "MMA N constraint / per-CTA B split");
   static_assert(ACC * BN + (KIND == KIND_MXF8 ? SF_SLOTS * SF_SLOT_COLS : 0) <= TMEM_COLS, "TMEM budget");
@@ -290,7 +311,7 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
     }
     for (int b = 0; b < ACC; ++b) {
       mbar_init(accf_bar(b), 1);
-      mbar_init(acce_bar(b), 4 * CG);
+      mbar_init(acce_bar(b), C::epi_warps(p.sf_mode) * CG);
     }
     mbar_init(drain_bar, 1);
     if constexpr (KIND == KIND_MXF8) {
@@ -432,7 +453,7 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
               // this thread stages the scales with tcgen05.cp; they arrived
               // with full[s].  Wait until the slot's previous readers (the
               // MMAs of iteration it - SF_SLOTS) have completed.
-              if (it >= static_cast<uint32_t>(C::SF_SLOTS)) {
+              if (C::SF_SLOT_WAIT && it >= static_cast<uint32_t>(C::SF_SLOTS)) {
                 const uint32_t j = it - C::SF_SLOTS;
                 if (!thread_wait(empty_bar(j % STAGES), (j / STAGES) & 1u, wctx, SITE_MMA_FULL)) {
                   ok = false;
@@ -504,7 +525,7 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
         uint32_t s = 0, ph = 0, issued = 0;
         for (uint32_t it = 0; it < total_it; ++it) {
           if (!thread_wait(full_bar(s), ph, wctx, SITE_MMA_FULL)) break;
-          if (it >= static_cast<uint32_t>(C::SF_SLOTS)) {
+          if (C::SF_SLOT_WAIT && it >= static_cast<uint32_t>(C::SF_SLOTS)) {
             const uint32_t j = it - C::SF_SLOTS;  // the slot's previous readers
             if (!thread_wait(empty_bar(j % STAGES), (j / STAGES) & 1u, wctx, SITE_MMA_FULL)) break;
           }
@@ -533,7 +554,7 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
         }
       }
     }
-  } else if (KIND == KIND_MXF8 && warp >= 8) {
+  } else if (KIND == KIND_MXF8 && warp >= 8 && p.sf_mode == SF_BY_WARPS) {
     // ------------------------------------------------------------ scale warps
     // Warp 8+q writes TMEM lane quadrant q of every scale slot: source row l
     // of a 512-byte chunk (bytes [16l, 16l+16)) goes to lane 32q + l, four
@@ -548,7 +569,7 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
         uint32_t s = 0, ph = 0;
         for (uint32_t it = 0; it < total_it; ++it) {
           if (!warp_wait(sfl_bar(s), ph, wctx, SITE_MMA_FULL)) break;
-          if (it >= static_cast<uint32_t>(C::SF_SLOTS)) {
+          if (C::SF_SLOT_WAIT && it >= static_cast<uint32_t>(C::SF_SLOTS)) {
             // the slot's previous readers: the MMAs of iteration it - SF_SLOTS
             const uint32_t j = it - C::SF_SLOTS;
             if (!warp_wait(empty_bar(j % STAGES), (j / STAGES) & 1u, wctx, SITE_MMA_FULL)) break;
@@ -581,7 +602,36 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    const int q = warp & 3;                  // TMEM lane quadrant this warp may access
+    const int nparts = C::epi_warps(p.sf_mode) / 4;
+    const int part = (warp - 4) >> 2;        // this warp drains chunks part, part + nparts, ...
+    // one accumulator, eight warps, 16-bit output: read everything, release, then store
+    const bool early = ACC == 1 && nparts == 2 && (p.acc_f16 || p.d_type != OUT_F32);
+    // TMA-store staging: this warp's EPI_BUFS tiles of 32 rows x 64 bytes
+    const uint32_t epi_base = sbase + C::EPI_OFF + static_cast<uint32_t>((warp - 4) * C::EPI_BUFS * C::EPI_TILE_BYTES);
+    uint32_t epi_n = 0;
+    // Store the warp's 32 x 32 block of 16-bit outputs (lane = row) at
+    // (row0, col0): each row's four 16-byte chunks go to the staging tile in
+    // the 64-byte swizzle (chunk j at j ^ ((row >> 1) & 3)), one lane issues
+    // the tile store; the tensor map clips rows >= M and columns >= N.
+    auto store_tile16 = [&](int row0, int col0, const uint32_t(&h)[16]) {
+      const uint32_t buf = epi_base + (epi_n % C::EPI_BUFS) * C::EPI_TILE_BYTES;
+      if (epi_n >= static_cast<uint32_t>(C::EPI_BUFS)) {
+        if (lane == 0) bulk_wait_group_read<C::EPI_BUFS - 1>();  // the buffer's last store has read it
+        __syncwarp();
+      }
+      const uint32_t rb = buf + 64u * static_cast<uint32_t>(lane);
+      const uint32_t sw = (static_cast<uint32_t>(lane) >> 1) & 3u;
+#pragma unroll
+      for (uint32_t j = 0; j < 4; ++j) st_shared_v4(rb + 16u * (j ^ sw), h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
+      fence_proxy_async_shared();
+      __syncwarp();
+      if (lane == 0) {
+        if (row0 < p.M) tma_store_2d(&p.tmap_d, buf, col0, row0);
+        bulk_commit_group();  // one group per staged tile (possibly empty), so the waits above count tiles
+      }
+      ++epi_n;
+    };
     uint32_t tcount = 0;
     for (int t = cluster_id; t < p.num_tiles; t += num_clusters, ++tcount) {
       const int b = static_cast<int>(tcount % ACC);
@@ -590,35 +640,95 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
       tc_fence_after();
       int mt, nt;
       tile_coords(t, p, mt, nt);
-      const int row = mt * C::MMA_M + static_cast<int>(rank) * C::BM + 32 * q + lane;
+      const int row0 = mt * C::MMA_M + static_cast<int>(rank) * C::BM + 32 * q;
+      const int row = row0 + lane;
       const int n0 = nt * BN;
       const uint32_t tb = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(b * BN);
+      auto release = [&]() {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if constexpr (CG == 2)
+            mbar_arrive_cluster(mapa_shared(acce_bar(b), 0));
+          else
+            mbar_arrive(acce_bar(b));
+        }
+      };
+      auto pack16 = [&](const uint32_t(&r)[32], uint32_t(&h)[16]) {
+        if (p.d_type == OUT_BF16) {
+#pragma unroll
+          for (int k = 0; k < 16; ++k) h[k] = pack_bf16(r[2 * k], r[2 * k + 1]);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 16; ++k) h[k] = pack_f16(r[2 * k], r[2 * k + 1]);
+        }
+      };
+      if (early) {
+        constexpr int HALF = (BN / 32 + 1) / 2;  // chunks per warp
+        uint32_t h[HALF][16];
+#pragma unroll
+        for (int i = 0; i < HALF; ++i) {
+          const int c = part + 2 * i;
+          if (c < BN / 32) {
+            if (p.acc_f16) {
+              tmem_ld_32x32b_x16_pack16(tb + 32 * c, h[i]);
+            } else {
+              uint32_t r[32];
+              tmem_ld_32x32b_x32(tb + 32 * c, r);
+              tc_wait_ld();
+              pack16(r, h[i]);
+            }
+          }
+        }
+        tc_wait_ld();
+        release();
+#pragma unroll
+        for (int i = 0; i < HALF; ++i) {
+          const int c = part + 2 * i;
+          if (c < BN / 32 && n0 + 32 * c < p.N) {
+            if (p.d_tma)
+              store_tile16(row0, n0 + 32 * c, h[i]);
+            else if (row < p.M)
+              store_row16(p, row, n0 + 32 * c, h[i]);
+          }
+        }
+        continue;
+      }
       if (p.acc_f16) {
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = part; c < BN / 32; c += nparts) {
           uint32_t h[16];
           tmem_ld_32x32b_x16_pack16(tb + 32 * c, h);
           tc_wait_ld();
-          if (row < p.M && n0 + 32 * c < p.N) store_row16(p, row, n0 + 32 * c, h);
+          if (n0 + 32 * c < p.N) {
+            if (p.d_tma)
+              store_tile16(row0, n0 + 32 * c, h);
+            else if (row < p.M)
+              store_row16(p, row, n0 + 32 * c, h);
+          }
         }
       } else {
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = part; c < BN / 32; c += nparts) {
           uint32_t r[32];
           tmem_ld_32x32b_x32(tb + 32 * c, r);
           tc_wait_ld();
-          if (row < p.M && n0 + 32 * c < p.N) store_row32(p, row, n0 + 32 * c, r);
+          if (n0 + 32 * c < p.N) {
+            if (p.d_tma) {
+              uint32_t h[16];
+              pack16(r, h);
+              store_tile16(row0, n0 + 32 * c, h);
+            } else if (row < p.M) {
+              store_row32(p, row, n0 + 32 * c, r);
+            }
+          }
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if constexpr (CG == 2)
-          mbar_arrive_cluster(mapa_shared(acce_bar(b), 0));
-        else
-          mbar_arrive(acce_bar(b));
-      }
+      release();
     }
+    // the staged tiles must be written out before the CTA ends
+    if (lane == 0) bulk_wait_group_all();
+    __syncwarp();
   }
 
   // ------------------------------------------------------------ teardown

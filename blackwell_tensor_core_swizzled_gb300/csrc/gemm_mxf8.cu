@@ -2,10 +2,11 @@
 // E4M3 operands, one e8m0 scale per 32 K elements) and the scale-factor
 // rearrangement kernel.
 //
-// TMEM budget (128 lanes x 512 columns, "tcgen05.cp" page, "TMEM shape and
-// replicas"): the CTA-pair variant keeps two 224-column accumulators (448
-// columns) and four 16-column scale slots; the single-CTA variant one
-// 256-column accumulator and four scale slots.
+// Both variants use N = 256 tiles: a block-scaled MMA issue costs about the
+// same time for N = 128 ... 256, so narrower tiles lose in proportion.  TMEM
+// (128 lanes x 512 columns, "tcgen05.cp" page, "TMEM shape and replicas")
+// then holds one 256-column accumulator and one 16-column scale slot per ring
+// stage; the epilogue releases the accumulator as soon as it has read it.
 #include "common.h"
 #include "gemm_kernel.cuh"
 
@@ -14,8 +15,8 @@ namespace tcg {
 
 KernelInfo kinfo_mxf8(int cta_group) {
   if (cta_group == 2) {
-    using C = GemmCfg<2, 224, 2, 6, KIND_MXF8>;
-    return {reinterpret_cast<const void*>(&gemm_kernel<2, 224, 2, 6, KIND_MXF8>), C::SMEM_BYTES, 2, 224,
+    using C = GemmCfg<2, 256, 1, 6, KIND_MXF8>;
+    return {reinterpret_cast<const void*>(&gemm_kernel<2, 256, 1, 6, KIND_MXF8>), C::SMEM_BYTES, 2, 256,
             KIND_MXF8, C::THREADS};
   }
   using C = GemmCfg<1, 256, 1, 4, KIND_MXF8>;

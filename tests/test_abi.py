@@ -76,9 +76,12 @@ def test_scale_image_sizes(tcg):
     assert tcg.mxf8_scale_image_bytes(8192, 8192, 128) == 64 * 64 * 512
     assert tcg.mxf8_scale_image_bytes(8192, 8192, 224) == 64 * 37 * 2 * 512
     assert tcg.mxf8_scale_image_bytes(300, 96, 128) == 1 * 3 * 512
-    assert tcg.mxf8_tile_n(8192, 8192, 8192, tcg.K_MAJOR, 2) == 224
-    assert tcg.mxf8_tile_n(8192, 8192, 8192, tcg.MN_MAJOR, 0) == 256
-    assert tcg.mxf8_tile_n(8192, 8192, 8192, tcg.MN_MAJOR, 2) == tcg.ERR_UNSUPPORTED
+    assert tcg.mxf8_scale_image_bytes(8192, 8192, 256) == 64 * 32 * 2 * 512
+    # N = 256 tiles for one CTA and for a pair (a pair's MN-major B half tile
+    # is one whole 128-byte swizzle span of E4M3)
+    for cg in (0, 1, 2):
+        assert tcg.mxf8_tile_n(8192, 8192, 8192, tcg.K_MAJOR, cg) == 256
+        assert tcg.mxf8_tile_n(8192, 8192, 8192, tcg.MN_MAJOR, cg) == 256
 
 
 @pytest.mark.skipif(os.environ.get("CUDA_VISIBLE_DEVICES_FORCE_GPU") is not None, reason="GPU present")

@@ -115,7 +115,8 @@ def test_blockscaled_identity_pins_scale_placement(tcg):
 @pytest.mark.parametrize("staging", [1, 2, 3])
 @pytest.mark.parametrize("am,bm,M,N,K,cg", [("k", "k", 300, 520, 256, 2), ("k", "k", 520, 300, 208, 1),
                                             ("mn", "mn", 200, 300, 256, 1), ("mn", "k", 260, 460, 640, 2),
-                                            ("k", "k", 1100, 1300, 1024, 2)])
+                                            ("k", "k", 1100, 1300, 1024, 2), ("k", "mn", 520, 600, 384, 2),
+                                            ("mn", "mn", 300, 300, 256, 2)])
 def test_blockscaled_scale_staging_modes(tcg, oracle_mod, am, bm, M, N, K, cg, staging):
     # every explicit scale path: tcgen05.st by the scale warps (1), and
     # tcgen05.cp .32x128b.warpx4 issued by the MMA thread (2) or by a
@@ -123,6 +124,16 @@ def test_blockscaled_scale_staging_modes(tcg, oracle_mod, am, bm, M, N, K, cg, s
     # case runs many k-blocks per tile through every scale slot
     x = make_case("e4m3", am, bm, M, N, K, seed=M + 3 * N + K)
     _check_full(tcg, oracle_mod, x, "f32", "f32", cg, sf_staging=staging)
+
+
+@pytest.mark.parametrize("staging", [2, 3])
+@pytest.mark.parametrize("out", ["bf16", "f16"])
+def test_blockscaled_pair_early_release(tcg, oracle_mod, staging, out):
+    # one TMEM accumulator per CTA pair: the eight epilogue warps read it into
+    # registers and release it before storing; 90 pair tiles on at most 76
+    # clusters, so some clusters reuse the accumulator for a second tile
+    x = make_case("e4m3", "k", "k", 2304, 2560, 256, seed=61 + staging)
+    _check_full(tcg, oracle_mod, x, out, "f32", 2, sf_staging=staging)
 
 
 # rows, K, tile rows, byte offset of the plain scales, byte offset of the image.
