@@ -135,7 +135,7 @@ struct GemmCfg {
   // iteration it completes only after the producer saw empty[s] of it - STAGES,
   // i.e. after the MMAs that last read slot it % STAGES retired.
   static constexpr int SF_SLOTS_FREE = (TMEM_COLS - ACC * BN) / SF_SLOT_COLS;
-  static constexpr int SF_SLOTS = SF_SLOTS_FREE < STAGES ? SF_SLOTS_FREE : STAGES;
+  static constexpr int SF_SLOTS = KIND != KIND_MXF8 ? 1 : SF_SLOTS_FREE < STAGES ? SF_SLOTS_FREE : STAGES;
   static constexpr bool SF_SLOT_WAIT = SF_SLOTS < STAGES;
   // epilogue staging for TMA stores: per epilogue warp EPI_BUFS tiles of
   // 32 rows x 64 bytes (32 16-bit columns), 64-byte swizzled
@@ -208,6 +208,12 @@ __device__ __forceinline__ bool thread_wait(uint32_t bar, uint32_t parity, const
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, WaitCtx w, uint32_t site) {
   const bool ok = wait_bounded(bar, parity, w, site);
   return __all_sync(0xffffffffu, ok);
+}
+
+// Warp-uniform wait for the single-issuer roles: one vote when the phase has
+// already completed (the common case), else every lane's bounded wait.
+__device__ __forceinline__ bool wait_uniform(uint32_t bar, uint32_t parity, const WaitCtx& w, uint32_t site) {
+  return __all_sync(0xffffffffu, mbar_try_wait(bar, parity)) || warp_wait(bar, parity, w, site);
 }
 
 // CTA-wide barrier 0 without the .aligned restriction: the threads of a warp
@@ -342,8 +348,11 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    // One thread; lanes 1..31 go straight to the teardown barrier.
-    if (lane == 0) {
+    // The whole warp runs the loop in uniform control flow (tile coordinates,
+    // addresses and the tensor-map operands stay warp-uniform) and waits with
+    // one vote; one elected lane issues the copies.  A lane-0-only loop
+    // measured markedly slower.
+    {
       uint32_t it = 0, s = 0, ph = 0;  // ring iteration, stage, phase of stage s
       bool ok = true;
       for (int t = cluster_id; t < p.num_tiles && ok; t += num_clusters) {
@@ -352,10 +361,11 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
         const int m0 = mt * C::MMA_M + static_cast<int>(rank) * C::BM;
         const int n0 = nt * BN + static_cast<int>(rank) * C::BN_LOCAL;
         for (int kb = 0; kb < p.num_k_blocks; ++kb) {
-          if (!thread_wait(empty_bar(s), ph ^ 1u, wctx, SITE_PROD_EMPTY)) {
+          if (!wait_uniform(empty_bar(s), ph ^ 1u, wctx, SITE_PROD_EMPTY)) {
             ok = false;
             break;
           }
+          if (elect_one()) {
           const uint32_t fb = (CG == 2) ? mapa_shared(full_bar(s), 0) : full_bar(s);
           const bool sf_on_full = KIND == KIND_MXF8 && p.sf_mode != SF_BY_WARPS;
           if (rank == 0) mbar_arrive_expect_tx(full_bar(s), C::TX_BYTES + (sf_on_full ? C::SF_TX_BYTES * CG : 0));
@@ -390,6 +400,8 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
               tma_load_2d(ssfb, &p.tmap_sfb, 0, kb * p.num_n_tiles + nt, sfl_bar(s));
             }
           }
+          }
+          __syncwarp();
           ++it;
           if (++s == STAGES) {
             s = 0;
@@ -397,7 +409,7 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
           }
         }
       }
-      if (!ok) {
+      if (!ok && elect_one()) {
         // Drain: let the copies this CTA issued land before the CTA can exit.
         const uint32_t n_out = it < static_cast<uint32_t>(STAGES) ? it : static_cast<uint32_t>(STAGES);
         if (KIND == KIND_MXF8 && p.sf_mode == SF_BY_WARPS) {
@@ -419,80 +431,93 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
           }
         }
       }
+      __syncwarp();
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    // One thread of the pair leader; lanes 1..31 go to the teardown barrier.
-    if (lane == 0 && (CG == 1 || rank == 0)) {
+    // The pair leader's warp 1.  The tensor pipe queues little ahead of the
+    // MMAs it executes, so the per-stage path must be short: the warp runs
+    // the loop in uniform control flow (descriptors are warp-uniform values:
+    // the stage-0 descriptors plus precomputed stage / K-step increments),
+    // waits with one vote, and one elected lane issues the MMAs and commits.
+    // Issuing from a lane-0-only branch measured slower.
+    if (CG == 1 || rank == 0) {
+      const uint64_t a_desc0 = sdesc(sbase, p.a_desc_hi);
+      const uint64_t b_desc0 = sdesc(sbase + C::A_BYTES, p.b_desc_hi);
+      const uint64_t a_step = p.a_kstep >> 4, b_step = p.b_kstep >> 4;  // 16-byte units
+      uint32_t idesc_j[C::KSTEPS];
+#pragma unroll
+      for (int j = 0; j < C::KSTEPS; ++j)
+        idesc_j[j] = KIND == KIND_MXF8 ? (p.idesc | idesc_sf_ids(j, j)) : p.idesc;
+      const int num_k_blocks = p.num_k_blocks;
+      // block scales staged by other threads: wait for sf_ready[slot] too
+      const bool sf_wait = KIND == KIND_MXF8 && p.sf_mode != SF_BY_MMA;
+      const bool sf_by_mma = KIND == KIND_MXF8 && p.sf_mode == SF_BY_MMA;
       uint32_t it = 0, s = 0, ph = 0, tcount = 0;
       bool ok = true;
       for (int t = cluster_id; t < p.num_tiles && ok; t += num_clusters, ++tcount) {
         const int b = static_cast<int>(tcount % ACC);
         const uint32_t aph = (tcount / ACC) & 1u;
-        if (!thread_wait(acce_bar(b), aph ^ 1u, wctx, SITE_MMA_ACC_EMPTY)) {
+        if (!wait_uniform(acce_bar(b), aph ^ 1u, wctx, SITE_MMA_ACC_EMPTY)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * BN);
-        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
-          if (!thread_wait(full_bar(s), ph, wctx, SITE_MMA_FULL)) {
+        for (int kb = 0; kb < num_k_blocks; ++kb) {
+          const uint32_t slot = it % C::SF_SLOTS;
+          if (!wait_uniform(full_bar(s), ph, wctx, SITE_MMA_FULL)) {
+            ok = false;
+            break;
+          }
+          if (sf_wait && !wait_uniform(sfr_bar(slot), (it / C::SF_SLOTS) & 1u, wctx, SITE_MMA_FULL)) {
+            // the scale warps of both CTAs (tcgen05.st) or the cp thread
+            // (tcgen05.cp + commit) fill this iteration's slot
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t sa = sbase + s * C::STAGE_BYTES;
-          const uint32_t sb = sa + C::A_BYTES;
-          const uint64_t adesc = sdesc(sa, p.a_desc_hi);
-          const uint64_t bdesc = sdesc(sb, p.b_desc_hi);
-          if constexpr (KIND == KIND_MXF8) {
-            // this iteration's scales go to TMEM slot it % SF_SLOTS
-            const uint32_t slot = it % C::SF_SLOTS;
-            const uint32_t sf_col = tmem_base + C::SF_COL0 + slot * C::SF_SLOT_COLS;
-            if (p.sf_mode == SF_BY_MMA) {
-              // this thread stages the scales with tcgen05.cp; they arrived
-              // with full[s].  Wait until the slot's previous readers (the
-              // MMAs of iteration it - SF_SLOTS) have completed.
-              if (C::SF_SLOT_WAIT && it >= static_cast<uint32_t>(C::SF_SLOTS)) {
-                const uint32_t j = it - C::SF_SLOTS;
-                if (!thread_wait(empty_bar(j % STAGES), (j / STAGES) & 1u, wctx, SITE_MMA_FULL)) {
-                  ok = false;
-                  break;
-                }
+          const uint64_t st = (s * static_cast<uint32_t>(C::STAGE_BYTES)) >> 4;
+          const uint64_t adesc = a_desc0 + st;
+          const uint64_t bdesc = b_desc0 + st;
+          const uint32_t sf_col = tmem_base + C::SF_COL0 + slot * C::SF_SLOT_COLS;
+          if (sf_by_mma) {
+            // this thread stages the scales with tcgen05.cp; they arrived
+            // with full[s].  The slot's previous readers (the MMAs of
+            // iteration it - SF_SLOTS) must have completed.
+            if (C::SF_SLOT_WAIT && it >= static_cast<uint32_t>(C::SF_SLOTS)) {
+              const uint32_t j = it - C::SF_SLOTS;
+              if (!wait_uniform(empty_bar(j % STAGES), (j / STAGES) & 1u, wctx, SITE_MMA_FULL)) {
+                ok = false;
+                break;
               }
-              const uint32_t ssfa = sb + C::B_BYTES;
-              // 32 rows x 16 bytes, rows 16 bytes apart: (ldo 16, sdo 128, no swizzle)
-              const uint64_t cp_hi = sdesc_hi(16, 128, SW_NONE);
+            }
+            const uint32_t ssfa = sbase + s * C::STAGE_BYTES + C::A_BYTES + C::B_BYTES;
+            // 32 rows x 16 bytes, rows 16 bytes apart: (ldo 16, sdo 128, no swizzle)
+            const uint64_t cp_hi = sdesc_hi(16, 128, SW_NONE);
+            if (elect_one()) {
               tc_cp_32x128b_warpx4<CG>(sf_col, sdesc(ssfa, cp_hi));
 #pragma unroll
               for (int c = 0; c < C::SFB_CHUNKS; ++c)
                 tc_cp_32x128b_warpx4<CG>(sf_col + 4 + 4 * c, sdesc(ssfa + C::SFA_BYTES + 512 * c, cp_hi));
-            } else {
-              // the scale warps of both CTAs (tcgen05.st) or the cp thread
-              // (tcgen05.cp + commit) have filled this iteration's slot
-              if (!thread_wait(sfr_bar(slot), (it / C::SF_SLOTS) & 1u, wctx, SITE_MMA_FULL)) {
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-            }
-#pragma unroll
-            for (int j = 0; j < C::KSTEPS; ++j) {
-              mma_mxf8<CG>(d_tmem, adesc + ((j * p.a_kstep) >> 4), bdesc + ((j * p.b_kstep) >> 4),
-                           p.idesc | idesc_sf_ids(j, j), sf_col, sf_col + 4, (kb | j) != 0);
-            }
-          } else {
-#pragma unroll
-            for (int j = 0; j < C::KSTEPS; ++j) {
-              const uint64_t ad = adesc + ((j * p.a_kstep) >> 4);
-              const uint64_t bd = bdesc + ((j * p.b_kstep) >> 4);
-              if constexpr (KIND == KIND_F16)
-                mma_f16<CG>(d_tmem, ad, bd, p.idesc, (kb | j) != 0);
-              else
-                mma_tf32<CG>(d_tmem, ad, bd, p.idesc, (kb | j) != 0);
             }
           }
+          if (elect_one()) {
+#pragma unroll
+          for (int j = 0; j < C::KSTEPS; ++j) {
+            const uint64_t ad = adesc + j * a_step;
+            const uint64_t bd = bdesc + j * b_step;
+            const uint32_t acc = (kb | j) != 0;
+            if constexpr (KIND == KIND_MXF8)
+              mma_mxf8<CG>(d_tmem, ad, bd, idesc_j[j], sf_col, sf_col + 4, acc);
+            else if constexpr (KIND == KIND_F16)
+              mma_f16<CG>(d_tmem, ad, bd, idesc_j[j], acc);
+            else
+              mma_tf32<CG>(d_tmem, ad, bd, idesc_j[j], acc);
+          }
           tc_commit<CG>(empty_bar(s));
+          }
+          __syncwarp();
           ++it;
           if (++s == STAGES) {
             s = 0;
@@ -500,50 +525,55 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
           }
         }
         if (!ok) break;
-        tc_commit<CG>(accf_bar(b));
+        if (elect_one()) tc_commit<CG>(accf_bar(b));
+        __syncwarp();
       }
-      if (!ok) {
+      if (!ok && elect_one()) {
         // Drain: wait (bounded) for every MMA / cp this thread issued.
         tc_commit<CG>(drain_bar);
         const uint64_t t0 = globaltimer();
         while (!mbar_try_wait(drain_bar, 0) && globaltimer() - t0 < 20000000ull) {
         }
       }
+      __syncwarp();
     }
   } else if (KIND == KIND_MXF8 && warp == 3) {
     // ------------------------------------------------------------ cp thread
-    // SF_BY_CP: one thread of the pair leader copies each stage's scales into
-    // its TMEM slot with tcgen05.cp .32x128b.warpx4 (both CTAs of a pair) and
-    // commits to sf_ready[slot]; the MMA thread's tensor-pipe stream then
-    // holds only MMAs.
+    // SF_BY_CP: the pair leader's warp 3 copies each stage's scales into its
+    // TMEM slot with tcgen05.cp .32x128b.warpx4 (both CTAs of a pair) and
+    // commits to sf_ready[slot]; the MMA warp's tensor-pipe stream then holds
+    // only MMAs.  Uniform loop, one elected lane issues (as for the MMAs).
     if constexpr (KIND == KIND_MXF8) {
-      if (p.sf_mode == SF_BY_CP && lane == 0 && (CG == 1 || rank == 0)) {
+      if (p.sf_mode == SF_BY_CP && (CG == 1 || rank == 0)) {
         const uint32_t my_tiles =
             cluster_id < p.num_tiles ? (p.num_tiles - cluster_id + num_clusters - 1) / num_clusters : 0;
         const uint32_t total_it = my_tiles * static_cast<uint32_t>(p.num_k_blocks);
         const uint64_t cp_hi = sdesc_hi(16, 128, SW_NONE);  // 32 rows x 16 B, rows 16 B apart
         uint32_t s = 0, ph = 0, issued = 0;
         for (uint32_t it = 0; it < total_it; ++it) {
-          if (!thread_wait(full_bar(s), ph, wctx, SITE_MMA_FULL)) break;
+          if (!wait_uniform(full_bar(s), ph, wctx, SITE_MMA_FULL)) break;
           if (C::SF_SLOT_WAIT && it >= static_cast<uint32_t>(C::SF_SLOTS)) {
             const uint32_t j = it - C::SF_SLOTS;  // the slot's previous readers
-            if (!thread_wait(empty_bar(j % STAGES), (j / STAGES) & 1u, wctx, SITE_MMA_FULL)) break;
+            if (!wait_uniform(empty_bar(j % STAGES), (j / STAGES) & 1u, wctx, SITE_MMA_FULL)) break;
           }
           tc_fence_after();
           const uint32_t ssfa = sbase + s * C::STAGE_BYTES + C::A_BYTES + C::B_BYTES;
           const uint32_t col = tmem_base + C::SF_COL0 + (it % C::SF_SLOTS) * C::SF_SLOT_COLS;
-          tc_cp_32x128b_warpx4<CG>(col, sdesc(ssfa, cp_hi));
+          if (elect_one()) {
+            tc_cp_32x128b_warpx4<CG>(col, sdesc(ssfa, cp_hi));
 #pragma unroll
-          for (int c = 0; c < C::SFB_CHUNKS; ++c)
-            tc_cp_32x128b_warpx4<CG>(col + 4 + 4 * c, sdesc(ssfa + C::SFA_BYTES + 512 * c, cp_hi));
-          tc_commit<CG>(sfr_bar(it % C::SF_SLOTS));
+            for (int c = 0; c < C::SFB_CHUNKS; ++c)
+              tc_cp_32x128b_warpx4<CG>(col + 4 + 4 * c, sdesc(ssfa + C::SFA_BYTES + 512 * c, cp_hi));
+            tc_commit<CG>(sfr_bar(it % C::SF_SLOTS));
+          }
+          __syncwarp();
           issued = it + 1;
           if (++s == STAGES) {
             s = 0;
             ph ^= 1u;
           }
         }
-        if (issued > 0) {
+        if (issued > 0 && elect_one()) {
           // let the copies land before the CTA can exit: the last commit
           // tracks every copy this thread issued
           const uint32_t j = issued - 1;
