@@ -400,12 +400,11 @@ int run_gemm(const tcg_gemm_args* args, cudaStream_t s) {
   }
   prm.err = d->err;
   prm.timeout_ns = g_timeout_ns.load();
-  // auto: in a pair the warps' tcgen05.st is slow and the dedicated cp thread
-  // fastest; a single CTA is fastest with the scale warps
+  // auto: the MMA warp copies the scales itself (fastest or tied for both
+  // CTA groups once the issue loops are warp-uniform; no extra barriers)
   prm.sf_mode = a.sf_staging == 1   ? SF_BY_WARPS
-                : a.sf_staging == 2 ? SF_BY_MMA
                 : a.sf_staging == 3 ? SF_BY_CP
-                                    : (cg == 2 ? SF_BY_CP : SF_BY_WARPS);
+                                    : SF_BY_MMA;
 
   int launches = 0;
   if (scaled) {

@@ -3,25 +3,29 @@
 //   D[m,n] = sum_k A[m,k] B[k,n]       (kind::f16, kind::tf32)
 //   D[m,n] = sum_k (SFA.A)[m,k] (SFB.B)[k,n]   (kind::mxf8f6f4.block_scale)
 //
-// Structure (one CTA per SM, or one CTA pair per two SMs for cta_group::2):
-//   warp 0      TMA producer (one thread): 128B-swizzled A/B tiles (and scale
-//               images) into a STAGES-deep ring, full[s] barriers counting
-//               bytes;
-//   warp 1      MMA issuer (one thread; pair leader only): for each ring stage
-//               KSTEPS tcgen05.mma issues, then tcgen05.commit -> empty[s]; at
-//               the end of a tile a commit -> acc_full[b];
+// Structure (one CTA per SM, or one CTA pair per two SMs for cta_group::2).
+// The issuing roles run their loops on the whole warp in uniform control flow
+// (one vote per barrier wait, warp-uniform operands) and one elected lane
+// issues:
+//   warp 0      TMA producer: 128B-swizzled A/B tiles (and scale images) into
+//               a STAGES-deep ring, full[s] barriers counting bytes;
+//   warp 1      MMA issuer (pair leader only): for each ring stage the scale
+//               copies when it stages them (tcgen05.cp .32x128b.warpx4, the
+//               default for block scaling), KSTEPS tcgen05.mma issues, then
+//               tcgen05.commit -> empty[s]; at the end of a tile a commit ->
+//               acc_full[b];
 //   warp 2      TMEM allocation / deallocation (512 columns);
+//   warp 3      (block scaling, GemmParams::sf_mode SF_BY_CP) a separate
+//               copy warp: tcgen05.cp + commit -> sf_ready[slot];
 //   warps 4..7  epilogue: tcgen05.ld .32x32b from accumulator b (warp w
-//               reads lanes 32*(w%4)..+31), convert, store to global, then
-//               arrive acc_empty[b];
-//   warps 8..11 (block scaling) scale staging: each writes its TMEM lane
-//               quadrant of the stage's scale slot with tcgen05.st and arrives
-//               sf_ready[slot].  Alternatively (GemmParams::sf_mode) the MMA
-//               thread stages the scales itself with tcgen05.cp .32x128b.warpx4
-//               (every cp then sits in its in-order tensor-pipe stream), or a
-//               dedicated thread (warp 3) does, committing to sf_ready[slot];
-//               warps 8..11 then join the epilogue (each of the two warps of a
-//               lane quadrant drains every other 32-column chunk).
+//               reads lanes 32*(w%4)..+31), convert, store to global (16-bit
+//               outputs through a shared staging tile and a TMA tile store),
+//               then arrive acc_empty[b];
+//   warps 8..11 (block scaling) with SF_BY_WARPS: scale staging, each warp
+//               writes its TMEM lane quadrant of the stage's scale slot with
+//               tcgen05.st and arrives sf_ready[slot]; otherwise they join
+//               the epilogue (the two warps of a lane quadrant drain
+//               alternate 32-column chunks).
 // With two accumulators the epilogue of one tile overlaps the main loop of the
 // next.  With one (a 256-column block-scaled tile leaves no TMEM for a second)
 // an eight-warp epilogue with 16-bit output reads the whole accumulator into
@@ -98,8 +102,8 @@ struct GemmParams {
   // block scaling, where the scales are staged into TMEM:
   //   SF_BY_WARPS  the four scale warps, tcgen05.st (scales complete on each
   //                CTA's own sf_loaded[s]);
-  //   SF_BY_MMA    the MMA thread, tcgen05.cp before its MMAs;
-  //   SF_BY_CP     a dedicated thread (warp 3), tcgen05.cp + commit to
+  //   SF_BY_MMA    the MMA warp, tcgen05.cp before its MMAs;
+  //   SF_BY_CP     a separate copy warp (warp 3), tcgen05.cp + commit to
   //                sf_ready[slot].
   // With tcgen05.cp (a pair copies both CTAs' smem) the scale images complete
   // on the pair leader's full[s] barrier together with A and B.

@@ -151,7 +151,7 @@ typedef struct {
   int cta_group;     /* 0 auto, 1 (one CTA per 128xN tile), 2 (CTA pair, 256xN) */
   int raster_group;  /* 0 auto; tiles are visited in groups of this many M tiles */
   int sf_staging;    /* block scaling, who stages the scales into TMEM:
-                        0 = auto (3 for CTA pairs, 1 for single CTAs),
+                        0 = auto (2),
                         1 = four scale warps per CTA with tcgen05.st,
                         2 = the MMA thread with tcgen05.cp .32x128b.warpx4
                             ("tcgen05.cp" page) before its MMAs,
