@@ -457,6 +457,9 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
       // block scales staged by other threads: wait for sf_ready[slot] too
       const bool sf_wait = KIND == KIND_MXF8 && p.sf_mode != SF_BY_MMA;
       const bool sf_by_mma = KIND == KIND_MXF8 && p.sf_mode == SF_BY_MMA;
+      // the copy warp commits sf_ready[slot] only after it saw full[s] of the
+      // same iteration, so that one wait covers both
+      const bool full_via_sfr = KIND == KIND_MXF8 && p.sf_mode == SF_BY_CP;
       uint32_t it = 0, s = 0, ph = 0, tcount = 0;
       bool ok = true;
       for (int t = cluster_id; t < p.num_tiles && ok; t += num_clusters, ++tcount) {
@@ -470,12 +473,12 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * BN);
         for (int kb = 0; kb < num_k_blocks; ++kb) {
           const uint32_t slot = it % C::SF_SLOTS;
-          if (!wait_uniform(full_bar(s), ph, wctx, SITE_MMA_FULL)) {
+          if (!full_via_sfr && !wait_uniform(full_bar(s), ph, wctx, SITE_MMA_FULL)) {
             ok = false;
             break;
           }
           if (sf_wait && !wait_uniform(sfr_bar(slot), (it / C::SF_SLOTS) & 1u, wctx, SITE_MMA_FULL)) {
-            // the scale warps of both CTAs (tcgen05.st) or the cp thread
+            // the scale warps of both CTAs (tcgen05.st) or the copy warp
             // (tcgen05.cp + commit) fill this iteration's slot
             ok = false;
             break;
