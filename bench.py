@@ -226,48 +226,78 @@ def run_workload(tcg, torch, w, steps, warmup, dist_ctx, measure_e2e=True):
     res = {"total_ms": total_ms, "kernel_ms": kernel_ms, "launches": launches[0], "t0": t_host0, "t1": t_host1}
 
     if measure_e2e:
-        # End to end through the C ABI: pinned host inputs copied in, GEMM,
-        # result copied out, every step.
-        hA = torch.from_numpy(x["A"].view({np.dtype(np.uint8): np.uint8, np.dtype(np.uint16): np.int16,
-                                           np.dtype(np.uint32): np.int32}[x["A"].dtype])).pin_memory()
-        hB = torch.from_numpy(x["B"].view({np.dtype(np.uint8): np.uint8, np.dtype(np.uint16): np.int16,
-                                           np.dtype(np.uint32): np.int32}[x["B"].dtype])).pin_memory()
-        hD = torch.empty((M, N), dtype=out_t).pin_memory()
-        e_steps = max(1, min(steps, 10))
+        # End to end through the C ABI: every step copies its inputs in from
+        # pinned host memory, runs the GEMM and copies the result out.  Steps
+        # are double buffered on three streams (upload, compute, download), so
+        # the upload of step i+1 and the download of step i-1 overlap the GEMM
+        # of step i, as a serving loop would run it.
+        view = {np.dtype(np.uint8): np.uint8, np.dtype(np.uint16): np.int16, np.dtype(np.uint32): np.int32}
+        hA = torch.from_numpy(x["A"].view(view[x["A"].dtype])).pin_memory()
+        hB = torch.from_numpy(x["B"].view(view[x["B"].dtype])).pin_memory()
+        hD = [torch.empty((M, N), dtype=out_t).pin_memory() for _ in range(2)]
+        e_steps = max(2, min(steps, 12))
         h2d = hA.numel() * hA.element_size() + hB.numel() * hB.element_size()
+        dA = [A, torch.empty_like(A)]
+        dB = [B, torch.empty_like(B)]
+        dD = [D, torch.empty_like(D)]
         if scaled:
             hSFA = torch.from_numpy(x["SFA"]).pin_memory()
             hSFB = torch.from_numpy(x["SFB"]).pin_memory()
             h2d += hSFA.numel() + hSFB.numel()
-        d2h = hD.numel() * hD.element_size()
+            dSFA = [SFA, torch.empty_like(SFA)]
+            dSFB = [SFB, torch.empty_like(SFB)]
+        d2h = hD[0].numel() * hD[0].element_size()
+        up, comp, down = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+        ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("up", "comp", "down")}
+        started = [[False, False]]
 
-        def e2e_step():
-            A.copy_(hA, non_blocking=True)
-            B.copy_(hB, non_blocking=True)
+        def e2e_step(i):
+            bi = i % 2
+            with torch.cuda.stream(up):
+                if started[0][bi]:
+                    up.wait_event(ev["comp"][bi])  # the GEMM of step i-2 has read this buffer
+                dA[bi].copy_(hA, non_blocking=True)
+                dB[bi].copy_(hB, non_blocking=True)
+                if scaled:
+                    dSFA[bi].copy_(hSFA, non_blocking=True)
+                    dSFB[bi].copy_(hSFB, non_blocking=True)
+                ev["up"][bi].record(up)
+            comp.wait_event(ev["up"][bi])
+            if started[0][bi]:
+                comp.wait_event(ev["down"][bi])  # the result of step i-2 has left this buffer
+            cs = comp.cuda_stream
             if scaled:
-                SFA.copy_(hSFA, non_blocking=True)
-                SFB.copy_(hSFB, non_blocking=True)
-                tcg.gemm_mxf8_blockscaled(M, N, K, A, a_maj, x["lda"], B, b_maj, x["ldb"], SFA, SFB, D,
-                                          OUT[w.out], N, ACC[w.acc], stream=sp)
+                tcg.gemm_mxf8_blockscaled(M, N, K, dA[bi], a_maj, x["lda"], dB[bi], b_maj, x["ldb"], dSFA[bi],
+                                          dSFB[bi], dD[bi], OUT[w.out], N, ACC[w.acc], stream=cs)
             else:
                 fn = {"f16": tcg.gemm_f16, "bf16": tcg.gemm_bf16, "tf32": tcg.gemm_tf32}[w.dtype]
-                fn(M, N, K, A, a_maj, x["lda"], B, b_maj, x["ldb"], D, OUT[w.out], N, ACC[w.acc], stream=sp)
-            hD.copy_(D, non_blocking=True)
+                fn(M, N, K, dA[bi], a_maj, x["lda"], dB[bi], b_maj, x["ldb"], dD[bi], OUT[w.out], N, ACC[w.acc],
+                   stream=cs)
+            ev["comp"][bi].record(comp)
+            with torch.cuda.stream(down):
+                down.wait_event(ev["comp"][bi])
+                hD[bi].copy_(dD[bi], non_blocking=True)
+                ev["down"][bi].record(down)
+            started[0][bi] = True
 
-        e2e_step()
+        for i in range(2):
+            e2e_step(i)
         torch.cuda.synchronize()
+        started[0] = [False, False]
         es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         dist_ctx.barrier()
         torch.cuda.synchronize()
-        es.record(stream)
-        for _ in range(e_steps):
-            e2e_step()
-        ee.record(stream)
+        es.record(up)
+        for i in range(e_steps):
+            e2e_step(i)
+        for k in range(2):
+            down.wait_event(ev["down"][k])
+        ee.record(down)
         torch.cuda.synchronize()
-        rc = tcg.check(sp)
+        rc = tcg.check(comp.cuda_stream)
         if rc != 0:
             raise RuntimeError(f"e2e run failed: {tcg.status_string(rc)}")
-        res.update({"e2e_ms": es.elapsed_time(ee) / e_steps, "h2d": h2d, "d2h": d2h})
+        res.update({"e2e_ms": es.elapsed_time(ee) / e_steps, "h2d": h2d, "d2h": d2h, "e2e_steps": e_steps})
     return res
 
 
@@ -448,7 +478,9 @@ def main():
         "roofline": rl,
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_val, 1), "unit": UNIT, "h2d_bytes_per_step": res["h2d"],
-                "d2h_bytes_per_step": res["d2h"], "ms_per_step": round(e2e_ms, 3)},
+                "d2h_bytes_per_step": res["d2h"], "ms_per_step": round(e2e_ms, 3), "steps": res["e2e_steps"],
+                "pipeline": "pinned host inputs in and result out every step; double buffered on upload / "
+                            "compute / download streams"},
         "gpu_launches": res["launches"],
         "clocks": clocks,
         "secondary": sec,
