@@ -53,6 +53,18 @@ struct Workspace {
 };
 std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
 
+// Split-K workspace per (device, stream): fp32 partial sums and per-chunk
+// counters.  Zeroed when allocated; every call leaves the parts it used zero
+// again.  A device-side failure can leave it dirty, so tcg_check bumps
+// g_error_gen and a workspace zeroed under an older generation is re-zeroed.
+struct SplitWorkspace {
+  void* ptr = nullptr;
+  size_t bytes = 0;
+  uint64_t gen = 0;
+};
+std::map<std::pair<int, cudaStream_t>, SplitWorkspace> g_split_ws;
+std::atomic<uint64_t> g_error_gen{1};
+
 void load_timeout_env() {
   static std::once_flag once;
   std::call_once(once, [] {
@@ -253,6 +265,32 @@ int workspace(int dev, cudaStream_t s, size_t bytes, void** out) {
   return TCG_OK;
 }
 
+int split_workspace(int dev, cudaStream_t s, size_t bytes, void** out) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  SplitWorkspace& w = g_split_ws[std::make_pair(dev, s)];
+  const uint64_t gen = g_error_gen.load();
+  if (w.bytes < bytes) {
+    if (w.ptr) {
+      cudaError_t e = cudaFree(w.ptr);  // synchronises: no queued kernel still uses it
+      w.ptr = nullptr;
+      w.bytes = 0;
+      if (e != cudaSuccess) return record_cuda(e);
+    }
+    const size_t want = std::max(bytes, static_cast<size_t>(1) << 20);
+    cudaError_t e = cudaMalloc(&w.ptr, want);
+    if (e != cudaSuccess) return record_cuda(e);
+    w.bytes = want;
+    w.gen = 0;
+  }
+  if (w.gen != gen) {
+    const cudaError_t e = cudaMemsetAsync(w.ptr, 0, w.bytes, s);
+    if (e != cudaSuccess) return record_cuda(e);
+    w.gen = gen;
+  }
+  *out = w.ptr;
+  return TCG_OK;
+}
+
 CUtensorMapDataType map_dtype(tcg_input t) {
   switch (t) {
     case TCG_IN_F16: return CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
@@ -314,7 +352,8 @@ int run_gemm(const tcg_gemm_args* args, cudaStream_t s) {
     return TCG_ERR_INVALID;
   if (a.acc_type == TCG_BF16) return TCG_ERR_UNSUPPORTED;
   if (a.acc_type == TCG_F16 && (a.in_type != TCG_IN_F16 || a.d_type != TCG_F16)) return TCG_ERR_UNSUPPORTED;
-  if (a.cta_group < 0 || a.cta_group > 2 || a.raster_group < 0 || a.sf_staging < 0 || a.sf_staging > 3)
+  if (a.cta_group < 0 || a.cta_group > 2 || a.raster_group < 0 || a.sf_staging < 0 || a.sf_staging > 3 ||
+      a.split_k < 0)
     return TCG_ERR_INVALID;
   if (a.M > INT32_MAX / 2 || a.N > INT32_MAX / 2 || a.K > INT32_MAX / 2) return TCG_ERR_UNSUPPORTED;
   if (a.M == 0 || a.N == 0) return TCG_OK;
@@ -439,7 +478,39 @@ int run_gemm(const tcg_gemm_args* args, cudaStream_t s) {
 
   int max_clusters = 0;
   if (int rc = max_clusters_for(d, ki, &max_clusters)) return rc;
-  const int clusters = std::max(1, std::min(prm.num_tiles, max_clusters));
+
+  // Problems with fewer output tiles than clusters (skinny M or N) would
+  // leave SMs idle: by default they run stream-K (each cluster takes an equal
+  // contiguous share of the (tile, k block) iterations; tiles cut between
+  // clusters meet in an fp32 workspace).  split_k >= 2 asks for a fixed split
+  // of every tile instead.  f16 accumulation keeps its single-pass path.
+  int split = 1;
+  bool stream_k = false;
+  if (a.acc_type != TCG_F16) {
+    if (a.split_k > 1)
+      split = static_cast<int>(std::min<int64_t>(a.split_k, prm.num_k_blocks));
+    else if (a.split_k == 0 && prm.num_tiles < max_clusters && prm.num_k_blocks >= 8)
+      stream_k = true;
+  }
+  prm.split = split;
+  prm.stream_k = stream_k ? 1 : 0;
+  prm.num_units = prm.num_tiles * split;
+  const int64_t iterations = static_cast<int64_t>(prm.num_tiles) * prm.num_k_blocks;
+  if (split > 1 || stream_k) {
+    prm.ldw = cdiv(a.N, 4) * 4;
+    const size_t wbytes = static_cast<size_t>(cdiv(static_cast<int64_t>(a.M) * prm.ldw * 4, 256) * 256);
+    const size_t cbytes = static_cast<size_t>(prm.num_tiles) * cg * 8 * sizeof(int);
+    void* ws = nullptr;
+    if (int rc = split_workspace(dev, s, wbytes + cbytes, &ws)) return rc;
+    prm.w = static_cast<float*>(ws);
+    prm.counters = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + wbytes);
+    if (int rc = make_map_2d(&prm.tmap_w, prm.w, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, static_cast<uint64_t>(a.N),
+                             static_cast<uint64_t>(a.M), static_cast<uint64_t>(prm.ldw), 16, 32,
+                             CU_TENSOR_MAP_SWIZZLE_64B))
+      return rc;
+  }
+  const int clusters = static_cast<int>(
+      std::max<int64_t>(1, std::min<int64_t>(stream_k ? iterations : prm.num_units, max_clusters)));
   if (int rc = launch_gemm(ki, prm, clusters, s)) return rc;
   t_last_launches = launches + 1;
   return TCG_OK;
@@ -599,7 +670,10 @@ int tcg_mxf8_prepare_scales_ab(const uint8_t* SFA, int64_t M, uint8_t* SFA_img, 
 
 int tcg_check(void* stream) {
   cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return record_cuda(e);
+  if (e != cudaSuccess) {
+    g_error_gen.fetch_add(1);  // split-K workspaces may be dirty
+    return record_cuda(e);
+  }
   int dev = 0;
   e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return record_cuda(e);
@@ -609,6 +683,7 @@ int tcg_check(void* stream) {
   e = cudaMemcpy(&w, st->err, sizeof w, cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return record_cuda(e);
   if (w == 0) return TCG_OK;
+  g_error_gen.fetch_add(1);  // an aborted kernel may have left split-K workspaces dirty
   e = cudaMemset(st->err, 0, sizeof w);
   if (e != cudaSuccess) return record_cuda(e);
   char buf[128];

@@ -77,10 +77,27 @@ struct GemmParams {
   CUtensorMap tmap_sfa;
   CUtensorMap tmap_sfb;
   CUtensorMap tmap_d;  // 16-bit D in 32 x 32 boxes, 64-byte swizzle (used when d_tma)
+  CUtensorMap tmap_w;  // fp32 split-K workspace [M][N] in 16 x 32 boxes, 64-byte swizzle
   int M, N, K;
   int num_m_tiles;   // tiles of 128*CG rows
   int num_n_tiles;   // tiles of BN columns
   int num_k_blocks;  // ring stages per tile (128 bytes of K each)
+  // split-K: every output tile is computed by `split` units over consecutive
+  // K ranges; num_units = num_tiles * split.  With split > 1 the units add
+  // their fp32 partial tiles into the workspace `w` (TMA reduce-add through
+  // tmap_w, 16 x 32 boxes) and the last unit to finish a chunk (counted in
+  // `counters`, one per tile, CTA of a pair and epilogue warp) converts it to
+  // D and clears it.
+  int split;
+  int num_units;
+  // stream-K: cluster c takes the global (tile, k block) iterations
+  // [c*T/G, (c+1)*T/G), T = num_tiles * num_k_blocks, G = clusters, cut at
+  // tile boundaries; a tile whose K blocks lie in one cluster is stored
+  // directly, the others meet in the workspace like split-K units
+  int stream_k;
+  float* w;
+  int64_t ldw;  // workspace row stride (elements)
+  int* counters;
   int num_tiles;
   int raster_group;
   int a_mn_major, b_mn_major;
@@ -236,6 +253,74 @@ __device__ __forceinline__ void tile_coords(int t, const GemmParams& p, int& mt,
   nt = r / gs;
 }
 
+// The units (one tile's K blocks [kb0, kb1)) a cluster processes, in order:
+// whole tiles cluster_id, +G, ... (split == 1); `split` consecutive K ranges
+// per tile, unit u -> tile u / split (split > 1); or the cluster's stream-K
+// range of the global iteration space, cut at tile boundaries.
+struct UnitCursor {
+  int64_t i, i1;  // stream-K position and end
+  int u;          // strided unit index
+  int tile, kb0, kb1;
+  bool valid;
+};
+
+__device__ __forceinline__ void cursor_load(UnitCursor& c, const GemmParams& p) {
+  if (p.stream_k) {
+    c.valid = c.i < c.i1;
+    if (!c.valid) return;
+    c.tile = static_cast<int>(c.i / p.num_k_blocks);
+    const int64_t t0 = static_cast<int64_t>(c.tile) * p.num_k_blocks;
+    c.kb0 = static_cast<int>(c.i - t0);
+    c.kb1 = static_cast<int>(min(static_cast<int64_t>(p.num_k_blocks), c.i1 - t0));
+  } else {
+    c.valid = c.u < p.num_units;
+    if (!c.valid) return;
+    c.tile = c.u / p.split;
+    const int ks = c.u - c.tile * p.split;
+    c.kb0 = static_cast<int>(static_cast<int64_t>(ks) * p.num_k_blocks / p.split);
+    c.kb1 = static_cast<int>(static_cast<int64_t>(ks + 1) * p.num_k_blocks / p.split);
+  }
+}
+
+__device__ __forceinline__ UnitCursor cursor_begin(int cluster_id, int num_clusters, const GemmParams& p) {
+  UnitCursor c;
+  const int64_t T = static_cast<int64_t>(p.num_tiles) * p.num_k_blocks;
+  c.i = cluster_id * T / num_clusters;
+  c.i1 = (cluster_id + 1) * T / num_clusters;
+  c.u = cluster_id;
+  cursor_load(c, p);
+  return c;
+}
+
+__device__ __forceinline__ void cursor_next(UnitCursor& c, int num_clusters, const GemmParams& p) {
+  if (p.stream_k)
+    c.i = static_cast<int64_t>(c.tile + 1) * p.num_k_blocks;
+  else
+    c.u += num_clusters;
+  cursor_load(c, p);
+}
+
+// Number of units that contribute to `tile` (the arrivals its reduction
+// counts): `split`, or under stream-K the clusters whose ranges meet it.
+__device__ __forceinline__ int tile_unit_count(int tile, int num_clusters, const GemmParams& p) {
+  if (!p.stream_k) return p.split;
+  const int64_t T = static_cast<int64_t>(p.num_tiles) * p.num_k_blocks;
+  const int64_t s0 = static_cast<int64_t>(tile) * p.num_k_blocks;
+  const int64_t s1 = s0 + p.num_k_blocks - 1;
+  // cluster owning iteration i: the largest c with c*T/G <= i
+  const int64_t c0 = ((s0 + 1) * num_clusters - 1) / T;
+  const int64_t c1 = ((s1 + 1) * num_clusters - 1) / T;
+  return static_cast<int>(c1 - c0 + 1);
+}
+
+// Ring iterations (k blocks) of all units a cluster processes.
+__device__ __forceinline__ uint32_t cluster_iterations(int cluster_id, int num_clusters, const GemmParams& p) {
+  uint32_t n = 0;
+  for (UnitCursor c = cursor_begin(cluster_id, num_clusters, p); c.valid; cursor_next(c, num_clusters, p))
+    n += static_cast<uint32_t>(c.kb1 - c.kb0);
+  return n;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(uint32_t lo, uint32_t hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(lo), __uint_as_float(hi));
   return *reinterpret_cast<uint32_t*>(&v);
@@ -359,12 +444,14 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
     {
       uint32_t it = 0, s = 0, ph = 0;  // ring iteration, stage, phase of stage s
       bool ok = true;
-      for (int t = cluster_id; t < p.num_tiles && ok; t += num_clusters) {
+      for (UnitCursor uc = cursor_begin(cluster_id, num_clusters, p); uc.valid && ok;
+           cursor_next(uc, num_clusters, p)) {
         int mt, nt;
-        tile_coords(t, p, mt, nt);
+        tile_coords(uc.tile, p, mt, nt);
+        const int kb0 = uc.kb0, kb1 = uc.kb1;
         const int m0 = mt * C::MMA_M + static_cast<int>(rank) * C::BM;
         const int n0 = nt * BN + static_cast<int>(rank) * C::BN_LOCAL;
-        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!wait_uniform(empty_bar(s), ph ^ 1u, wctx, SITE_PROD_EMPTY)) {
             ok = false;
             break;
@@ -453,7 +540,6 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
 #pragma unroll
       for (int j = 0; j < C::KSTEPS; ++j)
         idesc_j[j] = KIND == KIND_MXF8 ? (p.idesc | idesc_sf_ids(j, j)) : p.idesc;
-      const int num_k_blocks = p.num_k_blocks;
       // block scales staged by other threads: wait for sf_ready[slot] too
       const bool sf_wait = KIND == KIND_MXF8 && p.sf_mode != SF_BY_MMA;
       const bool sf_by_mma = KIND == KIND_MXF8 && p.sf_mode == SF_BY_MMA;
@@ -462,7 +548,9 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
       const bool full_via_sfr = KIND == KIND_MXF8 && p.sf_mode == SF_BY_CP;
       uint32_t it = 0, s = 0, ph = 0, tcount = 0;
       bool ok = true;
-      for (int t = cluster_id; t < p.num_tiles && ok; t += num_clusters, ++tcount) {
+      for (UnitCursor uc = cursor_begin(cluster_id, num_clusters, p); uc.valid && ok;
+           cursor_next(uc, num_clusters, p), ++tcount) {
+        const int kb0 = uc.kb0, kb1 = uc.kb1;
         const int b = static_cast<int>(tcount % ACC);
         const uint32_t aph = (tcount / ACC) & 1u;
         if (!wait_uniform(acce_bar(b), aph ^ 1u, wctx, SITE_MMA_ACC_EMPTY)) {
@@ -471,7 +559,7 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * BN);
-        for (int kb = 0; kb < num_k_blocks; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           const uint32_t slot = it % C::SF_SLOTS;
           if (!full_via_sfr && !wait_uniform(full_bar(s), ph, wctx, SITE_MMA_FULL)) {
             ok = false;
@@ -514,7 +602,7 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
           for (int j = 0; j < C::KSTEPS; ++j) {
             const uint64_t ad = adesc + j * a_step;
             const uint64_t bd = bdesc + j * b_step;
-            const uint32_t acc = (kb | j) != 0;
+            const uint32_t acc = (kb != kb0 || j != 0) ? 1u : 0u;
             if constexpr (KIND == KIND_MXF8)
               mma_mxf8<CG>(d_tmem, ad, bd, idesc_j[j], sf_col, sf_col + 4, acc);
             else if constexpr (KIND == KIND_F16)
@@ -552,9 +640,7 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
     // only MMAs.  Uniform loop, one elected lane issues (as for the MMAs).
     if constexpr (KIND == KIND_MXF8) {
       if (p.sf_mode == SF_BY_CP && (CG == 1 || rank == 0)) {
-        const uint32_t my_tiles =
-            cluster_id < p.num_tiles ? (p.num_tiles - cluster_id + num_clusters - 1) / num_clusters : 0;
-        const uint32_t total_it = my_tiles * static_cast<uint32_t>(p.num_k_blocks);
+        const uint32_t total_it = cluster_iterations(cluster_id, num_clusters, p);
         const uint64_t cp_hi = sdesc_hi(16, 128, SW_NONE);  // 32 rows x 16 B, rows 16 B apart
         uint32_t s = 0, ph = 0, issued = 0;
         for (uint32_t it = 0; it < total_it; ++it) {
@@ -600,9 +686,7 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
     if constexpr (KIND == KIND_MXF8) {
       if (p.sf_mode == SF_BY_WARPS) {
         const int q = warp & 3;
-        const uint32_t my_tiles =
-            cluster_id < p.num_tiles ? (p.num_tiles - cluster_id + num_clusters - 1) / num_clusters : 0;
-        const uint32_t total_it = my_tiles * static_cast<uint32_t>(p.num_k_blocks);
+        const uint32_t total_it = cluster_iterations(cluster_id, num_clusters, p);
         uint32_t s = 0, ph = 0;
         for (uint32_t it = 0; it < total_it; ++it) {
           if (!warp_wait(sfl_bar(s), ph, wctx, SITE_MMA_FULL)) break;
@@ -651,7 +735,7 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
     // (row0, col0): each row's four 16-byte chunks go to the staging tile in
     // the 64-byte swizzle (chunk j at j ^ ((row >> 1) & 3)), one lane issues
     // the tile store; the tensor map clips rows >= M and columns >= N.
-    auto store_tile16 = [&](int row0, int col0, const uint32_t(&h)[16]) {
+    auto stage_tile = [&](int row0, int col0, const uint32_t(&h)[16], bool reduce) {
       const uint32_t buf = epi_base + (epi_n % C::EPI_BUFS) * C::EPI_TILE_BYTES;
       if (epi_n >= static_cast<uint32_t>(C::EPI_BUFS)) {
         if (lane == 0) bulk_wait_group_read<C::EPI_BUFS - 1>();  // the buffer's last store has read it
@@ -664,19 +748,25 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
       fence_proxy_async_shared();
       __syncwarp();
       if (lane == 0) {
-        if (row0 < p.M) tma_store_2d(&p.tmap_d, buf, col0, row0);
+        if (row0 < p.M) {
+          if (reduce)
+            tma_reduce_add_2d(&p.tmap_w, buf, col0, row0);
+          else
+            tma_store_2d(&p.tmap_d, buf, col0, row0);
+        }
         bulk_commit_group();  // one group per staged tile (possibly empty), so the waits above count tiles
       }
       ++epi_n;
     };
+    auto store_tile16 = [&](int row0, int col0, const uint32_t(&h)[16]) { stage_tile(row0, col0, h, false); };
     uint32_t tcount = 0;
-    for (int t = cluster_id; t < p.num_tiles; t += num_clusters, ++tcount) {
+    for (UnitCursor uc = cursor_begin(cluster_id, num_clusters, p); uc.valid; cursor_next(uc, num_clusters, p), ++tcount) {
       const int b = static_cast<int>(tcount % ACC);
       const uint32_t aph = (tcount / ACC) & 1u;
       if (!warp_wait(accf_bar(b), aph, wctx, SITE_EPI_ACC_FULL)) break;
       tc_fence_after();
       int mt, nt;
-      tile_coords(t, p, mt, nt);
+      tile_coords(uc.tile, p, mt, nt);
       const int row0 = mt * C::MMA_M + static_cast<int>(rank) * C::BM + 32 * q;
       const int row = row0 + lane;
       const int n0 = nt * BN;
@@ -700,6 +790,117 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
           for (int k = 0; k < 16; ++k) h[k] = pack_f16(r[2 * k], r[2 * k + 1]);
         }
       };
+      if (uc.kb0 != 0 || uc.kb1 != p.num_k_blocks) {
+        // part of a tile (split-K or stream-K): add this unit's fp32 partial
+        // to the workspace (16-column halves of each 32-column chunk through
+        // the staging tiles), release the accumulator, then count; the unit
+        // that completes a (tile, CTA, warp) part last converts it from the
+        // workspace, clears it and resets the counter.  Quadrants whose rows
+        // all lie beyond M skip everything.
+        const bool rows_live = row0 < p.M;
+        if (rows_live) {
+#pragma unroll 1
+          for (int c = part; c < BN / 32; c += nparts) {
+            if (n0 + 32 * c >= p.N) break;
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(tb + 32 * c, r);
+            tc_wait_ld();
+            uint32_t h[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) h[k] = r[k];
+            stage_tile(row0, n0 + 32 * c, h, true);
+#pragma unroll
+            for (int k = 0; k < 16; ++k) h[k] = r[16 + k];
+            stage_tile(row0, n0 + 32 * c + 16, h, true);
+          }
+        }
+        release();
+        if (!rows_live) continue;
+        const int tile = uc.tile;
+        const int expected = tile_unit_count(tile, num_clusters, p);
+        // one counter per (tile, CTA of the pair, epilogue warp)
+        int* counter = p.counters + (static_cast<int64_t>(tile) * CG + rank) * 8 + (warp - 4);
+        int last = 0;
+        if (lane == 0) {
+          bulk_wait_group_all();       // this warp's reduce-adds are performed
+          fence_proxy_async_global();  // ... and ordered before the release below
+          __threadfence();
+          last = atomicAdd(counter, 1) == expected - 1;
+          if (last) *counter = 0;  // no other unit touches it again in this launch
+        }
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (last) {
+          __threadfence();  // acquire: every unit's additions are visible
+          // Convert this warp's rows (quadrant q: row0 .. row0+31, < M) and
+          // column chunks from the workspace, coalesced: one instruction
+          // covers 4 rows x 32 columns (8 lanes x 4 columns per row); 16-byte
+          // workspace loads, zeroing stores behind them.
+          const int sub_r = lane >> 3;         // row within a group of 4
+          const int sub_c = 4 * (lane & 7);    // first of this lane's 4 columns
+          const int nrows = min(32, p.M - row0);
+#pragma unroll 1
+          for (int c = part; c < BN / 32; c += nparts) {
+            const int col = n0 + 32 * c + sub_c;
+            if (n0 + 32 * c >= p.N) break;
+            const bool full4 = col + 3 < p.N;
+#pragma unroll 1
+            for (int rg = 0; rg < nrows; rg += 16) {
+              float4 v[4];
+#pragma unroll
+              for (int g = 0; g < 4; ++g) {
+                const int rr = rg + 4 * g + sub_r;
+                v[g] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (rr < nrows && col < p.N) {
+                  const float* src = p.w + static_cast<int64_t>(row0 + rr) * p.ldw + col;
+                  if (full4) {
+                    v[g] = __ldcg(reinterpret_cast<const float4*>(src));
+                  } else {
+                    v[g].x = __ldcg(src);
+                    if (col + 1 < p.N) v[g].y = __ldcg(src + 1);
+                    if (col + 2 < p.N) v[g].z = __ldcg(src + 2);
+                  }
+                }
+              }
+#pragma unroll
+              for (int g = 0; g < 4; ++g) {
+                const int rr = rg + 4 * g + sub_r;
+                if (rr >= nrows || col >= p.N) continue;
+                const int64_t grow = row0 + rr;
+                float* wsrc = p.w + grow * p.ldw + col;
+                const float vals[4] = {v[g].x, v[g].y, v[g].z, v[g].w};
+                if (p.d_type == OUT_F32) {
+                  float* dst = reinterpret_cast<float*>(p.D) + grow * p.ldd + col;
+                  if (full4 && p.d_vec_ok)
+                    *reinterpret_cast<float4*>(dst) = v[g];
+                  else
+                    for (int e = 0; e < 4; ++e)
+                      if (col + e < p.N) dst[e] = vals[e];
+                } else {
+                  uint16_t* dst = reinterpret_cast<uint16_t*>(p.D) + grow * p.ldd + col;
+                  const uint32_t lo = p.d_type == OUT_BF16 ? pack_bf16(__float_as_uint(vals[0]), __float_as_uint(vals[1]))
+                                                           : pack_f16(__float_as_uint(vals[0]), __float_as_uint(vals[1]));
+                  const uint32_t hi = p.d_type == OUT_BF16 ? pack_bf16(__float_as_uint(vals[2]), __float_as_uint(vals[3]))
+                                                           : pack_f16(__float_as_uint(vals[2]), __float_as_uint(vals[3]));
+                  if (full4 && p.d_vec_ok) {
+                    *reinterpret_cast<uint2*>(dst) = make_uint2(lo, hi);
+                  } else {
+                    const uint32_t w2[2] = {lo, hi};
+                    for (int e = 0; e < 4; ++e)
+                      if (col + e < p.N) dst[e] = static_cast<uint16_t>((w2[e >> 1] >> (16 * (e & 1))) & 0xFFFFu);
+                  }
+                }
+                if (full4) {
+                  __stcg(reinterpret_cast<float4*>(wsrc), make_float4(0.f, 0.f, 0.f, 0.f));
+                } else {
+                  for (int e = 0; e < 4; ++e)
+                    if (col + e < p.N) __stcg(wsrc + e, 0.0f);
+                }
+              }
+            }
+          }
+        }
+        continue;
+      }
       if (early) {
         constexpr int HALF = (BN / 32 + 1) / 2;  // chunks per warp
         uint32_t h[HALF][16];

@@ -121,6 +121,7 @@ extern "C" int tcg_gemm_mxf8_blockscaled_noalloc(int64_t M, int64_t N, int64_t K
   args.d_type = d_type;
   args.ldd = ldd;
   args.acc_type = acc_type;
+  args.split_k = 1;  // split-K would need the library's (allocated) workspace
   if (int rc = tcg_gemm(&args, stream)) return rc;
   tcg::set_launch_count(3);
   return TCG_OK;

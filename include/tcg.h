@@ -25,9 +25,11 @@
  * function says host) that must stay valid until the work queued on `stream`
  * has finished.  All calls are asynchronous on `stream` (a cudaStream_t; 0 is
  * the legacy default stream) and never synchronise the host, except
- * tcg_check().  The block-scaled GEMM with plain scale arrays uses a
- * library-owned device workspace per (device, stream), allocated on first use
- * and grown when needed; no other call allocates device memory.
+ * tcg_check().  The block-scaled GEMM with plain scale arrays, and split-K
+ * (see tcg_gemm_args::split_k; automatic for problems with few output tiles),
+ * use library-owned device workspaces per (device, stream), allocated on
+ * first use and grown when needed (growing frees the old one, which waits for
+ * the device); nothing else allocates device memory.
  *
  * Errors: every function returns TCG_OK (0) or a negative tcg_status.
  * Argument errors are detected on the host before anything is queued.
@@ -156,6 +158,16 @@ typedef struct {
                         2 = the MMA thread with tcgen05.cp .32x128b.warpx4
                             ("tcgen05.cp" page) before its MMAs,
                         3 = a dedicated thread with tcgen05.cp + commit */
+  int split_k;       /* K decomposition: 0 = auto (problems with fewer output
+                        tiles than the GPU runs at once, e.g. skinny M, use
+                        stream-K: every cluster takes an equal contiguous share
+                        of the (tile, K block) iterations), 1 = one pass per
+                        tile, n >= 2 = every tile split into n K ranges (capped
+                        at the number of 128-byte K blocks).  Tiles computed in
+                        parts meet in an fp32 workspace owned by the library
+                        per (device, stream); their sum order is not fixed, so
+                        results can differ in the last bits between runs.
+                        Ignored with TCG_F16 accumulation. */
 } tcg_gemm_args;
 
 int tcg_gemm(const tcg_gemm_args* args, void* stream);

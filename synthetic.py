@@ -60,6 +60,12 @@ WORKLOADS = {
                                  "normal", "f16", "f16", 2, False, 4),
     "mxf8_8192": Workload("mxf8_8192", 8192, 8192, 8192, "e4m3", "k", "k",
                           "normal1", "f32", "bf16", 2, True, 5),
+    # Skinny (decode-like) shapes: a few rows of activations against an
+    # 8192 x 8192 weight; bound by streaming B from HBM, reported in GB/s.
+    "bf16_skinny_m16": Workload("bf16_skinny_m16", 16, 8192, 8192, "bf16", "k", "k",
+                                "normal", "f32", "bf16", 1, False, 6),
+    "bf16_skinny_m128": Workload("bf16_skinny_m128", 128, 8192, 8192, "bf16", "k", "k",
+                                 "normal", "f32", "bf16", 1, False, 7),
 }
 
 

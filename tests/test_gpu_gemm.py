@@ -136,6 +136,39 @@ def test_blockscaled_pair_early_release(tcg, oracle_mod, staging, out):
     _check_full(tcg, oracle_mod, x, out, "f32", 2, sf_staging=staging)
 
 
+# Split-K: dtype, a_major, b_major, M, N, K, cta_group, out, split_k (0 = auto).
+# Auto splits when the output tiles fill at most half the GPU (all of these);
+# explicit splits that do not divide the K blocks give uneven K ranges.
+SPLIT = [
+    ("bf16", "k", "k", 16, 1000, 2048, 1, "bf16", 0),
+    ("bf16", "k", "mn", 1, 520, 1024, 1, "f32", 3),
+    ("bf16", "k", "k", 100, 300, 1000, 1, "bf16", 7),
+    ("bf16", "mn", "k", 200, 700, 1536, 2, "bf16", 4),
+    ("bf16", "k", "k", 256, 512, 4096, 2, "f16", 0),
+    ("f16", "k", "k", 128, 256, 2048, 1, "f16", 5),
+    ("tf32", "k", "k", 64, 300, 1024, 1, "f32", 4),
+    ("tf32", "mn", "k", 36, 130, 520, 1, "bf16", 0),
+    ("e4m3", "k", "k", 16, 520, 2048, 1, "bf16", 0),
+    ("e4m3", "k", "k", 300, 512, 1024, 2, "bf16", 3),
+    ("e4m3", "k", "mn", 64, 608, 4096, 2, "f32", 0),
+]
+
+
+@pytest.mark.parametrize("dtype,am,bm,M,N,K,cg,out,split", SPLIT)
+def test_split_k(tcg, oracle_mod, dtype, am, bm, M, N, K, cg, out, split):
+    x = make_case(dtype, am, bm, M, N, K, seed=7 * M + N + K)
+    # twice: the second call relies on the first leaving the workspace zero
+    for _ in range(2):
+        _check_full(tcg, oracle_mod, x, out, "f32", cg, split_k=split)
+
+
+def test_split_k_workspace_survives_shape_changes(tcg, oracle_mod):
+    # one stream, different shapes and splits back to back, then the first again
+    cases = [make_case("bf16", "k", "k", 16, 1000, 2048, seed=91), make_case("bf16", "k", "k", 120, 384, 3072, seed=92)]
+    for x, split in [(cases[0], 4), (cases[1], 6), (cases[0], 0), (cases[1], 2)]:
+        _check_full(tcg, oracle_mod, x, "bf16", "f32", 1, split_k=split)
+
+
 # rows, K, tile rows, byte offset of the plain scales, byte offset of the image.
 # K = 200 / 1000 (kblocks 7 / 32): byte loads / word loads (the row stride is
 # not a multiple of 16 bytes); K = 1024, 8192: 16-byte loads; offset scales:
@@ -232,7 +265,7 @@ def test_named_entry_points(tcg, oracle_mod):
 # ------------------------------------------------------------- full-size workloads
 
 FULL = ["tile_f16_128x128x64", "bf16_4096_kmn_cta1", "tf32_2048x2048x8192", "bf16_8192_cta2",
-        "f16acc_8192_cta2", "mxf8_8192"]
+        "f16acc_8192_cta2", "mxf8_8192", "bf16_skinny_m16", "bf16_skinny_m128"]
 
 
 @pytest.mark.parametrize("name", FULL)
