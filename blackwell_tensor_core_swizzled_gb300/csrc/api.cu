@@ -53,17 +53,14 @@ struct Workspace {
 };
 std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
 
-// Split-K workspace per (device, stream): fp32 partial sums and per-chunk
-// counters.  Zeroed when allocated; every call leaves the parts it used zero
-// again.  A device-side failure can leave it dirty, so tcg_check bumps
-// g_error_gen and a workspace zeroed under an older generation is re-zeroed.
+// Split-K / stream-K workspace per (device, stream): fp32 partial-tile slots,
+// written by the GEMM and read by the reduction kernel that follows it on the
+// same stream (their contents never need clearing).
 struct SplitWorkspace {
-  void* ptr = nullptr;
-  size_t bytes = 0;
-  uint64_t gen = 0;
+  void* slots = nullptr;
+  size_t slot_bytes = 0;
 };
 std::map<std::pair<int, cudaStream_t>, SplitWorkspace> g_split_ws;
-std::atomic<uint64_t> g_error_gen{1};
 
 void load_timeout_env() {
   static std::once_flag once;
@@ -135,6 +132,28 @@ int make_map_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int 
                   static_cast<int>(r), static_cast<unsigned long long>(inner),
                   static_cast<unsigned long long>(outer), static_cast<unsigned long long>(ld), box_inner, box_outer);
     t_last_error = buf;
+    return TCG_ERR_CUDA;
+  }
+  return TCG_OK;
+}
+
+// 3D map over a dense [outer][mid][inner] array (row strides inner*esize and
+// mid*inner*esize bytes).
+int make_map_3d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int esize, uint64_t inner,
+                uint64_t mid, uint64_t outer, uint32_t box_inner, uint32_t box_mid, CUtensorMapSwizzle sw) {
+  if (encode_ready() != TCG_OK) {
+    t_last_error = "cuTensorMapEncodeTiled entry point unavailable";
+    return TCG_ERR_CUDA;
+  }
+  const cuuint64_t dims[3] = {inner, mid, outer};
+  const cuuint64_t strides[2] = {inner * static_cast<uint64_t>(esize), inner * mid * static_cast<uint64_t>(esize)};
+  const cuuint32_t box[3] = {box_inner, box_mid, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = g_encode(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    t_last_error = "cuTensorMapEncodeTiled (3D) failed (" + std::to_string(static_cast<int>(r)) + ")";
     return TCG_ERR_CUDA;
   }
   return TCG_OK;
@@ -265,29 +284,26 @@ int workspace(int dev, cudaStream_t s, size_t bytes, void** out) {
   return TCG_OK;
 }
 
-int split_workspace(int dev, cudaStream_t s, size_t bytes, void** out) {
+int grow_buffer(void** ptr, size_t* have, size_t want) {
+  if (*have >= want) return TCG_OK;
+  if (*ptr) {
+    cudaError_t e = cudaFree(*ptr);  // synchronises: no queued kernel still uses it
+    *ptr = nullptr;
+    *have = 0;
+    if (e != cudaSuccess) return record_cuda(e);
+  }
+  const size_t bytes = std::max(want, static_cast<size_t>(1) << 20);
+  cudaError_t e = cudaMalloc(ptr, bytes);
+  if (e != cudaSuccess) return record_cuda(e);
+  *have = bytes;
+  return TCG_OK;
+}
+
+int split_workspace(int dev, cudaStream_t s, size_t slot_bytes, float** slots) {
   std::lock_guard<std::mutex> lk(g_mu);
   SplitWorkspace& w = g_split_ws[std::make_pair(dev, s)];
-  const uint64_t gen = g_error_gen.load();
-  if (w.bytes < bytes) {
-    if (w.ptr) {
-      cudaError_t e = cudaFree(w.ptr);  // synchronises: no queued kernel still uses it
-      w.ptr = nullptr;
-      w.bytes = 0;
-      if (e != cudaSuccess) return record_cuda(e);
-    }
-    const size_t want = std::max(bytes, static_cast<size_t>(1) << 20);
-    cudaError_t e = cudaMalloc(&w.ptr, want);
-    if (e != cudaSuccess) return record_cuda(e);
-    w.bytes = want;
-    w.gen = 0;
-  }
-  if (w.gen != gen) {
-    const cudaError_t e = cudaMemsetAsync(w.ptr, 0, w.bytes, s);
-    if (e != cudaSuccess) return record_cuda(e);
-    w.gen = gen;
-  }
-  *out = w.ptr;
+  if (int rc = grow_buffer(&w.slots, &w.slot_bytes, slot_bytes)) return rc;
+  *slots = static_cast<float*>(w.slots);
   return TCG_OK;
 }
 
@@ -496,23 +512,29 @@ int run_gemm(const tcg_gemm_args* args, cudaStream_t s) {
   prm.stream_k = stream_k ? 1 : 0;
   prm.num_units = prm.num_tiles * split;
   const int64_t iterations = static_cast<int64_t>(prm.num_tiles) * prm.num_k_blocks;
+  const int clusters = static_cast<int>(
+      std::max<int64_t>(1, std::min<int64_t>(stream_k ? iterations : prm.num_units, max_clusters)));
   if (split > 1 || stream_k) {
-    prm.ldw = cdiv(a.N, 4) * 4;
-    const size_t wbytes = static_cast<size_t>(cdiv(static_cast<int64_t>(a.M) * prm.ldw * 4, 256) * 256);
-    const size_t cbytes = static_cast<size_t>(prm.num_tiles) * cg * 8 * sizeof(int);
-    void* ws = nullptr;
-    if (int rc = split_workspace(dev, s, wbytes + cbytes, &ws)) return rc;
-    prm.w = static_cast<float*>(ws);
-    prm.counters = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + wbytes);
-    if (int rc = make_map_2d(&prm.tmap_w, prm.w, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, static_cast<uint64_t>(a.N),
-                             static_cast<uint64_t>(a.M), static_cast<uint64_t>(prm.ldw), 16, 32,
+    // partial-tile slots: under stream-K two per cluster (the two ends of its
+    // range), under split-K one per unit; each CG x min(128, M) x BN fp32
+    prm.w_rows = static_cast<int>(std::min<int64_t>(128, a.M));
+    const int64_t slots = stream_k ? 2 * static_cast<int64_t>(clusters) : static_cast<int64_t>(prm.num_units);
+    const int64_t wbytes = slots * cg * prm.w_rows * bn * 4;
+    if (int rc = split_workspace(dev, s, static_cast<size_t>(wbytes), &prm.w)) return rc;
+    prm.bn = bn;
+    if (int rc = make_map_3d(&prm.tmap_w, prm.w, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, static_cast<uint64_t>(bn),
+                             static_cast<uint64_t>(prm.w_rows), static_cast<uint64_t>(slots * cg), 16, 32,
                              CU_TENSOR_MAP_SWIZZLE_64B))
       return rc;
   }
-  const int clusters = static_cast<int>(
-      std::max<int64_t>(1, std::min<int64_t>(stream_k ? iterations : prm.num_units, max_clusters)));
   if (int rc = launch_gemm(ki, prm, clusters, s)) return rc;
-  t_last_launches = launches + 1;
+  launches += 1;
+  if (split > 1 || stream_k) {
+    const cudaError_t e = launch_splitk_reduce(prm, cg, clusters, s);
+    if (e != cudaSuccess) return record_cuda(e);
+    launches += 1;
+  }
+  t_last_launches = launches;
   return TCG_OK;
 }
 
@@ -670,10 +692,7 @@ int tcg_mxf8_prepare_scales_ab(const uint8_t* SFA, int64_t M, uint8_t* SFA_img, 
 
 int tcg_check(void* stream) {
   cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) {
-    g_error_gen.fetch_add(1);  // split-K workspaces may be dirty
-    return record_cuda(e);
-  }
+  if (e != cudaSuccess) return record_cuda(e);
   int dev = 0;
   e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return record_cuda(e);
@@ -683,7 +702,6 @@ int tcg_check(void* stream) {
   e = cudaMemcpy(&w, st->err, sizeof w, cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return record_cuda(e);
   if (w == 0) return TCG_OK;
-  g_error_gen.fetch_add(1);  // an aborted kernel may have left split-K workspaces dirty
   e = cudaMemset(st->err, 0, sizeof w);
   if (e != cudaSuccess) return record_cuda(e);
   char buf[128];

@@ -24,7 +24,7 @@ struct KernelInfo {
 // Variant getters (one per translation unit that instantiates kernels).
 KernelInfo kinfo_f16(int cta_group);
 KernelInfo kinfo_tf32(int cta_group);
-KernelInfo kinfo_mxf8(int cta_group);  // cta_group 2: BN 224, 2 accumulators; 1: BN 256, 1 accumulator
+KernelInfo kinfo_mxf8(int cta_group);  // BN 256, one accumulator (single CTA or CTA pair)
 
 // Scale-factor rearrangement kernel launch (gemm_mxf8.cu).
 cudaError_t launch_sf_prepare(const uint8_t* sf, int64_t rows, int64_t K, int tile_rows, uint8_t* img,
@@ -33,6 +33,10 @@ cudaError_t launch_sf_prepare(const uint8_t* sf, int64_t rows, int64_t K, int ti
 cudaError_t launch_sf_prepare_pair(const uint8_t* sfa, int64_t rows_a, int tile_a, uint8_t* img_a,
                                    const uint8_t* sfb, int64_t rows_b, int tile_b, uint8_t* img_b, int64_t K,
                                    cudaStream_t stream);
+
+// Sum of the partial-tile slots of a split-K / stream-K GEMM into D
+// (splitk_reduce.cu); launched after the GEMM on the same stream.
+cudaError_t launch_splitk_reduce(const GemmParams& p, int cg, int num_clusters, cudaStream_t stream);
 
 // Host state helpers (api.cu).
 int record_cuda(cudaError_t e);              // stores the message, returns TCG_ERR_CUDA (or TCG_OK)

@@ -77,17 +77,16 @@ struct GemmParams {
   CUtensorMap tmap_sfa;
   CUtensorMap tmap_sfb;
   CUtensorMap tmap_d;  // 16-bit D in 32 x 32 boxes, 64-byte swizzle (used when d_tma)
-  CUtensorMap tmap_w;  // fp32 split-K workspace [M][N] in 16 x 32 boxes, 64-byte swizzle
+  CUtensorMap tmap_w;  // fp32 partial-tile slots [slots][w_rows][BN] in 16 x 32 x 1 boxes, 64-byte swizzle
   int M, N, K;
   int num_m_tiles;   // tiles of 128*CG rows
   int num_n_tiles;   // tiles of BN columns
   int num_k_blocks;  // ring stages per tile (128 bytes of K each)
   // split-K: every output tile is computed by `split` units over consecutive
-  // K ranges; num_units = num_tiles * split.  With split > 1 the units add
-  // their fp32 partial tiles into the workspace `w` (TMA reduce-add through
-  // tmap_w, 16 x 32 boxes) and the last unit to finish a chunk (counted in
-  // `counters`, one per tile, CTA of a pair and epilogue warp) converts it to
-  // D and clears it.
+  // K ranges; num_units = num_tiles * split.  A unit that computes part of a
+  // tile stores its fp32 partial into its own slot of the workspace `w`
+  // ([slot * CG + rank][w_rows][BN], TMA stores through tmap_w in 16 x 32
+  // boxes); splitk_reduce_kernel then sums each tile's slots into D.
   int split;
   int num_units;
   // stream-K: cluster c takes the global (tile, k block) iterations
@@ -96,8 +95,8 @@ struct GemmParams {
   // directly, the others meet in the workspace like split-K units
   int stream_k;
   float* w;
-  int64_t ldw;  // workspace row stride (elements)
-  int* counters;
+  int w_rows;  // rows per slot: min(128, M)
+  int bn;      // tile columns (BN of the kernel variant)
   int num_tiles;
   int raster_group;
   int a_mn_major, b_mn_major;
@@ -258,8 +257,9 @@ __device__ __forceinline__ void tile_coords(int t, const GemmParams& p, int& mt,
 // per tile, unit u -> tile u / split (split > 1); or the cluster's stream-K
 // range of the global iteration space, cut at tile boundaries.
 struct UnitCursor {
-  int64_t i, i1;  // stream-K position and end
-  int u;          // strided unit index
+  int64_t i, i1;   // stream-K position and end
+  int u;           // strided unit index
+  int first_tile;  // stream-K: the tile the cluster's range starts in
   int tile, kb0, kb1;
   bool valid;
 };
@@ -288,6 +288,7 @@ __device__ __forceinline__ UnitCursor cursor_begin(int cluster_id, int num_clust
   c.i = cluster_id * T / num_clusters;
   c.i1 = (cluster_id + 1) * T / num_clusters;
   c.u = cluster_id;
+  c.first_tile = static_cast<int>(c.i / p.num_k_blocks);
   cursor_load(c, p);
   return c;
 }
@@ -311,6 +312,23 @@ __device__ __forceinline__ int tile_unit_count(int tile, int num_clusters, const
   const int64_t c0 = ((s0 + 1) * num_clusters - 1) / T;
   const int64_t c1 = ((s1 + 1) * num_clusters - 1) / T;
   return static_cast<int>(c1 - c0 + 1);
+}
+
+// Workspace slot of a partial unit: under stream-K a cluster has at most one
+// partial unit at each end of its range (head: its first tile, tail: any
+// later tile); under split-K the unit index.
+__device__ __forceinline__ int unit_slot(const UnitCursor& c, int cluster_id, const GemmParams& p) {
+  return p.stream_k ? 2 * cluster_id + (c.tile != c.first_tile ? 1 : 0) : c.u;
+}
+
+// Slot of the j-th unit (in K order) that contributes to `tile`.
+__device__ __forceinline__ int64_t tile_slot(int tile, int j, int num_clusters, const GemmParams& p) {
+  if (!p.stream_k) return static_cast<int64_t>(tile) * p.split + j;
+  const int64_t T = static_cast<int64_t>(p.num_tiles) * p.num_k_blocks;
+  const int64_t s0 = static_cast<int64_t>(tile) * p.num_k_blocks;
+  const int64_t cc = ((s0 + 1) * num_clusters - 1) / T + j;  // owner of the tile's first iteration, + j
+  const int first = static_cast<int>(cc * T / num_clusters / p.num_k_blocks);
+  return 2 * cc + (tile != first ? 1 : 0);
 }
 
 // Ring iterations (k blocks) of all units a cluster processes.
@@ -735,7 +753,8 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
     // (row0, col0): each row's four 16-byte chunks go to the staging tile in
     // the 64-byte swizzle (chunk j at j ^ ((row >> 1) & 3)), one lane issues
     // the tile store; the tensor map clips rows >= M and columns >= N.
-    auto stage_tile = [&](int row0, int col0, const uint32_t(&h)[16], bool reduce) {
+    // to_slot: (col0, row0, z) address the workspace slot map instead of D
+    auto stage_tile = [&](int row0, int col0, const uint32_t(&h)[16], bool to_slot, int z) {
       const uint32_t buf = epi_base + (epi_n % C::EPI_BUFS) * C::EPI_TILE_BYTES;
       if (epi_n >= static_cast<uint32_t>(C::EPI_BUFS)) {
         if (lane == 0) bulk_wait_group_read<C::EPI_BUFS - 1>();  // the buffer's last store has read it
@@ -748,17 +767,16 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
       fence_proxy_async_shared();
       __syncwarp();
       if (lane == 0) {
-        if (row0 < p.M) {
-          if (reduce)
-            tma_reduce_add_2d(&p.tmap_w, buf, col0, row0);
-          else
-            tma_store_2d(&p.tmap_d, buf, col0, row0);
+        if (to_slot) {
+          if (row0 < p.w_rows) tma_store_3d(&p.tmap_w, buf, col0, row0, z);
+        } else if (row0 < p.M) {
+          tma_store_2d(&p.tmap_d, buf, col0, row0);
         }
         bulk_commit_group();  // one group per staged tile (possibly empty), so the waits above count tiles
       }
       ++epi_n;
     };
-    auto store_tile16 = [&](int row0, int col0, const uint32_t(&h)[16]) { stage_tile(row0, col0, h, false); };
+    auto store_tile16 = [&](int row0, int col0, const uint32_t(&h)[16]) { stage_tile(row0, col0, h, false, 0); };
     uint32_t tcount = 0;
     for (UnitCursor uc = cursor_begin(cluster_id, num_clusters, p); uc.valid; cursor_next(uc, num_clusters, p), ++tcount) {
       const int b = static_cast<int>(tcount % ACC);
@@ -791,14 +809,14 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
         }
       };
       if (uc.kb0 != 0 || uc.kb1 != p.num_k_blocks) {
-        // part of a tile (split-K or stream-K): add this unit's fp32 partial
-        // to the workspace (16-column halves of each 32-column chunk through
-        // the staging tiles), release the accumulator, then count; the unit
-        // that completes a (tile, CTA, warp) part last converts it from the
-        // workspace, clears it and resets the counter.  Quadrants whose rows
-        // all lie beyond M skip everything.
-        const bool rows_live = row0 < p.M;
-        if (rows_live) {
+        // part of a tile (split-K or stream-K): store this unit's fp32
+        // partial into its own workspace slot (16-column halves of each
+        // 32-column chunk through the staging tiles) and release the
+        // accumulator; splitk_reduce_kernel, launched next on the stream,
+        // sums each tile's slots in a fixed order into D.  Quadrants whose
+        // rows all lie beyond M store nothing.
+        if (row0 < p.M) {
+          const int zslot = unit_slot(uc, cluster_id, p) * CG + static_cast<int>(rank);
 #pragma unroll 1
           for (int c = part; c < BN / 32; c += nparts) {
             if (n0 + 32 * c >= p.N) break;
@@ -808,97 +826,13 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
             uint32_t h[16];
 #pragma unroll
             for (int k = 0; k < 16; ++k) h[k] = r[k];
-            stage_tile(row0, n0 + 32 * c, h, true);
+            stage_tile(32 * q, 32 * c, h, true, zslot);
 #pragma unroll
             for (int k = 0; k < 16; ++k) h[k] = r[16 + k];
-            stage_tile(row0, n0 + 32 * c + 16, h, true);
+            stage_tile(32 * q, 32 * c + 16, h, true, zslot);
           }
         }
         release();
-        if (!rows_live) continue;
-        const int tile = uc.tile;
-        const int expected = tile_unit_count(tile, num_clusters, p);
-        // one counter per (tile, CTA of the pair, epilogue warp)
-        int* counter = p.counters + (static_cast<int64_t>(tile) * CG + rank) * 8 + (warp - 4);
-        int last = 0;
-        if (lane == 0) {
-          bulk_wait_group_all();       // this warp's reduce-adds are performed
-          fence_proxy_async_global();  // ... and ordered before the release below
-          __threadfence();
-          last = atomicAdd(counter, 1) == expected - 1;
-          if (last) *counter = 0;  // no other unit touches it again in this launch
-        }
-        last = __shfl_sync(0xffffffffu, last, 0);
-        if (last) {
-          __threadfence();  // acquire: every unit's additions are visible
-          // Convert this warp's rows (quadrant q: row0 .. row0+31, < M) and
-          // column chunks from the workspace, coalesced: one instruction
-          // covers 4 rows x 32 columns (8 lanes x 4 columns per row); 16-byte
-          // workspace loads, zeroing stores behind them.
-          const int sub_r = lane >> 3;         // row within a group of 4
-          const int sub_c = 4 * (lane & 7);    // first of this lane's 4 columns
-          const int nrows = min(32, p.M - row0);
-#pragma unroll 1
-          for (int c = part; c < BN / 32; c += nparts) {
-            const int col = n0 + 32 * c + sub_c;
-            if (n0 + 32 * c >= p.N) break;
-            const bool full4 = col + 3 < p.N;
-#pragma unroll 1
-            for (int rg = 0; rg < nrows; rg += 16) {
-              float4 v[4];
-#pragma unroll
-              for (int g = 0; g < 4; ++g) {
-                const int rr = rg + 4 * g + sub_r;
-                v[g] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (rr < nrows && col < p.N) {
-                  const float* src = p.w + static_cast<int64_t>(row0 + rr) * p.ldw + col;
-                  if (full4) {
-                    v[g] = __ldcg(reinterpret_cast<const float4*>(src));
-                  } else {
-                    v[g].x = __ldcg(src);
-                    if (col + 1 < p.N) v[g].y = __ldcg(src + 1);
-                    if (col + 2 < p.N) v[g].z = __ldcg(src + 2);
-                  }
-                }
-              }
-#pragma unroll
-              for (int g = 0; g < 4; ++g) {
-                const int rr = rg + 4 * g + sub_r;
-                if (rr >= nrows || col >= p.N) continue;
-                const int64_t grow = row0 + rr;
-                float* wsrc = p.w + grow * p.ldw + col;
-                const float vals[4] = {v[g].x, v[g].y, v[g].z, v[g].w};
-                if (p.d_type == OUT_F32) {
-                  float* dst = reinterpret_cast<float*>(p.D) + grow * p.ldd + col;
-                  if (full4 && p.d_vec_ok)
-                    *reinterpret_cast<float4*>(dst) = v[g];
-                  else
-                    for (int e = 0; e < 4; ++e)
-                      if (col + e < p.N) dst[e] = vals[e];
-                } else {
-                  uint16_t* dst = reinterpret_cast<uint16_t*>(p.D) + grow * p.ldd + col;
-                  const uint32_t lo = p.d_type == OUT_BF16 ? pack_bf16(__float_as_uint(vals[0]), __float_as_uint(vals[1]))
-                                                           : pack_f16(__float_as_uint(vals[0]), __float_as_uint(vals[1]));
-                  const uint32_t hi = p.d_type == OUT_BF16 ? pack_bf16(__float_as_uint(vals[2]), __float_as_uint(vals[3]))
-                                                           : pack_f16(__float_as_uint(vals[2]), __float_as_uint(vals[3]));
-                  if (full4 && p.d_vec_ok) {
-                    *reinterpret_cast<uint2*>(dst) = make_uint2(lo, hi);
-                  } else {
-                    const uint32_t w2[2] = {lo, hi};
-                    for (int e = 0; e < 4; ++e)
-                      if (col + e < p.N) dst[e] = static_cast<uint16_t>((w2[e >> 1] >> (16 * (e & 1))) & 0xFFFFu);
-                  }
-                }
-                if (full4) {
-                  __stcg(reinterpret_cast<float4*>(wsrc), make_float4(0.f, 0.f, 0.f, 0.f));
-                } else {
-                  for (int e = 0; e < 4; ++e)
-                    if (col + e < p.N) __stcg(wsrc + e, 0.0f);
-                }
-              }
-            }
-          }
-        }
         continue;
       }
       if (early) {

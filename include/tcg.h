@@ -163,11 +163,12 @@ typedef struct {
                         stream-K: every cluster takes an equal contiguous share
                         of the (tile, K block) iterations), 1 = one pass per
                         tile, n >= 2 = every tile split into n K ranges (capped
-                        at the number of 128-byte K blocks).  Tiles computed in
-                        parts meet in an fp32 workspace owned by the library
-                        per (device, stream); their sum order is not fixed, so
-                        results can differ in the last bits between runs.
-                        Ignored with TCG_F16 accumulation. */
+                        at the number of 128-byte K blocks).  Each unit that
+                        computes part of a tile stores an fp32 partial in a
+                        workspace owned by the library per (device, stream); a
+                        second kernel sums each tile's partials in K order
+                        (deterministic) into D.  Ignored with TCG_F16
+                        accumulation. */
 } tcg_gemm_args;
 
 int tcg_gemm(const tcg_gemm_args* args, void* stream);

@@ -157,7 +157,7 @@ SPLIT = [
 @pytest.mark.parametrize("dtype,am,bm,M,N,K,cg,out,split", SPLIT)
 def test_split_k(tcg, oracle_mod, dtype, am, bm, M, N, K, cg, out, split):
     x = make_case(dtype, am, bm, M, N, K, seed=7 * M + N + K)
-    # twice: the second call relies on the first leaving the workspace zero
+    # twice: the second call reuses the first one's workspace
     for _ in range(2):
         _check_full(tcg, oracle_mod, x, out, "f32", cg, split_k=split)
 
@@ -167,6 +167,9 @@ def test_split_k_workspace_survives_shape_changes(tcg, oracle_mod):
     cases = [make_case("bf16", "k", "k", 16, 1000, 2048, seed=91), make_case("bf16", "k", "k", 120, 384, 3072, seed=92)]
     for x, split in [(cases[0], 4), (cases[1], 6), (cases[0], 0), (cases[1], 2)]:
         _check_full(tcg, oracle_mod, x, "bf16", "f32", 1, split_k=split)
+        assert tcg.last_launch_count() == 2  # the GEMM and the partial-tile reduction
+    _check_full(tcg, oracle_mod, cases[1], "bf16", "f32", 1, split_k=1)
+    assert tcg.last_launch_count() == 1
 
 
 # rows, K, tile rows, byte offset of the plain scales, byte offset of the image.
