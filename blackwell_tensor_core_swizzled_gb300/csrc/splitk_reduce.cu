@@ -4,7 +4,9 @@
 // D.  One thread per (tile, CTA of a pair, row, 4 columns): 16-byte slot
 // loads (all slots of a thread are independent, so they overlap), an fp32
 // sum, the output conversion and one store.  Tiles computed whole by one
-// unit were stored to D directly and are skipped.
+// unit were stored to D directly and are skipped.  Launched as a programmatic
+// dependent of the GEMM (its launch overlaps the GEMM's last CTAs); it waits
+// for the GEMM's completion and memory flush before reading the slots.
 #include "common.h"
 #include "gemm_kernel.cuh"
 
@@ -12,6 +14,7 @@ namespace tcg {
 
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(const __grid_constant__ GemmParams p, int cg,
                                                             int num_clusters) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int q4 = p.bn / 4;
   const int64_t per_rank = static_cast<int64_t>(p.w_rows) * q4;
   const int64_t per_tile = cg * per_rank;
@@ -72,8 +75,16 @@ cudaError_t launch_splitk_reduce(const GemmParams& p, int cg, int num_clusters, 
   const int64_t blocks = (threads + 255) / 256;
   if (blocks <= 0) return cudaSuccess;
   if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
-  splitk_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p, cg, num_clusters);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel, p, cg, num_clusters);
 }
 
 }  // namespace tcg

@@ -63,9 +63,9 @@ WORKLOADS = {
     # Skinny (decode-like) shapes: a few rows of activations against an
     # 8192 x 8192 weight; bound by streaming B from HBM, reported in GB/s.
     "bf16_skinny_m16": Workload("bf16_skinny_m16", 16, 8192, 8192, "bf16", "k", "k",
-                                "normal", "f32", "bf16", 1, False, 6),
+                                "normal", "f32", "bf16", 1, False, 6, {"bound": "hbm"}),
     "bf16_skinny_m128": Workload("bf16_skinny_m128", 128, 8192, 8192, "bf16", "k", "k",
-                                 "normal", "f32", "bf16", 1, False, 7),
+                                 "normal", "f32", "bf16", 1, False, 7, {"bound": "hbm"}),
 }
 
 
