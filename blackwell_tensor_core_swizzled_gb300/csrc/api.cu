@@ -425,9 +425,12 @@ int run_gemm(const tcg_gemm_args* args, cudaStream_t s) {
   // M tiles per raster group (measured at 8192^3: 16 for 128-row tiles, 8 for
   // 256-row pair tiles, i.e. 2048 rows of A either way)
   prm.raster_group = a.raster_group > 0 ? a.raster_group : (cg == 1 ? 16 : 8);
-  if (int rc = setup_operand(a.A, a.in_type, a.a_major, a.M, a.K, a.lda, 128, &prm.tmap_a, &prm.a_mn_major,
+  // skinny single-CTA problems: the A box covers only the rows that exist
+  const int a_rows = (cg == 1 && a.a_major == TCG_K_MAJOR && a.M < 128) ? static_cast<int>(cdiv(a.M, 8) * 8) : 128;
+  if (int rc = setup_operand(a.A, a.in_type, a.a_major, a.M, a.K, a.lda, a_rows, &prm.tmap_a, &prm.a_mn_major,
                              &prm.a_boxes, &prm.a_box_mn, &prm.a_box_bytes, &prm.a_desc_hi, &prm.a_kstep))
     return rc;
+  prm.ab_tx_bytes = static_cast<uint32_t>((a_rows * 128 + (bn / cg) * 128) * cg);
   if (int rc = setup_operand(a.B, a.in_type, a.b_major, a.N, a.K, a.ldb, bn / cg, &prm.tmap_b, &prm.b_mn_major,
                              &prm.b_boxes, &prm.b_box_mn, &prm.b_box_bytes, &prm.b_desc_hi, &prm.b_kstep))
     return rc;

@@ -103,6 +103,10 @@ struct GemmParams {
   int a_boxes, b_boxes;  // TMA boxes per stage (1 for K-major)
   int a_box_mn, b_box_mn;  // M/N extent of one MN-major box
   uint32_t a_box_bytes, b_box_bytes;
+  // A and B bytes one stage brings in (both CTAs of a pair): the full tiles,
+  // except that a single-CTA K-major A with M < 128 loads only round_up(M, 8)
+  // rows (the rest of the smem tile is stale and feeds only rows >= M)
+  uint32_t ab_tx_bytes;
   uint64_t a_desc_hi, b_desc_hi;
   uint32_t a_kstep, b_kstep;  // descriptor start advance (bytes) per MMA K step
   uint32_t idesc;
@@ -477,7 +481,8 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
           if (elect_one()) {
           const uint32_t fb = (CG == 2) ? mapa_shared(full_bar(s), 0) : full_bar(s);
           const bool sf_on_full = KIND == KIND_MXF8 && p.sf_mode != SF_BY_WARPS;
-          if (rank == 0) mbar_arrive_expect_tx(full_bar(s), C::TX_BYTES + (sf_on_full ? C::SF_TX_BYTES * CG : 0));
+          if (rank == 0)
+            mbar_arrive_expect_tx(full_bar(s), p.ab_tx_bytes + (sf_on_full ? C::SF_TX_BYTES * CG : 0));
           const uint32_t sa = sbase + s * C::STAGE_BYTES;
           const uint32_t sb = sa + C::A_BYTES;
           const int k0 = kb * C::BK;
