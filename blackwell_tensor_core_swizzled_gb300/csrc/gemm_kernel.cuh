@@ -325,16 +325,6 @@ __device__ __forceinline__ int unit_slot(const UnitCursor& c, int cluster_id, co
   return p.stream_k ? 2 * cluster_id + (c.tile != c.first_tile ? 1 : 0) : c.u;
 }
 
-// Slot of the j-th unit (in K order) that contributes to `tile`.
-__device__ __forceinline__ int64_t tile_slot(int tile, int j, int num_clusters, const GemmParams& p) {
-  if (!p.stream_k) return static_cast<int64_t>(tile) * p.split + j;
-  const int64_t T = static_cast<int64_t>(p.num_tiles) * p.num_k_blocks;
-  const int64_t s0 = static_cast<int64_t>(tile) * p.num_k_blocks;
-  const int64_t cc = ((s0 + 1) * num_clusters - 1) / T + j;  // owner of the tile's first iteration, + j
-  const int first = static_cast<int>(cc * T / num_clusters / p.num_k_blocks);
-  return 2 * cc + (tile != first ? 1 : 0);
-}
-
 // Ring iterations (k blocks) of all units a cluster processes.
 __device__ __forceinline__ uint32_t cluster_iterations(int cluster_id, int num_clusters, const GemmParams& p) {
   uint32_t n = 0;

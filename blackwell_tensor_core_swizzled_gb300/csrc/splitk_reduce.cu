@@ -26,8 +26,21 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const __grid_constan
   r -= rank * per_rank;
   const int lrow = static_cast<int>(r / q4);
   const int c4 = static_cast<int>(r - static_cast<int64_t>(lrow) * q4);
-  const int n = tile_unit_count(tile, num_clusters, p);
-  if (n == 1 && p.split == 1) return;  // stream-K tile computed whole
+  // contributing units: `split` consecutive slots, or under stream-K the
+  // clusters c0 .. c0+n-1 whose ranges meet the tile; cluster c's slot is
+  // 2c for its head (its range starts inside this tile) else 2c+1 (start(c)
+  // = floor(c*T/G) < s0 exactly when c*T < s0*G)
+  int n = p.split;
+  int64_t c0 = 0, T = 0, s0g = 0;
+  if (p.stream_k) {
+    T = static_cast<int64_t>(p.num_tiles) * p.num_k_blocks;
+    const int64_t s0 = static_cast<int64_t>(tile) * p.num_k_blocks;
+    const int64_t G = num_clusters;
+    c0 = ((s0 + 1) * G - 1) / T;
+    n = static_cast<int>(((s0 + p.num_k_blocks) * G - 1) / T - c0 + 1);
+    s0g = s0 * G;
+    if (n == 1) return;  // computed whole, stored directly
+  }
   int mt, nt;
   tile_coords(tile, p, mt, nt);
   const int64_t row = static_cast<int64_t>(mt) * 128 * cg + 128 * rank + lrow;
@@ -36,7 +49,14 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const __grid_constan
   float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
   for (int j = 0; j < n; ++j) {
-    const int64_t z = tile_slot(tile, j, num_clusters, p) * cg + rank;
+    int64_t slot;
+    if (p.stream_k) {
+      const int64_t cc = c0 + j;
+      slot = 2 * cc + (cc * T < s0g ? 1 : 0);
+    } else {
+      slot = static_cast<int64_t>(tile) * p.split + j;
+    }
+    const int64_t z = slot * cg + rank;
     const float4 t = __ldcg(reinterpret_cast<const float4*>(p.w + (z * p.w_rows + lrow) * p.bn + 4 * c4));
     v.x += t.x;
     v.y += t.y;
