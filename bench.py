@@ -47,7 +47,8 @@ ESIZE = {"f16": 2, "bf16": 2, "tf32": 4, "e4m3": 1}
 # bf16/fp16 2.25, fp8 4.5 PFLOP/s)
 NOMINAL_RATIO = {"bf16": 1.0, "f16": 1.0, "tf32": 1.1 / 2.25, "e4m3": 2.0}
 PROFILE_DIR = os.path.join(ROOT, "profiles")
-KERNEL_SOURCES = ["gemm_kernel.cuh", "ptx.cuh", "desc.cuh", "gemm_f16.cu", "gemm_tf32.cu", "gemm_mxf8.cu", "api.cu"]
+KERNEL_SOURCES = ["gemm_kernel.cuh", "ptx.cuh", "desc.cuh", "gemm_f16.cu", "gemm_tf32.cu", "gemm_mxf8.cu", "api.cu",
+                  "splitk_reduce.cu"]
 
 
 def kernel_source_hash() -> str:
