@@ -56,10 +56,13 @@ SMALL = [
 ]
 
 
+@pytest.mark.parametrize("split_k", [0, 1])
 @pytest.mark.parametrize("dtype,am,bm,M,N,K,cg,out,acc", SMALL)
-def test_small_ragged_full_compare(tcg, oracle_mod, dtype, am, bm, M, N, K, cg, out, acc):
+def test_small_ragged_full_compare(tcg, oracle_mod, dtype, am, bm, M, N, K, cg, out, acc, split_k):
+    # split_k 0: these problems have fewer tiles than clusters, so (with at
+    # least 8 K blocks) they run stream-K; split_k 1: one pass per tile
     x = make_case(dtype, am, bm, M, N, K, seed=M + N + K)
-    _check_full(tcg, oracle_mod, x, out, acc, cg)
+    _check_full(tcg, oracle_mod, x, out, acc, cg, split_k=split_k)
 
 
 def test_identity_gives_b_exactly(tcg, oracle_mod):
