@@ -369,7 +369,7 @@ int run_gemm(const tcg_gemm_args* args, cudaStream_t s) {
   if (a.acc_type == TCG_BF16) return TCG_ERR_UNSUPPORTED;
   if (a.acc_type == TCG_F16 && (a.in_type != TCG_IN_F16 || a.d_type != TCG_F16)) return TCG_ERR_UNSUPPORTED;
   if (a.cta_group < 0 || a.cta_group > 2 || a.raster_group < 0 || a.sf_staging < 0 || a.sf_staging > 3 ||
-      a.split_k < 0)
+      a.split_k < -1)
     return TCG_ERR_INVALID;
   if (a.M > INT32_MAX / 2 || a.N > INT32_MAX / 2 || a.K > INT32_MAX / 2) return TCG_ERR_UNSUPPORTED;
   if (a.M == 0 || a.N == 0) return TCG_OK;
@@ -498,17 +498,25 @@ int run_gemm(const tcg_gemm_args* args, cudaStream_t s) {
   int max_clusters = 0;
   if (int rc = max_clusters_for(d, ki, &max_clusters)) return rc;
 
-  // Problems with fewer output tiles than clusters (skinny M or N) would
-  // leave SMs idle: by default they run stream-K (each cluster takes an equal
-  // contiguous share of the (tile, k block) iterations; tiles cut between
-  // clusters meet in an fp32 workspace).  split_k >= 2 asks for a fixed split
-  // of every tile instead.  f16 accumulation keeps its single-pass path.
+  // Problems with few output tiles (skinny M or N) leave most SMs idle: by
+  // default they run stream-K (each cluster takes an equal contiguous share
+  // of the (tile, k block) iterations; tiles cut between clusters meet in an
+  // fp32 workspace and a second kernel).  That costs a few microseconds and a
+  // second epilogue per cluster, so it is used only when the tiles fill at
+  // most a quarter of the clusters and the idle share times the K blocks is
+  // at least 60 (measured: 16 x 8192 x 8192 and 64 x 4096 x 16384 gain;
+  // 128 x 16384 x 4096, 512 x 4096 x 4096 and 2048^2 x 2048..8192 lose).
+  // split_k >= 2 asks for a fixed split of every tile instead.  f16
+  // accumulation keeps its single-pass path.
   int split = 1;
   bool stream_k = false;
   if (a.acc_type != TCG_F16) {
     if (a.split_k > 1)
       split = static_cast<int>(std::min<int64_t>(a.split_k, prm.num_k_blocks));
-    else if (a.split_k == 0 && prm.num_tiles < max_clusters && prm.num_k_blocks >= 8)
+    else if (a.split_k == -1)
+      stream_k = true;
+    else if (a.split_k == 0 && 4 * static_cast<int64_t>(prm.num_tiles) <= max_clusters &&
+             static_cast<int64_t>(max_clusters - prm.num_tiles) * prm.num_k_blocks >= 60LL * max_clusters)
       stream_k = true;
   }
   prm.split = split;

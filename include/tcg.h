@@ -158,10 +158,11 @@ typedef struct {
                         2 = the MMA thread with tcgen05.cp .32x128b.warpx4
                             ("tcgen05.cp" page) before its MMAs,
                         3 = a dedicated thread with tcgen05.cp + commit */
-  int split_k;       /* K decomposition: 0 = auto (problems with fewer output
-                        tiles than the GPU runs at once, e.g. skinny M, use
-                        stream-K: every cluster takes an equal contiguous share
-                        of the (tile, K block) iterations), 1 = one pass per
+  int split_k;       /* K decomposition: 0 = auto (problems whose output tiles
+                        fill at most a quarter of the GPU and have a long K,
+                        e.g. skinny M, use stream-K: every cluster takes an
+                        equal contiguous share of the (tile, K block)
+                        iterations), -1 = stream-K, 1 = one pass per
                         tile, n >= 2 = every tile split into n K ranges (capped
                         at the number of 128-byte K blocks).  Each unit that
                         computes part of a tile stores an fp32 partial in a

@@ -59,6 +59,9 @@ def test_host_validation_rejects_bad_arguments(tcg):
     assert _call(tcg, "bf16", acc=1, dt=1) == tcg.ERR_UNSUPPORTED   # bf16 with f16 accumulation
     assert _call(tcg, "f16", acc=1, dt=2) == tcg.ERR_UNSUPPORTED    # f16 accumulation needs f16 out
     assert _call(tcg, "tf32", dt=5) == tcg.ERR_INVALID
+    # generic entry point: split_k below -1 (stream-K) is not a mode
+    rc = tcg.gemm(256, 256, 64, 1, 0x10000, 0, 0, 0x20000, 0, 0, 0x30000, 2, 0, 0, split_k=-2, stream=0, check=False)
+    assert rc == tcg.ERR_INVALID
     # mxf8 without scales
     rc = tcg.raw_call("tcg_gemm_mxf8_blockscaled", 64, 64, 64, 0x10000, 0, 0, 0x20000, 0, 0, None, None,
                       0x30000, 2, 0, 0, None)

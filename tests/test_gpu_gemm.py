@@ -59,8 +59,8 @@ SMALL = [
 @pytest.mark.parametrize("split_k", [0, 1])
 @pytest.mark.parametrize("dtype,am,bm,M,N,K,cg,out,acc", SMALL)
 def test_small_ragged_full_compare(tcg, oracle_mod, dtype, am, bm, M, N, K, cg, out, acc, split_k):
-    # split_k 0: these problems have fewer tiles than clusters, so (with at
-    # least 8 K blocks) they run stream-K; split_k 1: one pass per tile
+    # split_k 0: the library's choice (one pass for these); 1: one pass
+    # per tile requested explicitly
     x = make_case(dtype, am, bm, M, N, K, seed=M + N + K)
     _check_full(tcg, oracle_mod, x, out, acc, cg, split_k=split_k)
 
@@ -139,21 +139,24 @@ def test_blockscaled_pair_early_release(tcg, oracle_mod, staging, out):
     _check_full(tcg, oracle_mod, x, out, "f32", 2, sf_staging=staging)
 
 
-# Split-K: dtype, a_major, b_major, M, N, K, cta_group, out, split_k (0 = auto).
-# Auto splits when the output tiles fill at most half the GPU (all of these);
-# explicit splits that do not divide the K blocks give uneven K ranges.
+# Split-K / stream-K: dtype, a_major, b_major, M, N, K, cta_group, out,
+# split_k (-1 = stream-K, 0 = the library's choice, n >= 2 = fixed split).
+# Explicit splits that do not divide the K blocks give uneven K ranges; the
+# auto cases are long-K few-tile problems for which the library picks stream-K.
 SPLIT = [
-    ("bf16", "k", "k", 16, 1000, 2048, 1, "bf16", 0),
+    ("bf16", "k", "k", 16, 1000, 2048, 1, "bf16", -1),
+    ("bf16", "k", "k", 16, 1000, 8192, 1, "bf16", 0),
     ("bf16", "k", "mn", 1, 520, 1024, 1, "f32", 3),
     ("bf16", "k", "k", 100, 300, 1000, 1, "bf16", 7),
-    ("bf16", "mn", "k", 200, 700, 1536, 2, "bf16", 4),
-    ("bf16", "k", "k", 256, 512, 4096, 2, "f16", 0),
+    ("bf16", "mn", "k", 200, 700, 1536, 2, "bf16", -1),
+    ("bf16", "k", "k", 256, 512, 4096, 2, "f16", -1),
     ("f16", "k", "k", 128, 256, 2048, 1, "f16", 5),
     ("tf32", "k", "k", 64, 300, 1024, 1, "f32", 4),
-    ("tf32", "mn", "k", 36, 130, 520, 1, "bf16", 0),
-    ("e4m3", "k", "k", 16, 520, 2048, 1, "bf16", 0),
+    ("tf32", "mn", "k", 36, 130, 520, 1, "bf16", -1),
+    ("e4m3", "k", "k", 16, 520, 2048, 1, "bf16", -1),
+    ("e4m3", "k", "k", 16, 520, 16384, 1, "bf16", 0),
     ("e4m3", "k", "k", 300, 512, 1024, 2, "bf16", 3),
-    ("e4m3", "k", "mn", 64, 608, 4096, 2, "f32", 0),
+    ("e4m3", "k", "mn", 64, 608, 4096, 2, "f32", -1),
 ]
 
 
@@ -168,7 +171,7 @@ def test_split_k(tcg, oracle_mod, dtype, am, bm, M, N, K, cg, out, split):
 def test_split_k_workspace_survives_shape_changes(tcg, oracle_mod):
     # one stream, different shapes and splits back to back, then the first again
     cases = [make_case("bf16", "k", "k", 16, 1000, 2048, seed=91), make_case("bf16", "k", "k", 120, 384, 3072, seed=92)]
-    for x, split in [(cases[0], 4), (cases[1], 6), (cases[0], 0), (cases[1], 2)]:
+    for x, split in [(cases[0], 4), (cases[1], 6), (cases[0], -1), (cases[1], 2)]:
         _check_full(tcg, oracle_mod, x, "bf16", "f32", 1, split_k=split)
         assert tcg.last_launch_count() == 2  # the GEMM and the partial-tile reduction
     _check_full(tcg, oracle_mod, cases[1], "bf16", "f32", 1, split_k=1)
