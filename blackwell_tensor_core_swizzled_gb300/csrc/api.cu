@@ -190,7 +190,10 @@ int get_plan(const tcg_gemm_args& a, Plan* plan) {
   plan->cta_group = cg;
   switch (a.in_type) {
     case TCG_IN_F16:
-    case TCG_IN_BF16: plan->ki = kinfo_f16(cg); break;
+    case TCG_IN_BF16:
+      // skinny (M <= 32): 64-column tiles, 32 staged A rows, 16-stage ring
+      plan->ki = kinfo_f16(cg, cg == 1 && a.M <= 32 && a.a_major == TCG_K_MAJOR);
+      break;
     case TCG_IN_TF32: plan->ki = kinfo_tf32(cg); break;
     case TCG_IN_E4M3: plan->ki = kinfo_mxf8(cg); break;
     default: return TCG_ERR_INVALID;

@@ -22,7 +22,7 @@ struct KernelInfo {
 };
 
 // Variant getters (one per translation unit that instantiates kernels).
-KernelInfo kinfo_f16(int cta_group);
+KernelInfo kinfo_f16(int cta_group, bool skinny = false);
 KernelInfo kinfo_tf32(int cta_group);
 KernelInfo kinfo_mxf8(int cta_group);  // BN 256, one accumulator (single CTA or CTA pair)
 

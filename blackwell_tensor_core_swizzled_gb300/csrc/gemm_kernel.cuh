@@ -130,11 +130,15 @@ struct GemmParams {
   int sf_mode;
 };
 
-template <int CG, int BN, int ACC, int STAGES, int KIND>
+// A_ROWS < 128 (single CTA, K-major A, M <= A_ROWS): only that many rows of
+// A are staged per ring stage, so many more stages fit; the MMA still reads a
+// 128-row operand, whose rows beyond A_ROWS are whatever follows in shared
+// memory and only feed accumulator rows >= M, which are never stored.
+template <int CG, int BN, int ACC, int STAGES, int KIND, int A_ROWS = 128>
 struct GemmCfg {
   static constexpr int BM = 128;            // accumulator rows per CTA
   static constexpr int BN_LOCAL = BN / CG;  // B rows staged per CTA
-  static constexpr int A_BYTES = BM * 128;
+  static constexpr int A_BYTES = A_ROWS * 128;
   static constexpr int B_BYTES = BN_LOCAL * 128;
   static constexpr int SFB_CHUNKS = (BN + 127) / 128;
   static constexpr int SFA_BYTES = KIND == KIND_MXF8 ? 512 : 0;
@@ -186,6 +190,10 @@ struct GemmCfg {
   static_assert(KIND != KIND_MXF8 || (SF_SLOTS >= 1 && SF_SLOTS <= STAGES), "scale slots");
   static_assert(KIND != KIND_MXF8 || SFB_CHUNKS * 4 + 4 <= SF_SLOT_COLS, "scale slot too small");
   static_assert(SMEM_BYTES <= 232448, "dynamic shared memory");
+  static_assert(A_ROWS % 8 == 0 && A_ROWS <= 128 && (A_ROWS == 128 || CG == 1), "staged A rows");
+  // the MMA's 128-row read of the last stage's A tile stays inside the
+  // allocation (it runs into that stage's B tile and the epilogue staging)
+  static_assert(BAR_OFF - (STAGES - 1) * STAGE_BYTES >= BM * 128, "A over-read in bounds");
 };
 
 struct WaitCtx {
@@ -385,9 +393,9 @@ __device__ __forceinline__ void store_row32(const GemmParams& p, int row, int co
   }
 }
 
-template <int CG, int BN, int ACC, int STAGES, int KIND>
+template <int CG, int BN, int ACC, int STAGES, int KIND, int A_ROWS = 128>
 __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
-  using C = GemmCfg<CG, BN, ACC, STAGES, KIND>;
+  using C = GemmCfg<CG, BN, ACC, STAGES, KIND, A_ROWS>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;

@@ -48,6 +48,9 @@ SMALL = [
     ("tf32", "mn", "mn", 260, 300, 72, 2, "f32", "f32"),
     ("tf32", "k", "mn", 128, 256, 128, 1, "f32", "f32"),
     ("tf32", "mn", "k", 384, 256, 96, 2, "bf16", "f32"),
+    ("bf16", "k", "k", 20, 700, 1000, 1, "bf16", "f32"),   # skinny variant: 32 staged A rows, 64-wide tiles
+    ("f16", "k", "mn", 32, 520, 640, 1, "f16", "f16"),
+    ("bf16", "k", "k", 1, 300, 200, 0, "f32", "f32"),
     ("e4m3", "k", "k", 300, 520, 256, 2, "bf16", "f32"),
     ("e4m3", "k", "k", 300, 520, 208, 1, "f32", "f32"),
     ("e4m3", "k", "k", 512, 448, 512, 2, "bf16", "f32"),
