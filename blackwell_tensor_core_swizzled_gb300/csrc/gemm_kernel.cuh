@@ -145,9 +145,8 @@ struct GemmCfg {
   static constexpr int SFB_BYTES = KIND == KIND_MXF8 ? 512 * SFB_CHUNKS : 0;
   static constexpr int LOAD_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
   static constexpr int STAGE_BYTES = (LOAD_BYTES + 1023) / 1024 * 1024;
-  // bytes the pair leader's full barrier counts (A and B of both CTAs); the
-  // scale images complete on each CTA's own scale barrier
-  static constexpr int TX_BYTES = (A_BYTES + B_BYTES) * CG;
+  // scale-image bytes of one stage (counted on the pair leader's full
+  // barrier for both CTAs, or on each CTA's sf_loaded barrier)
   static constexpr int SF_TX_BYTES = SFA_BYTES + SFB_BYTES;
   static constexpr int MMA_M = 128 * CG;
   static constexpr int MMA_K = KIND == KIND_F16 ? 16 : KIND == KIND_TF32 ? 8 : 32;
@@ -223,16 +222,6 @@ static __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, 
       return false;
     }
   }
-}
-
-// Single-thread wait: the common already-complete case stays inline, the
-// bounded slow path is a call.  The producer and MMA roles run on one thread
-// each, so their per-stage loop is this test, a few address adds and the
-// issues (a warp-wide wait + vote + warp sync per stage costs more issue time
-// than a 512-cycle stage of MMAs can hide).
-__device__ __forceinline__ bool thread_wait(uint32_t bar, uint32_t parity, const WaitCtx& w, uint32_t site) {
-  if (mbar_try_wait(bar, parity)) return true;
-  return wait_bounded(bar, parity, w, site);
 }
 
 // Every lane waits (each gets its own acquire), the outcome is made uniform
@@ -311,19 +300,6 @@ __device__ __forceinline__ void cursor_next(UnitCursor& c, int num_clusters, con
   else
     c.u += num_clusters;
   cursor_load(c, p);
-}
-
-// Number of units that contribute to `tile` (the arrivals its reduction
-// counts): `split`, or under stream-K the clusters whose ranges meet it.
-__device__ __forceinline__ int tile_unit_count(int tile, int num_clusters, const GemmParams& p) {
-  if (!p.stream_k) return p.split;
-  const int64_t T = static_cast<int64_t>(p.num_tiles) * p.num_k_blocks;
-  const int64_t s0 = static_cast<int64_t>(tile) * p.num_k_blocks;
-  const int64_t s1 = s0 + p.num_k_blocks - 1;
-  // cluster owning iteration i: the largest c with c*T/G <= i
-  const int64_t c0 = ((s0 + 1) * num_clusters - 1) / T;
-  const int64_t c1 = ((s1 + 1) * num_clusters - 1) / T;
-  return static_cast<int>(c1 - c0 + 1);
 }
 
 // Workspace slot of a partial unit: under stream-K a cluster has at most one
