@@ -29,7 +29,13 @@
  * (see tcg_gemm_args::split_k; automatic for problems with few output tiles),
  * use library-owned device workspaces per (device, stream), allocated on
  * first use and grown when needed (growing frees the old one, which waits for
- * the device); nothing else allocates device memory.
+ * the device); nothing else allocates device memory.  Calls on different
+ * streams use different workspaces and may run concurrently.  A call may be
+ * captured into a CUDA graph once an earlier call on the same stream has
+ * allocated a workspace at least as large (a workspace that would have to
+ * grow during capture fails the call with TCG_ERR_CUDA); the graph reuses
+ * that stream's workspace, so its replays must be ordered with that stream's
+ * other split-K / block-scaled work.
  *
  * Errors: every function returns TCG_OK (0) or a negative tcg_status.
  * Argument errors are detected on the host before anything is queued.
