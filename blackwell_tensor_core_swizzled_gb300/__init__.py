@@ -53,6 +53,7 @@ _SIGS = {
     "tcg_status_string": ([_i32], ctypes.c_char_p),
     "tcg_last_error_string": ([], ctypes.c_char_p),
     "tcg_last_launch_count": ([], _i32),
+    "tcg_last_plan_string": ([], ctypes.c_char_p),
     "tcg_probe_tmem_roundtrip": ([_vp, _vp, _i32, _vp], _i32),
     "tcg_probe_cp": ([_vp, _i32, _i32, _u32, _u32, _u32, _i32, _vp, _vp], _i32),
     "tcg_probe_ld_shape": ([_vp, _i32, _i32, _i32, _vp, _vp], _i32),
@@ -200,6 +201,10 @@ def last_error_string() -> str:
 
 def last_launch_count() -> int:
     return _lib.tcg_last_launch_count()
+
+
+def last_plan_string() -> str:
+    return _lib.tcg_last_plan_string().decode()
 
 
 def probe_tmem_roundtrip(inp, out, ncols, stream=None):

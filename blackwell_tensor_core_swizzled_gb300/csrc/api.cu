@@ -28,6 +28,7 @@ namespace {
 
 thread_local std::string t_last_error;
 thread_local int t_last_launches = 0;
+thread_local std::string t_last_plan;
 std::atomic<uint64_t> g_timeout_ns{2000000000ull};
 
 constexpr int kMaxDevices = 64;
@@ -191,8 +192,12 @@ int get_plan(const tcg_gemm_args& a, Plan* plan) {
   switch (a.in_type) {
     case TCG_IN_F16:
     case TCG_IN_BF16:
-      // skinny (M <= 32): 64-column tiles, 32 staged A rows, 16-stage ring
-      plan->ki = kinfo_f16(cg, cg == 1 && a.M <= 32 && a.a_major == TCG_K_MAJOR);
+      // narrow (N <= 32, K-major B): 32-column tiles; skinny (M <= 32, K-major
+      // A): 64-column tiles staging 32 rows of A
+      plan->ki = kinfo_f16(cg, cg != 1                                       ? F16_WIDE
+                               : a.N <= 32 && a.b_major == TCG_K_MAJOR       ? F16_NARROW_N
+                               : a.M <= 32 && a.a_major == TCG_K_MAJOR       ? F16_SKINNY_M
+                                                                             : F16_WIDE);
       break;
     case TCG_IN_TF32: plan->ki = kinfo_tf32(cg); break;
     case TCG_IN_E4M3: plan->ki = kinfo_mxf8(cg); break;
@@ -363,6 +368,7 @@ int setup_operand(const void* ptr, tcg_input it, tcg_major major, int64_t mn, in
 int run_gemm(const tcg_gemm_args* args, cudaStream_t s) {
   load_timeout_env();
   t_last_launches = 0;
+  t_last_plan.clear();
   if (!args) return TCG_ERR_INVALID;
   tcg_gemm_args a = *args;
   if (a.M < 0 || a.N < 0 || a.K < 0) return TCG_ERR_INVALID;
@@ -409,9 +415,34 @@ int run_gemm(const tcg_gemm_args* args, cudaStream_t s) {
                                             static_cast<size_t>(a.M), s);
     if (e != cudaSuccess) return record_cuda(e);
     t_last_launches = 1;
+    t_last_plan = "K = 0: D zeroed";
     return TCG_OK;
   }
 
+  // Few rows of A against very many columns of B (decode-like shapes whose
+  // 64-column skinny tiles would take more than one wave): compute the
+  // transposed product D^T = B^T A^T with the operands' roles swapped, so
+  // that B fills the 128-row MMA side (half as many tiles, one pass each); the
+  // few rows of A become a 32-column tile and the epilogue stores the result
+  // transposed.  Measured on 16-row problems: 16 x 16384 x 4096 35.5 us
+  // swapped vs 39.6 us skinny; 16 x 8192 x 8192 38.6 us skinny (128 tiles, one
+  // pass) vs 40.6 us swapped (64 tiles: stream-K).  f32 accumulation, single
+  // CTAs, K-major A.
+  const bool d_trans = !scaled && a.in_type != TCG_IN_TF32 && a.acc_type == TCG_F32 && plan.cta_group == 1 &&
+                       a.M <= 32 && a.a_major == TCG_K_MAJOR && cdiv(a.N, 64) > d->sms;
+  if (d_trans) {
+    tcg_gemm_args t = a;
+    t.M = a.N;
+    t.N = a.M;
+    t.A = a.B;
+    t.a_major = a.b_major;
+    t.lda = a.ldb;
+    t.B = a.A;
+    t.b_major = TCG_K_MAJOR;
+    t.ldb = a.lda;
+    a = t;
+    if (int rc = get_plan(a, &plan)) return rc;
+  }
   const KernelInfo& ki = plan.ki;
   const int cg = plan.cta_group;
   const int bn = ki.bn;
@@ -452,7 +483,8 @@ int run_gemm(const tcg_gemm_args* args, cudaStream_t s) {
   // 16-bit outputs leave through TMA tile stores when the map's alignment
   // rules hold (16-byte base and row stride); otherwise per-thread row stores
   prm.d_tma = 0;
-  if (a.d_type != TCG_F32 && prm.d_vec_ok) {
+  prm.d_trans = d_trans ? 1 : 0;
+  if (a.d_type != TCG_F32 && prm.d_vec_ok && !d_trans) {
     const CUtensorMapDataType dt = a.d_type == TCG_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     if (int rc = make_map_2d(&prm.tmap_d, a.D, dt, 2, static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.M),
                              static_cast<uint64_t>(a.ldd), 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
@@ -508,7 +540,10 @@ int run_gemm(const tcg_gemm_args* args, cudaStream_t s) {
   // second epilogue per cluster, so it is used only when the tiles fill at
   // most a quarter of the clusters and the idle share times the K blocks is
   // at least 60 (measured: 16 x 8192 x 8192 and 64 x 4096 x 16384 gain;
-  // 128 x 16384 x 4096, 512 x 4096 x 4096 and 2048^2 x 2048..8192 lose).
+  // 128 x 16384 x 4096, 512 x 4096 x 4096 and 2048^2 x 2048..8192 lose).  The
+  // narrow (32-column) and skinny (64-column) tiles carry so little work per
+  // tile that half the clusters suffice (16 x 4096 x 16384: 41 us stream-K vs
+  // 60 us one pass; 8192 x 16 x 8192: 40 vs 58 us).
   // split_k >= 2 asks for a fixed split of every tile instead.  f16
   // accumulation keeps its single-pass path.
   int split = 1;
@@ -518,7 +553,7 @@ int run_gemm(const tcg_gemm_args* args, cudaStream_t s) {
       split = static_cast<int>(std::min<int64_t>(a.split_k, prm.num_k_blocks));
     else if (a.split_k == -1)
       stream_k = true;
-    else if (a.split_k == 0 && 4 * static_cast<int64_t>(prm.num_tiles) <= max_clusters &&
+    else if (a.split_k == 0 && (bn <= 64 ? 2 : 4) * static_cast<int64_t>(prm.num_tiles) <= max_clusters &&
              static_cast<int64_t>(max_clusters - prm.num_tiles) * prm.num_k_blocks >= 60LL * max_clusters)
       stream_k = true;
   }
@@ -549,6 +584,12 @@ int run_gemm(const tcg_gemm_args* args, cudaStream_t s) {
     launches += 1;
   }
   t_last_launches = launches;
+  char buf[160];
+  std::snprintf(buf, sizeof buf, "cta_group %d, tile %dx%d%s, %d clusters, %s%s", cg, 128 * cg, bn,
+                d_trans ? " (operands swapped, D stored transposed)" : "", clusters,
+                stream_k ? "stream-K" : split > 1 ? "split-K " : "one pass per tile",
+                split > 1 ? std::to_string(split).c_str() : "");
+  t_last_plan = buf;
   return TCG_OK;
 }
 
@@ -745,5 +786,7 @@ const char* tcg_status_string(int status) {
 const char* tcg_last_error_string(void) { return t_last_error.c_str(); }
 
 int tcg_last_launch_count(void) { return t_last_launches; }
+
+const char* tcg_last_plan_string(void) { return t_last_plan.c_str(); }
 
 }  // extern "C"

@@ -22,7 +22,8 @@ struct KernelInfo {
 };
 
 // Variant getters (one per translation unit that instantiates kernels).
-KernelInfo kinfo_f16(int cta_group, bool skinny = false);
+enum F16Variant { F16_WIDE = 0, F16_SKINNY_M = 1, F16_NARROW_N = 2 };
+KernelInfo kinfo_f16(int cta_group, F16Variant v = F16_WIDE);
 KernelInfo kinfo_tf32(int cta_group);
 KernelInfo kinfo_mxf8(int cta_group);  // BN 256, one accumulator (single CTA or CTA pair)
 

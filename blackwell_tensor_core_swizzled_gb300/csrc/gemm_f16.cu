@@ -2,19 +2,28 @@
 //   cta_group::1: 128 x 256 tile per CTA, 4-stage ring, 2 TMEM accumulators.
 //   cta_group::2: 256 x 256 tile per CTA pair (each CTA stages its 128 rows of
 //                 A and 128 rows of B), 6-stage ring, 2 accumulators.
+//   skinny M:     128 x 64 tiles staging 32 rows of A, 16-stage ring.
+//   narrow N:     128 x 32 tiles, 10-stage ring.
 #include "common.h"
 #include "gemm_kernel.cuh"
 
 namespace tcg {
 
 
-KernelInfo kinfo_f16(int cta_group, bool skinny) {
-  if (skinny) {
+KernelInfo kinfo_f16(int cta_group, F16Variant v) {
+  if (v == F16_SKINNY_M) {
     // M <= 32, single CTA, K-major A: 64-column tiles (more CTAs), 32 staged
     // A rows, 16-stage ring (twice the B bytes in flight per SM)
     using C = GemmCfg<1, 64, 2, 16, KIND_F16, 32>;
     return {reinterpret_cast<const void*>(&gemm_kernel<1, 64, 2, 16, KIND_F16, 32>), C::SMEM_BYTES, 1, 64,
             KIND_F16, C::THREADS};
+  }
+  if (v == F16_NARROW_N) {
+    // N <= 32 (and few-row problems computed transposed), single CTA:
+    // 128 x 32 tiles, 10-stage ring of 16 KB A + 4 KB B stages
+    using C = GemmCfg<1, 32, 2, 10, KIND_F16>;
+    return {reinterpret_cast<const void*>(&gemm_kernel<1, 32, 2, 10, KIND_F16>), C::SMEM_BYTES, 1, 32, KIND_F16,
+            C::THREADS};
   }
   if (cta_group == 2) {
     using C = GemmCfg<2, 256, 2, 6, KIND_F16>;

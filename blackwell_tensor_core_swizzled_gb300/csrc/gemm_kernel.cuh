@@ -117,6 +117,10 @@ struct GemmParams {
   int acc_f16;
   int d_vec_ok;
   int d_tma;  // 16-bit output stored by TMA from a per-warp shared staging tile
+  // the kernel computes the transposed product: its (row r, column c) is
+  // D[c * ldd + r] (f32 accumulation, 32-column variant only; set by the host
+  // for few-row problems whose operands it swapped)
+  int d_trans;
   unsigned long long* err;
   uint64_t timeout_ns;
   // block scaling, where the scales are staged into TMEM:
@@ -366,6 +370,31 @@ __device__ __forceinline__ void store_row32(const GemmParams& p, int row, int co
       for (int i = 0; i < 16; ++i) h[i] = pack_f16(r[2 * i], r[2 * i + 1]);
     }
     store_row16(p, row, col0, h);
+  }
+}
+
+// Store 32 fp32 accumulator columns of one row of the transposed product:
+// column col0 + i goes to D[(col0 + i) * ldd + row], converted.  The 32 lanes
+// of a warp hold consecutive rows, so each column is one contiguous run.
+__device__ __forceinline__ void store_col32(const GemmParams& p, int row, int col0, const uint32_t (&r)[32]) {
+  const int ncols = min(32, p.N - col0);
+  const int64_t base = static_cast<int64_t>(col0) * p.ldd + row;
+  if (p.d_type == OUT_F32) {
+    uint32_t* dst = reinterpret_cast<uint32_t*>(p.D) + base;
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (i < ncols) dst[static_cast<int64_t>(i) * p.ldd] = r[i];
+  } else {
+    uint16_t* dst = reinterpret_cast<uint16_t*>(p.D) + base;
+    const bool bf = p.d_type == OUT_BF16;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      if (i < ncols) {
+        const float v = __uint_as_float(r[i]);
+        dst[static_cast<int64_t>(i) * p.ldd] =
+            bf ? __bfloat16_as_ushort(__float2bfloat16_rn(v)) : __half_as_ushort(__float2half_rn(v));
+      }
+    }
   }
 }
 
@@ -725,6 +754,8 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
     const int part = (warp - 4) >> 2;        // this warp drains chunks part, part + nparts, ...
     // one accumulator, eight warps, 16-bit output: read everything, release, then store
     const bool early = ACC == 1 && nparts == 2 && (p.acc_f16 || p.d_type != OUT_F32);
+    // transposed stores exist in the 32-column f16/bf16 variant only
+    constexpr bool TRANS = BN == 32 && KIND == KIND_F16;
     // TMA-store staging: this warp's EPI_BUFS tiles of 32 rows x 64 bytes
     const uint32_t epi_base = sbase + C::EPI_OFF + static_cast<uint32_t>((warp - 4) * C::EPI_BUFS * C::EPI_TILE_BYTES);
     uint32_t epi_n = 0;
@@ -865,7 +896,9 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
           tmem_ld_32x32b_x32(tb + 32 * c, r);
           tc_wait_ld();
           if (n0 + 32 * c < p.N) {
-            if (p.d_tma) {
+            if (TRANS && p.d_trans) {
+              if (row < p.M) store_col32(p, row, n0 + 32 * c, r);
+            } else if (p.d_tma) {
               uint32_t h[16];
               pack16(r, h);
               store_tile16(row0, n0 + 32 * c, h);

@@ -1,7 +1,8 @@
 // Final step of split-K / stream-K GEMMs: every output tile computed in parts
 // has one fp32 partial per contributing unit in the workspace slots (written
 // by the GEMM kernel's epilogue); this kernel sums them in K order and writes
-// D.  One thread per (tile, CTA of a pair, row, 4 columns): 16-byte slot
+// D (or, for a transposed product, D's transpose).  One thread per (tile, CTA
+// of a pair, row, 4 columns): 16-byte slot
 // loads (all slots of a thread are independent, so they overlap), an fp32
 // sum, the output conversion and one store.  Tiles computed whole by one
 // unit were stored to D directly and are skipped.  Launched as a programmatic
@@ -24,8 +25,16 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const __grid_constan
   int64_t r = idx - tile * per_tile;
   const int rank = static_cast<int>(r / per_rank);
   r -= rank * per_rank;
-  const int lrow = static_cast<int>(r / q4);
-  const int c4 = static_cast<int>(r - static_cast<int64_t>(lrow) * q4);
+  // rows fastest for a transposed D (a warp's 32 rows are one contiguous run
+  // of each D row), else 4-column groups fastest
+  int lrow, c4;
+  if (p.d_trans) {
+    c4 = static_cast<int>(r / p.w_rows);
+    lrow = static_cast<int>(r - static_cast<int64_t>(c4) * p.w_rows);
+  } else {
+    lrow = static_cast<int>(r / q4);
+    c4 = static_cast<int>(r - static_cast<int64_t>(lrow) * q4);
+  }
   // contributing units: `split` consecutive slots, or under stream-K the
   // clusters c0 .. c0+n-1 whose ranges meet the tile; cluster c's slot is
   // 2c for its head (its range starts inside this tile) else 2c+1 (start(c)
@@ -65,6 +74,20 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const __grid_constan
   }
   const bool full4 = col + 3 < p.N;
   const float vals[4] = {v.x, v.y, v.z, v.w};
+  if (p.d_trans) {
+    // element (row, col + e) of the transposed product is D[(col + e) * ldd + row]
+    for (int e = 0; e < 4; ++e) {
+      if (col + e >= p.N) break;
+      const int64_t off = static_cast<int64_t>(col + e) * p.ldd + row;
+      if (p.d_type == OUT_F32)
+        reinterpret_cast<float*>(p.D)[off] = vals[e];
+      else if (p.d_type == OUT_BF16)
+        reinterpret_cast<uint16_t*>(p.D)[off] = __bfloat16_as_ushort(__float2bfloat16_rn(vals[e]));
+      else
+        reinterpret_cast<uint16_t*>(p.D)[off] = __half_as_ushort(__float2half_rn(vals[e]));
+    }
+    return;
+  }
   if (p.d_type == OUT_F32) {
     float* dst = reinterpret_cast<float*>(p.D) + row * p.ldd + col;
     if (full4 && p.d_vec_ok) {

@@ -236,6 +236,12 @@ const char* tcg_last_error_string(void);
 /* Number of kernels the most recent successful call on this thread queued. */
 int tcg_last_launch_count(void);
 
+/* How the most recent successful GEMM call on this thread was run (kernel
+ * tile, CTA group, clusters, one pass / split-K / stream-K, operand swap), as
+ * text for logs and tests; empty if the call queued nothing.  The string is
+ * owned by the library and valid until this thread's next GEMM call. */
+const char* tcg_last_plan_string(void);
+
 /* ---------------------------------------------------------------------------
  * Layout probes: single-CTA kernels that expose one tcgen05 / ldmatrix
  * mechanism each, so the tests can compare it bit for bit with the pages'

@@ -48,9 +48,14 @@ SMALL = [
     ("tf32", "mn", "mn", 260, 300, 72, 2, "f32", "f32"),
     ("tf32", "k", "mn", 128, 256, 128, 1, "f32", "f32"),
     ("tf32", "mn", "k", 384, 256, 96, 2, "bf16", "f32"),
-    ("bf16", "k", "k", 20, 700, 1000, 1, "bf16", "f32"),   # skinny variant: 32 staged A rows, 64-wide tiles
-    ("f16", "k", "mn", 32, 520, 640, 1, "f16", "f16"),
+    # skinny variant (M <= 32, K-major A): 32 staged A rows, 64-wide tiles
+    ("bf16", "k", "k", 20, 700, 1000, 1, "bf16", "f32"),
     ("bf16", "k", "k", 1, 300, 200, 0, "f32", "f32"),
+    ("bf16", "k", "mn", 16, 520, 392, 1, "f16", "f32"),
+    ("f16", "k", "mn", 32, 520, 640, 1, "f16", "f16"),
+    # narrow N (N <= 32, K-major B): 128 x 32 tiles
+    ("bf16", "k", "k", 700, 20, 1000, 1, "bf16", "f32"),
+    ("f16", "mn", "k", 300, 32, 72, 0, "f16", "f32"),
     ("e4m3", "k", "k", 300, 520, 256, 2, "bf16", "f32"),
     ("e4m3", "k", "k", 300, 520, 208, 1, "f32", "f32"),
     ("e4m3", "k", "k", 512, 448, 512, 2, "bf16", "f32"),
@@ -150,6 +155,9 @@ SPLIT = [
     ("bf16", "k", "k", 16, 1000, 2048, 1, "bf16", -1),
     ("bf16", "k", "k", 16, 1000, 8192, 1, "bf16", 0),
     ("bf16", "k", "mn", 1, 520, 1024, 1, "f32", 3),
+    ("bf16", "k", "mn", 5, 2000, 4096, 0, "f32", 0),
+    ("f16", "k", "k", 24, 600, 1536, 1, "f16", 3),
+    ("bf16", "k", "k", 1000, 16, 4096, 1, "bf16", -1),
     ("bf16", "k", "k", 100, 300, 1000, 1, "bf16", 7),
     ("bf16", "mn", "k", 200, 700, 1536, 2, "bf16", -1),
     ("bf16", "k", "k", 256, 512, 4096, 2, "f16", -1),
@@ -179,6 +187,43 @@ def test_split_k_workspace_survives_shape_changes(tcg, oracle_mod):
         assert tcg.last_launch_count() == 2  # the GEMM and the partial-tile reduction
     _check_full(tcg, oracle_mod, cases[1], "bf16", "f32", 1, split_k=1)
     assert tcg.last_launch_count() == 1
+
+
+# Few rows of A against more columns than 64 x SMs: the library swaps the
+# operands (D^T = B^T A^T on 128 x 32 tiles) and stores D transposed.
+# dtype, b_major, M, K, out, split_k, extra columns of D's leading dimension
+TRANSPOSED = [
+    ("bf16", "k", 20, 1000, "bf16", 0, 0),
+    ("bf16", "k", 1, 200, "f32", 0, 0),
+    ("bf16", "mn", 16, 392, "f16", 0, 0),
+    ("f16", "k", 32, 136, "f32", 0, 0),
+    ("bf16", "k", 16, 520, "bf16", 0, 3),     # odd leading dimension of D
+    ("bf16", "k", 7, 2048, "f32", -1, 1),     # stream-K: partial tiles reduced into the transposed D
+    ("f16", "mn", 24, 1536, "bf16", 3, 0),    # fixed split
+]
+
+
+@pytest.mark.parametrize("dtype,bm,M,K,out,split,pad", TRANSPOSED)
+def test_transposed_few_row_path(tcg, oracle_mod, dtype, bm, M, K, out, split, pad):
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    N = 64 * sms + 77  # ragged in the 128-row swapped tiles
+    x = make_case(dtype, "k", bm, M, N, K, seed=M + K)
+    _check_full(tcg, oracle_mod, x, out, "f32", 0, ldd=N + pad, split_k=split)
+    plan = tcg.last_plan_string()
+    assert "operands swapped" in plan and "tile 128x32" in plan, plan
+    if split == -1:
+        assert "stream-K" in plan, plan
+
+
+def test_plan_choices_for_few_row_and_narrow_problems(tcg, oracle_mod):
+    # skinny 64-column tiles in one pass; narrow 32-column tiles under stream-K
+    x = make_case("bf16", "k", "k", 16, 4096, 1024, seed=61)
+    _check_full(tcg, oracle_mod, x, "bf16", "f32", 0)
+    assert "tile 128x64" in tcg.last_plan_string() and "swapped" not in tcg.last_plan_string()
+    x = make_case("bf16", "k", "k", 4096, 16, 8192, seed=62)
+    _check_full(tcg, oracle_mod, x, "bf16", "f32", 0)
+    plan = tcg.last_plan_string()
+    assert "tile 128x32" in plan and "stream-K" in plan and "swapped" not in plan, plan
 
 
 # rows, K, tile rows, byte offset of the plain scales, byte offset of the image.
