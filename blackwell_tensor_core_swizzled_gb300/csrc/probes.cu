@@ -4,7 +4,8 @@
 //   * TMEM st/ld round trip ("tcgen05.ld / tcgen05.st" page, Layout B example;
 //     the copy_async -> tcgen05_ldst page's 128x8 demonstration);
 //   * tcgen05.cp from a descriptor-walked shared image ("tcgen05.cp" page,
-//     shape table and "Shared descriptor address walk");
+//     shape table and "Shared descriptor address walk"), plain or with the
+//     FP4 / FP6 decompression ("Native FP4/FP6 decompression");
 //   * tcgen05.ld register images of the 16-row shapes ("Native images");
 //   * one MMA tile with generic-store swizzled operands ("tcgen05.mma" page,
 //     "four K16 issues" example);
@@ -123,11 +124,39 @@ __global__ void __launch_bounds__(128, 1) probe_cp_kernel(const uint32_t* image,
   tc_fence_after();
   if (threadIdx.x == 0) {
     const uint64_t d = sdesc(base + origin, desc_hi);
+    // shape + 4 * format: format 1 / 2 expand packed FP4 / FP6 blocks
+    // ("tcgen05.cp" page, "Native FP4/FP6 decompression")
     switch (shape) {
       case 0: asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(slot), "l"(d) : "memory"); break;
       case 1: asm volatile("tcgen05.cp.cta_group::1.128x128b [%0], %1;" ::"r"(slot), "l"(d) : "memory"); break;
       case 2: asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(slot), "l"(d) : "memory"); break;
-      default: asm volatile("tcgen05.cp.cta_group::1.4x256b [%0], %1;" ::"r"(slot), "l"(d) : "memory"); break;
+      case 3: asm volatile("tcgen05.cp.cta_group::1.4x256b [%0], %1;" ::"r"(slot), "l"(d) : "memory"); break;
+      case 4:
+        asm volatile("tcgen05.cp.cta_group::1.128x256b.b8x16.b4x16_p64 [%0], %1;" ::"r"(slot), "l"(d) : "memory");
+        break;
+      case 5:
+        asm volatile("tcgen05.cp.cta_group::1.128x128b.b8x16.b4x16_p64 [%0], %1;" ::"r"(slot), "l"(d) : "memory");
+        break;
+      case 6:
+        asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4.b8x16.b4x16_p64 [%0], %1;" ::"r"(slot), "l"(d)
+                     : "memory");
+        break;
+      case 7:
+        asm volatile("tcgen05.cp.cta_group::1.4x256b.b8x16.b4x16_p64 [%0], %1;" ::"r"(slot), "l"(d) : "memory");
+        break;
+      case 8:
+        asm volatile("tcgen05.cp.cta_group::1.128x256b.b8x16.b6x16_p32 [%0], %1;" ::"r"(slot), "l"(d) : "memory");
+        break;
+      case 9:
+        asm volatile("tcgen05.cp.cta_group::1.128x128b.b8x16.b6x16_p32 [%0], %1;" ::"r"(slot), "l"(d) : "memory");
+        break;
+      case 10:
+        asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4.b8x16.b6x16_p32 [%0], %1;" ::"r"(slot), "l"(d)
+                     : "memory");
+        break;
+      default:
+        asm volatile("tcgen05.cp.cta_group::1.4x256b.b8x16.b6x16_p32 [%0], %1;" ::"r"(slot), "l"(d) : "memory");
+        break;
     }
     tc_commit<1>(smem_u32(&bar));
   }
@@ -359,11 +388,13 @@ extern "C" int tcg_probe_tmem_roundtrip(const uint32_t* in, uint32_t* out, int n
 extern "C" int tcg_probe_cp(const uint32_t* image, int image_words, int shape, uint32_t origin_bytes, uint32_t ldo,
                             uint32_t sdo, int swizzle, uint32_t* out, void* stream) {
   if (!image || !out || image_words <= 0 || image_words > CP_IMAGE_MAX_WORDS) return TCG_ERR_INVALID;
-  if (shape < 0 || shape > 3 || swizzle < 0 || swizzle > 3) return TCG_ERR_INVALID;
+  if (shape < 0 || shape > 11 || swizzle < 0 || swizzle > 3) return TCG_ERR_INVALID;
   if (!sdesc_fields_ok(origin_bytes, ldo, sdo, swizzle, 0)) return TCG_ERR_INVALID;
-  // the copy's whole walk must stay inside the image
-  const uint32_t rows = shape == 2 ? 32u : shape == 3 ? 4u : 128u;
-  const uint32_t words = shape == 0 || shape == 3 ? 8u : 4u;
+  // the copy's whole walk must stay inside the image (decompression keeps
+  // the base shape's source footprint)
+  const int base_shape = shape % 4;
+  const uint32_t rows = base_shape == 2 ? 32u : base_shape == 3 ? 4u : 128u;
+  const uint32_t words = base_shape == 0 || base_shape == 3 ? 8u : 4u;
   const uint32_t rb = 16u << swizzle;
   const uint32_t last_row = ((rows - 1) / 8) * sdo + ((rows - 1) % 8) * rb;
   const uint32_t last_word = swizzle == 0 ? ((words - 1) / 4) * ldo + ((words - 1) % 4) * 4 : 4 * (words - 1);

@@ -256,10 +256,15 @@ int tcg_probe_tmem_roundtrip(const uint32_t* in, uint32_t* out, int ncols, void*
 
 /* "tcgen05.cp" page: fills a 1024-byte-aligned shared buffer with
  * `image_words` words of `image`, issues one tcgen05.cp of `shape`
- * (0 = 128x256b, 1 = 128x128b, 2 = 32x128b.warpx4, 3 = 4x256b) with the
- * descriptor (origin_bytes, ldo, sdo, swizzle 0..3), waits on its commit and
- * reads 128 lanes x 8 columns back with tcgen05.ld .32x32b.x8 into out
- * (128 x 8 words, lane-major).  image_words <= 12288. */
+ * (0 = 128x256b, 1 = 128x128b, 2 = 32x128b.warpx4, 3 = 4x256b; plus 4 for the
+ * same shape with .b8x16.b4x16_p64 FP4 decompression, plus 8 for
+ * .b8x16.b6x16_p32 FP6 decompression, "Native FP4/FP6 decompression": each
+ * 16-byte source block of packed values and padding becomes sixteen
+ * expanded bytes) with the descriptor (origin_bytes, ldo, sdo, swizzle 0..3),
+ * waits on its commit and reads 128 lanes x 8 columns back with
+ * tcgen05.ld .32x32b.x8 into out (128 x 8 words, lane-major; cells the copy
+ * does not write hold 0xDEADBEEF).  image_words <= 12288; the walk must stay
+ * inside the image (else TCG_ERR_INVALID before any launch). */
 int tcg_probe_cp(const uint32_t* image, int image_words, int shape,
                  uint32_t origin_bytes, uint32_t ldo, uint32_t sdo, int swizzle,
                  uint32_t* out, void* stream);

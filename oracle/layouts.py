@@ -89,6 +89,37 @@ def cp_physical(origin: int, r, w, ldo: int, sdo: int, swizzle: int, base_align:
     return swizzle_addr(base_align + origin + cp_walk(r, w, ldo, sdo, swizzle), swizzle) - base_align
 
 
+def cp_decompress(words, fmt: int):
+    """FP4 / FP6 decompression of tcgen05.cp ("tcgen05.cp" page, "Native
+    FP4/FP6 decompression").  ``words`` is an array (..., 4) of b32 words, one
+    16-byte source block per row of the last axis: sixteen packed values
+    followed by padding (FP4, fmt 4: 8 data bytes + 8 padding bytes; FP6,
+    fmt 6: 12 data bytes + 4 padding bytes).  The destination block is sixteen
+    bytes, value i in byte i; a 4-bit value gains two low zero bits
+    (byte = v << 2), a 6-bit value two high zero bits (byte = v).  The page
+    does not state the packing order; the reading taken is the little-endian
+    one: value i occupies bits [b*i, b*(i+1)) of the data bytes read as one
+    little-endian integer (b = 4 or 6).  Returns the (..., 4) destination
+    words (little-endian bytes)."""
+    w = np.asarray(words, dtype=np.uint64)
+    if w.shape[-1] != 4:
+        raise ValueError("blocks are 4 words")
+    if fmt not in (4, 6):
+        raise ValueError("fmt is 4 (FP4) or 6 (FP6)")
+    mask = (1 << fmt) - 1
+    flat = w.reshape(-1, 4)
+    out = np.zeros(flat.shape, dtype=np.uint32)
+    for n, blk in enumerate(flat):
+        data = sum(int(blk[j]) << (32 * j) for j in range(4))  # the block as a 128-bit integer
+        dst = 0
+        for i in range(16):
+            v = (data >> (fmt * i)) & mask
+            dst |= ((v << 2) if fmt == 4 else v) << (8 * i)
+        for j in range(4):
+            out[n, j] = (dst >> (32 * j)) & 0xFFFFFFFF
+    return out.reshape(w.shape)
+
+
 def mma_operand_offset(mn, k, elem_bytes: int, major: str, ldo: int, sdo: int, swizzle: int):
     """Logical byte offset of operand element (mn, k) of a tcgen05.mma shared
     operand ("tcgen05.mma" page, "Shared descriptors are byte-stride

@@ -66,6 +66,10 @@ def test_host_validation_rejects_bad_arguments(tcg):
     rc = tcg.raw_call("tcg_gemm_mxf8_blockscaled", 64, 64, 64, 0x10000, 0, 0, 0x20000, 0, 0, None, None,
                       0x30000, 2, 0, 0, None)
     assert rc == tcg.ERR_INVALID
+    # cp probe: shape codes 0..11 (4..11 decompressing), walk inside the image
+    for shape in (-1, 12):
+        assert tcg.raw_call("tcg_probe_cp", 0x10000, 512, shape, 0, 16, 128, 0, 0x20000, None) == tcg.ERR_INVALID
+    assert tcg.raw_call("tcg_probe_cp", 0x10000, 256, 9, 0, 16, 128, 0, 0x20000, None) == tcg.ERR_INVALID
 
 
 def test_empty_problems_are_noops(tcg):

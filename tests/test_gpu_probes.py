@@ -73,10 +73,15 @@ CP_WORDS = {0: 8, 1: 4, 2: 4, 3: 8}
 
 
 def _cp_expected(image, shape, origin, ldo, sdo, sw):
+    # shape + 4: FP4 decompression, shape + 8: FP6; same source walk
+    fmt = {0: None, 1: 4, 2: 6}[shape // 4]
+    shape %= 4
     exp = np.full((128, 8), 0xDEADBEEF, dtype=np.uint32)
     r, w = np.meshgrid(np.arange(CP_ROWS[shape]), np.arange(CP_WORDS[shape]), indexing="ij")
     phys = L.cp_physical(origin, r, w, ldo, sdo, sw)
     vals = image[phys // 4]
+    if fmt is not None:  # every 16-byte block of a row expands on its own
+        vals = L.cp_decompress(vals.reshape(vals.shape[0], -1, 4), fmt).reshape(vals.shape)
     if shape in (0, 1):
         exp[:, :CP_WORDS[shape]] = vals
     elif shape == 2:  # 32x128b.warpx4: four replicas 32 lanes apart
@@ -125,6 +130,32 @@ def test_cp_walk_and_swizzle(tcg, shape, origin, ldo, sdo, sw, words):
                              f"exp {[hex(exp[tuple(b)]) for b in bad]}")
     if shape == 1 and origin == 0 and sw == 0:
         assert np.array_equal(got[:, :4], np.arange(512).reshape(128, 4))  # page: out == x
+
+
+# FP4 / FP6 decompression ("tcgen05.cp" page, "Native FP4/FP6 decompression"):
+# every shape with each format; random words, so the padding bytes are
+# arbitrary and must not reach TMEM.
+DECOMP_CASES = [
+    (base + 4 * fmt, origin, ldo, sdo, sw, words)
+    for fmt in (1, 2)
+    for (base, origin, ldo, sdo, sw, words) in [
+        (0, 0, 256, 128, 0, 2048), (1, 0, 16, 128, 0, 512), (2, 0, 16, 128, 0, 128), (3, 0, 16, 128, 0, 64),
+        (0, 0, 16, 1024, 3, 4096), (1, 48, 16, 512, 2, 4352)]
+]
+
+
+@pytest.mark.parametrize("shape,origin,ldo,sdo,sw,words", DECOMP_CASES)
+def test_cp_decompression(tcg, shape, origin, ldo, sdo, sw, words):
+    image = np.random.default_rng(shape * 100 + sw).integers(0, 1 << 32, words, dtype=np.uint64).astype(np.uint32)
+    out = torch.zeros((128, 8), dtype=torch.int32, device="cuda")
+    tcg.probe_cp(_u32(image), words, shape, origin, ldo, sdo, sw, out)
+    assert tcg.check() == 0
+    got = _np(out)
+    exp = _cp_expected(image, shape, origin, ldo, sdo, sw)
+    if not np.array_equal(got, exp):
+        bad = np.argwhere(got != exp)[:6]
+        raise AssertionError(f"mismatch at {bad.tolist()}: got {[hex(got[tuple(b)]) for b in bad]} "
+                             f"exp {[hex(exp[tuple(b)]) for b in bad]}")
 
 
 # ------------------------------------------------------------- ld images

@@ -218,3 +218,60 @@ def test_sf_prepare_is_invertible(rows, kblocks, tile_rows):
         for kk in range(kblocks):
             ks, kb = divmod(kk, 4)
             assert img[ks, t, c, int(L.sf_chunk_offset(rc, kb))] == sf[r, kk]
+
+
+# ------------------------------------------------------------- cp decompression
+
+def _pack_bits(values, bits, rng):
+    """Independent packer: set the block's bits one by one (value i at bit
+    offsets bits*i .. bits*i + bits - 1, little-endian over the 16 bytes),
+    then fill the padding bytes with random data."""
+    block = bytearray(16)
+    for i, v in enumerate(values):
+        for b in range(bits):
+            if (v >> b) & 1:
+                pos = bits * i + b
+                block[pos // 8] |= 1 << (pos % 8)
+    data_bytes = 2 * bits  # 16 values x bits / 8
+    block[data_bytes:] = bytes(rng.integers(0, 256, 16 - data_bytes, dtype=np.uint8))
+    return np.frombuffer(bytes(block), dtype="<u4").copy()
+
+
+def test_cp_decompress_fp4_nibble_sequence():
+    # data bytes 0x10 0x32 ... 0xFE hold the nibbles 0, 1, ..., 15 in order;
+    # each gains two low zero bits, so byte i is 4 * i
+    block = np.array([0x76543210, 0xFEDCBA98, 0xDEADBEEF, 0x01234567], dtype=np.uint32)
+    out = L.cp_decompress(block, 4)
+    assert np.frombuffer(out.astype("<u4").tobytes(), dtype=np.uint8).tolist() == [4 * i for i in range(16)]
+
+
+@pytest.mark.parametrize("fmt", [4, 6])
+def test_cp_decompress_matches_bitwise_packer_and_ignores_padding(fmt):
+    rng = np.random.default_rng(fmt)
+    for _ in range(200):
+        vals = rng.integers(0, 1 << fmt, 16)
+        block = _pack_bits(vals, fmt, rng)
+        other = block.copy()
+        other[3] ^= 0xA5A5A5A5 if fmt == 4 else 0  # FP4 padding is all of word 3 (and word 2)
+        if fmt == 4:
+            other[2] ^= 0x5A5A5A5A
+        got = np.frombuffer(L.cp_decompress(block, fmt).astype("<u4").tobytes(), dtype=np.uint8)
+        exp = (vals << 2) if fmt == 4 else vals
+        assert got.tolist() == exp.tolist()
+        assert np.array_equal(L.cp_decompress(other, fmt), L.cp_decompress(block, fmt))
+        assert np.all(got >> 6 == 0)            # two high zero bits either way
+        if fmt == 4:
+            assert np.all(got & 3 == 0)         # FP4: two low zero bits
+
+
+def test_cp_decompress_fp6_padding_is_the_last_word():
+    rng = np.random.default_rng(9)
+    vals = rng.integers(0, 64, (5, 16))
+    blocks = np.stack([_pack_bits(v, 6, rng) for v in vals])
+    flipped = blocks.copy()
+    flipped[:, 3] ^= 0xFFFFFFFF
+    assert np.array_equal(L.cp_decompress(blocks, 6), L.cp_decompress(flipped, 6))
+    flipped = blocks.copy()
+    flipped[:, 2] ^= 1 << 31  # bit 95: the top bit of value 15
+    diff = L.cp_decompress(flipped, 6) != L.cp_decompress(blocks, 6)
+    assert diff[:, 3].all() and not diff[:, :3].any()
