@@ -455,6 +455,11 @@ int run_gemm(const tcg_gemm_args* args, cudaStream_t s) {
   prm.num_n_tiles = static_cast<int>(cdiv(a.N, bn));
   const int es = esize_of(a.in_type);
   prm.num_k_blocks = static_cast<int>(cdiv(a.K * es, 128));
+  // tile, unit and slot indices are 32-bit in the kernels
+  if (static_cast<int64_t>(prm.num_m_tiles) * prm.num_n_tiles > INT32_MAX / 4) {
+    t_last_error = "too many output tiles";
+    return TCG_ERR_UNSUPPORTED;
+  }
   prm.num_tiles = prm.num_m_tiles * prm.num_n_tiles;
   // M tiles per raster group (measured at 8192^3: 16 for 128-row tiles, 8 for
   // 256-row pair tiles, i.e. 2048 rows of A either way)
@@ -550,7 +555,8 @@ int run_gemm(const tcg_gemm_args* args, cudaStream_t s) {
   bool stream_k = false;
   if (a.acc_type != TCG_F16) {
     if (a.split_k > 1)
-      split = static_cast<int>(std::min<int64_t>(a.split_k, prm.num_k_blocks));
+      split = static_cast<int>(std::min<int64_t>({a.split_k, prm.num_k_blocks,
+                                                  std::max<int64_t>(1, (INT32_MAX / 4) / prm.num_tiles)}));
     else if (a.split_k == -1)
       stream_k = true;
     else if (a.split_k == 0 && (bn <= 64 ? 2 : 4) * static_cast<int64_t>(prm.num_tiles) <= max_clusters &&

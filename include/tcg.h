@@ -165,12 +165,15 @@ typedef struct {
                             ("tcgen05.cp" page) before its MMAs,
                         3 = a dedicated thread with tcgen05.cp + commit */
   int split_k;       /* K decomposition: 0 = auto (problems whose output tiles
-                        fill at most a quarter of the GPU and have a long K,
-                        e.g. skinny M, use stream-K: every cluster takes an
-                        equal contiguous share of the (tile, K block)
-                        iterations), -1 = stream-K, 1 = one pass per
-                        tile, n >= 2 = every tile split into n K ranges (capped
-                        at the number of 128-byte K blocks).  Each unit that
+                        fill at most a quarter of the GPU -- half for the
+                        32- and 64-column tiles of few-row and few-column
+                        problems -- and have a long K use stream-K: every
+                        cluster takes an equal contiguous share of the
+                        (tile, K block) iterations), -1 = stream-K, 1 = one
+                        pass per tile, n >= 2 = every tile split into n K
+                        ranges (capped at the number of 128-byte K blocks and
+                        at 2^29 / tiles units).  Problems with more than 2^29
+                        output tiles return TCG_ERR_UNSUPPORTED.  Each unit that
                         computes part of a tile stores an fp32 partial in a
                         workspace owned by the library per (device, stream); a
                         second kernel sums each tile's partials in K order

@@ -291,6 +291,16 @@ def test_padded_leading_dims_and_unaligned_output(tcg, oracle_mod):
     _check_full(tcg, oracle_mod, x, "f32", "f32", 2, ldd=320)
 
 
+def test_absurd_tile_counts_are_refused_before_any_launch(tcg):
+    # (2^30 - 1)^2 outputs: 2^44 pair tiles, far beyond 32-bit tile indices;
+    # refused on the host (the pointers are never touched)
+    M = N = (1 << 30) - 1
+    rc = tcg.gemm(M, N, 64, 1, 0x10000, 0, 64, 0x20000, 0, 64, 0x30000, 2, N, 0, check=False)
+    assert rc == tcg.ERR_UNSUPPORTED
+    assert "tiles" in tcg.last_error_string()
+    assert tcg.check() == 0
+
+
 def test_k_zero_zeroes_d_and_empty_is_noop(tcg):
     D = torch.full((64, 80), 7.0, dtype=torch.float32, device="cuda")
     tcg.gemm_bf16(64, 80, 0, 0, 0, 0, 0, 0, 0, D, 0, 80, 0)
