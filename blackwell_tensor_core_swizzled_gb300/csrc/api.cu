@@ -47,6 +47,8 @@ DeviceState g_dev[kMaxDevices];
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
+PFN_cuCtxGetCurrent_v4000 g_ctx_get = nullptr;
+std::once_flag g_ctx_get_once;
 
 struct Workspace {
   void* ptr = nullptr;
@@ -619,6 +621,24 @@ int current_device_checked(int* dev) {
   if (!st || !st->usable) {
     t_last_error = "current device is not an sm_103 GPU";
     return TCG_ERR_NO_DEVICE;
+  }
+  // The tensor maps are encoded with a driver call, which needs a context
+  // current on this thread; a host thread that has made no runtime call that
+  // binds one yet gets the device's primary context (the one the runtime
+  // itself would use).  A context the caller made current is left alone.
+  std::call_once(g_ctx_get_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_get = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+    else
+      cudaGetLastError();
+  });
+  CUcontext ctx = nullptr;
+  if (g_ctx_get && g_ctx_get(&ctx) == CUDA_SUCCESS && ctx == nullptr) {
+    e = cudaSetDevice(d);
+    if (e != cudaSuccess) return record_cuda(e);
   }
   *dev = d;
   return TCG_OK;

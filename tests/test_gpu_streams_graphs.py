@@ -94,3 +94,37 @@ def test_concurrent_streams(tcg, oracle_mod):
     for row in outs:
         for x, D in zip(cases, row):
             _check(oracle_mod, x, D, f"stream {x['w'].dtype}")
+
+
+def test_concurrent_host_threads(tcg, oracle_mod):
+    # two host threads, each with its own stream, issue GEMMs at the same time
+    # (the library's shared state is mutex-guarded; per-thread error strings)
+    import threading
+    cases = [_prepare(make_case("bf16", "k", "k", 16, 1000, 4096, seed=91)),
+             _prepare(make_case("e4m3", "k", "k", 260, 460, 512, seed=92))]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = [[torch.full((x["M"], x["N"]), float("nan"), dtype=torch.bfloat16, device="cuda") for x in cases]
+            for _ in streams]
+    torch.cuda.synchronize()
+    errors = []
+
+    def worker(i):
+        try:
+            for rep in range(10):
+                for x, D in zip(cases, outs[i]):
+                    _enqueue(tcg, x, D, streams[i].cuda_stream, -1 if x["w"].dtype == "bf16" else 0)
+        except Exception as e:  # surfaced below
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    torch.cuda.synchronize()
+    for st in streams:
+        assert tcg.check(st.cuda_stream) == 0
+    for row in outs:
+        for x, D in zip(cases, row):
+            _check(oracle_mod, x, D, f"thread {x['w'].dtype}")
