@@ -546,8 +546,9 @@ int run_gemm(const tcg_gemm_args* args, cudaStream_t s) {
   // fp32 workspace and a second kernel).  That costs a few microseconds and a
   // second epilogue per cluster, so it is used only when the tiles fill at
   // most a quarter of the clusters and the idle share times the K blocks is
-  // at least 60 (measured: 16 x 8192 x 8192 and 64 x 4096 x 16384 gain;
-  // 128 x 16384 x 4096, 512 x 4096 x 4096 and 2048^2 x 2048..8192 lose).  The
+  // at least 60 (measured with 128 x 256 tiles: 16 x 8192 x 8192 and
+  // 64 x 4096 x 16384 gain; 128 x 16384 x 4096, 512 x 4096 x 4096 and
+  // 2048^2 x 2048..8192 lose).  The
   // narrow (32-column) and skinny (64-column) tiles carry so little work per
   // tile that half the clusters suffice (16 x 4096 x 16384: 41 us stream-K vs
   // 60 us one pass; 8192 x 16 x 8192: 40 vs 58 us).

@@ -2,12 +2,12 @@
 // has one fp32 partial per contributing unit in the workspace slots (written
 // by the GEMM kernel's epilogue); this kernel sums them in K order and writes
 // D (or, for a transposed product, D's transpose).  One thread per (tile, CTA
-// of a pair, row, 4 columns): 16-byte slot
-// loads (all slots of a thread are independent, so they overlap), an fp32
-// sum, the output conversion and one store.  Tiles computed whole by one
-// unit were stored to D directly and are skipped.  Launched as a programmatic
-// dependent of the GEMM (its launch overlaps the GEMM's last CTAs); it waits
-// for the GEMM's completion and memory flush before reading the slots.
+// of a pair, row, 4 columns): 16-byte slot loads (all slots of a thread are
+// independent, so they overlap), an fp32 sum, the output conversion and the
+// stores.  Tiles computed whole by one unit were stored to D directly and are
+// skipped.  Launched as a programmatic dependent of the GEMM (its launch
+// overlaps the GEMM's last CTAs); it waits for the GEMM's completion and
+// memory flush before reading the slots.
 #include "common.h"
 #include "gemm_kernel.cuh"
 
