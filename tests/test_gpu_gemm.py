@@ -56,6 +56,7 @@ SMALL = [
     # narrow N (N <= 32, K-major B): 128 x 32 tiles
     ("bf16", "k", "k", 700, 20, 1000, 1, "bf16", "f32"),
     ("f16", "mn", "k", 300, 32, 72, 0, "f16", "f32"),
+    ("f16", "k", "k", 300, 24, 136, 1, "f16", "f16"),     # f16 accumulation: packed TMEM loads
     ("e4m3", "k", "k", 300, 520, 256, 2, "bf16", "f32"),
     ("e4m3", "k", "k", 300, 520, 208, 1, "f32", "f32"),
     ("e4m3", "k", "k", 512, 448, 512, 2, "bf16", "f32"),
