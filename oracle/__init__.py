@@ -11,8 +11,12 @@ CUDA path.
   register images, ldmatrix ownership and scale-factor placement.
 
 Parity status: every function here is pinned by ``tests/test_oracle_*.py``
-against library routines, closed forms and the pages' worked examples, except
-where DESIGN.md's readings table says "parity unpinned".
+against library routines, closed forms and the pages' worked examples.  Two
+properties of the hardware are not modelled and stay "parity unpinned" (bounded
+by the tolerance only): how the tensor cores round float32 storage to TF32
+(the oracle reads the float32 values exactly; the per-product relative error
+is at most 2^-10), and the order and rounding of fp16 accumulation inside the
+MMA (the oracle accumulates in float64).
 """
 from __future__ import annotations
 

@@ -4,8 +4,10 @@ TEST INFRASTRUCTURE ONLY: used by the tests to predict, bit for bit, what the
 GPU layout probes must return.  Shares nothing with the CUDA library.
 
 Every function cites the page and section it restates.  Readings of points the
-pages leave open are marked READING and are listed in the design doc's table of
-readings.
+pages leave open are marked READING in the function that takes them (the XOR
+of swizzle modes 1-3, the 16x64b register formula as printed, the packing
+order inside an FP4 / FP6 decompression block); each is pinned bit for bit by
+a GPU layout probe.
 """
 from __future__ import annotations
 
@@ -96,9 +98,9 @@ def cp_decompress(words, fmt: int):
     followed by padding (FP4, fmt 4: 8 data bytes + 8 padding bytes; FP6,
     fmt 6: 12 data bytes + 4 padding bytes).  The destination block is sixteen
     bytes, value i in byte i; a 4-bit value gains two low zero bits
-    (byte = v << 2), a 6-bit value two high zero bits (byte = v).  The page
-    does not state the packing order; the reading taken is the little-endian
-    one: value i occupies bits [b*i, b*(i+1)) of the data bytes read as one
+    (byte = v << 2), a 6-bit value two high zero bits (byte = v).
+    READING (the page does not state the packing order): little-endian,
+    value i occupies bits [b*i, b*(i+1)) of the data bytes read as one
     little-endian integer (b = 4 or 6).  Returns the (..., 4) destination
     words (little-endian bytes)."""
     w = np.asarray(words, dtype=np.uint64)
