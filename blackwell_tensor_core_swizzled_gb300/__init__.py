@@ -58,6 +58,7 @@ _SIGS = {
     "tcg_probe_cp": ([_vp, _i32, _i32, _u32, _u32, _u32, _i32, _vp, _vp], _i32),
     "tcg_probe_ld_shape": ([_vp, _i32, _i32, _i32, _vp, _vp], _i32),
     "tcg_probe_mma_tile": ([_vp, _vp, _i32, _i32, _i32, _vp, _vp], _i32),
+    "tcg_probe_mma_tile_ws": ([_vp, _vp, _i32, _i32, _i32, _vp, _vp], _i32),
     "tcg_probe_ldmatrix_x2": ([_vp, _vp, _vp], _i32),
     "tcg_probe_wait_timeout": ([_u64, _vp], _i32),
 }
@@ -222,6 +223,11 @@ def probe_ld_shape(inp, shape, num, half, out, stream=None):
 
 def probe_mma_tile(A, B, N, K, is_bf16, D, stream=None):
     return _ok(_lib.tcg_probe_mma_tile(_ptr(A), _ptr(B), N, K, is_bf16, _ptr(D), _stream(stream)), "probe_mma_tile")
+
+
+def probe_mma_tile_ws(A, B, N, K, is_bf16, D, stream=None):
+    return _ok(_lib.tcg_probe_mma_tile_ws(_ptr(A), _ptr(B), N, K, is_bf16, _ptr(D), _stream(stream)),
+               "probe_mma_tile_ws")
 
 
 def probe_ldmatrix_x2(x, out, stream=None):

@@ -8,7 +8,8 @@
 //     FP4 / FP6 decompression ("Native FP4/FP6 decompression");
 //   * tcgen05.ld register images of the 16-row shapes ("Native images");
 //   * one MMA tile with generic-store swizzled operands ("tcgen05.mma" page,
-//     "four K16 issues" example);
+//     "four K16 issues" example), dense or with the weight-stationary .ws
+//     opcode ("Weight-stationary and block scaling");
 //   * ldmatrix .x2 into separated register slots ("ldmatrix / stmatrix" page
 //     example);
 //   * a bounded wait that runs out (failure detection without a GPU fault).
@@ -239,8 +240,8 @@ __global__ void __launch_bounds__(128, 1) probe_ld_shape_kernel(const uint32_t* 
 // swizzle 128B): row r at (r/8)*1024 + (r%8)*128, element k at 2k, then the
 // mode-3 XOR), K/16 MMA issues whose start address advances 32 bytes each.
 __global__ void __launch_bounds__(128, 1) probe_mma_tile_kernel(const uint16_t* A, const uint16_t* B, int N, int K,
-                                                                uint32_t idesc, float* D, unsigned long long* err,
-                                                                uint64_t timeout_ns) {
+                                                                uint32_t idesc, int ws, float* D,
+                                                                unsigned long long* err, uint64_t timeout_ns) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint32_t slot;
   __shared__ __align__(8) uint64_t bar;
@@ -283,7 +284,18 @@ __global__ void __launch_bounds__(128, 1) probe_mma_tile_kernel(const uint16_t* 
   if (t == 0) {
     const uint64_t hi = sdesc_hi(16, 1024, SW_128B);
     for (int kr = 0; kr < K / 16; ++kr) {
-      mma_f16<1>(slot, sdesc(a_base + 32u * kr, hi), sdesc(b_base + 32u * kr, hi), idesc, kr > 0);
+      const uint64_t ad = sdesc(a_base + 32u * kr, hi), bd = sdesc(b_base + 32u * kr, hi);
+      if (ws) {
+        // weight-stationary opcode ("tcgen05.mma" page, "Weight-stationary and
+        // block scaling": selected in the opcode; M128 .ws uses Layout D)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.ws.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(slot),
+            "l"(ad), "l"(bd), "r"(idesc), "r"(kr > 0 ? 1u : 0u)
+            : "memory");
+      } else {
+        mma_f16<1>(slot, ad, bd, idesc, kr > 0);
+      }
     }
     tc_commit<1>(smem_u32(&bar));
   }
@@ -438,7 +450,23 @@ extern "C" int tcg_probe_mma_tile(const void* A, const void* B, int N, int K, in
   if (e != cudaSuccess) return record_cuda(e);
   const uint32_t idesc = idesc_f16(is_bf16 != 0, true, false, false, 128, N);
   probe_mma_tile_kernel<<<1, 128, smem, as_stream(stream)>>>(static_cast<const uint16_t*>(A),
-                                                             static_cast<const uint16_t*>(B), N, K, idesc, D,
+                                                             static_cast<const uint16_t*>(B), N, K, idesc, 0, D,
+                                                             device_error_word(dev), wait_timeout_ns());
+  return finish_launch(1);
+}
+
+extern "C" int tcg_probe_mma_tile_ws(const void* A, const void* B, int N, int K, int is_bf16, float* D,
+                                     void* stream) {
+  if (!A || !B || !D || (N != 64 && N != 128 && N != 256) || K < 16 || K > 64 || K % 16) return TCG_ERR_INVALID;
+  int dev;
+  if (int rc = current_device_checked(&dev)) return rc;
+  const size_t smem = 1024 + (128 + 256) * 128;
+  cudaError_t e = cudaFuncSetAttribute(probe_mma_tile_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return record_cuda(e);
+  const uint32_t idesc = idesc_f16(is_bf16 != 0, true, false, false, 128, N);
+  probe_mma_tile_kernel<<<1, 128, smem, as_stream(stream)>>>(static_cast<const uint16_t*>(A),
+                                                             static_cast<const uint16_t*>(B), N, K, idesc, 1, D,
                                                              device_error_word(dev), wait_timeout_ns());
   return finish_launch(1);
 }

@@ -290,6 +290,13 @@ int tcg_probe_ld_shape(const uint32_t* in, int shape, int num, int half,
 int tcg_probe_mma_tile(const void* A, const void* B, int N, int K, int is_bf16,
                        float* D, void* stream);
 
+/* "tcgen05.mma" page, "Weight-stationary and block scaling": the same tile as
+ * tcg_probe_mma_tile issued with the weight-stationary opcode
+ * tcgen05.mma.ws.cta_group::1.kind::f16 (M = 128, whose accumulator uses the
+ * same lane-per-row Layout D as the dense form).  N in {64, 128, 256} (the
+ * .ws shapes), K in {16, 32, 48, 64}. */
+int tcg_probe_mma_tile_ws(const void* A, const void* B, int N, int K, int is_bf16, float* D, void* stream);
+
 /* "ldmatrix / stmatrix" page example: x = 128 words viewed as (16,4,2) with
  * shared layout (16,4,2):(8,1,128); one warp issues two ldmatrix .m8n8.x2
  * into register slots {0,2} and {8,10} of a 12-word array preset to the

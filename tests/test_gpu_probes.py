@@ -212,6 +212,24 @@ def test_mma_tile_random(tcg, oracle_mod, N, K, bf16):
     assert np.all(err <= 2e-3 * S)
 
 
+@pytest.mark.parametrize("N,K,bf16", [(64, 64, 0), (128, 32, 1), (256, 64, 0), (256, 16, 1)])
+def test_mma_tile_weight_stationary(tcg, oracle_mod, N, K, bf16):
+    # .ws with M = 128: Layout D (lane = row), so the same exact result as the
+    # dense opcode; quarter-integer inputs make every sum exact in fp32
+    rng = np.random.default_rng(N + K + bf16)
+    a = (rng.integers(-4, 5, (128, K)) / 4).astype(np.float32)
+    b = (rng.integers(-4, 5, (N, K)) / 4).astype(np.float32)
+    dt = "bf16" if bf16 else "f16"
+    import synthetic as syn
+    ab, bb = syn.to_bits(a.astype(np.float64), dt), syn.to_bits(b.astype(np.float64), dt)
+    D = torch.full((128, N), float("nan"), dtype=torch.float32, device="cuda")
+    tcg.probe_mma_tile_ws(torch.from_numpy(ab.view(np.int16)).cuda(), torch.from_numpy(bb.view(np.int16)).cuda(),
+                          N, K, bf16, D)
+    assert tcg.check() == 0
+    ref, _ = oracle_mod.gemm(128, N, K, ab, 2 if bf16 else 1, 0, K, bb, 2 if bf16 else 1, 0, K)
+    assert np.array_equal(D.cpu().numpy().astype(np.float64), ref)
+
+
 # ------------------------------------------------------------- ldmatrix
 
 def test_ldmatrix_x2_page_example(tcg):
