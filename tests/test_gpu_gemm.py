@@ -53,6 +53,11 @@ SMALL = [
     ("bf16", "k", "k", 1, 300, 200, 0, "f32", "f32"),
     ("bf16", "k", "mn", 16, 520, 392, 1, "f16", "f32"),
     ("f16", "k", "mn", 32, 520, 640, 1, "f16", "f16"),
+    # 33..64 and 65..128 rows: the same 64-wide tiles with 64 / 128 staged A rows
+    ("bf16", "k", "k", 48, 700, 1000, 1, "bf16", "f32"),
+    ("f16", "k", "mn", 64, 330, 264, 0, "f32", "f32"),
+    ("bf16", "k", "k", 100, 520, 640, 0, "f16", "f32"),
+    ("f16", "k", "k", 127, 300, 136, 1, "f16", "f16"),
     # narrow N (N <= 32, K-major B): 128 x 32 tiles
     ("bf16", "k", "k", 700, 20, 1000, 1, "bf16", "f32"),
     ("f16", "mn", "k", 300, 32, 72, 0, "f16", "f32"),
@@ -221,6 +226,14 @@ def test_plan_choices_for_few_row_and_narrow_problems(tcg, oracle_mod):
     x = make_case("bf16", "k", "k", 16, 4096, 1024, seed=61)
     _check_full(tcg, oracle_mod, x, "bf16", "f32", 0)
     assert "tile 128x64" in tcg.last_plan_string() and "swapped" not in tcg.last_plan_string()
+    # 100 rows: 64-column tiles while they fit in one wave, else 128 x 256
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    x = make_case("bf16", "k", "k", 100, 2000, 512, seed=63)
+    _check_full(tcg, oracle_mod, x, "bf16", "f32", 0)
+    assert "tile 128x64" in tcg.last_plan_string(), tcg.last_plan_string()
+    x = make_case("bf16", "k", "k", 100, 64 * sms + 100, 64, seed=64)
+    _check_full(tcg, oracle_mod, x, "bf16", "f32", 0)
+    assert "tile 128x256" in tcg.last_plan_string(), tcg.last_plan_string()
     x = make_case("bf16", "k", "k", 4096, 16, 8192, seed=62)
     _check_full(tcg, oracle_mod, x, "bf16", "f32", 0)
     plan = tcg.last_plan_string()
