@@ -450,6 +450,12 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
       prefetch_tmap(&p.tmap_sfb);
     }
   }
+  // The kernel is launched as a programmatic dependent of the previous kernel
+  // on the stream: the prologue above overlaps that kernel's tail, and
+  // griddepcontrol.wait returns once it has completed and its memory is
+  // visible.  Every global access, and the TMEM allocation (a predecessor on
+  // this SM may still hold columns), comes after the wait.
+  griddep_wait();
   if (warp == 2) {
     tmem_alloc<CG>(smem_u32(tmem_slot), C::TMEM_COLS);
     tmem_relinquish<CG>();
@@ -459,6 +465,9 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
   if constexpr (CG == 2) cluster_sync();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // the next kernel on the stream may launch now; it waits for this grid's
+  // completion before it touches memory
+  griddep_launch_dependents();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer

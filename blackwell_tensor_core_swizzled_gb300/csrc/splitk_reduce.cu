@@ -15,7 +15,7 @@ namespace tcg {
 
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(const __grid_constant__ GemmParams p, int cg,
                                                             int num_clusters) {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  griddep_wait();
   const int q4 = p.bn / 4;
   const int64_t per_rank = static_cast<int64_t>(p.w_rows) * q4;
   const int64_t per_tile = cg * per_rank;

@@ -156,7 +156,8 @@ typedef struct {
   const uint8_t* SFA_img; const uint8_t* SFB_img;
   void* D; tcg_dtype d_type; int64_t ldd;
   tcg_dtype acc_type;
-  int cta_group;     /* 0 auto, 1 (one CTA per 128xN tile), 2 (CTA pair, 256xN) */
+  int cta_group;     /* 0 auto (pairs once M > 128 and N >= 1024), 1 (one CTA per
+                        128xN tile), 2 (CTA pair, 256xN) */
   int raster_group;  /* 0 auto; tiles are visited in groups of this many M tiles */
   int sf_staging;    /* block scaling, who stages the scales into TMEM:
                         0 = auto (2),
