@@ -452,6 +452,13 @@ int run_gemm(const tcg_gemm_args* args, cudaStream_t s) {
   if ((plan.ki.func == kinfo_f16(1, F16_SKINNY_M64).func || plan.ki.func == kinfo_f16(1, F16_SKINNY_M128).func) &&
       cdiv(a.N, 64) > d->sms)
     plan.ki = kinfo_f16(1, F16_WIDE);
+  // CTA pairs with few 256 x 256 tiles (at most a quarter of the SMs): 256 x
+  // 128 pair tiles, twice as many (back to back, 256 x 4096 x 4096 24.0 ->
+  // 19.0 us, 256 x 8192 x 8192 43.1 -> 35 us, 512 x 4096 x 4096 24.2 -> 19.7
+  // us; with more tiles the 128-column MMAs' lower efficiency loses: 512 x
+  // 8192 x 8192 45.4 -> 60.5 us)
+  if (plan.ki.func == kinfo_f16(2, F16_WIDE).func && 4 * cdiv(a.M, 256) * cdiv(a.N, 256) <= d->sms)
+    plan.ki = kinfo_f16(2, F16_PAIR_N128);
   if (d_trans) {
     tcg_gemm_args t = a;
     t.M = a.N;

@@ -22,7 +22,9 @@ struct KernelInfo {
 };
 
 // Variant getters (one per translation unit that instantiates kernels).
-enum F16Variant { F16_WIDE = 0, F16_SKINNY_M = 1, F16_NARROW_N = 2, F16_SKINNY_M64 = 3, F16_SKINNY_M128 = 4 };
+enum F16Variant {
+  F16_WIDE = 0, F16_SKINNY_M = 1, F16_NARROW_N = 2, F16_SKINNY_M64 = 3, F16_SKINNY_M128 = 4, F16_PAIR_N128 = 5
+};
 KernelInfo kinfo_f16(int cta_group, F16Variant v = F16_WIDE);
 KernelInfo kinfo_tf32(int cta_group);
 KernelInfo kinfo_mxf8(int cta_group);  // BN 256, one accumulator (single CTA or CTA pair)

@@ -5,6 +5,7 @@
 //   skinny M:     128 x 64 tiles staging 32 / 64 / 128 rows of A (M <= 32 /
 //                 64 / 128), 16- / 12- / 8-stage rings.
 //   narrow N:     128 x 32 tiles, 10-stage ring.
+//   pair N128:    256 x 128 pair tiles, 8-stage ring (few pair tiles).
 #include "common.h"
 #include "gemm_kernel.cuh"
 
@@ -36,6 +37,12 @@ KernelInfo kinfo_f16(int cta_group, F16Variant v) {
     // 128 x 32 tiles, 10-stage ring of 16 KB A + 4 KB B stages
     using C = GemmCfg<1, 32, 2, 10, KIND_F16>;
     return {reinterpret_cast<const void*>(&gemm_kernel<1, 32, 2, 10, KIND_F16>), C::SMEM_BYTES, 1, 32, KIND_F16,
+            C::THREADS};
+  }
+  if (v == F16_PAIR_N128) {
+    // few pair tiles: 256 x 128 pair tiles (twice as many), 8 stages
+    using C = GemmCfg<2, 128, 2, 8, KIND_F16>;
+    return {reinterpret_cast<const void*>(&gemm_kernel<2, 128, 2, 8, KIND_F16>), C::SMEM_BYTES, 2, 128, KIND_F16,
             C::THREADS};
   }
   if (cta_group == 2) {

@@ -234,6 +234,14 @@ def test_plan_choices_for_few_row_and_narrow_problems(tcg, oracle_mod):
     x = make_case("bf16", "k", "k", 100, 64 * sms + 100, 64, seed=64)
     _check_full(tcg, oracle_mod, x, "bf16", "f32", 0)
     assert "tile 128x256" in tcg.last_plan_string(), tcg.last_plan_string()
+    # CTA pairs: 256 x 128 pair tiles while the 256 x 256 ones would fill at
+    # most a quarter of the SMs, else 256 x 256
+    x = make_case("bf16", "k", "mn", 300, 1100, 512, seed=65)
+    _check_full(tcg, oracle_mod, x, "bf16", "f32", 0)
+    assert "cta_group 2, tile 256x128" in tcg.last_plan_string(), tcg.last_plan_string()
+    x = make_case("f16", "k", "k", 2100, 1100, 64, seed=66)   # 9 x 5 = 45 pair tiles > sms / 4
+    _check_full(tcg, oracle_mod, x, "f16", "f32", 0)
+    assert "cta_group 2, tile 256x256" in tcg.last_plan_string(), tcg.last_plan_string()
     x = make_case("bf16", "k", "k", 4096, 16, 8192, seed=62)
     _check_full(tcg, oracle_mod, x, "bf16", "f32", 0)
     plan = tcg.last_plan_string()
