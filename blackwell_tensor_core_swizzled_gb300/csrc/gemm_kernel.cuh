@@ -280,6 +280,12 @@ __device__ __forceinline__ void cursor_load(UnitCursor& c, const GemmParams& p) 
   } else {
     c.valid = c.u < p.num_units;
     if (!c.valid) return;
+    if (p.split == 1) {  // whole tiles: no divisions
+      c.tile = c.u;
+      c.kb0 = 0;
+      c.kb1 = p.num_k_blocks;
+      return;
+    }
     c.tile = c.u / p.split;
     const int ks = c.u - c.tile * p.split;
     c.kb0 = static_cast<int>(static_cast<int64_t>(ks) * p.num_k_blocks / p.split);
@@ -289,11 +295,15 @@ __device__ __forceinline__ void cursor_load(UnitCursor& c, const GemmParams& p) 
 
 __device__ __forceinline__ UnitCursor cursor_begin(int cluster_id, int num_clusters, const GemmParams& p) {
   UnitCursor c;
-  const int64_t T = static_cast<int64_t>(p.num_tiles) * p.num_k_blocks;
-  c.i = cluster_id * T / num_clusters;
-  c.i1 = (cluster_id + 1) * T / num_clusters;
   c.u = cluster_id;
-  c.first_tile = static_cast<int>(c.i / p.num_k_blocks);
+  c.i = c.i1 = 0;
+  c.first_tile = 0;
+  if (p.stream_k) {  // 64-bit divisions only where the stream-K range needs them
+    const int64_t T = static_cast<int64_t>(p.num_tiles) * p.num_k_blocks;
+    c.i = cluster_id * T / num_clusters;
+    c.i1 = (cluster_id + 1) * T / num_clusters;
+    c.first_tile = static_cast<int>(c.i / p.num_k_blocks);
+  }
   cursor_load(c, p);
   return c;
 }
@@ -424,7 +434,25 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
   const int num_clusters = gridDim.x / CG;
   const WaitCtx wctx{p.timeout_ns, p.err, abort_flag};
 
-  if (threadIdx.x == 0) {
+  // Prologue.  The roles' first unit (parameter reads, integer divisions)
+  // and the producer's first tile coordinates are computed while warp 3
+  // initialises the barriers and warp 2 allocates TMEM, so the first TMA
+  // copies leave right after the setup barrier.
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&p.tmap_a);
+    prefetch_tmap(&p.tmap_b);
+    if constexpr (KIND == KIND_MXF8) {
+      prefetch_tmap(&p.tmap_sfa);
+      prefetch_tmap(&p.tmap_sfb);
+    }
+  }
+  UnitCursor uc_first{};
+  int mt_first = 0, nt_first = 0;
+  if (warp != 2 && warp != 3) {
+    uc_first = cursor_begin(cluster_id, num_clusters, p);
+    if (warp == 0 && uc_first.valid) tile_coords(uc_first.tile, p, mt_first, nt_first);
+  }
+  if (threadIdx.x == 96) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
@@ -441,14 +469,6 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
     }
     *abort_flag = 0u;
     fence_mbarrier_init();
-  }
-  if (warp == 0 && lane == 0) {
-    prefetch_tmap(&p.tmap_a);
-    prefetch_tmap(&p.tmap_b);
-    if constexpr (KIND == KIND_MXF8) {
-      prefetch_tmap(&p.tmap_sfa);
-      prefetch_tmap(&p.tmap_sfb);
-    }
   }
   // The kernel is launched as a programmatic dependent of the previous kernel
   // on the stream: the prologue above overlaps that kernel's tail, and
@@ -478,10 +498,11 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
     {
       uint32_t it = 0, s = 0, ph = 0;  // ring iteration, stage, phase of stage s
       bool ok = true;
-      for (UnitCursor uc = cursor_begin(cluster_id, num_clusters, p); uc.valid && ok;
-           cursor_next(uc, num_clusters, p)) {
-        int mt, nt;
-        tile_coords(uc.tile, p, mt, nt);
+      bool first_unit = true;
+      for (UnitCursor uc = uc_first; uc.valid && ok; cursor_next(uc, num_clusters, p)) {
+        int mt = mt_first, nt = nt_first;
+        if (!first_unit) tile_coords(uc.tile, p, mt, nt);
+        first_unit = false;
         const int kb0 = uc.kb0, kb1 = uc.kb1;
         const int m0 = mt * C::MMA_M + static_cast<int>(rank) * C::BM;
         const int n0 = nt * BN + static_cast<int>(rank) * C::BN_LOCAL;
@@ -583,8 +604,7 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
       const bool full_via_sfr = KIND == KIND_MXF8 && p.sf_mode == SF_BY_CP;
       uint32_t it = 0, s = 0, ph = 0, tcount = 0;
       bool ok = true;
-      for (UnitCursor uc = cursor_begin(cluster_id, num_clusters, p); uc.valid && ok;
-           cursor_next(uc, num_clusters, p), ++tcount) {
+      for (UnitCursor uc = uc_first; uc.valid && ok; cursor_next(uc, num_clusters, p), ++tcount) {
         const int kb0 = uc.kb0, kb1 = uc.kb1;
         const int b = static_cast<int>(tcount % ACC);
         const uint32_t aph = (tcount / ACC) & 1u;
@@ -797,7 +817,7 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
     };
     auto store_tile16 = [&](int row0, int col0, const uint32_t(&h)[16]) { stage_tile(row0, col0, h, false, 0); };
     uint32_t tcount = 0;
-    for (UnitCursor uc = cursor_begin(cluster_id, num_clusters, p); uc.valid; cursor_next(uc, num_clusters, p), ++tcount) {
+    for (UnitCursor uc = uc_first; uc.valid; cursor_next(uc, num_clusters, p), ++tcount) {
       const int b = static_cast<int>(tcount % ACC);
       const uint32_t aph = (tcount / ACC) & 1u;
       if (!warp_wait(accf_bar(b), aph, wctx, SITE_EPI_ACC_FULL)) break;
