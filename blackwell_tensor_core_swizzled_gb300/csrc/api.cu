@@ -182,6 +182,8 @@ struct Plan {
   int cta_group;
 };
 
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
 int pick_cta_group(const tcg_gemm_args& a) {
   if (a.cta_group == 1 || a.cta_group == 2) return a.cta_group;
   // pairs halve the B traffic per SM and each MMA issue covers 256 rows; they
@@ -212,6 +214,39 @@ int get_plan(const tcg_gemm_args& a, Plan* plan) {
   }
   // an MN-major B half tile must be whole 128-byte swizzle spans
   if (a.b_major == TCG_MN_MAJOR && (plan->ki.bn / cg) % (128 / esize_of(a.in_type)) != 0) return TCG_ERR_UNSUPPORTED;
+  return TCG_OK;
+}
+
+// The variant for a problem on a device with `sms` SMs: get_plan's choice
+// refined by the tile counts, and whether to run the transposed product with
+// the operands swapped.
+int choose_plan(const tcg_gemm_args& a, int sms, Plan* plan, bool* swap_operands) {
+  if (int rc = get_plan(a, plan)) return rc;
+  const bool f16_kind = a.in_type == TCG_IN_F16 || a.in_type == TCG_IN_BF16;
+  const void* f = plan->ki.func;
+  // Few rows of A against very many columns of B (decode-like shapes whose
+  // 64-column skinny tiles would take more than one wave): compute the
+  // transposed product D^T = B^T A^T with the operands' roles swapped, so
+  // that B fills the 128-row MMA side (half as many tiles, one pass each); the
+  // few rows of A become a 32-column tile and the epilogue stores the result
+  // transposed.  Measured on 16-row problems: 16 x 16384 x 4096 35.5 us
+  // swapped vs 39.6 us skinny; 16 x 8192 x 8192 38.6 us skinny (128 tiles, one
+  // pass) vs 40.6 us swapped (64 tiles: stream-K).  f32 accumulation, single
+  // CTAs, K-major A.
+  *swap_operands = f16_kind && a.acc_type == TCG_F32 && plan->cta_group == 1 && a.M <= 32 &&
+                   a.a_major == TCG_K_MAJOR && cdiv(a.N, 64) > sms;
+  // 33..128 rows: the 64-column skinny tiles only while they fit in one wave
+  // (128 x 8192 x 8192: 43.6 us vs 47.7 us on 128 x 256 tiles; 128 x 32768 x
+  // 4096, 512 skinny tiles: 72.3 us vs 64.1 us)
+  if ((f == kinfo_f16(1, F16_SKINNY_M64).func || f == kinfo_f16(1, F16_SKINNY_M128).func) && cdiv(a.N, 64) > sms)
+    plan->ki = kinfo_f16(1, F16_WIDE);
+  // CTA pairs with few 256 x 256 tiles (at most a quarter of the SMs): 256 x
+  // 128 pair tiles, twice as many (back to back, 256 x 4096 x 4096 24.0 ->
+  // 19.0 us, 256 x 8192 x 8192 43.1 -> 35 us, 512 x 4096 x 4096 24.2 -> 19.7
+  // us; with more tiles the 128-column MMAs' lower efficiency loses: 512 x
+  // 8192 x 8192 45.4 -> 60.5 us)
+  if (f == kinfo_f16(2, F16_WIDE).func && 4 * cdiv(a.M, 256) * cdiv(a.N, 256) <= sms)
+    plan->ki = kinfo_f16(2, F16_PAIR_N128);
   return TCG_OK;
 }
 
@@ -281,8 +316,6 @@ int launch_gemm(const KernelInfo& ki, const GemmParams& prm, int clusters, cudaS
   if (e != cudaSuccess) return record_cuda(e);
   return TCG_OK;
 }
-
-int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 int64_t sf_image_bytes(int64_t rows, int64_t K, int tile_rows) {
   const int64_t ksteps = cdiv(cdiv(K, 32), 4);
@@ -435,30 +468,8 @@ int run_gemm(const tcg_gemm_args* args, cudaStream_t s) {
     return TCG_OK;
   }
 
-  // Few rows of A against very many columns of B (decode-like shapes whose
-  // 64-column skinny tiles would take more than one wave): compute the
-  // transposed product D^T = B^T A^T with the operands' roles swapped, so
-  // that B fills the 128-row MMA side (half as many tiles, one pass each); the
-  // few rows of A become a 32-column tile and the epilogue stores the result
-  // transposed.  Measured on 16-row problems: 16 x 16384 x 4096 35.5 us
-  // swapped vs 39.6 us skinny; 16 x 8192 x 8192 38.6 us skinny (128 tiles, one
-  // pass) vs 40.6 us swapped (64 tiles: stream-K).  f32 accumulation, single
-  // CTAs, K-major A.
-  const bool d_trans = !scaled && a.in_type != TCG_IN_TF32 && a.acc_type == TCG_F32 && plan.cta_group == 1 &&
-                       a.M <= 32 && a.a_major == TCG_K_MAJOR && cdiv(a.N, 64) > d->sms;
-  // 33..128 rows: the 64-column skinny tiles only while they fit in one wave
-  // (128 x 8192 x 8192: 43.6 us vs 47.7 us on 128 x 256 tiles; 128 x 32768 x
-  // 4096, 512 skinny tiles: 72.3 us vs 64.1 us)
-  if ((plan.ki.func == kinfo_f16(1, F16_SKINNY_M64).func || plan.ki.func == kinfo_f16(1, F16_SKINNY_M128).func) &&
-      cdiv(a.N, 64) > d->sms)
-    plan.ki = kinfo_f16(1, F16_WIDE);
-  // CTA pairs with few 256 x 256 tiles (at most a quarter of the SMs): 256 x
-  // 128 pair tiles, twice as many (back to back, 256 x 4096 x 4096 24.0 ->
-  // 19.0 us, 256 x 8192 x 8192 43.1 -> 35 us, 512 x 4096 x 4096 24.2 -> 19.7
-  // us; with more tiles the 128-column MMAs' lower efficiency loses: 512 x
-  // 8192 x 8192 45.4 -> 60.5 us)
-  if (plan.ki.func == kinfo_f16(2, F16_WIDE).func && 4 * cdiv(a.M, 256) * cdiv(a.N, 256) <= d->sms)
-    plan.ki = kinfo_f16(2, F16_PAIR_N128);
+  bool d_trans = false;
+  if (int rc = choose_plan(a, d->sms, &plan, &d_trans)) return rc;
   if (d_trans) {
     tcg_gemm_args t = a;
     t.M = a.N;
