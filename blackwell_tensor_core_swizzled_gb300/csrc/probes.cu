@@ -184,14 +184,20 @@ __device__ __forceinline__ void ld_shape(uint32_t taddr, uint32_t* r) {
     if constexpr (NUM == 1) ldx_32x32b_x1(taddr, r);
     if constexpr (NUM == 2) ldx_32x32b_x2(taddr, r);
     if constexpr (NUM == 4) ldx_32x32b_x4(taddr, r);
+    if constexpr (NUM == 8) ldx_32x32b_x8(taddr, r);
+    if constexpr (NUM == 16) ldx_32x32b_x16(taddr, r);
+    if constexpr (NUM == 32) ldx_32x32b_x32(taddr, r);
   } else if constexpr (SHAPE == 1) {
     if constexpr (NUM == 1) ldx_16x64b_x1(taddr, r);
     if constexpr (NUM == 2) ldx_16x64b_x2(taddr, r);
     if constexpr (NUM == 4) ldx_16x64b_x4(taddr, r);
+    if constexpr (NUM == 8) ldx_16x64b_x8(taddr, r);
+    if constexpr (NUM == 16) ldx_16x64b_x16(taddr, r);
   } else if constexpr (SHAPE == 2) {
     if constexpr (NUM == 1) ldx_16x128b_x1(taddr, r);
     if constexpr (NUM == 2) ldx_16x128b_x2(taddr, r);
     if constexpr (NUM == 4) ldx_16x128b_x4(taddr, r);
+    if constexpr (NUM == 8) ldx_16x128b_x8(taddr, r);
   } else {
     if constexpr (NUM == 1) ldx_16x256b_x1(taddr, r);
     if constexpr (NUM == 2) ldx_16x256b_x2(taddr, r);
@@ -432,9 +438,10 @@ extern "C" int tcg_probe_ld_shape(const uint32_t* in, int shape, int num, int ha
   const cudaStream_t s = as_stream(stream);
 #define TCG_LD_CASE(SH, NU) \
   if (shape == SH && num == NU) { probe_ld_shape_kernel<SH, NU><<<1, 128, 0, s>>>(in, half, out); return finish_launch(1); }
-  TCG_LD_CASE(0, 1) TCG_LD_CASE(0, 2) TCG_LD_CASE(0, 4)
-  TCG_LD_CASE(1, 1) TCG_LD_CASE(1, 2) TCG_LD_CASE(1, 4)
-  TCG_LD_CASE(2, 1) TCG_LD_CASE(2, 2) TCG_LD_CASE(2, 4)
+  // every repeat count whose columns fit the 32-column image
+  TCG_LD_CASE(0, 1) TCG_LD_CASE(0, 2) TCG_LD_CASE(0, 4) TCG_LD_CASE(0, 8) TCG_LD_CASE(0, 16) TCG_LD_CASE(0, 32)
+  TCG_LD_CASE(1, 1) TCG_LD_CASE(1, 2) TCG_LD_CASE(1, 4) TCG_LD_CASE(1, 8) TCG_LD_CASE(1, 16)
+  TCG_LD_CASE(2, 1) TCG_LD_CASE(2, 2) TCG_LD_CASE(2, 4) TCG_LD_CASE(2, 8)
   TCG_LD_CASE(3, 1) TCG_LD_CASE(3, 2) TCG_LD_CASE(3, 4)
 #undef TCG_LD_CASE
   return TCG_ERR_INVALID;

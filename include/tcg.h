@@ -277,7 +277,9 @@ int tcg_probe_cp(const uint32_t* image, int image_words, int shape,
  * columns, lane-major) with .32x32b.x32, then every warp loads lanes
  * [32w + half*16, +16) with tcgen05.ld.<shape>.x<num>; out receives, for
  * thread t, its registers at out[t*regs + r] (regs = registers per lane).
- * shape: 0 = 32x32b, 1 = 16x64b, 2 = 16x128b, 3 = 16x256b; num in {1,2,4};
+ * shape: 0 = 32x32b, 1 = 16x64b, 2 = 16x128b, 3 = 16x256b; num in {1,2,4} and
+ * the larger repeats whose columns fit the image (32x32b up to 32, 16x64b up
+ * to 16, 16x128b up to 8);
  * half in {0,1} (16-row shapes only). */
 int tcg_probe_ld_shape(const uint32_t* in, int shape, int num, int half,
                        uint32_t* out, void* stream);

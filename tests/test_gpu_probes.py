@@ -164,11 +164,13 @@ SHAPE_ID = {"32x32b": 0, "16x64b": 1, "16x128b": 2, "16x256b": 3}
 
 
 @pytest.mark.parametrize("shape", list(SHAPE_ID))
-@pytest.mark.parametrize("num", [1, 2, 4])
+@pytest.mark.parametrize("num", [1, 2, 4, 8, 16, 32])
 @pytest.mark.parametrize("half", [0, 1])
 def test_ld_register_images(tcg, shape, num, half):
     if shape == "32x32b" and half == 1:
         pytest.skip("32-row shape has no half")
+    if L.ld_atom_extent(shape, num)[1] > 32:
+        pytest.skip("wider than the 32-column image")
     image = (np.arange(128)[:, None] * 32 + np.arange(32)[None, :]).astype(np.uint32)
     out = torch.zeros((128, 4 * num), dtype=torch.int32, device="cuda")
     tcg.probe_ld_shape(_u32(image), SHAPE_ID[shape], num, half, out)
