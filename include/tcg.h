@@ -23,7 +23,8 @@
  *
  * Ownership: every pointer is caller-owned DEVICE memory (except where a
  * function says host) that must stay valid until the work queued on `stream`
- * has finished.  All calls are asynchronous on `stream` (a cudaStream_t; 0 is
+ * has finished.  D must not overlap A, B or the scale arrays (tiles of D are
+ * written while other tiles still read the operands).  All calls are asynchronous on `stream` (a cudaStream_t; 0 is
  * the legacy default stream) and never synchronise the host, except
  * tcg_check().  The block-scaled GEMM with plain scale arrays, and split-K
  * (see tcg_gemm_args::split_k; automatic for problems with few output tiles),
