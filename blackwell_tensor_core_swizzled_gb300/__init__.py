@@ -54,6 +54,7 @@ _SIGS = {
     "tcg_last_error_string": ([], ctypes.c_char_p),
     "tcg_last_launch_count": ([], _i32),
     "tcg_last_plan_string": ([], ctypes.c_char_p),
+    "tcg_trace_next": ([_vp, _i32], _i32),
     "tcg_probe_tmem_roundtrip": ([_vp, _vp, _i32, _vp], _i32),
     "tcg_probe_cp": ([_vp, _i32, _i32, _u32, _u32, _u32, _i32, _vp, _vp], _i32),
     "tcg_probe_ld_shape": ([_vp, _i32, _i32, _i32, _vp, _vp], _i32),
@@ -206,6 +207,11 @@ def last_launch_count() -> int:
 
 def last_plan_string() -> str:
     return _lib.tcg_last_plan_string().decode()
+
+
+def trace_next(buf, max_ctas: int):
+    """Record the next GEMM launch's phase stamps into ``buf`` (see tcg.h)."""
+    return _ok(_lib.tcg_trace_next(_ptr(buf), max_ctas), "trace_next")
 
 
 def probe_tmem_roundtrip(inp, out, ncols, stream=None):

@@ -29,6 +29,9 @@ namespace {
 thread_local std::string t_last_error;
 thread_local int t_last_launches = 0;
 thread_local std::string t_last_plan;
+// phase trace requested for the next GEMM launch on this thread
+thread_local unsigned long long* t_trace_buf = nullptr;
+thread_local int t_trace_ctas = 0;
 std::atomic<uint64_t> g_timeout_ns{2000000000ull};
 
 constexpr int kMaxDevices = 64;
@@ -538,6 +541,10 @@ int run_gemm(const tcg_gemm_args* args, cudaStream_t s) {
   }
   prm.err = d->err;
   prm.timeout_ns = g_timeout_ns.load();
+  prm.trace = t_trace_buf;
+  prm.trace_ctas = t_trace_ctas;
+  t_trace_buf = nullptr;
+  t_trace_ctas = 0;
   // auto: the MMA warp copies the scales itself (fastest or tied for both
   // CTA groups once the issue loops are warp-uniform; no extra barriers)
   prm.sf_mode = a.sf_staging == 1   ? SF_BY_WARPS
@@ -853,5 +860,13 @@ const char* tcg_last_error_string(void) { return t_last_error.c_str(); }
 int tcg_last_launch_count(void) { return t_last_launches; }
 
 const char* tcg_last_plan_string(void) { return t_last_plan.c_str(); }
+
+int tcg_trace_next(unsigned long long* buf, int max_ctas) {
+  if ((buf == nullptr) != (max_ctas == 0) || max_ctas < 0) return TCG_ERR_INVALID;
+  if (reinterpret_cast<uintptr_t>(buf) % 8) return TCG_ERR_ALIGNMENT;
+  t_trace_buf = buf;
+  t_trace_ctas = max_ctas;
+  return TCG_OK;
+}
 
 }  // extern "C"

@@ -132,7 +132,28 @@ struct GemmParams {
   // With tcgen05.cp (a pair copies both CTAs' smem) the scale images complete
   // on the pair leader's full[s] barrier together with A and B.
   int sf_mode;
+  // optional phase trace (null: off): per CTA, TRACE_SLOTS globaltimer
+  // stamps (see TraceSlot) and the number of units it processed
+  unsigned long long* trace;
+  int trace_ctas;
 };
+
+enum TraceSlot : int {
+  TRACE_ENTRY = 0,        // kernel entry
+  TRACE_SETUP = 1,        // barriers and TMEM ready
+  TRACE_PRODUCER = 2,     // producer starts its first unit
+  TRACE_FIRST_UNIT = 3,   // MMA warp has issued its first unit (pair leader / single CTA)
+  TRACE_LAST_COMMIT = 4,  // last tile's accumulator committed (MMA warp)
+  TRACE_EPI_DONE = 5,     // epilogue stores drained (warp 4)
+  TRACE_EXIT = 6,         // TMEM released, CTA about to exit
+  TRACE_UNITS = 7,        // units processed (MMA warp), not a time
+  TRACE_SLOTS = 8
+};
+
+__device__ __forceinline__ void trace_stamp(const GemmParams& p, int slot) {
+  if (p.trace && static_cast<int>(blockIdx.x) < p.trace_ctas)
+    p.trace[static_cast<int64_t>(blockIdx.x) * TRACE_SLOTS + slot] = globaltimer();
+}
 
 // A_ROWS < 128 (single CTA, K-major A, M <= A_ROWS): only that many rows of
 // A are staged per ring stage, so many more stages fit; the MMA still reads a
@@ -411,6 +432,7 @@ __device__ __forceinline__ void store_col32(const GemmParams& p, int row, int co
 template <int CG, int BN, int ACC, int STAGES, int KIND, int A_ROWS = 128>
 __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
   using C = GemmCfg<CG, BN, ACC, STAGES, KIND, A_ROWS>;
+  if (threadIdx.x == 0) trace_stamp(p, TRACE_ENTRY);
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -485,6 +507,7 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
   if constexpr (CG == 2) cluster_sync();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  if (threadIdx.x == 0) trace_stamp(p, TRACE_SETUP);
   // the next kernel on the stream may launch now; it waits for this grid's
   // completion before it touches memory
   griddep_launch_dependents();
@@ -499,6 +522,7 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
       uint32_t it = 0, s = 0, ph = 0;  // ring iteration, stage, phase of stage s
       bool ok = true;
       bool first_unit = true;
+      if (lane == 0) trace_stamp(p, TRACE_PRODUCER);
       for (UnitCursor uc = uc_first; uc.valid && ok; cursor_next(uc, num_clusters, p)) {
         int mt = mt_first, nt = nt_first;
         if (!first_unit) tile_coords(uc.tile, p, mt, nt);
@@ -677,6 +701,12 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
         if (!ok) break;
         if (elect_one()) tc_commit<CG>(accf_bar(b));
         __syncwarp();
+        if (tcount == 0 && lane == 0) trace_stamp(p, TRACE_FIRST_UNIT);
+      }
+      if (lane == 0) {
+        trace_stamp(p, TRACE_LAST_COMMIT);
+        if (p.trace && static_cast<int>(blockIdx.x) < p.trace_ctas)
+          p.trace[static_cast<int64_t>(blockIdx.x) * TRACE_SLOTS + TRACE_UNITS] = tcount;
       }
       if (!ok && elect_one()) {
         // Drain: wait (bounded) for every MMA / cp this thread issued.
@@ -942,6 +972,7 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
     // the staged tiles must be written out before the CTA ends
     if (lane == 0) bulk_wait_group_all();
     __syncwarp();
+    if (warp == 4 && lane == 0) trace_stamp(p, TRACE_EPI_DONE);
   }
 
   // ------------------------------------------------------------ teardown
@@ -950,7 +981,10 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
   __syncwarp();
   if constexpr (CG == 2) cluster_sync();
   tc_fence_after();
-  if (warp == 2) tmem_dealloc<CG>(tmem_base, C::TMEM_COLS);
+  if (warp == 2) {
+    tmem_dealloc<CG>(tmem_base, C::TMEM_COLS);
+    if (lane == 0) trace_stamp(p, TRACE_EXIT);
+  }
 }
 
 }  // namespace tcg

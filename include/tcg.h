@@ -247,6 +247,19 @@ int tcg_last_launch_count(void);
  * owned by the library and valid until this thread's next GEMM call. */
 const char* tcg_last_plan_string(void);
 
+/* Phase trace of the next GEMM kernel launched by this thread (tracing is off
+ * otherwise and costs one untaken branch per stamp).  buf: device memory of
+ * max_ctas x 8 uint64 (8-byte aligned); CTA c (c < max_ctas) writes slots
+ * [8c, 8c+8): globaltimer nanoseconds at 0 kernel entry, 1 barriers and TMEM
+ * ready, 2 producer starts its first unit, 3 first unit's MMAs issued, 4 last
+ * accumulator committed, 5 epilogue stores drained, 6 TMEM released; slot 7
+ * = units (tiles or tile parts) the CTA computed.  Slots 3, 4 and 7 are
+ * written by the pair leader only (CTA pairs issue from the leader).  No
+ * stamp sits inside the per-stage loops.
+ * Untouched slots keep their contents.  buf = NULL with max_ctas = 0 cancels
+ * a pending request. */
+int tcg_trace_next(unsigned long long* buf, int max_ctas);
+
 /* ---------------------------------------------------------------------------
  * Layout probes: single-CTA kernels that expose one tcgen05 / ldmatrix
  * mechanism each, so the tests can compare it bit for bit with the pages'

@@ -70,6 +70,11 @@ def test_host_validation_rejects_bad_arguments(tcg):
     for shape in (-1, 12):
         assert tcg.raw_call("tcg_probe_cp", 0x10000, 512, shape, 0, 16, 128, 0, 0x20000, None) == tcg.ERR_INVALID
     assert tcg.raw_call("tcg_probe_cp", 0x10000, 256, 9, 0, 16, 128, 0, 0x20000, None) == tcg.ERR_INVALID
+    # trace request: buffer and count go together; null + 0 cancels
+    assert tcg.raw_call("tcg_trace_next", None, 4) == tcg.ERR_INVALID
+    assert tcg.raw_call("tcg_trace_next", 0x10000, 0) == tcg.ERR_INVALID
+    assert tcg.raw_call("tcg_trace_next", 0x10004, 4) == tcg.ERR_ALIGNMENT
+    assert tcg.raw_call("tcg_trace_next", None, 0) == tcg.OK
     # .ws probe: N must be one of the weight-stationary widths 64 / 128 / 256
     for n in (32, 96, 512):
         assert tcg.raw_call("tcg_probe_mma_tile_ws", 0x10000, 0x20000, n, 64, 0, 0x30000, None) == tcg.ERR_INVALID

@@ -323,6 +323,35 @@ def test_absurd_tile_counts_are_refused_before_any_launch(tcg):
     assert tcg.check() == 0
 
 
+def test_phase_trace(tcg, oracle_mod):
+    # 1024 x 1024 x 512 on 256 x 128 pair tiles: 32 clusters, one tile each
+    import re
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    buf = torch.zeros((sms, 8), dtype=torch.int64, device="cuda")
+    x = make_case("bf16", "k", "k", 1024, 1024, 512, seed=72)
+    tcg.trace_next(buf, sms)
+    _check_full(tcg, oracle_mod, x, "bf16", "f32", 0)
+    plan = tcg.last_plan_string()
+    m = re.search(r"cta_group (\d), tile (\d+)x(\d+), (\d+) clusters", plan)
+    cg, clusters = int(m.group(1)), int(m.group(4))
+    tiles = -(-1024 // int(m.group(2))) * -(-1024 // int(m.group(3)))
+    t = buf.cpu().numpy()
+    ctas = cg * clusters
+    assert np.all(t[ctas:] == 0)                        # no stamps beyond the grid
+    units = 0
+    for c in range(ctas):
+        e, su, pr, fu, lc, ep, ex, un = t[c]
+        assert 0 < e <= su <= pr and su <= ep <= ex and ex - e < 10**9, (c, t[c])
+        if c % cg == 0:                                 # the MMA warp of the leader
+            assert pr <= fu <= lc <= ep and un >= 1, (c, t[c])
+            units += un
+    assert units == tiles
+    # the request covers one launch only
+    buf.zero_()
+    _check_full(tcg, oracle_mod, x, "bf16", "f32", 0)
+    assert int(buf.abs().sum().item()) == 0
+
+
 def test_k_zero_zeroes_d_and_empty_is_noop(tcg):
     D = torch.full((64, 80), 7.0, dtype=torch.float32, device="cuda")
     tcg.gemm_bf16(64, 80, 0, 0, 0, 0, 0, 0, 0, D, 0, 80, 0)
