@@ -15,8 +15,9 @@
 //               tcgen05.commit -> empty[s]; at the end of a tile a commit ->
 //               acc_full[b];
 //   warp 2      TMEM allocation / deallocation (512 columns);
-//   warp 3      (block scaling, GemmParams::sf_mode SF_BY_CP) a separate
-//               copy warp: tcgen05.cp + commit -> sf_ready[slot];
+//   warp 3      barrier initialisation; with block scaling and
+//               GemmParams::sf_mode SF_BY_CP a separate copy warp:
+//               tcgen05.cp + commit -> sf_ready[slot];
 //   warps 4..7  epilogue: tcgen05.ld .32x32b from accumulator b (warp w
 //               reads lanes 32*(w%4)..+31), convert, store to global (16-bit
 //               outputs through a shared staging tile and a TMA tile store),
@@ -39,6 +40,9 @@
 // tcgen05.fence::after_thread_sync, ld, wait::ld).  Block-scale placement in
 // TMEM is the page's "lane r%32, byte-column 4*(r//32)+sf, four replicas",
 // produced by tcgen05.cp .32x128b.warpx4 ("tcgen05.cp" page, shape table).
+//
+// The kernel is launched as a programmatic dependent of the previous kernel on
+// its stream (griddepcontrol.wait before any global access or TMEM allocation).
 //
 // Every mbarrier wait is bounded (GemmParams::timeout_ns); a wait that runs
 // out records an error word, raises a CTA-local abort flag and the kernel
