@@ -4,8 +4,12 @@ One step = one full GEMM of the workload (all hot-path stages: scale
 rearrangement for block-scaled inputs, TMA ring, descriptor walk, tcgen05.mma,
 tcgen05.ld epilogue), inputs already resident in HBM.  Default workload: bf16
 M=N=K=8192 with CTA pairs (cta_group::2, 256x256 pair tiles), fp32
-accumulation, bf16 output; the block-scaled MXFP8 8192^3 GEMM is measured the
-same way and reported under "secondary".
+accumulation, bf16 output.  The other workloads -- block-scaled MXFP8
+8192^3, bf16 4096^3 (A K-major, B MN-major, single CTAs), tf32 2048 x 2048 x
+8192, f16-in / f16-accumulate 8192^3 and the HBM-bound 16 x 8192 x 8192 --
+are measured the same way and reported under "secondary", and a ~1.5 s
+back-to-back pass of the headline ("sustained") is compared with the
+sustained cuBLAS figure, with the SM clock seen in that window.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 
@@ -46,6 +50,8 @@ ESIZE = {"f16": 2, "bf16": 2, "tf32": 4, "e4m3": 1}
 # nominal dense tensor rate relative to bf16 (NVIDIA GB300 figures: tf32 1.1,
 # bf16/fp16 2.25, fp8 4.5 PFLOP/s)
 NOMINAL_RATIO = {"bf16": 1.0, "f16": 1.0, "tf32": 1.1 / 2.25, "e4m3": 2.0}
+# NVIDIA's dense (no 2:4 sparsity) GB300 datasheet rates, TFLOP/s
+DATASHEET_DENSE_TFLOPS = {"bf16": 2250.0, "f16": 2250.0, "tf32": 1100.0, "e4m3": 4500.0}
 PROFILE_DIR = os.path.join(ROOT, "profiles")
 KERNEL_SOURCES = ["gemm_kernel.cuh", "ptx.cuh", "desc.cuh", "gemm_f16.cu", "gemm_tf32.cu", "gemm_mxf8.cu", "api.cu",
                   "splitk_reduce.cu"]
@@ -86,7 +92,7 @@ def profiled_traffic(workload: str):
 # ----------------------------------------------------------------- clocks
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 100 ms in a thread."""
+    """nvidia-smi clocks / throttle reasons sampled every 20 ms in a thread."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
@@ -106,7 +112,7 @@ class ClockSampler:
                 sel = ["-i", f"{getattr(props, 'pci_domain_id', 0):08X}:{bus:02X}:"
                              f"{getattr(props, 'pci_device_id', 0):02X}.0"]
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                                          "-lms", "100"] + sel, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                          "-lms", "20"] + sel, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
                                          text=True, bufsize=1)
         except Exception:
             self.proc = None
@@ -132,7 +138,7 @@ class ClockSampler:
         window = "timed region"
         if not inside:  # region shorter than the sampling period: nearest samples under load
             inside = sorted(self.samples, key=lambda s: min(abs(s[0] - t0), abs(s[0] - t1)))[:3]
-            window = "nearest samples to the timed region (shorter than 100 ms)"
+            window = "nearest samples to the timed region (shorter than the sampling period)"
 
         def num(v):
             try:
@@ -335,8 +341,11 @@ def roofline(w, kernel_ms, peaks, traffic, timed_s):
     peak = (peaks["bf16_tflops_sustained"] if regime == "sustained" else peaks["bf16_tflops"]) * ratio
     src = (f"{peaks['source']} bf16 {regime} (timed region {timed_s * 1e3:.0f} ms)"
            + ("" if ratio == 1.0 else f" x nominal {w.dtype}/bf16 ratio {ratio:g}"))
+    sheet = DATASHEET_DENSE_TFLOPS[w.dtype]
     return {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak, 1), "unit": "TFLOP/s",
             "frac": round(achieved / peak, 4), "traffic": traffic, "peak_source": src,
+            "frac_of_datasheet_dense": round(achieved / sheet, 4),
+            "datasheet_dense_peak": sheet,
             "kernel": "tcg::gemm_kernel", "algorithmic_flops_per_launch": flops}
 
 
@@ -417,8 +426,11 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="bf16_8192_cta2", choices=sorted(syn.WORKLOADS))
-    ap.add_argument("--secondary", default="mxf8_8192,bf16_skinny_m16",
+    ap.add_argument("--secondary",
+                    default="mxf8_8192,bf16_skinny_m16,bf16_4096_kmn_cta1,tf32_2048x2048x8192,f16acc_8192_cta2",
                     help="comma list of extra workloads ('' for none)")
+    ap.add_argument("--sustained-s", type=float, default=1.5,
+                    help="length of the back-to-back sustained pass of the headline workload (0: skip)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-rows", type=int, default=0, help="oracle rows in the CPU baseline (0: 2 per thread)")
     args = ap.parse_args()
@@ -463,8 +475,21 @@ def main():
     peaks = measured_peaks()
     sampler = ClockSampler(torch.cuda.current_device())
     sampler.start()
+    sustained = None
     try:
         res = run_workload(tcg, torch, w, args.steps, args.warmup, dctx)
+        if args.sustained_s > 0:
+            # Back-to-back headline GEMMs for ~1.5 s: long enough to reach the
+            # power-capped clock, compared with the sustained cuBLAS figure,
+            # with the clock record of that window.
+            n_sus = max(args.steps, int(args.sustained_s / max(res["kernel_ms"] * 1e-3, 1e-6)))
+            rs = run_workload(tcg, torch, w, n_sus, 0, dctx, measure_e2e=False)
+            v_s, t_s = whole_job(dctx, 2.0 * w.M * w.N * w.K, n_sus, rs["total_ms"])
+            rl_s = roofline(w, rs["total_ms"] / n_sus, peaks, None, rs["total_ms"] * 1e-3)
+            sustained = {"value": round(v_s, 1), "unit": UNIT, "steps": n_sus, "ms_per_step": round(t_s / n_sus, 4),
+                         "timed_s": round(rs["total_ms"] * 1e-3, 3), "frac": rl_s["frac"], "peak": rl_s["peak"],
+                         "peak_source": rl_s["peak_source"], "frac_of_datasheet_dense": rl_s["frac_of_datasheet_dense"],
+                         "clocks": sampler.summary(rs["t0"], rs["t1"])}
         sec = []
         for name in [s for s in args.secondary.split(",") if s and s != w.name]:
             ws = syn.WORKLOADS[name]
@@ -506,7 +531,8 @@ def main():
                    "l2": "inputs larger than L2 (no flush): A+B = "
                          f"{(w.M * w.K + w.N * w.K) * ESIZE[w.dtype] / 2**20:.0f} MiB",
                    "parallelism": f"replicas x{dctx.world}"},
-        "pct_dense_peak": round(100 * rl["frac"], 2),
+        "pct_of_measured_peak": round(100 * rl["frac"], 2),
+        "pct_of_datasheet_dense_peak": round(100 * rl["frac_of_datasheet_dense"], 2),
         "roofline": rl,
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_val, 1), "unit": UNIT, "h2d_bytes_per_step": res["h2d"],
@@ -515,6 +541,7 @@ def main():
                             "compute / download streams"},
         "gpu_launches": res["launches"],
         "clocks": clocks,
+        "sustained": sustained,
         "secondary": sec,
     }
     print(json.dumps(line))

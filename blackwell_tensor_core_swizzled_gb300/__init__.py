@@ -34,6 +34,12 @@ class GemmArgs(ctypes.Structure):
                 ("cta_group", _i32), ("raster_group", _i32), ("sf_staging", _i32), ("split_k", _i32)]
 
 
+class ProbeOperand(ctypes.Structure):
+    """Mirror of ``tcg_probe_operand``."""
+    _fields_ = [("image", _vp), ("bytes", _i32), ("major", _i32), ("ldo", _u32), ("sdo", _u32),
+                ("swizzle", _i32), ("start", _u32 * 8)]
+
+
 _GEMM_SIG = [_i64, _i64, _i64, _vp, _i32, _i64, _vp, _i32, _i64, _vp, _i32, _i64, _i32, _vp]
 _SIGS = {
     "tcg_gemm_f16": (_GEMM_SIG, _i32),
@@ -60,6 +66,8 @@ _SIGS = {
     "tcg_probe_ld_shape": ([_vp, _i32, _i32, _i32, _vp, _vp], _i32),
     "tcg_probe_mma_tile": ([_vp, _vp, _i32, _i32, _i32, _vp, _vp], _i32),
     "tcg_probe_mma_tile_ws": ([_vp, _vp, _i32, _i32, _i32, _vp, _vp], _i32),
+    "tcg_probe_mma_image": ([ctypes.POINTER(ProbeOperand), ctypes.POINTER(ProbeOperand), _i32, _i32, _i32, _vp,
+                             _vp], _i32),
     "tcg_probe_ldmatrix_x2": ([_vp, _vp, _vp], _i32),
     "tcg_probe_wait_timeout": ([_u64, _vp], _i32),
 }
@@ -234,6 +242,16 @@ def probe_mma_tile(A, B, N, K, is_bf16, D, stream=None):
 def probe_mma_tile_ws(A, B, N, K, is_bf16, D, stream=None):
     return _ok(_lib.tcg_probe_mma_tile_ws(_ptr(A), _ptr(B), N, K, is_bf16, _ptr(D), _stream(stream)),
                "probe_mma_tile_ws")
+
+
+def probe_operand(image, nbytes, major, ldo, sdo, swizzle, starts) -> ProbeOperand:
+    st = (_u32 * 8)(*(list(starts) + [0] * (8 - len(starts))))
+    return ProbeOperand(_ptr(image), nbytes, major, ldo, sdo, swizzle, st)
+
+
+def probe_mma_image(a: ProbeOperand, b: ProbeOperand, in_type, N, ksteps, D, stream=None):
+    return _ok(_lib.tcg_probe_mma_image(ctypes.byref(a), ctypes.byref(b), in_type, N, ksteps, _ptr(D),
+                                        _stream(stream)), "probe_mma_image")
 
 
 def probe_ldmatrix_x2(x, out, stream=None):

@@ -12,7 +12,9 @@
 // Limits and sharing:
 //  * the two scale images of one call must fit in kScratchBytes (16 MiB;
 //    an 8192 x 8192 x 8192 problem needs 4 MiB); larger problems are
-//    rejected with TCG_ERR_UNSUPPORTED before anything is queued;
+//    rejected with TCG_ERR_UNSUPPORTED.  Every argument (sizes, pointers,
+//    alignment, output and accumulator types, the device) is checked before
+//    anything is queued, so a call that fails leaves the array untouched;
 //  * every call on every stream of a device uses the same array, which keeps
 //    the previous call's contents.  Each call rewrites every byte of the image
 //    region it reads (padding included), so nothing needs clearing, but calls
@@ -23,6 +25,7 @@
 //    before any stream capture.
 #include <cuda_runtime.h>
 
+#include <cstdint>
 #include <cstring>
 #include <mutex>
 
@@ -70,6 +73,11 @@ extern "C" int tcg_gemm_mxf8_blockscaled_noalloc(int64_t M, int64_t N, int64_t K
     return tcg_gemm_mxf8_blockscaled(M, N, K, A, a_major, lda, B, b_major, ldb, SFA, SFB, D, d_type, ldd, acc_type,
                                      stream);
   if (!A || !B || !D || !SFA || !SFB) return TCG_ERR_INVALID;
+  if (d_type != TCG_F32 && d_type != TCG_F16 && d_type != TCG_BF16) return TCG_ERR_INVALID;
+  if (ldd == 0) ldd = N;
+  if (ldd < N) return TCG_ERR_INVALID;
+  if (reinterpret_cast<uintptr_t>(D) % (d_type == TCG_F32 ? 4 : 2)) return TCG_ERR_ALIGNMENT;
+  if (M > INT32_MAX / 2 || N > INT32_MAX / 2 || K > INT32_MAX / 2) return TCG_ERR_UNSUPPORTED;
   if (a_major != TCG_K_MAJOR && a_major != TCG_MN_MAJOR) return TCG_ERR_INVALID;
   if (b_major != TCG_K_MAJOR && b_major != TCG_MN_MAJOR) return TCG_ERR_INVALID;
   // operand checks before anything is queued (E4M3: one byte per element)
@@ -92,17 +100,14 @@ extern "C" int tcg_gemm_mxf8_blockscaled_noalloc(int64_t M, int64_t N, int64_t K
   }
 
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) {
-    cudaGetLastError();
-    return TCG_ERR_NO_DEVICE;
-  }
+  if (int rc = tcg::current_device_checked(&dev)) return rc;  // an sm_103 device is current
   void* scratch = nullptr;
   if (int rc = scratch_address(dev, &scratch)) return rc;
   uint8_t* img_a = static_cast<uint8_t*>(scratch);
   uint8_t* img_b = img_a + cdiv(bytes_a, 256) * 256;  // both images 256-byte aligned
 
-  if (int rc = tcg_mxf8_prepare_scales(SFA, M, K, 128, img_a, stream)) return rc;
-  if (int rc = tcg_mxf8_prepare_scales(SFB, N, K, tile_n, img_b, stream)) return rc;
+  // both images in one launch, then the GEMM reads them
+  if (int rc = tcg_mxf8_prepare_scales_ab(SFA, M, img_a, SFB, N, tile_n, img_b, K, stream)) return rc;
   tcg_gemm_args args;
   std::memset(&args, 0, sizeof args);
   args.M = M;
@@ -123,6 +128,6 @@ extern "C" int tcg_gemm_mxf8_blockscaled_noalloc(int64_t M, int64_t N, int64_t K
   args.acc_type = acc_type;
   args.split_k = 1;  // split-K would need the library's (allocated) workspace
   if (int rc = tcg_gemm(&args, stream)) return rc;
-  tcg::set_launch_count(3);
+  tcg::set_launch_count(2);
   return TCG_OK;
 }

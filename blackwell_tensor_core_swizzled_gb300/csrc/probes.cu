@@ -10,6 +10,10 @@
 //   * one MMA tile with generic-store swizzled operands ("tcgen05.mma" page,
 //     "four K16 issues" example), dense or with the weight-stationary .ws
 //     opcode ("Weight-stationary and block scaling");
+//   * MMAs reading operand images the caller laid out, through descriptors
+//     the caller chose (K-major or MN-major, swizzle modes 0..4): the
+//     hardware's descriptor walk against a layout model ("tcgen05.mma" page,
+//     "Shared descriptors are byte-stride contracts", "swizzle=4");
 //   * ldmatrix .x2 into separated register slots ("ldmatrix / stmatrix" page
 //     example);
 //   * a bounded wait that runs out (failure detection without a GPU fault).
@@ -324,6 +328,86 @@ __global__ void __launch_bounds__(128, 1) probe_mma_tile_kernel(const uint16_t* 
   if (warp == 0) tmem_dealloc<1>(slot, ncols);
 }
 
+// ------------------------------------------------------------------ MMA from caller images
+
+// One operand of tcg_probe_mma_image as the kernel sees it: where its image
+// sits in the CTA's shared memory and the descriptor of each issue.
+struct ImageOperand {
+  const uint4* image;
+  int words16;        // image size in 16-byte units
+  uint64_t desc_hi;   // LDO, SDO, version, layout type
+  uint32_t start[8];  // descriptor origin of issue j, bytes from the region start
+};
+
+constexpr uint32_t MMA_IMAGE_REGION = 96u * 1024u;  // bytes per operand region
+
+// A's region at the 1024-byte aligned base, B's MMA_IMAGE_REGION later; both
+// regions are zeroed, the images copied in with ordinary stores, and thread 0
+// issues `ksteps` MMAs of one kind (kind::f16 for f16 / bf16, kind::tf32),
+// accumulation off on the first.  The device computes no layout: which
+// element each descriptor step reads is decided by the images alone.
+__global__ void __launch_bounds__(128, 1) probe_mma_image_kernel(ImageOperand a, ImageOperand b, int tf32,
+                                                                 uint32_t idesc, int N, int ksteps, float* D,
+                                                                 unsigned long long* err, uint64_t timeout_ns) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint32_t slot;
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ uint32_t abort_flag;
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint4* g = reinterpret_cast<uint4*>(smem_raw + (base - raw));
+  const int warp = threadIdx.x >> 5;
+  const int t = threadIdx.x;
+  constexpr int REGION16 = MMA_IMAGE_REGION / 16;
+  for (int i = t; i < 2 * REGION16; i += blockDim.x) g[i] = make_uint4(0u, 0u, 0u, 0u);
+  __syncthreads();
+  for (int i = t; i < a.words16; i += blockDim.x) g[i] = a.image[i];
+  for (int i = t; i < b.words16; i += blockDim.x) g[REGION16 + i] = b.image[i];
+  uint32_t ncols = 32;
+  while (ncols < static_cast<uint32_t>(N)) ncols <<= 1;
+  if (warp == 0) {
+    tmem_alloc<1>(smem_u32(&slot), ncols);
+    tmem_relinquish<1>();
+  }
+  if (t == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  fence_proxy_async_shared();  // generic-proxy image stores -> the MMA's async reads
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (t == 0) {
+    for (int j = 0; j < ksteps; ++j) {
+      const uint64_t ad = sdesc(base + a.start[j], a.desc_hi);
+      const uint64_t bd = sdesc(base + MMA_IMAGE_REGION + b.start[j], b.desc_hi);
+      if (tf32)
+        mma_tf32<1>(slot, ad, bd, idesc, j > 0);
+      else
+        mma_f16<1>(slot, ad, bd, idesc, j > 0);
+    }
+    tc_commit<1>(smem_u32(&bar));
+  }
+  const bool ok = warp_wait(smem_u32(&bar), 0, probe_wait_ctx(err, timeout_ns, &abort_flag), SITE_PROBE);
+  tc_fence_after();
+  const uint32_t tb = slot + (static_cast<uint32_t>(32 * warp) << 16);
+  for (int c = 0; c < N; c += 32) {
+    uint32_t r[32];
+    tmem_ld_32x32b_x32(tb + c, r);
+    tc_wait_ld();
+    if (ok) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (c + j < N) D[t * N + c + j] = __uint_as_float(r[j]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc<1>(slot, ncols);
+}
+
 // ------------------------------------------------------------------ ldmatrix
 
 // x (16,4,2) row-major words; shared layout (16,4,2):(8,1,128).  Matrix m,
@@ -408,15 +492,20 @@ extern "C" int tcg_probe_cp(const uint32_t* image, int image_words, int shape, u
   if (!image || !out || image_words <= 0 || image_words > CP_IMAGE_MAX_WORDS) return TCG_ERR_INVALID;
   if (shape < 0 || shape > 11 || swizzle < 0 || swizzle > 3) return TCG_ERR_INVALID;
   if (!sdesc_fields_ok(origin_bytes, ldo, sdo, swizzle, 0)) return TCG_ERR_INVALID;
-  // the copy's whole walk must stay inside the image (decompression keeps
-  // the base shape's source footprint)
+  // The copy's whole walk must stay inside the image, and every row group it
+  // touches must be backed whole: the descriptor organises rows in groups of
+  // eight even when the shape reads fewer ("tcgen05.cp" page, "Shared
+  // descriptor address walk").  Unswizzled, a group is an 8 x 16-byte block
+  // per 16-byte column (columns LDO apart); swizzled, 8 rows of 16 << mode
+  // bytes, whose swizzle stays inside the period-aligned blocks it spans.
+  // Decompression keeps the base shape's source footprint.
   const int base_shape = shape % 4;
   const uint32_t rows = base_shape == 2 ? 32u : base_shape == 3 ? 4u : 128u;
   const uint32_t words = base_shape == 0 || base_shape == 3 ? 8u : 4u;
-  const uint32_t rb = 16u << swizzle;
-  const uint32_t last_row = ((rows - 1) / 8) * sdo + ((rows - 1) % 8) * rb;
-  const uint32_t last_word = swizzle == 0 ? ((words - 1) / 4) * ldo + ((words - 1) % 4) * 4 : 4 * (words - 1);
-  const uint32_t span = origin_bytes + last_row + last_word + 4;
+  const uint32_t groups = (rows + 7) / 8;
+  const uint32_t columns = swizzle == 0 ? (words + 3) / 4 : 1u;
+  const uint32_t block = 8u * (16u << swizzle);
+  const uint32_t span = origin_bytes + (groups - 1) * sdo + (columns - 1) * (swizzle == 0 ? ldo : 0u) + block;
   const uint32_t period = swizzle_period(swizzle);
   if ((span + period - 1) / period * period > static_cast<uint32_t>(image_words) * 4u) return TCG_ERR_INVALID;
   int dev;
@@ -475,6 +564,76 @@ extern "C" int tcg_probe_mma_tile_ws(const void* A, const void* B, int N, int K,
   probe_mma_tile_kernel<<<1, 128, smem, as_stream(stream)>>>(static_cast<const uint16_t*>(A),
                                                              static_cast<const uint16_t*>(B), N, K, idesc, 1, D,
                                                              device_error_word(dev), wait_timeout_ns());
+  return finish_launch(1);
+}
+
+namespace {
+
+// Largest distance past an issue's descriptor origin that its walk can reach
+// for an operand of `rows_mn` M/N rows: under the pages' assignment of LDO and
+// SDO and under the swapped one (so that a misreading still stays inside the
+// operand's region), plus the whole row-group block it lands in.
+uint32_t image_walk_reach(tcg_major major, int swizzle, int rows_mn, int esize, uint32_t ldo, uint32_t sdo) {
+  const uint32_t krows = 32u / static_cast<uint32_t>(esize);  // K per issue: 16 (16-bit), 8 (TF32)
+  uint32_t groups, chunks, block;
+  if (major == TCG_K_MAJOR) {
+    groups = (static_cast<uint32_t>(rows_mn) + 7u) / 8u;
+    chunks = swizzle == 0 ? 2u : 1u;  // 32 bytes of K: two 16-byte chunks unswizzled
+    block = swizzle == 0 ? 128u : 8u * (16u << swizzle);
+  } else {
+    const uint32_t rb = swizzle == 4 ? 128u : (16u << swizzle);
+    const uint32_t g = swizzle == 4 ? 4u : 8u;
+    groups = (krows + g - 1u) / g;
+    chunks = (static_cast<uint32_t>(rows_mn * esize) + rb - 1u) / rb;
+    block = g * rb;
+  }
+  const uint32_t r1 = (groups - 1u) * ldo + (chunks - 1u) * sdo;
+  const uint32_t r2 = (groups - 1u) * sdo + (chunks - 1u) * ldo;
+  return (r1 > r2 ? r1 : r2) + block;
+}
+
+int image_operand(const tcg_probe_operand* o, int rows_mn, int esize, bool tf32, int ksteps, ImageOperand* out) {
+  if (!o || !o->image || reinterpret_cast<uintptr_t>(o->image) % 16) return TCG_ERR_INVALID;
+  if (o->bytes <= 0 || o->bytes % 16 || static_cast<uint32_t>(o->bytes) > MMA_IMAGE_REGION) return TCG_ERR_INVALID;
+  if (o->major != TCG_K_MAJOR && o->major != TCG_MN_MAJOR) return TCG_ERR_INVALID;
+  if (o->swizzle < 0 || o->swizzle > 4) return TCG_ERR_INVALID;
+  // "swizzle=4" is the 32-bit MN-major mode; TF32 MN-major takes no other
+  if ((o->swizzle == 4) != (tf32 && o->major == TCG_MN_MAJOR)) return TCG_ERR_UNSUPPORTED;
+  if ((o->ldo | o->sdo) & 15u || o->ldo >= (1u << 18) || o->sdo >= (1u << 18)) return TCG_ERR_INVALID;
+  const uint32_t reach = image_walk_reach(o->major, o->swizzle, rows_mn, esize, o->ldo, o->sdo);
+  for (int j = 0; j < ksteps; ++j) {
+    if (o->start[j] & 15u) return TCG_ERR_INVALID;
+    // the walk, a swizzle period of slack and the whole block stay in the region
+    if (static_cast<uint64_t>(o->start[j]) + reach + 1024u > MMA_IMAGE_REGION) return TCG_ERR_INVALID;
+  }
+  out->image = static_cast<const uint4*>(o->image);
+  out->words16 = o->bytes / 16;
+  out->desc_hi = sdesc_hi(o->ldo, o->sdo, o->swizzle);
+  for (int j = 0; j < 8; ++j) out->start[j] = j < ksteps ? o->start[j] : 0u;
+  return TCG_OK;
+}
+
+}  // namespace
+
+extern "C" int tcg_probe_mma_image(const tcg_probe_operand* a, const tcg_probe_operand* b, tcg_input in_type, int N,
+                                   int ksteps, float* D, void* stream) {
+  if (!D || N < 16 || N > 256 || N % 16 || ksteps < 1 || ksteps > 8) return TCG_ERR_INVALID;
+  if (in_type != TCG_IN_F16 && in_type != TCG_IN_BF16 && in_type != TCG_IN_TF32) return TCG_ERR_INVALID;
+  const bool tf32 = in_type == TCG_IN_TF32;
+  const int esize = tf32 ? 4 : 2;
+  ImageOperand ia, ib;
+  if (int rc = image_operand(a, 128, esize, tf32, ksteps, &ia)) return rc;
+  if (int rc = image_operand(b, N, esize, tf32, ksteps, &ib)) return rc;
+  int dev;
+  if (int rc = current_device_checked(&dev)) return rc;
+  const size_t smem = 1024 + 2 * static_cast<size_t>(MMA_IMAGE_REGION);
+  cudaError_t e = cudaFuncSetAttribute(probe_mma_image_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return record_cuda(e);
+  const bool a_mn = a->major == TCG_MN_MAJOR, b_mn = b->major == TCG_MN_MAJOR;
+  const uint32_t idesc = tf32 ? idesc_tf32(a_mn, b_mn, 128, N) : idesc_f16(in_type == TCG_IN_BF16, true, a_mn, b_mn, 128, N);
+  probe_mma_image_kernel<<<1, 128, smem, as_stream(stream)>>>(ia, ib, tf32 ? 1 : 0, idesc, N, ksteps, D,
+                                                              device_error_word(dev), wait_timeout_ns());
   return finish_launch(1);
 }
 

@@ -127,8 +127,9 @@ int tcg_gemm_mxf8_blockscaled(int64_t M, int64_t N, int64_t K,
  * the source pages: it only changes where the scale-factor images live.
  * They are built in one fixed 16 MiB device array of the library (held by
  * every GPU that loads the library until exit) instead of the per-stream
- * workspace; problems whose two images need more return TCG_ERR_UNSUPPORTED
- * before anything is queued.  All calls on a device share that array (each
+ * workspace; problems whose two images need more return TCG_ERR_UNSUPPORTED.
+ * Every argument is checked before anything is queued, so a call that returns
+ * an error has not touched the array.  All calls on a device share it (each
  * call rewrites what it reads, so nothing needs clearing); calls whose GPU
  * work overlaps race on it and must be ordered.  The first call on a device
  * looks up the array's address with that device current: make it before any
@@ -282,7 +283,9 @@ int tcg_probe_tmem_roundtrip(const uint32_t* in, uint32_t* out, int ncols, void*
  * waits on its commit and reads 128 lanes x 8 columns back with
  * tcgen05.ld .32x32b.x8 into out (128 x 8 words, lane-major; cells the copy
  * does not write hold 0xDEADBEEF).  image_words <= 12288; the walk must stay
- * inside the image (else TCG_ERR_INVALID before any launch). */
+ * inside the image, with every 8-row group it touches backed whole ("tcgen05.cp"
+ * page: a 4-row region still needs the eight-row organisation's storage), else
+ * TCG_ERR_INVALID before any launch. */
 int tcg_probe_cp(const uint32_t* image, int image_words, int shape,
                  uint32_t origin_bytes, uint32_t ldo, uint32_t sdo, int swizzle,
                  uint32_t* out, void* stream);
@@ -313,6 +316,36 @@ int tcg_probe_mma_tile(const void* A, const void* B, int N, int K, int is_bf16,
  * same lane-per-row Layout D as the dense form).  N in {64, 128, 256} (the
  * .ws shapes), K in {16, 32, 48, 64}. */
 int tcg_probe_mma_tile_ws(const void* A, const void* B, int N, int K, int is_bf16, float* D, void* stream);
+
+/* "tcgen05.mma" page, "Shared descriptors are byte-stride contracts" and
+ * "swizzle=4": MMAs that read operands laid out by the caller.  One operand's
+ * shared-memory image and the descriptors that walk it: */
+typedef struct {
+  const void* image;  /* device memory, 16-byte aligned: the operand's bytes exactly as
+                         they must sit in shared memory from a 1024-byte aligned base */
+  int bytes;          /* image size: a multiple of 16, at most 96 KiB */
+  tcg_major major;    /* K-major or MN-major (the instruction descriptor's transpose bit) */
+  uint32_t ldo, sdo;  /* descriptor leading / stride byte offsets (16-byte multiples < 2^18) */
+  int swizzle;        /* the pages' logical mode 0..3; 4 (128-byte span, 32-byte atoms) is
+                         required for, and only allowed with, TF32 MN-major */
+  uint32_t start[8];  /* descriptor origin of MMA issue j, bytes from the image start
+                         (16-byte multiples) */
+} tcg_probe_operand;
+
+/* One CTA zeroes two 96 KiB shared regions, copies a->image into the first
+ * and b->image into the second, and one thread issues `ksteps` (1..8)
+ * tcgen05.mma.cta_group::1 of kind::f16 (in_type TCG_IN_F16 / TCG_IN_BF16) or
+ * kind::tf32 (TCG_IN_TF32), M = 128, N in {16..256} step 16, accumulation off
+ * on the first issue only; issue j's descriptors are (region + start[j], ldo,
+ * sdo, swizzle).  One commit, then D (128 x N fp32, row-major) is drained with
+ * tcgen05.ld .32x32b.  Each issue multiplies 128 x 16 (16-bit) or 128 x 8
+ * (TF32) of A by the same K of N rows of B.  The device computes no layout:
+ * which element each step of the hardware walk reads is decided by the images
+ * alone, so the result checks the caller's layout model.  Before any launch
+ * the host rejects (TCG_ERR_INVALID) a walk that could leave its region under
+ * either assignment of LDO and SDO. */
+int tcg_probe_mma_image(const tcg_probe_operand* a, const tcg_probe_operand* b, tcg_input in_type, int N,
+                        int ksteps, float* D, void* stream);
 
 /* "ldmatrix / stmatrix" page example: x = 128 words viewed as (16,4,2) with
  * shared layout (16,4,2):(8,1,128); one warp issues two ldmatrix .m8n8.x2

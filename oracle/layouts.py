@@ -70,8 +70,9 @@ def cp_walk(r, w, ldo: int, sdo: int, swizzle: int):
 def check_descriptor(origin: int, ldo: int, sdo: int, swizzle: int) -> None:
     """Field constraints ("tcgen05.cp" page, "Shared descriptor address walk";
     "tcgen05.mma" page, descriptor contract): strides are non-negative 16-byte
-    multiples below 2^18, origins 16-byte aligned, swizzled bases aligned to the
-    256/512/1024-byte period (512 for mode 4).  Raises ValueError."""
+    multiples below 2^18, origins 16-byte aligned, the mode one of 0..4.
+    Raises ValueError.  The rules that depend on the allocation (period
+    alignment, the physical walk, eight-row backing) are :func:`check_walk`'s."""
     for name, v in (("ldo", ldo), ("sdo", sdo)):
         if v < 0 or v % 16 or v >= (1 << 18):
             raise ValueError(f"{name}={v} must be a non-negative multiple of 16 below 2^18")
@@ -79,6 +80,69 @@ def check_descriptor(origin: int, ldo: int, sdo: int, swizzle: int) -> None:
         raise ValueError(f"origin {origin} is not 16-byte aligned")
     if swizzle not in (0, 1, 2, 3, 4):
         raise ValueError(f"swizzle mode {swizzle} not in 0..4")
+
+
+def check_base(base: int, swizzle: int) -> None:
+    """"period": an allocation read through a swizzled descriptor starts on
+    its mode's period, 256 / 512 / 1024 bytes for modes 1 / 2 / 3 ("tcgen05.cp"
+    page, "Shared descriptor address walk") and 512 for mode 4 ("tcgen05.mma"
+    page, "swizzle=4"; its backing allocations align to the full period).
+    Raises ValueError."""
+    if swizzle and base % SWIZZLE_PERIOD[swizzle]:
+        raise ValueError(f"period: base {base} is not aligned to the {SWIZZLE_PERIOD[swizzle]}-byte period of "
+                         f"mode {swizzle}")
+
+
+def check_walk(origin: int, rows: int, words: int, ldo: int, sdo: int, swizzle: int,
+               base: int = 0, backing: int | None = None):
+    """The descriptor rules of the "tcgen05.cp" page ("Shared descriptor
+    address walk") and the "tcgen05.mma" page's descriptor contract, applied
+    to a walk of ``rows`` rows x ``words`` b32 words from ``origin`` bytes into
+    an allocation that starts at shared byte address ``base`` and holds
+    ``backing`` bytes (None: unbounded).  Raises ValueError naming the rule
+    broken, in this order:
+
+    * the field constraints of :func:`check_descriptor`;
+    * "period": a swizzled allocation must start on its mode's period (256,
+      512, 1024 bytes for modes 1, 2, 3; 512 for mode 4);
+    * "physical": the complete physical walk, i.e. the swizzle applied to the
+      absolute address base + origin + walk (so the origin's position inside
+      its swizzle period, its phase, decides where each word lands), must stay
+      inside the backing;
+    * "eight-row": every row group the walk touches must be backed whole, as
+      the descriptor organises rows in groups of eight even when fewer are
+      used -- READING: for swizzled modes the group is 8 rows of 16 << mode
+      bytes from the group's first row; unswizzled it is the 8 x 16-byte block
+      of each 16-byte column the walk reads (LDO apart).
+
+    Returns the physical byte address of every word, shape (rows, words),
+    relative to ``base``."""
+    check_descriptor(origin, ldo, sdo, swizzle)
+    check_base(base, swizzle)
+    if swizzle == 4:
+        raise ValueError("mode 4 is an MMA operand mode; tcgen05.cp walks use modes 0..3")
+    r, w = np.meshgrid(np.arange(rows), np.arange(words), indexing="ij")
+    phys = swizzle_addr(base + origin + cp_walk(r, w, ldo, sdo, swizzle), swizzle) - base
+    if backing is None:
+        return phys
+    if phys.min() < 0 or phys.max() + 4 > backing:
+        raise ValueError(f"physical: the walk reaches bytes [{phys.min()}, {phys.max() + 4}) outside the "
+                         f"{backing}-byte backing")
+    rb = row_bytes(swizzle)
+    if swizzle == 0:
+        columns = [j * ldo for j in range(-(-words // 4))]
+        block = 8 * 16
+    else:
+        columns = [0]
+        block = 8 * rb
+    for g in range(-(-rows // 8)):
+        for c in columns:
+            lo = origin + g * sdo + c
+            chunk = swizzle_addr(base + np.arange(lo, lo + block, 16), swizzle) - base
+            if chunk.min() < 0 or chunk.max() + 16 > backing:
+                raise ValueError(f"eight-row: row group {g} occupies bytes up to {chunk.max() + 16}, beyond the "
+                                 f"{backing}-byte backing")
+    return phys
 
 
 def cp_physical(origin: int, r, w, ldo: int, sdo: int, swizzle: int, base_align: int = 0):

@@ -70,6 +70,27 @@ def test_host_validation_rejects_bad_arguments(tcg):
     for shape in (-1, 12):
         assert tcg.raw_call("tcg_probe_cp", 0x10000, 512, shape, 0, 16, 128, 0, 0x20000, None) == tcg.ERR_INVALID
     assert tcg.raw_call("tcg_probe_cp", 0x10000, 256, 9, 0, 16, 128, 0, 0x20000, None) == tcg.ERR_INVALID
+    # cp probe: a 4-row 4x256b walk whose 8-row blocks are not backed whole
+    # (192 of the 256 bytes its two 16-byte columns organise) is rejected
+    assert tcg.raw_call("tcg_probe_cp", 0x10000, 48, 3, 0, 128, 256, 0, 0x20000, None) == tcg.ERR_INVALID
+    assert tcg.raw_call("tcg_probe_cp", 0x10000, 64, 3, 0, 128, 256, 0, 0x20000, None) != tcg.ERR_INVALID
+    # MMA image probe: mode 4 is TF32 MN-major only, and a walk that could
+    # leave its 96 KiB region under either stride assignment is rejected
+    def op(major, sw, ldo, sdo, starts=(0,), nbytes=4096):
+        return tcg.probe_operand(0x10000, nbytes, major, ldo, sdo, sw, starts)
+    ok_a, ok_b = op(0, 3, 16, 1024), op(0, 3, 16, 1024)
+    assert tcg.raw_call("tcg_probe_mma_image", ok_a, ok_b, 1, 64, 1, 0x30000, None) == tcg.ERR_NO_DEVICE
+    assert tcg.raw_call("tcg_probe_mma_image", op(1, 4, 4096, 512), ok_b, 1, 64, 1, 0x30000,
+                        None) == tcg.ERR_UNSUPPORTED
+    assert tcg.raw_call("tcg_probe_mma_image", op(1, 3, 4096, 1024), ok_b, 2, 64, 1, 0x30000,
+                        None) == tcg.ERR_UNSUPPORTED                                   # TF32 MN-major needs mode 4
+    assert tcg.raw_call("tcg_probe_mma_image", op(1, 0, 128, 8192), ok_b, 1, 64, 1, 0x30000,
+                        None) == tcg.ERR_INVALID                                       # 15 chunks x 8 KiB
+    assert tcg.raw_call("tcg_probe_mma_image", op(0, 3, 16, 1024, starts=(8,)), ok_b, 1, 64, 1, 0x30000,
+                        None) == tcg.ERR_INVALID                                       # origin not 16-byte aligned
+    assert tcg.raw_call("tcg_probe_mma_image", ok_a, ok_b, 1, 72, 1, 0x30000, None) == tcg.ERR_INVALID
+    assert tcg.raw_call("tcg_probe_mma_image", op(0, 3, 16, 1024, nbytes=200 * 1024), ok_b, 1, 64, 1, 0x30000,
+                        None) == tcg.ERR_INVALID
     # trace request: buffer and count go together; null + 0 cancels
     assert tcg.raw_call("tcg_trace_next", None, 4) == tcg.ERR_INVALID
     assert tcg.raw_call("tcg_trace_next", 0x10000, 0) == tcg.ERR_INVALID

@@ -259,3 +259,43 @@ def test_bounded_wait_reports_timeout_and_context_survives(tcg):
     out = torch.zeros_like(vals)
     tcg.probe_tmem_roundtrip(vals, out, 8)  # the context is still usable
     assert tcg.check() == 0 and torch.equal(out, vals)
+
+
+# ------------------------------------------------------------- MMA from model-built images
+
+from mma_image_cases import CASES as IMAGE_CASES, build_image, kstep as _kstep  # noqa: E402
+
+_IN = {"f16": 0, "bf16": 1, "tf32": 2}
+_ORACLE_T = {"f16": 1, "bf16": 2, "tf32": 0}
+
+
+@pytest.mark.parametrize("case", IMAGE_CASES, ids=[c.name for c in IMAGE_CASES])
+def test_mma_reads_oracle_layout_model(tcg, oracle_mod, case):
+    """The oracle's operand walk (K-major and MN-major, swizzle modes 0..4)
+    lays out A and B; the hardware's descriptor walk must read back exactly
+    the logical operands: quarter-integer inputs make every sum exact, so the
+    product must equal the oracle's float64 GEMM bit for bit."""
+    import synthetic as syn
+    ks = case.K // _kstep(case.dtype)
+    rng = np.random.default_rng(len(case.name) * 7 + case.N)
+    a = rng.integers(-4, 5, (128, case.K)) / 4.0
+    b = rng.integers(-4, 5, (case.N, case.K)) / 4.0
+    ab, bb = syn.to_bits(a, case.dtype), syn.to_bits(b, case.dtype)
+    img_a = build_image(ab, case.a, case.dtype, ks)
+    img_b = build_image(bb, case.b, case.dtype, ks)
+    from mma_image_cases import issue_starts
+    da, db = torch.from_numpy(img_a).cuda(), torch.from_numpy(img_b).cuda()
+    opa = tcg.probe_operand(da, img_a.size, 0 if case.a.major == "k" else 1, case.a.ldo, case.a.sdo, case.a.swizzle,
+                            issue_starts(case.a, 128, case.dtype, ks))
+    opb = tcg.probe_operand(db, img_b.size, 0 if case.b.major == "k" else 1, case.b.ldo, case.b.sdo, case.b.swizzle,
+                            issue_starts(case.b, case.N, case.dtype, ks))
+    D = torch.full((128, case.N), float("nan"), dtype=torch.float32, device="cuda")
+    tcg.probe_mma_image(opa, opb, _IN[case.dtype], case.N, ks, D)
+    assert tcg.check() == 0
+    t = _ORACLE_T[case.dtype]
+    ref, _ = oracle_mod.gemm(128, case.N, case.K, ab, t, 0, case.K, bb, t, 0, case.K)
+    got = D.cpu().numpy().astype(np.float64)
+    if not np.array_equal(got, ref):
+        bad = np.argwhere(got != ref)[:6]
+        raise AssertionError(f"{case.name}: {int((got != ref).sum())} mismatches, first {bad.tolist()}: "
+                             f"got {[got[tuple(i)] for i in bad]} ref {[ref[tuple(i)] for i in bad]}")

@@ -275,3 +275,124 @@ def test_cp_decompress_fp6_padding_is_the_last_word():
     flipped[:, 2] ^= 1 << 31  # bit 95: the top bit of value 15
     diff = L.cp_decompress(flipped, 6) != L.cp_decompress(blocks, 6)
     assert diff[:, 3].all() and not diff[:, :3].any()
+
+
+# ---------------------------------------------------------------------------
+# The operand images the MMA image probe feeds to the hardware: every case is
+# a bijection into its image, and each case tells the pages' assignment of
+# LDO and SDO apart from the swapped one, so that the GPU comparison pins the
+# model's stride roles (not only its shape).
+# ---------------------------------------------------------------------------
+
+def test_mma_image_cases_are_injective_and_discriminating():
+    import sys, os
+    sys.path.insert(0, os.path.dirname(__file__))
+    from mma_image_cases import CASES, element_addresses, build_image, kstep
+
+    for c in CASES:
+        ks = c.K // kstep(c.dtype)
+        for spec, rows in ((c.a, 128), (c.b, c.N)):
+            bits = np.arange(rows * c.K, dtype=np.uint32).reshape(rows, c.K) + 1
+            if c.dtype != "tf32":
+                bits = bits.astype(np.uint16)
+            img = build_image(bits, spec, c.dtype, ks)
+            assert img.size <= 96 * 1024, c.name
+            addr = element_addresses(spec, rows, c.dtype, ks)
+            swapped = element_addresses(spec, rows, c.dtype, ks, ldo=spec.sdo, sdo=spec.ldo)
+            moved = addr != swapped
+            if spec.major == "k" and spec.swizzle != 0:
+                # swizzled K-major ignores LDO (atoms fit in one row): the
+                # swapped reading differs through SDO alone
+                assert moved.any() or spec.ldo == spec.sdo, c.name
+            else:
+                assert moved.any(), f"{c.name}: strides indistinguishable"
+
+
+def test_mma_operand_offset_mn_major_examples():
+    """Closed-form values of the MN-major walk, worked out from the page's
+    table: swizzled rows enumerate K (SDO between 8-row groups), contiguous
+    chunks of one row width along M/N are LDO apart; unswizzled the roles swap
+    (16-byte rows, LDO between 8-row groups of K, SDO between 8-element M/N
+    chunks); mode 4 groups four 128-byte K rows per SDO."""
+    # bf16, mode 3 (128-byte rows of 64 elements)
+    assert L.mma_operand_offset(0, 0, 2, "mn", 8192, 1024, 3) == 0
+    assert L.mma_operand_offset(63, 0, 2, "mn", 8192, 1024, 3) == 126
+    assert L.mma_operand_offset(64, 0, 2, "mn", 8192, 1024, 3) == 8192
+    assert L.mma_operand_offset(0, 7, 2, "mn", 8192, 1024, 3) == 7 * 128
+    assert L.mma_operand_offset(0, 8, 2, "mn", 8192, 1024, 3) == 1024
+    # bf16, mode 0: element (mn, k) in the 8x8 core block (k//8, mn//8)
+    assert L.mma_operand_offset(9, 3, 2, "mn", 128, 1024, 0) == 1 * 1024 + 3 * 16 + 2
+    assert L.mma_operand_offset(9, 11, 2, "mn", 128, 1024, 0) == 1 * 128 + 1 * 1024 + 3 * 16 + 2
+    # tf32, mode 4: 32 elements per 128-byte row, 4 K rows per 512-byte group
+    assert L.mma_operand_offset(33, 5, 4, "mn", 4096, 512, 4) == 4096 + 1 * 512 + 1 * 128 + 4
+    # K-major, mode 0: 8-row groups SDO apart, 16-byte K chunks LDO apart
+    assert L.mma_operand_offset(10, 9, 2, "k", 2048, 128, 0) == 1 * 128 + 2 * 16 + 1 * 2048 + 2
+
+
+# ---------------------------------------------------------------------------
+# Descriptor rules that depend on the allocation ("tcgen05.cp" page, "Shared
+# descriptor address walk", second paragraph; "tcgen05.mma" page, "Shared
+# descriptors are byte-stride contracts", last paragraph).  Each case is one
+# sentence of the pages turned into an accepted and a rejected example.
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("s,period", [(1, 256), (2, 512), (3, 1024), (4, 512)])
+def test_swizzled_bases_need_period_alignment(s, period):
+    # "Swizzled bases require 256/512/1024-byte period alignment for modes
+    # 1/2/3"; mode 4 has "a 512-byte period" and backing allocations "align to
+    # the full swizzle period".
+    L.check_base(period, s)
+    L.check_base(3 * period, s)
+    for bad in (period // 2, period + 16, 128 if period > 128 else 16):
+        with pytest.raises(ValueError, match="period"):
+            L.check_base(bad, s)
+    L.check_base(16, 0)  # unswizzled: any 16-byte aligned base
+
+
+def test_walk_origin_swizzle_phase_decides_the_physical_bytes():
+    # "The complete physical walk is checked, including the origin's swizzle
+    # phase": 16 bytes from origin 512 of a mode-3 allocation are logically
+    # bytes 512..527, inside a 576-byte backing, but the origin sits in row 4
+    # of its 1024-byte period, so the 16-byte chunk moves to 576..591.
+    with pytest.raises(ValueError, match="physical"):
+        L.check_walk(512, 1, 4, 16, 1024, 3, base=0, backing=576)
+    phys = L.check_walk(512, 1, 4, 16, 1024, 3, base=0, backing=None)
+    assert phys.ravel().tolist() == [576, 580, 584, 588]
+    # the same walk at phase 0 stays where it is
+    assert L.check_walk(0, 1, 4, 16, 1024, 3, base=0, backing=1024).ravel().tolist() == [0, 4, 8, 12]
+    # the phase is the absolute address's: a period-aligned base changes nothing
+    assert np.array_equal(L.check_walk(512, 1, 4, 16, 1024, 3, base=4096), phys)
+
+
+def test_four_row_region_needs_eight_row_backing():
+    # "A 4-row logical region still needs a backing storage block large enough
+    # for the descriptor's eight-row organization".  4 x 256b (4 rows, 8 words)
+    # unswizzled with LDO 128: the words touched end at byte 192, but the two
+    # 16-byte columns each belong to an 8-row block of 128 bytes.
+    phys = L.check_walk(0, 4, 8, 128, 256, 0, backing=1 << 20)
+    assert phys.max() + 4 == 192
+    with pytest.raises(ValueError, match="eight-row"):
+        L.check_walk(0, 4, 8, 128, 256, 0, backing=192)
+    L.check_walk(0, 4, 8, 128, 256, 0, backing=256)
+    # swizzled 128-byte rows: 4 rows use 512 bytes, the organisation 1024
+    with pytest.raises(ValueError, match="eight-row"):
+        L.check_walk(0, 4, 4, 16, 1024, 3, backing=512)
+    L.check_walk(0, 4, 4, 16, 1024, 3, backing=1024)
+
+
+def test_walk_rules_planted_mistakes_are_caught():
+    # a wrong period (mode 2 taken as 256 bytes) or a walk checked on logical
+    # instead of physical addresses would each let one of these through
+    with pytest.raises(ValueError, match="period"):
+        L.check_walk(0, 8, 4, 16, 512, 2, base=256, backing=4096)
+    with pytest.raises(ValueError, match="physical"):
+        L.check_walk(512 + 32, 1, 4, 16, 1024, 3, base=0, backing=512 + 64)
+
+
+def test_gpu_cp_probe_cases_obey_the_walk_rules():
+    # every tcgen05.cp case the GPU probe runs is a legal walk of its image
+    import test_gpu_probes as g
+    rows = {0: 128, 1: 128, 2: 32, 3: 4}
+    words = {0: 8, 1: 4, 2: 4, 3: 8}
+    for shape, origin, ldo, sdo, sw, nwords in g.CP_CASES + g.DECOMP_CASES:
+        L.check_walk(origin, rows[shape % 4], words[shape % 4], ldo, sdo, sw, base=0, backing=4 * nwords)
