@@ -165,18 +165,44 @@ int make_map_3d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int 
   return TCG_OK;
 }
 
-int esize_of(tcg_input t) { return t == TCG_IN_TF32 ? 4 : t == TCG_IN_E4M3 ? 1 : 2; }
+// Block-scaled formats (kind::mxf8f6f4): E4M3 / E5M2 bytes, E3M2 / E2M3 /
+// E2M1 packed in global memory.  Each element takes one byte of shared memory
+// (TMA expands the packed ones into 16-byte blocks of sixteen values and
+// padding, the layout the "tcgen05.cp" page's FP4 / FP6 shapes describe).
+bool is_mx(tcg_input t) {
+  return t == TCG_IN_E4M3 || t == TCG_IN_E5M2 || t == TCG_IN_E3M2 || t == TCG_IN_E2M3 || t == TCG_IN_E2M1;
+}
+bool is_packed(tcg_input t) { return t == TCG_IN_E3M2 || t == TCG_IN_E2M3 || t == TCG_IN_E2M1; }
+int bits_of(tcg_input t) {
+  return t == TCG_IN_TF32 ? 32 : t == TCG_IN_E2M1 ? 4 : (t == TCG_IN_E3M2 || t == TCG_IN_E2M3) ? 6 : is_mx(t) ? 8 : 16;
+}
+// bytes per element in shared memory (and in global memory for unpacked types)
+int esize_of(tcg_input t) { return t == TCG_IN_TF32 ? 4 : is_mx(t) ? 1 : 2; }
+// global bytes of `ld` elements
+int64_t row_bytes(tcg_input t, int64_t ld) { return ld * bits_of(t) / 8; }
+uint32_t mx_format(tcg_input t) {
+  return t == TCG_IN_E5M2 ? MXF_E5M2 : t == TCG_IN_E3M2 ? MXF_E3M2 : t == TCG_IN_E2M3 ? MXF_E2M3
+         : t == TCG_IN_E2M1 ? MXF_E2M1 : MXF_E4M3;
+}
 int dsize_of(tcg_dtype t) { return t == TCG_F32 ? 4 : 2; }
 
 // Validates one operand; fills its leading dimension when 0 (packed).
-int check_operand(const void* ptr, tcg_major major, int64_t mn, int64_t K, int64_t* ld, int esize) {
+// Packed 6- and 4-bit operands are K-major, K a multiple of 128, with 32-byte
+// aligned bases and row strides (the TMA rules of the padded element types).
+int check_operand(const void* ptr, tcg_major major, int64_t mn, int64_t K, int64_t* ld, tcg_input t) {
   if (major != TCG_K_MAJOR && major != TCG_MN_MAJOR) return TCG_ERR_INVALID;
   const int64_t inner = major == TCG_K_MAJOR ? K : mn;
   if (*ld == 0) *ld = inner;
   if (*ld < inner || *ld < 1) return TCG_ERR_INVALID;
   if (!ptr) return TCG_ERR_INVALID;
+  if (is_packed(t)) {
+    if (major != TCG_K_MAJOR) return TCG_ERR_UNSUPPORTED;
+    if (K % 128 || (*ld * bits_of(t)) % 8) return TCG_ERR_ALIGNMENT;
+    if (reinterpret_cast<uintptr_t>(ptr) % 32 || row_bytes(t, *ld) % 32) return TCG_ERR_ALIGNMENT;
+    return TCG_OK;
+  }
   if (reinterpret_cast<uintptr_t>(ptr) % 16) return TCG_ERR_ALIGNMENT;
-  if ((*ld * esize) % 16) return TCG_ERR_ALIGNMENT;
+  if ((*ld * esize_of(t)) % 16) return TCG_ERR_ALIGNMENT;
   return TCG_OK;
 }
 
@@ -212,7 +238,11 @@ int get_plan(const tcg_gemm_args& a, Plan* plan) {
                                                                              : F16_WIDE);
       break;
     case TCG_IN_TF32: plan->ki = kinfo_tf32(cg); break;
-    case TCG_IN_E4M3: plan->ki = kinfo_mxf8(cg); break;
+    case TCG_IN_E4M3:
+    case TCG_IN_E5M2:
+    case TCG_IN_E3M2:
+    case TCG_IN_E2M3:
+    case TCG_IN_E2M1: plan->ki = kinfo_mxf8(cg); break;
     default: return TCG_ERR_INVALID;
   }
   // an MN-major B half tile must be whole 128-byte swizzle spans
@@ -372,6 +402,11 @@ CUtensorMapDataType map_dtype(tcg_input t) {
     case TCG_IN_F16: return CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     case TCG_IN_BF16: return CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     case TCG_IN_TF32: return CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    // sixteen packed values per 16-byte block in shared memory (8 or 12 data
+    // bytes, then padding)
+    case TCG_IN_E2M1: return CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B;
+    case TCG_IN_E3M2:
+    case TCG_IN_E2M3: return CU_TENSOR_MAP_DATA_TYPE_16U6_ALIGN16B;
     default: return CU_TENSOR_MAP_DATA_TYPE_UINT8;
   }
 }
@@ -383,7 +418,7 @@ int setup_operand(const void* ptr, tcg_input it, tcg_major major, int64_t mn, in
                   uint32_t* kstep) {
   const int es = esize_of(it);
   const int bk = 128 / es;  // K elements per stage
-  const int mma_k = it == TCG_IN_TF32 ? 8 : it == TCG_IN_E4M3 ? 32 : 16;
+  const int mma_k = it == TCG_IN_TF32 ? 8 : is_mx(it) ? 32 : 16;
   const CUtensorMapDataType dt = map_dtype(it);
   if (major == TCG_K_MAJOR) {
     // rows enumerate M/N: one 128-byte swizzle row per M/N row, 8-row groups
@@ -394,8 +429,9 @@ int setup_operand(const void* ptr, tcg_input it, tcg_major major, int64_t mn, in
     *box_bytes = static_cast<uint32_t>(rows) * 128u;
     *desc_hi = sdesc_hi(16, 1024, SW_128B);
     *kstep = static_cast<uint32_t>(mma_k * es);
-    return make_map_2d(map, ptr, dt, es, static_cast<uint64_t>(K), static_cast<uint64_t>(mn),
-                       static_cast<uint64_t>(ld), static_cast<uint32_t>(bk), static_cast<uint32_t>(rows),
+    // the map's row stride is the global one (packed formats: ld * bits / 8)
+    return make_map_2d(map, ptr, dt, 1, static_cast<uint64_t>(K), static_cast<uint64_t>(mn),
+                       static_cast<uint64_t>(row_bytes(it, ld)), static_cast<uint32_t>(bk), static_cast<uint32_t>(rows),
                        CU_TENSOR_MAP_SWIZZLE_128B);
   }
   // MN-major: rows enumerate K; one 128-byte row holds 128/es M/N elements.
@@ -424,7 +460,7 @@ int run_gemm(const tcg_gemm_args* args, cudaStream_t s) {
   if (!args) return TCG_ERR_INVALID;
   tcg_gemm_args a = *args;
   if (a.M < 0 || a.N < 0 || a.K < 0) return TCG_ERR_INVALID;
-  if (a.in_type < TCG_IN_F16 || a.in_type > TCG_IN_E4M3) return TCG_ERR_INVALID;
+  if (a.in_type < TCG_IN_F16 || a.in_type > TCG_IN_E2M1) return TCG_ERR_INVALID;
   if (a.d_type < TCG_F32 || a.d_type > TCG_BF16 || a.acc_type < TCG_F32 || a.acc_type > TCG_BF16)
     return TCG_ERR_INVALID;
   if (a.acc_type == TCG_BF16) return TCG_ERR_UNSUPPORTED;
@@ -439,11 +475,10 @@ int run_gemm(const tcg_gemm_args* args, cudaStream_t s) {
   if (a.ldd < a.N) return TCG_ERR_INVALID;
   const int ds = dsize_of(a.d_type);
   if (reinterpret_cast<uintptr_t>(a.D) % ds) return TCG_ERR_ALIGNMENT;
-  const bool scaled = a.in_type == TCG_IN_E4M3;
+  const bool scaled = is_mx(a.in_type);
   if (a.K > 0) {
-    const int es = esize_of(a.in_type);
-    if (int rc = check_operand(a.A, a.a_major, a.M, a.K, &a.lda, es)) return rc;
-    if (int rc = check_operand(a.B, a.b_major, a.N, a.K, &a.ldb, es)) return rc;
+    if (int rc = check_operand(a.A, a.a_major, a.M, a.K, &a.lda, a.in_type)) return rc;
+    if (int rc = check_operand(a.B, a.b_major, a.N, a.K, &a.ldb, a.in_type)) return rc;
     if (scaled) {
       const bool plain = a.SFA || a.SFB;
       const bool img = a.SFA_img || a.SFB_img;
@@ -512,7 +547,11 @@ int run_gemm(const tcg_gemm_args* args, cudaStream_t s) {
   if (int rc = setup_operand(a.A, a.in_type, a.a_major, a.M, a.K, a.lda, a_rows, &prm.tmap_a, &prm.a_mn_major,
                              &prm.a_boxes, &prm.a_box_mn, &prm.a_box_bytes, &prm.a_desc_hi, &prm.a_kstep))
     return rc;
-  prm.ab_tx_bytes = static_cast<uint32_t>((a_rows * 128 + (bn / cg) * 128) * cg);
+  // bytes TMA writes per stage: 128 elements of K per row; the packed 6- and
+  // 4-bit types write only their data bytes (96 / 64 per row) and skip the
+  // padding of each 16-byte block
+  const int row_tx = static_cast<int>(row_bytes(a.in_type, 128 / esize_of(a.in_type)));
+  prm.ab_tx_bytes = static_cast<uint32_t>((a_rows + bn / cg) * row_tx * cg);
   if (int rc = setup_operand(a.B, a.in_type, a.b_major, a.N, a.K, a.ldb, bn / cg, &prm.tmap_b, &prm.b_mn_major,
                              &prm.b_boxes, &prm.b_box_mn, &prm.b_box_bytes, &prm.b_desc_hi, &prm.b_kstep))
     return rc;
@@ -520,7 +559,7 @@ int run_gemm(const tcg_gemm_args* args, cudaStream_t s) {
   if (a.in_type == TCG_IN_TF32)
     prm.idesc = idesc_tf32(a_mn, b_mn, 128 * cg, bn);
   else if (scaled)
-    prm.idesc = idesc_mxf8(a_mn, b_mn, 128 * cg, bn);
+    prm.idesc = idesc_mxf8(a_mn, b_mn, 128 * cg, bn, mx_format(a.in_type), mx_format(a.in_type));
   else
     prm.idesc = idesc_f16(a.in_type == TCG_IN_BF16, a.acc_type == TCG_F32, a_mn, b_mn, 128 * cg, bn);
   prm.D = a.D;
@@ -769,6 +808,24 @@ int tcg_gemm_mxf8_blockscaled(int64_t M, int64_t N, int64_t K, const void* A, tc
                               void* stream) {
   if (K > 0 && (!SFA || !SFB)) return TCG_ERR_INVALID;
   return named_gemm(TCG_IN_E4M3, M, N, K, A, a_major, lda, B, b_major, ldb, SFA, SFB, D, d_type, ldd, acc_type,
+                    stream);
+}
+
+int tcg_gemm_mxf6_blockscaled(tcg_input fmt, int64_t M, int64_t N, int64_t K, const void* A, tcg_major a_major,
+                              int64_t lda, const void* B, tcg_major b_major, int64_t ldb, const uint8_t* SFA,
+                              const uint8_t* SFB, void* D, tcg_dtype d_type, int64_t ldd, tcg_dtype acc_type,
+                              void* stream) {
+  if (fmt != TCG_IN_E3M2 && fmt != TCG_IN_E2M3) return TCG_ERR_INVALID;
+  if (K > 0 && (!SFA || !SFB)) return TCG_ERR_INVALID;
+  return named_gemm(fmt, M, N, K, A, a_major, lda, B, b_major, ldb, SFA, SFB, D, d_type, ldd, acc_type, stream);
+}
+
+int tcg_gemm_mxf4_blockscaled(int64_t M, int64_t N, int64_t K, const void* A, tcg_major a_major, int64_t lda,
+                              const void* B, tcg_major b_major, int64_t ldb, const uint8_t* SFA,
+                              const uint8_t* SFB, void* D, tcg_dtype d_type, int64_t ldd, tcg_dtype acc_type,
+                              void* stream) {
+  if (K > 0 && (!SFA || !SFB)) return TCG_ERR_INVALID;
+  return named_gemm(TCG_IN_E2M1, M, N, K, A, a_major, lda, B, b_major, ldb, SFA, SFB, D, d_type, ldd, acc_type,
                     stream);
 }
 

@@ -72,8 +72,9 @@ inline bool sdesc_fields_ok(uint32_t origin, uint32_t ldo, uint32_t sdo, int mod
 // tables.  kind::f16 / kind::tf32: D format [4,6) (0 F16, 1 F32), A format
 // [7,10), B format [10,13) (kind::f16: 0 F16, 1 BF16; kind::tf32: 2 TF32),
 // transpose (MN-major) A bit 15, B bit 16, N>>3 in [17,23), M>>4 in [24,29).
-// kind::mxf8f6f4 block-scaled: SFB id [4,6), A/B formats (0 = E4M3), majors,
-// N>>3, scale type bit 23 (1 = UE8M0), M>>4, SFA id [29,31).
+// kind::mxf8f6f4 block-scaled: SFB id [4,6), A/B formats (E4M3 0, E5M2 1,
+// E2M3 3, E3M2 4, E2M1 5), majors, N>>3, scale type bit 23 (1 = UE8M0), M>>4,
+// SFA id [29,31).
 // ---------------------------------------------------------------------------
 
 __host__ __device__ constexpr uint32_t idesc_f16(bool bf16, bool d_f32, bool a_mn, bool b_mn, int M, int N) {
@@ -89,8 +90,12 @@ __host__ __device__ constexpr uint32_t idesc_tf32(bool a_mn, bool b_mn, int M, i
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
-__host__ __device__ constexpr uint32_t idesc_mxf8(bool a_mn, bool b_mn, int M, int N) {
-  return (static_cast<uint32_t>(a_mn) << 15) | (static_cast<uint32_t>(b_mn) << 16) |
+// kind::mxf8f6f4 operand format codes (A bits [7,10), B bits [10,13)).
+enum MxFormat : uint32_t { MXF_E4M3 = 0, MXF_E5M2 = 1, MXF_E2M3 = 3, MXF_E3M2 = 4, MXF_E2M1 = 5 };
+
+__host__ __device__ constexpr uint32_t idesc_mxf8(bool a_mn, bool b_mn, int M, int N, uint32_t a_fmt = MXF_E4M3,
+                                                  uint32_t b_fmt = MXF_E4M3) {
+  return (a_fmt << 7) | (b_fmt << 10) | (static_cast<uint32_t>(a_mn) << 15) | (static_cast<uint32_t>(b_mn) << 16) |
          (static_cast<uint32_t>(N >> 3) << 17) | (1u << 23) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 

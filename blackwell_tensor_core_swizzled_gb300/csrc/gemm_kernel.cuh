@@ -54,6 +54,7 @@
 #include <cuda_fp16.h>
 
 #include <cstdint>
+#include <type_traits>
 
 #include "desc.cuh"
 #include "ptx.cuh"
@@ -109,7 +110,9 @@ struct GemmParams {
   uint32_t a_box_bytes, b_box_bytes;
   // A and B bytes one stage brings in (both CTAs of a pair): the full tiles,
   // except that a single-CTA K-major A with M < 128 loads only round_up(M, 8)
-  // rows (the rest of the smem tile is stale and feeds only rows >= M)
+  // rows (the rest of the smem tile is stale and feeds only rows >= M), and
+  // that packed 6- / 4-bit elements count only their data bytes (TMA leaves
+  // the padding of each 16-byte block unwritten)
   uint32_t ab_tx_bytes;
   uint64_t a_desc_hi, b_desc_hi;
   uint32_t a_kstep, b_kstep;  // descriptor start advance (bytes) per MMA K step
@@ -184,7 +187,9 @@ struct GemmCfg {
   static constexpr int KSTEPS = BK / MMA_K;    // MMA issues per stage
   static constexpr int SF_COL0 = ACC * BN;     // scale-factor slots follow the accumulators
   static constexpr int TMEM_COLS = 512;
-  static constexpr int SF_SLOT_COLS = 16;      // SFA 4 columns + SFB 4 per 128 rows
+  // a scale slot: SFA 4 columns, then SFB 4 per 128 rows (128-bit aligned
+  // column origins, as tcgen05.cp requires)
+  static constexpr int SF_SLOT_COLS = 4 + 4 * SFB_CHUNKS;
   // Scale slots rotate over the free TMEM columns; before a slot is
   // rewritten the MMA thread waits for the stage that last used it to retire.
   // With as many slots as ring stages the wait is implied: full[s] of
@@ -615,8 +620,11 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
     // the loop in uniform control flow (descriptors are warp-uniform values:
     // the stage-0 descriptors plus precomputed stage / K-step increments),
     // waits with one vote, and one elected lane issues the MMAs and commits.
-    // Issuing from a lane-0-only branch measured slower.
-    if (CG == 1 || rank == 0) {
+    // Issuing from a lane-0-only branch measured slower.  The loop is
+    // compiled once per scale-staging mode, so the per-stage path carries no
+    // runtime test of the mode (1.5 % at MXFP8 8192^3).
+    auto mma_role = [&](auto sf_mode_tag) {
+      constexpr int SFM = decltype(sf_mode_tag)::value;
       const uint64_t a_desc0 = sdesc(sbase, p.a_desc_hi);
       const uint64_t b_desc0 = sdesc(sbase + C::A_BYTES, p.b_desc_hi);
       const uint64_t a_step = p.a_kstep >> 4, b_step = p.b_kstep >> 4;  // 16-byte units
@@ -625,11 +633,11 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
       for (int j = 0; j < C::KSTEPS; ++j)
         idesc_j[j] = KIND == KIND_MXF8 ? (p.idesc | idesc_sf_ids(j, j)) : p.idesc;
       // block scales staged by other threads: wait for sf_ready[slot] too
-      const bool sf_wait = KIND == KIND_MXF8 && p.sf_mode != SF_BY_MMA;
-      const bool sf_by_mma = KIND == KIND_MXF8 && p.sf_mode == SF_BY_MMA;
+      constexpr bool sf_wait = KIND == KIND_MXF8 && SFM != SF_BY_MMA;
+      constexpr bool sf_by_mma = KIND == KIND_MXF8 && SFM == SF_BY_MMA;
       // the copy warp commits sf_ready[slot] only after it saw full[s] of the
       // same iteration, so that one wait covers both
-      const bool full_via_sfr = KIND == KIND_MXF8 && p.sf_mode == SF_BY_CP;
+      constexpr bool full_via_sfr = KIND == KIND_MXF8 && SFM == SF_BY_CP;
       uint32_t it = 0, s = 0, ph = 0, tcount = 0;
       bool ok = true;
       for (UnitCursor uc = uc_first; uc.valid && ok; cursor_next(uc, num_clusters, p), ++tcount) {
@@ -659,7 +667,7 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
           const uint64_t adesc = a_desc0 + st;
           const uint64_t bdesc = b_desc0 + st;
           const uint32_t sf_col = tmem_base + C::SF_COL0 + slot * C::SF_SLOT_COLS;
-          if (sf_by_mma) {
+          if constexpr (sf_by_mma) {
             // this thread stages the scales with tcgen05.cp; they arrived
             // with full[s].  The slot's previous readers (the MMAs of
             // iteration it - SF_SLOTS) must have completed.
@@ -720,6 +728,18 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
         }
       }
       __syncwarp();
+    };
+    if (CG == 1 || rank == 0) {
+      if constexpr (KIND == KIND_MXF8) {
+        if (p.sf_mode == SF_BY_MMA)
+          mma_role(std::integral_constant<int, SF_BY_MMA>{});
+        else if (p.sf_mode == SF_BY_CP)
+          mma_role(std::integral_constant<int, SF_BY_CP>{});
+        else
+          mma_role(std::integral_constant<int, SF_BY_WARPS>{});
+      } else {
+        mma_role(std::integral_constant<int, SF_BY_MMA>{});
+      }
     }
   } else if (KIND == KIND_MXF8 && warp == 3) {
     // ------------------------------------------------------------ cp thread

@@ -68,12 +68,26 @@ typedef enum { TCG_K_MAJOR = 0, TCG_MN_MAJOR = 1 } tcg_major;
 /* Accumulator / output element types. */
 typedef enum { TCG_F32 = 0, TCG_F16 = 1, TCG_BF16 = 2 } tcg_dtype;
 
-/* Operand storage types (generic entry point). */
+/* Operand storage types (generic entry point).  The last five are the
+ * element formats of kind::mxf8f6f4.block_scale.scale_vec::1X ("tcgen05.mma"
+ * page, "Weight-stationary and block scaling": ".kind and .scale_vec"), all
+ * with one e8m0 scale per 32 K elements.  E3M2, E2M3 and E2M1 are stored
+ * packed: element i of the array (i = row * ld + column, ld counted in
+ * elements) in bits [b*i, b*(i+1)) of the array read as one little-endian bit
+ * string (b = 6 or 4; an E2M1 byte holds element 2j in its low nibble).  In
+ * shared memory each sixteen of them fill a 16-byte block, data first and
+ * padding after -- the layout of the "tcgen05.cp" page's "Native FP4/FP6
+ * decompression" sources -- so a 128-byte row holds 128 elements of any of
+ * these formats. */
 typedef enum {
   TCG_IN_F16 = 0,   /* IEEE binary16, MMA kind::f16 */
   TCG_IN_BF16 = 1,  /* bfloat16, kind::f16 */
   TCG_IN_TF32 = 2,  /* float32 storage read as TF32, kind::tf32 */
-  TCG_IN_E4M3 = 3   /* OCP E4M3FN with e8m0 block scales, kind::mxf8f6f4.block_scale */
+  TCG_IN_E4M3 = 3,  /* OCP E4M3FN (FP8) */
+  TCG_IN_E5M2 = 4,  /* OCP E5M2 (FP8) */
+  TCG_IN_E3M2 = 5,  /* OCP MX E3M2 (FP6), packed */
+  TCG_IN_E2M3 = 6,  /* OCP MX E2M3 (FP6), packed */
+  TCG_IN_E2M1 = 7   /* OCP MX E2M1 (FP4), packed */
 } tcg_input;
 
 /* ---------------------------------------------------------------------------
@@ -120,6 +134,29 @@ int tcg_gemm_mxf8_blockscaled(int64_t M, int64_t N, int64_t K,
                               void* D, tcg_dtype d_type, int64_t ldd,
                               tcg_dtype acc_type, void* stream);
 
+/* Block-scaled FP6 (fmt TCG_IN_E3M2 or TCG_IN_E2M3) and FP4 (E2M1) GEMMs:
+ * the MXFP8 operation with 6- / 4-bit elements, on the same MMA kind
+ * (kind::mxf8f6f4, the format in the instruction descriptor) and the same
+ * scale layout (SFA [M][ceil(K/32)], SFB [N][ceil(K/32)] e8m0).  A and B are
+ * packed (see tcg_input), K-major only (TCG_ERR_UNSUPPORTED otherwise), lda /
+ * ldb count elements.  The tensor-map rules of the padded element types apply:
+ * K a multiple of 128, A and B 32-byte aligned, row strides (ld * 6 / 8 or
+ * ld * 4 / 8 bytes) multiples of 32 bytes (else TCG_ERR_ALIGNMENT).
+ * acc_type must be TCG_F32. */
+int tcg_gemm_mxf6_blockscaled(tcg_input fmt, int64_t M, int64_t N, int64_t K,
+                              const void* A, tcg_major a_major, int64_t lda,
+                              const void* B, tcg_major b_major, int64_t ldb,
+                              const uint8_t* SFA, const uint8_t* SFB,
+                              void* D, tcg_dtype d_type, int64_t ldd,
+                              tcg_dtype acc_type, void* stream);
+
+int tcg_gemm_mxf4_blockscaled(int64_t M, int64_t N, int64_t K,
+                              const void* A, tcg_major a_major, int64_t lda,
+                              const void* B, tcg_major b_major, int64_t ldb,
+                              const uint8_t* SFA, const uint8_t* SFB,
+                              void* D, tcg_dtype d_type, int64_t ldd,
+                              tcg_dtype acc_type, void* stream);
+
 /* Same operation and arguments as tcg_gemm_mxf8_blockscaled, for callers that
  * must not allocate device memory (for example a framework whose caching
  * allocator owns all device memory, or code that cannot afford the
@@ -150,7 +187,7 @@ typedef struct {
   tcg_input in_type;
   const void* A; tcg_major a_major; int64_t lda;
   const void* B; tcg_major b_major; int64_t ldb;
-  /* block scaling (TCG_IN_E4M3 only): either plain scales ... */
+  /* block scaling (TCG_IN_E4M3 .. TCG_IN_E2M1): either plain scales ... */
   const uint8_t* SFA; const uint8_t* SFB;
   /* ... or images already built by tcg_mxf8_prepare_scales (then SFA/SFB must
    * be NULL).  The images must have been prepared for the same M/N/K and the

@@ -6,7 +6,9 @@ product library never links, loads or calls it, and it shares no code with the
 CUDA path.
 
 * :func:`gemm` -- D = A.B (optionally block-scaled) and the error scale
-  S = sum |a||b| in float64, from the raw storage bits (C, ``gemm_oracle.c``).
+  S = sum |a||b| in float64, from the raw storage bits (C, ``gemm_oracle.c``):
+  fp32, f16, bf16, E4M3, E5M2, and the packed microscaling formats E3M2 /
+  E2M3 (6 bits) and E2M1 (4 bits).
 * :mod:`oracle.layouts` -- the pages' descriptor walk, swizzles, TMEM
   register images, ldmatrix ownership and scale-factor placement.
 
@@ -28,7 +30,9 @@ import numpy as np
 from . import layouts  # noqa: F401
 from .build import LIB, build
 
-F32, F16, BF16, E4M3 = 0, 1, 2, 3
+F32, F16, BF16, E4M3, E5M2, E3M2, E2M3, E2M1 = 0, 1, 2, 3, 4, 5, 6, 7
+#: bits per element of the packed formats (stored as a little-endian bit string)
+PACKED_BITS = {E3M2: 6, E2M3: 6, E2M1: 4}
 K_MAJOR, MN_MAJOR = 0, 1
 
 _lib = None
@@ -45,6 +49,8 @@ def _load():
         lib.oracle_gemm.restype = ci
         for name, t in (("oracle_dec_f16", ctypes.c_uint16), ("oracle_dec_bf16", ctypes.c_uint16),
                         ("oracle_dec_f32", ctypes.c_uint32), ("oracle_dec_e4m3", ctypes.c_uint8),
+                        ("oracle_dec_e5m2", ctypes.c_uint8), ("oracle_dec_e3m2", ctypes.c_uint8),
+                        ("oracle_dec_e2m3", ctypes.c_uint8), ("oracle_dec_e2m1", ctypes.c_uint8),
                         ("oracle_dec_e8m0", ctypes.c_uint8)):
             f = getattr(lib, name)
             f.argtypes = [t]
@@ -63,7 +69,8 @@ def decode(bits: np.ndarray, dtype: int) -> np.ndarray:
     (element by element; meant for pins and small arrays)."""
     lib = _load()
     f = {F32: lib.oracle_dec_f32, F16: lib.oracle_dec_f16, BF16: lib.oracle_dec_bf16,
-         E4M3: lib.oracle_dec_e4m3}[dtype]
+         E4M3: lib.oracle_dec_e4m3, E5M2: lib.oracle_dec_e5m2, E3M2: lib.oracle_dec_e3m2,
+         E2M3: lib.oracle_dec_e2m3, E2M1: lib.oracle_dec_e2m1}[dtype]
     flat = np.asarray(bits).ravel()
     return np.array([f(int(x)) for x in flat], dtype=np.float64).reshape(np.shape(bits))
 
@@ -75,7 +82,8 @@ def decode_e8m0(bits: np.ndarray) -> np.ndarray:
                     dtype=np.float64).reshape(np.shape(bits))
 
 
-_STORAGE = {F32: np.uint32, F16: np.uint16, BF16: np.uint16, E4M3: np.uint8}
+_STORAGE = {F32: np.uint32, F16: np.uint16, BF16: np.uint16, E4M3: np.uint8, E5M2: np.uint8, E3M2: np.uint8,
+            E2M3: np.uint8, E2M1: np.uint8}
 
 
 def gemm(M: int, N: int, K: int, A: np.ndarray, a_type: int, a_major: int, lda: int,
@@ -85,7 +93,9 @@ def gemm(M: int, N: int, K: int, A: np.ndarray, a_type: int, a_major: int, lda: 
     """Float64 D and S for the requested rows (all rows when ``rows`` is None).
 
     A/B are raw storage arrays (uint32 for fp32, uint16 for f16/bf16, uint8 for
-    e4m3) laid out as the C file's header states.  SFA/SFB are plain
+    e4m3 / e5m2, and uint8 bytes of the packed bit string for the 6- and 4-bit
+    formats, whose ld is still counted in elements) laid out as the C file's
+    header states.  SFA/SFB are plain
     row-major e8m0 arrays [M][ceil(K/32)] / [N][ceil(K/32)].
     Returns (D, S) of shape (len(rows), N).
     """

@@ -18,20 +18,27 @@
  * same page) every A element is multiplied by its row's e8m0 scale for the
  * 32-wide K block it falls in, and every B element by its column's:
  *
- *     dec(A)[m,k] = e4m3(A[m,k]) * 2^(SFA[m, k/32] - 127)
- *     dec(B)[k,n] = e4m3(B[k,n]) * 2^(SFB[n, k/32] - 127)
+ *     dec(A)[m,k] = fp(A[m,k]) * 2^(SFA[m, k/32] - 127)
+ *     dec(B)[k,n] = fp(B[k,n]) * 2^(SFB[n, k/32] - 127)
+ *
+ * where fp is the element format: E4M3 or E5M2 (one byte per element), E3M2 or
+ * E2M3 (6 bits, packed four to three bytes) or E2M1 (4 bits, packed two to a
+ * byte).
  *
  * S is the error scale the parity tolerance is stated against.
  *
  * Storage conventions (the page's "K-major rows enumerate M/N; MN-major rows
  * enumerate K"):  A K-major is M x K row-major, A MN-major is K x M
  * row-major; B K-major is N x K row-major, B MN-major is K x N row-major.
- * lda/ldb are the row strides of the stored matrices in elements.
+ * lda/ldb are the row strides of the stored matrices in elements.  Packed
+ * formats store element i of the whole array (i = row * ld + column) in bits
+ * [b*i, b*(i+1)) of the array read as one little-endian bit string (b = 4 or
+ * 6): an FP4 byte holds element 2j in its low nibble and 2j+1 in its high one.
  *
  * The decoders below are written from the IEEE-754 binary16 / binary32, the
- * bfloat16 (truncated binary32) and the OCP 8-bit floating point (E4M3FN,
- * E8M0) definitions by bit manipulation; every value they produce is exact in
- * float64.  FP32 storage is read exactly (no TF32 truncation): the GPU's TF32
+ * bfloat16 (truncated binary32), the OCP 8-bit floating point (E4M3FN, E5M2)
+ * and the OCP microscaling (E3M2, E2M3, E2M1, E8M0) definitions by bit
+ * manipulation; every value they produce is exact in float64.  FP32 storage is read exactly (no TF32 truncation): the GPU's TF32
  * rounding is covered by the tolerance, not by the oracle.
  */
 #include <math.h>
@@ -41,7 +48,7 @@
 #include <string.h>
 #include <unistd.h>
 
-enum { ORC_F32 = 0, ORC_F16 = 1, ORC_BF16 = 2, ORC_E4M3 = 3 };
+enum { ORC_F32 = 0, ORC_F16 = 1, ORC_BF16 = 2, ORC_E4M3 = 3, ORC_E5M2 = 4, ORC_E3M2 = 5, ORC_E2M3 = 6, ORC_E2M1 = 7 };
 enum { ORC_K_MAJOR = 0, ORC_MN_MAJOR = 1 };
 
 /* binary16: 1 sign, 5 exponent (bias 15), 10 fraction bits. */
@@ -98,10 +105,54 @@ double oracle_dec_e4m3(uint8_t x) {
   return s ? -v : v;
 }
 
+/* E5M2: 1 sign, 5 exponent (bias 15), 2 fraction bits, IEEE-like: exponent
+ * 31 is infinity (fraction 0) or NaN. */
+double oracle_dec_e5m2(uint8_t x) {
+  int s = x >> 7, e = (x >> 2) & 0x1f, f = x & 3;
+  double v;
+  if (e == 31)
+    v = f ? NAN : INFINITY;
+  else if (e == 0)
+    v = ldexp((double)f, -16); /* f/4 * 2^(1-15) */
+  else
+    v = ldexp((double)(f | 4), e - 17); /* (4+f) * 2^(e-15-2) */
+  return s ? -v : v;
+}
+
+/* The OCP microscaling element formats have no infinity or NaN: every code is
+ * a finite value (-1)^s * 2^(e-bias) * (1 + f/2^F), or 2^(1-bias) * f/2^F
+ * when e == 0. */
+static double dec_minifloat(unsigned x, int ebits, int fbits, int bias) {
+  const int s = (x >> (ebits + fbits)) & 1;
+  const int e = (x >> fbits) & ((1 << ebits) - 1);
+  const int f = x & ((1 << fbits) - 1);
+  const double v = e == 0 ? ldexp((double)f, 1 - bias - fbits) : ldexp((double)(f | (1 << fbits)), e - bias - fbits);
+  return s ? -v : v;
+}
+
+/* E3M2 (FP6): 1 sign, 3 exponent (bias 3), 2 fraction bits. */
+double oracle_dec_e3m2(uint8_t x) { return dec_minifloat(x & 0x3f, 3, 2, 3); }
+
+/* E2M3 (FP6): 1 sign, 2 exponent (bias 1), 3 fraction bits. */
+double oracle_dec_e2m3(uint8_t x) { return dec_minifloat(x & 0x3f, 2, 3, 1); }
+
+/* E2M1 (FP4): 1 sign, 2 exponent (bias 1), 1 fraction bit. */
+double oracle_dec_e2m1(uint8_t x) { return dec_minifloat(x & 0xf, 2, 1, 1); }
+
 /* E8M0: unsigned power of two 2^(b-127); 0xFF is NaN. */
 double oracle_dec_e8m0(uint8_t b) {
   if (b == 0xff) return NAN;
   return ldexp(1.0, (int)b - 127);
+}
+
+/* Code of element idx of a packed array of `bits`-bit values (little-endian
+ * bit string). */
+static unsigned packed_code(const uint8_t* p, int64_t idx, int bits) {
+  const int64_t bit = idx * bits;
+  const int sh = (int)(bit & 7);
+  unsigned two = (unsigned)p[bit >> 3];
+  if (sh + bits > 8) two |= (unsigned)p[(bit >> 3) + 1] << 8; /* the value straddles two bytes */
+  return (two >> sh) & ((1u << bits) - 1u);
 }
 
 static double dec_elem(const void* base, int type, int64_t idx) {
@@ -110,6 +161,10 @@ static double dec_elem(const void* base, int type, int64_t idx) {
     case ORC_F16: return oracle_dec_f16(((const uint16_t*)base)[idx]);
     case ORC_BF16: return oracle_dec_bf16(((const uint16_t*)base)[idx]);
     case ORC_E4M3: return oracle_dec_e4m3(((const uint8_t*)base)[idx]);
+    case ORC_E5M2: return oracle_dec_e5m2(((const uint8_t*)base)[idx]);
+    case ORC_E3M2: return oracle_dec_e3m2((uint8_t)packed_code((const uint8_t*)base, idx, 6));
+    case ORC_E2M3: return oracle_dec_e2m3((uint8_t)packed_code((const uint8_t*)base, idx, 6));
+    case ORC_E2M1: return oracle_dec_e2m1((uint8_t)packed_code((const uint8_t*)base, idx, 4));
   }
   return NAN;
 }

@@ -10,7 +10,10 @@ Storage conventions: A K-major is M x K row-major, A MN-major is K x M
 row-major; B K-major is N x K row-major, B MN-major is K x N row-major
 (rows of a K-major operand enumerate M/N, rows of an MN-major one enumerate
 K).  Scale factors are plain row-major e8m0 bytes, [M][ceil(K/32)] for A and
-[N][ceil(K/32)] for B.
+[N][ceil(K/32)] for B.  The 6- and 4-bit formats (E3M2, E2M3, E2M1) are drawn
+as uniformly random codes and stored packed, element i of the array in bits
+[b*i, b*(i+1)) of one little-endian bit string (b = 6 or 4; leading
+dimensions still count elements).
 """
 from __future__ import annotations
 
@@ -19,12 +22,16 @@ from dataclasses import dataclass, field
 import numpy as np
 import torch
 
-DTYPES = ("f16", "bf16", "tf32", "e4m3")
+DTYPES = ("f16", "bf16", "tf32", "e4m3", "e5m2", "e3m2", "e2m3", "e2m1")
+#: bits per element of the packed formats
+PACKED_BITS = {"e3m2": 6, "e2m3": 6, "e2m1": 4}
+#: formats with one e8m0 scale per 32 K elements
+BLOCK_SCALED = ("e4m3", "e5m2", "e3m2", "e2m3", "e2m1")
 
 _TORCH = {"f16": torch.float16, "bf16": torch.bfloat16, "tf32": torch.float32,
-          "e4m3": torch.float8_e4m3fn}
-_BITS = {"f16": torch.int16, "bf16": torch.int16, "tf32": torch.int32, "e4m3": torch.uint8}
-_NP_BITS = {"f16": np.uint16, "bf16": np.uint16, "tf32": np.uint32, "e4m3": np.uint8}
+          "e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}
+_BITS = {"f16": torch.int16, "bf16": torch.int16, "tf32": torch.int32, "e4m3": torch.uint8, "e5m2": torch.uint8}
+_NP_BITS = {"f16": np.uint16, "bf16": np.uint16, "tf32": np.uint32, "e4m3": np.uint8, "e5m2": np.uint8}
 
 
 @dataclass
@@ -34,7 +41,7 @@ class Workload:
     M: int
     N: int
     K: int
-    dtype: str                 # operand storage dtype: f16 | bf16 | tf32 | e4m3
+    dtype: str                 # operand storage dtype: one of DTYPES
     a_major: str = "k"         # "k" | "mn"
     b_major: str = "k"
     dist: str = "normal"       # "normal": N(0,1)/sqrt(K); "uniform": U[-1,1]; "normal1": N(0,1)
@@ -60,6 +67,12 @@ WORKLOADS = {
                                  "normal", "f16", "f16", 2, False, 4),
     "mxf8_8192": Workload("mxf8_8192", 8192, 8192, 8192, "e4m3", "k", "k",
                           "normal1", "f32", "bf16", 2, True, 5),
+    # Block-scaled FP6 / FP4 (the same MMA kind with 6- and 4-bit elements):
+    # uniformly random element codes, scales as for MXFP8.
+    "mxf6_e2m3_8192": Workload("mxf6_e2m3_8192", 8192, 8192, 8192, "e2m3", "k", "k",
+                               "codes", "f32", "bf16", 2, True, 8),
+    "mxf4_8192": Workload("mxf4_8192", 8192, 8192, 8192, "e2m1", "k", "k",
+                          "codes", "f32", "bf16", 2, True, 9),
     # Skinny (decode-like) shapes: a few rows of activations against an
     # 8192 x 8192 weight; bound by streaming B from HBM, reported in GB/s.
     "bf16_skinny_m16": Workload("bf16_skinny_m16", 16, 8192, 8192, "bf16", "k", "k",
@@ -86,10 +99,35 @@ def to_bits(x64: np.ndarray, dtype: str) -> np.ndarray:
     """Round float64 values to the storage dtype (torch RNE) and return the raw
     storage bits as a numpy unsigned array."""
     t = torch.from_numpy(np.ascontiguousarray(x64, dtype=np.float64))
-    if dtype in ("f16", "bf16", "e4m3"):
+    if dtype in ("f16", "bf16", "e4m3", "e5m2"):
         t = t.to(torch.float32)  # exact for the draws used; then one RNE rounding
     t = t.to(_TORCH[dtype]).contiguous()
     return t.view(_BITS[dtype]).numpy().view(_NP_BITS[dtype]).copy()
+
+
+def codes(shape, seed: int, bits: int) -> np.ndarray:
+    """Uniformly random element codes of a `bits`-bit format."""
+    rng = np.random.default_rng(seed)
+    return rng.integers(0, 1 << bits, size=shape, dtype=np.uint64).astype(np.uint8)
+
+
+def pack(c: np.ndarray, bits: int) -> np.ndarray:
+    """Pack a 2-D array of codes row by row into bytes: element j of a row in
+    bits [bits*j, bits*(j+1)) of the row's little-endian bit string.  The row
+    length times `bits` must be a multiple of 8."""
+    rows, n = c.shape
+    if (n * bits) % 8:
+        raise ValueError("rows must fill whole bytes")
+    v = c.astype(np.uint32)
+    if bits == 4:
+        out = v[:, 0::2] | (v[:, 1::2] << 4)
+        return out.astype(np.uint8)
+    if bits == 6:
+        g = v.reshape(rows, n // 4, 4)
+        word = g[..., 0] | (g[..., 1] << 6) | (g[..., 2] << 12) | (g[..., 3] << 18)
+        out = np.stack([word & 0xFF, (word >> 8) & 0xFF, (word >> 16) & 0xFF], axis=-1)
+        return out.reshape(rows, n // 4 * 3).astype(np.uint8)
+    raise ValueError(bits)
 
 
 def lay_out_a(a_logical: np.ndarray, major: str) -> np.ndarray:
@@ -120,12 +158,21 @@ def make_inputs(w: Workload, M: int | None = None, N: int | None = None, K: int 
     K = w.K if K is None else K
     dist = w.dist if dist is None else dist
     i = w.seed_base
-    a = draw((M, K), 1000 + i, dist, K)
-    b = draw((K, N), 2000 + i, dist, K)
-    A = lay_out_a(to_bits(a, w.dtype), w.a_major)
-    B = lay_out_b(to_bits(b, w.dtype), w.b_major)
-    out = {"A": A, "B": B, "lda": A.shape[1], "ldb": B.shape[1], "M": M, "N": N, "K": K,
-           "SFA": None, "SFB": None}
+    if w.dtype in PACKED_BITS:
+        # packed formats: K-major only; codes drawn per storage row
+        if w.a_major != "k" or w.b_major != "k":
+            raise ValueError("packed formats are stored K-major")
+        bits = PACKED_BITS[w.dtype]
+        A = pack(codes((M, K), 1000 + i, bits), bits)
+        B = pack(codes((N, K), 2000 + i, bits), bits)
+        out = {"A": A, "B": B, "lda": K, "ldb": K, "M": M, "N": N, "K": K, "SFA": None, "SFB": None}
+    else:
+        a = draw((M, K), 1000 + i, dist, K)
+        b = draw((K, N), 2000 + i, dist, K)
+        A = lay_out_a(to_bits(a, w.dtype), w.a_major)
+        B = lay_out_b(to_bits(b, w.dtype), w.b_major)
+        out = {"A": A, "B": B, "lda": A.shape[1], "ldb": B.shape[1], "M": M, "N": N, "K": K,
+               "SFA": None, "SFB": None}
     if w.block_scaled:
         out["SFA"] = scales(M, K, 3000 + i)
         out["SFB"] = scales(N, K, 4000 + i)

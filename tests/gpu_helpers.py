@@ -7,9 +7,9 @@ import torch
 
 import synthetic as syn
 
-IN_TYPE = {"f16": 0, "bf16": 1, "tf32": 2, "e4m3": 3}          # tcg_input
-ORACLE_TYPE = {"f16": 1, "bf16": 2, "tf32": 0, "e4m3": 3}       # oracle enum
-ESIZE = {"f16": 2, "bf16": 2, "tf32": 4, "e4m3": 1}
+IN_TYPE = {"f16": 0, "bf16": 1, "tf32": 2, "e4m3": 3, "e5m2": 4, "e3m2": 5, "e2m3": 6, "e2m1": 7}  # tcg_input
+ORACLE_TYPE = {"f16": 1, "bf16": 2, "tf32": 0, "e4m3": 3, "e5m2": 4, "e3m2": 5, "e2m3": 6, "e2m1": 7}  # oracle enum
+ESIZE = {"f16": 2, "bf16": 2, "tf32": 4, "e4m3": 1, "e5m2": 1}   # bytes per element (unpacked formats)
 OUT = {"f32": (0, torch.float32), "f16": (1, torch.float16), "bf16": (2, torch.bfloat16)}
 ACC = {"f32": 0, "f16": 1}
 TAU = {"f32": 2e-3, "f16": 1e-2}   # parity tolerance per accumulator type (x sum|a||b|)
@@ -39,8 +39,11 @@ def pad_ld(bits: np.ndarray, esize: int, seed: int) -> np.ndarray:
 
 
 def make_case(dtype, am, bm, M, N, K, dist="uniform", seed=7, extra_pad=0):
-    w = syn.Workload("case", M, N, K, dtype, am, bm, dist, block_scaled=(dtype == "e4m3"), seed_base=seed)
+    w = syn.Workload("case", M, N, K, dtype, am, bm, dist, block_scaled=(dtype in syn.BLOCK_SCALED), seed_base=seed)
     x = syn.make_inputs(w)
+    x["w"] = w
+    if dtype in syn.PACKED_BITS:  # packed rows of K elements (K a multiple of 128) are 32-byte multiples
+        return x
     es = ESIZE[dtype]
     A = pad_ld(x["A"], es, seed + 11)
     B = pad_ld(x["B"], es, seed + 12)
@@ -64,7 +67,7 @@ def run_gpu(tcg, x, out="bf16", acc="f32", cta_group=0, ldd=None, D=None, raster
     if D is None:
         D = torch.full((max(M, 1), ldd), float("nan"), dtype=tdt, device="cuda")
     kw = {}
-    if w.dtype == "e4m3":
+    if w.block_scaled:
         if sf_img is not None:
             kw = dict(SFA_img=sf_img[0], SFB_img=sf_img[1])
         else:

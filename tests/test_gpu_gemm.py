@@ -79,6 +79,64 @@ def test_small_ragged_full_compare(tcg, oracle_mod, dtype, am, bm, M, N, K, cg, 
     _check_full(tcg, oracle_mod, x, out, acc, cg, split_k=split_k)
 
 
+# The block-scaled formats on kind::mxf8f6f4 besides E4M3: E5M2 bytes, and the
+# packed FP6 (E3M2, E2M3) and FP4 (E2M1) formats, K-major and K a multiple of
+# 128 for the packed ones; ragged M and N, single CTAs and pairs.
+MX_FORMATS = [
+    ("e5m2", "k", "k", 300, 520, 256, 2, "bf16"),
+    ("e5m2", "mn", "k", 200, 300, 96, 1, "f32"),
+    ("e2m3", "k", "k", 300, 520, 256, 2, "bf16"),
+    ("e2m3", "k", "k", 200, 384, 384, 1, "f32"),
+    ("e3m2", "k", "k", 513, 700, 512, 2, "bf16"),
+    ("e3m2", "k", "k", 100, 300, 128, 1, "f32"),   # sums reach past the f16 range
+    ("e2m1", "k", "k", 300, 520, 256, 2, "bf16"),
+    ("e2m1", "k", "k", 1000, 1100, 640, 0, "bf16"),
+    ("e2m1", "k", "k", 64, 256, 128, 1, "f32"),
+]
+
+
+@pytest.mark.parametrize("dtype,am,bm,M,N,K,cg,out", MX_FORMATS)
+def test_block_scaled_formats_full_compare(tcg, oracle_mod, dtype, am, bm, M, N, K, cg, out):
+    x = make_case(dtype, am, bm, M, N, K, dist="codes" if dtype in syn.PACKED_BITS else "normal1", seed=M + K)
+    _check_full(tcg, oracle_mod, x, out, "f32", cg)
+
+
+@pytest.mark.parametrize("dtype,one", [("e2m1", 0x2), ("e2m3", 0x08), ("e3m2", 0x0C)])
+def test_packed_identity_reads_every_code_in_place(tcg, oracle_mod, dtype, one):
+    """A = I (the code of 1.0 on the diagonal, scales 2^0) and B random codes:
+    D[m, n] = B[n, m] decoded, exactly.  Pins how TMA expands the packed rows
+    into shared memory and where the MMA reads each code, bit for bit."""
+    bits = syn.PACKED_BITS[dtype]
+    n, N = 256, 384
+    A = syn.pack(np.where(np.eye(n, dtype=bool), one, 0).astype(np.uint8), bits)
+    codes = syn.codes((N, n), 41 + bits, bits)
+    B = syn.pack(codes, bits)
+    SFA = np.full((n, n // 32), 127, np.uint8)
+    SFB = np.full((N, n // 32), 127, np.uint8)
+    D = torch.full((n, N), float("nan"), dtype=torch.float32, device="cuda")
+    t = {"e2m1": tcg.IN_E2M1, "e2m3": tcg.IN_E2M3, "e3m2": tcg.IN_E3M2}[dtype]
+    tcg.gemm(n, N, n, t, to_device(A), 0, n, to_device(B), 0, n, D, 0, N, 0, SFA=to_device(SFA), SFB=to_device(SFB))
+    assert tcg.check() == 0
+    expect = oracle_mod.decode(codes, oracle_mod.E2M1 if dtype == "e2m1" else
+                               oracle_mod.E2M3 if dtype == "e2m3" else oracle_mod.E3M2).T
+    assert np.array_equal(D.double().cpu().numpy(), expect)
+
+
+def test_named_fp6_fp4_entry_points(tcg, oracle_mod):
+    for fmt, dtype in ((tcg.IN_E3M2, "e3m2"), (tcg.IN_E2M3, "e2m3"), (None, "e2m1")):
+        x = make_case(dtype, "k", "k", 256, 320, 256, dist="codes", seed=5)
+        D = torch.full((256, 320), float("nan"), dtype=torch.bfloat16, device="cuda")
+        args = (256, 320, 256, to_device(x["A"]), 0, 256, to_device(x["B"]), 0, 256, to_device(x["SFA"]),
+                to_device(x["SFB"]), D, 2, 320, 0)
+        if fmt is None:
+            tcg.gemm_mxf4_blockscaled(*args)
+        else:
+            tcg.gemm_mxf6_blockscaled(fmt, *args)
+        assert tcg.check() == 0
+        ref, S = oracle_rows(oracle_mod, x)
+        assert_parity(D.double().cpu().numpy(), ref, S, TAU["f32"], dtype, "bf16")
+
+
 def test_identity_gives_b_exactly(tcg, oracle_mod):
     # A = I: every D row is a B row, exact in bf16 out; pins the output layout.
     n, N = 256, 384
@@ -383,7 +441,7 @@ def test_named_entry_points(tcg, oracle_mod):
 # ------------------------------------------------------------- full-size workloads
 
 FULL = ["tile_f16_128x128x64", "bf16_4096_kmn_cta1", "tf32_2048x2048x8192", "bf16_8192_cta2",
-        "f16acc_8192_cta2", "mxf8_8192", "bf16_skinny_m16", "bf16_skinny_m128"]
+        "f16acc_8192_cta2", "mxf8_8192", "bf16_skinny_m16", "bf16_skinny_m128", "mxf6_e2m3_8192", "mxf4_8192"]
 
 
 @pytest.mark.parametrize("name", FULL)

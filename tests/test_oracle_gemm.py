@@ -203,3 +203,108 @@ def test_planted_mistakes_are_caught(oracle_mod):
     D_full, _ = oracle_mod.gemm(16, 16, 64, y["A"], 3, 0, 64, y["B"], 3, 0, 64,
                                 SFA=y["SFA"], SFB=y["SFB"])
     assert not np.allclose(D_noscale, D_full)
+
+
+# ---------------------------------------------------------------------------
+# E5M2 and the packed microscaling formats (E3M2, E2M3, E2M1)
+# ---------------------------------------------------------------------------
+
+def test_e5m2_decoder_matches_torch_over_all_codes(oracle_mod):
+    import torch
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e5m2).to(torch.float64).numpy()
+    got = oracle_mod.decode(codes, oracle_mod.E5M2)
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok])
+
+
+def _embed(code, ebits, fbits, wide_ebits, wide_fbits, wide_bias, bias):
+    """Bit fields of a normal narrow code re-based into a wider format's code
+    (same sign and fraction, exponent shifted by the bias difference)."""
+    s = (code >> (ebits + fbits)) & 1
+    e = (code >> fbits) & ((1 << ebits) - 1)
+    f = code & ((1 << fbits) - 1)
+    return (s << 7) | ((e - bias + wide_bias) << wide_fbits) | (f << (wide_fbits - fbits))
+
+
+@pytest.mark.parametrize("fmt,ebits,fbits,bias,wide", [
+    ("E2M3", 2, 3, 1, "e4m3"), ("E3M2", 3, 2, 3, "e5m2"), ("E2M1", 2, 1, 1, "e4m3")])
+def test_microscaling_normals_match_torch_8bit_decoders(oracle_mod, fmt, ebits, fbits, bias, wide):
+    """Every normal E2M3 / E2M1 value is exactly an E4M3 value and every
+    normal E3M2 value an E5M2 value (same fraction bits, exponent re-based):
+    torch's 8-bit decoders give the expected values independently of the
+    oracle's formula."""
+    import torch
+    bits = 1 + ebits + fbits
+    all_codes = np.arange(1 << bits, dtype=np.uint8)
+    normal = all_codes[((all_codes >> fbits) & ((1 << ebits) - 1)) != 0]
+    wb, wf, wbias = (4, 3, 7) if wide == "e4m3" else (5, 2, 15)
+    wide_codes = np.array([_embed(int(c), ebits, fbits, wb, wf, wbias, bias) for c in normal], dtype=np.uint8)
+    tdt = torch.float8_e4m3fn if wide == "e4m3" else torch.float8_e5m2
+    ref = torch.from_numpy(wide_codes).view(tdt).to(torch.float64).numpy()
+    got = oracle_mod.decode(normal, getattr(oracle_mod, fmt))
+    assert np.array_equal(got, ref), (fmt, got, ref)
+
+
+def test_microscaling_constants_from_the_ocp_spec(oracle_mod):
+    """The OCP Microscaling specification's tabulated limits: E2M3 max normal
+    7.5, min normal 1.0, max subnormal 0.875, min subnormal 0.125; E3M2 28,
+    0.25, 0.1875, 0.0625; E2M1 6, 1, 0.5 (its only subnormal); no infinities
+    or NaNs, the sign in the top bit."""
+    d = oracle_mod.decode
+    for fmt, codes_vals in ((oracle_mod.E2M3, {0x1F: 7.5, 0x08: 1.0, 0x07: 0.875, 0x01: 0.125, 0x3F: -7.5}),
+                            (oracle_mod.E3M2, {0x1F: 28.0, 0x04: 0.25, 0x03: 0.1875, 0x01: 0.0625, 0x3F: -28.0}),
+                            (oracle_mod.E2M1, {0x7: 6.0, 0x2: 1.0, 0x1: 0.5, 0xF: -6.0})):
+        for c, v in codes_vals.items():
+            assert d(np.array([c], np.uint8), fmt)[0] == v, (fmt, hex(c))
+    e2m1 = d(np.arange(16, dtype=np.uint8), oracle_mod.E2M1)
+    assert e2m1.tolist()[:8] == [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    assert np.array_equal(e2m1[8:], -e2m1[:8])
+    for fmt, bits in ((oracle_mod.E2M3, 6), (oracle_mod.E3M2, 6), (oracle_mod.E2M1, 4)):
+        v = d(np.arange(1 << bits, dtype=np.uint8), fmt)
+        assert np.all(np.isfinite(v))
+        pos = v[: 1 << (bits - 1)]
+        assert np.all(np.diff(pos) > 0)  # codes 0 .. 2^(b-1)-1 are increasing magnitudes
+
+
+def _bitstring_pack(codes_2d, bits):
+    """Reference packer, one bit at a time: element j of a row at bits
+    [bits*j, bits*(j+1)) of the row's little-endian bit string."""
+    rows, n = codes_2d.shape
+    out = np.zeros((rows, n * bits // 8), dtype=np.uint8)
+    for r in range(rows):
+        for j in range(n):
+            for b in range(bits):
+                if (int(codes_2d[r, j]) >> b) & 1:
+                    pos = j * bits + b
+                    out[r, pos // 8] |= np.uint8(1 << (pos % 8))
+    return out
+
+
+@pytest.mark.parametrize("fmt,bits,one", [("E2M3", 6, 0x08), ("E3M2", 6, 0x0C), ("E2M1", 4, 0x2)])
+def test_packed_fetch_through_an_identity_gemm(oracle_mod, fmt, bits, one):
+    """A (M x K codes, packed) times B = the K x K identity (code of 1.0 on the
+    diagonal, scales 2^0) returns every decoded element of A at its (m, k):
+    the oracle's packed-element fetch agrees with an independent bit-by-bit
+    packer and with the input generator's packer; swapping the nibble or
+    value order in the packing is caught."""
+    import synthetic as syn
+    M, K = 5, 64
+    rng = np.random.default_rng(bits)
+    codes = rng.integers(0, 1 << bits, size=(M, K)).astype(np.uint8)
+    A = _bitstring_pack(codes, bits)
+    assert np.array_equal(A, syn.pack(codes, bits))
+    eye = np.where(np.eye(K, dtype=bool), one, 0).astype(np.uint8)
+    B = _bitstring_pack(eye, bits)
+    t = getattr(oracle_mod, fmt)
+    sfa = np.full((M, K // 32), 127, np.uint8)
+    sfb = np.full((K, K // 32), 127, np.uint8)
+    D, _ = oracle_mod.gemm(M, K, K, A, t, 0, K, B, t, 0, K, SFA=sfa, SFB=sfb)
+    assert np.array_equal(D, oracle_mod.decode(codes, t))
+    # planted mistake: the values of each pair (FP4) or group of four (FP6)
+    # in reverse order
+    g = 2 if bits == 4 else 4
+    swapped = codes.reshape(M, K // g, g)[:, :, ::-1].reshape(M, K)
+    D2, _ = oracle_mod.gemm(M, K, K, _bitstring_pack(swapped, bits), t, 0, K, B, t, 0, K, SFA=sfa, SFB=sfb)
+    assert not np.array_equal(D2, D)
