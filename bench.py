@@ -43,15 +43,21 @@ import synthetic as syn  # noqa: E402
 
 METRIC = "GEMM TFLOP/s at 1 GB300 and % of dtype dense tensor peak (bf16/mxf8 8192^3)"
 UNIT = "TFLOP/s"
-IN_TYPE = {"f16": 0, "bf16": 1, "tf32": 2, "e4m3": 3}
+IN_TYPE = {"f16": 0, "bf16": 1, "tf32": 2, "e4m3": 3, "e5m2": 4, "e3m2": 5, "e2m3": 6, "e2m1": 7}
 OUT = {"f32": 0, "f16": 1, "bf16": 2}
 ACC = {"f32": 0, "f16": 1}
-ESIZE = {"f16": 2, "bf16": 2, "tf32": 4, "e4m3": 1}
+ESIZE = {"f16": 2, "bf16": 2, "tf32": 4, "e4m3": 1, "e5m2": 1, "e3m2": 0.75, "e2m3": 0.75, "e2m1": 0.5}
 # nominal dense tensor rate relative to bf16 (NVIDIA GB300 figures: tf32 1.1,
-# bf16/fp16 2.25, fp8 4.5 PFLOP/s)
-NOMINAL_RATIO = {"bf16": 1.0, "f16": 1.0, "tf32": 1.1 / 2.25, "e4m3": 2.0}
-# NVIDIA's dense (no 2:4 sparsity) GB300 datasheet rates, TFLOP/s
-DATASHEET_DENSE_TFLOPS = {"bf16": 2250.0, "f16": 2250.0, "tf32": 1100.0, "e4m3": 4500.0}
+# bf16/fp16 2.25, fp8 4.5 PFLOP/s).  FP6 and FP4 elements on the MMA kind
+# used here (kind::mxf8f6f4, one byte of shared memory per element) run at the
+# FP8 rate; the datasheet's 13.5 PFLOP/s FP4 figure is that of the packed
+# FP4 kinds.
+NOMINAL_RATIO = {"bf16": 1.0, "f16": 1.0, "tf32": 1.1 / 2.25, "e4m3": 2.0, "e5m2": 2.0, "e3m2": 2.0, "e2m3": 2.0,
+                 "e2m1": 2.0}
+# NVIDIA's dense (no 2:4 sparsity) GB300 datasheet rates, TFLOP/s, for the
+# MMA kind each format runs on
+DATASHEET_DENSE_TFLOPS = {"bf16": 2250.0, "f16": 2250.0, "tf32": 1100.0, "e4m3": 4500.0, "e5m2": 4500.0,
+                          "e3m2": 4500.0, "e2m3": 4500.0, "e2m1": 4500.0}
 PROFILE_DIR = os.path.join(ROOT, "profiles")
 KERNEL_SOURCES = ["gemm_kernel.cuh", "ptx.cuh", "desc.cuh", "gemm_f16.cu", "gemm_tf32.cu", "gemm_mxf8.cu", "api.cu",
                   "splitk_reduce.cu"]
@@ -199,7 +205,7 @@ def run_workload(tcg, torch, w, steps, warmup, dist_ctx, measure_e2e=True):
             n += 1
             if ev_pair:
                 ev_pair[0].record(stream)
-            tcg.gemm(M, N, K, 3, A, a_maj, x["lda"], B, b_maj, x["ldb"], D, OUT[w.out], N, ACC[w.acc],
+            tcg.gemm(M, N, K, IN_TYPE[w.dtype], A, a_maj, x["lda"], B, b_maj, x["ldb"], D, OUT[w.out], N, ACC[w.acc],
                      SFA_img=ia, SFB_img=ib, cta_group=w.cta_group, stream=sp)
         else:
             if ev_pair:
@@ -279,9 +285,18 @@ def run_workload(tcg, torch, w, steps, warmup, dist_ctx, measure_e2e=True):
             if started[0][bi]:
                 comp.wait_event(ev["down"][bi])  # the result of step i-2 has left this buffer
             cs = comp.cuda_stream
-            if scaled:
+            if scaled and w.dtype == "e4m3":
                 tcg.gemm_mxf8_blockscaled(M, N, K, dA[bi], a_maj, x["lda"], dB[bi], b_maj, x["ldb"], dSFA[bi],
                                           dSFB[bi], dD[bi], OUT[w.out], N, ACC[w.acc], stream=cs)
+            elif scaled and w.dtype == "e2m1":
+                tcg.gemm_mxf4_blockscaled(M, N, K, dA[bi], a_maj, x["lda"], dB[bi], b_maj, x["ldb"], dSFA[bi],
+                                          dSFB[bi], dD[bi], OUT[w.out], N, ACC[w.acc], stream=cs)
+            elif scaled and w.dtype in ("e3m2", "e2m3"):
+                tcg.gemm_mxf6_blockscaled(IN_TYPE[w.dtype], M, N, K, dA[bi], a_maj, x["lda"], dB[bi], b_maj,
+                                          x["ldb"], dSFA[bi], dSFB[bi], dD[bi], OUT[w.out], N, ACC[w.acc], stream=cs)
+            elif scaled:
+                tcg.gemm(M, N, K, IN_TYPE[w.dtype], dA[bi], a_maj, x["lda"], dB[bi], b_maj, x["ldb"], dD[bi],
+                         OUT[w.out], N, ACC[w.acc], SFA=dSFA[bi], SFB=dSFB[bi], stream=cs)
             else:
                 fn = {"f16": tcg.gemm_f16, "bf16": tcg.gemm_bf16, "tf32": tcg.gemm_tf32}[w.dtype]
                 fn(M, N, K, dA[bi], a_maj, x["lda"], dB[bi], b_maj, x["ldb"], dD[bi], OUT[w.out], N, ACC[w.acc],
@@ -361,7 +376,8 @@ def oracle_sample(w, x, rows_n: int):
     """Time the float64 oracle on `rows_n` output rows (all N columns) of the
     workload (inputs `x` already generated); returns (TFLOP/s, seconds, threads)."""
     import oracle
-    t = {"f16": oracle.F16, "bf16": oracle.BF16, "tf32": oracle.F32, "e4m3": oracle.E4M3}[w.dtype]
+    t = {"f16": oracle.F16, "bf16": oracle.BF16, "tf32": oracle.F32, "e4m3": oracle.E4M3, "e5m2": oracle.E5M2,
+         "e3m2": oracle.E3M2, "e2m3": oracle.E2M3, "e2m1": oracle.E2M1}[w.dtype]
     rows = np.linspace(0, w.M - 1, rows_n).astype(np.int64)
     threads = oracle.num_threads()
     t0 = time.perf_counter()
@@ -427,7 +443,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="bf16_8192_cta2", choices=sorted(syn.WORKLOADS))
     ap.add_argument("--secondary",
-                    default="mxf8_8192,bf16_skinny_m16,bf16_4096_kmn_cta1,tf32_2048x2048x8192,f16acc_8192_cta2",
+                    default="mxf8_8192,bf16_skinny_m16,bf16_4096_kmn_cta1,tf32_2048x2048x8192,f16acc_8192_cta2,"
+                            "mxf6_e2m3_8192,mxf4_8192",
                     help="comma list of extra workloads ('' for none)")
     ap.add_argument("--sustained-s", type=float, default=1.5,
                     help="length of the back-to-back sustained pass of the headline workload (0: skip)")

@@ -567,14 +567,20 @@ int run_gemm(const tcg_gemm_args* args, cudaStream_t s) {
   prm.d_type = a.d_type == TCG_F32 ? OUT_F32 : a.d_type == TCG_F16 ? OUT_F16 : OUT_BF16;
   prm.acc_f16 = a.acc_type == TCG_F16;
   prm.d_vec_ok = (reinterpret_cast<uintptr_t>(a.D) % 16 == 0) && ((a.ldd * ds) % 16 == 0);
-  // 16-bit outputs leave through TMA tile stores when the map's alignment
-  // rules hold (16-byte base and row stride); otherwise per-thread row stores
+  // Outputs leave through TMA tile stores (32 rows x 64 bytes: 32 columns of
+  // 16-bit values, 16 of fp32) when the map's alignment rules hold (16-byte
+  // base and row stride); otherwise per-thread row stores.  fp32 tiles
+  // replace per-lane row stores, in which one warp store instruction touches
+  // 32 rows.
   prm.d_tma = 0;
   prm.d_trans = d_trans ? 1 : 0;
-  if (a.d_type != TCG_F32 && prm.d_vec_ok && !d_trans) {
-    const CUtensorMapDataType dt = a.d_type == TCG_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    if (int rc = make_map_2d(&prm.tmap_d, a.D, dt, 2, static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.M),
-                             static_cast<uint64_t>(a.ldd), 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+  if (prm.d_vec_ok && !d_trans) {
+    const CUtensorMapDataType dt = a.d_type == TCG_BF16  ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                   : a.d_type == TCG_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                         : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    if (int rc = make_map_2d(&prm.tmap_d, a.D, dt, ds, static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.M),
+                             static_cast<uint64_t>(a.ldd), static_cast<uint32_t>(64 / ds), 32,
+                             CU_TENSOR_MAP_SWIZZLE_64B))
       return rc;
     prm.d_tma = 1;
   }

@@ -19,9 +19,9 @@
 //               GemmParams::sf_mode SF_BY_CP a separate copy warp:
 //               tcgen05.cp + commit -> sf_ready[slot];
 //   warps 4..7  epilogue: tcgen05.ld .32x32b from accumulator b (warp w
-//               reads lanes 32*(w%4)..+31), convert, store to global (16-bit
-//               outputs through a shared staging tile and a TMA tile store),
-//               then arrive acc_empty[b];
+//               reads lanes 32*(w%4)..+31), convert, store to global
+//               (through a shared staging tile and a TMA tile store when
+//               the output's alignment allows), then arrive acc_empty[b];
 //   warps 8..11 (block scaling) with SF_BY_WARPS: scale staging, each warp
 //               writes its TMEM lane quadrant of the stage's scale slot with
 //               tcgen05.st and arrives sf_ready[slot]; otherwise they join
@@ -81,7 +81,7 @@ struct GemmParams {
   CUtensorMap tmap_b;
   CUtensorMap tmap_sfa;
   CUtensorMap tmap_sfb;
-  CUtensorMap tmap_d;  // 16-bit D in 32 x 32 boxes, 64-byte swizzle (used when d_tma)
+  CUtensorMap tmap_d;  // D in 32-row x 64-byte boxes, 64-byte swizzle (used when d_tma)
   CUtensorMap tmap_w;  // fp32 partial-tile slots [slots][w_rows][BN] in 16 x 32 x 1 boxes, 64-byte swizzle
   int M, N, K;
   int num_m_tiles;   // tiles of 128*CG rows
@@ -123,7 +123,9 @@ struct GemmParams {
   int d_type;
   int acc_f16;
   int d_vec_ok;
-  int d_tma;  // 16-bit output stored by TMA from a per-warp shared staging tile
+  // output stored by TMA from per-warp 32-row x 64-byte shared staging tiles
+  // (32 columns of a 16-bit output, 16 of an fp32 one per tile)
+  int d_tma;
   // the kernel computes the transposed product: its (row r, column c) is
   // D[c * ldd + r] (f32 accumulation, 32-column variant only; set by the host
   // for few-row problems whose operands it swapped)
@@ -981,6 +983,15 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
           if (n0 + 32 * c < p.N) {
             if (TRANS && p.d_trans) {
               if (row < p.M) store_col32(p, row, n0 + 32 * c, r);
+            } else if (p.d_tma && p.d_type == OUT_F32) {
+              // fp32: two 16-column halves, each a 32 x 64-byte staging tile
+              uint32_t h[16];
+#pragma unroll
+              for (int k = 0; k < 16; ++k) h[k] = r[k];
+              store_tile16(row0, n0 + 32 * c, h);
+#pragma unroll
+              for (int k = 0; k < 16; ++k) h[k] = r[16 + k];
+              store_tile16(row0, n0 + 32 * c + 16, h);
             } else if (p.d_tma) {
               uint32_t h[16];
               pack16(r, h);
