@@ -28,6 +28,15 @@ namespace {
 
 thread_local std::string t_last_error;
 thread_local int t_last_launches = 0;
+// The last call's plan, formatted only when tcg_last_plan_string asks for it
+// (formatting on every call measured a quarter of a microsecond).
+struct PlanRecord {
+  bool valid = false;
+  bool k_zero = false;
+  int cg = 0, bn = 0, clusters = 0, split = 0;
+  bool swapped = false, stream_k = false;
+};
+thread_local PlanRecord t_plan;
 thread_local std::string t_last_plan;
 // phase trace requested for the next GEMM launch on this thread
 thread_local unsigned long long* t_trace_buf = nullptr;
@@ -117,6 +126,50 @@ int encode_ready() {
   return g_encode ? TCG_OK : TCG_ERR_CUDA;
 }
 
+// Encoded tensor maps, per host thread: a map is a pure function of its
+// encode arguments (data type, base address, extents, strides, box, swizzle),
+// so a map found under the same arguments is the map the driver would return
+// again.  A 64-slot direct-mapped table keyed by an FNV-1a hash of the
+// arguments; a colliding key replaces the slot.  Per thread, so no lock.
+struct MapKey {
+  uint64_t base;
+  uint64_t dims[3];
+  uint64_t strides[2];
+  uint32_t box[3];
+  uint32_t dt, rank, sw;
+};
+struct MapSlot {
+  MapKey key;
+  CUtensorMap map;
+  bool used;
+};
+constexpr int kMapSlots = 64;
+thread_local MapSlot t_maps[kMapSlots];
+
+uint64_t map_key_hash(const MapKey& k) {
+  const unsigned char* p = reinterpret_cast<const unsigned char*>(&k);
+  uint64_t h = 1469598103934665603ull;
+  for (size_t i = 0; i < sizeof k; ++i) h = (h ^ p[i]) * 1099511628211ull;
+  return h;
+}
+
+int encode_map(CUtensorMap* map, const MapKey& key, CUtensorMapDataType dt, void* base, const cuuint64_t* dims,
+               const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle sw) {
+  MapSlot& slot = t_maps[map_key_hash(key) % kMapSlots];
+  if (slot.used && std::memcmp(&slot.key, &key, sizeof key) == 0) {
+    *map = slot.map;
+    return TCG_OK;
+  }
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = g_encode(map, dt, key.rank, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return static_cast<int>(r);
+  slot.key = key;
+  slot.map = *map;
+  slot.used = true;
+  return TCG_OK;
+}
+
 // 2-D tiled tensor map over a row-major matrix: `inner` elements per row
 // (contiguous), `outer` rows, `ld` elements between rows.
 int make_map_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int esize, uint64_t inner,
@@ -128,11 +181,19 @@ int make_map_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int 
   const cuuint64_t dims[2] = {inner, outer};
   const cuuint64_t strides[1] = {ld * static_cast<uint64_t>(esize)};
   const cuuint32_t box[2] = {box_inner, box_outer};
-  const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = g_encode(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
-                              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) {
+  MapKey key;
+  std::memset(&key, 0, sizeof key);
+  key.base = reinterpret_cast<uint64_t>(base);
+  key.dims[0] = inner;
+  key.dims[1] = outer;
+  key.strides[0] = strides[0];
+  key.box[0] = box_inner;
+  key.box[1] = box_outer;
+  key.dt = static_cast<uint32_t>(dt);
+  key.rank = 2;
+  key.sw = static_cast<uint32_t>(sw);
+  const int r = encode_map(map, key, dt, const_cast<void*>(base), dims, strides, box, sw);
+  if (r != TCG_OK) {
     char buf[160];
     std::snprintf(buf, sizeof buf, "cuTensorMapEncodeTiled failed (%d): dims %llu x %llu, ld %llu, box %u x %u",
                   static_cast<int>(r), static_cast<unsigned long long>(inner),
@@ -154,11 +215,20 @@ int make_map_3d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int 
   const cuuint64_t dims[3] = {inner, mid, outer};
   const cuuint64_t strides[2] = {inner * static_cast<uint64_t>(esize), inner * mid * static_cast<uint64_t>(esize)};
   const cuuint32_t box[3] = {box_inner, box_mid, 1};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  const CUresult r = g_encode(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
-                              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) {
+  MapKey key;
+  std::memset(&key, 0, sizeof key);
+  key.base = reinterpret_cast<uint64_t>(base);
+  for (int i = 0; i < 3; ++i) key.dims[i] = dims[i];
+  key.strides[0] = strides[0];
+  key.strides[1] = strides[1];
+  key.box[0] = box_inner;
+  key.box[1] = box_mid;
+  key.box[2] = 1;
+  key.dt = static_cast<uint32_t>(dt);
+  key.rank = 3;
+  key.sw = static_cast<uint32_t>(sw);
+  const int r = encode_map(map, key, dt, const_cast<void*>(base), dims, strides, box, sw);
+  if (r != TCG_OK) {
     t_last_error = "cuTensorMapEncodeTiled (3D) failed (" + std::to_string(static_cast<int>(r)) + ")";
     return TCG_ERR_CUDA;
   }
@@ -456,7 +526,7 @@ int setup_operand(const void* ptr, tcg_input it, tcg_major major, int64_t mn, in
 int run_gemm(const tcg_gemm_args* args, cudaStream_t s) {
   load_timeout_env();
   t_last_launches = 0;
-  t_last_plan.clear();
+  t_plan = PlanRecord();
   if (!args) return TCG_ERR_INVALID;
   tcg_gemm_args a = *args;
   if (a.M < 0 || a.N < 0 || a.K < 0) return TCG_ERR_INVALID;
@@ -502,7 +572,8 @@ int run_gemm(const tcg_gemm_args* args, cudaStream_t s) {
                                             static_cast<size_t>(a.M), s);
     if (e != cudaSuccess) return record_cuda(e);
     t_last_launches = 1;
-    t_last_plan = "K = 0: D zeroed";
+    t_plan.valid = true;
+    t_plan.k_zero = true;
     return TCG_OK;
   }
 
@@ -683,12 +754,13 @@ int run_gemm(const tcg_gemm_args* args, cudaStream_t s) {
     launches += 1;
   }
   t_last_launches = launches;
-  char buf[160];
-  std::snprintf(buf, sizeof buf, "cta_group %d, tile %dx%d%s, %d clusters, %s%s", cg, 128 * cg, bn,
-                d_trans ? " (operands swapped, D stored transposed)" : "", clusters,
-                stream_k ? "stream-K" : split > 1 ? "split-K " : "one pass per tile",
-                split > 1 ? std::to_string(split).c_str() : "");
-  t_last_plan = buf;
+  t_plan.valid = true;
+  t_plan.cg = cg;
+  t_plan.bn = bn;
+  t_plan.clusters = clusters;
+  t_plan.split = split;
+  t_plan.swapped = d_trans;
+  t_plan.stream_k = stream_k;
   return TCG_OK;
 }
 
@@ -922,7 +994,22 @@ const char* tcg_last_error_string(void) { return t_last_error.c_str(); }
 
 int tcg_last_launch_count(void) { return t_last_launches; }
 
-const char* tcg_last_plan_string(void) { return t_last_plan.c_str(); }
+const char* tcg_last_plan_string(void) {
+  const PlanRecord& p = t_plan;
+  if (!p.valid) {
+    t_last_plan.clear();
+  } else if (p.k_zero) {
+    t_last_plan = "K = 0: D zeroed";
+  } else {
+    char buf[160];
+    std::snprintf(buf, sizeof buf, "cta_group %d, tile %dx%d%s, %d clusters, %s%s", p.cg, 128 * p.cg, p.bn,
+                  p.swapped ? " (operands swapped, D stored transposed)" : "", p.clusters,
+                  p.stream_k ? "stream-K" : p.split > 1 ? "split-K " : "one pass per tile",
+                  p.split > 1 ? std::to_string(p.split).c_str() : "");
+    t_last_plan = buf;
+  }
+  return t_last_plan.c_str();
+}
 
 int tcg_trace_next(unsigned long long* buf, int max_ctas) {
   if ((buf == nullptr) != (max_ctas == 0) || max_ctas < 0) return TCG_ERR_INVALID;

@@ -282,7 +282,8 @@ int tcg_last_launch_count(void);
 /* How the most recent successful GEMM call on this thread was run (kernel
  * tile, CTA group, clusters, one pass / split-K / stream-K, operand swap), as
  * text for logs and tests; empty if the call queued nothing.  The string is
- * owned by the library and valid until this thread's next GEMM call. */
+ * formatted by this call, owned by the library and valid until this thread's
+ * next tcg_last_plan_string call. */
 const char* tcg_last_plan_string(void);
 
 /* Phase trace of the next GEMM kernel launched by this thread (tracing is off
