@@ -70,6 +70,8 @@ _SIGS = {
     "tcg_probe_ld_shape": ([_vp, _i32, _i32, _i32, _vp, _vp], _i32),
     "tcg_probe_mma_tile": ([_vp, _vp, _i32, _i32, _i32, _vp, _vp], _i32),
     "tcg_probe_mma_tile_ws": ([_vp, _vp, _i32, _i32, _i32, _vp, _vp], _i32),
+    "tcg_probe_mma_tmem_a": ([_vp, _vp, _i32, _i32, _i32, _vp, _vp], _i32),
+    "tcg_probe_mma_ws64": ([_vp, _i32, _vp, _i32, _i32, _i32, _vp, _vp], _i32),
     "tcg_probe_mma_image": ([ctypes.POINTER(ProbeOperand), ctypes.POINTER(ProbeOperand), _i32, _i32, _i32, _vp,
                              _vp], _i32),
     "tcg_probe_ldmatrix_x2": ([_vp, _vp, _vp], _i32),
@@ -262,6 +264,16 @@ def probe_mma_tile(A, B, N, K, is_bf16, D, stream=None):
 def probe_mma_tile_ws(A, B, N, K, is_bf16, D, stream=None):
     return _ok(_lib.tcg_probe_mma_tile_ws(_ptr(A), _ptr(B), N, K, is_bf16, _ptr(D), _stream(stream)),
                "probe_mma_tile_ws")
+
+
+def probe_mma_tmem_a(A, B, N, K, is_bf16, D, stream=None):
+    return _ok(_lib.tcg_probe_mma_tmem_a(_ptr(A), _ptr(B), N, K, is_bf16, _ptr(D), _stream(stream)),
+               "probe_mma_tmem_a")
+
+
+def probe_mma_ws64(A, a_tmem, B, N, K, is_bf16, out, stream=None):
+    return _ok(_lib.tcg_probe_mma_ws64(_ptr(A), a_tmem, _ptr(B), N, K, is_bf16, _ptr(out), _stream(stream)),
+               "probe_mma_ws64")
 
 
 def probe_operand(image, nbytes, major, ldo, sdo, swizzle, starts) -> ProbeOperand:

@@ -10,6 +10,9 @@
 //   * one MMA tile with generic-store swizzled operands ("tcgen05.mma" page,
 //     "four K16 issues" example), dense or with the weight-stationary .ws
 //     opcode ("Weight-stationary and block scaling");
+//   * one MMA tile whose A operand is in tensor memory (Layout D, M = 128);
+//   * a weight-stationary M = 64 tile, A from shared memory or from a
+//     two-bank TMEM image, returning the raw accumulator image;
 //   * MMAs reading operand images the caller laid out, through descriptors
 //     the caller chose (K-major or MN-major, swizzle modes 0..4): the
 //     hardware's descriptor walk against a layout model ("tcgen05.mma" page,
@@ -328,6 +331,182 @@ __global__ void __launch_bounds__(128, 1) probe_mma_tile_kernel(const uint16_t* 
   if (warp == 0) tmem_dealloc<1>(slot, ncols);
 }
 
+// ------------------------------------------------------------------ A operand in TMEM
+
+// One MMA tile whose A operand sits in tensor memory ("tcgen05.mma" page,
+// "Operands and repeat axes": A from shared memory or TMEM, "A in TMEM is
+// packed according to its input format"; M = 128 uses Layout D): thread t
+// writes row t of A (K 16-bit values, two per 32-bit column, the lower K in
+// the low half) to TMEM lane t at columns [A_COL, A_COL + K/2) with
+// tcgen05.st .32x32b; B (N x K, K-major) is written into a 128B-swizzled
+// shared tile as in probe_mma_tile; K/16 MMAs read A from column A_COL + 8j
+// and B through descriptors advancing 32 bytes; D drains with .32x32b.
+constexpr uint32_t TMEM_A_COL = 256;
+
+__global__ void __launch_bounds__(128, 1) probe_mma_tmem_a_kernel(const uint16_t* A, const uint16_t* B, int N, int K,
+                                                                  uint32_t idesc, float* D, unsigned long long* err,
+                                                                  uint64_t timeout_ns) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint32_t slot;
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ uint32_t abort_flag;
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* g = smem_raw + (base - raw);
+  const int warp = threadIdx.x >> 5;
+  const int t = threadIdx.x;
+  for (int i = t; i < 256 * 128 / 4; i += blockDim.x) reinterpret_cast<uint32_t*>(g)[i] = 0u;
+  __syncthreads();
+  for (int i = t; i < N * K; i += blockDim.x) {
+    const int n = i / K, k = i % K;
+    const uint32_t logical = base + (n / 8) * 1024u + (n % 8) * 128u + 2u * k;
+    *reinterpret_cast<uint16_t*>(g + (swizzle_addr(logical, SW_128B) - base)) = B[i];
+  }
+  if (warp == 0) {
+    tmem_alloc<1>(smem_u32(&slot), 512);
+    tmem_relinquish<1>();
+  }
+  if (t == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  // row t of A into lane t: 32 columns hold K <= 64 values
+  uint32_t words[32];
+#pragma unroll
+  for (int c = 0; c < 32; ++c)
+    words[c] = 2 * c < K ? (static_cast<uint32_t>(A[t * K + 2 * c]) | (static_cast<uint32_t>(A[t * K + 2 * c + 1]) << 16))
+                         : 0u;
+  const uint32_t lane_base = slot + (static_cast<uint32_t>(32 * warp) << 16);
+  stx_32x32b_x32(lane_base + TMEM_A_COL, words);
+  tc_wait_st();
+  fence_proxy_async_shared();  // B's generic stores -> the MMA's async reads
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (t == 0) {
+    const uint64_t hi = sdesc_hi(16, 1024, SW_128B);
+    for (int kr = 0; kr < K / 16; ++kr)
+      mma_f16_tmem_a(slot, slot + TMEM_A_COL + 8u * kr, sdesc(base + 32u * kr, hi), idesc, kr > 0);
+    tc_commit<1>(smem_u32(&bar));
+  }
+  const bool ok = warp_wait(smem_u32(&bar), 0, probe_wait_ctx(err, timeout_ns, &abort_flag), SITE_PROBE);
+  tc_fence_after();
+  for (int c = 0; c < N; c += 32) {
+    uint32_t r[32];
+    tmem_ld_32x32b_x32(lane_base + c, r);
+    tc_wait_ld();
+    if (ok) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (c + j < N) D[t * N + c + j] = __uint_as_float(r[j]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc<1>(slot, 512);
+}
+
+// ------------------------------------------------------------------ weight-stationary M = 64
+
+// One weight-stationary MMA tile of M = 64 ("tcgen05.mma" page,
+// "Weight-stationary and block scaling": M64 .ws, N = 64 / 128 / 256, CTA
+// group 1; with A in TMEM "an atom bank axis: A ends in (2,64,K)").  A comes
+// from a 128B-swizzled shared tile (64 rows x K) or, with a_tmem, from tensor
+// memory: thread t writes row t of the (2, 64, K) bank image -- bank t / 64,
+// row t % 64 -- to lane t at columns [TMEM_A_COL, TMEM_A_COL + K/2).  B (N x
+// K, K-major) as in probe_mma_tile.  The raw accumulator image, 128 lanes x
+// N/2 columns, is read back with .32x32b and returned lane-major, so the test
+// can compare it with a layout model.
+__global__ void __launch_bounds__(128, 1) probe_mma_ws64_kernel(const uint16_t* A, const uint16_t* B, int N, int K,
+                                                                int a_tmem, uint32_t idesc, uint32_t* out,
+                                                                unsigned long long* err, uint64_t timeout_ns) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint32_t slot;
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ uint32_t abort_flag;
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* g = smem_raw + (base - raw);
+  const uint32_t a_base = base;              // 64 rows x 128 B (and zero rows after)
+  const uint32_t b_base = base + 128 * 128;  // up to 256 rows x 128 B
+  const int warp = threadIdx.x >> 5;
+  const int t = threadIdx.x;
+  for (int i = t; i < (128 + 256) * 128 / 4; i += blockDim.x) reinterpret_cast<uint32_t*>(g)[i] = 0u;
+  __syncthreads();
+  if (!a_tmem) {
+    for (int i = t; i < 64 * K; i += blockDim.x) {
+      const int m = i / K, k = i % K;
+      const uint32_t logical = a_base + (m / 8) * 1024u + (m % 8) * 128u + 2u * k;
+      *reinterpret_cast<uint16_t*>(g + (swizzle_addr(logical, SW_128B) - base)) = A[i];
+    }
+  }
+  for (int i = t; i < N * K; i += blockDim.x) {
+    const int n = i / K, k = i % K;
+    const uint32_t logical = b_base + (n / 8) * 1024u + (n % 8) * 128u + 2u * k;
+    *reinterpret_cast<uint16_t*>(g + (swizzle_addr(logical, SW_128B) - base)) = B[i];
+  }
+  if (warp == 0) {
+    tmem_alloc<1>(smem_u32(&slot), 512);
+    tmem_relinquish<1>();
+  }
+  if (t == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t lane_base = slot + (static_cast<uint32_t>(32 * warp) << 16);
+  if (a_tmem) {
+    uint32_t words[32];
+#pragma unroll
+    for (int c = 0; c < 32; ++c)
+      words[c] = 2 * c < K
+                     ? (static_cast<uint32_t>(A[t * K + 2 * c]) | (static_cast<uint32_t>(A[t * K + 2 * c + 1]) << 16))
+                     : 0u;
+    stx_32x32b_x32(lane_base + TMEM_A_COL, words);
+    tc_wait_st();
+  }
+  fence_proxy_async_shared();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (t == 0) {
+    const uint64_t hi = sdesc_hi(16, 1024, SW_128B);
+    for (int kr = 0; kr < K / 16; ++kr) {
+      const uint64_t bd = sdesc(b_base + 32u * kr, hi);
+      if (a_tmem)
+        mma_ws_f16_tmem_a(slot, slot + TMEM_A_COL + 8u * kr, bd, idesc, kr > 0);
+      else
+        mma_ws_f16(slot, sdesc(a_base + 32u * kr, hi), bd, idesc, kr > 0);
+    }
+    tc_commit<1>(smem_u32(&bar));
+  }
+  const bool ok = warp_wait(smem_u32(&bar), 0, probe_wait_ctx(err, timeout_ns, &abort_flag), SITE_PROBE);
+  tc_fence_after();
+  const int cols = N / 2;
+  for (int c = 0; c < cols; c += 32) {
+    uint32_t r[32];
+    tmem_ld_32x32b_x32(lane_base + c, r);
+    tc_wait_ld();
+    if (ok) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (c + j < cols) out[t * cols + c + j] = r[j];
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc<1>(slot, 512);
+}
+
 // ------------------------------------------------------------------ MMA from caller images
 
 // One operand of tcg_probe_mma_image as the kernel sees it: where its image
@@ -548,6 +727,37 @@ extern "C" int tcg_probe_mma_tile(const void* A, const void* B, int N, int K, in
   probe_mma_tile_kernel<<<1, 128, smem, as_stream(stream)>>>(static_cast<const uint16_t*>(A),
                                                              static_cast<const uint16_t*>(B), N, K, idesc, 0, D,
                                                              device_error_word(dev), wait_timeout_ns());
+  return finish_launch(1);
+}
+
+extern "C" int tcg_probe_mma_tmem_a(const void* A, const void* B, int N, int K, int is_bf16, float* D, void* stream) {
+  if (!A || !B || !D || N < 16 || N > 256 || N % 16 || K < 16 || K > 64 || K % 16) return TCG_ERR_INVALID;
+  int dev;
+  if (int rc = current_device_checked(&dev)) return rc;
+  const size_t smem = 1024 + 256 * 128;
+  cudaError_t e = cudaFuncSetAttribute(probe_mma_tmem_a_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return record_cuda(e);
+  const uint32_t idesc = idesc_f16(is_bf16 != 0, true, false, false, 128, N);
+  probe_mma_tmem_a_kernel<<<1, 128, smem, as_stream(stream)>>>(static_cast<const uint16_t*>(A),
+                                                               static_cast<const uint16_t*>(B), N, K, idesc, D,
+                                                               device_error_word(dev), wait_timeout_ns());
+  return finish_launch(1);
+}
+
+extern "C" int tcg_probe_mma_ws64(const void* A, int a_tmem, const void* B, int N, int K, int is_bf16, uint32_t* out,
+                                  void* stream) {
+  if (!A || !B || !out || (N != 64 && N != 128 && N != 256) || K < 16 || K > 64 || K % 16) return TCG_ERR_INVALID;
+  int dev;
+  if (int rc = current_device_checked(&dev)) return rc;
+  const size_t smem = 1024 + (128 + 256) * 128;
+  cudaError_t e = cudaFuncSetAttribute(probe_mma_ws64_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return record_cuda(e);
+  const uint32_t idesc = idesc_f16(is_bf16 != 0, true, false, false, 64, N);
+  probe_mma_ws64_kernel<<<1, 128, smem, as_stream(stream)>>>(static_cast<const uint16_t*>(A),
+                                                             static_cast<const uint16_t*>(B), N, K, a_tmem ? 1 : 0,
+                                                             idesc, out, device_error_word(dev), wait_timeout_ns());
   return finish_launch(1);
 }
 

@@ -236,6 +236,35 @@ __device__ __forceinline__ void mma_f16(uint32_t d, uint64_t a, uint64_t b, uint
         : "memory");
 }
 
+// kind::f16 with the A operand in tensor memory (cta_group::1): `a` is the
+// TMEM address of A's first column; B from a shared descriptor.
+__device__ __forceinline__ void mma_f16_tmem_a(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t accum) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+      "r"(a), "l"(b), "r"(idesc), "r"(accum)
+      : "memory");
+}
+
+// Weight-stationary kind::f16 (cta_group::1), A from a shared descriptor or
+// from tensor memory.
+__device__ __forceinline__ void mma_ws_f16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accum) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.ws.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(accum)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_ws_f16_tmem_a(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc,
+                                                  uint32_t accum) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.ws.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+      "r"(a), "l"(b), "r"(idesc), "r"(accum)
+      : "memory");
+}
+
 template <int CG>
 __device__ __forceinline__ void mma_tf32(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accum) {
   if constexpr (CG == 2)

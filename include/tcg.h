@@ -355,6 +355,27 @@ int tcg_probe_mma_tile(const void* A, const void* B, int N, int K, int is_bf16,
  * .ws shapes), K in {16, 32, 48, 64}. */
 int tcg_probe_mma_tile_ws(const void* A, const void* B, int N, int K, int is_bf16, float* D, void* stream);
 
+/* "tcgen05.mma" page, "Operands and repeat axes" (A "Shared or TMEM"; "A in
+ * TMEM is packed according to its input format"; M = 128 uses Layout D): the
+ * tile of tcg_probe_mma_tile with A read from tensor memory.  Thread t writes
+ * row t of A (K f16 / bf16 values, two per 32-bit column, element 2c in the
+ * low half of column c) to TMEM lane t with tcgen05.st .32x32b; K/16 MMAs
+ * kind::f16 (M = 128, N) take A from columns [8j, 8j+8) of that image and B
+ * (N x K, K-major) from a 128B-swizzled shared tile.  N in {16..256} step 16,
+ * K in {16, 32, 48, 64}; D is 128 x N fp32, row-major. */
+int tcg_probe_mma_tmem_a(const void* A, const void* B, int N, int K, int is_bf16, float* D, void* stream);
+
+/* "tcgen05.mma" page, "Weight-stationary and block scaling": one
+ * tcgen05.mma.ws.cta_group::1.kind::f16 tile of M = 64 (N in {64, 128, 256},
+ * K in {16, 32, 48, 64}).  a_tmem = 0: A is 64 x K (row-major f16 / bf16),
+ * written to a 128B-swizzled shared tile.  a_tmem = 1: A is the (2, 64, K)
+ * two-bank image the page gives for M64 .ws with A in TMEM; thread t writes
+ * bank t / 64, row t % 64 to TMEM lane t (two 16-bit values per column).  B is
+ * N x K, K-major.  `out` receives the raw accumulator image: 128 lanes x N/2
+ * fp32 columns, lane-major (out[lane * N/2 + column]). */
+int tcg_probe_mma_ws64(const void* A, int a_tmem, const void* B, int N, int K, int is_bf16, uint32_t* out,
+                       void* stream);
+
 /* "tcgen05.mma" page, "Shared descriptors are byte-stride contracts" and
  * "swizzle=4": MMAs that read operands laid out by the caller.  One operand's
  * shared-memory image and the descriptors that walk it: */

@@ -279,6 +279,23 @@ def layout_b_position(i, j):
     return i + 64 * (j // 64), j % 64
 
 
+def ws64_position(i, j, N: int):
+    """Where a weight-stationary M = 64 MMA leaves accumulator element (i, j)
+    of its 64 x N tile ("tcgen05.mma" page: "M64 .ws uses Layout E", and with
+    A in TMEM "A ends in (2,64,K)"; "splitting an M64 N128 operation into two
+    N64 issues changes each instruction's bank boundary from 64 to 32
+    columns").  READING: the N columns split into two banks at N/2; bank
+    b = j // (N/2) occupies lanes 64b .. 64b+63, so (i, j) sits at lane
+    i + 64*(j // (N/2)), column j % (N/2) -- for N = 128 exactly the page's
+    Layout B -- and a TMEM A operand holds one 64-row copy per bank, bank b
+    in lanes 64b .. 64b+63, feeding that bank's columns.
+    Returns (lane, column)."""
+    i = np.asarray(i)
+    j = np.asarray(j)
+    half = N // 2
+    return i + 64 * (j // half), j % half
+
+
 # ---------------------------------------------------------------------------
 # ldmatrix / stmatrix m8n8.b16 ("ldmatrix / stmatrix" page, "Address providers
 # and result owners", "Transpose and stores").

@@ -299,3 +299,58 @@ def test_mma_reads_oracle_layout_model(tcg, oracle_mod, case):
         bad = np.argwhere(got != ref)[:6]
         raise AssertionError(f"{case.name}: {int((got != ref).sum())} mismatches, first {bad.tolist()}: "
                              f"got {[got[tuple(i)] for i in bad]} ref {[ref[tuple(i)] for i in bad]}")
+
+
+@pytest.mark.parametrize("N,K,bf16", [(128, 64, 0), (256, 64, 1), (64, 16, 0), (48, 32, 1)])
+def test_mma_with_a_in_tmem(tcg, oracle_mod, N, K, bf16):
+    """A written to tensor memory (Layout D: row m in lane m, two 16-bit values
+    per column) and read by the MMA from there; quarter-integer inputs make
+    every sum exact, so the product equals the oracle's bit for bit."""
+    import synthetic as syn
+    rng = np.random.default_rng(3 * N + K + bf16)
+    a = rng.integers(-4, 5, (128, K)) / 4.0
+    b = rng.integers(-4, 5, (N, K)) / 4.0
+    dt = "bf16" if bf16 else "f16"
+    ab, bb = syn.to_bits(a, dt), syn.to_bits(b, dt)
+    D = torch.full((128, N), float("nan"), dtype=torch.float32, device="cuda")
+    tcg.probe_mma_tmem_a(torch.from_numpy(ab.view(np.int16)).cuda(), torch.from_numpy(bb.view(np.int16)).cuda(),
+                         N, K, bf16, D)
+    assert tcg.check() == 0
+    ref, _ = oracle_mod.gemm(128, N, K, ab, 2 if bf16 else 1, 0, K, bb, 2 if bf16 else 1, 0, K)
+    assert np.array_equal(D.cpu().numpy().astype(np.float64), ref)
+
+
+@pytest.mark.parametrize("N,K,bf16", [(64, 32, 0), (128, 64, 1), (256, 16, 0)])
+@pytest.mark.parametrize("a_tmem", [0, 1])
+def test_ws64_accumulator_and_tmem_a_banks(tcg, oracle_mod, N, K, bf16, a_tmem):
+    """M = 64 weight-stationary tile: the raw 128-lane x N/2-column
+    accumulator image equals the oracle product placed by the layout model
+    (columns split into two banks at N/2).  With A in TMEM the two banks hold
+    different A rows, so each bank's columns must come from its own bank."""
+    import synthetic as syn
+    rng = np.random.default_rng(7 * N + K + 2 * a_tmem + bf16)
+    dt = "bf16" if bf16 else "f16"
+    banks = rng.integers(-4, 5, (2, 64, K)) / 4.0
+    if not a_tmem:
+        banks[1] = banks[0]   # one A from shared memory serves both banks
+    b = rng.integers(-4, 5, (N, K)) / 4.0
+    ab = syn.to_bits(banks.reshape(128, K), dt)
+    bb = syn.to_bits(b, dt)
+    a_in = ab if a_tmem else ab[:64]
+    out = torch.zeros((128, N // 2), dtype=torch.int32, device="cuda")
+    tcg.probe_mma_ws64(torch.from_numpy(np.ascontiguousarray(a_in).view(np.int16)).cuda(), a_tmem,
+                       torch.from_numpy(bb.view(np.int16)).cuda(), N, K, bf16, out)
+    assert tcg.check() == 0
+    got = out.cpu().numpy().view(np.float32).astype(np.float64)
+    t = 2 if bf16 else 1
+    expect = np.full((128, N // 2), np.nan)
+    half = N // 2
+    for bank in range(2):
+        ref, _ = oracle_mod.gemm(64, N, K, ab[64 * bank:64 * bank + 64], t, 0, K, bb, t, 0, K)
+        i, j = np.meshgrid(np.arange(64), np.arange(bank * half, bank * half + half), indexing="ij")
+        lane, col = L.ws64_position(i, j, N)
+        expect[lane, col] = ref[i, j]
+    if not np.array_equal(got, expect):
+        bad = np.argwhere(got != expect)[:6]
+        raise AssertionError(f"{int((got != expect).sum())} cells differ; first {bad.tolist()}: "
+                             f"got {[got[tuple(x)] for x in bad]} expect {[expect[tuple(x)] for x in bad]}")

@@ -396,3 +396,14 @@ def test_gpu_cp_probe_cases_obey_the_walk_rules():
     words = {0: 8, 1: 4, 2: 4, 3: 8}
     for shape, origin, ldo, sdo, sw, nwords in g.CP_CASES + g.DECOMP_CASES:
         L.check_walk(origin, rows[shape % 4], words[shape % 4], ldo, sdo, sw, base=0, backing=4 * nwords)
+
+
+@pytest.mark.parametrize("N", [64, 128, 256])
+def test_ws64_layout_is_a_bijection_and_is_layout_b_at_n128(N):
+    i, j = np.meshgrid(np.arange(64), np.arange(N), indexing="ij")
+    lane, col = L.ws64_position(i, j, N)
+    cells = lane * (N // 2) + col
+    assert np.array_equal(np.sort(cells.ravel()), np.arange(64 * N))   # 128 lanes x N/2 columns, once each
+    if N == 128:  # the "tcgen05.ld / tcgen05.st" page's Layout B formula
+        lb, cb = L.layout_b_position(i, j)
+        assert np.array_equal(lane, lb) and np.array_equal(col, cb)
