@@ -6,7 +6,8 @@ tcgen05.ld epilogue), inputs already resident in HBM.  Default workload: bf16
 M=N=K=8192 with CTA pairs (cta_group::2, 256x256 pair tiles), fp32
 accumulation, bf16 output.  The other workloads -- block-scaled MXFP8
 8192^3, bf16 4096^3 (A K-major, B MN-major, single CTAs), tf32 2048 x 2048 x
-8192, f16-in / f16-accumulate 8192^3 and the HBM-bound 16 x 8192 x 8192 --
+8192, f16-in / f16-accumulate 8192^3, block-scaled FP6 / MXFP4 / NVFP4 8192^3
+and the HBM-bound 16 x 8192 x 8192 --
 are measured the same way and reported under "secondary", and a ~1.5 s
 back-to-back pass of the headline ("sustained") is compared with the
 sustained cuBLAS figure, with the SM clock seen in that window.
@@ -43,21 +44,20 @@ import synthetic as syn  # noqa: E402
 
 METRIC = "GEMM TFLOP/s at 1 GB300 and % of dtype dense tensor peak (bf16/mxf8 8192^3)"
 UNIT = "TFLOP/s"
-IN_TYPE = {"f16": 0, "bf16": 1, "tf32": 2, "e4m3": 3, "e5m2": 4, "e3m2": 5, "e2m3": 6, "e2m1": 7}
+IN_TYPE = {"f16": 0, "bf16": 1, "tf32": 2, "e4m3": 3, "e5m2": 4, "e3m2": 5, "e2m3": 6, "e2m1": 7, "nvf4": 8}
 OUT = {"f32": 0, "f16": 1, "bf16": 2}
 ACC = {"f32": 0, "f16": 1}
-ESIZE = {"f16": 2, "bf16": 2, "tf32": 4, "e4m3": 1, "e5m2": 1, "e3m2": 0.75, "e2m3": 0.75, "e2m1": 0.5}
+ESIZE = {"f16": 2, "bf16": 2, "tf32": 4, "e4m3": 1, "e5m2": 1, "e3m2": 0.75, "e2m3": 0.75, "e2m1": 0.5, "nvf4": 0.5}
 # nominal dense tensor rate relative to bf16 (NVIDIA GB300 figures: tf32 1.1,
-# bf16/fp16 2.25, fp8 4.5 PFLOP/s).  FP6 and FP4 elements on the MMA kind
-# used here (kind::mxf8f6f4, one byte of shared memory per element) run at the
-# FP8 rate; the datasheet's 13.5 PFLOP/s FP4 figure is that of the packed
-# FP4 kinds.
+# bf16/fp16 2.25, fp8 4.5, fp4 13.5 PFLOP/s).  FP6 elements run on the FP8
+# kind (kind::mxf8f6f4, one byte of shared memory per element) at the FP8
+# rate; FP4 (MXFP4, NVFP4) on the packed FP4 kinds at the FP4 rate.
 NOMINAL_RATIO = {"bf16": 1.0, "f16": 1.0, "tf32": 1.1 / 2.25, "e4m3": 2.0, "e5m2": 2.0, "e3m2": 2.0, "e2m3": 2.0,
-                 "e2m1": 2.0}
+                 "e2m1": 6.0, "nvf4": 6.0}
 # NVIDIA's dense (no 2:4 sparsity) GB300 datasheet rates, TFLOP/s, for the
 # MMA kind each format runs on
 DATASHEET_DENSE_TFLOPS = {"bf16": 2250.0, "f16": 2250.0, "tf32": 1100.0, "e4m3": 4500.0, "e5m2": 4500.0,
-                          "e3m2": 4500.0, "e2m3": 4500.0, "e2m1": 4500.0}
+                          "e3m2": 4500.0, "e2m3": 4500.0, "e2m1": 13500.0, "nvf4": 13500.0}
 PROFILE_DIR = os.path.join(ROOT, "profiles")
 KERNEL_SOURCES = ["gemm_kernel.cuh", "ptx.cuh", "desc.cuh", "gemm_f16.cu", "gemm_tf32.cu", "gemm_mxf8.cu", "api.cu",
                   "splitk_reduce.cu"]
@@ -186,9 +186,10 @@ def run_workload(tcg, torch, w, steps, warmup, dist_ctx, measure_e2e=True):
     if scaled:
         SFA = to_dev(x["SFA"], torch)
         SFB = to_dev(x["SFB"], torch)
+        fmt = IN_TYPE[w.dtype]
         tn = tcg.mxf8_tile_n(M, N, K, b_maj, w.cta_group)
-        ia = torch.empty(tcg.mxf8_scale_image_bytes(M, K, 128), dtype=torch.uint8, device="cuda")
-        ib = torch.empty(tcg.mxf8_scale_image_bytes(N, K, tn), dtype=torch.uint8, device="cuda")
+        ia = torch.empty(tcg.scale_image_bytes(fmt, M, K, 128), dtype=torch.uint8, device="cuda")
+        ib = torch.empty(tcg.scale_image_bytes(fmt, N, K, tn), dtype=torch.uint8, device="cuda")
 
     launches = [0]
     # Inputs of HBM-bound (skinny) workloads are not much larger than the
@@ -201,7 +202,7 @@ def run_workload(tcg, torch, w, steps, warmup, dist_ctx, measure_e2e=True):
         if flush is not None:
             flush.zero_()
         if scaled:
-            tcg.mxf8_prepare_scales_ab(SFA, M, ia, SFB, N, tn, ib, K, stream=sp)
+            tcg.prepare_scales_ab(fmt, SFA, M, ia, SFB, N, tn, ib, K, stream=sp)
             n += 1
             if ev_pair:
                 ev_pair[0].record(stream)
@@ -291,6 +292,9 @@ def run_workload(tcg, torch, w, steps, warmup, dist_ctx, measure_e2e=True):
             elif scaled and w.dtype == "e2m1":
                 tcg.gemm_mxf4_blockscaled(M, N, K, dA[bi], a_maj, x["lda"], dB[bi], b_maj, x["ldb"], dSFA[bi],
                                           dSFB[bi], dD[bi], OUT[w.out], N, ACC[w.acc], stream=cs)
+            elif scaled and w.dtype == "nvf4":
+                tcg.gemm_nvf4_blockscaled(M, N, K, dA[bi], a_maj, x["lda"], dB[bi], b_maj, x["ldb"], dSFA[bi],
+                                          dSFB[bi], dD[bi], OUT[w.out], N, ACC[w.acc], stream=cs)
             elif scaled and w.dtype in ("e3m2", "e2m3"):
                 tcg.gemm_mxf6_blockscaled(IN_TYPE[w.dtype], M, N, K, dA[bi], a_maj, x["lda"], dB[bi], b_maj,
                                           x["ldb"], dSFA[bi], dSFB[bi], dD[bi], OUT[w.out], N, ACC[w.acc], stream=cs)
@@ -377,12 +381,14 @@ def oracle_sample(w, x, rows_n: int):
     workload (inputs `x` already generated); returns (TFLOP/s, seconds, threads)."""
     import oracle
     t = {"f16": oracle.F16, "bf16": oracle.BF16, "tf32": oracle.F32, "e4m3": oracle.E4M3, "e5m2": oracle.E5M2,
-         "e3m2": oracle.E3M2, "e2m3": oracle.E2M3, "e2m1": oracle.E2M1}[w.dtype]
+         "e3m2": oracle.E3M2, "e2m3": oracle.E2M3, "e2m1": oracle.E2M1, "nvf4": oracle.E2M1}[w.dtype]
+    nv = w.dtype == "nvf4"
     rows = np.linspace(0, w.M - 1, rows_n).astype(np.int64)
     threads = oracle.num_threads()
     t0 = time.perf_counter()
     oracle.gemm(w.M, w.N, w.K, x["A"], t, 0 if w.a_major == "k" else 1, x["lda"], x["B"], t,
-                0 if w.b_major == "k" else 1, x["ldb"], SFA=x["SFA"], SFB=x["SFB"], rows=rows, nthreads=threads)
+                0 if w.b_major == "k" else 1, x["ldb"], SFA=x["SFA"], SFB=x["SFB"], rows=rows, nthreads=threads,
+                sf_block=16 if nv else 32, sf_kind=oracle.SF_UE4M3 if nv else oracle.SF_E8M0)
     dt = time.perf_counter() - t0
     return 2.0 * rows_n * w.N * w.K / dt / 1e12, dt, threads
 
@@ -444,7 +450,7 @@ def main():
     ap.add_argument("--workload", default="bf16_8192_cta2", choices=sorted(syn.WORKLOADS))
     ap.add_argument("--secondary",
                     default="mxf8_8192,bf16_skinny_m16,bf16_4096_kmn_cta1,tf32_2048x2048x8192,f16acc_8192_cta2,"
-                            "mxf6_e2m3_8192,mxf4_8192",
+                            "mxf6_e2m3_8192,mxf4_8192,nvf4_8192",
                     help="comma list of extra workloads ('' for none)")
     ap.add_argument("--sustained-s", type=float, default=1.5,
                     help="length of the back-to-back sustained pass of the headline workload (0: skip)")

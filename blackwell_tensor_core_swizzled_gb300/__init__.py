@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_HERE, "libtcg.so")
 OK, ERR_INVALID, ERR_ALIGNMENT, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_NO_DEVICE = 0, -1, -2, -3, -4, -5, -6
 K_MAJOR, MN_MAJOR = 0, 1
 F32, F16, BF16 = 0, 1, 2
-IN_F16, IN_BF16, IN_TF32, IN_E4M3, IN_E5M2, IN_E3M2, IN_E2M3, IN_E2M1 = 0, 1, 2, 3, 4, 5, 6, 7
+IN_F16, IN_BF16, IN_TF32, IN_E4M3, IN_E5M2, IN_E3M2, IN_E2M3, IN_E2M1, IN_NVF4 = 0, 1, 2, 3, 4, 5, 6, 7, 8
 
 _i64, _i32, _u32, _u64, _vp = ctypes.c_int64, ctypes.c_int, ctypes.c_uint32, ctypes.c_uint64, ctypes.c_void_p
 
@@ -53,6 +53,10 @@ _SIGS = {
                                    _i64, _i32, _vp], _i32),
     "tcg_gemm_mxf4_blockscaled": ([_i64, _i64, _i64, _vp, _i32, _i64, _vp, _i32, _i64, _vp, _vp, _vp, _i32,
                                    _i64, _i32, _vp], _i32),
+    "tcg_gemm_nvf4_blockscaled": ([_i64, _i64, _i64, _vp, _i32, _i64, _vp, _i32, _i64, _vp, _vp, _vp, _i32,
+                                   _i64, _i32, _vp], _i32),
+    "tcg_scale_image_bytes": ([_i32, _i64, _i64, _i32], _i64),
+    "tcg_prepare_scales_ab": ([_i32, _vp, _i64, _vp, _vp, _i64, _i32, _vp, _i64, _vp], _i32),
     "tcg_gemm": ([ctypes.POINTER(GemmArgs), _vp], _i32),
     "tcg_mxf8_scale_image_bytes": ([_i64, _i64, _i32], _i64),
     "tcg_mxf8_tile_n": ([_i64, _i64, _i64, _i32, _i32], _i32),
@@ -170,10 +174,27 @@ def gemm_mxf6_blockscaled(fmt, M, N, K, A, a_major, lda, B, b_major, ldb, SFA, S
 
 def gemm_mxf4_blockscaled(M, N, K, A, a_major, lda, B, b_major, ldb, SFA, SFB, D, d_type, ldd, acc_type=F32,
                           stream=None):
-    """Block-scaled FP4 (E2M1) GEMM (A and B packed, see tcg.h)."""
+    """MXFP4 GEMM: packed E2M1, e8m0 scales per 32 K elements (see tcg.h)."""
     return _ok(_lib.tcg_gemm_mxf4_blockscaled(M, N, K, _ptr(A), a_major, lda, _ptr(B), b_major, ldb, _ptr(SFA),
                                               _ptr(SFB), _ptr(D), d_type, ldd, acc_type, _stream(stream)),
                "gemm_mxf4_blockscaled")
+
+
+def gemm_nvf4_blockscaled(M, N, K, A, a_major, lda, B, b_major, ldb, SFA, SFB, D, d_type, ldd, acc_type=F32,
+                          stream=None):
+    """NVFP4 GEMM: packed E2M1, unsigned E4M3 scales per 16 K elements (see tcg.h)."""
+    return _ok(_lib.tcg_gemm_nvf4_blockscaled(M, N, K, _ptr(A), a_major, lda, _ptr(B), b_major, ldb, _ptr(SFA),
+                                              _ptr(SFB), _ptr(D), d_type, ldd, acc_type, _stream(stream)),
+               "gemm_nvf4_blockscaled")
+
+
+def scale_image_bytes(fmt, rows, K, tile_rows) -> int:
+    return _lib.tcg_scale_image_bytes(fmt, rows, K, tile_rows)
+
+
+def prepare_scales_ab(fmt, SFA, M, SFA_img, SFB, N, tile_n, SFB_img, K, stream=None):
+    return _ok(_lib.tcg_prepare_scales_ab(fmt, _ptr(SFA), M, _ptr(SFA_img), _ptr(SFB), N, tile_n, _ptr(SFB_img), K,
+                                          _stream(stream)), "prepare_scales_ab")
 
 
 def gemm_mxf8_blockscaled_noalloc(M, N, K, A, a_major, lda, B, b_major, ldb, SFA, SFB, D, d_type, ldd,

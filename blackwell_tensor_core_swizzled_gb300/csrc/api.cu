@@ -235,24 +235,34 @@ int make_map_3d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int 
   return TCG_OK;
 }
 
-// Block-scaled formats (kind::mxf8f6f4): E4M3 / E5M2 bytes, E3M2 / E2M3 /
-// E2M1 packed in global memory.  Each element takes one byte of shared memory
-// (TMA expands the packed ones into 16-byte blocks of sixteen values and
-// padding, the layout the "tcgen05.cp" page's FP4 / FP6 shapes describe).
+// Block-scaled formats.  E4M3 / E5M2 bytes and the FP6 formats (packed in
+// global memory) run on kind::mxf8f6f4 with one byte of shared memory per
+// element (TMA expands FP6 into 16-byte blocks of sixteen values and padding,
+// the layout the "tcgen05.cp" page's FP4 / FP6 shapes describe).  FP4 (E2M1
+// with e8m0 scales per 32, or the NVFP4 form with unsigned E4M3 scales per 16)
+// stays packed, two values per byte, on kind::mxf4 / kind::mxf4nvf4.
 bool is_mx(tcg_input t) {
-  return t == TCG_IN_E4M3 || t == TCG_IN_E5M2 || t == TCG_IN_E3M2 || t == TCG_IN_E2M3 || t == TCG_IN_E2M1;
+  return t == TCG_IN_E4M3 || t == TCG_IN_E5M2 || t == TCG_IN_E3M2 || t == TCG_IN_E2M3 || t == TCG_IN_E2M1 ||
+         t == TCG_IN_NVF4;
 }
-bool is_packed(tcg_input t) { return t == TCG_IN_E3M2 || t == TCG_IN_E2M3 || t == TCG_IN_E2M1; }
+bool is_fp6(tcg_input t) { return t == TCG_IN_E3M2 || t == TCG_IN_E2M3; }
+bool is_fp4(tcg_input t) { return t == TCG_IN_E2M1 || t == TCG_IN_NVF4; }
+bool is_packed(tcg_input t) { return is_fp6(t) || is_fp4(t); }
 int bits_of(tcg_input t) {
-  return t == TCG_IN_TF32 ? 32 : t == TCG_IN_E2M1 ? 4 : (t == TCG_IN_E3M2 || t == TCG_IN_E2M3) ? 6 : is_mx(t) ? 8 : 16;
+  return t == TCG_IN_TF32 ? 32 : is_fp4(t) ? 4 : is_fp6(t) ? 6 : is_mx(t) ? 8 : 16;
 }
-// bytes per element in shared memory (and in global memory for unpacked types)
+// bytes per element in shared memory (and in global memory for unpacked
+// types); packed FP4 is half a byte and handled by its own branches
 int esize_of(tcg_input t) { return t == TCG_IN_TF32 ? 4 : is_mx(t) ? 1 : 2; }
+// K elements per ring stage: one 128-byte shared row (packed FP4: 256)
+int stage_k(tcg_input t) { return is_fp4(t) ? 256 : 128 / esize_of(t); }
 // global bytes of `ld` elements
 int64_t row_bytes(tcg_input t, int64_t ld) { return ld * bits_of(t) / 8; }
+// bytes TMA writes per operand row per stage: the packed FP6 types write only
+// their data bytes (96 per 128 elements) and skip the padding of each block
+int stage_row_tx(tcg_input t) { return is_fp6(t) ? 96 : 128; }
 uint32_t mx_format(tcg_input t) {
-  return t == TCG_IN_E5M2 ? MXF_E5M2 : t == TCG_IN_E3M2 ? MXF_E3M2 : t == TCG_IN_E2M3 ? MXF_E2M3
-         : t == TCG_IN_E2M1 ? MXF_E2M1 : MXF_E4M3;
+  return t == TCG_IN_E5M2 ? MXF_E5M2 : t == TCG_IN_E3M2 ? MXF_E3M2 : t == TCG_IN_E2M3 ? MXF_E2M3 : MXF_E4M3;
 }
 int dsize_of(tcg_dtype t) { return t == TCG_F32 ? 4 : 2; }
 
@@ -265,10 +275,16 @@ int check_operand(const void* ptr, tcg_major major, int64_t mn, int64_t K, int64
   if (*ld == 0) *ld = inner;
   if (*ld < inner || *ld < 1) return TCG_ERR_INVALID;
   if (!ptr) return TCG_ERR_INVALID;
-  if (is_packed(t)) {
+  if (is_fp6(t)) {
     if (major != TCG_K_MAJOR) return TCG_ERR_UNSUPPORTED;
     if (K % 128 || (*ld * bits_of(t)) % 8) return TCG_ERR_ALIGNMENT;
     if (reinterpret_cast<uintptr_t>(ptr) % 32 || row_bytes(t, *ld) % 32) return TCG_ERR_ALIGNMENT;
+    return TCG_OK;
+  }
+  if (is_fp4(t)) {  // packed bytes: 16-byte aligned rows of K/2 bytes
+    if (major != TCG_K_MAJOR) return TCG_ERR_UNSUPPORTED;
+    if (K % 32 || *ld % 32) return TCG_ERR_ALIGNMENT;
+    if (reinterpret_cast<uintptr_t>(ptr) % 16) return TCG_ERR_ALIGNMENT;
     return TCG_OK;
   }
   if (reinterpret_cast<uintptr_t>(ptr) % 16) return TCG_ERR_ALIGNMENT;
@@ -311,8 +327,9 @@ int get_plan(const tcg_gemm_args& a, Plan* plan) {
     case TCG_IN_E4M3:
     case TCG_IN_E5M2:
     case TCG_IN_E3M2:
-    case TCG_IN_E2M3:
-    case TCG_IN_E2M1: plan->ki = kinfo_mxf8(cg); break;
+    case TCG_IN_E2M3: plan->ki = kinfo_mxf8(cg); break;
+    case TCG_IN_E2M1: plan->ki = kinfo_fp4(cg, false); break;
+    case TCG_IN_NVF4: plan->ki = kinfo_fp4(cg, true); break;
     default: return TCG_ERR_INVALID;
   }
   // an MN-major B half tile must be whole 128-byte swizzle spans
@@ -420,11 +437,6 @@ int launch_gemm(const KernelInfo& ki, const GemmParams& prm, int clusters, cudaS
   return TCG_OK;
 }
 
-int64_t sf_image_bytes(int64_t rows, int64_t K, int tile_rows) {
-  const int64_t ksteps = cdiv(cdiv(K, 32), 4);
-  return ksteps * cdiv(rows, tile_rows) * cdiv(tile_rows, 128) * 512;
-}
-
 int workspace(int dev, cudaStream_t s, size_t bytes, void** out) {
   std::lock_guard<std::mutex> lk(g_mu);
   Workspace& w = g_ws[std::make_pair(dev, s)];
@@ -472,9 +484,8 @@ CUtensorMapDataType map_dtype(tcg_input t) {
     case TCG_IN_F16: return CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     case TCG_IN_BF16: return CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     case TCG_IN_TF32: return CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
-    // sixteen packed values per 16-byte block in shared memory (8 or 12 data
+    // sixteen packed values per 16-byte block in shared memory (12 data
     // bytes, then padding)
-    case TCG_IN_E2M1: return CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B;
     case TCG_IN_E3M2:
     case TCG_IN_E2M3: return CU_TENSOR_MAP_DATA_TYPE_16U6_ALIGN16B;
     default: return CU_TENSOR_MAP_DATA_TYPE_UINT8;
@@ -487,8 +498,8 @@ int setup_operand(const void* ptr, tcg_input it, tcg_major major, int64_t mn, in
                   CUtensorMap* map, int* mn_major, int* boxes, int* box_mn, uint32_t* box_bytes, uint64_t* desc_hi,
                   uint32_t* kstep) {
   const int es = esize_of(it);
-  const int bk = 128 / es;  // K elements per stage
-  const int mma_k = it == TCG_IN_TF32 ? 8 : is_mx(it) ? 32 : 16;
+  const int bk = stage_k(it);  // K elements per stage
+  const int mma_k = it == TCG_IN_TF32 ? 8 : is_fp4(it) ? 64 : is_mx(it) ? 32 : 16;
   const CUtensorMapDataType dt = map_dtype(it);
   if (major == TCG_K_MAJOR) {
     // rows enumerate M/N: one 128-byte swizzle row per M/N row, 8-row groups
@@ -498,11 +509,15 @@ int setup_operand(const void* ptr, tcg_input it, tcg_major major, int64_t mn, in
     *box_mn = 0;
     *box_bytes = static_cast<uint32_t>(rows) * 128u;
     *desc_hi = sdesc_hi(16, 1024, SW_128B);
-    *kstep = static_cast<uint32_t>(mma_k * es);
-    // the map's row stride is the global one (packed formats: ld * bits / 8)
-    return make_map_2d(map, ptr, dt, 1, static_cast<uint64_t>(K), static_cast<uint64_t>(mn),
-                       static_cast<uint64_t>(row_bytes(it, ld)), static_cast<uint32_t>(bk), static_cast<uint32_t>(rows),
-                       CU_TENSOR_MAP_SWIZZLE_128B);
+    // shared bytes of K per MMA issue: 32 (FP6 takes one padded byte per
+    // element there; packed FP4 half a byte)
+    *kstep = static_cast<uint32_t>(is_fp4(it) ? mma_k / 2 : mma_k * es);
+    // the map's row stride is the global one (packed formats: ld * bits / 8);
+    // packed FP4 is mapped as bytes (128-byte boxes of 256 values)
+    const uint64_t inner = is_fp4(it) ? static_cast<uint64_t>(row_bytes(it, K)) : static_cast<uint64_t>(K);
+    const uint32_t box_inner = is_fp4(it) ? 128u : static_cast<uint32_t>(bk);
+    return make_map_2d(map, ptr, dt, 1, inner, static_cast<uint64_t>(mn), static_cast<uint64_t>(row_bytes(it, ld)),
+                       box_inner, static_cast<uint32_t>(rows), CU_TENSOR_MAP_SWIZZLE_128B);
   }
   // MN-major: rows enumerate K; one 128-byte row holds 128/es M/N elements.
   *mn_major = 1;
@@ -530,7 +545,9 @@ int run_gemm(const tcg_gemm_args* args, cudaStream_t s) {
   if (!args) return TCG_ERR_INVALID;
   tcg_gemm_args a = *args;
   if (a.M < 0 || a.N < 0 || a.K < 0) return TCG_ERR_INVALID;
-  if (a.in_type < TCG_IN_F16 || a.in_type > TCG_IN_E2M1) return TCG_ERR_INVALID;
+  if (a.in_type < TCG_IN_F16 || a.in_type > TCG_IN_NVF4) return TCG_ERR_INVALID;
+  // the packed-FP4 kinds stage their scales from the MMA thread only
+  if (is_fp4(a.in_type) && a.sf_staging != 0 && a.sf_staging != 2) return TCG_ERR_UNSUPPORTED;
   if (a.d_type < TCG_F32 || a.d_type > TCG_BF16 || a.acc_type < TCG_F32 || a.acc_type > TCG_BF16)
     return TCG_ERR_INVALID;
   if (a.acc_type == TCG_BF16) return TCG_ERR_UNSUPPORTED;
@@ -602,8 +619,7 @@ int run_gemm(const tcg_gemm_args* args, cudaStream_t s) {
   prm.K = static_cast<int>(a.K);
   prm.num_m_tiles = static_cast<int>(cdiv(a.M, 128 * cg));
   prm.num_n_tiles = static_cast<int>(cdiv(a.N, bn));
-  const int es = esize_of(a.in_type);
-  prm.num_k_blocks = static_cast<int>(cdiv(a.K * es, 128));
+  prm.num_k_blocks = static_cast<int>(cdiv(a.K, stage_k(a.in_type)));
   // tile, unit and slot indices are 32-bit in the kernels
   if (static_cast<int64_t>(prm.num_m_tiles) * prm.num_n_tiles > INT32_MAX / 4) {
     t_last_error = "too many output tiles";
@@ -621,14 +637,15 @@ int run_gemm(const tcg_gemm_args* args, cudaStream_t s) {
   // bytes TMA writes per stage: 128 elements of K per row; the packed 6- and
   // 4-bit types write only their data bytes (96 / 64 per row) and skip the
   // padding of each 16-byte block
-  const int row_tx = static_cast<int>(row_bytes(a.in_type, 128 / esize_of(a.in_type)));
-  prm.ab_tx_bytes = static_cast<uint32_t>((a_rows + bn / cg) * row_tx * cg);
+  prm.ab_tx_bytes = static_cast<uint32_t>((a_rows + bn / cg) * stage_row_tx(a.in_type) * cg);
   if (int rc = setup_operand(a.B, a.in_type, a.b_major, a.N, a.K, a.ldb, bn / cg, &prm.tmap_b, &prm.b_mn_major,
                              &prm.b_boxes, &prm.b_box_mn, &prm.b_box_bytes, &prm.b_desc_hi, &prm.b_kstep))
     return rc;
   const bool a_mn = a.a_major == TCG_MN_MAJOR, b_mn = a.b_major == TCG_MN_MAJOR;
   if (a.in_type == TCG_IN_TF32)
     prm.idesc = idesc_tf32(a_mn, b_mn, 128 * cg, bn);
+  else if (is_fp4(a.in_type))
+    prm.idesc = idesc_fp4(128 * cg, bn, a.in_type == TCG_IN_E2M1);
   else if (scaled)
     prm.idesc = idesc_mxf8(a_mn, b_mn, 128 * cg, bn, mx_format(a.in_type), mx_format(a.in_type));
   else
@@ -671,29 +688,31 @@ int run_gemm(const tcg_gemm_args* args, cudaStream_t s) {
   if (scaled) {
     const int sfa_tiles = static_cast<int>(cdiv(a.M, 128));
     const int chunks = static_cast<int>(cdiv(bn, 128));
-    const int64_t ksteps = cdiv(cdiv(a.K, 32), 4);
+    const int kch = scale_format(a.in_type).kch;  // 512-byte chunks per 128 rows per stage
+    const int64_t ba = sf_image_bytes_fmt(a.in_type, a.M, a.K, 128);
+    const int64_t bb = sf_image_bytes_fmt(a.in_type, a.N, a.K, bn);
     const uint8_t* sfa_img = a.SFA_img;
     const uint8_t* sfb_img = a.SFB_img;
     if (!sfa_img) {
-      const size_t ba = static_cast<size_t>(sf_image_bytes(a.M, a.K, 128));
-      const size_t bb = static_cast<size_t>(sf_image_bytes(a.N, a.K, bn));
       void* ws = nullptr;
-      if (int rc = workspace(dev, s, ba + bb, &ws)) return rc;
+      if (int rc = workspace(dev, s, static_cast<size_t>(ba + bb), &ws)) return rc;
       uint8_t* wa = static_cast<uint8_t*>(ws);
       uint8_t* wb = wa + ba;  // ba is a multiple of 512
-      const cudaError_t e = launch_sf_prepare_pair(a.SFA, a.M, 128, wa, a.SFB, a.N, bn, wb, a.K, s);
+      const cudaError_t e = launch_sf_prepare_pair(a.in_type, a.SFA, a.M, 128, wa, a.SFB, a.N, bn, wb, a.K, s);
       if (e != cudaSuccess) return record_cuda(e);
       launches += 1;
       sfa_img = wa;
       sfb_img = wb;
     }
     prm.sf_a_tiles = sfa_tiles;
+    // one 512-byte chunk (128 words) per map row; a stage loads its kch
+    // (SFA) or kch x chunks (SFB) consecutive rows in one box
     if (int rc = make_map_2d(&prm.tmap_sfa, sfa_img, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, 128,
-                             static_cast<uint64_t>(ksteps * sfa_tiles), 128, 128, 1, CU_TENSOR_MAP_SWIZZLE_NONE))
+                             static_cast<uint64_t>(ba / 512), 128, 128, static_cast<uint32_t>(kch),
+                             CU_TENSOR_MAP_SWIZZLE_NONE))
       return rc;
-    if (int rc = make_map_2d(&prm.tmap_sfb, sfb_img, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4,
-                             static_cast<uint64_t>(128 * chunks), static_cast<uint64_t>(ksteps * prm.num_n_tiles),
-                             static_cast<uint64_t>(128 * chunks), static_cast<uint32_t>(128 * chunks), 1,
+    if (int rc = make_map_2d(&prm.tmap_sfb, sfb_img, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, 128,
+                             static_cast<uint64_t>(bb / 512), 128, 128, static_cast<uint32_t>(kch * chunks),
                              CU_TENSOR_MAP_SWIZZLE_NONE))
       return rc;
   }
@@ -907,9 +926,36 @@ int tcg_gemm_mxf4_blockscaled(int64_t M, int64_t N, int64_t K, const void* A, tc
                     stream);
 }
 
+int tcg_gemm_nvf4_blockscaled(int64_t M, int64_t N, int64_t K, const void* A, tcg_major a_major, int64_t lda,
+                              const void* B, tcg_major b_major, int64_t ldb, const uint8_t* SFA,
+                              const uint8_t* SFB, void* D, tcg_dtype d_type, int64_t ldd, tcg_dtype acc_type,
+                              void* stream) {
+  if (K > 0 && (!SFA || !SFB)) return TCG_ERR_INVALID;
+  return named_gemm(TCG_IN_NVF4, M, N, K, A, a_major, lda, B, b_major, ldb, SFA, SFB, D, d_type, ldd, acc_type,
+                    stream);
+}
+
+int64_t tcg_scale_image_bytes(tcg_input fmt, int64_t rows, int64_t K, int tile_rows) {
+  if (rows < 0 || K < 0 || tile_rows <= 0 || !is_mx(fmt)) return -1;
+  return sf_image_bytes_fmt(fmt, rows, K, tile_rows);
+}
+
+int tcg_prepare_scales_ab(tcg_input fmt, const uint8_t* SFA, int64_t M, uint8_t* SFA_img, const uint8_t* SFB,
+                          int64_t N, int tile_n, uint8_t* SFB_img, int64_t K, void* stream) {
+  if (!is_mx(fmt) || M < 0 || N < 0 || K < 0 || tile_n <= 0 || tile_n > 65536) return TCG_ERR_INVALID;
+  if (K == 0 || (M == 0 && N == 0)) return TCG_OK;
+  if ((M > 0 && (!SFA || !SFA_img)) || (N > 0 && (!SFB || !SFB_img))) return TCG_ERR_INVALID;
+  int dev;
+  if (int rc = current_device_checked(&dev)) return rc;
+  const cudaError_t e = launch_sf_prepare_pair(fmt, M > 0 ? SFA : nullptr, M, 128, SFA_img, N > 0 ? SFB : nullptr,
+                                               N, tile_n, SFB_img, K, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return record_cuda(e);
+  set_launch_count(1);
+  return TCG_OK;
+}
+
 int64_t tcg_mxf8_scale_image_bytes(int64_t rows, int64_t K, int tile_rows) {
-  if (rows < 0 || K < 0 || tile_rows <= 0) return -1;
-  return sf_image_bytes(rows, K, tile_rows);
+  return tcg_scale_image_bytes(TCG_IN_E4M3, rows, K, tile_rows);
 }
 
 int tcg_mxf8_tile_n(int64_t M, int64_t N, int64_t K, tcg_major b_major, int cta_group) {
@@ -932,7 +978,8 @@ int tcg_mxf8_prepare_scales(const uint8_t* sf, int64_t rows, int64_t K, int tile
   if (!sf || !img) return TCG_ERR_INVALID;
   int dev;
   if (int rc = current_device_checked(&dev)) return rc;
-  const cudaError_t e = launch_sf_prepare(sf, rows, K, tile_rows, img, reinterpret_cast<cudaStream_t>(stream));
+  const cudaError_t e =
+      launch_sf_prepare(TCG_IN_E4M3, sf, rows, K, tile_rows, img, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return record_cuda(e);
   set_launch_count(1);
   return TCG_OK;
@@ -940,16 +987,7 @@ int tcg_mxf8_prepare_scales(const uint8_t* sf, int64_t rows, int64_t K, int tile
 
 int tcg_mxf8_prepare_scales_ab(const uint8_t* SFA, int64_t M, uint8_t* SFA_img, const uint8_t* SFB, int64_t N,
                                int tile_n, uint8_t* SFB_img, int64_t K, void* stream) {
-  if (M < 0 || N < 0 || K < 0 || tile_n <= 0 || tile_n > 65536) return TCG_ERR_INVALID;
-  if (K == 0 || (M == 0 && N == 0)) return TCG_OK;
-  if ((M > 0 && (!SFA || !SFA_img)) || (N > 0 && (!SFB || !SFB_img))) return TCG_ERR_INVALID;
-  int dev;
-  if (int rc = current_device_checked(&dev)) return rc;
-  const cudaError_t e = launch_sf_prepare_pair(M > 0 ? SFA : nullptr, M, 128, SFA_img, N > 0 ? SFB : nullptr, N,
-                                               tile_n, SFB_img, K, reinterpret_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return record_cuda(e);
-  set_launch_count(1);
-  return TCG_OK;
+  return tcg_prepare_scales_ab(TCG_IN_E4M3, SFA, M, SFA_img, SFB, N, tile_n, SFB_img, K, stream);
 }
 
 int tcg_check(void* stream) {

@@ -28,12 +28,25 @@ enum F16Variant {
 KernelInfo kinfo_f16(int cta_group, F16Variant v = F16_WIDE);
 KernelInfo kinfo_tf32(int cta_group);
 KernelInfo kinfo_mxf8(int cta_group);  // BN 256, one accumulator (single CTA or CTA pair)
+// packed FP4: kind::mxf4 (scale_vec::2X, e8m0) or kind::mxf4nvf4 (scale_vec::4X, UE4M3)
+KernelInfo kinfo_fp4(int cta_group, bool nvf4);
 
+// How a block-scaled format's scales are staged: K elements per scale, K
+// steps (of four scales per row, one 512-byte chunk per 128 rows) per ring
+// stage, and the byte that stands for a scale of one.
+struct ScaleFormat {
+  int block;
+  int kch;
+  uint32_t fill;
+};
+ScaleFormat scale_format(tcg_input t);
+// Bytes of the scale image of `rows` rows and K elements, tiles of tile_rows.
+int64_t sf_image_bytes_fmt(tcg_input t, int64_t rows, int64_t K, int tile_rows);
 // Scale-factor rearrangement kernel launch (gemm_mxf8.cu).
-cudaError_t launch_sf_prepare(const uint8_t* sf, int64_t rows, int64_t K, int tile_rows, uint8_t* img,
+cudaError_t launch_sf_prepare(tcg_input t, const uint8_t* sf, int64_t rows, int64_t K, int tile_rows, uint8_t* img,
                               cudaStream_t stream);
 // Both operands' images in one launch.
-cudaError_t launch_sf_prepare_pair(const uint8_t* sfa, int64_t rows_a, int tile_a, uint8_t* img_a,
+cudaError_t launch_sf_prepare_pair(tcg_input t, const uint8_t* sfa, int64_t rows_a, int tile_a, uint8_t* img_a,
                                    const uint8_t* sfb, int64_t rows_b, int tile_b, uint8_t* img_b, int64_t K,
                                    cudaStream_t stream);
 

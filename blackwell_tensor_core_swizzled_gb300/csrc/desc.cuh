@@ -99,6 +99,14 @@ __host__ __device__ constexpr uint32_t idesc_mxf8(bool a_mn, bool b_mn, int M, i
          (static_cast<uint32_t>(N >> 3) << 17) | (1u << 23) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// kind::mxf4 / kind::mxf4nvf4: A and B are E2M1 (code 1), K-major; bit 23 the
+// scale type (1 UE8M0 for scale_vec::2X, 0 UE4M3 for scale_vec::4X); bit 31
+// (K = 96 for sparse forms) stays 0 for K = 64.
+__host__ __device__ constexpr uint32_t idesc_fp4(int M, int N, bool ue8m0) {
+  return (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(ue8m0) << 23) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
 // Scale-factor ids: which byte of the 32-bit scale column each operand's
 // scales are read from.
 __host__ __device__ constexpr uint32_t idesc_sf_ids(uint32_t sfa_id, uint32_t sfb_id) {

@@ -61,7 +61,10 @@
 
 namespace tcg {
 
-enum Kind : int { KIND_F16 = 0, KIND_TF32 = 1, KIND_MXF8 = 2 };
+// KIND_MXF8: kind::mxf8f6f4 block-scaled (E4M3 / E5M2 / FP6 / padded FP4);
+// KIND_MXF4 / KIND_NVF4: packed FP4, kind::mxf4 with two e8m0 scales per MMA
+// row, kind::mxf4nvf4 with four unsigned E4M3 scales per MMA row.
+enum Kind : int { KIND_F16 = 0, KIND_TF32 = 1, KIND_MXF8 = 2, KIND_MXF4 = 3, KIND_NVF4 = 4 };
 enum OutType : int { OUT_F32 = 0, OUT_F16 = 1, OUT_BF16 = 2 };
 enum SfMode : int { SF_BY_WARPS = 0, SF_BY_MMA = 1, SF_BY_CP = 2 };
 
@@ -170,60 +173,75 @@ __device__ __forceinline__ void trace_stamp(const GemmParams& p, int slot) {
 // memory and only feed accumulator rows >= M, which are never stored.
 template <int CG, int BN, int ACC, int STAGES, int KIND, int A_ROWS = 128>
 struct GemmCfg {
+  static constexpr bool SCALED = KIND >= KIND_MXF8;  // block-scaled kinds
   static constexpr int BM = 128;            // accumulator rows per CTA
   static constexpr int BN_LOCAL = BN / CG;  // B rows staged per CTA
   static constexpr int A_BYTES = A_ROWS * 128;
   static constexpr int B_BYTES = BN_LOCAL * 128;
   static constexpr int SFB_CHUNKS = (BN + 127) / 128;
-  static constexpr int SFA_BYTES = KIND == KIND_MXF8 ? 512 : 0;
-  static constexpr int SFB_BYTES = KIND == KIND_MXF8 ? 512 * SFB_CHUNKS : 0;
+  // 512-byte scale chunks (128 rows x 4 scale bytes) per 128 rows per stage:
+  // a stage holds 4 (MX 8/6-bit), 8 (MXFP4) or 16 (NVFP4) scales per row
+  static constexpr int SF_KCH = KIND == KIND_MXF4 ? 2 : KIND == KIND_NVF4 ? 4 : 1;
+  static constexpr int SFA_BYTES = SCALED ? 512 * SF_KCH : 0;
+  static constexpr int SFB_BYTES = SCALED ? 512 * SFB_CHUNKS * SF_KCH : 0;
   static constexpr int LOAD_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
   static constexpr int STAGE_BYTES = (LOAD_BYTES + 1023) / 1024 * 1024;
   // scale-image bytes of one stage (counted on the pair leader's full
   // barrier for both CTAs, or on each CTA's sf_loaded barrier)
   static constexpr int SF_TX_BYTES = SFA_BYTES + SFB_BYTES;
   static constexpr int MMA_M = 128 * CG;
-  static constexpr int MMA_K = KIND == KIND_F16 ? 16 : KIND == KIND_TF32 ? 8 : 32;
-  static constexpr int ELEM_BYTES = KIND == KIND_F16 ? 2 : KIND == KIND_TF32 ? 4 : 1;
-  static constexpr int BK = 128 / ELEM_BYTES;  // K elements per stage
+  static constexpr int MMA_K = KIND == KIND_F16 ? 16 : KIND == KIND_TF32 ? 8 : KIND == KIND_MXF8 ? 32 : 64;
+  // K elements per stage: one 128-byte row (packed FP4: two per byte)
+  static constexpr int BK = KIND == KIND_F16 ? 64 : KIND == KIND_TF32 ? 32 : KIND == KIND_MXF8 ? 128 : 256;
   static constexpr int KSTEPS = BK / MMA_K;    // MMA issues per stage
+  // K extent of a stage in the operand maps' units: packed FP4 is mapped as
+  // bytes, every other type in elements
+  static constexpr int MAP_K = (KIND == KIND_MXF4 || KIND == KIND_NVF4) ? 128 : BK;
+  // scale columns MMA issue j reads (relative to its slot): the chunk group of
+  // its K, then the scale id (the byte within the column)
+  static constexpr int SF_GROUP_MMAS = KSTEPS / SF_KCH;  // issues per 4-byte scale group
+  __host__ __device__ static constexpr int sfa_col(int j) { return 4 * (j / SF_GROUP_MMAS); }
+  __host__ __device__ static constexpr int sfb_col(int j) { return 4 * SF_KCH + 4 * SFB_CHUNKS * (j / SF_GROUP_MMAS); }
+  __host__ __device__ static constexpr uint32_t sf_id(int j) {
+    return static_cast<uint32_t>((j % SF_GROUP_MMAS) * (4 / SF_GROUP_MMAS));
+  }
   static constexpr int SF_COL0 = ACC * BN;     // scale-factor slots follow the accumulators
   static constexpr int TMEM_COLS = 512;
-  // a scale slot: SFA 4 columns, then SFB 4 per 128 rows (128-bit aligned
-  // column origins, as tcgen05.cp requires)
-  static constexpr int SF_SLOT_COLS = 4 + 4 * SFB_CHUNKS;
+  // a scale slot: SFA 4 columns per chunk group, then SFB 4 per 128 rows per
+  // group (128-bit aligned column origins, as tcgen05.cp requires)
+  static constexpr int SF_SLOT_COLS = 4 * SF_KCH * (1 + SFB_CHUNKS);
   // Scale slots rotate over the free TMEM columns; before a slot is
   // rewritten the MMA thread waits for the stage that last used it to retire.
   // With as many slots as ring stages the wait is implied: full[s] of
   // iteration it completes only after the producer saw empty[s] of it - STAGES,
   // i.e. after the MMAs that last read slot it % STAGES retired.
   static constexpr int SF_SLOTS_FREE = (TMEM_COLS - ACC * BN) / SF_SLOT_COLS;
-  static constexpr int SF_SLOTS = KIND != KIND_MXF8 ? 1 : SF_SLOTS_FREE < STAGES ? SF_SLOTS_FREE : STAGES;
+  static constexpr int SF_SLOTS = !SCALED ? 1 : SF_SLOTS_FREE < STAGES ? SF_SLOTS_FREE : STAGES;
   static constexpr bool SF_SLOT_WAIT = SF_SLOTS < STAGES;
   // epilogue staging for TMA stores: per epilogue warp EPI_BUFS tiles of
   // 32 rows x 64 bytes (32 16-bit columns), 64-byte swizzled
-  static constexpr int EPI_WARPS_MAX = KIND == KIND_MXF8 ? 8 : 4;
-  static constexpr int EPI_BUFS = KIND == KIND_MXF8 ? 1 : 2;
+  static constexpr int EPI_WARPS_MAX = SCALED ? 8 : 4;
+  static constexpr int EPI_BUFS = SCALED ? 1 : 2;
   static constexpr int EPI_TILE_BYTES = 32 * 64;
   static constexpr int EPI_OFF = STAGES * STAGE_BYTES;
   static constexpr int BAR_OFF = EPI_OFF + EPI_WARPS_MAX * EPI_BUFS * EPI_TILE_BYTES;
   // full[S], empty[S], acc_full[ACC], acc_empty[ACC], drain, and for block
   // scaling sf_loaded[S] (scale bytes in smem) and sf_ready[SF_SLOTS] (scales
   // written to TMEM by the scale warps)
-  static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC + 1 + (KIND == KIND_MXF8 ? STAGES + SF_SLOTS : 0);
+  static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC + 1 + (SCALED ? STAGES + SF_SLOTS : 0);
   static constexpr int SMEM_BYTES = 1024 + BAR_OFF + NUM_BARS * 8 + 16;
   // warps 0..7 as described above; block scaling adds warps 8..11, one per
   // TMEM lane quadrant, which stage the scale factors into TMEM
-  static constexpr int THREADS = KIND == KIND_MXF8 ? 384 : 256;
+  static constexpr int THREADS = SCALED ? 384 : 256;
   // epilogue warps: 4..7, plus 8..11 when block scales are staged by tcgen05.cp
   __host__ __device__ static constexpr int epi_warps(int sf_mode) {
-    return KIND == KIND_MXF8 && sf_mode != SF_BY_WARPS ? 8 : 4;
+    return SCALED && sf_mode != SF_BY_WARPS ? 8 : 4;
   }
   static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "epilogue drains 32-column chunks");
   static_assert(BN % (16 * CG) == 0, "MMA N constraint / per-CTA B split");
-  static_assert(ACC * BN + (KIND == KIND_MXF8 ? SF_SLOTS * SF_SLOT_COLS : 0) <= TMEM_COLS, "TMEM budget");
-  static_assert(KIND != KIND_MXF8 || (SF_SLOTS >= 1 && SF_SLOTS <= STAGES), "scale slots");
-  static_assert(KIND != KIND_MXF8 || SFB_CHUNKS * 4 + 4 <= SF_SLOT_COLS, "scale slot too small");
+  static_assert(ACC * BN + (SCALED ? SF_SLOTS * SF_SLOT_COLS : 0) <= TMEM_COLS, "TMEM budget");
+  static_assert(!SCALED || (SF_SLOTS >= 1 && SF_SLOTS <= STAGES), "scale slots");
+  static_assert(KSTEPS % SF_KCH == 0, "scale groups split the stage's MMAs evenly");
   static_assert(SMEM_BYTES <= 232448, "dynamic shared memory");
   static_assert(A_ROWS % 8 == 0 && A_ROWS <= 128 && (A_ROWS == 128 || CG == 1), "staged A rows");
   // the MMA's 128-row read of the last stage's A tile stays inside the
@@ -441,7 +459,7 @@ __device__ __forceinline__ void store_col32(const GemmParams& p, int row, int co
 }
 
 template <int CG, int BN, int ACC, int STAGES, int KIND, int A_ROWS = 128>
-__global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
+__global__ void __launch_bounds__(KIND >= KIND_MXF8 ? 384 : 256, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
   using C = GemmCfg<CG, BN, ACC, STAGES, KIND, A_ROWS>;
   if (threadIdx.x == 0) trace_stamp(p, TRACE_ENTRY);
   extern __shared__ uint8_t smem_raw[];
@@ -474,7 +492,7 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&p.tmap_a);
     prefetch_tmap(&p.tmap_b);
-    if constexpr (KIND == KIND_MXF8) {
+    if constexpr (C::SCALED) {
       prefetch_tmap(&p.tmap_sfa);
       prefetch_tmap(&p.tmap_sfb);
     }
@@ -495,7 +513,7 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
       mbar_init(acce_bar(b), C::epi_warps(p.sf_mode) * CG);
     }
     mbar_init(drain_bar, 1);
-    if constexpr (KIND == KIND_MXF8) {
+    if constexpr (C::SCALED) {
       for (int s = 0; s < STAGES; ++s) mbar_init(sfl_bar(s), 1);
       // sf_ready: one arrival per scale warp of each CTA, or one commit
       for (int k = 0; k < C::SF_SLOTS; ++k) mbar_init(sfr_bar(k), p.sf_mode == SF_BY_WARPS ? 4 * CG : 1);
@@ -548,12 +566,12 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
           }
           if (elect_one()) {
           const uint32_t fb = (CG == 2) ? mapa_shared(full_bar(s), 0) : full_bar(s);
-          const bool sf_on_full = KIND == KIND_MXF8 && p.sf_mode != SF_BY_WARPS;
+          const bool sf_on_full = C::SCALED && p.sf_mode != SF_BY_WARPS;
           if (rank == 0)
             mbar_arrive_expect_tx(full_bar(s), p.ab_tx_bytes + (sf_on_full ? C::SF_TX_BYTES * CG : 0));
           const uint32_t sa = sbase + s * C::STAGE_BYTES;
           const uint32_t sb = sa + C::A_BYTES;
-          const int k0 = kb * C::BK;
+          const int k0 = kb * C::MAP_K;
           if (!p.a_mn_major) {
             tma_load<CG>(sa, &p.tmap_a, k0, m0, fb);
           } else {
@@ -564,22 +582,25 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
           } else {
             for (int i = 0; i < p.b_boxes; ++i) tma_load<CG>(sb + i * p.b_box_bytes, &p.tmap_b, n0 + i * p.b_box_mn, k0, fb);
           }
-          if constexpr (KIND == KIND_MXF8) {
+          if constexpr (C::SCALED) {
             const uint32_t ssfa = sb + C::B_BYTES;
             const uint32_t ssfb = ssfa + C::SFA_BYTES;
             // a pair tile's second half may lie wholly beyond M: its A rows are
-            // zero-filled, so any valid scale row will do
+            // zero-filled, so any valid scale row will do.  The scale maps have
+            // one 512-byte chunk per row; a stage's chunks are consecutive rows.
             const int sfa_tile = min(mt * CG + static_cast<int>(rank), p.sf_a_tiles - 1);
+            const int ya = (kb * p.sf_a_tiles + sfa_tile) * C::SF_KCH;
+            const int yb = (kb * p.num_n_tiles + nt) * C::SF_KCH * C::SFB_CHUNKS;
             if (sf_on_full) {
               // a tcgen05.cp of a pair reads both CTAs' smem: complete with A, B
-              tma_load<CG>(ssfa, &p.tmap_sfa, 0, kb * p.sf_a_tiles + sfa_tile, fb);
-              tma_load<CG>(ssfb, &p.tmap_sfb, 0, kb * p.num_n_tiles + nt, fb);
+              tma_load<CG>(ssfa, &p.tmap_sfa, 0, ya, fb);
+              tma_load<CG>(ssfb, &p.tmap_sfb, 0, yb, fb);
             } else {
               // the scale warps of this CTA consume these: they complete on
               // this CTA's own sf_loaded[s]
               mbar_arrive_expect_tx(sfl_bar(s), C::SF_TX_BYTES);
-              tma_load_2d(ssfa, &p.tmap_sfa, 0, kb * p.sf_a_tiles + sfa_tile, sfl_bar(s));
-              tma_load_2d(ssfb, &p.tmap_sfb, 0, kb * p.num_n_tiles + nt, sfl_bar(s));
+              tma_load_2d(ssfa, &p.tmap_sfa, 0, ya, sfl_bar(s));
+              tma_load_2d(ssfb, &p.tmap_sfb, 0, yb, sfl_bar(s));
             }
           }
           }
@@ -633,13 +654,13 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
       uint32_t idesc_j[C::KSTEPS];
 #pragma unroll
       for (int j = 0; j < C::KSTEPS; ++j)
-        idesc_j[j] = KIND == KIND_MXF8 ? (p.idesc | idesc_sf_ids(j, j)) : p.idesc;
+        idesc_j[j] = C::SCALED ? (p.idesc | idesc_sf_ids(C::sf_id(j), C::sf_id(j))) : p.idesc;
       // block scales staged by other threads: wait for sf_ready[slot] too
-      constexpr bool sf_wait = KIND == KIND_MXF8 && SFM != SF_BY_MMA;
-      constexpr bool sf_by_mma = KIND == KIND_MXF8 && SFM == SF_BY_MMA;
+      constexpr bool sf_wait = C::SCALED && SFM != SF_BY_MMA;
+      constexpr bool sf_by_mma = C::SCALED && SFM == SF_BY_MMA;
       // the copy warp commits sf_ready[slot] only after it saw full[s] of the
       // same iteration, so that one wait covers both
-      constexpr bool full_via_sfr = KIND == KIND_MXF8 && SFM == SF_BY_CP;
+      constexpr bool full_via_sfr = C::SCALED && SFM == SF_BY_CP;
       uint32_t it = 0, s = 0, ph = 0, tcount = 0;
       bool ok = true;
       for (UnitCursor uc = uc_first; uc.valid && ok; cursor_next(uc, num_clusters, p), ++tcount) {
@@ -684,10 +705,17 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
             // 32 rows x 16 bytes, rows 16 bytes apart: (ldo 16, sdo 128, no swizzle)
             const uint64_t cp_hi = sdesc_hi(16, 128, SW_NONE);
             if (elect_one()) {
-              tc_cp_32x128b_warpx4<CG>(sf_col, sdesc(ssfa, cp_hi));
+              // chunk group g (4 scales per row) of SFA to columns 4g; of SFB,
+              // 128-row chunk c of group g to 4*SF_KCH + 4*(g*SFB_CHUNKS + c)
 #pragma unroll
-              for (int c = 0; c < C::SFB_CHUNKS; ++c)
-                tc_cp_32x128b_warpx4<CG>(sf_col + 4 + 4 * c, sdesc(ssfa + C::SFA_BYTES + 512 * c, cp_hi));
+              for (int g = 0; g < C::SF_KCH; ++g)
+                tc_cp_32x128b_warpx4<CG>(sf_col + 4 * g, sdesc(ssfa + 512 * g, cp_hi));
+#pragma unroll
+              for (int g = 0; g < C::SF_KCH; ++g)
+#pragma unroll
+                for (int c = 0; c < C::SFB_CHUNKS; ++c)
+                  tc_cp_32x128b_warpx4<CG>(sf_col + 4 * C::SF_KCH + 4 * (g * C::SFB_CHUNKS + c),
+                                           sdesc(ssfa + C::SFA_BYTES + 512 * (g * C::SFB_CHUNKS + c), cp_hi));
             }
           }
           if (elect_one()) {
@@ -697,7 +725,11 @@ __global__ void __launch_bounds__(KIND == KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
             const uint64_t bd = bdesc + j * b_step;
             const uint32_t acc = (kb != kb0 || j != 0) ? 1u : 0u;
             if constexpr (KIND == KIND_MXF8)
-              mma_mxf8<CG>(d_tmem, ad, bd, idesc_j[j], sf_col, sf_col + 4, acc);
+              mma_mxf8<CG>(d_tmem, ad, bd, idesc_j[j], sf_col + C::sfa_col(j), sf_col + C::sfb_col(j), acc);
+            else if constexpr (KIND == KIND_MXF4)
+              mma_mxf4<CG>(d_tmem, ad, bd, idesc_j[j], sf_col + C::sfa_col(j), sf_col + C::sfb_col(j), acc);
+            else if constexpr (KIND == KIND_NVF4)
+              mma_nvf4<CG>(d_tmem, ad, bd, idesc_j[j], sf_col + C::sfa_col(j), sf_col + C::sfb_col(j), acc);
             else if constexpr (KIND == KIND_F16)
               mma_f16<CG>(d_tmem, ad, bd, idesc_j[j], acc);
             else

@@ -24,6 +24,31 @@ KernelInfo kinfo_mxf8(int cta_group) {
           KIND_MXF8, C::THREADS};
 }
 
+// Packed FP4 (kind::mxf4 with e8m0 scales per 32, kind::mxf4nvf4 with
+// unsigned E4M3 scales per 16): a stage carries 256 K of two-per-byte values
+// and 8 or 16 scales per row (2 or 4 chunks), so five stages fit for CTA
+// pairs (three for single NVFP4 CTAs, whose 256-row B tile is twice as large).
+KernelInfo kinfo_fp4(int cta_group, bool nvf4) {
+  if (cta_group == 2 && nvf4) {
+    using C = GemmCfg<2, 256, 1, 5, KIND_NVF4>;
+    return {reinterpret_cast<const void*>(&gemm_kernel<2, 256, 1, 5, KIND_NVF4>), C::SMEM_BYTES, 2, 256, KIND_NVF4,
+            C::THREADS};
+  }
+  if (cta_group == 2) {
+    using C = GemmCfg<2, 256, 1, 5, KIND_MXF4>;
+    return {reinterpret_cast<const void*>(&gemm_kernel<2, 256, 1, 5, KIND_MXF4>), C::SMEM_BYTES, 2, 256, KIND_MXF4,
+            C::THREADS};
+  }
+  if (nvf4) {
+    using C = GemmCfg<1, 256, 1, 3, KIND_NVF4>;
+    return {reinterpret_cast<const void*>(&gemm_kernel<1, 256, 1, 3, KIND_NVF4>), C::SMEM_BYTES, 1, 256, KIND_NVF4,
+            C::THREADS};
+  }
+  using C = GemmCfg<1, 256, 1, 4, KIND_MXF4>;
+  return {reinterpret_cast<const void*>(&gemm_kernel<1, 256, 1, 4, KIND_MXF4>), C::SMEM_BYTES, 1, 256, KIND_MXF4,
+          C::THREADS};
+}
+
 // Rearranges plain row-major e8m0 scales sf[rows][kblocks] into the image the
 // GEMM streams: for every K step of four scale blocks and every tile of
 // tile_rows rows, ceil(tile_rows/128) chunks of 512 bytes in which the scale
@@ -52,8 +77,16 @@ struct SfJob {
 
 constexpr int SF_WARPS = 8;  // warps per block
 
+// kblocks: scale blocks per row of the plain arrays; ksteps: K steps (of
+// four blocks) that hold any of them; ksteps_img: K steps of the image, a
+// multiple of kch, the K steps per ring stage (1 for MXFP8, 2 for MXFP4, 4
+// for NVFP4); the image is [stage][tile][K step of the stage][chunk][512 B].
+// Blocks and rows that do not exist hold `fill` (a scale of one in the
+// scale's own encoding: the matching operand values are zero, and 0 x NaN
+// would not be).
 __global__ void __launch_bounds__(32 * SF_WARPS) sf_prepare_kernel(SfJob ja, SfJob jb, int64_t kblocks,
-                                                                   int64_t ksteps, int64_t kgroups) {
+                                                                   int64_t ksteps, int64_t ksteps_img, int kch,
+                                                                   uint32_t fill, int64_t kgroups) {
   const int64_t gw = static_cast<int64_t>(blockIdx.x) * SF_WARPS + (threadIdx.x >> 5);
   const int i = threadIdx.x & 31;
   int64_t blk = gw / kgroups;
@@ -69,7 +102,9 @@ __global__ void __launch_bounds__(32 * SF_WARPS) sf_prepare_kernel(SfJob ja, SfJ
       max(static_cast<int64_t>(0), min(min(static_cast<int64_t>(j.tile_rows) - 128 * c, j.rows - row0),
                                        static_cast<int64_t>(128))));
   const int64_t ks0 = 4 * kg;
-  const int nks = static_cast<int>(min(static_cast<int64_t>(4), ksteps - ks0));
+  // K steps read from the plain arrays (nks) and written to the image (nks_img)
+  const int nks = static_cast<int>(max(static_cast<int64_t>(0), min(static_cast<int64_t>(4), ksteps - ks0)));
+  const int nks_img = static_cast<int>(min(static_cast<int64_t>(4), ksteps_img - ks0));
   const uintptr_t base = reinterpret_cast<uintptr_t>(j.sf);
   const bool quad_loads = nks == 4 && kblocks % 16 == 0 && base % 16 == 0;
   const bool word_loads = kblocks % 4 == 0 && base % 4 == 0;
@@ -80,7 +115,7 @@ __global__ void __launch_bounds__(32 * SF_WARPS) sf_prepare_kernel(SfJob ja, SfJ
     const uint8_t* src = j.sf + (row0 + rl) * kblocks + 4 * ks0;
     if (rl >= valid) {
 #pragma unroll
-      for (int k = 0; k < 4; ++k) v[g][k] = 0x7F7F7F7Fu;
+      for (int k = 0; k < 4; ++k) v[g][k] = fill;
     } else if (quad_loads) {
       const uint4 q = *reinterpret_cast<const uint4*>(src);
       v[g][0] = q.x;
@@ -91,14 +126,14 @@ __global__ void __launch_bounds__(32 * SF_WARPS) sf_prepare_kernel(SfJob ja, SfJ
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         if (k >= nks) {
-          v[g][k] = 0x7F7F7F7Fu;
+          v[g][k] = fill;
         } else if (word_loads) {
           v[g][k] = reinterpret_cast<const uint32_t*>(src)[k];
         } else {
           uint32_t w = 0u;
           for (int b = 0; b < 4; ++b) {
             const int64_t kb = 4 * (ks0 + k) + b;
-            w |= (kb < kblocks ? static_cast<uint32_t>(src[4 * k + b]) : 127u) << (8 * b);
+            w |= (kb < kblocks ? static_cast<uint32_t>(src[4 * k + b]) : (fill & 0xFFu)) << (8 * b);
           }
           v[g][k] = w;
         }
@@ -108,8 +143,9 @@ __global__ void __launch_bounds__(32 * SF_WARPS) sf_prepare_kernel(SfJob ja, SfJ
   const bool quad_stores = reinterpret_cast<uintptr_t>(j.img) % 16 == 0;
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    if (k < nks) {
-      uint32_t* dst = j.img + (((ks0 + k) * j.tiles + t) * j.chunks + c) * 128 + 4 * i;
+    if (k < nks_img) {
+      const int64_t ks = ks0 + k;
+      uint32_t* dst = j.img + ((((ks / kch) * j.tiles + t) * kch + ks % kch) * j.chunks + c) * 128 + 4 * i;
       if (quad_stores) {
         *reinterpret_cast<uint4*>(dst) = make_uint4(v[0][k], v[1][k], v[2][k], v[3][k]);
       } else {
@@ -133,25 +169,46 @@ SfJob make_job(const uint8_t* sf, int64_t rows, int tile_rows, uint8_t* img) {
 }
 }  // namespace
 
-cudaError_t launch_sf_prepare_pair(const uint8_t* sfa, int64_t rows_a, int tile_a, uint8_t* img_a,
+ScaleFormat scale_format(tcg_input t) {
+  // MXFP8 / FP6 / FP4 on kind::mxf8f6f4: e8m0 per 32, one 128-K step per stage;
+  // packed MXFP4: e8m0 per 32, stages of 256 K; NVFP4: unsigned E4M3 per 16,
+  // stages of 256 K
+  if (t == TCG_IN_E2M1) return {32, 2, 0x7Fu};
+  if (t == TCG_IN_NVF4) return {16, 4, 0x38u};
+  return {32, 1, 0x7Fu};
+}
+
+int64_t sf_image_bytes_fmt(tcg_input t, int64_t rows, int64_t K, int tile_rows) {
+  const ScaleFormat f = scale_format(t);
+  const int64_t kblocks = (K + f.block - 1) / f.block;
+  const int64_t ksteps = (kblocks + 3) / 4;
+  const int64_t ksteps_img = (ksteps + f.kch - 1) / f.kch * f.kch;
+  return ksteps_img * ((rows + tile_rows - 1) / tile_rows) * ((tile_rows + 127) / 128) * 512;
+}
+
+cudaError_t launch_sf_prepare_pair(tcg_input t, const uint8_t* sfa, int64_t rows_a, int tile_a, uint8_t* img_a,
                                    const uint8_t* sfb, int64_t rows_b, int tile_b, uint8_t* img_b, int64_t K,
                                    cudaStream_t stream) {
-  const int64_t kblocks = (K + 31) / 32;
+  const ScaleFormat f = scale_format(t);
+  const int64_t kblocks = (K + f.block - 1) / f.block;
   const int64_t ksteps = (kblocks + 3) / 4;
-  const int64_t kgroups = (ksteps + 3) / 4;
+  const int64_t ksteps_img = (ksteps + f.kch - 1) / f.kch * f.kch;
+  const int64_t kgroups = (ksteps_img + 3) / 4;
   const SfJob ja = make_job(sfa, rows_a, tile_a, img_a);
   const SfJob jb = make_job(sfb, rows_b, tile_b, img_b);
   const int64_t warps = (ja.tiles * ja.chunks + jb.tiles * jb.chunks) * kgroups;
   if (warps == 0 || kblocks == 0) return cudaSuccess;
   const int64_t blocks = (warps + SF_WARPS - 1) / SF_WARPS;
   if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
-  sf_prepare_kernel<<<static_cast<unsigned>(blocks), 32 * SF_WARPS, 0, stream>>>(ja, jb, kblocks, ksteps, kgroups);
+  const uint32_t fill4 = f.fill * 0x01010101u;
+  sf_prepare_kernel<<<static_cast<unsigned>(blocks), 32 * SF_WARPS, 0, stream>>>(ja, jb, kblocks, ksteps, ksteps_img,
+                                                                                f.kch, fill4, kgroups);
   return cudaGetLastError();
 }
 
-cudaError_t launch_sf_prepare(const uint8_t* sf, int64_t rows, int64_t K, int tile_rows, uint8_t* img,
+cudaError_t launch_sf_prepare(tcg_input t, const uint8_t* sf, int64_t rows, int64_t K, int tile_rows, uint8_t* img,
                               cudaStream_t stream) {
-  return launch_sf_prepare_pair(sf, rows, tile_rows, img, nullptr, 0, 128, nullptr, K, stream);
+  return launch_sf_prepare_pair(t, sf, rows, tile_rows, img, nullptr, 0, 128, nullptr, K, stream);
 }
 
 }  // namespace tcg

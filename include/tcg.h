@@ -68,17 +68,21 @@ typedef enum { TCG_K_MAJOR = 0, TCG_MN_MAJOR = 1 } tcg_major;
 /* Accumulator / output element types. */
 typedef enum { TCG_F32 = 0, TCG_F16 = 1, TCG_BF16 = 2 } tcg_dtype;
 
-/* Operand storage types (generic entry point).  The last five are the
- * element formats of kind::mxf8f6f4.block_scale.scale_vec::1X ("tcgen05.mma"
- * page, "Weight-stationary and block scaling": ".kind and .scale_vec"), all
- * with one e8m0 scale per 32 K elements.  E3M2, E2M3 and E2M1 are stored
- * packed: element i of the array (i = row * ld + column, ld counted in
- * elements) in bits [b*i, b*(i+1)) of the array read as one little-endian bit
- * string (b = 6 or 4; an E2M1 byte holds element 2j in its low nibble).  In
- * shared memory each sixteen of them fill a 16-byte block, data first and
- * padding after -- the layout of the "tcgen05.cp" page's "Native FP4/FP6
- * decompression" sources -- so a 128-byte row holds 128 elements of any of
- * these formats. */
+/* Operand storage types (generic entry point).  The block-scaled formats
+ * ("tcgen05.mma" page, "Weight-stationary and block scaling": ".kind and
+ * .scale_vec::1X/2X/4X"):
+ *   E4M3, E5M2, E3M2, E2M3  kind::mxf8f6f4.block_scale.scale_vec::1X, one e8m0
+ *                           scale per 32 K elements;
+ *   E2M1 (MXFP4)            kind::mxf4.block_scale.scale_vec::2X, e8m0 per 32;
+ *   NVF4 (NVFP4)            E2M1 elements, kind::mxf4nvf4.block_scale.
+ *                           scale_vec::4X, one unsigned E4M3 scale per 16.
+ * E3M2, E2M3 and the FP4 formats are stored packed: element i of the array
+ * (i = row * ld + column, ld counted in elements) in bits [b*i, b*(i+1)) of
+ * the array read as one little-endian bit string (b = 6 or 4; an FP4 byte
+ * holds element 2j in its low nibble).  In shared memory the FP6 values sit
+ * sixteen to a 16-byte block, data first and padding after -- the layout of
+ * the "tcgen05.cp" page's "Native FP4/FP6 decompression" sources -- so a
+ * 128-byte row holds 128 of them; FP4 stays packed, 256 to a row. */
 typedef enum {
   TCG_IN_F16 = 0,   /* IEEE binary16, MMA kind::f16 */
   TCG_IN_BF16 = 1,  /* bfloat16, kind::f16 */
@@ -87,7 +91,8 @@ typedef enum {
   TCG_IN_E5M2 = 4,  /* OCP E5M2 (FP8) */
   TCG_IN_E3M2 = 5,  /* OCP MX E3M2 (FP6), packed */
   TCG_IN_E2M3 = 6,  /* OCP MX E2M3 (FP6), packed */
-  TCG_IN_E2M1 = 7   /* OCP MX E2M1 (FP4), packed */
+  TCG_IN_E2M1 = 7,  /* OCP MX E2M1 (FP4), packed, e8m0 scales per 32 */
+  TCG_IN_NVF4 = 8   /* E2M1 (FP4), packed, unsigned E4M3 scales per 16 (NVFP4) */
 } tcg_input;
 
 /* ---------------------------------------------------------------------------
@@ -134,15 +139,22 @@ int tcg_gemm_mxf8_blockscaled(int64_t M, int64_t N, int64_t K,
                               void* D, tcg_dtype d_type, int64_t ldd,
                               tcg_dtype acc_type, void* stream);
 
-/* Block-scaled FP6 (fmt TCG_IN_E3M2 or TCG_IN_E2M3) and FP4 (E2M1) GEMMs:
- * the MXFP8 operation with 6- / 4-bit elements, on the same MMA kind
- * (kind::mxf8f6f4, the format in the instruction descriptor) and the same
- * scale layout (SFA [M][ceil(K/32)], SFB [N][ceil(K/32)] e8m0).  A and B are
- * packed (see tcg_input), K-major only (TCG_ERR_UNSUPPORTED otherwise), lda /
- * ldb count elements.  The tensor-map rules of the padded element types apply:
- * K a multiple of 128, A and B 32-byte aligned, row strides (ld * 6 / 8 or
- * ld * 4 / 8 bytes) multiples of 32 bytes (else TCG_ERR_ALIGNMENT).
- * acc_type must be TCG_F32. */
+/* Block-scaled FP6 GEMM (fmt TCG_IN_E3M2 or TCG_IN_E2M3): the MXFP8 operation
+ * with 6-bit elements on the same MMA kind (kind::mxf8f6f4, the format in the
+ * instruction descriptor) and scale layout (SFA [M][ceil(K/32)], SFB
+ * [N][ceil(K/32)] e8m0).  A and B are packed (see tcg_input), K-major only
+ * (TCG_ERR_UNSUPPORTED otherwise), lda / ldb count elements.  The tensor-map
+ * rules of the padded element type apply: K a multiple of 128, A and B
+ * 32-byte aligned, row strides (ld * 6 / 8 bytes) multiples of 32 bytes (else
+ * TCG_ERR_ALIGNMENT).  acc_type must be TCG_F32.
+ *
+ * Block-scaled FP4 GEMMs: MXFP4 (E2M1, e8m0 scales [rows][ceil(K/32)],
+ * kind::mxf4.block_scale.scale_vec::2X) and NVFP4 (E2M1, unsigned E4M3 scales
+ * [rows][ceil(K/16)], kind::mxf4nvf4.block_scale.scale_vec::4X).  A and B are
+ * packed two values per byte, K-major only; K and lda / ldb (in elements)
+ * multiples of 32, A and B 16-byte aligned (else TCG_ERR_ALIGNMENT).  The
+ * values stay packed in shared memory, 256 of K per 128-byte row and K = 64
+ * per MMA.  acc_type must be TCG_F32. */
 int tcg_gemm_mxf6_blockscaled(tcg_input fmt, int64_t M, int64_t N, int64_t K,
                               const void* A, tcg_major a_major, int64_t lda,
                               const void* B, tcg_major b_major, int64_t ldb,
@@ -151,6 +163,13 @@ int tcg_gemm_mxf6_blockscaled(tcg_input fmt, int64_t M, int64_t N, int64_t K,
                               tcg_dtype acc_type, void* stream);
 
 int tcg_gemm_mxf4_blockscaled(int64_t M, int64_t N, int64_t K,
+                              const void* A, tcg_major a_major, int64_t lda,
+                              const void* B, tcg_major b_major, int64_t ldb,
+                              const uint8_t* SFA, const uint8_t* SFB,
+                              void* D, tcg_dtype d_type, int64_t ldd,
+                              tcg_dtype acc_type, void* stream);
+
+int tcg_gemm_nvf4_blockscaled(int64_t M, int64_t N, int64_t K,
                               const void* A, tcg_major a_major, int64_t lda,
                               const void* B, tcg_major b_major, int64_t ldb,
                               const uint8_t* SFA, const uint8_t* SFB,
@@ -239,6 +258,15 @@ int tcg_gemm(const tcg_gemm_args* args, void* stream);
 /* Bytes of the image for `rows` rows, K elements, tiles of tile_rows rows. */
 int64_t tcg_mxf8_scale_image_bytes(int64_t rows, int64_t K, int tile_rows);
 
+/* The same for any block-scaled format (fmt TCG_IN_E4M3 .. TCG_IN_NVF4): a
+ * ring stage covers 128 K (MX 8- and 6-bit formats) or 256 K (FP4), i.e. 4,
+ * 8 (MXFP4) or 16 (NVFP4) scales per row, so the image is, per stage and
+ * tile, ceil(tile_rows/128) x (1, 2 or 4) chunks of 512 bytes:
+ * [stage][tile][group of 4 scales][chunk][512 B]; missing rows and scales
+ * hold the scale of one (e8m0 127, E4M3 0x38).  -1 for a non-block-scaled
+ * fmt or negative sizes. */
+int64_t tcg_scale_image_bytes(tcg_input fmt, int64_t rows, int64_t K, int tile_rows);
+
 /* tile_rows the GEMM uses for SFA (always 128 per CTA) and SFB (the N tile),
  * for a given problem and cta_group request (0 = auto). */
 int tcg_mxf8_tile_n(int64_t M, int64_t N, int64_t K, tcg_major b_major, int cta_group);
@@ -255,6 +283,14 @@ int tcg_mxf8_prepare_scales(const uint8_t* sf, int64_t rows, int64_t K, int tile
 int tcg_mxf8_prepare_scales_ab(const uint8_t* SFA, int64_t M, uint8_t* SFA_img,
                                const uint8_t* SFB, int64_t N, int tile_n, uint8_t* SFB_img,
                                int64_t K, void* stream);
+
+/* tcg_mxf8_prepare_scales_ab for any block-scaled format: plain scales of fmt
+ * (e8m0 per 32, or unsigned E4M3 per 16 for TCG_IN_NVF4) into the images
+ * tcg_gemm reads (sizes from tcg_scale_image_bytes; tile_n from
+ * tcg_mxf8_tile_n, which holds for every block-scaled format). */
+int tcg_prepare_scales_ab(tcg_input fmt, const uint8_t* SFA, int64_t M, uint8_t* SFA_img,
+                          const uint8_t* SFB, int64_t N, int tile_n, uint8_t* SFB_img,
+                          int64_t K, void* stream);
 
 /* ---------------------------------------------------------------------------
  * Status and configuration.

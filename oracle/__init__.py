@@ -45,13 +45,13 @@ def _load():
         lib = ctypes.CDLL(path)
         i64, vp, ci, dp = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p
         lib.oracle_gemm.argtypes = [i64, i64, i64, vp, ci, ci, i64, vp, ci, ci, i64,
-                                    vp, i64, vp, i64, vp, i64, dp, dp, ci]
+                                    vp, i64, vp, i64, ci, ci, vp, i64, dp, dp, ci]
         lib.oracle_gemm.restype = ci
         for name, t in (("oracle_dec_f16", ctypes.c_uint16), ("oracle_dec_bf16", ctypes.c_uint16),
                         ("oracle_dec_f32", ctypes.c_uint32), ("oracle_dec_e4m3", ctypes.c_uint8),
                         ("oracle_dec_e5m2", ctypes.c_uint8), ("oracle_dec_e3m2", ctypes.c_uint8),
                         ("oracle_dec_e2m3", ctypes.c_uint8), ("oracle_dec_e2m1", ctypes.c_uint8),
-                        ("oracle_dec_e8m0", ctypes.c_uint8)):
+                        ("oracle_dec_e8m0", ctypes.c_uint8), ("oracle_dec_ue4m3", ctypes.c_uint8)):
             f = getattr(lib, name)
             f.argtypes = [t]
             f.restype = ctypes.c_double
@@ -75,6 +75,16 @@ def decode(bits: np.ndarray, dtype: int) -> np.ndarray:
     return np.array([f(int(x)) for x in flat], dtype=np.float64).reshape(np.shape(bits))
 
 
+def decode_ue4m3(bits: np.ndarray) -> np.ndarray:
+    lib = _load()
+    flat = np.asarray(bits).ravel()
+    return np.array([lib.oracle_dec_ue4m3(int(x)) for x in flat], dtype=np.float64).reshape(np.shape(bits))
+
+
+#: scale encodings
+SF_E8M0, SF_UE4M3 = 0, 1
+
+
 def decode_e8m0(bits: np.ndarray) -> np.ndarray:
     lib = _load()
     flat = np.asarray(bits).ravel()
@@ -89,14 +99,16 @@ _STORAGE = {F32: np.uint32, F16: np.uint16, BF16: np.uint16, E4M3: np.uint8, E5M
 def gemm(M: int, N: int, K: int, A: np.ndarray, a_type: int, a_major: int, lda: int,
          B: np.ndarray, b_type: int, b_major: int, ldb: int,
          SFA: np.ndarray | None = None, SFB: np.ndarray | None = None,
-         rows=None, nthreads: int = 0):
+         rows=None, nthreads: int = 0, sf_block: int = 32, sf_kind: int = 0):
     """Float64 D and S for the requested rows (all rows when ``rows`` is None).
 
     A/B are raw storage arrays (uint32 for fp32, uint16 for f16/bf16, uint8 for
     e4m3 / e5m2, and uint8 bytes of the packed bit string for the 6- and 4-bit
     formats, whose ld is still counted in elements) laid out as the C file's
     header states.  SFA/SFB are plain
-    row-major e8m0 arrays [M][ceil(K/32)] / [N][ceil(K/32)].
+    row-major scale arrays [M][ceil(K/sf_block)] / [N][ceil(K/sf_block)]:
+    e8m0 (sf_kind SF_E8M0, blocks of 32) or unsigned E4M3 (SF_UE4M3, the NVFP4
+    blocks of 16).
     Returns (D, S) of shape (len(rows), N).
     """
     lib = _load()
@@ -112,7 +124,7 @@ def gemm(M: int, N: int, K: int, A: np.ndarray, a_type: int, a_major: int, lda: 
             raise ValueError("row index out of range")
     D = np.zeros((nrows, N), dtype=np.float64)
     S = np.zeros((nrows, N), dtype=np.float64)
-    kb = -(-K // 32)
+    kb = -(-K // sf_block)
     sfa_p = sfb_p = None
     if SFA is not None:
         SFA = np.ascontiguousarray(SFA, dtype=np.uint8)
@@ -124,7 +136,7 @@ def gemm(M: int, N: int, K: int, A: np.ndarray, a_type: int, a_major: int, lda: 
         sfb_p = SFB.ctypes.data
     rc = lib.oracle_gemm(M, N, K, A.ctypes.data, a_type, a_major, lda,
                          B.ctypes.data, b_type, b_major, ldb,
-                         sfa_p, kb, sfb_p, kb,
+                         sfa_p, kb, sfb_p, kb, sf_block, sf_kind,
                          None if rows_arr is None else rows_arr.ctypes.data, nrows,
                          D.ctypes.data, S.ctypes.data, nthreads)
     if rc != 0:

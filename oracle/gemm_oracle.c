@@ -15,11 +15,14 @@
  *     S[m,n] = sum_k |dec(A)[m,k]| * |dec(B)[k,n]|
  *
  * For the block-scaled variant ("Weight-stationary and block scaling" on the
- * same page) every A element is multiplied by its row's e8m0 scale for the
- * 32-wide K block it falls in, and every B element by its column's:
+ * same page) every A element is multiplied by its row's scale for the K block
+ * it falls in, and every B element by its column's:
  *
- *     dec(A)[m,k] = fp(A[m,k]) * 2^(SFA[m, k/32] - 127)
- *     dec(B)[k,n] = fp(B[k,n]) * 2^(SFB[n, k/32] - 127)
+ *     dec(A)[m,k] = fp(A[m,k]) * scale(SFA[m, k/blk])
+ *     dec(B)[k,n] = fp(B[k,n]) * scale(SFB[n, k/blk])
+ *
+ * with blk = 32 and e8m0 scales 2^(b-127) (the MX formats), or blk = 16 and
+ * unsigned E4M3 scales (the NVFP4 format).
  *
  * where fp is the element format: E4M3 or E5M2 (one byte per element), E3M2 or
  * E2M3 (6 bits, packed four to three bytes) or E2M1 (4 bits, packed two to a
@@ -139,6 +142,10 @@ double oracle_dec_e2m3(uint8_t x) { return dec_minifloat(x & 0x3f, 2, 3, 1); }
 /* E2M1 (FP4): 1 sign, 2 exponent (bias 1), 1 fraction bit. */
 double oracle_dec_e2m1(uint8_t x) { return dec_minifloat(x & 0xf, 2, 1, 1); }
 
+/* UE4M3: the E4M3FN encoding without its sign bit (scales are positive);
+ * 0x7F is NaN, codes with the top bit set are not scales. */
+double oracle_dec_ue4m3(uint8_t x) { return x & 0x80 ? NAN : oracle_dec_e4m3(x); }
+
 /* E8M0: unsigned power of two 2^(b-127); 0xFF is NaN. */
 double oracle_dec_e8m0(uint8_t b) {
   if (b == 0xff) return NAN;
@@ -169,8 +176,11 @@ static double dec_elem(const void* base, int type, int64_t idx) {
   return NAN;
 }
 
+enum { ORC_SF_E8M0 = 0, ORC_SF_UE4M3 = 1 };
+
 typedef struct {
   int64_t M, N, K;
+  int sf_block, sf_kind;
   const void* A; int a_type, a_major; int64_t lda;
   const void* B; int b_type, b_major; int64_t ldb;
   const uint8_t* SFA; int64_t ldsfa;
@@ -181,6 +191,8 @@ typedef struct {
   int nthreads, tid;
 } job_t;
 
+static double dec_scale(uint8_t b, int kind) { return kind == ORC_SF_UE4M3 ? oracle_dec_ue4m3(b) : oracle_dec_e8m0(b); }
+
 /* Step 1: decode (and scale) B into a dense K x N float64 matrix. */
 static void* decode_b(void* p) {
   job_t* j = (job_t*)p;
@@ -188,7 +200,7 @@ static void* decode_b(void* p) {
     for (int64_t n = 0; n < j->N; ++n) {
       int64_t idx = (j->b_major == ORC_K_MAJOR) ? n * j->ldb + k : k * j->ldb + n;
       double b = dec_elem(j->B, j->b_type, idx);
-      if (j->SFB) b *= oracle_dec_e8m0(j->SFB[n * j->ldsfb + k / 32]);
+      if (j->SFB) b *= dec_scale(j->SFB[n * j->ldsfb + k / j->sf_block], j->sf_kind);
       j->Bd[k * j->N + n] = b;
     }
   }
@@ -204,7 +216,7 @@ static void* rows_job(void* p) {
     for (int64_t k = 0; k < j->K; ++k) {
       int64_t idx = (j->a_major == ORC_K_MAJOR) ? m * j->lda + k : k * j->lda + m;
       double v = dec_elem(j->A, j->a_type, idx);
-      if (j->SFA) v *= oracle_dec_e8m0(j->SFA[m * j->ldsfa + k / 32]);
+      if (j->SFA) v *= dec_scale(j->SFA[m * j->ldsfa + k / j->sf_block], j->sf_kind);
       a[k] = v;
     }
     double* d = j->D + i * j->N;
@@ -255,7 +267,8 @@ int oracle_num_threads(void) {
  *   rows == NULL: all M rows, written to D/S as M x N (row-major).
  *   rows != NULL: nrows rows; output row i is D row rows[i].
  * SFA/SFB may be NULL (no block scaling).  ldsfa/ldsfb are the row strides of
- * the plain [M][K/32] / [N][K/32] e8m0 arrays.  nthreads <= 0 uses all
+ * the plain [M][ceil(K/blk)] / [N][ceil(K/blk)] scale arrays; sf_block is blk
+ * (32 or 16) and sf_kind the scale encoding (0 e8m0, 1 unsigned E4M3).  nthreads <= 0 uses all
  * online cores.  Returns 0, or a negative value on invalid arguments or
  * allocation failure.
  */
@@ -263,10 +276,11 @@ int oracle_gemm(int64_t M, int64_t N, int64_t K,
                 const void* A, int a_type, int a_major, int64_t lda,
                 const void* B, int b_type, int b_major, int64_t ldb,
                 const uint8_t* SFA, int64_t ldsfa,
-                const uint8_t* SFB, int64_t ldsfb,
+                const uint8_t* SFB, int64_t ldsfb, int sf_block, int sf_kind,
                 const int64_t* rows, int64_t nrows,
                 double* D, double* S, int nthreads) {
   if (M < 0 || N < 0 || K < 0 || !D || !S) return -1;
+  if (sf_block != 16 && sf_block != 32) return -1;
   if (!rows) nrows = M;
   if (nrows == 0 || N == 0) return 0;
   if (K > 0 && (!A || !B)) return -1;
@@ -277,6 +291,7 @@ int oracle_gemm(int64_t M, int64_t N, int64_t K,
   base.A = A; base.a_type = a_type; base.a_major = a_major; base.lda = lda;
   base.B = B; base.b_type = b_type; base.b_major = b_major; base.ldb = ldb;
   base.SFA = SFA; base.ldsfa = ldsfa; base.SFB = SFB; base.ldsfb = ldsfb;
+  base.sf_block = sf_block; base.sf_kind = sf_kind;
   base.rows = rows; base.nrows = nrows;
   base.D = D; base.S = S;
   base.nthreads = nthreads;

@@ -22,11 +22,14 @@ from dataclasses import dataclass, field
 import numpy as np
 import torch
 
-DTYPES = ("f16", "bf16", "tf32", "e4m3", "e5m2", "e3m2", "e2m3", "e2m1")
-#: bits per element of the packed formats
-PACKED_BITS = {"e3m2": 6, "e2m3": 6, "e2m1": 4}
-#: formats with one e8m0 scale per 32 K elements
-BLOCK_SCALED = ("e4m3", "e5m2", "e3m2", "e2m3", "e2m1")
+DTYPES = ("f16", "bf16", "tf32", "e4m3", "e5m2", "e3m2", "e2m3", "e2m1", "nvf4")
+#: bits per element of the packed formats ("nvf4": E2M1 elements of the
+#: NVFP4 format, whose scales are unsigned E4M3 per 16 K elements)
+PACKED_BITS = {"e3m2": 6, "e2m3": 6, "e2m1": 4, "nvf4": 4}
+#: block-scaled formats: one e8m0 scale per 32 K elements, or for "nvf4" one
+#: unsigned E4M3 scale per 16
+BLOCK_SCALED = ("e4m3", "e5m2", "e3m2", "e2m3", "e2m1", "nvf4")
+SCALE_BLOCK = {"nvf4": 16}
 
 _TORCH = {"f16": torch.float16, "bf16": torch.bfloat16, "tf32": torch.float32,
           "e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}
@@ -74,6 +77,8 @@ WORKLOADS = {
                                "codes", "f32", "bf16", 2, True, 8),
     "mxf4_8192": Workload("mxf4_8192", 8192, 8192, 8192, "e2m1", "k", "k",
                           "codes", "f32", "bf16", 2, True, 9),
+    "nvf4_8192": Workload("nvf4_8192", 8192, 8192, 8192, "nvf4", "k", "k",
+                          "codes", "f32", "bf16", 2, True, 10),
     # Skinny (decode-like) shapes: a few rows of activations against an
     # 8192 x 8192 weight; bound by streaming B from HBM, reported in GB/s.
     "bf16_skinny_m16": Workload("bf16_skinny_m16", 16, 8192, 8192, "bf16", "k", "k",
@@ -147,6 +152,16 @@ def scales(rows: int, K: int, seed: int, lo: int = -4, hi: int = 4) -> np.ndarra
     return (127 + rng.integers(lo, hi + 1, size=(rows, -(-K // 32)))).astype(np.uint8)
 
 
+def ue4m3_scales(rows: int, K: int, seed: int) -> np.ndarray:
+    """Unsigned E4M3 scale bytes, one per 16 K elements per row: exponent
+    field uniform in 3..11 (2^-4 .. 2^4) and a uniform 3-bit fraction."""
+    rng = np.random.default_rng(seed)
+    shape = (rows, -(-K // 16))
+    e = rng.integers(3, 12, size=shape)
+    f = rng.integers(0, 8, size=shape)
+    return ((e << 3) | f).astype(np.uint8)
+
+
 def make_inputs(w: Workload, M: int | None = None, N: int | None = None, K: int | None = None,
                 dist: str | None = None):
     """Storage-bit arrays (A, B, SFA, SFB) for a workload, optionally resized.
@@ -174,7 +189,10 @@ def make_inputs(w: Workload, M: int | None = None, N: int | None = None, K: int 
         B = lay_out_b(to_bits(b, w.dtype), w.b_major)
         out = {"A": A, "B": B, "lda": A.shape[1], "ldb": B.shape[1], "M": M, "N": N, "K": K,
                "SFA": None, "SFB": None}
-    if w.block_scaled:
+    if w.block_scaled and w.dtype == "nvf4":
+        out["SFA"] = ue4m3_scales(M, K, 3000 + i)
+        out["SFB"] = ue4m3_scales(N, K, 4000 + i)
+    elif w.block_scaled:
         out["SFA"] = scales(M, K, 3000 + i)
         out["SFB"] = scales(N, K, 4000 + i)
     return out

@@ -7,8 +7,10 @@ import torch
 
 import synthetic as syn
 
-IN_TYPE = {"f16": 0, "bf16": 1, "tf32": 2, "e4m3": 3, "e5m2": 4, "e3m2": 5, "e2m3": 6, "e2m1": 7}  # tcg_input
-ORACLE_TYPE = {"f16": 1, "bf16": 2, "tf32": 0, "e4m3": 3, "e5m2": 4, "e3m2": 5, "e2m3": 6, "e2m1": 7}  # oracle enum
+IN_TYPE = {"f16": 0, "bf16": 1, "tf32": 2, "e4m3": 3, "e5m2": 4, "e3m2": 5, "e2m3": 6, "e2m1": 7,
+           "nvf4": 8}  # tcg_input
+ORACLE_TYPE = {"f16": 1, "bf16": 2, "tf32": 0, "e4m3": 3, "e5m2": 4, "e3m2": 5, "e2m3": 6, "e2m1": 7,
+               "nvf4": 7}  # oracle element enum (NVFP4 elements are E2M1)
 ESIZE = {"f16": 2, "bf16": 2, "tf32": 4, "e4m3": 1, "e5m2": 1}   # bytes per element (unpacked formats)
 OUT = {"f32": (0, torch.float32), "f16": (1, torch.float16), "bf16": (2, torch.bfloat16)}
 ACC = {"f32": 0, "f16": 1}
@@ -84,9 +86,11 @@ def run_gpu(tcg, x, out="bf16", acc="f32", cta_group=0, ldd=None, D=None, raster
 def oracle_rows(oracle, x, rows=None):
     w = x["w"]
     t = ORACLE_TYPE[w.dtype]
+    nv = w.dtype == "nvf4"  # unsigned E4M3 scales per 16 K elements
     return oracle.gemm(x["M"], x["N"], x["K"], x["A"], t, 0 if w.a_major == "k" else 1, x["lda"],
                        x["B"], t, 0 if w.b_major == "k" else 1, x["ldb"],
-                       SFA=x["SFA"], SFB=x["SFB"], rows=rows)
+                       SFA=x["SFA"], SFB=x["SFB"], rows=rows, sf_block=16 if nv else 32,
+                       sf_kind=oracle.SF_UE4M3 if nv else oracle.SF_E8M0)
 
 
 def assert_parity(got: np.ndarray, ref: np.ndarray, S: np.ndarray, tau: float, what: str = "",

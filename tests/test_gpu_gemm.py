@@ -92,6 +92,11 @@ MX_FORMATS = [
     ("e2m1", "k", "k", 300, 520, 256, 2, "bf16"),
     ("e2m1", "k", "k", 1000, 1100, 640, 0, "bf16"),
     ("e2m1", "k", "k", 64, 256, 128, 1, "f32"),
+    ("e2m1", "k", "k", 200, 300, 96, 1, "f32"),      # K not a multiple of the 256-K stage
+    ("nvf4", "k", "k", 300, 520, 256, 2, "bf16"),
+    ("nvf4", "k", "k", 513, 1100, 320, 0, "bf16"),   # 20 scales per row: a padded last stage
+    ("nvf4", "k", "k", 100, 300, 64, 1, "f32"),
+    ("nvf4", "k", "k", 256, 1024, 1024, 2, "bf16"),
 ]
 
 
@@ -101,7 +106,7 @@ def test_block_scaled_formats_full_compare(tcg, oracle_mod, dtype, am, bm, M, N,
     _check_full(tcg, oracle_mod, x, out, "f32", cg)
 
 
-@pytest.mark.parametrize("dtype,one", [("e2m1", 0x2), ("e2m3", 0x08), ("e3m2", 0x0C)])
+@pytest.mark.parametrize("dtype,one", [("e2m1", 0x2), ("e2m3", 0x08), ("e3m2", 0x0C), ("nvf4", 0x2)])
 def test_packed_identity_reads_every_code_in_place(tcg, oracle_mod, dtype, one):
     """A = I (the code of 1.0 on the diagonal, scales 2^0) and B random codes:
     D[m, n] = B[n, m] decoded, exactly.  Pins how TMA expands the packed rows
@@ -111,25 +116,28 @@ def test_packed_identity_reads_every_code_in_place(tcg, oracle_mod, dtype, one):
     A = syn.pack(np.where(np.eye(n, dtype=bool), one, 0).astype(np.uint8), bits)
     codes = syn.codes((N, n), 41 + bits, bits)
     B = syn.pack(codes, bits)
-    SFA = np.full((n, n // 32), 127, np.uint8)
-    SFB = np.full((N, n // 32), 127, np.uint8)
+    nv = dtype == "nvf4"  # scales of one: e8m0 127 per 32, or unsigned E4M3 0x38 per 16
+    SFA = np.full((n, n // (16 if nv else 32)), 0x38 if nv else 127, np.uint8)
+    SFB = np.full((N, n // (16 if nv else 32)), 0x38 if nv else 127, np.uint8)
     D = torch.full((n, N), float("nan"), dtype=torch.float32, device="cuda")
-    t = {"e2m1": tcg.IN_E2M1, "e2m3": tcg.IN_E2M3, "e3m2": tcg.IN_E3M2}[dtype]
+    t = {"e2m1": tcg.IN_E2M1, "e2m3": tcg.IN_E2M3, "e3m2": tcg.IN_E3M2, "nvf4": tcg.IN_NVF4}[dtype]
     tcg.gemm(n, N, n, t, to_device(A), 0, n, to_device(B), 0, n, D, 0, N, 0, SFA=to_device(SFA), SFB=to_device(SFB))
     assert tcg.check() == 0
-    expect = oracle_mod.decode(codes, oracle_mod.E2M1 if dtype == "e2m1" else
+    expect = oracle_mod.decode(codes, oracle_mod.E2M1 if dtype in ("e2m1", "nvf4") else
                                oracle_mod.E2M3 if dtype == "e2m3" else oracle_mod.E3M2).T
     assert np.array_equal(D.double().cpu().numpy(), expect)
 
 
 def test_named_fp6_fp4_entry_points(tcg, oracle_mod):
-    for fmt, dtype in ((tcg.IN_E3M2, "e3m2"), (tcg.IN_E2M3, "e2m3"), (None, "e2m1")):
+    for fmt, dtype in ((tcg.IN_E3M2, "e3m2"), (tcg.IN_E2M3, "e2m3"), (None, "e2m1"), ("nv", "nvf4")):
         x = make_case(dtype, "k", "k", 256, 320, 256, dist="codes", seed=5)
         D = torch.full((256, 320), float("nan"), dtype=torch.bfloat16, device="cuda")
         args = (256, 320, 256, to_device(x["A"]), 0, 256, to_device(x["B"]), 0, 256, to_device(x["SFA"]),
                 to_device(x["SFB"]), D, 2, 320, 0)
         if fmt is None:
             tcg.gemm_mxf4_blockscaled(*args)
+        elif fmt == "nv":
+            tcg.gemm_nvf4_blockscaled(*args)
         else:
             tcg.gemm_mxf6_blockscaled(fmt, *args)
         assert tcg.check() == 0
@@ -441,7 +449,8 @@ def test_named_entry_points(tcg, oracle_mod):
 # ------------------------------------------------------------- full-size workloads
 
 FULL = ["tile_f16_128x128x64", "bf16_4096_kmn_cta1", "tf32_2048x2048x8192", "bf16_8192_cta2",
-        "f16acc_8192_cta2", "mxf8_8192", "bf16_skinny_m16", "bf16_skinny_m128", "mxf6_e2m3_8192", "mxf4_8192"]
+        "f16acc_8192_cta2", "mxf8_8192", "bf16_skinny_m16", "bf16_skinny_m128", "mxf6_e2m3_8192", "mxf4_8192",
+        "nvf4_8192"]
 
 
 @pytest.mark.parametrize("name", FULL)

@@ -308,3 +308,40 @@ def test_packed_fetch_through_an_identity_gemm(oracle_mod, fmt, bits, one):
     swapped = codes.reshape(M, K // g, g)[:, :, ::-1].reshape(M, K)
     D2, _ = oracle_mod.gemm(M, K, K, _bitstring_pack(swapped, bits), t, 0, K, B, t, 0, K, SFA=sfa, SFB=sfb)
     assert not np.array_equal(D2, D)
+
+
+def test_ue4m3_scale_decoder_matches_torch(oracle_mod):
+    """The NVFP4 scale is the E4M3FN encoding without a sign: codes 0..127
+    decode as torch's float8_e4m3fn; codes with the top bit set are no scale."""
+    import torch
+    codes = np.arange(128, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = oracle_mod.decode_ue4m3(codes)
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    assert np.array_equal(got[~np.isnan(ref)], ref[~np.isnan(ref)])
+    assert np.all(np.isnan(oracle_mod.decode_ue4m3(np.arange(128, 256, dtype=np.uint8))))
+
+
+def test_block16_scales_identity_closed_form(oracle_mod):
+    """A = I in E2M1 with one unsigned-E4M3 scale per 16 K elements: D[m, n]
+    = sfa[m, m//16] * sfb[n, m//16] * B[n, m] exactly; a 32-wide block read
+    (the MX rule) or an A/B scale swap is caught."""
+    import synthetic as syn
+    K, N = 64, 40
+    A = syn.pack(np.where(np.eye(K, dtype=bool), 0x2, 0).astype(np.uint8), 4)
+    codes = syn.codes((N, K), 77, 4)
+    B = syn.pack(codes, 4)
+    sfa = syn.ue4m3_scales(K, K, 78)
+    sfb = syn.ue4m3_scales(N, K, 79)
+    D, _ = oracle_mod.gemm(K, N, K, A, oracle_mod.E2M1, 0, K, B, oracle_mod.E2M1, 0, K, SFA=sfa, SFB=sfb,
+                           sf_block=16, sf_kind=oracle_mod.SF_UE4M3)
+    m = np.arange(K)
+    expect = (oracle_mod.decode_ue4m3(sfa[m, m // 16])[:, None] * oracle_mod.decode_ue4m3(sfb[:, m // 16]).T
+              * oracle_mod.decode(codes, oracle_mod.E2M1).T)
+    assert np.array_equal(D, expect)
+    # planted mistake: blocks of 32 read the wrong scale for half the rows
+    sfa32 = sfa[:, ::2].copy()
+    sfb32 = sfb[:, ::2].copy()
+    D32, _ = oracle_mod.gemm(K, N, K, A, oracle_mod.E2M1, 0, K, B, oracle_mod.E2M1, 0, K, SFA=sfa32, SFB=sfb32,
+                             sf_block=32, sf_kind=oracle_mod.SF_UE4M3)
+    assert not np.array_equal(D32, D)
