@@ -555,7 +555,8 @@ def main():
                          f"{(w.M * w.K + w.N * w.K) * ESIZE[w.dtype] / 2**20:.0f} MiB",
                    "parallelism": f"replicas x{dctx.world}"},
         "pct_of_measured_peak": round(100 * rl["frac"], 2),
-        "pct_of_datasheet_dense_peak": round(100 * rl["frac_of_datasheet_dense"], 2),
+        "pct_of_datasheet_dense_peak": (round(100 * rl["frac_of_datasheet_dense"], 2)
+                                        if "frac_of_datasheet_dense" in rl else None),
         "roofline": rl,
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_val, 1), "unit": UNIT, "h2d_bytes_per_step": res["h2d"],
