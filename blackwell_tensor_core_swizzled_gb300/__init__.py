@@ -79,6 +79,8 @@ _SIGS = {
     "tcg_probe_mma_image": ([ctypes.POINTER(ProbeOperand), ctypes.POINTER(ProbeOperand), _i32, _i32, _i32, _vp,
                              _vp], _i32),
     "tcg_probe_ldmatrix_x2": ([_vp, _vp, _vp], _i32),
+    "tcg_probe_stmatrix": ([_vp, _vp, _i32, _i32, _vp, _vp], _i32),
+    "tcg_probe_ld_split": ([_vp, _i32, _i32, _i32, _vp, _vp, _vp], _i32),
     "tcg_probe_wait_timeout": ([_u64, _vp], _i32),
 }
 
@@ -309,6 +311,16 @@ def probe_mma_image(a: ProbeOperand, b: ProbeOperand, in_type, N, ksteps, D, str
 
 def probe_ldmatrix_x2(x, out, stream=None):
     return _ok(_lib.tcg_probe_ldmatrix_x2(_ptr(x), _ptr(out), _stream(stream)), "probe_ldmatrix_x2")
+
+
+def probe_stmatrix(regs, row_off, count, trans, out, stream=None):
+    return _ok(_lib.tcg_probe_stmatrix(_ptr(regs), _ptr(row_off), count, int(bool(trans)), _ptr(out),
+                                       _stream(stream)), "probe_stmatrix")
+
+
+def probe_ld_split(inp, num, imm_lanes, imm_cols, out_ld, out_st, stream=None):
+    return _ok(_lib.tcg_probe_ld_split(_ptr(inp), num, imm_lanes, imm_cols, _ptr(out_ld), _ptr(out_st),
+                                       _stream(stream)), "probe_ld_split")
 
 
 def probe_wait_timeout(timeout_ns, stream=None):

@@ -18,7 +18,10 @@
 //     hardware's descriptor walk against a layout model ("tcgen05.mma" page,
 //     "Shared descriptors are byte-stride contracts", "swizzle=4");
 //   * ldmatrix .x2 into separated register slots ("ldmatrix / stmatrix" page
-//     example);
+//     example) and stmatrix .x1/.x2/.x4 with and without .trans ("Transpose
+//     and stores");
+//   * tcgen05.ld / st .16x32bx2 split accesses ("tcgen05.ld / tcgen05.st"
+//     page, "Split accesses: 16x32bx2");
 //   * a bounded wait that runs out (failure detection without a GPU fault).
 #include <cuda_runtime.h>
 
@@ -587,6 +590,104 @@ __global__ void __launch_bounds__(128, 1) probe_mma_image_kernel(ImageOperand a,
   if (warp == 0) tmem_dealloc<1>(slot, ncols);
 }
 
+// ------------------------------------------------------------------ split accesses 16x32bx2
+
+// Every thread stores in[t*32 .. t*32+32) to TMEM lane t, columns [0, 32),
+// and zeroes columns [32, 64); each warp then loads its quadrant with
+// tcgen05.ld .16x32bx2.x<NUM> (second access IMM after the first) into
+// out_ld, stores distinct words 0x10000 * t + r + 1 with tcgen05.st
+// .16x32bx2.x<NUM> at column 32, and every thread reads columns [32, 64) of
+// its lane back into out_st.
+template <int NUM, uint32_t IMM>
+__global__ void __launch_bounds__(128, 1) probe_split_kernel(const uint32_t* in, uint32_t* out_ld, uint32_t* out_st) {
+  __shared__ uint32_t slot;
+  const int warp = threadIdx.x >> 5;
+  const int t = threadIdx.x;
+  if (warp == 0) {
+    tmem_alloc<1>(smem_u32(&slot), 64);
+    tmem_relinquish<1>();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t lane_base = slot + (static_cast<uint32_t>(32 * warp) << 16);
+  uint32_t img[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) img[j] = in[t * 32 + j];
+  stx_32x32b_x32(lane_base, img);
+#pragma unroll
+  for (int j = 0; j < 32; ++j) img[j] = 0u;
+  stx_32x32b_x32(lane_base + 32, img);
+  tc_wait_st();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  uint32_t r[NUM];
+  if constexpr (NUM == 1) ldx_16x32bx2_x1<IMM>(lane_base, r);
+  if constexpr (NUM == 2) ldx_16x32bx2_x2<IMM>(lane_base, r);
+  if constexpr (NUM == 4) ldx_16x32bx2_x4<IMM>(lane_base, r);
+  if constexpr (NUM == 8) ldx_16x32bx2_x8<IMM>(lane_base, r);
+  tc_wait_ld();
+#pragma unroll
+  for (int j = 0; j < NUM; ++j) out_ld[t * NUM + j] = r[j];
+#pragma unroll
+  for (int j = 0; j < NUM; ++j) r[j] = 0x10000u * static_cast<uint32_t>(t) + static_cast<uint32_t>(j) + 1u;
+  if constexpr (NUM == 1) stx_16x32bx2_x1<IMM>(lane_base + 32, r);
+  if constexpr (NUM == 2) stx_16x32bx2_x2<IMM>(lane_base + 32, r);
+  if constexpr (NUM == 4) stx_16x32bx2_x4<IMM>(lane_base + 32, r);
+  if constexpr (NUM == 8) stx_16x32bx2_x8<IMM>(lane_base + 32, r);
+  tc_wait_st();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  ldx_32x32b_x32(lane_base + 32, img);
+  tc_wait_ld();
+#pragma unroll
+  for (int j = 0; j < 32; ++j) out_st[t * 32 + j] = img[j];
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc<1>(slot, 64);
+}
+
+// ------------------------------------------------------------------ stmatrix
+
+// One warp: lane l holds COUNT words regs[l*4 .. l*4+COUNT) and provides the
+// shared address of row (l % (8*COUNT)) of the matrices: row_off[that row]
+// bytes (masked to a 16-byte multiple below 1024) into a zeroed 1 KB buffer; stmatrix .m8n8.x<COUNT>[.trans].b16
+// writes, and the buffer comes back in out (256 words).
+template <int COUNT, bool TRANS>
+__global__ void probe_stmatrix_kernel(const uint32_t* regs, const uint32_t* row_off, uint32_t* out) {
+  __shared__ __align__(16) uint32_t sm[256];
+  const int lane = threadIdx.x & 31;
+  for (int i = lane; i < 256; i += 32) sm[i] = 0u;
+  __syncwarp();
+  const uint32_t addr = smem_u32(sm) + (row_off[lane % (8 * COUNT)] & 1008u);
+  uint32_t r[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) r[i] = regs[lane * 4 + i];
+  if constexpr (COUNT == 1 && !TRANS)
+    asm volatile("stmatrix.sync.aligned.m8n8.x1.shared.b16 [%0], {%1};" ::"r"(addr), "r"(r[0]) : "memory");
+  if constexpr (COUNT == 1 && TRANS)
+    asm volatile("stmatrix.sync.aligned.m8n8.x1.trans.shared.b16 [%0], {%1};" ::"r"(addr), "r"(r[0]) : "memory");
+  if constexpr (COUNT == 2 && !TRANS)
+    asm volatile("stmatrix.sync.aligned.m8n8.x2.shared.b16 [%0], {%1, %2};" ::"r"(addr), "r"(r[0]), "r"(r[1])
+                 : "memory");
+  if constexpr (COUNT == 2 && TRANS)
+    asm volatile("stmatrix.sync.aligned.m8n8.x2.trans.shared.b16 [%0], {%1, %2};" ::"r"(addr), "r"(r[0]), "r"(r[1])
+                 : "memory");
+  if constexpr (COUNT == 4 && !TRANS)
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(r[0]),
+                 "r"(r[1]), "r"(r[2]), "r"(r[3])
+                 : "memory");
+  if constexpr (COUNT == 4 && TRANS)
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(r[0]),
+                 "r"(r[1]), "r"(r[2]), "r"(r[3])
+                 : "memory");
+  __syncwarp();
+  for (int i = lane; i < 256; i += 32) out[i] = sm[i];
+}
+
 // ------------------------------------------------------------------ ldmatrix
 
 // x (16,4,2) row-major words; shared layout (16,4,2):(8,1,128).  Matrix m,
@@ -844,6 +945,46 @@ extern "C" int tcg_probe_mma_image(const tcg_probe_operand* a, const tcg_probe_o
   const uint32_t idesc = tf32 ? idesc_tf32(a_mn, b_mn, 128, N) : idesc_f16(in_type == TCG_IN_BF16, true, a_mn, b_mn, 128, N);
   probe_mma_image_kernel<<<1, 128, smem, as_stream(stream)>>>(ia, ib, tf32 ? 1 : 0, idesc, N, ksteps, D,
                                                               device_error_word(dev), wait_timeout_ns());
+  return finish_launch(1);
+}
+
+extern "C" int tcg_probe_ld_split(const uint32_t* in, int num, int imm_lanes, int imm_cols, uint32_t* out_ld,
+                                  uint32_t* out_st, void* stream) {
+  if (!in || !out_ld || !out_st) return TCG_ERR_INVALID;
+  const bool num_ok = num == 1 || num == 2 || num == 4 || num == 8;
+  const bool imm_ok = (imm_lanes == 16 && (imm_cols == 0 || imm_cols == 8 || imm_cols == 16)) ||
+                      (imm_lanes == 0 && imm_cols == 16);
+  if (!num_ok || !imm_ok) return TCG_ERR_INVALID;
+  int dev;
+  if (int rc = current_device_checked(&dev)) return rc;
+  const cudaStream_t s = as_stream(stream);
+#define TCG_SPLIT_CASE(NU, IL, IC)                                                                        \
+  if (num == NU && imm_lanes == IL && imm_cols == IC) {                                                  \
+    probe_split_kernel<NU, (static_cast<uint32_t>(IL) << 16) + IC><<<1, 128, 0, s>>>(in, out_ld, out_st); \
+    return finish_launch(1);                                                                             \
+  }
+#define TCG_SPLIT_NUMS(IL, IC) \
+  TCG_SPLIT_CASE(1, IL, IC) TCG_SPLIT_CASE(2, IL, IC) TCG_SPLIT_CASE(4, IL, IC) TCG_SPLIT_CASE(8, IL, IC)
+  TCG_SPLIT_NUMS(16, 8) TCG_SPLIT_NUMS(16, 0) TCG_SPLIT_NUMS(0, 16) TCG_SPLIT_NUMS(16, 16)
+#undef TCG_SPLIT_NUMS
+#undef TCG_SPLIT_CASE
+  return TCG_ERR_INVALID;
+}
+
+extern "C" int tcg_probe_stmatrix(const uint32_t* regs, const uint32_t* row_off, int count, int trans, uint32_t* out,
+                                  void* stream) {
+  if (!regs || !row_off || !out) return TCG_ERR_INVALID;
+  if (count != 1 && count != 2 && count != 4) return TCG_ERR_INVALID;
+  int dev;
+  if (int rc = current_device_checked(&dev)) return rc;
+  const cudaStream_t s = as_stream(stream);
+  if (count == 1 && !trans) probe_stmatrix_kernel<1, false><<<1, 32, 0, s>>>(regs, row_off, out);
+  else if (count == 1) probe_stmatrix_kernel<1, true><<<1, 32, 0, s>>>(regs, row_off, out);
+  else if (count == 2 && !trans) probe_stmatrix_kernel<2, false><<<1, 32, 0, s>>>(regs, row_off, out);
+  else if (count == 2) probe_stmatrix_kernel<2, true><<<1, 32, 0, s>>>(regs, row_off, out);
+  else if (count == 4 && !trans) probe_stmatrix_kernel<4, false><<<1, 32, 0, s>>>(regs, row_off, out);
+  else if (count == 4) probe_stmatrix_kernel<4, true><<<1, 32, 0, s>>>(regs, row_off, out);
+  else return TCG_ERR_INVALID;
   return finish_launch(1);
 }
 

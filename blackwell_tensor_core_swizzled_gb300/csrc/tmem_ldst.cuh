@@ -162,4 +162,55 @@ __device__ __forceinline__ void ldx_16x256b_x4(uint32_t taddr, uint32_t* r) {
                : "r"(taddr));
 }
 
+
+// .16x32bx2: two 16-lane accesses in one instruction ("tcgen05.ld /
+// tcgen05.st" page, "Split accesses: 16x32bx2"): lane l reads / writes row
+// l % 16 of access l / 16, columns [0, N); access 1 starts at the TMEM
+// address plus the immediate IMM (lane offset in bits 16 and up, column
+// offset in the low bits).
+template <uint32_t IMM>
+__device__ __forceinline__ void ldx_16x32bx2_x1(uint32_t taddr, uint32_t* r) {
+  asm volatile("tcgen05.ld.sync.aligned.16x32bx2.x1.b32 {%0}, [%1], %2;" : "=r"(r[0]) : "r"(taddr), "n"(IMM));
+}
+template <uint32_t IMM>
+__device__ __forceinline__ void ldx_16x32bx2_x2(uint32_t taddr, uint32_t* r) {
+  asm volatile("tcgen05.ld.sync.aligned.16x32bx2.x2.b32 {%0,%1}, [%2], %3;"
+               : "=r"(r[0]), "=r"(r[1])
+               : "r"(taddr), "n"(IMM));
+}
+template <uint32_t IMM>
+__device__ __forceinline__ void ldx_16x32bx2_x4(uint32_t taddr, uint32_t* r) {
+  asm volatile("tcgen05.ld.sync.aligned.16x32bx2.x4.b32 {%0,%1,%2,%3}, [%4], %5;"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(taddr), "n"(IMM));
+}
+template <uint32_t IMM>
+__device__ __forceinline__ void ldx_16x32bx2_x8(uint32_t taddr, uint32_t* r) {
+  asm volatile("tcgen05.ld.sync.aligned.16x32bx2.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8], %9;"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr), "n"(IMM));
+}
+template <uint32_t IMM>
+__device__ __forceinline__ void stx_16x32bx2_x1(uint32_t taddr, const uint32_t* r) {
+  asm volatile("tcgen05.st.sync.aligned.16x32bx2.x1.b32 [%0], %1, {%2};" ::"r"(taddr), "n"(IMM), "r"(r[0]) : "memory");
+}
+template <uint32_t IMM>
+__device__ __forceinline__ void stx_16x32bx2_x2(uint32_t taddr, const uint32_t* r) {
+  asm volatile("tcgen05.st.sync.aligned.16x32bx2.x2.b32 [%0], %1, {%2,%3};" ::"r"(taddr), "n"(IMM), "r"(r[0]),
+               "r"(r[1])
+               : "memory");
+}
+template <uint32_t IMM>
+__device__ __forceinline__ void stx_16x32bx2_x4(uint32_t taddr, const uint32_t* r) {
+  asm volatile("tcgen05.st.sync.aligned.16x32bx2.x4.b32 [%0], %1, {%2,%3,%4,%5};" ::"r"(taddr), "n"(IMM), "r"(r[0]),
+               "r"(r[1]), "r"(r[2]), "r"(r[3])
+               : "memory");
+}
+template <uint32_t IMM>
+__device__ __forceinline__ void stx_16x32bx2_x8(uint32_t taddr, const uint32_t* r) {
+  asm volatile("tcgen05.st.sync.aligned.16x32bx2.x8.b32 [%0], %1, {%2,%3,%4,%5,%6,%7,%8,%9};" ::"r"(taddr), "n"(IMM),
+               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
+
 }  // namespace tcg

@@ -448,6 +448,37 @@ int tcg_probe_mma_image(const tcg_probe_operand* a, const tcg_probe_operand* b, 
  * sentinel 4294966519; out is 32 x 12 words. */
 int tcg_probe_ldmatrix_x2(const uint32_t* x, uint32_t* out, void* stream);
 
+/* "ldmatrix / stmatrix" page, "Address providers and result owners" and
+ * "Transpose and stores": one warp issues stmatrix .m8n8.x<count>[.trans].b16
+ * (count 1, 2 or 4; trans 0 or 1) into a zeroed 1 KB shared buffer.  `regs`
+ * (device, 128 words) gives lane l its registers regs[4l .. 4l+count);
+ * `row_off` (device, 8*count words) gives the byte offset in the buffer of
+ * row r of matrix m at row_off[8m + r]; lane l supplies row_off[l % (8*count)]
+ * (so x1 / x2 repeat valid addresses).  Offsets must be multiples of 16 below
+ * 1024: the kernel masks each with 1008, so no access leaves the buffer, and
+ * a caller that breaks the rule simply gets a different image.  `out`
+ * (device, 256 words) receives the buffer.  Returns TCG_ERR_INVALID for a
+ * null pointer or another count. */
+int tcg_probe_stmatrix(const uint32_t* regs, const uint32_t* row_off, int count, int trans, uint32_t* out,
+                       void* stream);
+
+/* "tcgen05.ld / tcgen05.st" page, "Split accesses: 16x32bx2": lane l owns
+ * (access l/16, row l%16, column r); access 1 starts at the first address
+ * plus the immediate (imm_lanes << 16) + imm_cols.  One CTA of 128 threads
+ * allocates 64 columns; thread t stores in[32t .. 32t+32) (device, 128 x 32
+ * words) to its TMEM lane t, columns 0..31, and zeroes columns 32..63.  Warp
+ * w then issues, at lane 32w column 0,
+ *     tcgen05.ld.16x32bx2.x<num>   -> out_ld[t*num + r]      (128 x num words)
+ * and, at lane 32w column 32, stores the words 0x10000*t + r + 1 with
+ *     tcgen05.st.16x32bx2.x<num>;
+ * every thread then reads columns 32..63 of its lane into out_st[32t + c]
+ * (128 x 32 words).  num in {1, 2, 4, 8}; (imm_lanes, imm_cols) one of
+ * (16, 8), (16, 0), (0, 16), (16, 16) -- each keeps both accesses inside the
+ * warp's 32 lanes and the allocation.  Anything else: TCG_ERR_INVALID, no
+ * launch. */
+int tcg_probe_ld_split(const uint32_t* in, int num, int imm_lanes, int imm_cols, uint32_t* out_ld,
+                       uint32_t* out_st, void* stream);
+
 /* Failure-detection probe: launches one CTA that waits on an mbarrier no one
  * arrives at, bounded by `timeout_ns`; the kernel records TCG_ERR_TIMEOUT in
  * the error word and returns.  Returns the launch status; tcg_check() then

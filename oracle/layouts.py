@@ -271,6 +271,42 @@ def ld_image(shape: str, n: int, tmem_word):
     return tmem_word(row, col)
 
 
+def split_owner(lane, reg, imm_lanes: int, imm_cols: int):
+    """Split accesses ``16x32bx2`` ("tcgen05.ld / tcgen05.st" page, "Split
+    accesses: 16x32bx2"): lane l owns (access l//16, row l%16, column r), and
+    access 1 starts at the first address plus the immediate
+    ``(imm_lanes << 16) + imm_cols`` -- lane 16 adds no sixteen-row shift of
+    its own.  Returns the (lane, column) offset from the first address."""
+    l = np.asarray(lane)
+    r = np.asarray(reg)
+    access = l // 16
+    return l % 16 + access * imm_lanes + 0 * r, r + access * imm_cols + 0 * l
+
+
+def split_load(num: int, imm_lanes: int, imm_cols: int, tmem_word):
+    """Registers (32, num) that ``tcgen05.ld.16x32bx2.x<num>`` gives a warp,
+    with ``tmem_word(lane, col)`` relative to the first address."""
+    lanes = np.arange(32)[:, None]
+    rr = np.arange(num)[None, :]
+    return tmem_word(*split_owner(lanes, rr, imm_lanes, imm_cols))
+
+
+def split_store(regs, imm_lanes: int, imm_cols: int, shape=(32, 32)):
+    """Tensor-memory image (zero where nothing is written) that
+    ``tcgen05.st.16x32bx2.x<num>`` of ``regs`` (32, num) leaves, relative to
+    the first address.  Two registers landing on one cell is an error here:
+    the page gives such a store no defined result."""
+    regs = np.asarray(regs)
+    lanes = np.arange(32)[:, None]
+    rr = np.arange(regs.shape[1])[None, :]
+    row, col = split_owner(lanes, rr, imm_lanes, imm_cols)
+    if np.unique(row * 4096 + col).size != row.size:
+        raise ValueError("the two accesses overlap")
+    img = np.zeros(shape, dtype=regs.dtype)
+    img[row, col] = regs
+    return img
+
+
 def layout_b_position(i, j):
     """Layout B ("tcgen05.ld / tcgen05.st" page, example): logical [i, j] of a
     (64, 128) tile sits at lane i + 64*(j//64), column j % 64."""
@@ -337,6 +373,35 @@ def ldmatrix_load(shared_rows, count: int, trans: bool = False):
                     hi = halves[row][2 * word + 1]
                 regs[lane][reg] = lo | (hi << 16)
     return regs
+
+
+def stmatrix_store(regs, count: int, trans: bool = False):
+    """Simulate ``stmatrix.m8n8.x<count>[.trans].b16`` ("Transpose and
+    stores": the register image of the load is the store's input, each
+    provider's row address its output).  ``regs[lane][matrix]`` are b32 ints;
+    returns rows[matrix][row] = the four b32 words written to the 16-byte row
+    whose address lane 8*matrix + row provides.  Register word
+    (matrix, row, word) is lane 4*row + word's ``matrix``-th register; with
+    .trans, shared element (r, c) of a matrix receives register element
+    (c, r) of 16-bit values."""
+
+    def reg_half(m, row, c):
+        return (regs[4 * row + c // 2][m] >> (16 * (c % 2))) & 0xFFFF
+
+    rows = []
+    for m in range(count):
+        mat = []
+        for r in range(8):
+            words = []
+            for w in range(4):
+                if trans:
+                    lo, hi = reg_half(m, 2 * w, r), reg_half(m, 2 * w + 1, r)
+                else:
+                    lo, hi = reg_half(m, r, 2 * w), reg_half(m, r, 2 * w + 1)
+                words.append(lo | (hi << 16))
+            mat.append(words)
+        rows.append(mat)
+    return rows
 
 
 # ---------------------------------------------------------------------------

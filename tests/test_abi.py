@@ -99,6 +99,13 @@ def test_host_validation_rejects_bad_arguments(tcg):
     # .ws probe: N must be one of the weight-stationary widths 64 / 128 / 256
     for n in (32, 96, 512):
         assert tcg.raw_call("tcg_probe_mma_tile_ws", 0x10000, 0x20000, n, 64, 0, 0x30000, None) == tcg.ERR_INVALID
+    # split-access probe: repeat counts 1/2/4/8 and the four in-bounds immediates only
+    for num, il, ic in ((3, 16, 8), (16, 16, 8), (4, 16, 4), (4, 0, 8), (4, 8, 0), (8, 32, 0)):
+        assert tcg.raw_call("tcg_probe_ld_split", 0x10000, num, il, ic, 0x20000, 0x30000, None) == tcg.ERR_INVALID
+    assert tcg.raw_call("tcg_probe_ld_split", None, 4, 16, 8, 0x20000, 0x30000, None) == tcg.ERR_INVALID
+    # stmatrix probe: x1 / x2 / x4 only
+    for count in (0, 3, 8):
+        assert tcg.raw_call("tcg_probe_stmatrix", 0x10000, 0x20000, count, 0, 0x30000, None) == tcg.ERR_INVALID
 
 
 def test_empty_problems_are_noops(tcg):

@@ -248,6 +248,45 @@ def test_ldmatrix_x2_page_example(tcg):
     assert np.array_equal(_np(out).astype(np.uint64), expected)
 
 
+@pytest.mark.parametrize("count", [1, 2, 4])
+@pytest.mark.parametrize("trans", [False, True])
+def test_stmatrix_rows_land_at_provider_addresses(tcg, count, trans):
+    # rows scattered over a 1 KB buffer in a seeded order with gaps between them
+    rng = np.random.default_rng(100 + 2 * count + int(trans))
+    slots = rng.permutation(64)[:8 * count]
+    row_off = (16 * slots).astype(np.uint32)
+    regs = rng.integers(0, 2**32, size=(32, 4), dtype=np.uint64)
+    out = torch.zeros(256, dtype=torch.int32, device="cuda")
+    tcg.probe_stmatrix(_u32(regs.astype(np.uint32).reshape(-1)), _u32(row_off), count, trans, out)
+    assert tcg.check() == 0
+    rows = L.stmatrix_store([[int(v) for v in regs[l, :count]] for l in range(32)], count, trans)
+    expected = np.zeros(256, dtype=np.uint64)
+    for m in range(count):
+        for r in range(8):
+            expected[row_off[8 * m + r] // 4 + np.arange(4)] = rows[m][r]
+    assert np.array_equal(_np(out).astype(np.uint64), expected)
+
+
+@pytest.mark.parametrize("num", [1, 2, 4, 8])
+@pytest.mark.parametrize("imm", [(16, 8), (16, 0), (0, 16), (16, 16)])
+def test_split_16x32bx2_load_and_store(tcg, num, imm):
+    il, ic = imm
+    rng = np.random.default_rng(7 * num + il + ic)
+    image = rng.integers(0, 2**32, size=(128, 32), dtype=np.uint64).astype(np.uint32)
+    out_ld = torch.zeros(128 * num, dtype=torch.int32, device="cuda")
+    out_st = torch.full((128 * 32,), -1, dtype=torch.int32, device="cuda")
+    tcg.probe_ld_split(_u32(image.reshape(-1)), num, il, ic, out_ld, out_st)
+    assert tcg.check() == 0
+    got_ld = _np(out_ld).reshape(128, num)
+    got_st = _np(out_st).reshape(128, 32)
+    for w in range(4):
+        exp = L.split_load(num, il, ic, lambda r, c: image[32 * w + r, c])
+        assert np.array_equal(got_ld[32 * w:32 * w + 32], exp), (num, imm, w)
+        t = 32 * w + np.arange(32)[:, None]
+        regs = (0x10000 * t + np.arange(num)[None, :] + 1).astype(np.uint64)
+        assert np.array_equal(got_st[32 * w:32 * w + 32].astype(np.uint64), L.split_store(regs, il, ic)), (num, imm, w)
+
+
 # ------------------------------------------------------------- failure detection
 
 def test_bounded_wait_reports_timeout_and_context_survives(tcg):

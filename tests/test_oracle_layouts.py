@@ -188,6 +188,72 @@ def test_ldmatrix_address_providers_and_trans():
         assert lo == 16 * (2 * w) + row and hi == 16 * (2 * w + 1) + row
 
 
+def test_stmatrix_inverts_ldmatrix():
+    # "Transpose and stores": stmatrix takes the load's register image as input
+    # and writes each provider's row, so a store followed by a load (same count,
+    # same .trans) returns the registers, and a load then a store the rows.
+    rng = np.random.default_rng(11)
+    for count in (1, 2, 4):
+        for trans in (False, True):
+            regs = [[int(v) for v in rng.integers(0, 2**32, size=count, dtype=np.uint64)] for _ in range(32)]
+            rows = L.stmatrix_store(regs, count, trans)
+            assert L.ldmatrix_load(rows, count, trans) == regs
+            rows2 = [[[int(v) for v in rng.integers(0, 2**32, size=4, dtype=np.uint64)] for _ in range(8)]
+                     for _ in range(count)]
+            assert L.stmatrix_store(L.ldmatrix_load(rows2, count, trans), count, trans) == rows2
+
+
+def test_stmatrix_owners_and_trans_direct():
+    # non-transposed: row r word w of matrix m comes whole from lane 4r + w's
+    # m-th register ("Register word (matrix,row,word) belongs to lane 4*row+word")
+    regs = [[1000 * lane + m for m in range(4)] for lane in range(32)]
+    rows = L.stmatrix_store(regs, 4)
+    for m, r, w in itertools.product(range(4), range(8), range(4)):
+        assert rows[m][r][w] == 1000 * (4 * r + w) + m
+    # .trans of 16-bit elements: register element (i, j) = 16i + j (lane 4i + j//2,
+    # half j%2) lands at shared element (j, i)
+    regs = [[(16 * (lane // 4) + 2 * (lane % 4)) | ((16 * (lane // 4) + 2 * (lane % 4) + 1) << 16)]
+            for lane in range(32)]
+    rows = L.stmatrix_store(regs, 1, trans=True)
+    for r, c in itertools.product(range(8), range(8)):
+        assert (rows[0][r][c // 2] >> (16 * (c % 2))) & 0xFFFF == 16 * c + r
+
+
+# ------------------------------------------------------------ split accesses
+
+SPLIT_IMMS = [(16, 8), (16, 0), (0, 16), (16, 16)]
+
+
+def test_split_page_example_quadrants():
+    # "Split accesses: 16x32bx2" example: .x4 with imm_half_splitoff (16 << 16) + 8
+    # reads mem[:, :16, :4] for the first access and mem[:, 16:32, 8:12] for the second
+    row, col = L.split_owner(np.arange(32)[:, None], np.arange(4)[None, :], 16, 8)
+    assert set(zip(row[:16].ravel(), col[:16].ravel())) == {(i, j) for i in range(16) for j in range(4)}
+    assert set(zip(row[16:].ravel(), col[16:].ravel())) == {(i, j) for i in range(16, 32) for j in range(8, 12)}
+    # lane l owns (access l//16, row l%16, column r)
+    assert np.array_equal(row, np.arange(32)[:, None] % 16 + 16 * (np.arange(32)[:, None] // 16) + 0 * col)
+    assert np.array_equal(col, np.arange(4)[None, :] + 8 * (np.arange(32)[:, None] // 16))
+
+
+def test_split_with_sixteen_lane_offset_is_the_32_lane_shape():
+    # immediate (16 << 16) + 0: the two 16-lane accesses stack into the 32x32b image
+    for num in (1, 2, 4, 8):
+        lanes, regs = np.arange(32)[:, None], np.arange(num)[None, :]
+        assert all(np.array_equal(a, b) for a, b in
+                   zip(L.split_owner(lanes, regs, 16, 0), L.ld_owner("32x32b", lanes, regs)))
+
+
+def test_split_store_inverts_split_load():
+    rng = np.random.default_rng(5)
+    for (il, ic), num in itertools.product(SPLIT_IMMS, (1, 2, 4, 8)):
+        regs = rng.integers(1, 2**32, size=(32, num), dtype=np.uint64)
+        img = L.split_store(regs, il, ic)
+        assert np.count_nonzero(img) == 32 * num
+        assert np.array_equal(L.split_load(num, il, ic, lambda r, c: img[r, c]), regs)
+    with pytest.raises(ValueError):
+        L.split_store(np.ones((32, 4), dtype=np.uint64), 0, 2)  # second access overlaps the first
+
+
 # ------------------------------------------------------------ scale factors
 
 def test_sf_chunk_offset_through_cp_warpx4_lands_where_mma_reads():
