@@ -187,7 +187,7 @@ def run_workload(tcg, torch, w, steps, warmup, dist_ctx, measure_e2e=True):
         SFA = to_dev(x["SFA"], torch)
         SFB = to_dev(x["SFB"], torch)
         fmt = IN_TYPE[w.dtype]
-        tn = tcg.mxf8_tile_n(M, N, K, b_maj, w.cta_group)
+        tn = tcg.tile_n(fmt, M, N, K, b_maj, w.cta_group)
         ia = torch.empty(tcg.scale_image_bytes(fmt, M, K, 128), dtype=torch.uint8, device="cuda")
         ib = torch.empty(tcg.scale_image_bytes(fmt, N, K, tn), dtype=torch.uint8, device="cuda")
 

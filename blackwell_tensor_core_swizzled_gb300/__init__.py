@@ -60,6 +60,7 @@ _SIGS = {
     "tcg_gemm": ([ctypes.POINTER(GemmArgs), _vp], _i32),
     "tcg_mxf8_scale_image_bytes": ([_i64, _i64, _i32], _i64),
     "tcg_mxf8_tile_n": ([_i64, _i64, _i64, _i32, _i32], _i32),
+    "tcg_tile_n": ([_i32, _i64, _i64, _i64, _i32, _i32], _i32),
     "tcg_mxf8_prepare_scales": ([_vp, _i64, _i64, _i32, _vp, _vp], _i32),
     "tcg_mxf8_prepare_scales_ab": ([_vp, _i64, _vp, _vp, _i64, _i32, _vp, _i64, _vp], _i32),
     "tcg_check": ([_vp], _i32),
@@ -225,6 +226,10 @@ def mxf8_scale_image_bytes(rows, K, tile_rows) -> int:
 
 def mxf8_tile_n(M, N, K, b_major=K_MAJOR, cta_group=0) -> int:
     return _lib.tcg_mxf8_tile_n(M, N, K, b_major, cta_group)
+
+
+def tile_n(fmt, M, N, K, b_major=K_MAJOR, cta_group=0) -> int:
+    return _lib.tcg_tile_n(fmt, M, N, K, b_major, cta_group)
 
 
 def mxf8_prepare_scales(sf, rows, K, tile_rows, img, stream=None):

@@ -28,8 +28,9 @@ enum F16Variant {
 KernelInfo kinfo_f16(int cta_group, F16Variant v = F16_WIDE);
 KernelInfo kinfo_tf32(int cta_group);
 KernelInfo kinfo_mxf8(int cta_group);  // BN 256, one accumulator (single CTA or CTA pair)
-// packed FP4: kind::mxf4 (scale_vec::2X, e8m0) or kind::mxf4nvf4 (scale_vec::4X, UE4M3)
-KernelInfo kinfo_fp4(int cta_group, bool nvf4);
+// packed FP4: kind::mxf4 (scale_vec::2X, e8m0) or kind::mxf4nvf4 (scale_vec::4X,
+// UE4M3); wide: CTA pairs with 256 x 384 tiles (two MMAs per K step), K-major B
+KernelInfo kinfo_fp4(int cta_group, bool nvf4, bool wide = false);
 
 // How a block-scaled format's scales are staged: K elements per scale, K
 // steps (of four scales per row, one 512-byte chunk per 128 rows) per ring

@@ -171,9 +171,17 @@ __device__ __forceinline__ void trace_stamp(const GemmParams& p, int slot) {
 // A are staged per ring stage, so many more stages fit; the MMA still reads a
 // 128-row operand, whose rows beyond A_ROWS are whatever follows in shared
 // memory and only feed accumulator rows >= M, which are never stored.
+//
+// BN = 384 (block-scaled CTA pairs, K-major B): each K step issues two MMAs,
+// N = 256 into accumulator columns 0..255 and N = 128 into 256..383.  A pair
+// MMA of N columns reads N/2 B rows from each CTA at the same shared offset,
+// the first CTA's giving columns [0, N/2); so CTA r stages tile columns
+// 128r .. 128r+127 in its B rows 0..127 and 256+64r .. 256+64r+63 in rows
+// 128..191 (three 64-row boxes), and accumulator column c is tile column c.
 template <int CG, int BN, int ACC, int STAGES, int KIND, int A_ROWS = 128>
 struct GemmCfg {
   static constexpr bool SCALED = KIND >= KIND_MXF8;  // block-scaled kinds
+  static constexpr bool WIDE = BN > 256;             // two MMAs per K step
   static constexpr int BM = 128;            // accumulator rows per CTA
   static constexpr int BN_LOCAL = BN / CG;  // B rows staged per CTA
   static constexpr int A_BYTES = A_ROWS * 128;
@@ -237,7 +245,8 @@ struct GemmCfg {
   __host__ __device__ static constexpr int epi_warps(int sf_mode) {
     return SCALED && sf_mode != SF_BY_WARPS ? 8 : 4;
   }
-  static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "epilogue drains 32-column chunks");
+  static_assert(BN % 32 == 0 && BN >= 32 && (BN <= 256 || (BN == 384 && CG == 2 && SCALED && ACC == 1)),
+                "epilogue drains 32-column chunks; MMA N <= 256 except the two-MMA pair tile");
   static_assert(BN % (16 * CG) == 0, "MMA N constraint / per-CTA B split");
   static_assert(ACC * BN + (SCALED ? SF_SLOTS * SF_SLOT_COLS : 0) <= TMEM_COLS, "TMEM budget");
   static_assert(!SCALED || (SF_SLOTS >= 1 && SF_SLOTS <= STAGES), "scale slots");
@@ -577,7 +586,13 @@ __global__ void __launch_bounds__(KIND >= KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
           } else {
             for (int i = 0; i < p.a_boxes; ++i) tma_load<CG>(sa + i * p.a_box_bytes, &p.tmap_a, m0 + i * p.a_box_mn, k0, fb);
           }
-          if (!p.b_mn_major) {
+          if constexpr (C::WIDE) {
+            // 64-row boxes: tile columns 128r + [0, 128) and 256 + 64r + [0, 64)
+            const int nb = nt * BN;
+            tma_load<CG>(sb, &p.tmap_b, k0, nb + 128 * static_cast<int>(rank), fb);
+            tma_load<CG>(sb + 64 * 128, &p.tmap_b, k0, nb + 128 * static_cast<int>(rank) + 64, fb);
+            tma_load<CG>(sb + 128 * 128, &p.tmap_b, k0, nb + 256 + 64 * static_cast<int>(rank), fb);
+          } else if (!p.b_mn_major) {
             tma_load<CG>(sb, &p.tmap_b, k0, n0, fb);
           } else {
             for (int i = 0; i < p.b_boxes; ++i) tma_load<CG>(sb + i * p.b_box_bytes, &p.tmap_b, n0 + i * p.b_box_mn, k0, fb);
@@ -655,6 +670,11 @@ __global__ void __launch_bounds__(KIND >= KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
 #pragma unroll
       for (int j = 0; j < C::KSTEPS; ++j)
         idesc_j[j] = C::SCALED ? (p.idesc | idesc_sf_ids(C::sf_id(j), C::sf_id(j))) : p.idesc;
+      // BN = 384: the second MMA of a K step has N = 128 (p.idesc carries 256),
+      // reads B rows 128.. (16 KiB on) and the third SFB chunk
+      constexpr uint32_t N_FIELD = 0x3Fu << 17;
+      constexpr uint32_t N128 = (128u >> 3) << 17;
+      constexpr uint64_t B_HI_OFF = (128u * 128u) >> 4;
       // block scales staged by other threads: wait for sf_ready[slot] too
       constexpr bool sf_wait = C::SCALED && SFM != SF_BY_MMA;
       constexpr bool sf_by_mma = C::SCALED && SFM == SF_BY_MMA;
@@ -734,6 +754,17 @@ __global__ void __launch_bounds__(KIND >= KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
               mma_f16<CG>(d_tmem, ad, bd, idesc_j[j], acc);
             else
               mma_tf32<CG>(d_tmem, ad, bd, idesc_j[j], acc);
+            if constexpr (C::WIDE) {
+              // the same kind as the first issue (WIDE implies a block-scaled kind)
+              const uint32_t id2 = (idesc_j[j] & ~N_FIELD) | N128;
+              const uint32_t sfb2 = sf_col + C::sfb_col(j) + 8;
+              if constexpr (KIND == KIND_MXF8)
+                mma_mxf8<CG>(d_tmem + 256, ad, bd + B_HI_OFF, id2, sf_col + C::sfa_col(j), sfb2, acc);
+              else if constexpr (KIND == KIND_MXF4)
+                mma_mxf4<CG>(d_tmem + 256, ad, bd + B_HI_OFF, id2, sf_col + C::sfa_col(j), sfb2, acc);
+              else
+                mma_nvf4<CG>(d_tmem + 256, ad, bd + B_HI_OFF, id2, sf_col + C::sfa_col(j), sfb2, acc);
+            }
           }
           tc_commit<CG>(empty_bar(s));
           }
@@ -844,10 +875,8 @@ __global__ void __launch_bounds__(KIND >= KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
           const uint32_t col =
               tmem_base + (static_cast<uint32_t>(32 * q) << 16) + C::SF_COL0 + slot * C::SF_SLOT_COLS;
           tmem_st_32x32b_x4(col, sf[lane]);  // SFA: 4 columns
-          if constexpr (C::SFB_CHUNKS == 2)
-            tmem_st_32x32b_x8(col + 4, sf[32 + lane], sf[64 + lane]);  // SFB: 8 columns
-          else
-            tmem_st_32x32b_x4(col + 4, sf[32 + lane]);
+#pragma unroll
+          for (int c = 0; c < C::SFB_CHUNKS; ++c) tmem_st_32x32b_x4(col + 4 + 4 * c, sf[32 * (1 + c) + lane]);  // SFB
           tc_wait_st();
           tc_fence_before();
           __syncwarp();

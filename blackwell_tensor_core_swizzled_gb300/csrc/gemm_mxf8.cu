@@ -27,8 +27,19 @@ KernelInfo kinfo_mxf8(int cta_group) {
 // Packed FP4 (kind::mxf4 with e8m0 scales per 32, kind::mxf4nvf4 with
 // unsigned E4M3 scales per 16): a stage carries 256 K of two-per-byte values
 // and 8 or 16 scales per row (2 or 4 chunks), so five stages fit for CTA
-// pairs (three for single NVFP4 CTAs, whose 256-row B tile is twice as large).
-KernelInfo kinfo_fp4(int cta_group, bool nvf4) {
+// pairs (three for single NVFP4 CTAs, whose 256-row B tile is twice as large)
+// and four for the 256 x 384 pair tiles (192 B rows per CTA).
+KernelInfo kinfo_fp4(int cta_group, bool nvf4, bool wide) {
+  if (cta_group == 2 && wide && nvf4) {
+    using C = GemmCfg<2, 384, 1, 4, KIND_NVF4>;
+    return {reinterpret_cast<const void*>(&gemm_kernel<2, 384, 1, 4, KIND_NVF4>), C::SMEM_BYTES, 2, 384, KIND_NVF4,
+            C::THREADS};
+  }
+  if (cta_group == 2 && wide) {
+    using C = GemmCfg<2, 384, 1, 4, KIND_MXF4>;
+    return {reinterpret_cast<const void*>(&gemm_kernel<2, 384, 1, 4, KIND_MXF4>), C::SMEM_BYTES, 2, 384, KIND_MXF4,
+            C::THREADS};
+  }
   if (cta_group == 2 && nvf4) {
     using C = GemmCfg<2, 256, 1, 5, KIND_NVF4>;
     return {reinterpret_cast<const void*>(&gemm_kernel<2, 256, 1, 5, KIND_NVF4>), C::SMEM_BYTES, 2, 256, KIND_NVF4,

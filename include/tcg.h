@@ -210,7 +210,7 @@ typedef struct {
   const uint8_t* SFA; const uint8_t* SFB;
   /* ... or images already built by tcg_mxf8_prepare_scales (then SFA/SFB must
    * be NULL).  The images must have been prepared for the same M/N/K and the
-   * tile_n this call resolves to (tcg_mxf8_tile_n). */
+   * tile_n this call resolves to (tcg_tile_n). */
   const uint8_t* SFA_img; const uint8_t* SFB_img;
   void* D; tcg_dtype d_type; int64_t ldd;
   tcg_dtype acc_type;
@@ -268,7 +268,14 @@ int64_t tcg_mxf8_scale_image_bytes(int64_t rows, int64_t K, int tile_rows);
 int64_t tcg_scale_image_bytes(tcg_input fmt, int64_t rows, int64_t K, int tile_rows);
 
 /* tile_rows the GEMM uses for SFA (always 128 per CTA) and SFB (the N tile),
- * for a given problem and cta_group request (0 = auto). */
+ * for a given block-scaled format, problem and cta_group request (0 = auto):
+ * 256, or 384 for packed FP4 (TCG_IN_E2M1, TCG_IN_NVF4) on CTA pairs with
+ * K-major B and at least 300 tiles of 256 x 384.  Depends on the arguments
+ * alone (no device query).  TCG_ERR_INVALID for a format without block
+ * scales. */
+int tcg_tile_n(tcg_input fmt, int64_t M, int64_t N, int64_t K, tcg_major b_major, int cta_group);
+
+/* tcg_tile_n for TCG_IN_E4M3. */
 int tcg_mxf8_tile_n(int64_t M, int64_t N, int64_t K, tcg_major b_major, int cta_group);
 
 /* Device-side rearrangement: `sf` plain [rows][ceil(K/32)] (device) -> `img`
@@ -287,7 +294,7 @@ int tcg_mxf8_prepare_scales_ab(const uint8_t* SFA, int64_t M, uint8_t* SFA_img,
 /* tcg_mxf8_prepare_scales_ab for any block-scaled format: plain scales of fmt
  * (e8m0 per 32, or unsigned E4M3 per 16 for TCG_IN_NVF4) into the images
  * tcg_gemm reads (sizes from tcg_scale_image_bytes; tile_n from
- * tcg_mxf8_tile_n, which holds for every block-scaled format). */
+ * tcg_tile_n for the same format). */
 int tcg_prepare_scales_ab(tcg_input fmt, const uint8_t* SFA, int64_t M, uint8_t* SFA_img,
                           const uint8_t* SFB, int64_t N, int tile_n, uint8_t* SFB_img,
                           int64_t K, void* stream);

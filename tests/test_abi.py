@@ -121,10 +121,20 @@ def test_scale_image_sizes(tcg):
     assert tcg.mxf8_scale_image_bytes(300, 96, 128) == 1 * 3 * 512
     assert tcg.mxf8_scale_image_bytes(8192, 8192, 256) == 64 * 32 * 2 * 512
     # N = 256 tiles for one CTA and for a pair (a pair's MN-major B half tile
-    # is one whole 128-byte swizzle span of E4M3)
+    # is one whole 128-byte swizzle span of E4M3); pairs with K-major B over
+    # at least 300 tiles of 256 x 384 take those
     for cg in (0, 1, 2):
         assert tcg.mxf8_tile_n(8192, 8192, 8192, tcg.K_MAJOR, cg) == 256
         assert tcg.mxf8_tile_n(8192, 8192, 8192, tcg.MN_MAJOR, cg) == 256
+        for fmt in (tcg.IN_E5M2, tcg.IN_E3M2, tcg.IN_E2M3):
+            assert tcg.tile_n(fmt, 8192, 8192, 8192, tcg.K_MAJOR, cg) == 256
+        # packed FP4 pairs with K-major B over at least 300 tiles of 256 x 384
+        for fmt in (tcg.IN_E2M1, tcg.IN_NVF4):
+            assert tcg.tile_n(fmt, 8192, 8192, 8192, tcg.K_MAJOR, cg) == (256 if cg == 1 else 384)
+    assert tcg.tile_n(tcg.IN_E2M1, 4096, 4096, 4096, tcg.K_MAJOR, 2) == 256      # 16 x 11 = 176 tiles
+    assert tcg.tile_n(tcg.IN_NVF4, 2600, 10668, 256, tcg.K_MAJOR, 0) == 384      # 11 x 28 = 308
+    assert tcg.tile_n(tcg.IN_BF16, 8192, 8192, 8192, tcg.K_MAJOR, 0) == tcg.ERR_INVALID
+    assert tcg.scale_image_bytes(tcg.IN_E2M1, 8192, 8192, 384) == 32 * 22 * 3 * 2 * 512
 
 
 @pytest.mark.skipif(os.environ.get("CUDA_VISIBLE_DEVICES_FORCE_GPU") is not None, reason="GPU present")

@@ -11,7 +11,7 @@ import pytest
 import torch
 
 import synthetic as syn
-from gpu_helpers import TAU, assert_parity, make_case, oracle_rows, run_gpu, sample_rows, to_device
+from gpu_helpers import IN_TYPE, TAU, assert_parity, make_case, oracle_rows, run_gpu, sample_rows, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -444,6 +444,49 @@ def test_named_entry_points(tcg, oracle_mod):
     assert tcg.check() == 0
     ref, S = oracle_rows(oracle_mod, x)
     assert_parity(D.double().cpu().numpy(), ref, S, TAU["f32"], "gemm_mxf8_blockscaled", "bf16")
+
+
+# ------------------------------------------------------------- 256 x 384 pair tiles
+
+# Packed-FP4 CTA pairs over at least 300 tiles of 256 x 384 take the two-MMA
+# tile (N = 256 then N = 128 per K step).  M = 2600 leaves the last pair
+# tile's second CTA wholly beyond M; N = 10668 ends on a tile whose 300
+# columns reach into the second MMA's first CTA half.
+WIDE = [
+    # dtype, K, out, split
+    ("e2m1", 320, "bf16", 0),
+    ("e2m1", 256, "f32", 0),
+    ("e2m1", 1024, "f32", 3),
+    ("nvf4", 512, "bf16", 0),
+    ("nvf4", 256, "f32", 0),
+    ("nvf4", 768, "bf16", 2),
+]
+
+
+@pytest.mark.parametrize("dtype,K,out,split", WIDE)
+def test_wide_pair_tiles_sampled_rows(tcg, oracle_mod, dtype, K, out, split):
+    M, N = 2600, 27 * 384 + 300
+    x = make_case(dtype, "k", "k", M, N, K, dist="codes", seed=K + len(dtype))
+    assert tcg.tile_n(IN_TYPE[dtype], M, N, K, 0, 0) == 384
+    D = run_gpu(tcg, x, out=out, cta_group=0, split_k=split)
+    plan = tcg.last_plan_string()
+    assert "cta_group 2, tile 256x384" in plan, plan
+    rows = sample_rows(M, n=16, seed=K)
+    got = D[rows, :N].double().cpu().numpy()
+    ref, S = oracle_rows(oracle_mod, x, rows=rows)
+    assert_parity(got, ref, S, TAU["f32"], f"{dtype} 256x384 split {split}", out)
+
+
+def test_eight_bit_and_fp6_keep_256_wide_pair_tiles(tcg, oracle_mod):
+    M, N, K = 2600, 27 * 384 + 300, 256
+    for dtype in ("e4m3", "e2m3"):
+        assert tcg.tile_n(IN_TYPE[dtype], M, N, K, 0, 0) == 256
+    x = make_case("e4m3", "k", "k", M, N, K, seed=5)
+    D = run_gpu(tcg, x, out="bf16", cta_group=0)
+    assert "cta_group 2, tile 256x256" in tcg.last_plan_string(), tcg.last_plan_string()
+    rows = sample_rows(M, n=6, seed=5)
+    ref, S = oracle_rows(oracle_mod, x, rows=rows)
+    assert_parity(D[rows, :N].double().cpu().numpy(), ref, S, TAU["f32"], "e4m3 256x256", "bf16")
 
 
 # ------------------------------------------------------------- full-size workloads
