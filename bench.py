@@ -171,6 +171,12 @@ def to_dev(bits, torch):
     return torch.from_numpy(np.ascontiguousarray(bits).view(view)).cuda()
 
 
+# tcg_gemm_args.epilogue for the device-timed calls (--epilogue): 0 auto,
+# 1 .32x32b rows, 2 .16x256b fragments written with stmatrix
+EPILOGUE = {"auto": 0, "rows": 1, "frag": 2}
+_epilogue = 0
+
+
 def run_workload(tcg, torch, w, steps, warmup, dist_ctx, measure_e2e=True):
     x = syn.make_inputs(w)
     M, N, K = w.M, w.N, w.K
@@ -207,12 +213,12 @@ def run_workload(tcg, torch, w, steps, warmup, dist_ctx, measure_e2e=True):
             if ev_pair:
                 ev_pair[0].record(stream)
             tcg.gemm(M, N, K, IN_TYPE[w.dtype], A, a_maj, x["lda"], B, b_maj, x["ldb"], D, OUT[w.out], N, ACC[w.acc],
-                     SFA_img=ia, SFB_img=ib, cta_group=w.cta_group, stream=sp)
+                     SFA_img=ia, SFB_img=ib, cta_group=w.cta_group, stream=sp, epilogue=_epilogue)
         else:
             if ev_pair:
                 ev_pair[0].record(stream)
             tcg.gemm(M, N, K, IN_TYPE[w.dtype], A, a_maj, x["lda"], B, b_maj, x["ldb"], D, OUT[w.out], N,
-                     ACC[w.acc], cta_group=w.cta_group, stream=sp)
+                     ACC[w.acc], cta_group=w.cta_group, stream=sp, epilogue=_epilogue)
         n += tcg.last_launch_count()
         if ev_pair:
             ev_pair[1].record(stream)
@@ -456,7 +462,11 @@ def main():
                     help="length of the back-to-back sustained pass of the headline workload (0: skip)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-rows", type=int, default=0, help="oracle rows in the CPU baseline (0: 2 per thread)")
+    ap.add_argument("--epilogue", default="auto", choices=sorted(EPILOGUE),
+                    help="how 16-bit outputs leave TMEM in the device-timed calls (frag: .16x256b + stmatrix)")
     args = ap.parse_args()
+    global _epilogue
+    _epilogue = EPILOGUE[args.epilogue]
     w = syn.WORKLOADS[args.workload]
 
     if args.impl == "reference":
@@ -553,7 +563,8 @@ def main():
                    "b_major": w.b_major, "acc": w.acc, "out": w.out, "cta_group": w.cta_group,
                    "l2": "inputs larger than L2 (no flush): A+B = "
                          f"{(w.M * w.K + w.N * w.K) * ESIZE[w.dtype] / 2**20:.0f} MiB",
-                   "parallelism": f"replicas x{dctx.world}"},
+                   "parallelism": f"replicas x{dctx.world}",
+                   **({"epilogue": args.epilogue} if args.epilogue != "auto" else {})},
         "pct_of_measured_peak": round(100 * rl["frac"], 2),
         "pct_of_datasheet_dense_peak": (round(100 * rl["frac_of_datasheet_dense"], 2)
                                         if "frac_of_datasheet_dense" in rl else None),

@@ -31,7 +31,8 @@ class GemmArgs(ctypes.Structure):
                 ("B", _vp), ("b_major", _i32), ("ldb", _i64),
                 ("SFA", _vp), ("SFB", _vp), ("SFA_img", _vp), ("SFB_img", _vp),
                 ("D", _vp), ("d_type", _i32), ("ldd", _i64), ("acc_type", _i32),
-                ("cta_group", _i32), ("raster_group", _i32), ("sf_staging", _i32), ("split_k", _i32)]
+                ("cta_group", _i32), ("raster_group", _i32), ("sf_staging", _i32), ("split_k", _i32),
+                ("epilogue", _i32)]
 
 
 class ProbeOperand(ctypes.Structure):
@@ -211,11 +212,11 @@ def gemm_mxf8_blockscaled_noalloc(M, N, K, A, a_major, lda, B, b_major, ldb, SFA
 
 def gemm(M, N, K, in_type, A, a_major, lda, B, b_major, ldb, D, d_type, ldd, acc_type=F32, SFA=None, SFB=None,
          SFA_img=None, SFB_img=None, cta_group=0, raster_group=0, stream=None, check=True, sf_staging=0,
-         split_k=0):
+         split_k=0, epilogue=0):
     """Generic entry point (``tcg_gemm``); returns the status (raises if ``check``)."""
     a = GemmArgs(M, N, K, in_type, _ptr(A), a_major, lda, _ptr(B), b_major, ldb, _ptr(SFA), _ptr(SFB),
                  _ptr(SFA_img), _ptr(SFB_img), _ptr(D), d_type, ldd, acc_type, cta_group, raster_group,
-                 sf_staging, split_k)
+                 sf_staging, split_k, epilogue)
     rc = _lib.tcg_gemm(ctypes.byref(a), _stream(stream))
     return _ok(rc, "gemm") if check else rc
 

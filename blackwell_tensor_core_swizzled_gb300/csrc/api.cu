@@ -34,7 +34,7 @@ struct PlanRecord {
   bool valid = false;
   bool k_zero = false;
   int cg = 0, bn = 0, clusters = 0, split = 0;
-  bool swapped = false, stream_k = false;
+  bool swapped = false, stream_k = false, frag = false;
 };
 thread_local PlanRecord t_plan;
 thread_local std::string t_last_plan;
@@ -247,7 +247,6 @@ bool is_mx(tcg_input t) {
 }
 bool is_fp6(tcg_input t) { return t == TCG_IN_E3M2 || t == TCG_IN_E2M3; }
 bool is_fp4(tcg_input t) { return t == TCG_IN_E2M1 || t == TCG_IN_NVF4; }
-bool is_packed(tcg_input t) { return is_fp6(t) || is_fp4(t); }
 int bits_of(tcg_input t) {
   return t == TCG_IN_TF32 ? 32 : is_fp4(t) ? 4 : is_fp6(t) ? 6 : is_mx(t) ? 8 : 16;
 }
@@ -566,7 +565,7 @@ int run_gemm(const tcg_gemm_args* args, cudaStream_t s) {
   if (a.acc_type == TCG_BF16) return TCG_ERR_UNSUPPORTED;
   if (a.acc_type == TCG_F16 && (a.in_type != TCG_IN_F16 || a.d_type != TCG_F16)) return TCG_ERR_UNSUPPORTED;
   if (a.cta_group < 0 || a.cta_group > 2 || a.raster_group < 0 || a.sf_staging < 0 || a.sf_staging > 3 ||
-      a.split_k < -1)
+      a.split_k < -1 || a.epilogue < 0 || a.epilogue > 2)
     return TCG_ERR_INVALID;
   if (a.M > INT32_MAX / 2 || a.N > INT32_MAX / 2 || a.K > INT32_MAX / 2) return TCG_ERR_UNSUPPORTED;
   if (a.M == 0 || a.N == 0) return TCG_OK;
@@ -688,6 +687,8 @@ int run_gemm(const tcg_gemm_args* args, cudaStream_t s) {
       return rc;
     prm.d_tma = 1;
   }
+  prm.epi_frag = a.epilogue == 2 ? 1 : 0;
+  const bool frag_used = prm.epi_frag && prm.d_tma && a.d_type != TCG_F32 && a.acc_type == TCG_F32;
   prm.err = d->err;
   prm.timeout_ns = g_timeout_ns.load();
   prm.trace = t_trace_buf;
@@ -796,6 +797,7 @@ int run_gemm(const tcg_gemm_args* args, cudaStream_t s) {
   t_plan.split = split;
   t_plan.swapped = d_trans;
   t_plan.stream_k = stream_k;
+  t_plan.frag = frag_used;
   return TCG_OK;
 }
 
@@ -1060,11 +1062,12 @@ const char* tcg_last_plan_string(void) {
   } else if (p.k_zero) {
     t_last_plan = "K = 0: D zeroed";
   } else {
-    char buf[160];
-    std::snprintf(buf, sizeof buf, "cta_group %d, tile %dx%d%s, %d clusters, %s%s", p.cg, 128 * p.cg, p.bn,
+    char buf[200];
+    std::snprintf(buf, sizeof buf, "cta_group %d, tile %dx%d%s, %d clusters, %s%s%s", p.cg, 128 * p.cg, p.bn,
                   p.swapped ? " (operands swapped, D stored transposed)" : "", p.clusters,
                   p.stream_k ? "stream-K" : p.split > 1 ? "split-K " : "one pass per tile",
-                  p.split > 1 ? std::to_string(p.split).c_str() : "");
+                  p.split > 1 ? std::to_string(p.split).c_str() : "",
+                  p.frag ? ", 16x256b + stmatrix epilogue" : "");
     t_last_plan = buf;
   }
   return t_last_plan.c_str();

@@ -133,6 +133,10 @@ struct GemmParams {
   // D[c * ldd + r] (f32 accumulation, 32-column variant only; set by the host
   // for few-row problems whose operands it swapped)
   int d_trans;
+  // 16-bit outputs through the staging tiles, fp32 accumulation: drain with
+  // tcgen05.ld .16x256b (fragments) and write the staging tile with stmatrix
+  // instead of .32x32b rows and st.shared.v4
+  int epi_frag;
   unsigned long long* err;
   uint64_t timeout_ns;
   // block scaling, where the scales are staged into TMEM:
@@ -670,11 +674,6 @@ __global__ void __launch_bounds__(KIND >= KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
 #pragma unroll
       for (int j = 0; j < C::KSTEPS; ++j)
         idesc_j[j] = C::SCALED ? (p.idesc | idesc_sf_ids(C::sf_id(j), C::sf_id(j))) : p.idesc;
-      // BN = 384: the second MMA of a K step has N = 128 (p.idesc carries 256),
-      // reads B rows 128.. (16 KiB on) and the third SFB chunk
-      constexpr uint32_t N_FIELD = 0x3Fu << 17;
-      constexpr uint32_t N128 = (128u >> 3) << 17;
-      constexpr uint64_t B_HI_OFF = (128u * 128u) >> 4;
       // block scales staged by other threads: wait for sf_ready[slot] too
       constexpr bool sf_wait = C::SCALED && SFM != SF_BY_MMA;
       constexpr bool sf_by_mma = C::SCALED && SFM == SF_BY_MMA;
@@ -755,7 +754,12 @@ __global__ void __launch_bounds__(KIND >= KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
             else
               mma_tf32<CG>(d_tmem, ad, bd, idesc_j[j], acc);
             if constexpr (C::WIDE) {
-              // the same kind as the first issue (WIDE implies a block-scaled kind)
+              // BN = 384: the second issue, of the same kind (WIDE implies a
+              // block-scaled kind), has N = 128 (p.idesc carries 256), reads B
+              // rows 128.. (16 KiB on) and the third SFB chunk
+              constexpr uint32_t N_FIELD = 0x3Fu << 17;
+              constexpr uint32_t N128 = (128u >> 3) << 17;
+              constexpr uint64_t B_HI_OFF = (128u * 128u) >> 4;
               const uint32_t id2 = (idesc_j[j] & ~N_FIELD) | N128;
               const uint32_t sfb2 = sf_col + C::sfb_col(j) + 8;
               if constexpr (KIND == KIND_MXF8)
@@ -910,16 +914,30 @@ __global__ void __launch_bounds__(KIND >= KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
     // the 64-byte swizzle (chunk j at j ^ ((row >> 1) & 3)), one lane issues
     // the tile store; the tensor map clips rows >= M and columns >= N.
     // to_slot: (col0, row0, z) address the workspace slot map instead of D
-    auto stage_tile = [&](int row0, int col0, const uint32_t(&h)[16], bool to_slot, int z) {
+    // frag: h holds fragments (frag_load16's order) written with stmatrix,
+    // each matrix an 8-row x 16-byte block of the same swizzled tile.
+    auto stage_tile = [&](int row0, int col0, const uint32_t(&h)[16], bool to_slot, int z, bool frag = false) {
       const uint32_t buf = epi_base + (epi_n % C::EPI_BUFS) * C::EPI_TILE_BYTES;
       if (epi_n >= static_cast<uint32_t>(C::EPI_BUFS)) {
         if (lane == 0) bulk_wait_group_read<C::EPI_BUFS - 1>();  // the buffer's last store has read it
         __syncwarp();
       }
-      const uint32_t rb = buf + 64u * static_cast<uint32_t>(lane);
-      const uint32_t sw = (static_cast<uint32_t>(lane) >> 1) & 3u;
+      if (frag) {
+        // lane 8m + i addresses row i of matrix m (16-byte chunk m of its row)
+        const uint32_t m = static_cast<uint32_t>(lane) >> 3, i = static_cast<uint32_t>(lane) & 7u;
 #pragma unroll
-      for (uint32_t j = 0; j < 4; ++j) st_shared_v4(rb + 16u * (j ^ sw), h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
+        for (uint32_t g = 0; g < 4; ++g) {  // g = 2a + half: rows 16a + 8half + [0, 8)
+          const uint32_t row = 8u * g + i;
+          stmatrix_x4(buf + 64u * row + 16u * (m ^ ((row >> 1) & 3u)), h[4 * g], h[4 * g + 1], h[4 * g + 2],
+                      h[4 * g + 3]);
+        }
+      } else {
+        const uint32_t rb = buf + 64u * static_cast<uint32_t>(lane);
+        const uint32_t sw = (static_cast<uint32_t>(lane) >> 1) & 3u;
+#pragma unroll
+        for (uint32_t j = 0; j < 4; ++j)
+          st_shared_v4(rb + 16u * (j ^ sw), h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
+      }
       fence_proxy_async_shared();
       __syncwarp();
       if (lane == 0) {
@@ -933,6 +951,27 @@ __global__ void __launch_bounds__(KIND >= KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
       ++epi_n;
     };
     auto store_tile16 = [&](int row0, int col0, const uint32_t(&h)[16]) { stage_tile(row0, col0, h, false, 0); };
+    // The warp's 32 x 32 fp32 block at TMEM address t as two .16x256b.x4
+    // loads (lanes +0 and +16), packed to 16-bit pairs in stmatrix order:
+    // h[4g + j] = row 8g + lane/4, columns 8j + 2(lane%4) + {0, 1}.
+    auto frag_load16 = [&](uint32_t t, uint32_t(&h)[16]) {
+      uint32_t r0[16], r1[16];
+      tmem_ld_16x256b_x4(t, r0);
+      tmem_ld_16x256b_x4(t + (16u << 16), r1);
+      tc_wait_ld();
+      const bool bf = p.d_type == OUT_BF16;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          h[4 * hh + j] = bf ? pack_bf16(r0[4 * j + 2 * hh], r0[4 * j + 2 * hh + 1])
+                             : pack_f16(r0[4 * j + 2 * hh], r0[4 * j + 2 * hh + 1]);
+          h[8 + 4 * hh + j] = bf ? pack_bf16(r1[4 * j + 2 * hh], r1[4 * j + 2 * hh + 1])
+                                 : pack_f16(r1[4 * j + 2 * hh], r1[4 * j + 2 * hh + 1]);
+        }
+    };
+    // fragments only where they are staged for a TMA store of 16-bit values
+    const bool frag16 = p.epi_frag && p.d_tma && p.d_type != OUT_F32 && !p.acc_f16;
     uint32_t tcount = 0;
     for (UnitCursor uc = uc_first; uc.valid; cursor_next(uc, num_clusters, p), ++tcount) {
       const int b = static_cast<int>(tcount % ACC);
@@ -1000,6 +1039,8 @@ __global__ void __launch_bounds__(KIND >= KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
           if (c < BN / 32) {
             if (p.acc_f16) {
               tmem_ld_32x32b_x16_pack16(tb + 32 * c, h[i]);
+            } else if (frag16) {
+              frag_load16(tb + 32 * c, h[i]);
             } else {
               uint32_t r[32];
               tmem_ld_32x32b_x32(tb + 32 * c, r);
@@ -1015,7 +1056,7 @@ __global__ void __launch_bounds__(KIND >= KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
           const int c = part + 2 * i;
           if (c < BN / 32 && n0 + 32 * c < p.N) {
             if (p.d_tma)
-              store_tile16(row0, n0 + 32 * c, h[i]);
+              stage_tile(row0, n0 + 32 * c, h[i], false, 0, frag16);
             else if (row < p.M)
               store_row16(p, row, n0 + 32 * c, h[i]);
           }
@@ -1034,6 +1075,13 @@ __global__ void __launch_bounds__(KIND >= KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
             else if (row < p.M)
               store_row16(p, row, n0 + 32 * c, h);
           }
+        }
+      } else if (frag16) {
+#pragma unroll 1
+        for (int c = part; c < BN / 32; c += nparts) {
+          uint32_t h[16];
+          frag_load16(tb + 32 * c, h);
+          if (n0 + 32 * c < p.N) stage_tile(row0, n0 + 32 * c, h, false, 0, true);
         }
       } else {
 #pragma unroll 1

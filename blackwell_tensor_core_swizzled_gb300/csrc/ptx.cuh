@@ -378,6 +378,30 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
       : "r"(taddr));
 }
 
+// tcgen05.ld .16x256b.x4: 16 lanes (base .. base+15) x 32 columns; lane l
+// receives in register r row l/4 + 8*((r/2)%2), column r%2 + 2*(l%4) +
+// 8*(r/4) ("tcgen05.ld / tcgen05.st" page, "Native images") -- the
+// m16n8 accumulator fragment of each 8-column group.
+__device__ __forceinline__ void tmem_ld_16x256b_x4(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32"
+      " {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15])
+      : "r"(taddr));
+}
+
+// stmatrix .m8n8.x4.b16: lane 8m+i supplies the shared address of row i of
+// matrix m; register m of lane 4i+w holds that matrix's row i, 16-bit
+// columns 2w and 2w+1 ("ldmatrix / stmatrix" page, "Address providers and
+// result owners", "Transpose and stores").
+__device__ __forceinline__ void stmatrix_x4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b),
+               "r"(c), "r"(d)
+               : "memory");
+}
+
 // tcgen05.ld .32x32b.x16.pack::16b: 16 registers covering 32 columns; each
 // register holds the low 16 bits of columns 2c and 2c+1 ("tcgen05.ld /
 // tcgen05.st" page, "Pack/unpack is a different TMEM image").

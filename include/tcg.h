@@ -238,6 +238,13 @@ typedef struct {
                         second kernel sums each tile's partials in K order
                         (deterministic) into D.  Ignored with TCG_F16
                         accumulation. */
+  int epilogue;      /* how 16-bit outputs (f16 / bf16 D, fp32 accumulation,
+                        16-byte aligned D and ldd) leave TMEM: 0 = auto (1),
+                        1 = tcgen05.ld .32x32b rows written to the staging tile
+                        with st.shared.v4, 2 = tcgen05.ld .16x256b fragments
+                        written with stmatrix .m8n8.x4 ("ldmatrix / stmatrix"
+                        page).  Same values either way; other outputs ignore
+                        it.  Anything else: TCG_ERR_INVALID. */
 } tcg_gemm_args;
 
 int tcg_gemm(const tcg_gemm_args* args, void* stream);

@@ -59,7 +59,7 @@ def make_case(dtype, am, bm, M, N, K, dist="uniform", seed=7, extra_pad=0):
 
 
 def run_gpu(tcg, x, out="bf16", acc="f32", cta_group=0, ldd=None, D=None, raster_group=0, sf_img=None, sf_staging=0,
-            check=True, split_k=0):
+            check=True, split_k=0, epilogue=0):
     w = x["w"]
     M, N, K = x["M"], x["N"], x["K"]
     dt, tdt = OUT[out]
@@ -76,7 +76,7 @@ def run_gpu(tcg, x, out="bf16", acc="f32", cta_group=0, ldd=None, D=None, raster
             kw = dict(SFA=to_device(x["SFA"]), SFB=to_device(x["SFB"]))
     tcg.gemm(M, N, K, IN_TYPE[w.dtype], A, 0 if w.a_major == "k" else 1, x["lda"], B,
              0 if w.b_major == "k" else 1, x["ldb"], D, dt, ldd, ACC[acc], cta_group=cta_group,
-             raster_group=raster_group, sf_staging=sf_staging, split_k=split_k, **kw)
+             raster_group=raster_group, sf_staging=sf_staging, split_k=split_k, epilogue=epilogue, **kw)
     if check:
         rc = tcg.check()
         assert rc == 0, f"{tcg.status_string(rc)}: {tcg.last_error_string()}"

@@ -108,6 +108,13 @@ def test_host_validation_rejects_bad_arguments(tcg):
         assert tcg.raw_call("tcg_probe_stmatrix", 0x10000, 0x20000, count, 0, 0x30000, None) == tcg.ERR_INVALID
 
 
+def test_generic_entry_point_rejects_unknown_epilogue(tcg):
+    for ep in (-1, 3):
+        rc = tcg.gemm(256, 256, 64, tcg.IN_BF16, 0x10000, 0, 64, 0x20000, 0, 64, 0x30000, 2, 256,
+                      check=False, epilogue=ep, stream=0)
+        assert rc == tcg.ERR_INVALID
+
+
 def test_empty_problems_are_noops(tcg):
     # M == 0 or N == 0 returns before any device work, even with null pointers
     assert _call(tcg, "bf16", M=0, A=None, B=None, D=None) == tcg.OK

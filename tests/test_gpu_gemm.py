@@ -489,6 +489,54 @@ def test_eight_bit_and_fp6_keep_256_wide_pair_tiles(tcg, oracle_mod):
     assert_parity(D[rows, :N].double().cpu().numpy(), ref, S, TAU["f32"], "e4m3 256x256", "bf16")
 
 
+# ------------------------------------------------------------- fragment epilogue
+
+# epilogue = 2: 16-bit outputs drained with tcgen05.ld .16x256b and written to
+# the staging tile with stmatrix.  Every variant that stages 16-bit outputs:
+# 128 x 256 and pair tiles (two accumulators), 256 x 128 pair tiles, the
+# 64-column skinny and 32-column narrow tiles, TF32, MXFP8 pairs (one
+# accumulator read whole before release, eight warps) and the 256 x 384 FP4
+# pair tile; ragged M and N throughout.
+FRAG = [
+    # dtype, am, bm, M, N, K, cg, out  (N a multiple of 8: 16-byte output rows)
+    ("bf16", "k", "k", 300, 520, 200, 1, "bf16"),
+    ("f16", "mn", "k", 513, 1096, 136, 2, "f16"),
+    ("bf16", "k", "mn", 300, 1096, 512, 0, "bf16"),
+    ("bf16", "k", "k", 100, 520, 640, 1, "f16"),
+    ("bf16", "k", "k", 700, 24, 1000, 1, "bf16"),
+    ("tf32", "k", "k", 300, 520, 200, 2, "bf16"),
+    ("e4m3", "k", "k", 300, 1096, 256, 2, "bf16"),
+    ("e4m3", "mn", "k", 260, 232, 160, 1, "f16"),
+    ("e2m1", "k", "k", 2600, 27 * 384 + 296, 256, 0, "bf16"),
+]
+
+
+@pytest.mark.parametrize("dtype,am,bm,M,N,K,cg,out", FRAG)
+def test_fragment_epilogue_matches_row_epilogue_bit_for_bit(tcg, oracle_mod, dtype, am, bm, M, N, K, cg, out):
+    x = make_case(dtype, am, bm, M, N, K, dist="codes" if dtype in syn.PACKED_BITS else "uniform", seed=M + N)
+    rows_d = run_gpu(tcg, x, out=out, cta_group=cg, epilogue=1)
+    assert "stmatrix" not in tcg.last_plan_string()
+    frag_d = run_gpu(tcg, x, out=out, cta_group=cg, epilogue=2)
+    assert "16x256b + stmatrix epilogue" in tcg.last_plan_string(), tcg.last_plan_string()
+    assert torch.equal(rows_d.view(torch.int16), frag_d.view(torch.int16))
+    rows = sample_rows(M, n=8, seed=N) if M > 512 else list(range(M))
+    ref, S = oracle_rows(oracle_mod, x, rows=rows)
+    assert_parity(frag_d[rows, :N].double().cpu().numpy(), ref, S, TAU["f32"], f"{dtype} fragment epilogue", out)
+
+
+def test_fragment_epilogue_request_is_ignored_where_it_does_not_apply(tcg, oracle_mod):
+    # fp32 output, and a 16-bit output whose ldd is not a 16-byte multiple
+    # (per-lane row stores, no staging tile): the row path serves both
+    x = make_case("bf16", "k", "k", 300, 520, 200, seed=3)
+    run_gpu(tcg, x, out="f32", cta_group=1, epilogue=2)
+    assert "stmatrix" not in tcg.last_plan_string()
+    D = torch.full((300, 523), float("nan"), dtype=torch.bfloat16, device="cuda")
+    run_gpu(tcg, x, out="bf16", cta_group=1, epilogue=2, ldd=523, D=D)
+    assert "stmatrix" not in tcg.last_plan_string()
+    ref, S = oracle_rows(oracle_mod, x)
+    assert_parity(D[:, :520].double().cpu().numpy(), ref, S, TAU["f32"], "row path", "bf16")
+
+
 # ------------------------------------------------------------- full-size workloads
 
 FULL = ["tile_f16_128x128x64", "bf16_4096_kmn_cta1", "tf32_2048x2048x8192", "bf16_8192_cta2",
