@@ -638,9 +638,17 @@ int run_gemm(const tcg_gemm_args* args, cudaStream_t s) {
     return TCG_ERR_UNSUPPORTED;
   }
   prm.num_tiles = prm.num_m_tiles * prm.num_n_tiles;
-  // M tiles per raster group (measured at 8192^3: 16 for 128-row tiles, 8 for
-  // 256-row pair tiles, i.e. 2048 rows of A either way)
-  prm.raster_group = a.raster_group > 0 ? a.raster_group : (cg == 1 ? 16 : 8);
+  // M tiles per raster group: the rows of A whose tiles sweep N together
+  // hold about 32 MiB (kept between 2048 and 8192 rows), so that they stay in
+  // the L2 while B streams past.  Best group sizes measured (pairs, 8192^3
+  // unless stated): bf16 8 (2048 rows), E4M3 16 (4096), E2M3 16-24, E2M1 32
+  // (8192); bf16 K = 4096 16, K = 16384 8; E4M3 16384 x 8192 x 4096 16-32,
+  // K = 16384 8; single CTAs bf16 8192^3 16 (2048 rows).
+  const int64_t group_rows = std::min<int64_t>(8192, std::max<int64_t>(2048, (32LL << 20) / std::max<int64_t>(1, row_bytes(a.in_type, a.K))));
+  prm.raster_group = a.raster_group > 0 ? a.raster_group : static_cast<int>(group_rows / (128 * cg));
+  // a group of all M tiles is the widest there is (and keeps group x N tiles
+  // within the tile count's 32-bit range)
+  prm.raster_group = std::min(prm.raster_group, prm.num_m_tiles);
   // skinny single-CTA problems: the A box covers only the rows that exist
   const int a_rows = (cg == 1 && a.a_major == TCG_K_MAJOR && a.M < 128) ? static_cast<int>(cdiv(a.M, 8) * 8) : 128;
   if (int rc = setup_operand(a.A, a.in_type, a.a_major, a.M, a.K, a.lda, a_rows, &prm.tmap_a, &prm.a_mn_major,
