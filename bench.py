@@ -203,7 +203,10 @@ def run_workload(tcg, torch, w, steps, warmup, dist_ctx, measure_e2e=True):
     # GEMM's events; such workloads report the GEMM time, not the step time).
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda") if w.extra.get("bound") == "hbm" else None
 
-    def step(ev_pair=None):
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    trace_buf = torch.zeros((sms, 10), dtype=torch.int64, device="cuda")
+
+    def step(ev_pair=None, trace=False):
         n = 0
         if flush is not None:
             flush.zero_()
@@ -212,11 +215,15 @@ def run_workload(tcg, torch, w, steps, warmup, dist_ctx, measure_e2e=True):
             n += 1
             if ev_pair:
                 ev_pair[0].record(stream)
+            if trace:
+                tcg.trace_next(trace_buf, sms)
             tcg.gemm(M, N, K, IN_TYPE[w.dtype], A, a_maj, x["lda"], B, b_maj, x["ldb"], D, OUT[w.out], N, ACC[w.acc],
                      SFA_img=ia, SFB_img=ib, cta_group=w.cta_group, stream=sp, epilogue=_epilogue)
         else:
             if ev_pair:
                 ev_pair[0].record(stream)
+            if trace:
+                tcg.trace_next(trace_buf, sms)
             tcg.gemm(M, N, K, IN_TYPE[w.dtype], A, a_maj, x["lda"], B, b_maj, x["ldb"], D, OUT[w.out], N,
                      ACC[w.acc], cta_group=w.cta_group, stream=sp, epilogue=_epilogue)
         n += tcg.last_launch_count()
@@ -239,7 +246,9 @@ def run_workload(tcg, torch, w, steps, warmup, dist_ctx, measure_e2e=True):
     t_host0 = time.time()
     start.record(stream)
     for i in range(steps):
-        step(kev[i])
+        # the last timed launch records its CTAs' globaltimer and SM cycle
+        # counters at entry and exit: the SM clock it actually ran at
+        step(kev[i], trace=(i == steps - 1))
     end.record(stream)
     torch.cuda.synchronize()
     t_host1 = time.time()
@@ -249,7 +258,13 @@ def run_workload(tcg, torch, w, steps, warmup, dist_ctx, measure_e2e=True):
         raise RuntimeError(f"timed run failed: {tcg.status_string(rc)} {tcg.last_error_string()}")
     total_ms = start.elapsed_time(end)
     kernel_ms = float(np.mean([a.elapsed_time(b) for a, b in kev]))
-    res = {"total_ms": total_ms, "kernel_ms": kernel_ms, "launches": launches[0], "t0": t_host0, "t1": t_host1}
+    tr = trace_buf.cpu().numpy()
+    ok = (tr[:, 6] > tr[:, 0]) & (tr[:, 9] > tr[:, 8])
+    ghz = (tr[ok, 9] - tr[ok, 8]) / (tr[ok, 6] - tr[ok, 0]) if ok.any() else np.array([])
+    res = {"total_ms": total_ms, "kernel_ms": kernel_ms, "launches": launches[0], "t0": t_host0, "t1": t_host1,
+           "kernel_sm_mhz": round(float(np.median(ghz)) * 1000, 1) if ghz.size else None,
+           "kernel_sm_mhz_range": [round(float(ghz.min()) * 1000, 1), round(float(ghz.max()) * 1000, 1)]
+           if ghz.size else None}
 
     if measure_e2e:
         # End to end through the C ABI: every step copies its inputs in from
@@ -522,7 +537,9 @@ def main():
             sustained = {"value": round(v_s, 1), "unit": UNIT, "steps": n_sus, "ms_per_step": round(t_s / n_sus, 4),
                          "timed_s": round(rs["total_ms"] * 1e-3, 3), "frac": rl_s["frac"], "peak": rl_s["peak"],
                          "peak_source": rl_s["peak_source"], "frac_of_datasheet_dense": rl_s["frac_of_datasheet_dense"],
-                         "clocks": sampler.summary(rs["t0"], rs["t1"])}
+                         "clocks": {**sampler.summary(rs["t0"], rs["t1"]),
+                                    "kernel_sm_mhz": rs["kernel_sm_mhz"],
+                                    "kernel_sm_mhz_range": rs["kernel_sm_mhz_range"]}}
         sec = []
         for name in [s for s in args.secondary.split(",") if s and s != w.name]:
             ws = syn.WORKLOADS[name]
@@ -532,12 +549,16 @@ def main():
             v2, t2 = whole_job(dctx, 2.0 * ws.M * ws.N * ws.K, args.steps, local)
             sec.append({"workload": name, "value": round(v2, 1),
                         "unit": UNIT, "ms_per_step": round(t2 / args.steps, 4), "dtype": ws.dtype,
-                        "gpu_launches": r2["launches"],
+                        "gpu_launches": r2["launches"], "kernel_sm_mhz": r2["kernel_sm_mhz"],
                         "roofline": roofline(ws, r2["kernel_ms"], peaks, profiled_traffic(name),
                                                     r2["total_ms"] * 1e-3)})
     finally:
         sampler.stop()
     clocks = sampler.summary(res["t0"], res["t1"])
+    # the SM clock of the last timed launch, from its CTAs' own counters
+    # (median and range over CTAs of cycles / nanoseconds between entry and exit)
+    clocks["kernel_sm_mhz"] = res["kernel_sm_mhz"]
+    clocks["kernel_sm_mhz_range"] = res["kernel_sm_mhz_range"]
 
     flops_step = 2.0 * w.M * w.N * w.K
     value, total_ms = whole_job(dctx, flops_step, args.steps, res["total_ms"])

@@ -163,12 +163,25 @@ enum TraceSlot : int {
   TRACE_EPI_DONE = 5,     // epilogue stores drained (warp 4)
   TRACE_EXIT = 6,         // TMEM released, CTA about to exit
   TRACE_UNITS = 7,        // units processed (MMA warp), not a time
-  TRACE_SLOTS = 8
+  TRACE_CLK_ENTRY = 8,    // SM cycle counter next to TRACE_ENTRY
+  TRACE_CLK_EXIT = 9,     // SM cycle counter next to TRACE_EXIT
+  TRACE_SLOTS = 10
 };
 
 __device__ __forceinline__ void trace_stamp(const GemmParams& p, int slot) {
   if (p.trace && static_cast<int>(blockIdx.x) < p.trace_ctas)
     p.trace[static_cast<int64_t>(blockIdx.x) * TRACE_SLOTS + slot] = globaltimer();
+}
+
+// A globaltimer stamp and the SM's cycle counter read back to back: the two
+// pairs (entry, exit) give the CTA's average SM clock over the kernel.
+__device__ __forceinline__ void trace_stamp_clock(const GemmParams& p, int slot, int clk_slot) {
+  if (p.trace && static_cast<int>(blockIdx.x) < p.trace_ctas) {
+    const uint64_t t = globaltimer();
+    const uint64_t c = clock64();
+    p.trace[static_cast<int64_t>(blockIdx.x) * TRACE_SLOTS + slot] = t;
+    p.trace[static_cast<int64_t>(blockIdx.x) * TRACE_SLOTS + clk_slot] = c;
+  }
 }
 
 // A_ROWS < 128 (single CTA, K-major A, M <= A_ROWS): only that many rows of
@@ -474,7 +487,7 @@ __device__ __forceinline__ void store_col32(const GemmParams& p, int row, int co
 template <int CG, int BN, int ACC, int STAGES, int KIND, int A_ROWS = 128>
 __global__ void __launch_bounds__(KIND >= KIND_MXF8 ? 384 : 256, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
   using C = GemmCfg<CG, BN, ACC, STAGES, KIND, A_ROWS>;
-  if (threadIdx.x == 0) trace_stamp(p, TRACE_ENTRY);
+  if (threadIdx.x == 0) trace_stamp_clock(p, TRACE_ENTRY, TRACE_CLK_ENTRY);
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -1127,7 +1140,7 @@ __global__ void __launch_bounds__(KIND >= KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
   tc_fence_after();
   if (warp == 2) {
     tmem_dealloc<CG>(tmem_base, C::TMEM_COLS);
-    if (lane == 0) trace_stamp(p, TRACE_EXIT);
+    if (lane == 0) trace_stamp_clock(p, TRACE_EXIT, TRACE_CLK_EXIT);
   }
 }
 

@@ -338,13 +338,15 @@ const char* tcg_last_plan_string(void);
 
 /* Phase trace of the next GEMM kernel launched by this thread (tracing is off
  * otherwise and costs one untaken branch per stamp).  buf: device memory of
- * max_ctas x 8 uint64 (8-byte aligned); CTA c (c < max_ctas) writes slots
- * [8c, 8c+8): globaltimer nanoseconds at 0 kernel entry, 1 barriers and TMEM
- * ready, 2 producer starts its first unit, 3 first unit's MMAs issued, 4 last
- * accumulator committed, 5 epilogue stores drained, 6 TMEM released; slot 7
- * = units (tiles or tile parts) the CTA computed.  Slots 3, 4 and 7 are
- * written by the pair leader only (CTA pairs issue from the leader).  No
- * stamp sits inside the per-stage loops.
+ * max_ctas x 10 uint64 (8-byte aligned); CTA c (c < max_ctas) writes slots
+ * [10c, 10c+10): globaltimer nanoseconds at 0 kernel entry, 1 barriers and
+ * TMEM ready, 2 producer starts its first unit, 3 first unit's MMAs issued,
+ * 4 last accumulator committed, 5 epilogue stores drained, 6 TMEM released;
+ * slot 7 = units (tiles or tile parts) the CTA computed; slots 8 and 9 = the
+ * SM's cycle counter (clock64) read right after the stamps of slots 0 and 6,
+ * so (s9 - s8) / (s6 - s0) is the CTA's average SM clock in GHz.  Slots 3, 4
+ * and 7 are written by the pair leader only (CTA pairs issue from the
+ * leader).  No stamp sits inside the per-stage loops.
  * Untouched slots keep their contents.  buf = NULL with max_ctas = 0 cancels
  * a pending request. */
 int tcg_trace_next(unsigned long long* buf, int max_ctas);

@@ -393,7 +393,7 @@ def test_phase_trace(tcg, oracle_mod):
     # 1024 x 1024 x 512 on 256 x 128 pair tiles: 32 clusters, one tile each
     import re
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    buf = torch.zeros((sms, 8), dtype=torch.int64, device="cuda")
+    buf = torch.zeros((sms, 10), dtype=torch.int64, device="cuda")
     x = make_case("bf16", "k", "k", 1024, 1024, 512, seed=72)
     tcg.trace_next(buf, sms)
     _check_full(tcg, oracle_mod, x, "bf16", "f32", 0)
@@ -406,8 +406,10 @@ def test_phase_trace(tcg, oracle_mod):
     assert np.all(t[ctas:] == 0)                        # no stamps beyond the grid
     units = 0
     for c in range(ctas):
-        e, su, pr, fu, lc, ep, ex, un = t[c]
+        e, su, pr, fu, lc, ep, ex, un, c0, c1 = t[c]
         assert 0 < e <= su <= pr and su <= ep <= ex and ex - e < 10**9, (c, t[c])
+        # cycles over nanoseconds: an SM clock between 0.5 and 2.5 GHz
+        assert 0.5 * (ex - e) <= c1 - c0 <= 2.5 * (ex - e), (c, t[c])
         if c % cg == 0:                                 # the MMA warp of the leader
             assert pr <= fu <= lc <= ep and un >= 1, (c, t[c])
             units += un
