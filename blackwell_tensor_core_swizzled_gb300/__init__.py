@@ -59,6 +59,7 @@ _SIGS = {
     "tcg_scale_image_bytes": ([_i32, _i64, _i64, _i32], _i64),
     "tcg_prepare_scales_ab": ([_i32, _vp, _i64, _vp, _vp, _i64, _i32, _vp, _i64, _vp], _i32),
     "tcg_gemm": ([ctypes.POINTER(GemmArgs), _vp], _i32),
+    "tcg_gemm_chain": ([_i32, _i64, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp, _i32, _i64, _vp], _i32),
     "tcg_mxf8_scale_image_bytes": ([_i64, _i64, _i32], _i64),
     "tcg_mxf8_tile_n": ([_i64, _i64, _i64, _i32, _i32], _i32),
     "tcg_tile_n": ([_i32, _i64, _i64, _i64, _i32, _i32], _i32),
@@ -208,6 +209,13 @@ def gemm_mxf8_blockscaled_noalloc(M, N, K, A, a_major, lda, B, b_major, ldb, SFA
     return _ok(_lib.tcg_gemm_mxf8_blockscaled_noalloc(M, N, K, _ptr(A), a_major, lda, _ptr(B), b_major, ldb,
                                                       _ptr(SFA), _ptr(SFB), _ptr(D), d_type, ldd, acc_type,
                                                       _stream(stream)), "gemm_mxf8_blockscaled_noalloc")
+
+
+def gemm_chain(in_type, M, N1, N2, K, A, lda, B1, ldb1, B2, ldb2, E, e_type, lde, stream=None, check=True):
+    """Chained GEMM E = round(A . B1) . B2 with the intermediate in TMEM (``tcg_gemm_chain``)."""
+    rc = _lib.tcg_gemm_chain(in_type, M, N1, N2, K, _ptr(A), lda, _ptr(B1), ldb1, _ptr(B2), ldb2, _ptr(E), e_type,
+                             lde, _stream(stream))
+    return _ok(rc, "gemm_chain") if check else rc
 
 
 def gemm(M, N, K, in_type, A, a_major, lda, B, b_major, ldb, D, d_type, ldd, acc_type=F32, SFA=None, SFB=None,

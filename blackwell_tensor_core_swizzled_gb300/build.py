@@ -21,7 +21,7 @@ BUILD_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libtcg.so")
 
 SOURCES = ["api.cu", "gemm_f16.cu", "gemm_tf32.cu", "gemm_mxf8.cu", "probes.cu", "gemm_mxf8_noalloc.cu",
-           "splitk_reduce.cu"]
+           "splitk_reduce.cu", "gemm_chain.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -16,6 +16,7 @@
 #include <utility>
 
 #include "common.h"
+#include "gemm_chain.cuh"
 #include "gemm_kernel.cuh"
 
 namespace tcg {
@@ -896,9 +897,105 @@ int named_gemm(tcg_input in, int64_t M, int64_t N, int64_t K, const void* A, tcg
   return run_gemm(&a, reinterpret_cast<cudaStream_t>(stream));
 }
 
+// E = round(A . B1) . B2 through one kernel (gemm_chain.cu).
+int run_chain(tcg_input in, int64_t M, int64_t N1, int64_t N2, int64_t K, const void* A, int64_t lda,
+              const void* B1, int64_t ldb1, const void* B2, int64_t ldb2, void* E, tcg_dtype e_type, int64_t lde,
+              cudaStream_t s) {
+  t_last_launches = 0;
+  t_plan.valid = false;
+  if (in != TCG_IN_F16 && in != TCG_IN_BF16) return TCG_ERR_INVALID;
+  if (M < 0 || N2 < 0 || K < 0 || N1 < 16 || N1 > 256 || N1 % 16) return TCG_ERR_INVALID;
+  if (e_type < TCG_F32 || e_type > TCG_BF16) return TCG_ERR_INVALID;
+  if (M > INT32_MAX / 2 || N2 > INT32_MAX / 2 || K > INT32_MAX / 2) return TCG_ERR_UNSUPPORTED;
+  if (M == 0 || N2 == 0) return TCG_OK;
+  if (!E) return TCG_ERR_INVALID;
+  if (lde == 0) lde = N2;
+  if (lde < N2) return TCG_ERR_INVALID;
+  const int es = dsize_of(e_type);
+  // E leaves through TMA tile stores: 16-byte base and row stride
+  if (reinterpret_cast<uintptr_t>(E) % 16 || (lde * es) % 16) return TCG_ERR_ALIGNMENT;
+  if (K > 0) {
+    if (int rc = check_operand(A, TCG_K_MAJOR, M, K, &lda, in)) return rc;
+    if (int rc = check_operand(B1, TCG_K_MAJOR, N1, K, &ldb1, in)) return rc;
+  }
+  if (int rc = check_operand(B2, TCG_K_MAJOR, N2, N1, &ldb2, in)) return rc;
+  int dev;
+  if (int rc = current_device_checked(&dev)) return rc;
+  DeviceState* d = device_state(dev);
+  if (K == 0) {  // C = 0, so E = 0
+    const cudaError_t e = cudaMemset2DAsync(E, static_cast<size_t>(lde) * es, 0, static_cast<size_t>(N2) * es,
+                                            static_cast<size_t>(M), s);
+    if (e != cudaSuccess) return record_cuda(e);
+    t_last_launches = 1;
+    return TCG_OK;
+  }
+  const CUtensorMapDataType dt = in == TCG_IN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  ChainParams p;
+  std::memset(&p, 0, sizeof p);
+  if (int rc = make_map_2d(&p.tmap_a, A, dt, 2, static_cast<uint64_t>(K), static_cast<uint64_t>(M),
+                           static_cast<uint64_t>(lda), 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+    return rc;
+  if (int rc = make_map_2d(&p.tmap_b1, B1, dt, 2, static_cast<uint64_t>(K), static_cast<uint64_t>(N1),
+                           static_cast<uint64_t>(ldb1), 64, static_cast<uint32_t>(N1), CU_TENSOR_MAP_SWIZZLE_128B))
+    return rc;
+  if (int rc = make_map_2d(&p.tmap_b2, B2, dt, 2, static_cast<uint64_t>(N1), static_cast<uint64_t>(N2),
+                           static_cast<uint64_t>(ldb2), 64, CHAIN_BN2, CU_TENSOR_MAP_SWIZZLE_128B))
+    return rc;
+  const CUtensorMapDataType et = e_type == TCG_BF16  ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                 : e_type == TCG_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                     : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  if (int rc = make_map_2d(&p.tmap_e, E, et, es, static_cast<uint64_t>(N2), static_cast<uint64_t>(M),
+                           static_cast<uint64_t>(lde), static_cast<uint32_t>(64 / es), 32, CU_TENSOR_MAP_SWIZZLE_64B))
+    return rc;
+  p.M = static_cast<int>(M);
+  p.N1 = static_cast<int>(N1);
+  p.N2 = static_cast<int>(N2);
+  p.K = static_cast<int>(K);
+  p.m_tiles = static_cast<int>(cdiv(M, 128));
+  p.n2_tiles = static_cast<int>(cdiv(N2, CHAIN_BN2));
+  // Fewer row tiles than SMs: split the E tiles into groups (each group's
+  // unit recomputes its 128 rows of C) so that about every SM has a unit.
+  const int64_t groups_wanted = std::max<int64_t>(1, std::min<int64_t>(p.n2_tiles, d->sms / p.m_tiles));
+  p.tiles_per_group = static_cast<int>(cdiv(p.n2_tiles, groups_wanted));
+  const int64_t groups = cdiv(p.n2_tiles, p.tiles_per_group);
+  if (static_cast<int64_t>(p.m_tiles) * groups > INT32_MAX / 2) return TCG_ERR_UNSUPPORTED;
+  p.num_units = static_cast<int>(p.m_tiles * groups);
+  p.k1_blocks = static_cast<int>(cdiv(K, 64));
+  p.k2_blocks = static_cast<int>(cdiv(N1, 64));
+  p.k2_steps = static_cast<int>(N1 / 16);
+  const bool bf = in == TCG_IN_BF16;
+  p.idesc1 = idesc_f16(bf, true, false, false, 128, static_cast<int>(N1));
+  p.idesc2 = idesc_f16(bf, true, false, false, 128, CHAIN_BN2);
+  p.in_bf16 = bf ? 1 : 0;
+  p.e_type = e_type == TCG_F32 ? OUT_F32 : e_type == TCG_F16 ? OUT_F16 : OUT_BF16;
+  p.err = d->err;
+  p.timeout_ns = g_timeout_ns.load();
+  const int grid = static_cast<int>(std::min<int64_t>(p.num_units, d->sms));
+  const cudaError_t e = launch_chain(p, grid, s);
+  if (e != cudaSuccess) return record_cuda(e);
+  t_last_launches = 1;
+  t_plan.valid = true;
+  t_plan.k_zero = false;
+  t_plan.cg = 1;
+  t_plan.bn = CHAIN_BN2;
+  t_plan.clusters = grid;
+  t_plan.split = 1;
+  t_plan.swapped = false;
+  t_plan.stream_k = false;
+  t_plan.frag = false;
+  return TCG_OK;
+}
+
 }  // namespace
 
 extern "C" {
+
+int tcg_gemm_chain(tcg_input in_type, int64_t M, int64_t N1, int64_t N2, int64_t K, const void* A, int64_t lda,
+                   const void* B1, int64_t ldb1, const void* B2, int64_t ldb2, void* E, tcg_dtype e_type, int64_t lde,
+                   void* stream) {
+  return run_chain(in_type, M, N1, N2, K, A, lda, B1, ldb1, B2, ldb2, E, e_type, lde,
+                   reinterpret_cast<cudaStream_t>(stream));
+}
 
 int tcg_gemm(const tcg_gemm_args* args, void* stream) {
   return run_gemm(args, reinterpret_cast<cudaStream_t>(stream));

@@ -55,6 +55,10 @@ cudaError_t launch_sf_prepare_pair(tcg_input t, const uint8_t* sfa, int64_t rows
 // (splitk_reduce.cu); launched after the GEMM on the same stream.
 cudaError_t launch_splitk_reduce(const GemmParams& p, int cg, int num_clusters, cudaStream_t stream);
 
+// Chained GEMM kernel launch (gemm_chain.cu).
+struct ChainParams;
+cudaError_t launch_chain(const ChainParams& p, int grid, cudaStream_t stream);
+
 // Host state helpers (api.cu).
 int record_cuda(cudaError_t e);              // stores the message, returns TCG_ERR_CUDA (or TCG_OK)
 int current_device_checked(int* dev);        // TCG_OK if the current device is usable sm_103

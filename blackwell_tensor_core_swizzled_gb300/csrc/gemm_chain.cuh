@@ -1,0 +1,49 @@
+// Chained GEMM E = round(A . B1) . B2 with the intermediate kept in tensor
+// memory as the second product's A operand ("tcgen05.mma" page, "Operands and
+// repeat axes": A may come from shared memory or TMEM).  Parameters shared by
+// the kernel (gemm_chain.cu) and the host entry point (api.cu).
+#pragma once
+
+#include <cuda.h>
+
+#include <cstdint>
+
+namespace tcg {
+
+struct ChainParams {
+  CUtensorMap tmap_a;   // A [M][K], 64-element x 128-row boxes, 128-byte swizzle
+  CUtensorMap tmap_b1;  // B1 [N1][K], 64-element x N1-row boxes
+  CUtensorMap tmap_b2;  // B2 [N2][N1], 64-element x CHAIN_BN2-row boxes
+  CUtensorMap tmap_e;   // E [M][N2], 32-row x 64-byte boxes, 64-byte swizzle
+  int M, N1, N2, K;
+  int m_tiles;          // 128-row tiles of A / E
+  int n2_tiles;         // CHAIN_BN2-column tiles of E
+  int tiles_per_group;  // E tiles one unit computes
+  int num_units;        // m_tiles x groups; unit u -> (u % m_tiles, group u / m_tiles)
+  int k1_blocks;        // ring stages of the first product (64 K each)
+  int k2_blocks;        // ring stages of the second product (64 of N1 each)
+  int k2_steps;         // second-product MMAs: N1 / 16
+  uint32_t idesc1, idesc2;
+  int in_bf16;          // operand type (and the intermediate's): bf16, else f16
+  int e_type;           // OutType of E
+  unsigned long long* err;
+  uint64_t timeout_ns;
+};
+
+// E tiles of 128 columns in two accumulators at TMEM columns 256 and 384,
+// beside the intermediate (fp32 at columns [0, N1), rewritten in place as
+// 16-bit pairs at [0, N1/2) for the second product's A operand)
+constexpr int CHAIN_BN2 = 128;
+constexpr int CHAIN_D_COL0 = 256;
+constexpr int CHAIN_STAGES = 4;
+constexpr int CHAIN_STAGE_BYTES = 48 * 1024;  // A (16 KiB) + B1 (up to 256 rows, 32 KiB); B2 uses 16 KiB
+constexpr int CHAIN_EPI_WARPS = 8;
+constexpr int CHAIN_THREADS = 32 * (4 + CHAIN_EPI_WARPS);
+constexpr int CHAIN_EPI_OFF = CHAIN_STAGES * CHAIN_STAGE_BYTES;
+constexpr int CHAIN_BAR_OFF = CHAIN_EPI_OFF + CHAIN_EPI_WARPS * 32 * 64;
+// full[S], empty[S], c_full, a2_ready, conv_mid, d_full[2], d_empty[2], drain
+constexpr int CHAIN_NUM_BARS = 2 * CHAIN_STAGES + 8;
+constexpr int CHAIN_SMEM_BYTES = 1024 + CHAIN_BAR_OFF + CHAIN_NUM_BARS * 8 + 16;
+static_assert(CHAIN_SMEM_BYTES <= 232448, "dynamic shared memory");
+
+}  // namespace tcg

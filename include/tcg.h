@@ -250,6 +250,32 @@ typedef struct {
 int tcg_gemm(const tcg_gemm_args* args, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Chained GEMM with the intermediate in tensor memory ("tcgen05.mma" page,
+ * "Operands and repeat axes": the A operand may come from shared memory or
+ * from TMEM).
+ *
+ *     C = A . B1            fp32 accumulation, rounded (RNE) to in_type
+ *     E = C . B2            fp32 accumulation, stored as e_type
+ *
+ * A [M][K], B1 [N1][K] and B2 [N2][N1] are f16 or bf16 (in_type TCG_IN_F16 /
+ * TCG_IN_BF16), all K-major with 16-byte aligned bases and leading
+ * dimensions in elements (0 = packed) whose byte size is a multiple of 16;
+ * E is row-major [M][lde] (0 = N2) with a 16-byte aligned base and row
+ * stride (TCG_ERR_ALIGNMENT otherwise).  N1 is a multiple of 16 in [16, 256]
+ * (TCG_ERR_INVALID otherwise).  The result equals two tcg_gemm calls with a
+ * C of in_type in between, without C ever reaching global memory: each CTA
+ * computes 128 rows of C into TMEM, rewrites them there as 16-bit pairs
+ * (row m in lane m, element k in column k/2) and issues the second product's
+ * MMAs with A read from TMEM, for 128-column tiles of E.  When there are
+ * fewer 128-row tiles than SMs the E tiles are split into groups and each
+ * group recomputes its rows of C.  M == 0 or N2 == 0: no-op; K == 0: E is
+ * zeroed.  One kernel launch; asynchronous on `stream`. */
+int tcg_gemm_chain(tcg_input in_type, int64_t M, int64_t N1, int64_t N2, int64_t K,
+                   const void* A, int64_t lda, const void* B1, int64_t ldb1,
+                   const void* B2, int64_t ldb2, void* E, tcg_dtype e_type, int64_t lde,
+                   void* stream);
+
+/* ---------------------------------------------------------------------------
  * Block-scale layout (the scale-factor rearrangement step).
  *
  * The "tcgen05.mma" page places the scale of row r at TMEM lane r%32,

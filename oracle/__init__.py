@@ -9,6 +9,8 @@ CUDA path.
   S = sum |a||b| in float64, from the raw storage bits (C, ``gemm_oracle.c``):
   fp32, f16, bf16, E4M3, E5M2, and the packed microscaling formats E3M2 /
   E2M3 (6 bits) and E2M1 (4 bits).
+* :func:`gemm_chain` -- E = round(A.B1).B2, the product through a 16-bit
+  intermediate, as two :func:`gemm` calls around :func:`encode_rne`.
 * :mod:`oracle.layouts` -- the pages' descriptor walk, swizzles, TMEM
   register images, ldmatrix ownership and scale-factor placement.
 
@@ -142,3 +144,37 @@ def gemm(M: int, N: int, K: int, A: np.ndarray, a_type: int, a_major: int, lda: 
     if rc != 0:
         raise RuntimeError(f"oracle_gemm failed with {rc}")
     return D, S
+
+
+def encode_rne(x: np.ndarray, dtype: int) -> np.ndarray:
+    """Round float64 values to f16 or bf16, nearest with ties to even, and
+    return the storage bits (uint16).  f16 is numpy's correctly rounded
+    float64 -> float16 conversion; bf16 (8 significant bits, exponent range
+    of fp32) rounds x / q to an even integer with q the spacing of bf16
+    numbers at |x| (2^(e-8) for |x| in [2^(e-1), 2^e), 2^-133 below the
+    normal range), which is exact because q is a power of two; the result
+    is an fp32 value whose upper 16 bits are the bf16 bits."""
+    x = np.asarray(x, dtype=np.float64)
+    if dtype == F16:
+        return x.astype(np.float16).view(np.uint16)
+    if dtype != BF16:
+        raise ValueError("encode_rne: f16 or bf16")
+    _, e = np.frexp(x)
+    q = np.ldexp(1.0, np.maximum(e - 8, -133))
+    y = np.rint(x / q) * q
+    y = np.where(np.abs(y) > 3.3895313892515355e38, np.copysign(np.inf, x), y)
+    return (y.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+def gemm_chain(M: int, N1: int, N2: int, K: int, A: np.ndarray, B1: np.ndarray, B2: np.ndarray, dtype: int,
+               lda: int = 0, ldb1: int = 0, ldb2: int = 0, rows=None):
+    """E = round(A . B1) . B2 in float64 for the requested rows, with the
+    intermediate C = A . B1 rounded to ``dtype`` (f16 / bf16) as a 16-bit
+    intermediate would be; A [M][K], B1 [N1][K], B2 [N2][N1] are K-major
+    storage bits.  Returns (E, S2, C, S1): S2 = sum |round(C)||B2| and
+    S1 = sum |A||B1| are the error scales of the two products, C the exact
+    float64 intermediate."""
+    C, S1 = gemm(M, N1, K, A, dtype, K_MAJOR, lda or K, B1, dtype, K_MAJOR, ldb1 or K, rows=rows)
+    Cbits = encode_rne(C, dtype)
+    E, S2 = gemm(C.shape[0], N2, N1, Cbits, dtype, K_MAJOR, N1, B2, dtype, K_MAJOR, ldb2 or N1)
+    return E, S2, C, S1

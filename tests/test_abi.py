@@ -115,6 +115,27 @@ def test_generic_entry_point_rejects_unknown_epilogue(tcg):
         assert rc == tcg.ERR_INVALID
 
 
+def test_chain_validation_before_any_device_work(tcg):
+    # tcg_gemm_chain(in, M, N1, N2, K, A, lda, B1, ldb1, B2, ldb2, E, e_type, lde, stream)
+    def call(in_type=1, M=64, N1=32, N2=64, K=64, A=0x10000, lda=64, B1=0x20000, ldb1=64, B2=0x30000, ldb2=32,
+             E=0x40000, et=0, lde=64):
+        return tcg.raw_call("tcg_gemm_chain", in_type, M, N1, N2, K, A, lda, B1, ldb1, B2, ldb2, E, et, lde, None)
+    assert call(in_type=2) == tcg.ERR_INVALID                 # tf32: 16-bit operands only
+    for n1 in (0, 8, 40, 272):
+        assert call(N1=n1) == tcg.ERR_INVALID                 # N1 a multiple of 16 in [16, 256]
+    assert call(M=-1) == tcg.ERR_INVALID
+    assert call(et=5) == tcg.ERR_INVALID
+    assert call(E=None) == tcg.ERR_INVALID
+    assert call(lde=32) == tcg.ERR_INVALID                    # lde < N2
+    assert call(E=0x40008) == tcg.ERR_ALIGNMENT               # E base
+    assert call(et=2, lde=68) == tcg.ERR_ALIGNMENT            # 136-byte rows of E
+    assert call(A=0x10008) == tcg.ERR_ALIGNMENT
+    assert call(lda=60) == tcg.ERR_INVALID                    # lda < K
+    assert call(ldb2=16) == tcg.ERR_INVALID                   # ldb2 < N1
+    assert call(M=0, A=None, B1=None, B2=None, E=None) == tcg.OK
+    assert call(N2=0, A=None, B1=None, B2=None, E=None) == tcg.OK
+
+
 def test_empty_problems_are_noops(tcg):
     # M == 0 or N == 0 returns before any device work, even with null pointers
     assert _call(tcg, "bf16", M=0, A=None, B=None, D=None) == tcg.OK

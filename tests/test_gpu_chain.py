@@ -1,0 +1,150 @@
+"""Chained GEMM E = round(A.B1).B2 with the intermediate kept in tensor memory
+as the second product's A operand, against the float64 oracle's
+``gemm_chain`` (two oracle products around a round-to-nearest-even 16-bit
+intermediate)."""
+import numpy as np
+import pytest
+import torch
+
+from gpu_helpers import OUT, U_OUT
+
+pytestmark = pytest.mark.gpu
+
+TAU = 2e-3
+IN = {"f16": (0, torch.float16), "bf16": (1, torch.bfloat16)}   # tcg_input
+ORACLE = {"f16": 1, "bf16": 2}
+ULP = {"f16": 2.0 ** -10, "bf16": 2.0 ** -7}   # spacing of 16-bit numbers, relative
+
+
+@pytest.fixture(scope="module")
+def tcg():
+    assert torch.cuda.is_available(), "GPU tests need a GPU"
+    from blackwell_tensor_core_swizzled_gb300 import build
+    build.build()
+    import blackwell_tensor_core_swizzled_gb300 as m
+    return m
+
+
+def _inputs(dt, M, N1, N2, K, seed, integers=False):
+    g = torch.Generator().manual_seed(seed)
+    tdt = IN[dt][1]
+    if integers:
+        mk = lambda *s: torch.randint(-2, 3, s, generator=g).to(tdt)
+    else:
+        mk = lambda *s: torch.randn(*s, generator=g).to(tdt)
+    return mk(M, K), mk(N1, K), mk(N2, N1)
+
+
+def _bits(t):
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def _run(tcg, dt, A, B1, B2, out, lde=None, E=None):
+    M, K = A.shape
+    N1, N2 = B1.shape[0], B2.shape[0]
+    lde = lde or N2
+    if E is None:
+        E = torch.full((M, lde), float("nan"), dtype=OUT[out][1], device="cuda")
+    tcg.gemm_chain(IN[dt][0], M, N1, N2, K, A.cuda(), K, B1.cuda(), K, B2.cuda(), N1, E, OUT[out][0], lde)
+    assert tcg.check() == 0
+    return E
+
+
+def _check(oracle_mod, dt, A, B1, B2, E, out, rows):
+    M, K = A.shape
+    N1, N2 = B1.shape[0], B2.shape[0]
+    ref, S2, C, S1 = oracle_mod.gemm_chain(M, N1, N2, K, _bits(A), _bits(B1), _bits(B2), ORACLE[dt], rows=rows)
+    got = E[rows, :N2].double().cpu().numpy()
+    assert np.all(np.isfinite(got))
+    # the GPU's fp32 intermediate is within TAU*S1 of the exact one; rounding
+    # both to 16 bits can differ by that plus one spacing of the type
+    dC = TAU * S1 + ULP[dt] * (np.abs(C) + TAU * S1)
+    bound = dC @ np.abs(B2.double().numpy()).T + TAU * S2
+    bound = bound + U_OUT[out] * (np.abs(ref) + bound)
+    bad = np.abs(got - ref) > bound
+    assert not bad.any(), (int(bad.sum()), np.argwhere(bad)[:5].tolist())
+
+
+EXACT = [
+    # dt, M, N1, N2, K   (integers in [-2, 2]: every step exact, E bit for bit)
+    ("bf16", 128, 16, 128, 64),
+    ("bf16", 300, 48, 520, 120),
+    ("f16", 257, 256, 200, 48),
+    ("bf16", 1000, 128, 1032, 72),
+    ("f16", 64, 80, 384, 200),
+]
+
+
+@pytest.mark.parametrize("dt,M,N1,N2,K", EXACT)
+def test_chain_exact_on_small_integers(tcg, oracle_mod, dt, M, N1, N2, K):
+    A, B1, B2 = _inputs(dt, M, N1, N2, K, seed=M + N1, integers=True)
+    E = _run(tcg, dt, A, B1, B2, "f32")
+    ref, _, _, _ = oracle_mod.gemm_chain(M, N1, N2, K, _bits(A), _bits(B1), _bits(B2), ORACLE[dt])
+    assert np.array_equal(E.double().cpu().numpy(), ref)
+
+
+RANDOM = [
+    # dt, M, N1, N2, K, out
+    ("bf16", 300, 64, 520, 256, "bf16"),
+    ("bf16", 2048, 256, 1024, 512, "f32"),
+    ("f16", 1000, 112, 2000, 1000, "f16"),
+    ("bf16", 256, 256, 4000, 4096, "bf16"),     # 2 row tiles: E tiles split over many units
+    ("bf16", 152 * 128 * 2 + 77, 128, 384, 512, "bf16"),  # more row tiles than SMs, ragged
+]
+
+
+@pytest.mark.parametrize("dt,M,N1,N2,K,out", RANDOM)
+def test_chain_random_within_the_composed_bound(tcg, oracle_mod, dt, M, N1, N2, K, out):
+    A, B1, B2 = _inputs(dt, M, N1, N2, K, seed=7 * M + K)
+    E = _run(tcg, dt, A, B1, B2, out)
+    rows = list(range(M)) if M <= 1024 else sorted({0, 1, 127, 128, 255, M // 2, M - 129, M - 2, M - 1} |
+                                                    set(np.random.default_rng(M).integers(0, M, 16).tolist()))
+    _check(oracle_mod, dt, A, B1, B2, E, out, rows)
+
+
+def test_chain_matches_two_calls_through_a_16_bit_intermediate(tcg):
+    # the same products through global memory: C = A.B1 stored as bf16, then
+    # E = C.B2 (fp32 accumulation both times).  The MMAs see the same operands
+    # in the same K order whether A comes from shared memory or from TMEM, so
+    # the two agree bit for bit (measured); the bound below is what the
+    # arithmetic alone guarantees
+    dt, M, N1, N2, K = "bf16", 1024, 192, 640, 768
+    A, B1, B2 = _inputs(dt, M, N1, N2, K, seed=11)
+    E = _run(tcg, dt, A, B1, B2, "f32")
+    C = torch.empty((M, N1), dtype=torch.bfloat16, device="cuda")
+    tcg.gemm_bf16(M, N1, K, A.cuda(), 0, K, B1.cuda(), 0, K, C, 2, N1, 0)
+    E2 = torch.empty((M, N2), dtype=torch.float32, device="cuda")
+    tcg.gemm_bf16(M, N2, N1, C, 0, N1, B2.cuda(), 0, N1, E2, 0, N2, 0)
+    assert tcg.check() == 0
+    S = (C.double().abs() @ B2.cuda().double().abs().T)
+    diff = (E.double() - E2.double()).abs()
+    # an intermediate element may round the other way (one 16-bit spacing)
+    assert bool((diff <= (ULP[dt] + 2 * TAU) * S + 1e-30).all())
+    assert torch.equal(E, E2)
+
+
+def test_chain_edges(tcg, oracle_mod):
+    dt = "bf16"
+    # K = 0: E is zeroed
+    E = torch.full((50, 40), 3.0, dtype=torch.float32, device="cuda")
+    z = torch.zeros(0, dtype=torch.bfloat16, device="cuda")
+    B2 = torch.zeros((40, 16), dtype=torch.bfloat16, device="cuda")
+    tcg.gemm_chain(1, 50, 16, 40, 0, z, 0, z, 0, B2, 16, E, 0, 40)
+    assert tcg.check() == 0 and bool((E == 0).all())
+    # M == 0 / N2 == 0: nothing happens, even with null pointers
+    assert tcg.gemm_chain(1, 0, 16, 40, 64, None, 0, None, 0, None, 0, None, 0, 0, check=False) == 0
+    assert tcg.gemm_chain(1, 50, 16, 0, 64, None, 0, None, 0, None, 0, None, 0, 0, check=False) == 0
+    A, B1, B2 = _inputs(dt, 64, 32, 64, 64, seed=1)
+    A, B1, B2 = A.cuda(), B1.cuda(), B2.cuda()
+    E = torch.zeros((64, 72), dtype=torch.float32, device="cuda")
+    for n1 in (0, 8, 24, 272):   # N1 a multiple of 16 in [16, 256]
+        assert tcg.gemm_chain(1, 64, n1, 64, 64, A, 64, B1, 64, B2, 32, E, 0, 72, check=False) == tcg.ERR_INVALID
+    # E's row stride must be a 16-byte multiple for its tile stores
+    Ebf = torch.zeros((64, 68), dtype=torch.bfloat16, device="cuda")
+    assert tcg.gemm_chain(1, 64, 32, 64, 64, A, 64, B1, 64, B2, 32, Ebf, 2, 67,
+                          check=False) == tcg.ERR_ALIGNMENT
+    # a padded E (lde > N2) leaves the padding alone
+    E = torch.full((64, 72), 5.0, dtype=torch.float32, device="cuda")
+    tcg.gemm_chain(1, 64, 32, 64, 64, A, 64, B1, 64, B2, 32, E, 0, 72)
+    assert tcg.check() == 0 and bool((E[:, 64:] == 5.0).all())
+    _check(oracle_mod, dt, A.cpu(), B1.cpu(), B2.cpu(), E, "f32", list(range(64)))

@@ -345,3 +345,76 @@ def test_block16_scales_identity_closed_form(oracle_mod):
     D32, _ = oracle_mod.gemm(K, N, K, A, oracle_mod.E2M1, 0, K, B, oracle_mod.E2M1, 0, K, SFA=sfa32, SFB=sfb32,
                              sf_block=32, sf_kind=oracle_mod.SF_UE4M3)
     assert not np.array_equal(D32, D)
+
+
+# ------------------------------------------------------------------ chained product
+
+def test_encode_rne_bf16_matches_torch_rounding_of_fp32(oracle_mod):
+    # torch rounds fp32 -> bf16 to nearest, ties to even; on fp32 inputs the
+    # float64 encoder must agree bit for bit, including ties, subnormals and
+    # values that round up into the next binade
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal(20000).astype(np.float32) * np.float32(2.0) ** rng.integers(-20, 20, 20000)
+    ties = (np.arange(0x3F800000, 0x3F800000 + 64 * 0x10000, 0x10000, dtype=np.uint64) + 0x8000).astype(np.uint32)
+    special = np.array([0x3FFF8000, 0x3FFFFFFF, 0x00008000, 0x00018000, 0x007F8000, 0x80018000, 0x3F808000,
+                        0x3F818000], dtype=np.uint32)
+    x = np.concatenate([x, ties.view(np.float32), special.view(np.float32)])
+    got = oracle_mod.encode_rne(x.astype(np.float64), oracle_mod.BF16)
+    want = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(got, want)
+
+
+def test_encode_rne_closed_forms(oracle_mod):
+    # halfway cases go to the even neighbour: bf16 has 8 significant bits,
+    # f16 11 (1.0 = 0x3F80 / 0x3C00)
+    bf = oracle_mod.encode_rne(np.array([1.0, 1 + 2 ** -7, 1 + 2 ** -8, 1 + 3 * 2 ** -8, -(1 + 2 ** -9)]),
+                               oracle_mod.BF16)
+    assert bf.tolist() == [0x3F80, 0x3F81, 0x3F80, 0x3F82, 0xBF80]
+    h = oracle_mod.encode_rne(np.array([1.0, 1 + 2 ** -10, 1 + 2 ** -11, 1 + 3 * 2 ** -11, 65504.0]),
+                              oracle_mod.F16)
+    assert h.tolist() == [0x3C00, 0x3C01, 0x3C00, 0x3C02, 0x7BFF]
+
+
+def _bits16(x, dtype):
+    t = torch.from_numpy(np.asarray(x, dtype=np.float32)).to(dtype)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f16"])
+def test_gemm_chain_small_integers_is_the_plain_product(oracle_mod, dt):
+    # integers in [-2, 2] with K = 48: C is an integer of magnitude <= 192,
+    # exact in both 16-bit types, so E = (A B1) B2 exactly
+    rng = np.random.default_rng(5)
+    M, N1, N2, K = 40, 32, 24, 48
+    a, b1, b2 = (rng.integers(-2, 3, size=s).astype(np.float64) for s in ((M, K), (N1, K), (N2, N1)))
+    tdt, odt = {"bf16": (torch.bfloat16, oracle_mod.BF16), "f16": (torch.float16, oracle_mod.F16)}[dt]
+    E, S2, C, S1 = oracle_mod.gemm_chain(M, N1, N2, K, _bits16(a, tdt), _bits16(b1, tdt), _bits16(b2, tdt), odt)
+    assert np.array_equal(C, a @ b1.T)
+    assert np.array_equal(E, (a @ b1.T) @ b2.T)
+    assert np.array_equal(S2, np.abs(a @ b1.T) @ np.abs(b2.T))
+    assert np.array_equal(S1, np.abs(a) @ np.abs(b1.T))
+
+
+def test_gemm_chain_rounds_the_intermediate(oracle_mod):
+    # C = 1 + 2^-9 is not a bf16 number and rounds to 1 (f16 keeps it), so
+    # E = B2 row sums scaled by the rounded C, not by the exact one
+    M, N1, N2, K = 1, 16, 8, 2
+    a = np.array([[1.0, 2 ** -9]])
+    b1 = np.ones((N1, K))
+    b2 = np.arange(N2 * N1, dtype=np.float64).reshape(N2, N1) / 16
+    for tdt, odt, c in ((torch.bfloat16, oracle_mod.BF16, 1.0), (torch.float16, oracle_mod.F16, 1 + 2 ** -9)):
+        E, _, C, _ = oracle_mod.gemm_chain(M, N1, N2, K, _bits16(a, tdt), _bits16(b1, tdt), _bits16(b2, tdt), odt)
+        assert np.all(C == 1 + 2 ** -9)
+        assert np.array_equal(E, np.full((1, N1), c) @ b2.T)
+
+
+def test_gemm_chain_identity_second_factor_returns_the_rounded_intermediate(oracle_mod):
+    rng = np.random.default_rng(9)
+    M, N1, K = 30, 48, 200
+    a = rng.standard_normal((M, K)).astype(np.float32)
+    b1 = rng.standard_normal((N1, K)).astype(np.float32)
+    eye = np.eye(N1, dtype=np.float32)
+    E, _, C, _ = oracle_mod.gemm_chain(M, N1, N1, K, _bits16(a, torch.bfloat16), _bits16(b1, torch.bfloat16),
+                                       _bits16(eye, torch.bfloat16), oracle_mod.BF16)
+    rounded = torch.from_numpy(oracle_mod.encode_rne(C, oracle_mod.BF16).view(np.int16)).view(torch.bfloat16)
+    assert np.array_equal(E, rounded.double().numpy())
