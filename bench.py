@@ -389,6 +389,69 @@ def roofline(w, kernel_ms, peaks, traffic, timed_s):
             "kernel": "tcg::gemm_kernel", "algorithmic_flops_per_launch": flops}
 
 
+def run_chain_workload(tcg, torch, w, steps, warmup):
+    """Device-timed chained GEMM E = round(A.B1).B2 (tcg_gemm_chain): one
+    launch per step, CUDA events around each.  Inputs (A and E larger than the
+    L2) are resident on the device."""
+    x = syn.make_chain_inputs(w)
+    M, N1, N2, K = x["M"], x["N1"], x["N2"], x["K"]
+    A, B1, B2 = (to_dev(x[k], torch) for k in ("A", "B1", "B2"))
+    out_t = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[w.out]
+    E = torch.empty((M, N2), dtype=out_t, device="cuda")
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+
+    def call():
+        tcg.gemm_chain(IN_TYPE[w.dtype], M, N1, N2, K, A, K, B1, K, B2, N1, E, OUT[w.out], N2, stream=sp)
+
+    for _ in range(warmup):
+        call()
+    rc = tcg.check(sp)
+    if rc != 0:
+        raise RuntimeError(f"chain warm-up failed: {tcg.status_string(rc)} {tcg.last_error_string()}")
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    torch.cuda.synchronize()
+    launches = 0
+    t0 = time.time()
+    for i in range(steps):
+        kev[i][0].record(stream)
+        call()
+        launches += tcg.last_launch_count()
+        kev[i][1].record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    rc = tcg.check(sp)
+    if rc != 0:
+        raise RuntimeError(f"chain run failed: {tcg.status_string(rc)}")
+    kernel_ms = float(np.mean([a.elapsed_time(b) for a, b in kev]))
+    return {"kernel_ms": kernel_ms, "launches": launches, "t0": t0, "t1": t1,
+            "flops": 2.0 * M * K * N1 + 2.0 * M * N1 * N2,
+            "bytes": float(ESIZE[w.dtype] * (M * K + N1 * K + N2 * N1) + OUT_BYTES[w.out] * M * N2)}
+
+
+def chain_roofline(w, r, peaks):
+    """The chain's roofline is the larger of its tensor time (both products at
+    the bf16 peak) and its HBM time (A, B1, B2 read and E written once)."""
+    t_tensor = r["flops"] / (peaks["bf16_tflops"] * 1e12)
+    t_hbm = r["bytes"] / (peaks["hbm_gbs"] * 1e9)
+    t = r["kernel_ms"] * 1e-3
+    if t_hbm >= t_tensor:
+        achieved = r["bytes"] / t / 1e9
+        return {"bound": "hbm", "achieved": round(achieved, 1), "peak": round(peaks["hbm_gbs"], 1), "unit": "GB/s",
+                "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+                "peak_source": f"{peaks['source']} HBM copy bandwidth (tensor time at the bf16 burst peak: "
+                               f"{t_tensor * 1e6:.1f} us, HBM time {t_hbm * 1e6:.1f} us)",
+                "kernel": "tcg::gemm_chain_kernel", "algorithmic_bytes_per_launch": r["bytes"],
+                "algorithmic_flops_per_launch": r["flops"]}
+    achieved = r["flops"] / t / 1e12
+    return {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(peaks["bf16_tflops"], 1),
+            "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": None,
+            "peak_source": f"{peaks['source']} bf16 burst (HBM time {t_hbm * 1e6:.1f} us, tensor time "
+                           f"{t_tensor * 1e6:.1f} us)",
+            "kernel": "tcg::gemm_chain_kernel", "algorithmic_bytes_per_launch": r["bytes"],
+            "algorithmic_flops_per_launch": r["flops"]}
+
+
 # ----------------------------------------------------------------- CPU (oracle) arm
 
 def oracle_inputs(w):
@@ -468,10 +531,11 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="bf16_8192_cta2", choices=sorted(syn.WORKLOADS))
+    ap.add_argument("--workload", default="bf16_8192_cta2",
+                    choices=sorted(n for n, v in syn.WORKLOADS.items() if "chain_n1" not in v.extra))
     ap.add_argument("--secondary",
                     default="mxf8_8192,bf16_skinny_m16,bf16_4096_kmn_cta1,tf32_2048x2048x8192,f16acc_8192_cta2,"
-                            "mxf6_e2m3_8192,mxf4_8192,nvf4_8192",
+                            "mxf6_e2m3_8192,mxf4_8192,nvf4_8192,chain_bf16_38912x256x4096",
                     help="comma list of extra workloads ('' for none)")
     ap.add_argument("--sustained-s", type=float, default=1.5,
                     help="length of the back-to-back sustained pass of the headline workload (0: skip)")
@@ -543,6 +607,13 @@ def main():
         sec = []
         for name in [s for s in args.secondary.split(",") if s and s != w.name]:
             ws = syn.WORKLOADS[name]
+            if "chain_n1" in ws.extra:
+                rc2 = run_chain_workload(tcg, torch, ws, args.steps, args.warmup)
+                rl2 = chain_roofline(ws, rc2, peaks)
+                sec.append({"workload": name, "value": round(rc2["flops"] / (rc2["kernel_ms"] * 1e-3) / 1e12, 1),
+                            "unit": UNIT, "ms_per_step": round(rc2["kernel_ms"], 4), "dtype": ws.dtype,
+                            "gpu_launches": rc2["launches"], "roofline": rl2})
+                continue
             r2 = run_workload(tcg, torch, ws, args.steps, args.warmup, dctx, measure_e2e=False)
             # steps of an hbm workload include an L2 flush: count the GEMM time only
             local = r2["kernel_ms"] * args.steps if ws.extra.get("bound") == "hbm" else r2["total_ms"]

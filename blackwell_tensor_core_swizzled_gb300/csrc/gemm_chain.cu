@@ -230,14 +230,15 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) gemm_chain_kernel(const __gr
     const int q = warp & 3;           // TMEM lane quadrant
     const int part = (warp - 4) >> 2;  // 0 or 1: which half of the columns
     const uint32_t lanes = tmem_base + (static_cast<uint32_t>(32 * q) << 16);
-    const uint32_t buf = sbase + CHAIN_EPI_OFF + static_cast<uint32_t>((warp - 4) * 32 * 64);
+    const uint32_t buf0 = sbase + CHAIN_EPI_OFF + static_cast<uint32_t>((warp - 4) * CHAIN_EPI_BUFS * 32 * 64);
     const bool bf = p.in_bf16 != 0;
     uint32_t dt = 0, uc = 0, stores = 0;
     bool ok = true;
     // one 32-row x 64-byte tile of E at (row0, col0) through the staging buffer
     auto stage = [&](int row0, int col0, const uint32_t* h) {
-      if (stores > 0) {
-        if (lane == 0) bulk_wait_group_read<0>();  // the previous store has read the buffer
+      const uint32_t buf = buf0 + (stores % CHAIN_EPI_BUFS) * 32u * 64u;
+      if (stores >= static_cast<uint32_t>(CHAIN_EPI_BUFS)) {
+        if (lane == 0) bulk_wait_group_read<CHAIN_EPI_BUFS - 1>();  // this buffer's last store has read it
         __syncwarp();
       }
       const uint32_t rb = buf + 64u * static_cast<uint32_t>(lane);
@@ -264,16 +265,17 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) gemm_chain_kernel(const __gr
       tc_fence_after();
       uint32_t packed[4][16];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 4; c += 2) {  // two loads in flight per wait
         const int col = 128 * part + 32 * c;
-        if (col < p.N1) {
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(lanes + static_cast<uint32_t>(col), r);
-          tc_wait_ld();
+        uint32_t r[2][32];
+        if (col < p.N1) tmem_ld_32x32b_x32(lanes + static_cast<uint32_t>(col), r[0]);
+        if (col + 32 < p.N1) tmem_ld_32x32b_x32(lanes + static_cast<uint32_t>(col + 32), r[1]);
+        tc_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
 #pragma unroll
           for (int k = 0; k < 16; ++k)
-            packed[c][k] = bf ? pack_bf16(r[2 * k], r[2 * k + 1]) : pack_f16(r[2 * k], r[2 * k + 1]);
-        }
+            packed[c + i][k] = bf ? pack_bf16(r[i][2 * k], r[i][2 * k + 1]) : pack_f16(r[i][2 * k], r[i][2 * k + 1]);
       }
       tc_fence_before();
       __syncwarp();
@@ -299,28 +301,36 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) gemm_chain_kernel(const __gr
         }
         tc_fence_after();
         const uint32_t dcol = CHAIN_D_COL0 + CHAIN_BN2 * b;
-#pragma unroll 1
-        for (int c = part; c < CHAIN_BN2 / 32; c += 2) {
-          const int n0 = CHAIN_BN2 * t + 32 * c;
-          if (n0 >= p.N2) break;
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(lanes + dcol + 32u * c, r);
-          tc_wait_ld();
-          if (row0 >= p.M) continue;  // the map clips the rest of a ragged tile
-          if (p.e_type == OUT_F32) {
-            stage(row0, n0, r);
-            stage(row0, n0 + 16, r + 16);
-          } else {
-            uint32_t h[16];
-#pragma unroll
-            for (int k = 0; k < 16; ++k)
-              h[k] = p.e_type == OUT_BF16 ? pack_bf16(r[2 * k], r[2 * k + 1]) : pack_f16(r[2 * k], r[2 * k + 1]);
-            stage(row0, n0, h);
-          }
-        }
+        // this warp's two 32-column chunks (part, part + 2), both loads in
+        // flight before one wait, then the accumulator buffer is released
+        // before the stores
+        static_assert(CHAIN_BN2 == 128, "two chunks per epilogue warp");
+        const int n0 = CHAIN_BN2 * t + 32 * part;
+        uint32_t r[2][32];
+        tmem_ld_32x32b_x32(lanes + dcol + 32u * part, r[0]);
+        tmem_ld_32x32b_x32(lanes + dcol + 32u * (part + 2), r[1]);
+        tc_wait_ld();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(d_empty(b));
+        if (row0 < p.M) {  // the map clips the rest of a ragged tile
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const int col0 = n0 + 64 * i;
+            if (col0 >= p.N2) break;
+            if (p.e_type == OUT_F32) {
+              stage(row0, col0, r[i]);
+              stage(row0, col0 + 16, r[i] + 16);
+            } else {
+              uint32_t h[16];
+#pragma unroll
+              for (int k = 0; k < 16; ++k)
+                h[k] = p.e_type == OUT_BF16 ? pack_bf16(r[i][2 * k], r[i][2 * k + 1])
+                                            : pack_f16(r[i][2 * k], r[i][2 * k + 1]);
+              stage(row0, col0, h);
+            }
+          }
+        }
       }
     }
     if (lane == 0) bulk_wait_group_all();

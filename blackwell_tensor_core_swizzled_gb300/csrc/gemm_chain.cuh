@@ -39,8 +39,11 @@ constexpr int CHAIN_STAGES = 4;
 constexpr int CHAIN_STAGE_BYTES = 48 * 1024;  // A (16 KiB) + B1 (up to 256 rows, 32 KiB); B2 uses 16 KiB
 constexpr int CHAIN_EPI_WARPS = 8;
 constexpr int CHAIN_THREADS = 32 * (4 + CHAIN_EPI_WARPS);
+// per epilogue warp, CHAIN_EPI_BUFS staging tiles of 32 rows x 64 bytes: a
+// tile is rewritten only once the store before the last has read it
+constexpr int CHAIN_EPI_BUFS = 2;
 constexpr int CHAIN_EPI_OFF = CHAIN_STAGES * CHAIN_STAGE_BYTES;
-constexpr int CHAIN_BAR_OFF = CHAIN_EPI_OFF + CHAIN_EPI_WARPS * 32 * 64;
+constexpr int CHAIN_BAR_OFF = CHAIN_EPI_OFF + CHAIN_EPI_WARPS * CHAIN_EPI_BUFS * 32 * 64;
 // full[S], empty[S], c_full, a2_ready, conv_mid, d_full[2], d_empty[2], drain
 constexpr int CHAIN_NUM_BARS = 2 * CHAIN_STAGES + 8;
 constexpr int CHAIN_SMEM_BYTES = 1024 + CHAIN_BAR_OFF + CHAIN_NUM_BARS * 8 + 16;

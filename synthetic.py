@@ -85,7 +85,23 @@ WORKLOADS = {
                                 "normal", "f32", "bf16", 1, False, 6, {"bound": "hbm"}),
     "bf16_skinny_m128": Workload("bf16_skinny_m128", 128, 8192, 8192, "bf16", "k", "k",
                                  "normal", "f32", "bf16", 1, False, 7, {"bound": "hbm"}),
+    # Chained product E = round(A.B1).B2 with a 256-wide intermediate kept in
+    # tensor memory: M = 2 x 152 x 128 rows (two row tiles per SM), N = N2.
+    "chain_bf16_38912x256x4096": Workload("chain_bf16_38912x256x4096", 38912, 4096, 4096, "bf16", "k", "k",
+                                          "normal", "f32", "bf16", 1, False, 11, {"chain_n1": 256}),
 }
+
+
+def make_chain_inputs(w: Workload) -> dict:
+    """Storage bits of a chained workload: A [M][K], B1 [N1][K] and B2
+    [N][N1], all K-major; N(0,1) scaled by 1/sqrt of each product's K.
+    Seeds 1000+i (A), 2000+i (B1), 2500+i (B2)."""
+    n1 = w.extra["chain_n1"]
+    i = w.seed_base
+    A = to_bits(draw((w.M, w.K), 1000 + i, w.dist, w.K), w.dtype)
+    B1 = to_bits(draw((n1, w.K), 2000 + i, w.dist, w.K), w.dtype)
+    B2 = to_bits(draw((w.N, n1), 2500 + i, w.dist, n1), w.dtype)
+    return {"A": A, "B1": B1, "B2": B2, "M": w.M, "N1": n1, "N2": w.N, "K": w.K}
 
 
 def draw(shape, seed: int, dist: str, K: int) -> np.ndarray:

@@ -148,3 +148,17 @@ def test_chain_edges(tcg, oracle_mod):
     tcg.gemm_chain(1, 64, 32, 64, 64, A, 64, B1, 64, B2, 32, E, 0, 72)
     assert tcg.check() == 0 and bool((E[:, 64:] == 5.0).all())
     _check(oracle_mod, dt, A.cpu(), B1.cpu(), B2.cpu(), E, "f32", list(range(64)))
+
+
+def test_chain_bench_workload_sampled_rows(tcg, oracle_mod):
+    # the benchmark's chained workload at full size, its seeded inputs
+    import synthetic as syn
+    w = syn.WORKLOADS["chain_bf16_38912x256x4096"]
+    x = syn.make_chain_inputs(w)
+    to = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+    A, B1, B2 = to(x["A"]), to(x["B1"]), to(x["B2"])
+    E = _run(tcg, "bf16", A, B1, B2, w.out)
+    M = w.M
+    rows = sorted({0, 1, 31, 32, 127, 128, 255, 19456, M - 129, M - 2, M - 1} |
+                  set(np.random.default_rng(3).integers(0, M, 12).tolist()))
+    _check(oracle_mod, "bf16", A, B1, B2, E, w.out, rows)
