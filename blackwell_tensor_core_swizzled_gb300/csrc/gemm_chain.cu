@@ -9,9 +9,9 @@
 //            product in column k/2 -- the layout an A operand in tensor memory
 //            has ("tcgen05.mma" page, "Operands and repeat axes": A from
 //            "Shared or TMEM"; the layout pinned by the TMEM-A probe);
-//   phase 2  for each 128-column tile of E: N1/16 tcgen05.mma with A read
+//   phase 2  for each 192-column tile of E: N1/16 tcgen05.mma with A read
 //            from TMEM column 8*step and B2 from shared memory, into one of
-//            two accumulators (columns 256 and 384), drained by the epilogue
+//            two accumulators (columns 128 and 320), drained by the epilogue
 //            while the other fills.
 //
 // Warp roles as in the main kernel: warp 0 TMA producer (one ring for both
@@ -145,13 +145,15 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) gemm_chain_kernel(const __gr
     for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uc) {
       int mt, t0, t1;
       unit_tiles(u, mt, t0, t1);
-      // C and its 16-bit copy are rewritten: the previous unit's second
-      // product, which reads that copy, must have completed (its last
-      // accumulator commit)
-      if (dt > 0 && !wait_uniform(d_full((dt - 1) & 1u), ((dt - 1) >> 1) & 1u, wctx, SITE_MMA_ACC_EMPTY)) {
-        ok = false;
-        break;
+      // C (fp32) overlaps the first accumulator and its 16-bit copy is read
+      // by the previous unit's second product: both accumulators must have
+      // been drained (which follows their last MMAs' completion)
+      for (uint32_t back = 1; back <= 2 && ok; ++back) {
+        if (dt < back) break;
+        const uint32_t t = dt - back;
+        if (!wait_uniform(d_empty(t & 1u), (t >> 1) & 1u, wctx, SITE_MMA_ACC_EMPTY)) ok = false;
       }
+      if (!ok) break;
       tc_fence_after();
       for (int kb = 0; kb < p.k1_blocks; ++kb) {
         if (!wait_uniform(full_bar(s), ph, wctx, SITE_MMA_FULL)) {
@@ -301,36 +303,39 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) gemm_chain_kernel(const __gr
         }
         tc_fence_after();
         const uint32_t dcol = CHAIN_D_COL0 + CHAIN_BN2 * b;
-        // this warp's two 32-column chunks (part, part + 2), both loads in
-        // flight before one wait, then the accumulator buffer is released
-        // before the stores
-        static_assert(CHAIN_BN2 == 128, "two chunks per epilogue warp");
+        // this warp's three 32-column chunks (part, part + 2, part + 4): two
+        // loads in flight, their stores, the third load, then the
+        // accumulator is released before the third store
+        static_assert(CHAIN_BN2 == 192, "three chunks per epilogue warp");
         const int n0 = CHAIN_BN2 * t + 32 * part;
-        uint32_t r[2][32];
-        tmem_ld_32x32b_x32(lanes + dcol + 32u * part, r[0]);
-        tmem_ld_32x32b_x32(lanes + dcol + 32u * (part + 2), r[1]);
+        auto store_chunk = [&](int col0, const uint32_t* r) {
+          if (row0 >= p.M || col0 >= p.N2) return;  // the map clips the rest of a ragged tile
+          if (p.e_type == OUT_F32) {
+            stage(row0, col0, r);
+            stage(row0, col0 + 16, r + 16);
+          } else {
+            uint32_t h[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k)
+              h[k] = p.e_type == OUT_BF16 ? pack_bf16(r[2 * k], r[2 * k + 1]) : pack_f16(r[2 * k], r[2 * k + 1]);
+            stage(row0, col0, h);
+          }
+        };
+        {
+          uint32_t r[2][32];
+          tmem_ld_32x32b_x32(lanes + dcol + 32u * part, r[0]);
+          tmem_ld_32x32b_x32(lanes + dcol + 32u * (part + 2), r[1]);
+          tc_wait_ld();
+          store_chunk(n0, r[0]);
+          store_chunk(n0 + 64, r[1]);
+        }
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(lanes + dcol + 32u * (part + 4), r);
         tc_wait_ld();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(d_empty(b));
-        if (row0 < p.M) {  // the map clips the rest of a ragged tile
-#pragma unroll
-          for (int i = 0; i < 2; ++i) {
-            const int col0 = n0 + 64 * i;
-            if (col0 >= p.N2) break;
-            if (p.e_type == OUT_F32) {
-              stage(row0, col0, r[i]);
-              stage(row0, col0 + 16, r[i] + 16);
-            } else {
-              uint32_t h[16];
-#pragma unroll
-              for (int k = 0; k < 16; ++k)
-                h[k] = p.e_type == OUT_BF16 ? pack_bf16(r[i][2 * k], r[i][2 * k + 1])
-                                            : pack_f16(r[i][2 * k], r[i][2 * k + 1]);
-              stage(row0, col0, h);
-            }
-          }
-        }
+        store_chunk(n0 + 128, r);
       }
     }
     if (lane == 0) bulk_wait_group_all();

@@ -30,13 +30,15 @@ struct ChainParams {
   uint64_t timeout_ns;
 };
 
-// E tiles of 128 columns in two accumulators at TMEM columns 256 and 384,
-// beside the intermediate (fp32 at columns [0, N1), rewritten in place as
-// 16-bit pairs at [0, N1/2) for the second product's A operand)
-constexpr int CHAIN_BN2 = 128;
-constexpr int CHAIN_D_COL0 = 256;
+// E tiles of 192 columns in two accumulators at TMEM columns 128 and 320,
+// beside the 16-bit A operand at [0, N1/2) (the intermediate C, fp32 at
+// [0, N1), is rewritten there in place; while it is fp32 it overlaps the
+// first accumulator, so a row tile's first product starts once the previous
+// tile's accumulators are drained)
+constexpr int CHAIN_BN2 = 192;
+constexpr int CHAIN_D_COL0 = 128;
 constexpr int CHAIN_STAGES = 4;
-constexpr int CHAIN_STAGE_BYTES = 48 * 1024;  // A (16 KiB) + B1 (up to 256 rows, 32 KiB); B2 uses 16 KiB
+constexpr int CHAIN_STAGE_BYTES = 48 * 1024;  // A (16 KiB) + B1 (up to 256 rows, 32 KiB); B2 uses 24 KiB
 constexpr int CHAIN_EPI_WARPS = 8;
 constexpr int CHAIN_THREADS = 32 * (4 + CHAIN_EPI_WARPS);
 // per epilogue warp, CHAIN_EPI_BUFS staging tiles of 32 rows x 64 bytes: a
