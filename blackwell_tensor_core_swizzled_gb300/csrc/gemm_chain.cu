@@ -23,6 +23,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "common.h"
 #include "gemm_chain.cuh"
 #include "gemm_kernel.cuh"
@@ -353,10 +355,18 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) gemm_chain_kernel(const __gr
 }  // namespace
 
 cudaError_t launch_chain(const ChainParams& p, int grid, cudaStream_t s) {
-  // per device (the attribute belongs to the current device's context)
-  const cudaError_t e =
-      cudaFuncSetAttribute(gemm_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, CHAIN_SMEM_BYTES);
+  // The shared-memory attribute is set once per device (it belongs to the
+  // device's context), so that calls captured into a CUDA graph make no
+  // attribute call.
+  static std::atomic<bool> attr_set[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !attr_set[dev].load()) {
+    e = cudaFuncSetAttribute(gemm_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, CHAIN_SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev].store(true);
+  }
   gemm_chain_kernel<<<grid, CHAIN_THREADS, CHAIN_SMEM_BYTES, s>>>(p);
   return cudaGetLastError();
 }

@@ -162,3 +162,26 @@ def test_chain_bench_workload_sampled_rows(tcg, oracle_mod):
     rows = sorted({0, 1, 31, 32, 127, 128, 255, 19456, M - 129, M - 2, M - 1} |
                   set(np.random.default_rng(3).integers(0, M, 12).tolist()))
     _check(oracle_mod, "bf16", A, B1, B2, E, w.out, rows)
+
+
+def test_chain_graph_capture_and_replay(tcg):
+    # one chained launch captured into a CUDA graph and replayed: identical
+    # to the eager call every time
+    dt, M, N1, N2, K = "bf16", 700, 96, 600, 320
+    A, B1, B2 = (t.cuda() for t in _inputs(dt, M, N1, N2, K, seed=21))
+    eager = torch.empty((M, N2), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty((M, N2), dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        tcg.gemm_chain(1, M, N1, N2, K, A, K, B1, K, B2, N1, eager, 2, N2, stream=s.cuda_stream)
+        s.synchronize()
+        assert tcg.check(s.cuda_stream) == 0
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            tcg.gemm_chain(1, M, N1, N2, K, A, K, B1, K, B2, N1, out, 2, N2, stream=s.cuda_stream)
+    for _ in range(3):
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert tcg.check() == 0
+        assert torch.equal(out, eager)
