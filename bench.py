@@ -60,7 +60,7 @@ DATASHEET_DENSE_TFLOPS = {"bf16": 2250.0, "f16": 2250.0, "tf32": 1100.0, "e4m3":
                           "e3m2": 4500.0, "e2m3": 4500.0, "e2m1": 13500.0, "nvf4": 13500.0}
 PROFILE_DIR = os.path.join(ROOT, "profiles")
 KERNEL_SOURCES = ["gemm_kernel.cuh", "ptx.cuh", "desc.cuh", "gemm_f16.cu", "gemm_tf32.cu", "gemm_mxf8.cu", "api.cu",
-                  "splitk_reduce.cu"]
+                  "splitk_reduce.cu", "gemm_chain.cu", "gemm_chain.cuh", "tmem_ldst.cuh"]
 
 
 def kernel_source_hash() -> str:
@@ -429,7 +429,7 @@ def run_chain_workload(tcg, torch, w, steps, warmup):
             "bytes": float(ESIZE[w.dtype] * (M * K + N1 * K + N2 * N1) + OUT_BYTES[w.out] * M * N2)}
 
 
-def chain_roofline(w, r, peaks):
+def chain_roofline(w, r, peaks, traffic=None):
     """The chain's roofline is the larger of its tensor time (both products at
     the bf16 peak) and its HBM time (A, B1, B2 read and E written once)."""
     t_tensor = r["flops"] / (peaks["bf16_tflops"] * 1e12)
@@ -438,14 +438,14 @@ def chain_roofline(w, r, peaks):
     if t_hbm >= t_tensor:
         achieved = r["bytes"] / t / 1e9
         return {"bound": "hbm", "achieved": round(achieved, 1), "peak": round(peaks["hbm_gbs"], 1), "unit": "GB/s",
-                "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+                "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
                 "peak_source": f"{peaks['source']} HBM copy bandwidth (tensor time at the bf16 burst peak: "
                                f"{t_tensor * 1e6:.1f} us, HBM time {t_hbm * 1e6:.1f} us)",
                 "kernel": "tcg::gemm_chain_kernel", "algorithmic_bytes_per_launch": r["bytes"],
                 "algorithmic_flops_per_launch": r["flops"]}
     achieved = r["flops"] / t / 1e12
     return {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(peaks["bf16_tflops"], 1),
-            "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": None,
+            "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": traffic,
             "peak_source": f"{peaks['source']} bf16 burst (HBM time {t_hbm * 1e6:.1f} us, tensor time "
                            f"{t_tensor * 1e6:.1f} us)",
             "kernel": "tcg::gemm_chain_kernel", "algorithmic_bytes_per_launch": r["bytes"],
@@ -609,7 +609,7 @@ def main():
             ws = syn.WORKLOADS[name]
             if "chain_n1" in ws.extra:
                 rc2 = run_chain_workload(tcg, torch, ws, args.steps, args.warmup)
-                rl2 = chain_roofline(ws, rc2, peaks)
+                rl2 = chain_roofline(ws, rc2, peaks, profiled_traffic(name))
                 sec.append({"workload": name, "value": round(rc2["flops"] / (rc2["kernel_ms"] * 1e-3) / 1e12, 1),
                             "unit": UNIT, "ms_per_step": round(rc2["kernel_ms"], 4), "dtype": ws.dtype,
                             "gpu_launches": rc2["launches"], "roofline": rl2})
