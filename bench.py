@@ -58,6 +58,12 @@ NOMINAL_RATIO = {"bf16": 1.0, "f16": 1.0, "tf32": 1.1 / 2.25, "e4m3": 2.0, "e5m2
 # MMA kind each format runs on
 DATASHEET_DENSE_TFLOPS = {"bf16": 2250.0, "f16": 2250.0, "tf32": 1100.0, "e4m3": 4500.0, "e5m2": 4500.0,
                           "e3m2": 4500.0, "e2m3": 4500.0, "e2m1": 13500.0, "nvf4": 13500.0}
+# Tensor-pipe rate of each MMA kind relative to kind::f16, as measured on this
+# GPU (a pair of CTAs issuing M = 256, N = 256 MMAs back to back on zero
+# operands: 128 cycles per MMA for f16 K = 16, mxf8f6f4 K = 32 and both FP4
+# kinds K = 64).  The packed-FP4 kinds run at 4x, not the datasheet's 6x;
+# reported beside the nominal fraction, which stays the roofline's peak.
+MEASURED_PIPE_RATIO = {"e2m1": 4.0, "nvf4": 4.0}
 PROFILE_DIR = os.path.join(ROOT, "profiles")
 KERNEL_SOURCES = ["gemm_kernel.cuh", "ptx.cuh", "desc.cuh", "gemm_f16.cu", "gemm_tf32.cu", "gemm_mxf8.cu", "api.cu",
                   "splitk_reduce.cu", "gemm_chain.cu", "gemm_chain.cuh", "tmem_ldst.cuh"]
@@ -382,11 +388,17 @@ def roofline(w, kernel_ms, peaks, traffic, timed_s):
     src = (f"{peaks['source']} bf16 {regime} (timed region {timed_s * 1e3:.0f} ms)"
            + ("" if ratio == 1.0 else f" x nominal {w.dtype}/bf16 ratio {ratio:g}"))
     sheet = DATASHEET_DENSE_TFLOPS[w.dtype]
-    return {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak, 1), "unit": "TFLOP/s",
+    line = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak, 1), "unit": "TFLOP/s",
             "frac": round(achieved / peak, 4), "traffic": traffic, "peak_source": src,
             "frac_of_datasheet_dense": round(achieved / sheet, 4),
             "datasheet_dense_peak": sheet,
             "kernel": "tcg::gemm_kernel", "algorithmic_flops_per_launch": flops}
+    if w.dtype in MEASURED_PIPE_RATIO:
+        mp = peak / ratio * MEASURED_PIPE_RATIO[w.dtype]
+        line.update({"measured_pipe_peak": round(mp, 1), "frac_of_measured_pipe": round(achieved / mp, 4),
+                     "measured_pipe_source": f"bf16 {regime} peak x the measured per-clock ratio "
+                                             f"{MEASURED_PIPE_RATIO[w.dtype]:g} of this MMA kind"})
+    return line
 
 
 def run_chain_workload(tcg, torch, w, steps, warmup):
