@@ -467,7 +467,7 @@ def chain_roofline(w, r, peaks, traffic=None):
 # ----------------------------------------------------------------- CPU (oracle) arm
 
 # seconds of host work in the CPU baseline reported beside the GPU numbers
-CPU_BASELINE_S = 10.0
+CPU_BASELINE_S = 15.0
 
 def oracle_inputs(w):
     import oracle
