@@ -313,8 +313,8 @@ int pick_cta_group(const tcg_gemm_args& a) {
 // 128 x 384 outputs instead of 256 per 128 x 256, a sixth fewer bytes per
 // product, and 8 (MXFP4) or 16 (NVFP4) scale copies per 384 columns instead
 // of 6 or 12 per 256.  Measured at 8192^3: MXFP4 +3.5 %, NVFP4 +1 %; for
-// MXFP8 and FP6 the same tile lost 0.7 % (a block-scaled N = 128 MMA takes
-// nearly the tensor-pipe time of an N = 256 one), so those keep 256 x 256.
+// MXFP8 and FP6 the same tile lost 0.7 % (and 1 % as two N = 192 MMAs), so
+// those keep 256 x 256.
 // The rule depends on the format and shape alone, so that scale images
 // prepared for tcg_tile_n always match.
 bool wide_tiles(const tcg_gemm_args& a, int cg) {
