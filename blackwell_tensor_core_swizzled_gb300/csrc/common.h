@@ -57,7 +57,11 @@ cudaError_t launch_splitk_reduce(const GemmParams& p, int cg, int num_clusters, 
 
 // Chained GEMM kernel launch (gemm_chain.cu).
 struct ChainParams;
-cudaError_t launch_chain(const ChainParams& p, int grid, cudaStream_t stream);
+// The chained kernel for clusters of `cluster` CTAs (1 or 2) sharing B
+// tiles by multicast (gemm_chain.cu); KernelInfo::cta_group carries the
+// cluster size.
+KernelInfo kinfo_chain(int cluster);
+cudaError_t launch_chain(const ChainParams& p, int cluster, int grid, cudaStream_t stream);
 
 // Host state helpers (api.cu).
 int record_cuda(cudaError_t e);              // stores the message, returns TCG_ERR_CUDA (or TCG_OK)

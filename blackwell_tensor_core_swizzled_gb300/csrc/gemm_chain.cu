@@ -10,7 +10,8 @@
 //            has ("tcgen05.mma" page, "Operands and repeat axes": A from
 //            "Shared or TMEM"; the layout pinned by the TMEM-A probe);
 //   phase 2  for each 192-column tile of E: N1/16 tcgen05.mma with A read
-//            from TMEM column 8*step and B2 from shared memory, into one of
+//            from TMEM column 8*step and B2 from shared memory (stages of
+//            128 of N1, two tiles' worth in flight for N1 = 256), into one of
 //            two accumulators (columns 128 and 320), drained by the epilogue
 //            while the other fills.
 //
@@ -18,12 +19,19 @@
 // phases), warp 1 MMA issuer, warp 2 TMEM allocation, warp 3 barrier set-up,
 // warps 4..11 epilogue (two per TMEM lane quadrant).  Work units are (128-row
 // tile, group of E tiles); with fewer row tiles than SMs the E tiles are
-// split into groups and each group's unit recomputes its C.  Every wait is
-// bounded; a timeout records an error word and the CTA drains and exits.
+// split into groups and each group's unit recomputes its C.
+//
+// Clusters of CS CTAs (CS = 1 or 2) take CS neighbouring row tiles of the
+// same group, so they walk the same B1 / B2 tiles in the same order: each CTA
+// loads 1/CS of every B tile and multicasts it into the same stage of all CS
+// CTAs, which cuts the B bytes an SM pulls from L2 by CS.  The MMAs stay
+// cta_group::1 (every CTA issues its own from its own shared memory and
+// TMEM); a stage is refilled once all CS CTAs' MMAs have read it (each MMA
+// warp's commit arrives on the empty barrier of every CTA in the cluster).
+// Every wait is bounded; a timeout records an error word and the CTA drains
+// and exits.
 #include <cuda.h>
 #include <cuda_runtime.h>
-
-#include <atomic>
 
 #include "common.h"
 #include "gemm_chain.cuh"
@@ -34,8 +42,11 @@ namespace tcg {
 
 namespace {
 
-constexpr uint32_t CHAIN_A_BYTES = 128 * 128;  // one 128-row x 64-element stage of A
+constexpr uint32_t CHAIN_A_BYTES = 128 * 128;            // one 128-row x 64-element stage of A
+constexpr uint32_t CHAIN_B2_BOX_BYTES = CHAIN_BN2 * 128;  // one CHAIN_BN2-row x 64-element box of B2
+static_assert(2 * CHAIN_B2_BOX_BYTES <= CHAIN_STAGE_BYTES, "two B2 boxes per stage");
 
+template <int CS>
 __global__ void __launch_bounds__(CHAIN_THREADS, 1) gemm_chain_kernel(const __grid_constant__ ChainParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -56,6 +67,10 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) gemm_chain_kernel(const __gr
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const WaitCtx wctx{p.timeout_ns, p.err, abort_flag};
+  const uint32_t rank = CS > 1 ? cluster_ctarank() : 0u;
+  const int cluster_id = blockIdx.x / CS;
+  const int num_clusters = gridDim.x / CS;
+  constexpr uint16_t CLUSTER_MASK = static_cast<uint16_t>((1u << CS) - 1u);
 
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&p.tmap_a);
@@ -66,7 +81,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) gemm_chain_kernel(const __gr
   if (threadIdx.x == 96) {
     for (int s = 0; s < CHAIN_STAGES; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
+      mbar_init(empty_bar(s), CS);  // one commit from each CTA's MMA warp
     }
     mbar_init(c_full, 1);
     mbar_init(a2_ready, CHAIN_EPI_WARPS);
@@ -85,13 +100,17 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) gemm_chain_kernel(const __gr
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (CS > 1) cluster_sync();  // peers' barriers are initialised before any multicast
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  // unit u: row tile u % m_tiles, E tiles [t0, t1) of group u / m_tiles
+  // cluster unit u: this CTA's row tile CS * (u % m_blocks) + rank (past
+  // the last tile for some CTAs of the last block: those load zero-filled A,
+  // keep the cluster's B multicasts going and store nothing), E tiles
+  // [t0, t1) of group u / m_blocks
   auto unit_tiles = [&](int u, int& mt, int& t0, int& t1) {
-    mt = u % p.m_tiles;
-    t0 = (u / p.m_tiles) * p.tiles_per_group;
+    mt = CS * (u % p.m_blocks) + static_cast<int>(rank);
+    t0 = (u / p.m_blocks) * p.tiles_per_group;
     t1 = min(p.n2_tiles, t0 + p.tiles_per_group);
   };
 
@@ -99,26 +118,45 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) gemm_chain_kernel(const __gr
     // ------------------------------------------------------------ producer
     uint32_t it = 0, s = 0, ph = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+    for (int u = cluster_id; u < p.num_units && ok; u += num_clusters) {
       int mt, t0, t1;
       unit_tiles(u, mt, t0, t1);
       const int stages = p.k1_blocks + (t1 - t0) * p.k2_blocks;
+      const int m0 = 128 * mt;
       for (int i = 0; i < stages; ++i) {
         if (!wait_uniform(empty_bar(s), ph ^ 1u, wctx, SITE_PROD_EMPTY)) {
           ok = false;
           break;
         }
         if (elect_one()) {
+          // this stage's full barrier counts the whole tile: this CTA's A,
+          // plus every CTA's slice of B (this one's own included)
           const uint32_t sa = sbase + s * CHAIN_STAGE_BYTES;
+          auto load_b = [&](uint32_t dst, const CUtensorMap* map, int x, int y) {
+            if constexpr (CS > 1)
+              tma_load_2d_multicast(dst, map, x, y, full_bar(s), CLUSTER_MASK);
+            else
+              tma_load_2d(dst, map, x, y, full_bar(s));
+          };
           if (i < p.k1_blocks) {
+            const int rows = p.N1 / CS;
             mbar_arrive_expect_tx(full_bar(s), CHAIN_A_BYTES + static_cast<uint32_t>(p.N1) * 128u);
-            tma_load<1>(sa, &p.tmap_a, 64 * i, 128 * mt, full_bar(s));
-            tma_load<1>(sa + CHAIN_A_BYTES, &p.tmap_b1, 64 * i, 0, full_bar(s));
+            tma_load_2d(sa, &p.tmap_a, 64 * i, m0, full_bar(s));
+            load_b(sa + CHAIN_A_BYTES + static_cast<uint32_t>(rank * rows) * 128u, &p.tmap_b1, 64 * i,
+                   static_cast<int>(rank) * rows);
           } else {
+            // a second-product stage holds up to two 64-column boxes of the
+            // E tile's B2 rows (128 of N1), so that the ring keeps two
+            // tiles' B2 in flight
             const int j = i - p.k1_blocks;
             const int t = t0 + j / p.k2_blocks;
-            mbar_arrive_expect_tx(full_bar(s), CHAIN_BN2 * 128u);
-            tma_load<1>(sa, &p.tmap_b2, 64 * (j % p.k2_blocks), CHAIN_BN2 * t, full_bar(s));
+            const int x0 = 128 * (j % p.k2_blocks);
+            const uint32_t boxes = x0 + 64 < p.N1 ? 2u : 1u;
+            constexpr int rows = CHAIN_BN2 / CS;
+            mbar_arrive_expect_tx(full_bar(s), boxes * CHAIN_BN2 * 128u);
+            for (uint32_t bx = 0; bx < boxes; ++bx)
+              load_b(sa + bx * CHAIN_B2_BOX_BYTES + rank * rows * 128u, &p.tmap_b2, x0 + 64 * static_cast<int>(bx),
+                     CHAIN_BN2 * t + static_cast<int>(rank) * rows);
           }
         }
         __syncwarp();
@@ -134,7 +172,8 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) gemm_chain_kernel(const __gr
       const uint32_t n_out = it < static_cast<uint32_t>(CHAIN_STAGES) ? it : static_cast<uint32_t>(CHAIN_STAGES);
       for (uint32_t j = it - n_out; j < it; ++j) {
         const uint64_t t0 = globaltimer();
-        while (!mbar_try_wait(full_bar(j % CHAIN_STAGES), (j / CHAIN_STAGES) & 1u) && globaltimer() - t0 < 20000000ull) {
+        while (!mbar_try_wait(full_bar(j % CHAIN_STAGES), (j / CHAIN_STAGES) & 1u) &&
+               globaltimer() - t0 < 20000000ull) {
         }
       }
     }
@@ -142,9 +181,17 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) gemm_chain_kernel(const __gr
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     const uint64_t hi = sdesc_hi(16, 1024, SW_128B);
+    // stage s has been read by this CTA's MMAs: tell every CTA whose
+    // multicast refills it
+    auto release = [&](uint32_t s) {
+      if constexpr (CS > 1)
+        tc_commit_multicast(empty_bar(s), CLUSTER_MASK);
+      else
+        tc_commit<1>(empty_bar(s));
+    };
     uint32_t s = 0, ph = 0, dt = 0, uc = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uc) {
+    for (int u = cluster_id; u < p.num_units && ok; u += num_clusters, ++uc) {
       int mt, t0, t1;
       unit_tiles(u, mt, t0, t1);
       // C (fp32) overlaps the first accumulator and its 16-bit copy is read
@@ -169,7 +216,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) gemm_chain_kernel(const __gr
 #pragma unroll
           for (int j = 0; j < 4; ++j)  // 16 K elements = 32 bytes = 2 descriptor units per step
             mma_f16<1>(tmem_base, ad + 2 * j, bd + 2 * j, p.idesc1, (kb | j) ? 1u : 0u);
-          tc_commit<1>(empty_bar(s));
+          release(s);
         }
         __syncwarp();
         if (++s == CHAIN_STAGES) {
@@ -201,15 +248,16 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) gemm_chain_kernel(const __gr
           }
           tc_fence_after();
           if (elect_one()) {
-            const uint64_t bd = sdesc(sbase + s * CHAIN_STAGE_BYTES, hi);
+            const uint32_t sa = sbase + s * CHAIN_STAGE_BYTES;
+            const uint64_t bd0 = sdesc(sa, hi), bd1 = sdesc(sa + CHAIN_B2_BOX_BYTES, hi);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const int step = 4 * kb + j;
+            for (int j = 0; j < 8; ++j) {  // 16 of N1 per MMA, four per 64-column box
+              const int step = 8 * kb + j;
               if (step < p.k2_steps)
-                mma_f16_tmem_a(d_tmem, tmem_base + 8u * static_cast<uint32_t>(step), bd + 2 * j, p.idesc2,
-                               step ? 1u : 0u);
+                mma_f16_tmem_a(d_tmem, tmem_base + 8u * static_cast<uint32_t>(step), (j < 4 ? bd0 : bd1) + 2 * (j & 3),
+                               p.idesc2, step ? 1u : 0u);
             }
-            tc_commit<1>(empty_bar(s));
+            release(s);
           }
           __syncwarp();
           if (++s == CHAIN_STAGES) {
@@ -257,7 +305,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) gemm_chain_kernel(const __gr
       }
       ++stores;
     };
-    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uc) {
+    for (int u = cluster_id; u < p.num_units && ok; u += num_clusters, ++uc) {
       int mt, t0, t1;
       unit_tiles(u, mt, t0, t1);
       const int row0 = 128 * mt + 32 * q;
@@ -348,27 +396,39 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) gemm_chain_kernel(const __gr
   tc_fence_before();
   cta_barrier_unaligned();
   __syncwarp();
+  if constexpr (CS > 1) cluster_sync();  // no peer multicasts into this CTA or arrives on its barriers any more
   tc_fence_after();
   if (warp == 2) tmem_dealloc<1>(tmem_base, 512);
 }
 
 }  // namespace
 
-cudaError_t launch_chain(const ChainParams& p, int grid, cudaStream_t s) {
-  // The shared-memory attribute is set once per device (it belongs to the
-  // device's context), so that calls captured into a CUDA graph make no
-  // attribute call.
-  static std::atomic<bool> attr_set[64];
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64 || !attr_set[dev].load()) {
-    e = cudaFuncSetAttribute(gemm_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, CHAIN_SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_set[dev].store(true);
-  }
-  gemm_chain_kernel<<<grid, CHAIN_THREADS, CHAIN_SMEM_BYTES, s>>>(p);
-  return cudaGetLastError();
+KernelInfo kinfo_chain(int cluster) {
+  const void* fn = cluster == 2 ? reinterpret_cast<const void*>(&gemm_chain_kernel<2>)
+                                : reinterpret_cast<const void*>(&gemm_chain_kernel<1>);
+  return KernelInfo{fn, CHAIN_SMEM_BYTES, cluster == 2 ? 2 : 1, CHAIN_BN2, KIND_F16, CHAIN_THREADS};
+}
+
+// The shared-memory attribute was set when the cluster capacity was queried
+// (max_clusters_for on the host side, once per device and variant), so that
+// calls captured into a CUDA graph make no attribute call.
+cudaError_t launch_chain(const ChainParams& p, int cluster, int grid, cudaStream_t s) {
+  const KernelInfo ki = kinfo_chain(cluster);
+  if (ki.cta_group != cluster) return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(CHAIN_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = CHAIN_SMEM_BYTES;
+  cfg.stream = s;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = cluster;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = cluster > 1 ? 1 : 0;
+  void* args[] = {const_cast<ChainParams*>(&p)};
+  return cudaLaunchKernelExC(&cfg, ki.func, args);
 }
 
 }  // namespace tcg

@@ -17,11 +17,12 @@ struct ChainParams {
   CUtensorMap tmap_e;   // E [M][N2], 32-row x 64-byte boxes, 64-byte swizzle
   int M, N1, N2, K;
   int m_tiles;          // 128-row tiles of A / E
+  int m_blocks;         // cluster-sized blocks of row tiles: cdiv(m_tiles, cluster size)
   int n2_tiles;         // CHAIN_BN2-column tiles of E
   int tiles_per_group;  // E tiles one unit computes
-  int num_units;        // m_tiles x groups; unit u -> (u % m_tiles, group u / m_tiles)
+  int num_units;        // m_blocks x groups; cluster unit u -> (block u % m_blocks, group u / m_blocks)
   int k1_blocks;        // ring stages of the first product (64 K each)
-  int k2_blocks;        // ring stages of the second product (64 of N1 each)
+  int k2_blocks;        // ring stages per E tile of the second product (128 of N1 each)
   int k2_steps;         // second-product MMAs: N1 / 16
   uint32_t idesc1, idesc2;
   int in_bf16;          // operand type (and the intermediate's): bf16, else f16
@@ -38,7 +39,7 @@ struct ChainParams {
 constexpr int CHAIN_BN2 = 192;
 constexpr int CHAIN_D_COL0 = 128;
 constexpr int CHAIN_STAGES = 4;
-constexpr int CHAIN_STAGE_BYTES = 48 * 1024;  // A (16 KiB) + B1 (up to 256 rows, 32 KiB); B2 uses 24 KiB
+constexpr int CHAIN_STAGE_BYTES = 48 * 1024;  // A (16 KiB) + B1 (up to 256 rows, 32 KiB), or two B2 boxes
 constexpr int CHAIN_EPI_WARPS = 8;
 constexpr int CHAIN_THREADS = 32 * (4 + CHAIN_EPI_WARPS);
 // per epilogue warp, CHAIN_EPI_BUFS staging tiles of 32 rows x 64 bytes: a

@@ -140,6 +140,18 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* map, 
       : "memory");
 }
 
+// Tile load global -> shared of every CTA in `mask` (cluster ranks): the
+// tile lands at the same CTA-relative address `dst` in each, and each
+// destination's mbarrier at offset `bar` receives its bytes.
+__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const void* map, int32_t x, int32_t y,
+                                                      uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "h"(mask)
+      : "memory");
+}
+
 template <int CG>
 __device__ __forceinline__ void tma_load(uint32_t dst, const void* map, int32_t x, int32_t y, uint32_t bar) {
   if constexpr (CG == 2)
@@ -350,6 +362,14 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
   else
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                  : "memory");
+}
+
+// Completion of this CTA's earlier tcgen05 operations, signalled as one
+// arrival on the mbarrier at offset `bar` in every CTA of `mask`.
+__device__ __forceinline__ void tc_commit_multicast(uint32_t bar, uint16_t mask) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+               "h"(mask)
+               : "memory");
 }
 
 template <int CG>

@@ -266,10 +266,12 @@ int tcg_gemm(const tcg_gemm_args* args, void* stream);
  * C of in_type in between, without C ever reaching global memory: each CTA
  * computes 128 rows of C into TMEM, rewrites them there as 16-bit pairs
  * (row m in lane m, element k in column k/2) and issues the second product's
- * MMAs with A read from TMEM, for 128-column tiles of E.  When there are
+ * MMAs with A read from TMEM, for 192-column tiles of E.  When there are
  * fewer 128-row tiles than SMs the E tiles are split into groups and each
- * group recomputes its rows of C.  M == 0 or N2 == 0: no-op; K == 0: E is
- * zeroed.  One kernel launch; asynchronous on `stream`. */
+ * group recomputes its rows of C.  With at least 16 row tiles and N1 >= 128
+ * the CTAs of neighbouring row tiles run as clusters of two that load half of
+ * every B1 / B2 tile each and share it by TMA multicast.  M == 0 or N2 == 0:
+ * no-op; K == 0: E is zeroed.  One kernel launch; asynchronous on `stream`. */
 int tcg_gemm_chain(tcg_input in_type, int64_t M, int64_t N1, int64_t N2, int64_t K,
                    const void* A, int64_t lda, const void* B1, int64_t ldb1,
                    const void* B2, int64_t ldb2, void* E, tcg_dtype e_type, int64_t lde,

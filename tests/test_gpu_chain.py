@@ -72,6 +72,8 @@ EXACT = [
     ("f16", 257, 256, 200, 48),
     ("bf16", 1000, 128, 1032, 72),
     ("f16", 64, 80, 384, 200),
+    ("bf16", 520, 16, 200, 64),    # N1 = 16: single CTAs even with several row tiles
+    ("bf16", 2100, 128, 200, 64),  # B shared by CTA pairs; odd row-tile count: the last pair's second CTA idles
 ]
 
 
@@ -90,6 +92,7 @@ RANDOM = [
     ("f16", 1000, 112, 2000, 1000, "f16"),
     ("bf16", 256, 256, 4000, 4096, "bf16"),     # 2 row tiles: E tiles split over many units
     ("bf16", 152 * 128 * 2 + 77, 128, 384, 512, "bf16"),  # more row tiles than SMs, ragged
+    ("f16", 4000, 192, 700, 320, "f32"),     # CTA pairs, a B2 stage of one 64-column box after a full one
 ]
 
 
