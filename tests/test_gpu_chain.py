@@ -167,10 +167,11 @@ def test_chain_bench_workload_sampled_rows(tcg, oracle_mod):
     _check(oracle_mod, "bf16", A, B1, B2, E, w.out, rows)
 
 
-def test_chain_graph_capture_and_replay(tcg):
+@pytest.mark.parametrize("M,N1", [(700, 96), (2100, 128)])   # single CTAs; clusters of two sharing B
+def test_chain_graph_capture_and_replay(tcg, M, N1):
     # one chained launch captured into a CUDA graph and replayed: identical
     # to the eager call every time
-    dt, M, N1, N2, K = "bf16", 700, 96, 600, 320
+    dt, N2, K = "bf16", 600, 320
     A, B1, B2 = (t.cuda() for t in _inputs(dt, M, N1, N2, K, seed=21))
     eager = torch.empty((M, N2), dtype=torch.bfloat16, device="cuda")
     out = torch.empty((M, N2), dtype=torch.bfloat16, device="cuda")
@@ -188,3 +189,16 @@ def test_chain_graph_capture_and_replay(tcg):
         torch.cuda.synchronize()
         assert tcg.check() == 0
         assert torch.equal(out, eager)
+
+
+def test_chain_cluster_rule(tcg):
+    # clusters of two sharing B from 16 row tiles and N1 = 128 up; the parity
+    # cases above cover both kinds of launch only if this rule holds
+    A, B1, B2 = (t.cuda() for t in _inputs("bf16", 2100, 128, 200, 64, seed=5))
+    E = torch.empty((2100, 200), dtype=torch.bfloat16, device="cuda")
+    for n1, shared in ((128, True), (64, False)):
+        tcg.gemm_chain(1, 2100, n1, 200, 64, A, 64, B1, 64, B2, 128, E, 2, 200)
+        assert ("of 2 sharing B by multicast" in tcg.last_plan_string()) == shared, tcg.last_plan_string()
+    tcg.gemm_chain(1, 1900, 128, 200, 64, A, 64, B1, 64, B2, 128, E, 2, 200)   # 15 row tiles
+    assert "sharing B" not in tcg.last_plan_string()
+    assert tcg.check() == 0
