@@ -560,8 +560,9 @@ int run_gemm(const tcg_gemm_args* args, cudaStream_t s) {
   tcg_gemm_args a = *args;
   if (a.M < 0 || a.N < 0 || a.K < 0) return TCG_ERR_INVALID;
   if (a.in_type < TCG_IN_F16 || a.in_type > TCG_IN_NVF4) return TCG_ERR_INVALID;
-  // the packed-FP4 kinds stage their scales from the MMA thread only
-  if (is_fp4(a.in_type) && a.sf_staging != 0 && a.sf_staging != 2) return TCG_ERR_UNSUPPORTED;
+  // the packed-FP4 kinds stage their scales with tcgen05.cp, from the MMA
+  // thread or a copy thread (no tcgen05.st scale warps)
+  if (is_fp4(a.in_type) && a.sf_staging == 1) return TCG_ERR_UNSUPPORTED;
   if (a.d_type < TCG_F32 || a.d_type > TCG_BF16 || a.acc_type < TCG_F32 || a.acc_type > TCG_BF16)
     return TCG_ERR_INVALID;
   if (a.acc_type == TCG_BF16) return TCG_ERR_UNSUPPORTED;

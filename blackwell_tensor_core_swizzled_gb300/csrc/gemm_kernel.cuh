@@ -819,17 +819,23 @@ __global__ void __launch_bounds__(KIND >= KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
           mma_role(std::integral_constant<int, SF_BY_CP>{});
         else
           mma_role(std::integral_constant<int, SF_BY_WARPS>{});
+      } else if constexpr (C::SCALED) {
+        // packed FP4: the MMA warp or a copy warp stages the scales
+        if (p.sf_mode == SF_BY_CP)
+          mma_role(std::integral_constant<int, SF_BY_CP>{});
+        else
+          mma_role(std::integral_constant<int, SF_BY_MMA>{});
       } else {
         mma_role(std::integral_constant<int, SF_BY_MMA>{});
       }
     }
-  } else if (KIND == KIND_MXF8 && warp == 3) {
+  } else if (C::SCALED && warp == 3) {
     // ------------------------------------------------------------ cp thread
     // SF_BY_CP: the pair leader's warp 3 copies each stage's scales into its
     // TMEM slot with tcgen05.cp .32x128b.warpx4 (both CTAs of a pair) and
     // commits to sf_ready[slot]; the MMA warp's tensor-pipe stream then holds
     // only MMAs.  Uniform loop, one elected lane issues (as for the MMAs).
-    if constexpr (KIND == KIND_MXF8) {
+    if constexpr (C::SCALED) {
       if (p.sf_mode == SF_BY_CP && (CG == 1 || rank == 0)) {
         const uint32_t total_it = cluster_iterations(cluster_id, num_clusters, p);
         const uint64_t cp_hi = sdesc_hi(16, 128, SW_NONE);  // 32 rows x 16 B, rows 16 B apart
@@ -844,10 +850,18 @@ __global__ void __launch_bounds__(KIND >= KIND_MXF8 ? 384 : 256, 1) gemm_kernel(
           const uint32_t ssfa = sbase + s * C::STAGE_BYTES + C::A_BYTES + C::B_BYTES;
           const uint32_t col = tmem_base + C::SF_COL0 + (it % C::SF_SLOTS) * C::SF_SLOT_COLS;
           if (elect_one()) {
-            tc_cp_32x128b_warpx4<CG>(col, sdesc(ssfa, cp_hi));
+            // the slot layout the MMA path's copies produce: chunk group g of
+            // SFA to columns 4g, 128-row chunk c of group g of SFB to
+            // 4*SF_KCH + 4*(g*SFB_CHUNKS + c)
 #pragma unroll
-            for (int c = 0; c < C::SFB_CHUNKS; ++c)
-              tc_cp_32x128b_warpx4<CG>(col + 4 + 4 * c, sdesc(ssfa + C::SFA_BYTES + 512 * c, cp_hi));
+            for (int g = 0; g < C::SF_KCH; ++g)
+              tc_cp_32x128b_warpx4<CG>(col + 4 * g, sdesc(ssfa + 512 * g, cp_hi));
+#pragma unroll
+            for (int g = 0; g < C::SF_KCH; ++g)
+#pragma unroll
+              for (int c = 0; c < C::SFB_CHUNKS; ++c)
+                tc_cp_32x128b_warpx4<CG>(col + 4 * C::SF_KCH + 4 * (g * C::SFB_CHUNKS + c),
+                                         sdesc(ssfa + C::SFA_BYTES + 512 * (g * C::SFB_CHUNKS + c), cp_hi));
             tc_commit<CG>(sfr_bar(it % C::SF_SLOTS));
           }
           __syncwarp();

@@ -219,7 +219,9 @@ typedef struct {
   int raster_group;  /* 0 auto; tiles are visited in groups of this many M tiles */
   int sf_staging;    /* block scaling, who stages the scales into TMEM:
                         0 = auto (2),
-                        1 = four scale warps per CTA with tcgen05.st,
+                        1 = four scale warps per CTA with tcgen05.st
+                            (8- and 6-bit formats; packed FP4:
+                            TCG_ERR_UNSUPPORTED),
                         2 = the MMA thread with tcgen05.cp .32x128b.warpx4
                             ("tcgen05.cp" page) before its MMAs,
                         3 = a dedicated thread with tcgen05.cp + commit */

@@ -106,6 +106,16 @@ def test_block_scaled_formats_full_compare(tcg, oracle_mod, dtype, am, bm, M, N,
     _check_full(tcg, oracle_mod, x, out, "f32", cg)
 
 
+@pytest.mark.parametrize("dtype,am,bm,M,N,K,cg,out", [c for c in MX_FORMATS if c[0] in ("e2m1", "nvf4")])
+def test_packed_fp4_copy_thread_staging(tcg, oracle_mod, dtype, am, bm, M, N, K, cg, out):
+    # the packed-FP4 kinds' scales staged by a dedicated copy thread
+    # (tcgen05.cp + commit to the slot's barrier) instead of the MMA thread
+    x = make_case(dtype, am, bm, M, N, K, dist="codes", seed=M + K + 1)
+    _check_full(tcg, oracle_mod, x, out, "f32", cg, sf_staging=3)
+    with pytest.raises(tcg.TcgError):   # no tcgen05.st scale warps for these kinds
+        run_gpu(tcg, x, out=out, cta_group=cg, sf_staging=1)
+
+
 @pytest.mark.parametrize("dtype,one", [("e2m1", 0x2), ("e2m3", 0x08), ("e3m2", 0x0C), ("nvf4", 0x2)])
 def test_packed_identity_reads_every_code_in_place(tcg, oracle_mod, dtype, one):
     """A = I (the code of 1.0 on the diagonal, scales 2^0) and B random codes:
@@ -465,12 +475,13 @@ WIDE = [
 ]
 
 
+@pytest.mark.parametrize("staging", [0, 3])
 @pytest.mark.parametrize("dtype,K,out,split", WIDE)
-def test_wide_pair_tiles_sampled_rows(tcg, oracle_mod, dtype, K, out, split):
+def test_wide_pair_tiles_sampled_rows(tcg, oracle_mod, dtype, K, out, split, staging):
     M, N = 2600, 27 * 384 + 300
     x = make_case(dtype, "k", "k", M, N, K, dist="codes", seed=K + len(dtype))
     assert tcg.tile_n(IN_TYPE[dtype], M, N, K, 0, 0) == 384
-    D = run_gpu(tcg, x, out=out, cta_group=0, split_k=split)
+    D = run_gpu(tcg, x, out=out, cta_group=0, split_k=split, sf_staging=staging)
     plan = tcg.last_plan_string()
     assert "cta_group 2, tile 256x384" in plan, plan
     rows = sample_rows(M, n=16, seed=K)
