@@ -264,13 +264,8 @@ def run_workload(tcg, torch, w, steps, warmup, dist_ctx, measure_e2e=True):
         raise RuntimeError(f"timed run failed: {tcg.status_string(rc)} {tcg.last_error_string()}")
     total_ms = start.elapsed_time(end)
     kernel_ms = float(np.mean([a.elapsed_time(b) for a, b in kev]))
-    tr = trace_buf.cpu().numpy()
-    ok = (tr[:, 6] > tr[:, 0]) & (tr[:, 9] > tr[:, 8])
-    ghz = (tr[ok, 9] - tr[ok, 8]) / (tr[ok, 6] - tr[ok, 0]) if ok.any() else np.array([])
     res = {"total_ms": total_ms, "kernel_ms": kernel_ms, "launches": launches[0], "t0": t_host0, "t1": t_host1,
-           "kernel_sm_mhz": round(float(np.median(ghz)) * 1000, 1) if ghz.size else None,
-           "kernel_sm_mhz_range": [round(float(ghz.min()) * 1000, 1), round(float(ghz.max()) * 1000, 1)]
-           if ghz.size else None}
+           **kernel_clock(trace_buf)}
 
     if measure_e2e:
         # End to end through the C ABI: every step copies its inputs in from
@@ -401,6 +396,19 @@ def roofline(w, kernel_ms, peaks, traffic, timed_s):
     return line
 
 
+def kernel_clock(trace_buf):
+    """The SM clock a traced launch ran at (tcg_trace_next slots 0/6 =
+    globaltimer at entry / exit, 8/9 = clock64 next to them): median and
+    range over its CTAs, in MHz."""
+    tr = trace_buf.cpu().numpy()
+    ok = (tr[:, 6] > tr[:, 0]) & (tr[:, 9] > tr[:, 8])
+    ghz = (tr[ok, 9] - tr[ok, 8]) / (tr[ok, 6] - tr[ok, 0]) if ok.any() else np.array([])
+    if not ghz.size:
+        return {"kernel_sm_mhz": None, "kernel_sm_mhz_range": None}
+    return {"kernel_sm_mhz": round(float(np.median(ghz)) * 1000, 1),
+            "kernel_sm_mhz_range": [round(float(ghz.min()) * 1000, 1), round(float(ghz.max()) * 1000, 1)]}
+
+
 def run_chain_workload(tcg, torch, w, steps, warmup):
     """Device-timed chained GEMM E = round(A.B1).B2 (tcg_gemm_chain): one
     launch per step, CUDA events around each.  Inputs (A and E larger than the
@@ -422,11 +430,15 @@ def run_chain_workload(tcg, torch, w, steps, warmup):
     if rc != 0:
         raise RuntimeError(f"chain warm-up failed: {tcg.status_string(rc)} {tcg.last_error_string()}")
     kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    trace_buf = torch.zeros((sms, 10), dtype=torch.int64, device="cuda")
     torch.cuda.synchronize()
     launches = 0
     t0 = time.time()
     for i in range(steps):
         kev[i][0].record(stream)
+        if i == steps - 1:  # the last timed launch records the SM clock it ran at
+            tcg.trace_next(trace_buf, sms)
         call()
         launches += tcg.last_launch_count()
         kev[i][1].record(stream)
@@ -436,7 +448,7 @@ def run_chain_workload(tcg, torch, w, steps, warmup):
     if rc != 0:
         raise RuntimeError(f"chain run failed: {tcg.status_string(rc)}")
     kernel_ms = float(np.mean([a.elapsed_time(b) for a, b in kev]))
-    return {"kernel_ms": kernel_ms, "launches": launches, "t0": t0, "t1": t1,
+    return {"kernel_ms": kernel_ms, "launches": launches, "t0": t0, "t1": t1, **kernel_clock(trace_buf),
             "flops": 2.0 * M * K * N1 + 2.0 * M * N1 * N2,
             "bytes": float(ESIZE[w.dtype] * (M * K + N1 * K + N2 * N1) + OUT_BYTES[w.out] * M * N2)}
 
@@ -627,7 +639,7 @@ def main():
                 rl2 = chain_roofline(ws, rc2, peaks, profiled_traffic(name))
                 sec.append({"workload": name, "value": round(rc2["flops"] / (rc2["kernel_ms"] * 1e-3) / 1e12, 1),
                             "unit": UNIT, "ms_per_step": round(rc2["kernel_ms"], 4), "dtype": ws.dtype,
-                            "gpu_launches": rc2["launches"], "roofline": rl2})
+                            "gpu_launches": rc2["launches"], "kernel_sm_mhz": rc2["kernel_sm_mhz"], "roofline": rl2})
                 continue
             r2 = run_workload(tcg, torch, ws, args.steps, args.warmup, dctx, measure_e2e=False)
             # steps of an hbm workload include an L2 flush: count the GEMM time only

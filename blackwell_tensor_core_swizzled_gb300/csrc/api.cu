@@ -985,6 +985,10 @@ int run_chain(tcg_input in, int64_t M, int64_t N1, int64_t N2, int64_t K, const 
   p.e_type = e_type == TCG_F32 ? OUT_F32 : e_type == TCG_F16 ? OUT_F16 : OUT_BF16;
   p.err = d->err;
   p.timeout_ns = g_timeout_ns.load();
+  p.trace = t_trace_buf;
+  p.trace_ctas = t_trace_ctas;
+  t_trace_buf = nullptr;
+  t_trace_ctas = 0;
   const int grid = cs * static_cast<int>(std::min<int64_t>(p.num_units, clusters));
   const cudaError_t e = launch_chain(p, cs, grid, s);
   if (e != cudaSuccess) return record_cuda(e);

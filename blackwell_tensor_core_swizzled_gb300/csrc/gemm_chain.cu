@@ -48,6 +48,16 @@ static_assert(2 * CHAIN_B2_BOX_BYTES <= CHAIN_STAGE_BYTES, "two B2 boxes per sta
 
 template <int CS>
 __global__ void __launch_bounds__(CHAIN_THREADS, 1) gemm_chain_kernel(const __grid_constant__ ChainParams p) {
+  // trace: globaltimer and the SM cycle counter read back to back
+  auto trace_clock = [&](int slot, int clk_slot) {
+    if (p.trace && static_cast<int>(blockIdx.x) < p.trace_ctas) {
+      const uint64_t t = globaltimer();
+      const uint64_t c = clock64();
+      p.trace[static_cast<int64_t>(blockIdx.x) * TRACE_SLOTS + slot] = t;
+      p.trace[static_cast<int64_t>(blockIdx.x) * TRACE_SLOTS + clk_slot] = c;
+    }
+  };
+  if (threadIdx.x == 0) trace_clock(TRACE_ENTRY, TRACE_CLK_ENTRY);
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -270,6 +280,8 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) gemm_chain_kernel(const __gr
         __syncwarp();
       }
     }
+    if (lane == 0 && p.trace && static_cast<int>(blockIdx.x) < p.trace_ctas)
+      p.trace[static_cast<int64_t>(blockIdx.x) * TRACE_SLOTS + TRACE_UNITS] = uc;
     if (!ok && elect_one()) {
       tc_commit<1>(drain_bar);
       const uint64_t t0 = globaltimer();
@@ -398,7 +410,10 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) gemm_chain_kernel(const __gr
   __syncwarp();
   if constexpr (CS > 1) cluster_sync();  // no peer multicasts into this CTA or arrives on its barriers any more
   tc_fence_after();
-  if (warp == 2) tmem_dealloc<1>(tmem_base, 512);
+  if (warp == 2) {
+    tmem_dealloc<1>(tmem_base, 512);
+    if (lane == 0) trace_clock(TRACE_EXIT, TRACE_CLK_EXIT);
+  }
 }
 
 }  // namespace

@@ -29,6 +29,11 @@ struct ChainParams {
   int e_type;           // OutType of E
   unsigned long long* err;
   uint64_t timeout_ns;
+  // optional trace (null: off), the GEMM kernel's slot layout: per CTA
+  // globaltimer at entry (0) and exit (6), units computed (7), and the SM
+  // cycle counter next to the two stamps (8, 9)
+  unsigned long long* trace;
+  int trace_ctas;
 };
 
 // E tiles of 192 columns in two accumulators at TMEM columns 128 and 320,

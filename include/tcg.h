@@ -366,8 +366,10 @@ int tcg_last_launch_count(void);
  * next tcg_last_plan_string call. */
 const char* tcg_last_plan_string(void);
 
-/* Phase trace of the next GEMM kernel launched by this thread (tracing is off
- * otherwise and costs one untaken branch per stamp).  buf: device memory of
+/* Phase trace of the next GEMM kernel launched by this thread (tcg_gemm and
+ * its wrappers; tcg_gemm_chain's kernel writes slots 0, 6, 7, 8 and 9 only).
+ * Tracing is off otherwise and costs one untaken branch per stamp.  buf:
+ * device memory of
  * max_ctas x 10 uint64 (8-byte aligned); CTA c (c < max_ctas) writes slots
  * [10c, 10c+10): globaltimer nanoseconds at 0 kernel entry, 1 barriers and
  * TMEM ready, 2 producer starts its first unit, 3 first unit's MMAs issued,

@@ -202,3 +202,26 @@ def test_chain_cluster_rule(tcg):
     tcg.gemm_chain(1, 1900, 128, 200, 64, A, 64, B1, 64, B2, 128, E, 2, 200)   # 15 row tiles
     assert "sharing B" not in tcg.last_plan_string()
     assert tcg.check() == 0
+
+
+def test_chain_trace_records_entry_exit_and_units(tcg):
+    # tcg_trace_next also covers the chained kernel: entry / exit stamps, the
+    # cycle counter beside them, and the units each CTA's MMA warp computed
+    A, B1, B2 = (t.cuda() for t in _inputs("bf16", 4096, 256, 1000, 256, seed=8))
+    E = torch.empty((4096, 1000), dtype=torch.bfloat16, device="cuda")
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    buf = torch.zeros((sms, 10), dtype=torch.int64, device="cuda")
+    tcg.trace_next(buf, sms)
+    tcg.gemm_chain(1, 4096, 256, 1000, 256, A, 256, B1, 256, B2, 256, E, 2, 1000)
+    assert tcg.check() == 0
+    tr = buf.cpu().numpy()
+    ran = tr[:, 0] > 0
+    assert ran.sum() >= 32   # 32 row tiles, and the E tiles split into groups over the rest
+    assert (tr[ran, 6] > tr[ran, 0]).all() and (tr[ran, 9] > tr[ran, 8]).all()
+    assert (tr[ran, 7] >= 1).all() and tr[ran, 7].sum() >= 32
+    ghz = (tr[ran, 9] - tr[ran, 8]) / (tr[ran, 6] - tr[ran, 0])
+    assert ((ghz > 0.3) & (ghz < 3.0)).all(), ghz
+    # the request is consumed: the next call writes nothing
+    buf.zero_()
+    tcg.gemm_chain(1, 4096, 256, 1000, 256, A, 256, B1, 256, B2, 256, E, 2, 1000)
+    assert tcg.check() == 0 and int(buf.abs().sum()) == 0
