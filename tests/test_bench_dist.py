@@ -68,3 +68,23 @@ def test_reference_arm_runs_on_rank_zero_only():
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
     assert line["e2e"] == {"value": line["value"], "unit": line["unit"], "h2d_bytes_per_step": 0,
                            "d2h_bytes_per_step": 0}
+
+
+def test_kernel_clock_from_trace_stamps():
+    # the SM clock the bench reports for a traced launch: per CTA, cycles
+    # between the clock64 stamps over nanoseconds between the globaltimer
+    # stamps; CTAs that did not run (zero slots) are left out
+    import numpy as np
+    import torch
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import bench
+    tr = torch.zeros((4, 10), dtype=torch.int64)
+    for c, (ns, ghz) in enumerate([(30_000, 1.6), (31_000, 1.8), (29_000, 2.0)]):
+        tr[c, 0], tr[c, 6] = 1_000_000, 1_000_000 + ns
+        tr[c, 8], tr[c, 9] = 5_000, 5_000 + int(ns * ghz)
+    got = bench.kernel_clock(tr)
+    assert got["kernel_sm_mhz"] == 1800.0
+    assert got["kernel_sm_mhz_range"] == [1600.0, 2000.0]
+    assert bench.kernel_clock(torch.zeros((3, 10), dtype=torch.int64)) == {"kernel_sm_mhz": None,
+                                                                           "kernel_sm_mhz_range": None}
+    assert np.isfinite(got["kernel_sm_mhz"])
