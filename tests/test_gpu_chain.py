@@ -93,6 +93,7 @@ RANDOM = [
     ("bf16", 256, 256, 4000, 4096, "bf16"),     # 2 row tiles: E tiles split over many units
     ("bf16", 152 * 128 * 2 + 77, 128, 384, 512, "bf16"),  # more row tiles than SMs, ragged
     ("f16", 4000, 192, 700, 320, "f32"),     # CTA pairs, a B2 stage of one 64-column box after a full one
+    ("f16", 2304, 256, 904, 320, "f16"),     # CTA pairs, f16 E, a ragged last E tile
 ]
 
 
