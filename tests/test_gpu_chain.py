@@ -226,3 +226,17 @@ def test_chain_trace_records_entry_exit_and_units(tcg):
     buf.zero_()
     tcg.gemm_chain(1, 4096, 256, 1000, 256, A, 256, B1, 256, B2, 256, E, 2, 1000)
     assert tcg.check() == 0 and int(buf.abs().sum()) == 0
+
+
+def test_chain_single_ctas_and_clusters_agree_bit_for_bit(tcg):
+    # 1900 rows (15 row tiles: single CTAs) and 2100 rows (17: clusters of
+    # two sharing B by multicast) run the same MMAs in the same order on the
+    # first 1900 rows of A, so those rows of E are identical
+    A, B1, B2 = (t.cuda() for t in _inputs("bf16", 2100, 256, 700, 512, seed=13))
+    E = {}
+    for M in (1900, 2100):
+        E[M] = torch.full((M, 700), float("nan"), dtype=torch.float32, device="cuda")
+        tcg.gemm_chain(1, M, 256, 700, 512, A, 512, B1, 512, B2, 256, E[M], 0, 700)
+        assert tcg.check() == 0
+        assert ("sharing B" in tcg.last_plan_string()) == (M == 2100), tcg.last_plan_string()
+    assert torch.equal(E[1900], E[2100][:1900])
