@@ -568,3 +568,27 @@ def test_full_size_workloads_sampled_rows(tcg, oracle_mod, name):
     ref, S = oracle_rows(oracle_mod, x, rows=rows)
     ratio = assert_parity(got, ref, S, TAU[w.acc], name, w.out)
     print(f"{name}: max err/S {ratio:.3e} over {len(rows)} rows")
+
+
+def test_one_pass_plans_agree_bit_for_bit(tcg):
+    # every one-pass plan accumulates each output over K in the same order of
+    # K-16 MMA steps, whatever its tile: CTA pairs, single CTAs, the skinny
+    # 64-column tiles (few rows) and the narrow 32-column tiles (few columns)
+    # give identical fp32 outputs on the rows / columns they share
+    g = torch.Generator().manual_seed(77)
+    M, N, K = 1000, 1100, 640
+    A = torch.randn(M, K, generator=g).to(torch.bfloat16).cuda()
+    B = torch.randn(N, K, generator=g).to(torch.bfloat16).cuda()
+
+    def run(m, n, cg):
+        D = torch.full((m, n), float("nan"), dtype=torch.float32, device="cuda")
+        tcg.gemm(m, n, K, tcg.IN_BF16, A, 0, K, B, 0, K, D, tcg.F32, n, tcg.F32, cta_group=cg, split_k=1)
+        assert tcg.check() == 0
+        return D, tcg.last_plan_string()
+
+    ref, p2 = run(M, N, 2)
+    assert "cta_group 2" in p2, p2
+    for m, n, cg, tile in ((M, N, 1, "128x256"), (100, N, 0, "128x64"), (20, N, 0, "128x64"), (M, 24, 0, "128x32")):
+        D, plan = run(m, n, cg)
+        assert tile in plan, plan
+        assert torch.equal(D, ref[:m, :n]), plan
