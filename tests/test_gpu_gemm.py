@@ -592,3 +592,33 @@ def test_one_pass_plans_agree_bit_for_bit(tcg):
         D, plan = run(m, n, cg)
         assert tile in plan, plan
         assert torch.equal(D, ref[:m, :n]), plan
+
+
+def _rows_of(x, m):
+    # the first m rows of a case (A and its scales), same B
+    y = dict(x)
+    y["M"] = m
+    y["A"] = x["A"][:m]
+    if "SFA" in x:
+        y["SFA"] = x["SFA"][:m]
+    return y
+
+
+@pytest.mark.parametrize("dtype,M,N,K", [("e4m3", 1000, 1100, 256), ("e2m1", 2600, 27 * 384 + 300, 256),
+                                         ("nvf4", 2600, 27 * 384 + 300, 512)])
+def test_block_scaled_plans_agree_bit_for_bit(tcg, dtype, M, N, K):
+    # the same operands through different tiles: MXFP8 CTA pairs and single
+    # CTAs; packed FP4 on 256 x 384 pair tiles (two MMAs per K step, chosen
+    # for many tiles) and, for the first 256 rows alone, 256 x 256 pair tiles
+    x = make_case(dtype, "k", "k", M, N, K, dist="codes" if dtype in syn.PACKED_BITS else "normal1", seed=M + K)
+    ref = run_gpu(tcg, x, out="f32", cta_group=0, split_k=1)
+    plan_ref = tcg.last_plan_string()
+    if dtype == "e4m3":
+        D = run_gpu(tcg, x, out="f32", cta_group=1, split_k=1)
+        assert "cta_group 1" in tcg.last_plan_string() and "cta_group 2" in plan_ref
+        assert torch.equal(D, ref)
+    else:
+        assert "tile 256x384" in plan_ref, plan_ref
+        D = run_gpu(tcg, _rows_of(x, 256), out="f32", cta_group=0, split_k=1)
+        assert "tile 256x256" in tcg.last_plan_string(), tcg.last_plan_string()
+        assert torch.equal(D, ref[:256]), tcg.last_plan_string()
