@@ -1,7 +1,8 @@
 // Persistent, warp-specialised tcgen05 GEMM for sm_103a.
 //
 //   D[m,n] = sum_k A[m,k] B[k,n]       (kind::f16, kind::tf32)
-//   D[m,n] = sum_k (SFA.A)[m,k] (SFB.B)[k,n]   (kind::mxf8f6f4.block_scale)
+//   D[m,n] = sum_k (SFA.A)[m,k] (SFB.B)[k,n]   (kind::mxf8f6f4 / mxf4 / mxf4nvf4
+//                                              .block_scale)
 //
 // Structure (one CTA per SM, or one CTA pair per two SMs for cta_group::2).
 // The issuing roles run their loops on the whole warp in uniform control flow
@@ -22,7 +23,8 @@
 //               reads lanes 32*(w%4)..+31), convert, store to global
 //               (through a shared staging tile and a TMA tile store when
 //               the output's alignment allows), then arrive acc_empty[b];
-//   warps 8..11 (block scaling) with SF_BY_WARPS: scale staging, each warp
+//   warps 8..11 (block scaling) with SF_BY_WARPS (8- and 6-bit formats
+//               only): scale staging, each warp
 //               writes its TMEM lane quadrant of the stage's scale slot with
 //               tcgen05.st and arrives sf_ready[slot]; otherwise they join
 //               the epilogue (the two warps of a lane quadrant drain
